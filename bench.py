@@ -1,0 +1,462 @@
+#!/usr/bin/env python
+"""Benchmark of the chunked gated delta rule with state / W fake QDQ on GB300.
+
+One step = one pass of the hot path over one batch of the single-layer
+workload (B=4, T=4096, H=16, Dk=Dv=128, E4M3 state and W QDQ, h0 ~ N(0, 0.1^2)):
+the forward (saving the QDQ context) followed by the identity-STE backward
+(``--mode fwdbwd``, the default once the backward is present), or the
+forward alone (``--mode fwd``).  Inputs are synthetic (seeded) and resident
+in HBM when the timed region starts; per step the inputs (~350 MB) exceed
+the 129 MB L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
+(fp64 chunked reference) on a bounded sample of the same workload instead.
+Under torchrun every rank runs its own batch (weak scaling, no collective).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "GDN chunk fwd(+STE bwd) tokens/s at H=16,D=128,T=4096; % of roofline"
+
+
+# ----------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend)
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _barrier(ws):
+    if ws > 1:
+        torch.distributed.barrier()
+
+
+def _max_over_ranks(x, ws, device):
+    if ws == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.th.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def _source_hash(files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(profile_md, source_files, workload_key):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", profile_md)
+    try:
+        txt = open(path).read()
+    except OSError:
+        return None
+    m_src = re.search(r"source_sha256_16:\s*([0-9a-f]{16})", txt)
+    m_tr = re.search(r"traffic_bytes_per_launch\[%s\]:\s*([0-9.eE+]+)" % re.escape(workload_key), txt)
+    if not m_src or not m_tr or m_src.group(1) != _source_hash(source_files):
+        return None
+    return float(m_tr.group(1))
+
+
+FWD_SOURCES = ["gated_delta_rule_54_gb300/csrc/fwd.cu", "gated_delta_rule_54_gb300/csrc/common.cuh"]
+BWD_SOURCES = ["gated_delta_rule_54_gb300/csrc/bwd.cu", "gated_delta_rule_54_gb300/csrc/common.cuh"]
+
+
+def fwd_alg_bytes(w, save_ctx):
+    """Algorithmic HBM bytes of one forward launch: inputs read once, outputs written once."""
+    tok = w.B * w.T
+    b = tok * w.Hk * w.Dk * 2 * 2            # q, k bf16
+    b += tok * w.Hv * w.Dv * 2               # v bf16
+    b += tok * w.Hv * 4 * 2                  # beta, g f32
+    b += tok * w.Hv * w.Dv * 4               # o f32
+    b += w.B * w.Hv * w.Dk * w.Dv * 4 * (2 if w.h0 else 1)   # h0 read, ht write
+    if save_ctx:
+        nch = w.B * (-(-w.T // 64))
+        b += tok * w.Hv * w.Dk + nch * w.Hv * 4                          # W codes + scales
+        b += nch * w.Hv * w.Dk * w.Dv + nch * w.Hv * (w.Dv // 64) * 4    # state codes + scales
+    return b
+
+
+def bwd_alg_bytes(w):
+    """Algorithmic HBM bytes of one backward pass: q,k,v,beta,g,dO, saved context
+    and dht read once; dq,dk,dv,dbeta,dg,dh0 written once."""
+    tok = w.B * w.T
+    nch = w.B * (-(-w.T // 64))
+    b = tok * w.Hk * w.Dk * 2 * 2 + tok * w.Hv * w.Dv * 2 + tok * w.Hv * 4 * 2
+    b += tok * w.Hv * w.Dv * 2                                           # dO bf16
+    b += tok * w.Hv * w.Dk + nch * w.Hv * 4                              # W codes + scales
+    b += nch * w.Hv * w.Dk * w.Dv + nch * w.Hv * (w.Dv // 64) * 4        # state codes + scales
+    b += w.B * w.Hv * w.Dk * w.Dv * 4 * 2                                # dht in, dh0 out
+    b += tok * w.Hk * w.Dk * 4 * 2 + tok * w.Hv * w.Dv * 4 + tok * w.Hv * 4 * 2  # grads out
+    return b
+
+
+def fwd_alg_flops(w):
+    """Algorithmic forward FLOPs (triangular products at half): 9.0 MFLOP per
+    64-token chunk-head at Dk = Dv = 128, i.e. 140.6 kFLOP per token-head."""
+    C, Dk, Dv = 64, w.Dk, w.Dv
+    per_chunk = (C * C * Dk + C ** 3 / 3 + C * C * Dk + C * C * Dv + 2 * C * Dk * Dv * 3
+                 + C * C * Dk + C * C * Dv)
+    return per_chunk / C * w.B * w.T * w.Hv
+
+
+# ----------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------
+def run_ours(args, ws, rank, local):
+    from gated_delta_rule_54_gb300 import api, synth
+    from gated_delta_rule_54_gb300._lib import load
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    load()
+    w = synth.WORKLOADS[args.workload]
+    w = synth.Workload(**{**w.__dict__, "seed": w.seed + rank})
+    bwd = args.mode == "fwdbwd"
+    cpu = synth.make_inputs(w)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in cpu.items()}
+    q, k, v, beta, g, h0 = d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"]
+    sm, wm = w.state_mode, w.w_mode
+    p = api.make_problem(q, k, v, None, 1.0, sm, wm)
+    o = torch.empty(w.B, w.T, w.Hv, w.Dv, device=dev)
+    ht = torch.empty(w.B, w.Hv, w.Dk, w.Dv, device=dev)
+    ctx = torch.empty(api.gdn_ctx_bytes(p), device=dev, dtype=torch.uint8) if bwd else None
+    if bwd:
+        gen = torch.Generator().manual_seed(1000 + rank)
+        do = torch.randn(w.B, w.T, w.Hv, w.Dv, generator=gen).to(torch.bfloat16).to(dev)
+        dht = (torch.randn(w.B, w.Hv, w.Dk, w.Dv, generator=gen) * 0.01).to(dev)
+        wsb = torch.empty(max(api.gdn_bwd_workspace_bytes(p), 1), device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    fwd_times, bwd_times = [], []
+
+    def step(record=False):
+        e0 = ev() if record else None
+        if record:
+            e0.record(stream)
+        api.gdn_chunk_fwd_qdq(q, k, v, beta, g, h0, state_mode=sm, w_mode=wm, out=(o, ht, ctx))
+        if record:
+            e1 = ev()
+            e1.record(stream)
+            fwd_times.append((e0, e1))
+        if bwd:
+            api.gdn_chunk_bwd_ste(q, k, v, beta, g, ctx, do, dht, state_mode=sm, w_mode=wm,
+                                  workspace=wsb)
+            if record:
+                e2 = ev()
+                e2.record(stream)
+                bwd_times.append((e1, e2))
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    _barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_start, t_end = ev(), ev()
+        t_start.record(stream)
+        for _ in range(args.steps):
+            step(record=True)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    _barrier(ws)
+    ms_total = t_start.elapsed_time(t_end)
+    ms_total = _max_over_ranks(ms_total, ws, dev)
+    ms_step = ms_total / args.steps
+    tokens = w.B * w.T
+    value = tokens * ws * args.steps / (ms_total / 1e3)
+    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fwd_times)
+    bwd_ms = statistics.mean(a.elapsed_time(b) for a, b in bwd_times) if bwd else None
+    launches_per_step = 1 + (args.bwd_launches if bwd else 0)
+
+    # roofline of the dominant kernel
+    peak, peak_kind = _peaks()
+    if bwd and bwd_ms > fwd_ms:
+        alg = bwd_alg_bytes(w)
+        dur = bwd_ms
+        kernel = "gdn backward (all launches of one call)"
+        traffic = _traffic("bwd_fwd_bwd_workload.md", BWD_SOURCES, args.workload)
+    else:
+        alg = fwd_alg_bytes(w, bwd)
+        dur = fwd_ms
+        kernel = "gdn_fwd_kernel"
+        traffic = _traffic("gdn_fwd_kernel_single_layer.md", FWD_SOURCES,
+                           args.workload + ("+ctx" if bwd else ""))
+    achieved = alg / (dur / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel,
+            "peak_source": peak_kind, "alg_bytes_per_launch": alg,
+            "launch_ms": round(dur, 4)}
+
+    # end to end through the public API from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        host = {kk: (vv.pin_memory() if isinstance(vv, torch.Tensor) else vv) for kk, vv in cpu.items()}
+        o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        ht_h = torch.empty(ht.shape, dtype=ht.dtype).pin_memory()
+        bufs = dict(q=q, k=k, v=v, beta=beta, g=g, h0=h0)
+        h2d = sum(host[n].numel() * host[n].element_size() for n in bufs if host[n] is not None)
+        d2h = o_h.numel() * 4 + ht_h.numel() * 4
+        if bwd:
+            do_h = do.cpu().pin_memory()
+            dht_h = dht.cpu().pin_memory()
+            h2d += do_h.numel() * 2 + dht_h.numel() * 4
+            grads_h = None
+
+        def e2e_step():
+            for n, t in bufs.items():
+                if t is not None:
+                    t.copy_(host[n], non_blocking=True)
+            api.gdn_chunk_fwd_qdq(q, k, v, beta, g, h0, state_mode=sm, w_mode=wm, out=(o, ht, ctx))
+            o_h.copy_(o, non_blocking=True)
+            ht_h.copy_(ht, non_blocking=True)
+            out = 0
+            if bwd:
+                do.copy_(do_h, non_blocking=True)
+                dht.copy_(dht_h, non_blocking=True)
+                gr = api.gdn_chunk_bwd_ste(q, k, v, beta, g, ctx, do, dht, state_mode=sm,
+                                           w_mode=wm, workspace=wsb)
+                for t in gr:
+                    if t is not None:
+                        t.cpu()
+            return out
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        _barrier(ws)
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e_ms = _max_over_ranks(a.elapsed_time(b), ws, dev)
+        if bwd:
+            d2h += (2 * q.numel() + v.numel() + 2 * beta.numel() + ht.numel()) * 4
+        e2e = {"value": round(tokens * ws * args.steps / (e_ms / 1e3), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e_ms / args.steps, 4)}
+
+    cpu_base = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu_base = cpu_baseline(w, cpu, bwd, budget_s=args.cpu_budget)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), beta=sigmoid, g=-softplus)",
+        "config": {"workload": w.name, "mode": args.mode, "B": w.B, "T": w.T, "Hk": w.Hk,
+                   "Hv": w.Hv, "Dk": w.Dk, "Dv": w.Dv, "state_mode": sm, "w_mode": wm,
+                   "chunk": 64, "block_v": 64, "global_batch_tokens": w.B * w.T * ws,
+                   "l2": "inputs larger than L2 (no flush needed)",
+                   "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(bwd_ms, 4) if bwd else None,
+                   "fwd_tflops_alg": round(fwd_alg_flops(w) / (fwd_ms / 1e3) / 1e12, 2)},
+        "clocks": clk.summary(), "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
+        "roofline": roof, "cpu_baseline": cpu_base,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def cpu_baseline(w, cpu, bwd, budget_s=20.0):
+    """The fp64 chunked oracle, as it stands, on whole sequences of the workload
+    (all heads), until the budget is used; tokens/s scaled from the sample."""
+    from oracle.chunked import chunked
+    t0 = time.time()
+    done = 0
+    for n in range(w.B):
+        sl = slice(n, n + 1)
+        args = [cpu[x][sl] for x in ("q", "k", "v", "beta", "g")]
+        h0 = cpu["h0"][sl] if cpu["h0"] is not None else None
+        if bwd:
+            xs = [a.double().requires_grad_(True) for a in args] + (
+                [h0.double().requires_grad_(True)] if h0 is not None else [None])
+            o, ht = chunked(*xs, state_mode=w.state_mode, w_mode=w.w_mode)
+            (o.sum() + ht.sum()).backward()
+        else:
+            chunked(*args, h0, state_mode=w.state_mode, w_mode=w.w_mode)
+        done += 1
+        if time.time() - t0 > budget_s * 0.5:
+            break
+    dt = time.time() - t0
+    return {"value": round(done * w.T / dt, 2), "unit": "tokens/s", "cores": torch.get_num_threads(),
+            "kind": "oracle",
+            "sample": "%d of %d sequences (T=%d, all %d heads), fp64 chunked oracle %s" % (
+                done, w.B, w.T, w.Hv, "fwd+autograd bwd" if bwd else "fwd")}
+
+
+# ----------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ----------------------------------------------------------------------------
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return
+    from gated_delta_rule_54_gb300 import synth
+    from oracle.chunked import chunked
+    w = synth.WORKLOADS[args.workload]
+    bwd = args.mode == "fwdbwd"
+    T_s = 1024   # bounded sample per step: one sequence, all heads, 1024 tokens
+    ws_ = synth.Workload(**{**w.__dict__, "B": 1, "T": T_s})
+    cpu = synth.make_inputs(ws_)
+    xs = [cpu[x] for x in ("q", "k", "v", "beta", "g", "h0")]
+
+    def step():
+        if bwd:
+            ys = [a.double().requires_grad_(True) if a is not None else None for a in xs]
+            o, ht = chunked(*ys, state_mode=w.state_mode, w_mode=w.w_mode)
+            (o.sum() + ht.sum()).backward()
+        else:
+            chunked(*xs, state_mode=w.state_mode, w_mode=w.w_mode)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.time()
+    for _ in range(args.steps):
+        step()
+    dt = time.time() - t0
+    value = T_s * args.steps / dt
+    sample = "1 sequence x %d tokens, all %d heads per step (fp64 chunked oracle %s)" % (
+        T_s, w.Hv, "fwd+autograd bwd" if bwd else "fwd")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "mode": args.mode, "B": w.B, "T": w.T, "Hk": w.Hk,
+                       "Hv": w.Hv, "Dk": w.Dk, "Dv": w.Dv, "state_mode": w.state_mode,
+                       "w_mode": w.w_mode},
+            "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s",
+                             "cores": torch.get_num_threads(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="layer")
+    ap.add_argument("--mode", default=None, choices=["fwd", "fwdbwd"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    if args.mode is None:
+        args.mode = "fwdbwd" if _backward_available() else "fwd"
+    args.bwd_launches = BWD_LAUNCHES
+    ws, rank, local = _dist()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+BWD_LAUNCHES = 0   # kernels one backward call launches
+
+
+def _backward_available():
+    return BWD_LAUNCHES > 0
+
+
+if __name__ == "__main__":
+    main()

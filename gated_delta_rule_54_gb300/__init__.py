@@ -1,1 +1,15 @@
-"""GB300-native chunked gated delta rule with state/W fake QDQ (placeholder, filled below)."""
+"""GB300-native (sm_103a) chunked gated delta rule with state / W fake QDQ.
+
+The compute lives in the CUDA library ``libgdn_qdq.so`` (C ABI in
+``include/gdn_qdq.h``); this package is its thin binding:
+
+  gdn_chunk_fwd_qdq   forward (chunk 64, exact solve, state + W QDQ)
+  gdn_chunk_bwd_ste   identity straight-through backward
+  fake_qdq_e4m3 / fake_qdq_int8   the grouped QDQ primitive
+
+``synth`` holds the seeded synthetic-input generators.
+"""
+from .api import (fake_qdq_e4m3, fake_qdq_int8, gdn_bwd_workspace_bytes, gdn_chunk_bwd_ste,  # noqa: F401
+                  gdn_chunk_fwd_qdq, gdn_ctx_bytes, gdn_num_chunk_slots, gdn_validate,
+                  make_problem, split_ctx)
+from ._lib import GdnError, load  # noqa: F401

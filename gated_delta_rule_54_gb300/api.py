@@ -1,0 +1,187 @@
+"""Thin Python binding of the C ABI (``include/gdn_qdq.h``): argument marshalling only.
+
+PyTorch provides device memory and the current CUDA stream; every step of
+the computation runs in the CUDA library.  There is no CPU or PyTorch
+fallback: a missing library or a rejected configuration raises.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from ._lib import DTYPES, QDQ_MODES, GdnError, GdnProblem, check, load
+
+_DT = {torch.bfloat16: DTYPES["bf16"], torch.float16: DTYPES["fp16"], torch.float32: DTYPES["fp32"]}
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device) -> ctypes.c_void_p:
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _mode(m) -> int:
+    if isinstance(m, str):
+        if m not in QDQ_MODES:
+            raise ValueError("QDQ mode must be one of %s, got %r" % (sorted(QDQ_MODES), m))
+        return QDQ_MODES[m]
+    return int(m)
+
+
+def make_problem(q, k, v, cu_seqlens=None, scale=1.0, state_mode="e4m3", w_mode="e4m3",
+                 block_v=64, chunk=64, N=None) -> GdnProblem:
+    B, T, Hk, Dk = k.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    p = GdnProblem()
+    p.B, p.T, p.Hk, p.Hv, p.Dk, p.Dv = B, T, Hk, Hv, Dk, Dv
+    p.N = (cu_seqlens.numel() - 1) if cu_seqlens is not None else (B if N is None else N)
+    p.cu_seqlens = cu_seqlens.data_ptr() if cu_seqlens is not None else None
+    p.scale = float(scale)
+    p.state_mode, p.w_mode = _mode(state_mode), _mode(w_mode)
+    p.block_v, p.chunk = block_v, chunk
+    p.dtype = _DT.get(q.dtype, 99)
+    return p
+
+
+def _check_dev(name, t, device):
+    if t is None:
+        return
+    if not t.is_cuda or t.device != device:
+        raise ValueError("%s must be a CUDA tensor on %s" % (name, device))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+
+
+def gdn_validate(p: GdnProblem) -> int:
+    return load().gdn_validate(ctypes.byref(p))
+
+
+def gdn_ctx_bytes(p: GdnProblem) -> int:
+    return int(load().gdn_ctx_bytes(ctypes.byref(p)))
+
+
+def gdn_num_chunk_slots(p: GdnProblem) -> int:
+    return int(load().gdn_num_chunk_slots(ctypes.byref(p)))
+
+
+def gdn_bwd_workspace_bytes(p: GdnProblem) -> int:
+    return int(load().gdn_bwd_workspace_bytes(ctypes.byref(p)))
+
+
+def gdn_chunk_fwd_qdq(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, state_mode="e4m3",
+                      w_mode="e4m3", output_final_state=True, save_ctx=False, out=None):
+    """Forward.  q, k [B,T,Hk,Dk] bf16; v [B,T,Hv,Dv] bf16; beta, g [B,T,Hv] f32;
+    h0 [N,Hv,Dk,Dv] f32 or None; cu_seqlens [N+1] int32 or None (B == 1).
+
+    Returns (o [B,T,Hv,Dv] f32, ht [N,Hv,Dk,Dv] f32 or None, ctx uint8 or None).
+    ``out`` may pass preallocated (o, ht, ctx) buffers.
+    """
+    lib = load()
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g), ("h0", h0),
+                    ("cu_seqlens", cu_seqlens)):
+        _check_dev(name, t, dev)
+    p = make_problem(q, k, v, cu_seqlens, scale, state_mode, w_mode)
+    check("gdn_validate", lib.gdn_validate(ctypes.byref(p)))
+    B, T, Hv, Dv = v.shape
+    if out is not None:
+        o, ht, ctx = out
+    else:
+        o = torch.empty(B, T, Hv, Dv, device=dev, dtype=torch.float32)
+        ht = (torch.empty(p.N, Hv, k.shape[3], Dv, device=dev, dtype=torch.float32)
+              if output_final_state else None)
+        ctx = (torch.empty(int(lib.gdn_ctx_bytes(ctypes.byref(p))), device=dev, dtype=torch.uint8)
+               if save_ctx else None)
+    st = lib.gdn_chunk_fwd_qdq(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
+                               _ptr(h0), _ptr(o), _ptr(ht), _ptr(ctx), _stream(dev))
+    check("gdn_chunk_fwd_qdq", st)
+    return o, ht, ctx
+
+
+def gdn_chunk_bwd_ste(q, k, v, beta, g, ctx, do, dht=None, cu_seqlens=None, scale=1.0,
+                      state_mode="e4m3", w_mode="e4m3", need_dh0=True, workspace=None):
+    """Identity-STE backward.  Returns (dq, dk, dv, dbeta, dg, dh0 or None)."""
+    lib = load()
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g), ("ctx", ctx),
+                    ("do", do), ("dht", dht), ("cu_seqlens", cu_seqlens)):
+        _check_dev(name, t, dev)
+    if do.dtype != torch.bfloat16:
+        raise GdnError("gdn_chunk_bwd_ste", -2)
+    p = make_problem(q, k, v, cu_seqlens, scale, state_mode, w_mode)
+    check("gdn_validate", lib.gdn_validate(ctypes.byref(p)))
+    f32 = dict(device=dev, dtype=torch.float32)
+    dq = torch.empty(k.shape, **f32)
+    dk = torch.empty(k.shape, **f32)
+    dv = torch.empty(v.shape, **f32)
+    dbeta = torch.empty(beta.shape, **f32)
+    dg = torch.empty(g.shape, **f32)
+    dh0 = torch.empty(p.N, v.shape[2], k.shape[3], v.shape[3], **f32) if need_dh0 else None
+    need = int(lib.gdn_bwd_workspace_bytes(ctypes.byref(p)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device=dev, dtype=torch.uint8)
+    st = lib.gdn_chunk_bwd_ste(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
+                               _ptr(ctx), _ptr(do), _ptr(dht), _ptr(dq), _ptr(dk), _ptr(dv),
+                               _ptr(dbeta), _ptr(dg), _ptr(dh0), _ptr(workspace),
+                               ctypes.c_size_t(workspace.numel()), _stream(dev))
+    check("gdn_chunk_bwd_ste", st)
+    return dq, dk, dv, dbeta, dg, dh0
+
+
+def _fake_qdq(fn_name, x, group_cols, with_codes=False, out=None):
+    lib = load()
+    if not x.is_cuda or x.dtype != torch.float32 or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA float32 tensor")
+    if x.dim() == 1:
+        b, r, c = 1, 1, x.shape[0]
+    elif x.dim() == 2:
+        b, r, c = 1, x.shape[0], x.shape[1]
+    else:
+        b, r, c = x[..., 0, 0].numel(), x.shape[-2], x.shape[-1]
+    y = torch.empty_like(x) if out is None else out
+    scales = torch.empty(b, c // group_cols if group_cols > 0 else 0, device=x.device,
+                         dtype=torch.float32)
+    codes = torch.empty(x.shape, device=x.device, dtype=torch.uint8) if with_codes else None
+    st = getattr(lib, fn_name)(_ptr(x), _ptr(y), _ptr(scales), _ptr(codes), b, r, c, group_cols,
+                               _stream(x.device))
+    check(fn_name, st)
+    return (y, scales, codes) if with_codes else (y, scales)
+
+
+def fake_qdq_e4m3(x, group_cols, with_codes=False, out=None):
+    """Grouped dynamic E4M3 fake QDQ of a [batch, rows, cols] float32 CUDA tensor."""
+    return _fake_qdq("fake_qdq_e4m3", x, group_cols, with_codes, out)
+
+
+def fake_qdq_int8(x, group_cols, with_codes=False, out=None):
+    """Grouped dynamic INT8 fake QDQ of a [batch, rows, cols] float32 CUDA tensor."""
+    return _fake_qdq("fake_qdq_int8", x, group_cols, with_codes, out)
+
+
+def split_ctx(ctx: torch.Tensor, p: GdnProblem):
+    """Views of the forward's saved context segments (layout of gdn_ctx_bytes)."""
+    B, T, Hv, Dk, Dv = p.B, p.T, p.Hv, p.Dk, p.Dv
+    ns = gdn_num_chunk_slots(p)
+    al = lambda x: (x + 255) // 256 * 256
+    off = 0
+    out = {}
+    if p.w_mode != 0:
+        n = B * T * Hv * Dk
+        out["w_codes"] = ctx[off:off + n].view(B, T, Hv, Dk)
+        off = al(off + n)
+        out["w_scales"] = ctx[off:off + 4 * ns * Hv].view(torch.float32).view(ns, Hv)
+        off = al(off + 4 * ns * Hv)
+    if p.state_mode != 0:
+        n = ns * Hv * Dk * Dv
+        out["h_codes"] = ctx[off:off + n].view(ns, Hv, Dk, Dv)
+        off = al(off + n)
+        m = ns * Hv * (Dv // 64)
+        out["h_scales"] = ctx[off:off + 4 * m].view(torch.float32).view(ns, Hv, Dv // 64)
+    else:
+        n = ns * Hv * Dk * Dv
+        out["h_full"] = ctx[off:off + 4 * n].view(torch.float32).view(ns, Hv, Dk, Dv)
+    return out

@@ -1,0 +1,189 @@
+// C ABI entry points: host-side validation, size queries and dispatch.
+// Everything here runs on the host; nothing is launched until a problem has
+// passed validation (first QAT page, "What does this PR do?": unsupported
+// formats and FP32 inputs are rejected before launch).
+#include <cuda_runtime.h>
+
+#include "../../include/gdn_qdq.h"
+#include "launch.h"
+
+namespace gdn {
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+Dims dims_of(const gdn_problem& p) {
+  Dims d;
+  d.B = p.B;
+  d.T = p.T;
+  d.Hk = p.Hk;
+  d.Hv = p.Hv;
+  d.Dk = p.Dk;
+  d.Dv = p.Dv;
+  d.packed = p.cu_seqlens != nullptr;
+  d.N = d.packed ? p.N : p.B;
+  d.nt_fixed = (p.T + kChunkLen - 1) / kChunkLen;
+  d.n_slots = d.packed ? (p.T / kChunkLen + p.N) : p.B * d.nt_fixed;
+  return d;
+}
+
+CtxLayout ctx_layout(const gdn_problem& p) {
+  const Dims d = dims_of(p);
+  CtxLayout L{};
+  size_t off = 0;
+  const size_t tokens = (size_t)(d.B * d.T);
+  if (p.w_mode != GDN_QDQ_NONE) {
+    L.w_codes = off;
+    off = align256(off + tokens * d.Hv * d.Dk);
+    L.w_scales = off;
+    off = align256(off + sizeof(float) * (size_t)d.n_slots * d.Hv);
+  }
+  const size_t per_slot = (size_t)d.n_slots * d.Hv * d.Dk * d.Dv;
+  if (p.state_mode != GDN_QDQ_NONE) {
+    L.h_codes = off;
+    off = align256(off + per_slot);
+    L.h_scales = off;
+    off = align256(off + sizeof(float) * (size_t)d.n_slots * d.Hv * (d.Dv / kChunkLen));
+  } else {
+    L.h_full = off;
+    off = align256(off + sizeof(float) * per_slot);
+  }
+  L.total = off;
+  return L;
+}
+
+static bool valid_mode(int m) {
+  return m == GDN_QDQ_NONE || m == GDN_QDQ_E4M3 || m == GDN_QDQ_INT8;
+}
+
+static gdn_status validate(const gdn_problem* p) {
+  if (!p) return GDN_ERR_INVALID_ARG;
+  if (p->B < 0 || p->T < 0 || p->Hk <= 0 || p->Hv <= 0 || p->Dk <= 0 || p->Dv <= 0)
+    return GDN_ERR_INVALID_ARG;
+  if (!valid_mode(p->state_mode) || !valid_mode(p->w_mode)) return GDN_ERR_INVALID_ARG;
+  if (p->dtype != GDN_DTYPE_BF16) {
+    if (p->dtype == GDN_DTYPE_FP16 || p->dtype == GDN_DTYPE_FP32) return GDN_ERR_UNSUPPORTED_DTYPE;
+    return GDN_ERR_INVALID_ARG;
+  }
+  if (p->chunk != kChunkLen) return GDN_ERR_UNSUPPORTED_SHAPE;
+  if (p->block_v != kChunkLen) return GDN_ERR_UNSUPPORTED_MODE;
+  if ((p->Dk != 64 && p->Dk != 128) || (p->Dv != 64 && p->Dv != 128))
+    return GDN_ERR_UNSUPPORTED_SHAPE;
+  if (p->Hv % p->Hk != 0) return GDN_ERR_UNSUPPORTED_SHAPE;
+  if (p->cu_seqlens) {
+    if (p->B != 1 || p->N < 1) return GDN_ERR_INVALID_ARG;
+  } else if (p->N != p->B) {
+    return GDN_ERR_INVALID_ARG;
+  }
+  if (p->T > ((int64_t)1 << 31) - 1 || p->B * p->T > ((int64_t)1 << 31) - 1)
+    return GDN_ERR_UNSUPPORTED_SHAPE;  // token indices are int32 on the device
+  if (!(p->scale == p->scale)) return GDN_ERR_INVALID_ARG;  // NaN scale
+  return GDN_OK;
+}
+
+static bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15) == 0; }
+
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+const char* gdn_status_string(int s) {
+  switch (s) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG: null pointer, negative size or bad enum";
+    case GDN_ERR_UNSUPPORTED_DTYPE: return "GDN_ERR_UNSUPPORTED_DTYPE: q/k/v/dO must be bf16";
+    case GDN_ERR_UNSUPPORTED_SHAPE: return "GDN_ERR_UNSUPPORTED_SHAPE: Dk/Dv must be 64 or 128, Hv % Hk == 0, chunk 64";
+    case GDN_ERR_UNSUPPORTED_MODE: return "GDN_ERR_UNSUPPORTED_MODE: QDQ mode or block_v not supported";
+    case GDN_ERR_WORKSPACE_TOO_SMALL: return "GDN_ERR_WORKSPACE_TOO_SMALL";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a kernel launch failed";
+    case GDN_ERR_MISALIGNED: return "GDN_ERR_MISALIGNED: pointers must be 16-byte aligned";
+    default: return "unknown gdn_status";
+  }
+}
+
+int gdn_abi_version(void) { return GDN_QDQ_ABI_VERSION; }
+
+gdn_status gdn_validate(const gdn_problem* p) { return validate(p); }
+
+int64_t gdn_num_chunk_slots(const gdn_problem* p) {
+  if (validate(p) != GDN_OK) return -1;
+  return dims_of(*p).n_slots;
+}
+
+size_t gdn_ctx_bytes(const gdn_problem* p) {
+  if (validate(p) != GDN_OK) return 0;
+  return ctx_layout(*p).total;
+}
+
+gdn_status gdn_chunk_fwd_qdq(const gdn_problem* p, const void* q, const void* k, const void* v,
+                             const float* beta, const float* g, const float* h0, float* o,
+                             float* ht, void* ctx, void* stream) {
+  gdn_status s = validate(p);
+  if (s != GDN_OK) return s;
+  const Dims d = dims_of(*p);
+  if (d.B * d.T > 0 && (!q || !k || !v || !beta || !g || !o)) return GDN_ERR_INVALID_ARG;
+  for (const void* ptr : {q, k, v, (const void*)beta, (const void*)g, (const void*)h0,
+                          (const void*)o, (const void*)ht, (const void*)ctx,
+                          (const void*)p->cu_seqlens})
+    if (ptr && !aligned16(ptr)) return GDN_ERR_MISALIGNED;
+  if (ctx && ((uintptr_t)ctx & 255)) return GDN_ERR_MISALIGNED;
+  if (d.N == 0 || (d.B * d.T == 0 && !ht)) return GDN_OK;
+  return launch_fwd(*p, d, q, k, v, beta, g, h0, o, ht, ctx, (cudaStream_t)stream);
+}
+
+size_t gdn_bwd_workspace_bytes(const gdn_problem* p) {
+  if (validate(p) != GDN_OK) return 0;
+  return bwd_workspace_bytes(*p, dims_of(*p));
+}
+
+gdn_status gdn_chunk_bwd_ste(const gdn_problem* p, const void* q, const void* k, const void* v,
+                             const float* beta, const float* g, const void* ctx, const void* dO,
+                             const float* dht, float* dq, float* dk, float* dv, float* dbeta,
+                             float* dg, float* dh0, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  gdn_status s = validate(p);
+  if (s != GDN_OK) return s;
+  const Dims d = dims_of(*p);
+  const bool any_tokens = d.B * d.T > 0;
+  if (any_tokens && (!q || !k || !v || !beta || !g || !ctx || !dO || !dq || !dk || !dv ||
+                     !dbeta || !dg))
+    return GDN_ERR_INVALID_ARG;
+  for (const void* ptr : {q, k, v, (const void*)beta, (const void*)g, ctx, dO,
+                          (const void*)dht, (const void*)dq, (const void*)dk, (const void*)dv,
+                          (const void*)dbeta, (const void*)dg, (const void*)dh0, (const void*)workspace,
+                          (const void*)p->cu_seqlens})
+    if (ptr && !aligned16(ptr)) return GDN_ERR_MISALIGNED;
+  const size_t need = bwd_workspace_bytes(*p, d);
+  if (workspace_bytes < need || (need > 0 && !workspace)) return GDN_ERR_WORKSPACE_TOO_SMALL;
+  if (d.N == 0) return GDN_OK;
+  return launch_bwd(*p, d, q, k, v, beta, g, ctx, dO, dht, dq, dk, dv, dbeta, dg, dh0,
+                    workspace, (cudaStream_t)stream);
+}
+
+static gdn_status fake_qdq_common(int mode, const float* x, float* y, float* scales,
+                                  uint8_t* codes, int64_t batch, int64_t rows, int64_t cols,
+                                  int64_t group_cols, void* stream) {
+  if (batch < 0 || rows < 0 || cols < 0 || group_cols <= 0 || cols % group_cols != 0)
+    return GDN_ERR_INVALID_ARG;
+  if (batch * (cols / group_cols) == 0) return GDN_OK;
+  if (!x || !y || !scales) return GDN_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(scales) || (codes && !aligned16(codes)))
+    return GDN_ERR_MISALIGNED;
+  return launch_fake_qdq(mode, x, y, scales, codes, batch, rows, cols, group_cols,
+                         (cudaStream_t)stream);
+}
+
+gdn_status fake_qdq_e4m3(const float* x, float* y, float* scales, uint8_t* codes, int64_t batch,
+                         int64_t rows, int64_t cols, int64_t group_cols, void* stream) {
+  return fake_qdq_common(GDN_QDQ_E4M3, x, y, scales, codes, batch, rows, cols, group_cols,
+                         stream);
+}
+
+gdn_status fake_qdq_int8(const float* x, float* y, float* scales, uint8_t* codes, int64_t batch,
+                         int64_t rows, int64_t cols, int64_t group_cols, void* stream) {
+  return fake_qdq_common(GDN_QDQ_INT8, x, y, scales, codes, batch, rows, cols, group_cols,
+                         stream);
+}
+
+}  // extern "C"

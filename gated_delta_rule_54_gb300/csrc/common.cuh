@@ -1,0 +1,199 @@
+// Shared device helpers for the sm_103a kernels: fake QDQ arithmetic,
+// tensor-core fragments, shared-memory swizzle and async copies.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdn_qdq.h"
+
+namespace gdn {
+
+constexpr int kChunk = 64;   // chunk length (first QAT page, "What does this PR do?")
+constexpr int kBlockV = 64;  // state-scale tile width (`state.block_v 64`)
+
+// ---------------------------------------------------------------------------
+// Fake QDQ arithmetic (bit-exact with the definition in gdn_qdq.h).
+// Compiled without fast-math: '/' and the reciprocal are IEEE correctly
+// rounded, and each multiply below is a single rounding (no contraction can
+// apply: none of them feeds an add).
+// ---------------------------------------------------------------------------
+template <int MODE>
+struct QdqMax;
+template <>
+struct QdqMax<GDN_QDQ_E4M3> {
+  static constexpr float value = 448.0f;
+};
+template <>
+struct QdqMax<GDN_QDQ_INT8> {
+  static constexpr float value = 127.0f;
+};
+
+// Scale and its reciprocal from the group amax.  amax == 0 gives s = 0 and
+// rcp = 0 (the caller keeps the inputs, which are all zero).
+template <int MODE>
+__device__ __forceinline__ void qdq_scale(float amax, float& s, float& rcp) {
+  if (amax == 0.0f) {
+    s = 0.0f;
+    rcp = 0.0f;
+  } else {
+    s = __fdiv_rn(amax, QdqMax<MODE>::value);
+    rcp = __frcp_rn(s);
+  }
+}
+
+// Code byte of x for scale reciprocal rcp (RNE; E4M3 saturates to finite).
+template <int MODE>
+__device__ __forceinline__ uint8_t qdq_code(float x, float rcp) {
+  const float u = __fmul_rn(x, rcp);
+  if constexpr (MODE == GDN_QDQ_E4M3) {
+    return (uint8_t)__nv_cvt_float_to_fp8(u, __NV_SATFINITE, __NV_E4M3);
+  } else {
+    int c = __float2int_rn(u);
+    c = c > 127 ? 127 : (c < -127 ? -127 : c);
+    return (uint8_t)(int8_t)c;
+  }
+}
+
+// Value of a code byte (exact in fp32 and in bf16).
+template <int MODE>
+__device__ __forceinline__ float qdq_code_value(uint8_t c) {
+  if constexpr (MODE == GDN_QDQ_E4M3) {
+    __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)c, __NV_E4M3);
+    return __half2float(__half(hr));
+  } else {
+    return (float)(int8_t)c;
+  }
+}
+
+// For amax == 0 a group passes through unchanged; its codes are signed zeros
+// for E4M3 and zeros for INT8.
+template <int MODE>
+__device__ __forceinline__ uint8_t qdq_zero_code(float x) {
+  if constexpr (MODE == GDN_QDQ_E4M3) return signbit(x) ? 0x80 : 0x00;
+  return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Warp / block reductions
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Tensor-core fragments: mma.sync m16n8k16 bf16 x bf16 -> f32.
+// A 16x16 row-major, B 16x8 (k x n), C 16x8.  Lane l: g = l/4, t = l%4;
+// C holds (g, 2t), (g, 2t+1), (g+8, 2t), (g+8, 2t+1).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+// ---------------------------------------------------------------------------
+// bf16 tiles in shared memory: rows of RL elements (RL*2 bytes = 8 or 16
+// chunks of 16 bytes); chunk ch of row r is stored at chunk ch ^ (r & 7) so
+// that ldmatrix of 8 rows touches 8 distinct bank groups.
+// ---------------------------------------------------------------------------
+template <int RL>
+__device__ __forceinline__ int swz(int row, int col) {
+  // element offset of (row, col)
+  return row * RL + ((((col >> 3) ^ (row & 7))) << 3) + (col & 7);
+}
+
+// ldmatrix.x4 address of a 16x16 A fragment at (r0, c0) of a row-major tile.
+template <int RL>
+__device__ __forceinline__ uint32_t a_frag_addr(const __nv_bfloat16* base, int r0, int c0,
+                                                int lane) {
+  const int r = r0 + (lane & 7) + ((lane >> 3) & 1) * 8;
+  const int c = c0 + (lane >> 4) * 8;
+  return smem_u32(base + swz<RL>(r, c));
+}
+
+// ldmatrix.x4.trans address of a 16x16 A fragment (rows m0.., cols k0..)
+// when the tile stores A transposed (tile row = k, tile col = m).
+template <int RL>
+__device__ __forceinline__ uint32_t at_frag_addr(const __nv_bfloat16* base, int m0, int k0,
+                                                 int lane) {
+  const int mi = lane >> 3;
+  const int r = k0 + (lane & 7) + (mi >> 1) * 8;
+  const int c = m0 + (mi & 1) * 8;
+  return smem_u32(base + swz<RL>(r, c));
+}
+
+// ldmatrix.x4.trans address for two B fragments (k0..k0+15, n0..n0+15) of a
+// tile stored [k][n] (n contiguous): regs {b(n0)[0], b(n0)[1], b(n0+8)[0], b(n0+8)[1]}.
+template <int RL>
+__device__ __forceinline__ uint32_t bkn_frag_addr(const __nv_bfloat16* base, int k0, int n0,
+                                                  int lane) {
+  const int mi = lane >> 3;
+  const int r = k0 + (lane & 7) + (mi & 1) * 8;
+  const int c = n0 + (mi >> 1) * 8;
+  return smem_u32(base + swz<RL>(r, c));
+}
+
+// ldmatrix.x4 (no trans) address for two B fragments of a tile stored [n][k]
+// (k contiguous): regs {b(n0)[0], b(n0)[1], b(n0+8)[0], b(n0+8)[1]}.
+template <int RL>
+__device__ __forceinline__ uint32_t bnk_frag_addr(const __nv_bfloat16* base, int n0, int k0,
+                                                  int lane) {
+  const int mi = lane >> 3;
+  const int r = n0 + (lane & 7) + (mi >> 1) * 8;
+  const int c = k0 + (mi & 1) * 8;
+  return smem_u32(base + swz<RL>(r, c));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Split x into hi + lo bf16 with hi = bf16(x), lo = bf16(x - hi).
+__device__ __forceinline__ void split_bf16(float x, float& hi, float& lo) {
+  hi = __bfloat162float(__float2bfloat16_rn(x));
+  lo = x - hi;
+}
+
+__device__ __forceinline__ void st_bf16x2(__nv_bfloat16* p, float a, float b) {
+  *reinterpret_cast<uint32_t*>(p) = pack_bf16(a, b);
+}
+
+// ---------------------------------------------------------------------------
+// Async global -> shared copies (16 bytes; src_bytes == 0 zero-fills).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(src_bytes));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+}  // namespace gdn

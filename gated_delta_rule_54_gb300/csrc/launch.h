@@ -1,0 +1,43 @@
+// Internal launchers behind the C ABI (host side; arguments already validated).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdn_qdq.h"
+
+namespace gdn {
+
+constexpr int kChunkLen = 64;  // chunk length and state-scale tile width
+
+// Derived sizes of a validated problem.
+struct Dims {
+  int64_t B, T, N, n_slots, nt_fixed;  // nt_fixed = ceil(T/64) for fixed-length rows
+  int Hk, Hv, Dk, Dv;
+  bool packed;
+};
+
+// Byte offsets of the saved context segments (see gdn_ctx_bytes).
+struct CtxLayout {
+  size_t w_codes, w_scales, h_codes, h_scales, h_full, total;
+};
+
+Dims dims_of(const gdn_problem& p);
+CtxLayout ctx_layout(const gdn_problem& p);
+
+gdn_status launch_fake_qdq(int mode, const float* x, float* y, float* scales, uint8_t* codes,
+                           int64_t batch, int64_t rows, int64_t cols, int64_t group_cols,
+                           cudaStream_t st);
+
+gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const void* k,
+                      const void* v, const float* beta, const float* g, const float* h0,
+                      float* o, float* ht, void* ctx, cudaStream_t st);
+
+size_t bwd_workspace_bytes(const gdn_problem& p, const Dims& d);
+
+gdn_status launch_bwd(const gdn_problem& p, const Dims& d, const void* q, const void* k,
+                      const void* v, const float* beta, const float* g, const void* ctx,
+                      const void* dO, const float* dht, float* dq, float* dk, float* dv,
+                      float* dbeta, float* dg, float* dh0, void* ws, cudaStream_t st);
+
+}  // namespace gdn

@@ -1,0 +1,185 @@
+/*
+ * gdn_qdq.h — C ABI of the GB300 (sm_103a) chunked gated delta rule with
+ * dynamic fake quantize-dequantize (QDQ) at the recurrent-state and WY "W"
+ * sites, and its identity straight-through (STE) backward.
+ *
+ * Sources of the contract (GatedDeltaNet QAT pull-request pages):
+ *   "[1/4] GDN state/W QAT foundation", section "What does this PR do?":
+ *       chunk size 64, dynamic FP8 E4M3 fake QDQ at the state and W sites,
+ *       identity STE, exact triangular solve, the quantized W saved for
+ *       backward; unsupported formats and FP32 inputs are rejected before
+ *       launch; BF16 Q/K/V; grouped heads; packed sequences.
+ *   same page, section "Usage": state quantizer `axis (0, 1)` with
+ *       `state.block_v 64`, W quantizer `axis (0, 1, 2)`.
+ *   "[2/4] GDN/KDA decode QAT with INT8 recurrent state", sections "What
+ *       does this PR do?" and "Testing": signed symmetric dynamic INT8
+ *       (zero point 0, codes in [-127, 127], nearest-even rounding, per-head
+ *       [Dk, block_v] scales), gradients through initial states and split
+ *       carry, scale arithmetic x * fl(1/s).
+ *
+ * Conventions that hold for every entry point:
+ *   - Every tensor argument is a DEVICE pointer to contiguous row-major
+ *     memory owned by the caller.  The library never allocates, frees or
+ *     synchronizes; work is enqueued on `stream` (a cudaStream_t passed as
+ *     void*, NULL = legacy default stream) and returns before it finishes.
+ *   - Arguments are validated on the host before anything is launched; an
+ *     invalid call returns a negative gdn_status and enqueues nothing.  No
+ *     silent fallback exists: a configuration that is not supported is an
+ *     error.  GDN_ERR_CUDA reports a launch failure (cudaGetLastError).
+ *   - Notation: B batch rows, T tokens per row, Hk query/key heads, Hv value
+ *     heads (Hv % Hk == 0, value head h reads key head h / (Hv / Hk)), Dk key
+ *     dim, Dv value dim.  With packed sequences (cu_seqlens != NULL) B == 1,
+ *     T is the total token count and N sequences are described by the N+1
+ *     int32 offsets of cu_seqlens (device memory, cu[0] == 0, non-decreasing,
+ *     cu[N] == T).  Without it N == B and each row is one sequence.
+ *   - Chunks are 64 tokens from each sequence's start; a sequence's last
+ *     chunk may be shorter.  Per-chunk data is stored at a "chunk slot":
+ *       fixed length: slot(n, c) = n * ceil(T / 64) + c,  n_slots = B * ceil(T/64)
+ *       packed:       slot(n, c) = floor(cu[n] / 64) + n + c,  n_slots = floor(T/64) + N
+ *     (the packed formula is injective for any lengths; unused slots are
+ *     left untouched).
+ */
+#ifndef GDN_QDQ_H_
+#define GDN_QDQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GDN_QDQ_ABI_VERSION 1
+
+typedef enum {
+  GDN_QDQ_NONE = 0, /* site not quantized                                   */
+  GDN_QDQ_E4M3 = 1, /* dynamic FP8 E4M3: s = amax/448, RNE, satfinite      */
+  GDN_QDQ_INT8 = 2  /* dynamic signed symmetric INT8: s = amax/127, RNE    */
+} gdn_qdq_mode;
+
+typedef enum {
+  GDN_DTYPE_BF16 = 0, /* the only accepted q/k/v (and dO) element type    */
+  GDN_DTYPE_FP16 = 1, /* rejected                                          */
+  GDN_DTYPE_FP32 = 2  /* rejected before launch (first page, "What")       */
+} gdn_dtype;
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = -1,       /* null pointer, negative size, bad enum   */
+  GDN_ERR_UNSUPPORTED_DTYPE = -2, /* q/k/v/dO not bf16                        */
+  GDN_ERR_UNSUPPORTED_SHAPE = -3, /* Dk/Dv not 64/128, Hv % Hk, chunk != 64  */
+  GDN_ERR_UNSUPPORTED_MODE = -4,  /* QDQ mode or block_v not supported       */
+  GDN_ERR_WORKSPACE_TOO_SMALL = -5,
+  GDN_ERR_CUDA = -6,              /* a launch failed                         */
+  GDN_ERR_MISALIGNED = -7         /* a pointer is not 16-byte aligned        */
+} gdn_status;
+
+/* One problem description, shared by the forward and the backward. */
+typedef struct {
+  int64_t B;                  /* batch rows (1 when packed)                     */
+  int64_t T;                  /* tokens per row (total tokens when packed)      */
+  int32_t Hk, Hv, Dk, Dv;     /* heads and head dims; Dk, Dv in {64, 128}       */
+  int32_t N;                  /* sequences: == B, or packed count (>= 1)        */
+  const int32_t* cu_seqlens;  /* device [N + 1] int32, or NULL                  */
+  float scale;                /* output scale (1.0 for o_t = S_t q_t)           */
+  int32_t state_mode;         /* gdn_qdq_mode at the state site                 */
+  int32_t w_mode;             /* gdn_qdq_mode at the W site                     */
+  int32_t block_v;            /* state-scale tile width; must be 64            */
+  int32_t chunk;              /* chunk length; must be 64                      */
+  int32_t dtype;              /* gdn_dtype of q, k, v (and dO); must be BF16    */
+} gdn_problem;
+
+/* Human-readable name of a status code (static string). */
+const char* gdn_status_string(int status);
+
+/* GDN_QDQ_ABI_VERSION of the loaded library. */
+int gdn_abi_version(void);
+
+/* Host-only validation of a problem description (no CUDA call). */
+gdn_status gdn_validate(const gdn_problem* p);
+
+/* Number of chunk slots (see the header comment), or -1 if p is invalid. */
+int64_t gdn_num_chunk_slots(const gdn_problem* p);
+
+/*
+ * Bytes of the saved-for-backward context written by the forward when its
+ * `ctx` argument is non-NULL, or 0 if p is invalid.  Layout (each segment
+ * starts on a 256-byte boundary, in this order):
+ *   w_codes   u8  [B, T, Hv, Dk]        quantized W codes    (w_mode != NONE)
+ *   w_scales  f32 [n_slots, Hv]         W scale per chunk    (w_mode != NONE)
+ *   h_codes   u8  [n_slots, Hv, Dk, Dv] state codes entering each chunk (state_mode != NONE)
+ *   h_scales  f32 [n_slots, Hv, Dv/64]  state scale per [Dk, 64] tile  (state_mode != NONE)
+ *   h_full    f32 [n_slots, Hv, Dk, Dv] unquantized state entering each chunk (state_mode == NONE)
+ * E4M3 codes are OCP E4M3FN bytes; INT8 codes are two's-complement bytes.
+ * Code times scale (fp32 multiply) is the dequantized value; the context
+ * therefore holds the quantized W and states exactly.
+ */
+size_t gdn_ctx_bytes(const gdn_problem* p);
+
+/*
+ * Forward: o = chunked gated delta rule with state/W fake QDQ.
+ *   q, k  bf16 [B, T, Hk, Dk]      v   bf16 [B, T, Hv, Dv]
+ *   beta  f32  [B, T, Hv]          g   f32  [B, T, Hv] (log decay, alpha = exp g)
+ *   h0    f32  [N, Hv, Dk, Dv] initial state H = S^T, or NULL for zeros
+ *   o     f32  [B, T, Hv, Dv]      (written)
+ *   ht    f32  [N, Hv, Dk, Dv] final state, unquantized, or NULL (written)
+ *   ctx   gdn_ctx_bytes(p) bytes, 256-byte aligned, or NULL (written)
+ * Per chunk (method of the first page; the pages print no equations, this is
+ * the published WY form of the gated delta rule): gamma = in-chunk cumsum of
+ * g; A = strictly-lower(beta_i exp(gamma_i - gamma_j) k_i.k_j); T = (I+A)^-1;
+ * W = T diag(beta exp(gamma)) K, Q_W over the whole [L, Dk] tile; U = T
+ * diag(beta) V; H^ = Q_S(H) per [Dk, 64] tile (h0 included); Delta = U - W^ H^;
+ * o = scale (diag(exp(gamma)) Q H^ + (lower-incl(exp(gamma_i-gamma_j) q_i.k_j)) Delta);
+ * H <- exp(gamma_L) H^ + (diag(exp(gamma_L - gamma)) K)^T Delta.
+ * A sequence of length 0 returns ht = h0 (not quantized).
+ * All pointers must be 16-byte aligned (GDN_ERR_MISALIGNED otherwise).
+ */
+gdn_status gdn_chunk_fwd_qdq(const gdn_problem* p, const void* q, const void* k,
+                             const void* v, const float* beta, const float* g,
+                             const float* h0, float* o, float* ht, void* ctx, void* stream);
+
+/*
+ * Scratch bytes the backward needs in its `workspace` argument (caller
+ * allocated, 256-byte aligned), or 0 if p is invalid.
+ */
+size_t gdn_bwd_workspace_bytes(const gdn_problem* p);
+
+/*
+ * Backward with identity STE through both QDQ sites (first page, "What":
+ * identity straight-through; the quantized W saved by the forward is reused,
+ * no second quantizer call).  `ctx` is the forward's context for the same
+ * inputs.  Gradients of L = <dO, o> + <dht, ht>:
+ *   dO    bf16 [B, T, Hv, Dv]          dht f32 [N, Hv, Dk, Dv] or NULL (zeros)
+ *   dq,dk f32  [B, T, Hk, Dk]  (summed over the value heads sharing a key head)
+ *   dv    f32  [B, T, Hv, Dv]          dbeta, dg f32 [B, T, Hv]
+ *   dh0   f32  [N, Hv, Dk, Dv] or NULL
+ * All outputs are overwritten (not accumulated into).
+ */
+gdn_status gdn_chunk_bwd_ste(const gdn_problem* p, const void* q, const void* k,
+                             const void* v, const float* beta, const float* g, const void* ctx,
+                             const void* dO, const float* dht, float* dq, float* dk, float* dv,
+                             float* dbeta, float* dg, float* dh0, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/*
+ * Standalone fake QDQ of x: a contiguous f32 tensor [batch, rows, cols];
+ * one group per (batch index, block of group_cols consecutive columns)
+ * spanning all rows — [Dk, 64] state tiles are (rows = Dk, group_cols = 64),
+ * a whole-tensor group is (batch = 1, rows = 1, group_cols = cols).
+ *   y       f32 like x (written; may alias x)
+ *   scales  f32 [batch, cols / group_cols] (written; required)
+ *   codes   u8 like x, or NULL (written)
+ * Bit-exact definition: a = max|x|; a == 0 gives s = 0, y = x, signed-zero
+ * codes; else s = fl(a/M), r = fl(1/s), u = fl(x*r), code = RNE onto the
+ * E4M3FN grid with finite saturation (M = 448) or nearest-even integer
+ * clamped to [-127, 127] (M = 127), y = fl(code * s).
+ */
+gdn_status fake_qdq_e4m3(const float* x, float* y, float* scales, uint8_t* codes, int64_t batch,
+                         int64_t rows, int64_t cols, int64_t group_cols, void* stream);
+gdn_status fake_qdq_int8(const float* x, float* y, float* scales, uint8_t* codes, int64_t batch,
+                         int64_t rows, int64_t cols, int64_t group_cols, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* GDN_QDQ_H_ */

@@ -1,0 +1,100 @@
+"""Shared tolerance checks and oracle runners for the GPU parity tests.
+
+Tolerances (stated once, used everywhere):
+  outputs / final states:  max |x - r| <= 1e-2 * max|r|, and at least 99.9% of
+      elements satisfy |x - r| <= 1e-2 * |r| + 1e-6 * max|r| (the tiny floor
+      only absorbs exact zeros of r);
+  state codes (saved context): every differing code is one quantization step
+      away, and at most 0.1% of the codes differ;
+  gradients: relative L2 error ||x - r|| / ||r|| <= 2e-2 per tensor.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from oracle.chunked import chunked
+
+REL = 1e-2
+FLOOR = 1e-6
+FRAC = 1e-3
+CODE_FRAC = 1e-3
+GRAD_L2 = 2e-2
+
+
+def close_report(x, ref):
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    mx = float(np.abs(ref).max()) if ref.size else 0.0
+    err = np.abs(x - ref)
+    bad = err > REL * np.abs(ref) + FLOOR * mx
+    return dict(max_rel=float(err.max() / mx) if mx > 0 else float(err.max() if err.size else 0),
+                frac_bad=float(bad.mean()) if bad.size else 0.0, n=int(ref.size),
+                finite=bool(np.isfinite(x).all()))
+
+
+def assert_close(x, ref, what=""):
+    r = close_report(x, ref)
+    assert r["finite"], "%s: non-finite values" % what
+    assert r["max_rel"] <= REL, "%s: max |err| / max|ref| = %.3e" % (what, r["max_rel"])
+    assert r["frac_bad"] <= FRAC, "%s: %.3e of elements outside 1e-2 relative" % (what, r["frac_bad"])
+    return r
+
+
+def code_steps(a, b, mode):
+    """Distance in quantization steps between two code arrays (u8)."""
+    a = np.asarray(a, dtype=np.uint8)
+    b = np.asarray(b, dtype=np.uint8)
+    if mode == "int8":
+        return np.abs(a.view(np.int8).astype(np.int32) - b.view(np.int8).astype(np.int32))
+    sa = np.where(a & 0x80, -1, 1) * (a & 0x7F).astype(np.int32)
+    sb = np.where(b & 0x80, -1, 1) * (b & 0x7F).astype(np.int32)
+    return np.abs(sa - sb)
+
+
+def assert_codes(a, b, mode, what="codes"):
+    d = code_steps(a, b, mode)
+    frac = float((d > 0).mean()) if d.size else 0.0
+    assert d.max(initial=0) <= 1, "%s: a code differs by %d steps" % (what, int(d.max()))
+    assert frac <= CODE_FRAC, "%s: %.3e of codes differ" % (what, frac)
+    return frac
+
+
+def grad_rel_l2(x, ref):
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    den = np.linalg.norm(ref)
+    return float(np.linalg.norm(x - ref) / den) if den > 0 else float(np.linalg.norm(x))
+
+
+def slot_map(lengths, packed, T):
+    """For each dense chunk index (sequence after sequence), its chunk slot in
+    the library's context layout (see include/gdn_qdq.h)."""
+    out = []
+    if packed:
+        start = 0
+        for n, L in enumerate(lengths):
+            for c in range(-(-L // 64)):
+                out.append(start // 64 + n + c)
+            start += L
+    else:
+        nt = -(-T // 64)
+        for n in range(len(lengths)):
+            for c in range(nt):
+                out.append(n * nt + c)
+    return np.array(out, dtype=np.int64)
+
+
+def run_oracle(d, state_mode, w_mode, scale=1.0, record=False):
+    """O2 (chunked, fp64) on CPU inputs dict from synth.make_inputs."""
+    return chunked(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"],
+                   cu_seqlens=d.get("cu_seqlens"), scale=scale, state_mode=state_mode,
+                   w_mode=w_mode, record=record)
+
+
+def to_dev(d, device="cuda"):
+    out = {}
+    for k, v in d.items():
+        out[k] = v.to(device) if isinstance(v, torch.Tensor) else v
+    return out

@@ -1,0 +1,139 @@
+"""Host-side tests of the C ABI: the library loads without a GPU, exports every
+symbol the header declares, and rejects invalid problems before any CUDA call."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_delta_rule_54_gb300 import _lib
+from gated_delta_rule_54_gb300._lib import GdnProblem
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    src = open(os.path.join(ROOT, "include", "gdn_qdq.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*[\w\s\*]+?\b(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(n for n in names if n not in ("defined",)))
+
+
+def test_header_symbols_all_exported_and_bound():
+    lib = _lib.load()
+    declared = _declared_symbols()
+    assert "gdn_chunk_fwd_qdq" in declared and "fake_qdq_int8" in declared
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert set(declared) == set(_lib.SIGNATURES)
+
+
+def _problem(**kw):
+    p = GdnProblem()
+    p.B, p.T, p.Hk, p.Hv, p.Dk, p.Dv, p.N = 2, 300, 2, 4, 128, 128, 2
+    p.cu_seqlens = None
+    p.scale = 1.0
+    p.state_mode, p.w_mode, p.block_v, p.chunk, p.dtype = 1, 1, 64, 64, 0
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def _validate(p):
+    return _lib.load().gdn_validate(ctypes.byref(p))
+
+
+def test_validate_accepts_supported_problems():
+    assert _validate(_problem()) == 0
+    assert _validate(_problem(Dk=64, Dv=64)) == 0
+    assert _validate(_problem(state_mode=2, w_mode=1, Hv=8)) == 0
+    assert _validate(_problem(state_mode=0, w_mode=0)) == 0
+    assert _validate(_problem(B=1, N=5, cu_seqlens=4096)) == 0
+    assert _validate(_problem(T=0)) == 0
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(dtype=2), -2),                 # FP32 q/k/v rejected before launch
+    (dict(dtype=1), -2),
+    (dict(dtype=7), -1),
+    (dict(Dk=96), -3), (dict(Dv=256), -3),
+    (dict(Hv=3), -3),                    # Hv % Hk
+    (dict(chunk=32), -3),
+    (dict(block_v=32), -4),
+    (dict(state_mode=3), -1), (dict(w_mode=-1), -1),
+    (dict(B=-1), -1), (dict(Hk=0), -1),
+    (dict(N=3), -1),                     # N != B without cu_seqlens
+    (dict(B=2, N=2, cu_seqlens=4096), -1),  # packed needs B == 1
+    (dict(scale=float("nan")), -1),
+])
+def test_validate_rejects(kw, code):
+    assert _validate(_problem(**kw)) == code
+
+
+def test_sizes():
+    lib = _lib.load()
+    p = _problem()
+    nt = -(-300 // 64)
+    assert lib.gdn_num_chunk_slots(ctypes.byref(p)) == 2 * nt
+    al = lambda x: (x + 255) // 256 * 256
+    ns = 2 * nt
+    exp = al(2 * 300 * 4 * 128) + al(4 * ns * 4) + al(ns * 4 * 128 * 128) + al(4 * ns * 4 * 2)
+    assert lib.gdn_ctx_bytes(ctypes.byref(p)) == exp
+    p0 = _problem(state_mode=0, w_mode=0)
+    assert lib.gdn_ctx_bytes(ctypes.byref(p0)) == al(4 * ns * 4 * 128 * 128)
+    pk = _problem(B=1, T=1000, N=7, cu_seqlens=4096)
+    assert lib.gdn_num_chunk_slots(ctypes.byref(pk)) == 1000 // 64 + 7
+    assert lib.gdn_ctx_bytes(ctypes.byref(_problem(Dk=96))) == 0
+    assert lib.gdn_num_chunk_slots(ctypes.byref(_problem(Dk=96))) == -1
+
+
+def test_packed_slot_formula_is_injective():
+    # slot(n, c) = floor(cu[n]/64) + n + c never collides and stays below floor(T/64) + N
+    import numpy as np
+    rng = np.random.default_rng(0)
+    for _ in range(200):
+        lens = rng.integers(0, 300, rng.integers(1, 12))
+        cu = np.concatenate([[0], np.cumsum(lens)])
+        T, N = int(cu[-1]), len(lens)
+        slots = [cu[n] // 64 + n + c for n in range(N) for c in range(-(-int(lens[n]) // 64))]
+        assert len(set(slots)) == len(slots)
+        assert all(0 <= s < T // 64 + N for s in slots)
+
+
+def test_entry_points_reject_before_launch():
+    lib = _lib.load()
+    bad = _problem(dtype=2)
+    P = ctypes.c_void_p
+    fake = P(4096)
+    assert lib.gdn_chunk_fwd_qdq(ctypes.byref(bad), fake, fake, fake, fake, fake, None, fake,
+                                 None, None, None) == -2
+    ok = _problem()
+    # null inputs
+    assert lib.gdn_chunk_fwd_qdq(ctypes.byref(ok), None, fake, fake, fake, fake, None, fake,
+                                 None, None, None) == -1
+    # misaligned pointer
+    assert lib.gdn_chunk_fwd_qdq(ctypes.byref(ok), P(4097), fake, fake, fake, fake, None, fake,
+                                 None, None, None) == -7
+    # ctx must be 256-byte aligned
+    assert lib.gdn_chunk_fwd_qdq(ctypes.byref(ok), fake, fake, fake, fake, fake, None, fake,
+                                 None, P(4096 + 16), None) == -7
+    # backward: workspace too small
+    need = lib.gdn_bwd_workspace_bytes(ctypes.byref(ok))
+    if need > 0:
+        args = [fake] * 14
+        st = lib.gdn_chunk_bwd_ste(ctypes.byref(ok), *args[:6], fake, None, *[fake] * 5, None,
+                                   fake, ctypes.c_size_t(need - 1), None)
+        assert st == -5
+    # fake QDQ argument checks
+    assert lib.fake_qdq_e4m3(fake, fake, fake, None, 1, 4, 100, 64, None) == -1   # 100 % 64
+    assert lib.fake_qdq_int8(fake, fake, None, None, 1, 4, 128, 64, None) == -1   # scales required
+    assert lib.fake_qdq_int8(P(4098), fake, fake, None, 1, 4, 128, 64, None) == -7
+    assert lib.fake_qdq_e4m3(None, None, None, None, 0, 4, 128, 64, None) == 0     # empty
+
+
+def test_status_strings():
+    lib = _lib.load()
+    for code in range(-7, 1):
+        s = lib.gdn_status_string(code).decode()
+        assert s.startswith("GDN_")
+    assert lib.gdn_abi_version() == 1

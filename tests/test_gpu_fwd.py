@@ -1,0 +1,165 @@
+"""GPU parity of the forward (gdn_chunk_fwd_qdq, through the C ABI) against the fp64 oracle.
+
+Small cases span several chunks and ragged tails and are compared element by
+element; the full-size workloads run in the benchmark's launch configuration
+and are compared on sampled (sequence, key-head group) sub-problems that the
+oracle computes independently.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gated_delta_rule_54_gb300 import gdn_chunk_fwd_qdq, make_problem, split_ctx, synth
+
+from _parity import assert_close, assert_codes, run_oracle, slot_map, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _gpu_fwd(d, sm, wm, scale=1.0, save_ctx=True):
+    dd = to_dev(d)
+    o, ht, ctx = gdn_chunk_fwd_qdq(dd["q"], dd["k"], dd["v"], dd["beta"], dd["g"], dd["h0"],
+                                   cu_seqlens=dd["cu_seqlens"], scale=scale, state_mode=sm,
+                                   w_mode=wm, save_ctx=save_ctx)
+    torch.cuda.synchronize()
+    return dd, o, ht, ctx
+
+
+def _check_case(w, lengths=None, scale=1.0):
+    d = synth.make_inputs(w, lengths=lengths)
+    sm, wm = w.state_mode, w.w_mode
+    dd, o, ht, ctx = _gpu_fwd(d, sm, wm, scale)
+    o_ref, ht_ref, rec = run_oracle(d, sm, wm, scale=scale, record=True)
+    assert_close(o.cpu().numpy(), o_ref.numpy(), "o")
+    assert_close(ht.cpu().numpy(), ht_ref.numpy(), "ht")
+    p = make_problem(dd["q"], dd["k"], dd["v"], dd["cu_seqlens"], scale, sm, wm)
+    seg = split_ctx(ctx, p)
+    lens = lengths if lengths is not None else [w.T] * w.B
+    smap = slot_map(lens, lengths is not None, d["T"])
+    if sm != "none":
+        codes = seg["h_codes"].cpu().numpy()[smap]
+        assert_codes(codes, rec["state_codes"], sm, "state codes")
+        sc = seg["h_scales"].cpu().numpy()[smap]
+        assert np.allclose(sc, rec["state_scales"], rtol=1e-2, atol=0)
+    else:
+        hf = seg["h_full"].cpu().numpy()[smap]
+        assert hf.shape[0] == len(smap)
+    if wm != "none":
+        wc = seg["w_codes"].cpu().numpy().reshape(-1, w.Hv, w.Dk)
+        wref = np.concatenate(rec["w_codes"], 0).reshape(-1, w.Hv, w.Dk)
+        assert_codes(wc, wref, wm, "W codes")
+        ws = seg["w_scales"].cpu().numpy()[smap]
+        assert np.allclose(ws, rec["w_scales"], rtol=1e-3, atol=0)
+    return o, o_ref
+
+
+MODES = [("e4m3", "e4m3"), ("int8", "e4m3"), ("none", "none"), ("e4m3", "none"),
+         ("none", "e4m3"), ("int8", "int8"), ("int8", "none"), ("e4m3", "int8"), ("none", "int8")]
+
+
+@pytest.mark.parametrize("sm,wm", MODES)
+def test_fwd_modes(sm, wm):
+    w = synth.small(B=2, T=200, Hk=2, Hv=4, Dk=128, Dv=128, state_mode=sm, w_mode=wm, h0=True,
+                    seed=3)
+    _check_case(w)
+
+
+@pytest.mark.parametrize("T", [1, 3, 63, 64, 65, 127, 128, 257])
+def test_fwd_lengths(T):
+    w = synth.small(B=2, T=T, Hk=1, Hv=2, Dk=64, Dv=64, h0=(T % 2 == 1), seed=T)
+    _check_case(w)
+
+
+@pytest.mark.parametrize("Dk,Dv", [(64, 128), (128, 64), (64, 64)])
+def test_fwd_head_dims(Dk, Dv):
+    w = synth.small(B=1, T=190, Hk=2, Hv=2, Dk=Dk, Dv=Dv, h0=True, seed=Dk + Dv)
+    _check_case(w)
+
+
+def test_fwd_grouped_heads_int8_state():
+    w = synth.small(B=2, T=150, Hk=2, Hv=8, Dk=128, Dv=128, state_mode="int8", h0=True, seed=9)
+    _check_case(w)
+
+
+def test_fwd_packed_ragged_with_empty_sequence():
+    lengths = [0, 1, 64, 97, 130, 5, 200, 0, 63]
+    w = synth.small(B=1, T=0, Hk=2, Hv=4, Dk=128, Dv=128, h0=True, seed=4)
+    _check_case(w, lengths=lengths)
+
+
+def test_fwd_scale_and_tiny_workload():
+    _check_case(synth.WORKLOADS["tiny"])
+    w = synth.small(B=1, T=130, Hk=1, Hv=1, Dk=128, Dv=128, h0=True, seed=5)
+    _check_case(w, scale=128 ** -0.5)
+
+
+def test_fwd_qdq_sensitivity_and_disabled_path():
+    w = synth.small(B=1, T=256, Hk=2, Hv=2, Dk=128, Dv=128, h0=True, seed=6)
+    d = synth.make_inputs(w)
+    _, o_q, _, _ = _gpu_fwd(d, "e4m3", "e4m3")
+    _, o_n, _, _ = _gpu_fwd(d, "none", "none")
+    assert (o_q - o_n).abs().max().item() > 1e-3 * o_n.abs().max().item()
+    o1, _ = oracle.recurrent(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"])
+    assert_close(o_n.cpu().numpy(), o1, "disabled path vs token recurrence")
+
+
+def test_fwd_without_optional_outputs_and_zero_tokens():
+    w = synth.small(B=2, T=100, Hk=1, Hv=1, Dk=64, Dv=64, seed=7)
+    d = to_dev(synth.make_inputs(w))
+    o, ht, ctx = gdn_chunk_fwd_qdq(d["q"], d["k"], d["v"], d["beta"], d["g"],
+                                   output_final_state=False, save_ctx=False)
+    o2, _, _ = gdn_chunk_fwd_qdq(d["q"], d["k"], d["v"], d["beta"], d["g"], save_ctx=True)
+    assert ht is None and ctx is None
+    assert torch.equal(o, o2)   # deterministic, and saving the context changes nothing
+    # zero tokens: ht == h0, untouched by QDQ
+    z = {k: (v[:, :0].contiguous() if isinstance(v, torch.Tensor) and v.dim() >= 3 and k not in ("h0",) else v)
+         for k, v in d.items()}
+    h0 = torch.randn(2, 1, 64, 64, device="cuda")
+    o, ht, _ = gdn_chunk_fwd_qdq(z["q"], z["k"], z["v"], z["beta"], z["g"], h0)
+    torch.cuda.synchronize()
+    assert o.numel() == 0 and torch.equal(ht, h0)
+
+
+# ----------------------------------------------------------------------------
+# Full-size workloads, in the benchmark's launch configuration, on samples.
+# ----------------------------------------------------------------------------
+def _sample_check(name, picks):
+    w = synth.WORKLOADS[name]
+    d = synth.make_inputs(w)
+    dd, o, ht, ctx = _gpu_fwd(d, w.state_mode, w.w_mode, save_ctx=False)
+    o = o.cpu()
+    ht = ht.cpu()
+    G = w.Hv // w.Hk
+    cu = d["cu_seqlens"]
+    for n, hk in picks:
+        if cu is None:
+            q, k = d["q"][n:n + 1], d["k"][n:n + 1]
+            v, b, g = d["v"][n:n + 1], d["beta"][n:n + 1], d["g"][n:n + 1]
+            o_gpu = o[n:n + 1]
+        else:
+            a, e = int(cu[n]), int(cu[n + 1])
+            q, k = d["q"][:, a:e], d["k"][:, a:e]
+            v, b, g = d["v"][:, a:e], d["beta"][:, a:e], d["g"][:, a:e]
+            o_gpu = o[:, a:e]
+        hv = slice(hk * G, (hk + 1) * G)
+        h0 = d["h0"][n:n + 1, hv] if d["h0"] is not None else None
+        o_ref, ht_ref = run_oracle(dict(q=q[:, :, hk:hk + 1], k=k[:, :, hk:hk + 1],
+                                        v=v[:, :, hv], beta=b[:, :, hv], g=g[:, :, hv], h0=h0),
+                                   w.state_mode, w.w_mode)
+        assert_close(o_gpu[:, :, hv].numpy(), o_ref.numpy(), "%s o (n=%d, hk=%d)" % (name, n, hk))
+        assert_close(ht[n:n + 1, hv].numpy(), ht_ref.numpy(), "%s ht (n=%d, hk=%d)" % (name, n, hk))
+
+
+def test_full_single_layer_sampled():
+    _sample_check("layer", [(0, 0), (3, 15), (2, 7)])
+
+
+def test_full_grouped_int8_sampled():
+    _sample_check("grouped_int8", [(0, 0), (1, 15)])
+
+
+def test_full_packed_varlen_sampled():
+    lens = synth.varlen_lengths(32768)
+    picks = [(0, 0), (len(lens) - 1, 31), (int(np.argmax(lens)), 5), (int(np.argmin(lens)), 17)]
+    _sample_check("varlen", picks)
