@@ -61,61 +61,110 @@ def _max_over_ranks(x, ws, device):
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    """SM clock and clock-event (throttle) reasons sampled every millisecond
+    through NVML (read-only queries) while the timed region runs; falls back to
+    ``nvidia-smi -lms 200`` when NVML cannot be loaded."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
-    def __init__(self, device_index):
-        self.idx = device_index
+    def __init__(self, device):
+        self.device = device
+        self.samples = []      # (sm_mhz, max_mhz, reasons_mask)
+        self.stop = threading.Event()
+        self.nvml = None
         self.proc = None
         self.lines = []
 
+    def _open_nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            return None
+        prop = torch.cuda.get_device_properties(self.device)
+        bus = ("%04x:%02x:%02x.0" % (getattr(prop, "pci_domain_id", 0), prop.pci_bus_id,
+                                     prop.pci_device_id)).encode()
+        h = ctypes.c_void_p()
+        if lib.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+            cnt = ctypes.c_uint()
+            if lib.nvmlDeviceGetCount_v2(ctypes.byref(cnt)) != 0 or cnt.value != 1 or \
+                    lib.nvmlDeviceGetHandleByIndex_v2(0, ctypes.byref(h)) != 0:
+                return None
+        self._c = ctypes
+        return lib, h
+
+    def _poll(self):
+        lib, h = self.nvml
+        c = self._c
+        sm, mx, rs = c.c_uint(), c.c_uint(), c.c_ulonglong()
+        fn_r = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self.stop.is_set():
+            if lib.nvmlDeviceGetClockInfo(h, 1, c.byref(sm)) == 0 and \
+                    lib.nvmlDeviceGetMaxClockInfo(h, 1, c.byref(mx)) == 0 and \
+                    fn_r(h, c.byref(rs)) == 0:
+                self.samples.append((sm.value, mx.value, rs.value))
+            time.sleep(0.001)
+
     def __enter__(self):
         try:
+            self.nvml = self._open_nvml()
+        except (OSError, AttributeError):
+            self.nvml = None
+        if self.nvml is not None:
+            self.th = threading.Thread(target=self._poll, daemon=True)
+            self.th.start()
+            t0 = time.time()
+            while not self.samples and time.time() - t0 < 2.0:
+                time.sleep(0.001)
+            self.samples.clear()
+            return self
+        try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                ["nvidia-smi", "-i", str(self.device.index), "--query-gpu=clocks.sm,clocks.max.sm,"
+                 "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap",
                  "--format=csv,noheader,nounits", "-lms", "200"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.th = threading.Thread(target=self._read, daemon=True)
             self.th.start()
-        except (OSError, FileNotFoundError):
+            time.sleep(0.5)
+        except OSError:
             self.proc = None
         return self
 
     def _read(self):
+        names = [0x8, 0x40, 0x20, 0x4]
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            f = [x.strip() for x in line.split(",")]
+            try:
+                mask = sum(b for b, v in zip(names, f[2:6]) if v.lower() == "active")
+                self.samples.append((float(f[0]), float(f[1]), mask))
+            except (ValueError, IndexError):
+                continue
 
     def __exit__(self, *a):
+        self.stop.set()
         if self.proc is not None:
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
                 self.proc.kill()
+        if hasattr(self, "th"):
             self.th.join(timeout=2)
 
     def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            f = [x.strip() for x in ln.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                mx.append(float(f[2]))
-            except ValueError:
-                continue
-            for nm, val in zip(names, f[5:9]):
-                if val.lower() == "active":
-                    reasons.add(nm)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "source": "nvml" if self.nvml else "nvidia-smi"}
+        mask = 0
+        for _, _, m in self.samples:
+            mask |= m
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples),
+                "sm_max_mhz": max(s[1] for s in self.samples),
+                "reasons": sorted(v for b, v in self.REASONS.items() if mask & b),
+                "samples": len(self.samples), "source": "nvml" if self.nvml else "nvidia-smi"}
 
 
 def _peaks():
@@ -245,7 +294,7 @@ def run_ours(args, ws, rank, local):
     torch.cuda.synchronize()
     _barrier(ws)
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with ClockSampler(dev) as clk:
         t_start, t_end = ev(), ev()
         t_start.record(stream)
         for _ in range(args.steps):

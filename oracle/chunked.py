@@ -170,6 +170,8 @@ def _collect(recs, Hv, Dk, Dv, chunk, block_v, state_mode, w_mode):
     sc_codes, sc_scales, w_codes, w_scales = [], [], [], []
     for rec, S, L in recs:
         nchk = -(-L // chunk)
+        if nchk == 0:        # an empty sequence has no chunk boundary and no W tile
+            continue
         if state_mode != "none":
             # rec["s"][c] = (codes [S*Hv,Dk,Dv], scales [S*Hv, Dv/block_v])
             cds = np.stack([c for c, _ in rec["s"]], 0).reshape(nchk, S, Hv, Dk, Dv)
@@ -187,10 +189,10 @@ def _collect(recs, Hv, Dk, Dv, chunk, block_v, state_mode, w_mode):
                     w_scales.append(sc.reshape(S, Hv)[s])
                 w_codes.append(np.concatenate(per, 0))
     out = {}
-    if state_mode != "none":
+    if state_mode != "none" and sc_codes:
         out["state_codes"] = np.concatenate(sc_codes, 0)
         out["state_scales"] = np.concatenate(sc_scales, 0)
-    if w_mode != "none":
+    if w_mode != "none" and w_codes:
         out["w_codes"] = w_codes
         out["w_scales"] = np.stack(w_scales, 0)
     return out
