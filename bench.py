@@ -500,7 +500,7 @@ def main():
         torch.distributed.destroy_process_group()
 
 
-BWD_LAUNCHES = 0   # kernels one backward call launches
+BWD_LAUNCHES = 2   # kernels one backward call launches (reverse scan + chunk gradients)
 
 
 def _backward_available():

@@ -197,3 +197,111 @@ __device__ __forceinline__ void cp_async_wait() {
 }
 
 }  // namespace gdn
+
+namespace gdn {
+
+// ---------------------------------------------------------------------------
+// Warp-level tile GEMM on tensor cores:
+//   acc[NT][4] += A[m0:m0+16, k0:k1] * B[k0:k1, n0:n0+8*NT]      (k in steps of 16)
+// A is a row-major [m][k] tile (AT = false) or is stored transposed as [k][m]
+// (AT = true); B is stored [k][n] (BKN = true) or [n][k] (BKN = false).
+// RLA / RLB are the row lengths (elements) of the swizzled tiles.
+// ---------------------------------------------------------------------------
+template <int NT, bool AT, bool BKN, int RLA, int RLB>
+__device__ __forceinline__ void wgemm(float (&acc)[NT][4], const __nv_bfloat16* A, int m0,
+                                      const __nv_bfloat16* B, int n0, int k0, int k1, int lane) {
+  static_assert(NT % 2 == 0, "n tiles come in pairs");
+  for (int k = k0; k < k1; k += 16) {
+    uint32_t a[4];
+    if constexpr (AT)
+      ldsm_x4_t(a, at_frag_addr<RLA>(A, m0, k, lane));
+    else
+      ldsm_x4(a, a_frag_addr<RLA>(A, m0, k, lane));
+#pragma unroll
+    for (int np = 0; np < NT / 2; ++np) {
+      uint32_t b[4];
+      if constexpr (BKN)
+        ldsm_x4_t(b, bkn_frag_addr<RLB>(B, k, n0 + 16 * np, lane));
+      else
+        ldsm_x4(b, bnk_frag_addr<RLB>(B, n0 + 16 * np, k, lane));
+      mma_bf16(acc[2 * np], a, b[0], b[1]);
+      mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
+    }
+  }
+}
+
+template <int NT>
+__device__ __forceinline__ void zero_acc(float (&acc)[NT][4]) {
+#pragma unroll
+  for (int i = 0; i < NT; ++i)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
+}
+
+// ---------------------------------------------------------------------------
+// T = (I + A)^-1 for a strictly lower-triangular fp32 A [64][64] in shared
+// memory (row stride 64), written to Ts (lower triangle and diagonal; the
+// strictly upper part of Ts is left undefined).  Blocked forward
+// substitution: the four 16x16 diagonal blocks by substitution (one thread
+// per column), then T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22, then
+// the lower-left 32x32 block T_LL = -T_LR A_LL T_UL.  The strictly upper part
+// of As is used as scratch.  All 256 threads of the CTA must call this; it
+// synchronizes internally and on return Ts is complete.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void solve_unit_lower64(float* As, float* Ts) {
+  const int tid = threadIdx.x;
+  if (tid < 64) {
+    const int b = tid >> 4, cc = tid & 15;
+    const float* Ab = As + (16 * b) * 64 + 16 * b;
+    float x[16];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      float acc = 0.f;
+#pragma unroll
+      for (int j = 0; j < r; ++j) acc = fmaf(Ab[r * 64 + j], x[j], acc);
+      x[r] = (r == cc) ? 1.f : (r < cc ? 0.f : -acc);
+    }
+#pragma unroll
+    for (int r = 0; r < 16; ++r) Ts[(16 * b + r) * 64 + 16 * b + cc] = x[r];
+  }
+  __syncthreads();
+  for (int e = tid; e < 512; e += 256) {
+    const int pr = e >> 8, i = (e >> 4) & 15, j = e & 15;
+    const int base = 32 * pr;
+    float acc = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk)
+      acc = fmaf(As[(base + 16 + i) * 64 + base + kk], Ts[(base + kk) * 64 + base + j], acc);
+    As[(base + i) * 64 + base + 16 + j] = acc;
+  }
+  __syncthreads();
+  for (int e = tid; e < 512; e += 256) {
+    const int pr = e >> 8, i = (e >> 4) & 15, j = e & 15;
+    const int base = 32 * pr;
+    float acc = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < 16; ++kk)
+      acc = fmaf(Ts[(base + 16 + i) * 64 + base + 16 + kk], As[(base + kk) * 64 + base + 16 + j],
+                 acc);
+    Ts[(base + 16 + i) * 64 + base + j] = -acc;
+  }
+  __syncthreads();
+  for (int e = tid; e < 1024; e += 256) {
+    const int i = e >> 5, j = e & 31;
+    float acc = 0.f;
+    const int k0 = (j >= 16) ? 16 : 0;
+    for (int kk = k0; kk < 32; ++kk) acc = fmaf(As[(32 + i) * 64 + kk], Ts[kk * 64 + j], acc);
+    As[i * 64 + 32 + j] = acc;
+  }
+  __syncthreads();
+  for (int e = tid; e < 1024; e += 256) {
+    const int i = e >> 5, j = e & 31;
+    float acc = 0.f;
+    const int k1 = (i < 16) ? 16 : 32;
+    for (int kk = 0; kk < k1; ++kk) acc = fmaf(Ts[(32 + i) * 64 + 32 + kk], As[kk * 64 + 32 + j], acc);
+    Ts[(32 + i) * 64 + j] = -acc;
+  }
+  __syncthreads();
+}
+
+}  // namespace gdn

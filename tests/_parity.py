@@ -2,10 +2,16 @@
 
 Tolerances (stated once, used everywhere):
   outputs / final states:  max |x - r| <= 1e-2 * max|r|, and at least 99.9% of
-      elements satisfy |x - r| <= 1e-2 * |r| + 1e-6 * max|r| (the tiny floor
-      only absorbs exact zeros of r);
-  state codes (saved context): every differing code is one quantization step
-      away, and at most 0.1% of the codes differ;
+      elements satisfy |x - r| <= 1e-2 * |r| + 1e-3 * max|r| (relative error,
+      with an absolute floor ten times below the max-abs bound for elements
+      of r near zero);
+  state / W codes: every differing code is one quantization step away, and at
+      most 0.1% of the codes differ;
+  units with a permitted flip: a (sequence, value head) whose state or W codes
+      contain a one-step flip may deviate by the consequences of that flip —
+      one E4M3 step is at most 2^-3 of the flipped element, so its outputs and
+      final state are held to max |x - r| <= 2^-3 * max|r| instead; every
+      other unit keeps the bounds above;
   gradients: relative L2 error ||x - r|| / ||r|| <= 2e-2 per tensor.
 """
 from __future__ import annotations
@@ -17,7 +23,8 @@ import oracle
 from oracle.chunked import chunked
 
 REL = 1e-2
-FLOOR = 1e-6
+FLOOR = 1e-3
+FLIP_REL = 2.0 ** -3
 FRAC = 1e-3
 CODE_FRAC = 1e-3
 GRAD_L2 = 2e-2
@@ -40,6 +47,25 @@ def assert_close(x, ref, what=""):
     assert r["max_rel"] <= REL, "%s: max |err| / max|ref| = %.3e" % (what, r["max_rel"])
     assert r["frac_bad"] <= FRAC, "%s: %.3e of elements outside 1e-2 relative" % (what, r["frac_bad"])
     return r
+
+
+def assert_close_units(x, ref, unit_of, flipped, what=""):
+    """x, ref indexed [..., unit-major]; unit_of(idx) -> key; flipped: set of keys.
+    Applies assert_close to the union of unflipped units and the looser
+    FLIP_REL bound to each flipped unit."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    mask = unit_of(x.shape)           # integer unit key per element
+    keys = set(np.unique(mask).tolist())
+    ok = np.isin(mask, [k for k in keys if k not in flipped])
+    if ok.any():
+        assert_close(x[ok], ref[ok], what + " (units without flips)")
+    for k in keys & set(flipped):
+        sel = mask == k
+        mx = float(np.abs(ref[sel]).max())
+        err = float(np.abs(x[sel] - ref[sel]).max())
+        assert np.isfinite(x[sel]).all()
+        assert err <= FLIP_REL * mx + 1e-30, "%s: unit %s with a flip deviates %.3e" % (what, k, err / mx)
 
 
 def code_steps(a, b, mode):

@@ -12,7 +12,8 @@ import torch
 import oracle
 from gated_delta_rule_54_gb300 import gdn_chunk_fwd_qdq, make_problem, split_ctx, synth
 
-from _parity import assert_close, assert_codes, run_oracle, slot_map, to_dev
+from _parity import (assert_close, assert_close_units, assert_codes, code_steps, run_oracle,
+                     slot_map, to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -31,17 +32,22 @@ def _check_case(w, lengths=None, scale=1.0):
     sm, wm = w.state_mode, w.w_mode
     dd, o, ht, ctx = _gpu_fwd(d, sm, wm, scale)
     o_ref, ht_ref, rec = run_oracle(d, sm, wm, scale=scale, record=True)
-    assert_close(o.cpu().numpy(), o_ref.numpy(), "o")
-    assert_close(ht.cpu().numpy(), ht_ref.numpy(), "ht")
     p = make_problem(dd["q"], dd["k"], dd["v"], dd["cu_seqlens"], scale, sm, wm)
     seg = split_ctx(ctx, p)
-    lens = lengths if lengths is not None else [w.T] * w.B
-    smap = slot_map(lens, lengths is not None, d["T"])
+    packed = lengths is not None
+    lens = list(lengths) if packed else [w.T] * w.B
+    smap = slot_map(lens, packed, d["T"])
+    # sequence index of every dense chunk and of every token
+    chunk_seq = np.concatenate([[n] * (-(-L // 64)) for n, L in enumerate(lens)] or [[]]).astype(int)
+    flipped = set()
     if sm != "none":
         codes = seg["h_codes"].cpu().numpy()[smap]
         assert_codes(codes, rec["state_codes"], sm, "state codes")
         sc = seg["h_scales"].cpu().numpy()[smap]
         assert np.allclose(sc, rec["state_scales"], rtol=1e-2, atol=0)
+        diff = code_steps(codes, rec["state_codes"], sm).reshape(len(smap), w.Hv, -1).max(-1)
+        for ci, h in zip(*np.nonzero(diff)):
+            flipped.add((int(chunk_seq[ci]), int(h)))
     else:
         hf = seg["h_full"].cpu().numpy()[smap]
         assert hf.shape[0] == len(smap)
@@ -51,6 +57,27 @@ def _check_case(w, lengths=None, scale=1.0):
         assert_codes(wc, wref, wm, "W codes")
         ws = seg["w_scales"].cpu().numpy()[smap]
         assert np.allclose(ws, rec["w_scales"], rtol=1e-3, atol=0)
+        tok_seq = np.concatenate([[n] * L for n, L in enumerate(lens)] or [[]]).astype(int)
+        diff = code_steps(wc, wref, wm).max(-1)
+        for t, h in zip(*np.nonzero(diff)):
+            flipped.add((int(tok_seq[t]), int(h)))
+    Hv = w.Hv
+    key = lambda n, h: n * Hv + h
+    fl = {key(n, h) for n, h in flipped}
+    tok_seq = np.concatenate([[n] * L for n, L in enumerate(lens)] or [[]]).astype(int)
+
+    def o_units(shape):           # o [B, T, Hv, Dv]
+        B, T = shape[0], shape[1]
+        seq = tok_seq.reshape(B, T) if B * T else np.zeros((B, T), int)
+        return (seq[:, :, None, None] * Hv + np.arange(Hv)[None, None, :, None]) + 0 * np.zeros(shape, int)
+
+    def h_units(shape):           # ht [N, Hv, Dk, Dv]
+        return (np.arange(shape[0])[:, None, None, None] * Hv +
+                np.arange(Hv)[None, :, None, None]) + 0 * np.zeros(shape, int)
+
+    if o.numel():
+        assert_close_units(o.cpu().numpy(), o_ref.numpy(), o_units, fl, "o")
+    assert_close_units(ht.cpu().numpy(), ht_ref.numpy(), h_units, fl, "ht")
     return o, o_ref
 
 
