@@ -6,7 +6,8 @@ Tolerances (stated once, used everywhere):
       with an absolute floor ten times below the max-abs bound for elements
       of r near zero);
   state / W codes: every differing code is one quantization step away, and at
-      most 0.1% of the codes differ;
+      most 0.1% of the codes differ (at least one flip is always allowed: a
+      single flip in a few hundred codes is consistent with a 1e-5 flip rate);
   units with a permitted flip: a (sequence, value head) whose state or W codes
       contain a one-step flip may deviate by the consequences of that flip —
       one E4M3 step is at most 2^-3 of the flipped element, so its outputs and
@@ -81,9 +82,10 @@ def code_steps(a, b, mode):
 
 def assert_codes(a, b, mode, what="codes"):
     d = code_steps(a, b, mode)
-    frac = float((d > 0).mean()) if d.size else 0.0
+    nflip = int((d > 0).sum())
+    frac = nflip / d.size if d.size else 0.0
     assert d.max(initial=0) <= 1, "%s: a code differs by %d steps" % (what, int(d.max()))
-    assert frac <= CODE_FRAC, "%s: %.3e of codes differ" % (what, frac)
+    assert nflip <= max(1, CODE_FRAC * d.size), "%s: %.3e of codes differ" % (what, frac)
     return frac
 
 
