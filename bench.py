@@ -334,34 +334,31 @@ def run_ours(args, ws, rank, local):
     e2e = None
     if not args.no_e2e:
         host = {kk: (vv.pin_memory() if isinstance(vv, torch.Tensor) else vv) for kk, vv in cpu.items()}
-        o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-        ht_h = torch.empty(ht.shape, dtype=ht.dtype).pin_memory()
         bufs = dict(q=q, k=k, v=v, beta=beta, g=g, h0=h0)
-        h2d = sum(host[n].numel() * host[n].element_size() for n in bufs if host[n] is not None)
-        d2h = o_h.numel() * 4 + ht_h.numel() * 4
         if bwd:
-            do_h = do.cpu().pin_memory()
-            dht_h = dht.cpu().pin_memory()
-            h2d += do_h.numel() * 2 + dht_h.numel() * 4
-            grads_h = None
+            host["do"] = do.cpu().pin_memory()
+            host["dht"] = dht.cpu().pin_memory()
+            bufs.update(do=do, dht=dht)
+            grads = (torch.empty_like(q, dtype=torch.float32), torch.empty_like(k, dtype=torch.float32),
+                     torch.empty_like(v, dtype=torch.float32), torch.empty_like(beta),
+                     torch.empty_like(g), torch.empty_like(ht))
+            results = (o, ht) + grads
+        else:
+            results = (o, ht)
+        res_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in results]
+        h2d = sum(host[n].numel() * host[n].element_size() for n in bufs if host[n] is not None)
+        d2h = sum(t.numel() * t.element_size() for t in res_h)
 
         def e2e_step():
             for n, t in bufs.items():
                 if t is not None:
                     t.copy_(host[n], non_blocking=True)
             api.gdn_chunk_fwd_qdq(q, k, v, beta, g, h0, state_mode=sm, w_mode=wm, out=(o, ht, ctx))
-            o_h.copy_(o, non_blocking=True)
-            ht_h.copy_(ht, non_blocking=True)
-            out = 0
             if bwd:
-                do.copy_(do_h, non_blocking=True)
-                dht.copy_(dht_h, non_blocking=True)
-                gr = api.gdn_chunk_bwd_ste(q, k, v, beta, g, ctx, do, dht, state_mode=sm,
-                                           w_mode=wm, workspace=wsb)
-                for t in gr:
-                    if t is not None:
-                        t.cpu()
-            return out
+                api.gdn_chunk_bwd_ste(q, k, v, beta, g, ctx, do, dht, state_mode=sm, w_mode=wm,
+                                      workspace=wsb, out=grads)
+            for dst, src in zip(res_h, results):
+                dst.copy_(src, non_blocking=True)
 
         for _ in range(max(1, args.warmup)):
             e2e_step()
@@ -374,8 +371,6 @@ def run_ours(args, ws, rank, local):
         b.record(stream)
         torch.cuda.synchronize()
         e_ms = _max_over_ranks(a.elapsed_time(b), ws, dev)
-        if bwd:
-            d2h += (2 * q.numel() + v.numel() + 2 * beta.numel() + ht.numel()) * 4
         e2e = {"value": round(tokens * ws * args.steps / (e_ms / 1e3), 1), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(e_ms / args.steps, 4)}

@@ -103,8 +103,10 @@ def gdn_chunk_fwd_qdq(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, sta
 
 
 def gdn_chunk_bwd_ste(q, k, v, beta, g, ctx, do, dht=None, cu_seqlens=None, scale=1.0,
-                      state_mode="e4m3", w_mode="e4m3", need_dh0=True, workspace=None):
-    """Identity-STE backward.  Returns (dq, dk, dv, dbeta, dg, dh0 or None)."""
+                      state_mode="e4m3", w_mode="e4m3", need_dh0=True, workspace=None, out=None):
+    """Identity-STE backward.  Returns (dq, dk, dv, dbeta, dg, dh0 or None).
+
+    ``out`` may pass preallocated (dq, dk, dv, dbeta, dg, dh0) buffers."""
     lib = load()
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g), ("ctx", ctx),
@@ -115,12 +117,15 @@ def gdn_chunk_bwd_ste(q, k, v, beta, g, ctx, do, dht=None, cu_seqlens=None, scal
     p = make_problem(q, k, v, cu_seqlens, scale, state_mode, w_mode)
     check("gdn_validate", lib.gdn_validate(ctypes.byref(p)))
     f32 = dict(device=dev, dtype=torch.float32)
-    dq = torch.empty(k.shape, **f32)
-    dk = torch.empty(k.shape, **f32)
-    dv = torch.empty(v.shape, **f32)
-    dbeta = torch.empty(beta.shape, **f32)
-    dg = torch.empty(g.shape, **f32)
-    dh0 = torch.empty(p.N, v.shape[2], k.shape[3], v.shape[3], **f32) if need_dh0 else None
+    if out is not None:
+        dq, dk, dv, dbeta, dg, dh0 = out
+    else:
+        dq = torch.empty(k.shape, **f32)
+        dk = torch.empty(k.shape, **f32)
+        dv = torch.empty(v.shape, **f32)
+        dbeta = torch.empty(beta.shape, **f32)
+        dg = torch.empty(g.shape, **f32)
+        dh0 = torch.empty(p.N, v.shape[2], k.shape[3], v.shape[3], **f32) if need_dh0 else None
     need = int(lib.gdn_bwd_workspace_bytes(ctypes.byref(p)))
     if workspace is None:
         workspace = torch.empty(max(need, 1), device=dev, dtype=torch.uint8)
