@@ -55,6 +55,8 @@ def _barrier(ws):
 def _max_over_ranks(x, ws, device):
     if ws == 1:
         return x
+    if torch.distributed.get_backend() == "gloo":
+        device = torch.device("cpu")
     t = torch.tensor([x], dtype=torch.float64, device=device)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
