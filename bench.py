@@ -319,7 +319,7 @@ def run_ours(args, ws, rank, local):
         alg = bwd_alg_bytes(w)
         dur = bwd_ms
         kernel = "gdn backward (all launches of one call)"
-        traffic = _traffic("bwd_fwd_bwd_workload.md", BWD_SOURCES, args.workload)
+        traffic = _traffic("gdn_bwd_kernels_single_layer.md", BWD_SOURCES, args.workload)
     else:
         alg = fwd_alg_bytes(w, bwd)
         dur = fwd_ms
