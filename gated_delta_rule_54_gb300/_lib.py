@@ -48,6 +48,8 @@ SIGNATURES = {
     "gdn_bwd_workspace_bytes": (_SZ, [_PP]),
     "gdn_chunk_bwd_ste": (ctypes.c_int, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                                          _P, _P, _P, _SZ, _P]),
+    "gdn_chunk_bwd_ste_noalloc": (ctypes.c_int, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                                 _P, _P, _P, _P]),
     "fake_qdq_e4m3": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
     "fake_qdq_int8": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
 }

@@ -162,6 +162,29 @@ gdn_status gdn_chunk_bwd_ste(const gdn_problem* p, const void* q, const void* k,
                              size_t workspace_bytes, void* stream);
 
 /*
+ * Allocation-free backward.  The paper has no counterpart: this is an entry
+ * point for callers that cannot allocate device memory when they call the
+ * backward (for example a runtime that reserved the device's memory up front
+ * for its own pool, or code where an allocation would synchronize the
+ * device), so they cannot provide gdn_chunk_bwd_ste's workspace.
+ * Same arguments, meaning and results as gdn_chunk_bwd_ste without
+ * `workspace` / `workspace_bytes`: the scratch comes from a fixed device array
+ * of GDN_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
+ * the library holds until the process exits.  Problems whose
+ * gdn_bwd_workspace_bytes(p) exceeds that size are rejected before any launch
+ * with GDN_ERR_WORKSPACE_TOO_SMALL.  The first call on a device looks up the
+ * array's device address (once per device, that device current) — make it
+ * before any stream capture.  Calls share the array: calls that overlap on the
+ * GPU race; the call clears what must start at zero.  Allocates nothing.
+ */
+#define GDN_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+gdn_status gdn_chunk_bwd_ste_noalloc(const gdn_problem* p, const void* q, const void* k,
+                                     const void* v, const float* beta, const float* g,
+                                     const void* ctx, const void* dO, const float* dht, float* dq,
+                                     float* dk, float* dv, float* dbeta, float* dg, float* dh0,
+                                     void* stream);
+
+/*
  * Standalone fake QDQ of x: a contiguous f32 tensor [batch, rows, cols];
  * one group per (batch index, block of group_cols consecutive columns)
  * spanning all rows — [Dk, 64] state tiles are (rows = Dk, group_cols = 64),
