@@ -32,7 +32,8 @@ namespace gdn {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
 
 struct BwdParams {
   const __nv_bfloat16* q;
@@ -154,8 +155,8 @@ struct ScanSmem {
   static constexpr int DD = EDO + kTile64;               // dDelta bf16
   static constexpr int DH = DD + kTile64;                // dH bf16 [DK][64]
   static constexpr int AS = DH + DK * 64 * 2;            // f32 [64][64] (W recompute only)
-  static constexpr int TS = AS + (WM == GDN_QDQ_NONE ? 16384 : 0);
-  static constexpr int TW = TS + (WM == GDN_QDQ_NONE ? 16384 : 0);
+  static constexpr int TS = AS + (WM == GDN_QDQ_NONE ? kF32Tile : 0);
+  static constexpr int TW = TS + (WM == GDN_QDQ_NONE ? kF32Tile : 0);
   static constexpr int BYTES = TW + (WM == GDN_QDQ_NONE ? kTile64 : 0);
   static_assert(BYTES <= 232448, "shared memory budget");
 };
@@ -208,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const BwdPara
   __nv_bfloat16* dHb = reinterpret_cast<__nv_bfloat16*>(sm + S::DH);
 
   // state-gradient tile layout: as the forward's state tile
-  constexpr int HM = DK / 16, HN = 8 / HM, NTH = 8 / HN;
+  constexpr int HM = DK / 16, HN = kWarps / HM, NTH = 8 / HN;
   const int h_row0 = (warp % HM) * 16;
   const int h_col0 = (warp / HM) * (64 / HN);
   float dH[NTH][4];
@@ -238,7 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const BwdPara
   }
   cp_async_commit();
 
-  const int rt = warp & 3, ch = warp >> 2;
+  const int rt = warp & 3, cq = warp >> 2;
+  const int row0 = rt * 16, col0 = cq * 16;
   for (int it = 0; it < nch; ++it) {
     const int c = nch - 1 - it;
     const int buf = it & 1;
@@ -278,22 +280,19 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const BwdPara
       *reinterpret_cast<uint4*>(p.ws_dh + ((slot * p.Hv + h) * DK + d) * p.Dv + vb * 64 + c8 * 8) = val;
     }
     // P = lower-incl(Gamma QK^T) and e^gamma dO
-    {
-      const int row0 = rt * 16, col0 = ch * 32;
-      if (col0 <= row0 + 15) {
-        float acc[4][4];
-        zero_acc(acc);
-        wgemm<4, false, false, DK, DK>(acc, Qs, row0, Ks, col0, 0, DK, lane);
+    if (cq <= rt) {
+      float acc[2][4];
+      zero_acc(acc);
+      wgemm<2, false, false, DK, DK>(acc, Qs, row0, Ks, col0, 0, DK, lane);
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-          for (int e2 = 0; e2 < 2; ++e2) {
-            const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-            const float x0 = (j <= i) ? expf(gam[i] - gam[j]) * acc[nt][2 * e2] : 0.f;
-            const float x1 = (j + 1 <= i) ? expf(gam[i] - gam[j + 1]) * acc[nt][2 * e2 + 1] : 0.f;
-            st_bf16x2(Pb + swz<64>(i, j), x0, x1);
-          }
-      }
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
+          const float x0 = (j <= i) ? expf(gam[i] - gam[j]) * acc[nt][2 * e2] : 0.f;
+          const float x1 = (j + 1 <= i) ? expf(gam[i] - gam[j + 1]) * acc[nt][2 * e2 + 1] : 0.f;
+          st_bf16x2(Pb + swz<64>(i, j), x0, x1);
+        }
     }
     for (int e = threadIdx.x; e < kChunk * 32; e += kThreads) {
       const int r = e >> 5, col = (e & 31) * 2;
@@ -307,41 +306,38 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const BwdPara
       float* Ts = reinterpret_cast<float*>(sm + S::TS);
       __nv_bfloat16* Tw = reinterpret_cast<__nv_bfloat16*>(sm + S::TW);
       const float* bs = bg;
-      {
-        const int row0 = rt * 16, col0 = ch * 32;
-        if (col0 <= row0 + 15) {
-          float acc[4][4];
-          zero_acc(acc);
-          wgemm<4, false, false, DK, DK>(acc, Ks, row0, Ks, col0, 0, DK, lane);
+      if (cq <= rt) {
+        float acc[2][4];
+        zero_acc(acc);
+        wgemm<2, false, false, DK, DK>(acc, Ks, row0, Ks, col0, 0, DK, lane);
 #pragma unroll
-          for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int i = row0 + gq + 8 * (e >> 1), j = col0 + nt * 8 + 2 * tq + (e & 1);
-              As[i * 64 + j] = (j < i) ? bs[i] * expf(gam[i] - gam[j]) * acc[nt][e] : 0.f;
-            }
-        }
+          for (int e = 0; e < 4; ++e) {
+            const int i = row0 + gq + 8 * (e >> 1), j = col0 + nt * 8 + 2 * tq + (e & 1);
+            As[i * kSA + j] = (j < i) ? bs[i] * expf(gam[i] - gam[j]) * acc[nt][e] : 0.f;
+          }
       }
       __syncthreads();
-      solve_unit_lower64(As, Ts);
+      solve_unit_lower64<kThreads>(As, Ts);
       for (int e = threadIdx.x; e < 64 * 32; e += kThreads) {
         const int i = e >> 5, j = (e & 31) * 2;
-        const float t0 = (j <= i) ? Ts[i * 64 + j] * beg[j] : 0.f;
-        const float t1 = (j + 1 <= i) ? Ts[i * 64 + j + 1] * beg[j + 1] : 0.f;
+        const float t0 = (j <= i) ? Ts[i * kSA + j] * beg[j] : 0.f;
+        const float t1 = (j + 1 <= i) ? Ts[i * kSA + j + 1] * beg[j + 1] : 0.f;
         st_bf16x2(Tw + swz<64>(i, j), t0, t1);
       }
       __syncthreads();
       {
-        constexpr int NTW = DK / 16;
-        const int row0 = rt * 16, col0 = ch * (DK / 2);
+        constexpr int NTW = DK / 32;
+        const int wcol0 = cq * (DK / 4);
         float acc[NTW][4];
         zero_acc(acc);
-        wgemm<NTW, false, true, 64, DK>(acc, Tw, row0, Ks, col0, 0, 64, lane);
+        wgemm<NTW, false, true, 64, DK>(acc, Tw, row0, Ks, wcol0, 0, 64, lane);
 #pragma unroll
         for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
-            const int i = row0 + gq + 8 * e2, col = col0 + nt * 8 + 2 * tq;
+            const int i = row0 + gq + 8 * e2, col = wcol0 + nt * 8 + 2 * tq;
             st_bf16x2(Wv + swz<DK>(i, col), acc[nt][2 * e2], acc[nt][2 * e2 + 1]);
           }
       }
@@ -350,14 +346,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const BwdPara
 
     // dDelta = scale P^T dO + dec_i (K dH)
     {
-      const int row0 = rt * 16, col0 = ch * 32;
-      float a1[4][4], a2[4][4];
+      float a1[2][4], a2[2][4];
       zero_acc(a1);
       zero_acc(a2);
-      wgemm<4, true, true, 64, 64>(a1, Pb, row0, dOs, col0, row0, 64, lane);
-      wgemm<4, false, true, DK, 64>(a2, Ks, row0, dHb, col0, 0, DK, lane);
+      wgemm<2, true, true, 64, 64>(a1, Pb, row0, dOs, col0, row0, 64, lane);
+      wgemm<2, false, true, DK, 64>(a2, Ks, row0, dHb, col0, 0, DK, lane);
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -418,9 +413,9 @@ struct ChunkSmem {
   static constexpr int WV = DO + kTile64;          // W^ values bf16 [64][DK] -> later dW
   static constexpr int HH = WV + kTileK;           // H^ values bf16 [DK][64] -> later dT, X, dKK
   static constexpr int DHP = HH + DK * 64 * 2;     // dH' bf16 [DK][64]
-  static constexpr int AS = DHP + DK * 64 * 2;     // f32 [64][64]: A (lower), solve scratch (upper)
-  static constexpr int TS = AS + 16384;            // f32 [64][64]: T; u8 code staging before that
-  static constexpr int GKK = TS + 16384;           // bf16 Gamma KK (strict lower)
+  static constexpr int AS = DHP + DK * 64 * 2;     // f32 [64][kSA]: A (lower), solve scratch (upper)
+  static constexpr int TS = AS + kF32Tile;         // f32 [64][kSA]: T; u8 code staging before that
+  static constexpr int GKK = TS + kF32Tile;        // bf16 Gamma KK (strict lower)
   static constexpr int PB = GKK + kTile64;         // bf16 P
   static constexpr int TB = PB + kTile64;          // bf16 T
   static constexpr int TU = TB + kTile64;          // bf16 T diag(beta) -> later Gm
@@ -428,23 +423,25 @@ struct ChunkSmem {
   static constexpr int DDB = DB + kTile64;         // bf16 dDelta
   static constexpr int VEC = DDB + kTile64;        // gam, eg, dec, bet, beg, bg staging (2 x 64)
   static constexpr int RACC = VEC + 7 * 256;       // per-row partial sums [kSlots][64] + 8 scalars
-  static constexpr int kSlots = 22;
-  static constexpr int BYTES = RACC + kSlots * 256 + 64;
+  static constexpr int kSlots = 36;
+  static constexpr int BYTES = RACC + kSlots * 256 + 4 * (16 + 2);
   static_assert(BYTES <= 232448, "shared memory budget");
   static_assert(2 * kChunk * DK <= 32768, "code staging fits in As + Ts");
 };
 
 // racc slot indices (each a [64] row of partial sums; written exactly once)
+// (four slots per kind: one per column quarter for row sums, one per row
+// quarter for column sums)
 enum : int {
-  R_PPR = 0,   // 2: row sums of dP * P, per column half
-  R_PPC = 2,   // 4: column sums of dP * P, per row quarter
-  R_AAR = 6,   // 2: row sums of dA * A
-  R_AAC = 8,   // 4: column sums of dA * A
-  R_OH = 12,   // 2: sum_d q_id (dQ_inter)_id
-  R_TT = 14,   // 2: sum_d k_id (Delta dH'^T)_id  (times dec_i)
-  R_KW = 16,   // 2: sum_d k_id (T^T dW)_id
-  R_BU = 18,   // 2: sum_n v_in (T^T dU)_in
-  R_BA = 20,   // 2: sum_j dA_ij Gamma_ij KK_ij
+  R_PPR = 0,   // row sums of dP * P
+  R_PPC = 4,   // column sums of dP * P
+  R_AAR = 8,   // row sums of dA * A
+  R_AAC = 12,  // column sums of dA * A
+  R_OH = 16,   // sum_d q_id (dQ_inter)_id
+  R_TT = 20,   // sum_d k_id (Delta dH'^T)_id  (times dec_i)
+  R_KW = 24,   // sum_d k_id (T^T dW)_id
+  R_BU = 28,   // sum_n v_in (T^T dU)_in
+  R_BA = 32,   // sum_j dA_ij Gamma_ij KK_ij
 };
 
 // Row partial sums of a warp's [16 x 8*NT] accumulator tile: returns, for
@@ -464,11 +461,12 @@ __device__ __forceinline__ void row_sums(const float (&x)[NT][4], float& r0, flo
   r1 += __shfl_xor_sync(0xffffffffu, r1, 2);
 }
 
-// Column partial sums of a warp's [16 x 32] tile (NT = 4): for lanes with
-// gq == 0, c[nt][e] is the sum over the 16 rows of column 8 nt + 2 tq + e.
-__device__ __forceinline__ void col_sums4(const float (&x)[4][4], float (&c)[4][2]) {
+// Column partial sums of a warp's [16 x 8*NT] tile: for lanes with gq == 0,
+// c[nt][e] is the sum over the 16 rows of column 8 nt + 2 tq + e.
+template <int NT>
+__device__ __forceinline__ void col_sums(const float (&x)[NT][4], float (&c)[NT][2]) {
 #pragma unroll
-  for (int nt = 0; nt < 4; ++nt)
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       float s = x[nt][e] + x[nt][2 + e];
@@ -488,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
   const int hk = h / p.G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
-  const int rt = warp & 3, ch = warp >> 2;
+  const int rt = warp & 3, ch = warp >> 2;   // row quarter, column quarter
 
   // chunk slot -> (sequence, chunk)
   int n, c;
@@ -538,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
   float* gs = gam + 320;   // g staging
   float* bsg = gam + 384;  // beta staging
   float* racc = reinterpret_cast<float*>(sm + S::RACC);
-  float* hd_part = racc + S::kSlots * 64;  // [8]
+  float* hd_part = racc + S::kSlots * 64;  // [kWarps] <H^, dH'> partials, then [2] sums of t_i
 
   // ---- loads ----
   load_rows_bf16<DK>(Ks, p.k + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
@@ -617,15 +615,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
 
   // ---- KK^T -> A (f32) and Gamma KK (bf16); QK^T -> P (bf16) ----
   {
-    const int row0 = rt * 16, col0 = ch * 32;
-    if (col0 <= row0 + 15) {
-      float akk[4][4], aqk[4][4];
+    const int row0 = rt * 16, col0 = ch * 16;
+    if (ch <= rt) {
+      float akk[2][4], aqk[2][4];
       zero_acc(akk);
       zero_acc(aqk);
-      wgemm<4, false, false, DK, DK>(akk, Ks, row0, Ks, col0, 0, DK, lane);
-      wgemm<4, false, false, DK, DK>(aqk, Qs, row0, Ks, col0, 0, DK, lane);
+      wgemm<2, false, false, DK, DK>(akk, Ks, row0, Ks, col0, 0, DK, lane);
+      wgemm<2, false, false, DK, DK>(aqk, Qs, row0, Ks, col0, 0, DK, lane);
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -633,15 +631,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
           const float x1 = (j + 1 <= i) ? expf(gam[i] - gam[j + 1]) : 0.f;
           const float gk0 = (j < i) ? x0 * akk[nt][2 * e2] : 0.f;
           const float gk1 = (j + 1 < i) ? x1 * akk[nt][2 * e2 + 1] : 0.f;
-          As[i * 64 + j] = bet[i] * gk0;
-          As[i * 64 + j + 1] = bet[i] * gk1;
+          As[i * kSA + j] = bet[i] * gk0;
+          As[i * kSA + j + 1] = bet[i] * gk1;
           st_bf16x2(GKKb + swz<64>(i, j), gk0, gk1);
           st_bf16x2(Pb + swz<64>(i, j), x0 * aqk[nt][2 * e2], x1 * aqk[nt][2 * e2 + 1]);
         }
     } else {
       // strictly-upper tiles of GKK and P are read by the transposed products
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -653,11 +651,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
   __syncthreads();
 
   // ---- a3: T = (I + A)^-1 ----
-  solve_unit_lower64(As, Ts);
+  solve_unit_lower64<kThreads>(As, Ts);
   for (int e = threadIdx.x; e < 64 * 32; e += kThreads) {
     const int i = e >> 5, j = (e & 31) * 2;
-    const float t0 = (j <= i) ? Ts[i * 64 + j] : 0.f;
-    const float t1 = (j + 1 <= i) ? Ts[i * 64 + j + 1] : 0.f;
+    const float t0 = (j <= i) ? Ts[i * kSA + j] : 0.f;
+    const float t1 = (j + 1 <= i) ? Ts[i * kSA + j + 1] : 0.f;
     st_bf16x2(Tb + swz<64>(i, j), t0, t1);
     if constexpr (WM == GDN_QDQ_NONE)
       st_bf16x2(Tub + swz<64>(i, j), t0 * beg[j], t1 * beg[j + 1]);
@@ -667,8 +665,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
   __syncthreads();
   if constexpr (WM == GDN_QDQ_NONE) {
     // W = (T diag(beta e^gamma)) K, then Tu = T diag(beta) in the same buffer
-    constexpr int NTW = DK / 16;
-    const int row0 = rt * 16, col0 = ch * (DK / 2);
+    constexpr int NTW = DK / 32;
+    const int row0 = rt * 16, col0 = ch * (DK / 4);
     float acc[NTW][4];
     zero_acc(acc);
     wgemm<NTW, false, true, 64, DK>(acc, Tub, row0, Ks, col0, 0, 64, lane);
@@ -682,8 +680,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
     __syncthreads();
     for (int e = threadIdx.x; e < 64 * 32; e += kThreads) {
       const int i = e >> 5, j = (e & 31) * 2;
-      const float t0 = (j <= i) ? Ts[i * 64 + j] : 0.f;
-      const float t1 = (j + 1 <= i) ? Ts[i * 64 + j + 1] : 0.f;
+      const float t0 = (j <= i) ? Ts[i * kSA + j] : 0.f;
+      const float t1 = (j + 1 <= i) ? Ts[i * kSA + j + 1] : 0.f;
       st_bf16x2(Tub + swz<64>(i, j), t0 * bet[j], t1 * bet[j + 1]);
     }
     __syncthreads();
@@ -691,19 +689,19 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
 
   // ---- Delta = Tu V - W^ H^;  dDelta = scale P^T dO + dec (K dH') ----
   {
-    const int row0 = rt * 16, col0 = ch * 32;
-    float u[4][4], wh[4][4];
+    const int row0 = rt * 16, col0 = ch * 16;
+    float u[2][4], wh[2][4];
     zero_acc(u);
     zero_acc(wh);
-    wgemm<4, false, true, 64, 64>(u, Tub, row0, Vs, col0, 0, 64, lane);
-    wgemm<4, false, true, DK, 64>(wh, Wv, row0, Hh, col0, 0, DK, lane);
-    float a1[4][4], a2[4][4];
+    wgemm<2, false, true, 64, 64>(u, Tub, row0, Vs, col0, 0, 64, lane);
+    wgemm<2, false, true, DK, 64>(wh, Wv, row0, Hh, col0, 0, DK, lane);
+    float a1[2][4], a2[2][4];
     zero_acc(a1);
     zero_acc(a2);
-    wgemm<4, true, true, 64, 64>(a1, Pb, row0, dOs, col0, row0, 64, lane);
-    wgemm<4, false, true, DK, 64>(a2, Ks, row0, dHp, col0, 0, DK, lane);
+    wgemm<2, true, true, 64, 64>(a1, Pb, row0, dOs, col0, row0, 64, lane);
+    wgemm<2, false, true, DK, 64>(a2, Ks, row0, dHp, col0, 0, DK, lane);
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -716,8 +714,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
   }
   __syncthreads();
 
-  constexpr int NTW = DK / 16;
-  const int wrow0 = rt * 16, wcol0 = ch * (DK / 2);
+  constexpr int NTW = DK / 32;
+  const int wrow0 = rt * 16, wcol0 = ch * (DK / 4);
   float dQ[NTW][4], dK[NTW][4];
   zero_acc(dQ);
   zero_acc(dK);
@@ -725,13 +723,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
   // ---- output-side products ----
   {
     // dP = lower-incl(scale dO Delta^T); Gm = dP Gamma (into Tu's buffer); PP = dP P
-    const int row0 = rt * 16, col0 = ch * 32;
-    float dp[4][4];
+    const int row0 = rt * 16, col0 = ch * 16;
+    float dp[2][4];
     zero_acc(dp);
-    wgemm<4, false, false, 64, 64>(dp, dOs, row0, Db, col0, 0, 64, lane);
-    float pp[4][4];
+    wgemm<2, false, false, 64, 64>(dp, dOs, row0, Db, col0, 0, 64, lane);
+    float pp[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -747,16 +745,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
         st_bf16x2(Gmb + swz<64>(i, j), gm[0], gm[1]);
       }
     float r0, r1;
-    row_sums<4>(pp, r0, r1);
+    row_sums<2>(pp, r0, r1);
     if (tq == 0) {
       racc[(R_PPR + ch) * 64 + row0 + gq] = r0;
       racc[(R_PPR + ch) * 64 + row0 + gq + 8] = r1;
     }
-    float cs[4][2];
-    col_sums4(pp, cs);
+    float cs[2][2];
+    col_sums<2>(pp, cs);
     if (gq == 0)
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) racc[(R_PPC + rt) * 64 + col0 + nt * 8 + 2 * tq + e] = cs[nt][e];
   }
@@ -822,14 +820,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
 
   {
     // dT = (dDelta V^T) diag(beta) + (dW K^T) diag(beta e^gamma)  -> dTb
-    const int row0 = rt * 16, col0 = ch * 32;
-    float a1[4][4], a2[4][4];
+    const int row0 = rt * 16, col0 = ch * 16;
+    float a1[2][4], a2[2][4];
     zero_acc(a1);
     zero_acc(a2);
-    wgemm<4, false, false, 64, 64>(a1, dDb, row0, Vs, col0, 0, 64, lane);
-    wgemm<4, false, false, DK, DK>(a2, dWb, row0, Ks, col0, 0, DK, lane);
+    wgemm<2, false, false, 64, 64>(a1, dDb, row0, Vs, col0, 0, 64, lane);
+    wgemm<2, false, false, DK, DK>(a2, dWb, row0, Ks, col0, 0, DK, lane);
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -837,12 +835,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
                   a1[nt][2 * e2 + 1] * bet[j + 1] + a2[nt][2 * e2 + 1] * beg[j + 1]);
       }
     // T^T dU: dV = beta (T^T dDelta); row sums of v * (T^T dDelta)
-    float tu[4][4];
+    float tu[2][4];
     zero_acc(tu);
-    wgemm<4, true, true, 64, 64>(tu, Tb, row0, dDb, col0, 0, 64, lane);
-    float bv[4][4];
+    wgemm<2, true, true, 64, 64>(tu, Tb, row0, dDb, col0, 0, 64, lane);
+    float bv[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -854,7 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
               make_float2(bet[i] * tu[nt][2 * e2], bet[i] * tu[nt][2 * e2 + 1]);
       }
     float r0, r1;
-    row_sums<4>(bv, r0, r1);
+    row_sums<2>(bv, r0, r1);
     if (tq == 0) {
       racc[(R_BU + ch) * 64 + row0 + gq] = r0;
       racc[(R_BU + ch) * 64 + row0 + gq + 8] = r1;
@@ -887,12 +885,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
   __syncthreads();  // dT complete
   {
     // X = T^T dT
-    const int row0 = rt * 16, col0 = ch * 32;
-    float acc[4][4];
+    const int row0 = rt * 16, col0 = ch * 16;
+    float acc[2][4];
     zero_acc(acc);
-    wgemm<4, true, true, 64, 64>(acc, Tb, row0, dTb, col0, 0, 64, lane);
+    wgemm<2, true, true, 64, 64>(acc, Tb, row0, dTb, col0, 0, 64, lane);
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -902,13 +900,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
   __syncthreads();
   {
     // dA = -X T^T (strictly lower): dKK = dA beta_i Gamma_ij; dbeta += dA GKK; AA = dA A
-    const int row0 = rt * 16, col0 = ch * 32;
-    float acc[4][4];
+    const int row0 = rt * 16, col0 = ch * 16;
+    float acc[2][4];
     zero_acc(acc);
-    wgemm<4, false, false, 64, 64>(acc, Xb, row0, Tb, col0, 0, 64, lane);
-    float ba[4][4], aa[4][4];
+    wgemm<2, false, false, 64, 64>(acc, Xb, row0, Tb, col0, 0, 64, lane);
+    float ba[2][4], aa[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -920,26 +918,26 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
           const float gkk = __bfloat162float(GKKb[swz<64>(i, jj)]);
           kk[e] = da * bet[i] * ((jj < i) ? expf(gam[i] - gam[jj]) : 0.f);
           ba[nt][2 * e2 + e] = da * gkk;
-          aa[nt][2 * e2 + e] = da * As[i * 64 + jj] * ((jj < i) ? 1.f : 0.f);
+          aa[nt][2 * e2 + e] = da * As[i * kSA + jj] * ((jj < i) ? 1.f : 0.f);
         }
         st_bf16x2(dKKb + swz<64>(i, j), kk[0], kk[1]);
       }
     float r0, r1;
-    row_sums<4>(ba, r0, r1);
+    row_sums<2>(ba, r0, r1);
     if (tq == 0) {
       racc[(R_BA + ch) * 64 + row0 + gq] = r0;
       racc[(R_BA + ch) * 64 + row0 + gq + 8] = r1;
     }
-    row_sums<4>(aa, r0, r1);
+    row_sums<2>(aa, r0, r1);
     if (tq == 0) {
       racc[(R_AAR + ch) * 64 + row0 + gq] = r0;
       racc[(R_AAR + ch) * 64 + row0 + gq + 8] = r1;
     }
-    float cs[4][2];
-    col_sums4(aa, cs);
+    float cs[2][2];
+    col_sums<2>(aa, cs);
     if (gq == 0)
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) racc[(R_AAC + rt) * 64 + col0 + nt * 8 + 2 * tq + e] = cs[nt][e];
   }
@@ -951,17 +949,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
   // ---- dgamma -> dg (reverse cumsum), dbeta (warps 0-1, fixed-order sums) ----
   if (warp < 2) {
     const int i = threadIdx.x;  // row 0..63
-    const float rr = racc[(R_PPR) * 64 + i] + racc[(R_PPR + 1) * 64 + i];
-    const float cc = racc[(R_PPC) * 64 + i] + racc[(R_PPC + 1) * 64 + i] +
-                     racc[(R_PPC + 2) * 64 + i] + racc[(R_PPC + 3) * 64 + i];
-    const float ar = racc[(R_AAR) * 64 + i] + racc[(R_AAR + 1) * 64 + i];
-    const float ac = racc[(R_AAC) * 64 + i] + racc[(R_AAC + 1) * 64 + i] +
-                     racc[(R_AAC + 2) * 64 + i] + racc[(R_AAC + 3) * 64 + i];
-    const float oh = racc[(R_OH) * 64 + i] + racc[(R_OH + 1) * 64 + i];
-    const float tt = racc[(R_TT) * 64 + i] + racc[(R_TT + 1) * 64 + i];
-    const float kw = racc[(R_KW) * 64 + i] + racc[(R_KW + 1) * 64 + i];
-    const float bu = racc[(R_BU) * 64 + i] + racc[(R_BU + 1) * 64 + i];
-    const float ba = racc[(R_BA) * 64 + i] + racc[(R_BA + 1) * 64 + i];
+    auto sum4 = [&](int slot) {
+      return (racc[slot * 64 + i] + racc[(slot + 1) * 64 + i]) +
+             (racc[(slot + 2) * 64 + i] + racc[(slot + 3) * 64 + i]);
+    };
+    const float rr = sum4(R_PPR), cc = sum4(R_PPC), ar = sum4(R_AAR), ac = sum4(R_AAC);
+    const float oh = sum4(R_OH), tt = sum4(R_TT), kw = sum4(R_KW), bu = sum4(R_BU);
+    const float ba = sum4(R_BA);
     float dgam = (rr - cc) + (ar - ac) + oh - tt + beg[i] * kw;
     const float dbeta = bu + eg[i] * kw + ba;
     // gamma_L (row 63) collects e^{gL} <H^, dH'> + sum_i t_i
@@ -970,14 +964,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
     for (int o = 16; o > 0; o >>= 1) tsum += __shfl_xor_sync(0xffffffffu, tsum, o);
     racc[i] = dgam;           // reuse slot 0 (fully consumed above by this thread only)
     racc[64 + i] = dbeta;
-    if (lane == 0) hd_part[8 + warp] = tsum;
+    if (lane == 0) hd_part[kWarps + warp] = tsum;
   }
   __syncthreads();
   if (warp == 0) {
     float hd = 0.f;
 #pragma unroll
-    for (int w = 0; w < 8; ++w) hd += hd_part[w];
-    const float extra = eg[63] * hd + hd_part[8] + hd_part[9];
+    for (int w = 0; w < kWarps; ++w) hd += hd_part[w];
+    const float extra = eg[63] * hd + hd_part[kWarps] + hd_part[kWarps + 1];
     // reverse cumsum over rows 63..0 of dgamma (row 63 gets the gamma_L terms)
     const float x1 = racc[2 * lane + 1] + (lane == 31 ? extra : 0.f);
     const float x0 = racc[2 * lane];

@@ -92,7 +92,7 @@ __device__ __forceinline__ float warp_max(float v) {
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
                                          uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
@@ -238,68 +238,126 @@ __device__ __forceinline__ void zero_acc(float (&acc)[NT][4]) {
     for (int e = 0; e < 4; ++e) acc[i][e] = 0.f;
 }
 
+// Row stride (floats) of the fp32 [64][64] tiles A and T in shared memory:
+// 72 keeps 64-bit accesses of 16 rows conflict free and rows 16-byte aligned.
+constexpr int kSA = 72;
+constexpr int kF32Tile = 64 * kSA * 4;  // bytes
+
 // ---------------------------------------------------------------------------
-// T = (I + A)^-1 for a strictly lower-triangular fp32 A [64][64] in shared
-// memory (row stride 64), written to Ts (lower triangle and diagonal; the
-// strictly upper part of Ts is left undefined).  Blocked forward
-// substitution: the four 16x16 diagonal blocks by substitution (one thread
-// per column), then T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32 T_22, then
-// the lower-left 32x32 block T_LL = -T_LR A_LL T_UL.  The strictly upper part
-// of As is used as scratch.  All 256 threads of the CTA must call this; it
-// synchronizes internally and on return Ts is complete.
+// T = (I + A)^-1 for a strictly lower-triangular fp32 A [64][kSA] in shared
+// memory, written to Ts (lower triangle and diagonal; the strictly upper part
+// of Ts is left undefined).  Blocked forward substitution: the four 16x16
+// diagonal blocks by right-looking substitution (one thread per column; after
+// x_j is known its contribution is pushed to all later rows, so the dependent
+// chain is 16 FMAs long), then T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32
+// T_22, then the lower-left 32x32 block T_LL = -T_LR A_LL T_UL.  The block
+// products give each thread four consecutive columns (one 16-byte load of the
+// right operand per step).  The strictly upper part of As is scratch.  All
+// NTHREADS threads of the CTA call this; it synchronizes internally and Ts is
+// complete on return.
 // ---------------------------------------------------------------------------
+template <int NTHREADS>
 __device__ __forceinline__ void solve_unit_lower64(float* As, float* Ts) {
+  static_assert(NTHREADS == 256 || NTHREADS == 512, "thread count");
   const int tid = threadIdx.x;
   if (tid < 64) {
     const int b = tid >> 4, cc = tid & 15;
-    const float* Ab = As + (16 * b) * 64 + 16 * b;
-    float x[16];
+    const float* Ab = As + (16 * b) * kSA + 16 * b;
+    float x[16], acc[16];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      float acc = 0.f;
+    for (int r = 0; r < 16; ++r) acc[r] = 0.f;
 #pragma unroll
-      for (int j = 0; j < r; ++j) acc = fmaf(Ab[r * 64 + j], x[j], acc);
-      x[r] = (r == cc) ? 1.f : (r < cc ? 0.f : -acc);
+    for (int j = 0; j < 16; ++j) {
+      x[j] = (j == cc) ? 1.f : ((j < cc) ? 0.f : -acc[j]);
+#pragma unroll
+      for (int r = j + 1; r < 16; ++r) acc[r] = fmaf(Ab[r * kSA + j], x[j], acc[r]);
     }
 #pragma unroll
-    for (int r = 0; r < 16; ++r) Ts[(16 * b + r) * 64 + 16 * b + cc] = x[r];
+    for (int r = 0; r < 16; ++r) Ts[(16 * b + r) * kSA + 16 * b + cc] = x[r];
   }
   __syncthreads();
-  for (int e = tid; e < 512; e += 256) {
-    const int pr = e >> 8, i = (e >> 4) & 15, j = e & 15;
-    const int base = 32 * pr;
-    float acc = 0.f;
+  // X = A_10 T_00 -> As[0:16][16:32];  Y = A_32 T_22 -> As[32:48][48:64]
+  if (tid < 128) {
+    const int base = 32 * (tid >> 6), i = (tid >> 2) & 15, j0 = (tid & 3) * 4;
+    const float* a = As + (base + 16 + i) * kSA + base;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk)
-      acc = fmaf(As[(base + 16 + i) * 64 + base + kk], Ts[(base + kk) * 64 + base + j], acc);
-    As[(base + i) * 64 + base + 16 + j] = acc;
+    for (int kk = 0; kk < 16; ++kk) {
+      const float av = a[kk];
+      const float4 t = *reinterpret_cast<const float4*>(Ts + (base + kk) * kSA + base + j0);
+      acc.x = fmaf(av, t.x, acc.x);
+      acc.y = fmaf(av, t.y, acc.y);
+      acc.z = fmaf(av, t.z, acc.z);
+      acc.w = fmaf(av, t.w, acc.w);
+    }
+    *reinterpret_cast<float4*>(As + (base + i) * kSA + base + 16 + j0) = acc;
   }
   __syncthreads();
-  for (int e = tid; e < 512; e += 256) {
-    const int pr = e >> 8, i = (e >> 4) & 15, j = e & 15;
-    const int base = 32 * pr;
-    float acc = 0.f;
+  // T_10 = -T_11 X;  T_32 = -T_33 Y
+  if (tid < 128) {
+    const int base = 32 * (tid >> 6), i = (tid >> 2) & 15, j0 = (tid & 3) * 4;
+    const float* t = Ts + (base + 16 + i) * kSA + base + 16;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int kk = 0; kk < 16; ++kk)
-      acc = fmaf(Ts[(base + 16 + i) * 64 + base + 16 + kk], As[(base + kk) * 64 + base + 16 + j],
-                 acc);
-    Ts[(base + 16 + i) * 64 + base + j] = -acc;
+    for (int kk = 0; kk < 16; ++kk) {
+      const float tv = t[kk];
+      const float4 x = *reinterpret_cast<const float4*>(As + (base + kk) * kSA + base + 16 + j0);
+      acc.x = fmaf(tv, x.x, acc.x);
+      acc.y = fmaf(tv, x.y, acc.y);
+      acc.z = fmaf(tv, x.z, acc.z);
+      acc.w = fmaf(tv, x.w, acc.w);
+    }
+    *reinterpret_cast<float4*>(Ts + (base + 16 + i) * kSA + base + j0) =
+        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
   }
   __syncthreads();
-  for (int e = tid; e < 1024; e += 256) {
-    const int i = e >> 5, j = e & 31;
-    float acc = 0.f;
-    const int k0 = (j >= 16) ? 16 : 0;
-    for (int kk = k0; kk < 32; ++kk) acc = fmaf(As[(32 + i) * 64 + kk], Ts[kk * 64 + j], acc);
-    As[i * 64 + 32 + j] = acc;
+  // Z = A_LL T_UL -> As[0:32][32:64]; T_UL's upper block T_01 is zero (skipped)
+  if (tid < 256) {
+    const int i = tid >> 3, j0 = (tid & 7) * 4;
+    const float* a = As + (32 + i) * kSA;
+    const bool upper_cols = j0 >= 16;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int kk = 0; kk < 32; ++kk) {
+      const float av = (kk < 16 && upper_cols) ? 0.f : a[kk];
+      float4 t = *reinterpret_cast<const float4*>(Ts + kk * kSA + j0);
+      if (kk < 16 && upper_cols) t = make_float4(0.f, 0.f, 0.f, 0.f);
+      acc.x = fmaf(av, t.x, acc.x);
+      acc.y = fmaf(av, t.y, acc.y);
+      acc.z = fmaf(av, t.z, acc.z);
+      acc.w = fmaf(av, t.w, acc.w);
+    }
+    *reinterpret_cast<float4*>(As + i * kSA + 32 + j0) = acc;
   }
   __syncthreads();
-  for (int e = tid; e < 1024; e += 256) {
-    const int i = e >> 5, j = e & 31;
-    float acc = 0.f;
-    const int k1 = (i < 16) ? 16 : 32;
-    for (int kk = 0; kk < k1; ++kk) acc = fmaf(Ts[(32 + i) * 64 + 32 + kk], As[kk * 64 + 32 + j], acc);
-    Ts[(32 + i) * 64 + j] = -acc;
+  // T_LL = -T_LR Z; rows i < 16 of T_LR end at column 16 (its upper block is undefined)
+  if (tid < 256) {
+    const int i = tid >> 3, j0 = (tid & 7) * 4;
+    const float* t = Ts + (32 + i) * kSA + 32;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (i < 16) {
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk) {
+        const float tv = t[kk];
+        const float4 z = *reinterpret_cast<const float4*>(As + kk * kSA + 32 + j0);
+        acc.x = fmaf(tv, z.x, acc.x);
+        acc.y = fmaf(tv, z.y, acc.y);
+        acc.z = fmaf(tv, z.z, acc.z);
+        acc.w = fmaf(tv, z.w, acc.w);
+      }
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < 32; ++kk) {
+        const float tv = t[kk];
+        const float4 z = *reinterpret_cast<const float4*>(As + kk * kSA + 32 + j0);
+        acc.x = fmaf(tv, z.x, acc.x);
+        acc.y = fmaf(tv, z.y, acc.y);
+        acc.z = fmaf(tv, z.z, acc.z);
+        acc.w = fmaf(tv, z.w, acc.w);
+      }
+    }
+    *reinterpret_cast<float4*>(Ts + (32 + i) * kSA + j0) =
+        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
   }
   __syncthreads();
 }

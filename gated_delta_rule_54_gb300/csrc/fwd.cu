@@ -33,7 +33,8 @@ namespace gdn {
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
+constexpr int kWarps = kThreads / 32;
 
 struct FwdParams {
   const __nv_bfloat16* q;
@@ -60,7 +61,7 @@ template <int DK, int SM, int WM>
 struct Smem {
   static constexpr int kTileK = kChunk * DK * 2;      // bf16 [64][DK]
   static constexpr int kTile64 = kChunk * 64 * 2;     // bf16 [64][64]
-  static constexpr int kF32 = kChunk * 64 * 4;        // f32  [64][64]
+  static constexpr int kF32 = kF32Tile;                // f32  [64][kSA]
   static constexpr int K = 0;                          // 2 buffers
   static constexpr int Q = K + 2 * kTileK;             // 2 buffers
   static constexpr int V = Q + 2 * kTileK;
@@ -125,7 +126,7 @@ template <int DK, int SM, int WM>
 __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_kernel(const FwdParams p) {
   using S = Smem<DK, SM, WM>;
   extern __shared__ __align__(1024) unsigned char sm[];
-  __shared__ float red[2][8];
+  __shared__ float red[2][kWarps];
 
   const int vb = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
   const int hk = h / p.G;
@@ -170,12 +171,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_kernel(const FwdParams p)
   __nv_bfloat16* DL = TuL;
   uint8_t* Hstage = reinterpret_cast<uint8_t*>(sm + S::TW);  // [DK][64] codes
   uint8_t* Wstage = reinterpret_cast<uint8_t*>(sm + S::TT);  // [64][DK] codes
-  float* Ostage = As;                                         // [64][72] f32 (spans A and T)
-  constexpr int OSTR = 72;
+  float* Ostage = As;                                         // [64][kSA] f32
+  constexpr int OSTR = kSA;
 
-  // State tile layout (output of the [DK x 64] state-update GEMM).
+  // warp tiles: [64 x 64] outputs -> 16 x 16 per warp; [64 x DK] -> 16 x DK/4
+  const int rt = warp & 3, cq = warp >> 2;
+  const int row0 = rt * 16, col0 = cq * 16;
+  constexpr int NTW = DK / 32;
+  const int wcol0 = cq * (DK / 4);
+  // state tile [DK x 64]
   constexpr int HM = DK / 16;            // row tiles
-  constexpr int HN = 8 / HM;             // warps per row tile
+  constexpr int HN = kWarps / HM;        // warps per row tile
   constexpr int NTH = 8 / HN;            // 8-wide n tiles per warp
   const int h_row0 = (warp % HM) * 16;
   const int h_col0 = (warp / HM) * (64 / HN);
@@ -253,50 +259,41 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_kernel(const FwdParams p)
     __syncthreads();
 
     // ---- a2 (+ QK^T for a8): A = strict-lower(beta_i Gamma_ij KK^T), P = lower-incl(Gamma QK^T) ----
-    {
-      const int rt = warp & 3, ch = warp >> 2;
-      const int row0 = rt * 16, col0 = ch * 32;
-      if (col0 <= row0 + 15) {
-        float akk[4][4], aqk[4][4];
+    if (cq <= rt) {
+      float akk[2][4], aqk[2][4];
+      zero_acc(akk);
+      zero_acc(aqk);
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) akk[i][e] = aqk[i][e] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < DK / 16; ++ks) {
-          uint32_t ak[4], aq[4];
-          ldsm_x4(ak, a_frag_addr<DK>(Ks, row0, ks * 16, lane));
-          ldsm_x4(aq, a_frag_addr<DK>(Qs, row0, ks * 16, lane));
-#pragma unroll
-          for (int np = 0; np < 2; ++np) {
-            uint32_t b[4];
-            ldsm_x4(b, bnk_frag_addr<DK>(Ks, col0 + np * 16, ks * 16, lane));
-            mma_bf16(akk[2 * np], ak, b[0], b[1]);
-            mma_bf16(akk[2 * np + 1], ak, b[2], b[3]);
-            mma_bf16(aqk[2 * np], aq, b[0], b[1]);
-            mma_bf16(aqk[2 * np + 1], aq, b[2], b[3]);
-          }
-        }
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-          for (int e2 = 0; e2 < 2; ++e2) {
-            const int i = row0 + gq + 8 * e2;
-            const int j = col0 + nt * 8 + 2 * tq;
-            const float gi = gam[i];
-            const float x0 = (j <= i) ? expf(gi - gam[j]) : 0.f;
-            const float x1 = (j + 1 <= i) ? expf(gi - gam[j + 1]) : 0.f;
-            const float bi = bet[i];
-            As[i * 64 + j] = (j < i) ? bi * x0 * akk[nt][2 * e2] : 0.f;
-            As[i * 64 + j + 1] = (j + 1 < i) ? bi * x1 * akk[nt][2 * e2 + 1] : 0.f;
-            const float p0 = x0 * aqk[nt][2 * e2], p1 = x1 * aqk[nt][2 * e2 + 1];
-            float h0v, l0v, h1v, l1v;
-            split_bf16(p0, h0v, l0v);
-            split_bf16(p1, h1v, l1v);
-            st_bf16x2(PH + swz<64>(i, j), h0v, h1v);
-            st_bf16x2(PL + swz<64>(i, j), l0v, l1v);
-          }
+      for (int ks = 0; ks < DK / 16; ++ks) {
+        uint32_t ak[4], aq[4], b[4];
+        ldsm_x4(ak, a_frag_addr<DK>(Ks, row0, ks * 16, lane));
+        ldsm_x4(aq, a_frag_addr<DK>(Qs, row0, ks * 16, lane));
+        ldsm_x4(b, bnk_frag_addr<DK>(Ks, col0, ks * 16, lane));
+        mma_bf16(akk[0], ak, b[0], b[1]);
+        mma_bf16(akk[1], ak, b[2], b[3]);
+        mma_bf16(aqk[0], aq, b[0], b[1]);
+        mma_bf16(aqk[1], aq, b[2], b[3]);
       }
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int i = row0 + gq + 8 * e2;
+          const int j = col0 + nt * 8 + 2 * tq;
+          const float gi = gam[i];
+          const float x0 = (j <= i) ? expf(gi - gam[j]) : 0.f;
+          const float x1 = (j + 1 <= i) ? expf(gi - gam[j + 1]) : 0.f;
+          const float bi = bet[i];
+          *reinterpret_cast<float2*>(As + i * kSA + j) =
+              make_float2((j < i) ? bi * x0 * akk[nt][2 * e2] : 0.f,
+                          (j + 1 < i) ? bi * x1 * akk[nt][2 * e2 + 1] : 0.f);
+          const float p0 = x0 * aqk[nt][2 * e2], p1 = x1 * aqk[nt][2 * e2 + 1];
+          float h0v, l0v, h1v, l1v;
+          split_bf16(p0, h0v, l0v);
+          split_bf16(p1, h1v, l1v);
+          st_bf16x2(PH + swz<64>(i, j), h0v, h1v);
+          st_bf16x2(PL + swz<64>(i, j), l0v, l1v);
+        }
     }
 
     // ---- a6: state QDQ (every thread holds a piece of the state tile) ----
@@ -304,7 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_kernel(const FwdParams p)
     {
       float amax = red[0][0];
 #pragma unroll
-      for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[0][i]);
+      for (int i = 1; i < kWarps; ++i) amax = fmaxf(amax, red[0][i]);
       if constexpr (SM != GDN_QDQ_NONE) {
         float rcp;
         qdq_scale<SM>(amax, sH, rcp);
@@ -367,71 +364,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_kernel(const FwdParams p)
       }
     }
 
-    // ---- a3: T = (I + A)^-1, blocked forward substitution in fp32 ----
-    // diagonal 16x16 blocks: thread (b, c) owns column c of block b
-    if (threadIdx.x < 64) {
-      const int b = threadIdx.x >> 4, cc = threadIdx.x & 15;
-      const float* Ab = As + (16 * b) * 64 + 16 * b;
-      float x[16];
-#pragma unroll
-      for (int r = 0; r < 16; ++r) {
-        float acc = 0.f;
-#pragma unroll
-        for (int j = 0; j < r; ++j) acc = fmaf(Ab[r * 64 + j], x[j], acc);
-        x[r] = (r == cc) ? 1.f : (r < cc ? 0.f : -acc);
-      }
-#pragma unroll
-      for (int r = 0; r < 16; ++r) Ts[(16 * b + r) * 64 + 16 * b + cc] = x[r];
-    }
-    __syncthreads();
-    // level 1: X = A_10 T_00 (into As[0:16][16:32]), Y = A_32 T_22 (into As[32:48][48:64])
-    for (int e = threadIdx.x; e < 512; e += kThreads) {
-      const int pr = e >> 8, i = (e >> 4) & 15, j = e & 15;
-      const int base = 32 * pr;
-      float acc = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 16; ++kk)
-        acc = fmaf(As[(base + 16 + i) * 64 + base + kk], Ts[(base + kk) * 64 + base + j], acc);
-      As[(base + i) * 64 + base + 16 + j] = acc;
-    }
-    __syncthreads();
-    // T_10 = -T_11 X, T_32 = -T_33 Y
-    for (int e = threadIdx.x; e < 512; e += kThreads) {
-      const int pr = e >> 8, i = (e >> 4) & 15, j = e & 15;
-      const int base = 32 * pr;
-      float acc = 0.f;
-#pragma unroll
-      for (int kk = 0; kk < 16; ++kk)
-        acc = fmaf(Ts[(base + 16 + i) * 64 + base + 16 + kk], As[(base + kk) * 64 + base + 16 + j],
-                   acc);
-      Ts[(base + 16 + i) * 64 + base + j] = -acc;
-    }
-    __syncthreads();
-    // level 2: Z = A_LL T_UL (into As[0:32][32:64]); T_UL is lower-triangular
-    for (int e = threadIdx.x; e < 1024; e += kThreads) {
-      const int i = e >> 5, j = e & 31;
-      float acc = 0.f;
-      const int k0 = (j >= 16) ? 16 : 0;
-      for (int kk = k0; kk < 32; ++kk) acc = fmaf(As[(32 + i) * 64 + kk], Ts[kk * 64 + j], acc);
-      As[i * 64 + 32 + j] = acc;
-    }
-    __syncthreads();
-    // T_LL = -T_LR Z; T_LR is lower-triangular
-    for (int e = threadIdx.x; e < 1024; e += kThreads) {
-      const int i = e >> 5, j = e & 31;
-      float acc = 0.f;
-      const int k1 = (i < 16) ? 16 : 32;
-      for (int kk = 0; kk < k1; ++kk)
-        acc = fmaf(Ts[(32 + i) * 64 + 32 + kk], As[kk * 64 + 32 + j], acc);
-      Ts[(32 + i) * 64 + j] = -acc;
-    }
-    __syncthreads();
+    // ---- a3: T = (I + A)^-1 ----
+    solve_unit_lower64<kThreads>(As, Ts);
 
     // ---- a4 operands: Tw = T diag(beta e^gamma), Tu = T diag(beta), split hi/lo ----
     for (int e = threadIdx.x; e < 64 * 32; e += kThreads) {
       const int i = e >> 5, j = (e & 31) * 2;
-      const float t0 = (j <= i) ? Ts[i * 64 + j] : 0.f;
-      const float t1 = (j + 1 <= i) ? Ts[i * 64 + j + 1] : 0.f;
+      const float2 tt = *reinterpret_cast<const float2*>(Ts + i * kSA + j);
+      const float t0 = (j <= i) ? tt.x : 0.f;
+      const float t1 = (j + 1 <= i) ? tt.y : 0.f;
       float a0, a1, b0, b1;
       split_bf16(t0 * beg[j], a0, b0);
       split_bf16(t1 * beg[j + 1], a1, b1);
@@ -444,48 +385,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_kernel(const FwdParams p)
     }
     __syncthreads();
 
-    // ---- a4: W = Tw K  [64 x DK] and U = Tu V  [64 x 64] ----
-    const int rt = warp & 3, ch = warp >> 2;
-    const int row0 = rt * 16;
-    constexpr int NTW = DK / 16;
-    const int wcol0 = ch * (DK / 2);
+    // ---- a4: W = Tw K  [64 x DK] and U = Tu V  [64 x 64] (hi and lo passes) ----
     float wacc[NTW][4];
-#pragma unroll
-    for (int i = 0; i < NTW; ++i)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) wacc[i][e] = 0.f;
-    float uacc[4][4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) uacc[i][e] = 0.f;
-    const int col0 = ch * 32;
-#pragma unroll
-    for (int ks = 0; ks < 4; ++ks) {
-      uint32_t ah[4], al[4];
-      ldsm_x4(ah, a_frag_addr<64>(TwH, row0, ks * 16, lane));
-      ldsm_x4(al, a_frag_addr<64>(TwL, row0, ks * 16, lane));
-#pragma unroll
-      for (int np = 0; np < NTW / 2; ++np) {
-        uint32_t b[4];
-        ldsm_x4_t(b, bkn_frag_addr<DK>(Ks, ks * 16, wcol0 + np * 16, lane));
-        mma_bf16(wacc[2 * np], ah, b[0], b[1]);
-        mma_bf16(wacc[2 * np], al, b[0], b[1]);
-        mma_bf16(wacc[2 * np + 1], ah, b[2], b[3]);
-        mma_bf16(wacc[2 * np + 1], al, b[2], b[3]);
-      }
-      ldsm_x4(ah, a_frag_addr<64>(TuH, row0, ks * 16, lane));
-      ldsm_x4(al, a_frag_addr<64>(TuL, row0, ks * 16, lane));
-#pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        uint32_t b[4];
-        ldsm_x4_t(b, bkn_frag_addr<64>(Vs, ks * 16, col0 + np * 16, lane));
-        mma_bf16(uacc[2 * np], ah, b[0], b[1]);
-        mma_bf16(uacc[2 * np], al, b[0], b[1]);
-        mma_bf16(uacc[2 * np + 1], ah, b[2], b[3]);
-        mma_bf16(uacc[2 * np + 1], al, b[2], b[3]);
-      }
-    }
+    zero_acc(wacc);
+    float uacc[2][4];
+    zero_acc(uacc);
+    wgemm<NTW, false, true, 64, DK>(wacc, TwH, row0, Ks, wcol0, 0, 64, lane);
+    wgemm<2, false, true, 64, 64>(uacc, TuH, row0, Vs, col0, 0, 64, lane);
+    wgemm<NTW, false, true, 64, DK>(wacc, TwL, row0, Ks, wcol0, 0, 64, lane);
+    wgemm<2, false, true, 64, 64>(uacc, TuL, row0, Vs, col0, 0, 64, lane);
     {
       float m = 0.f;
 #pragma unroll
@@ -506,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_kernel(const FwdParams p)
     {
       float amax = red[1][0];
 #pragma unroll
-      for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red[1][i]);
+      for (int i = 1; i < kWarps; ++i) amax = fmaxf(amax, red[1][i]);
       if constexpr (WM != GDN_QDQ_NONE) {
         float rcp;
         qdq_scale<WM>(amax, sW, rcp);
@@ -560,99 +468,48 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_kernel(const FwdParams p)
     }
 
     // ---- a7: Delta = U - W^ H^ ----
-    float dacc[4][4];
+    {
+      float dacc[2][4];
+      zero_acc(dacc);
+      wgemm<2, false, true, DK, 64>(dacc, WcH, row0, HcH, col0, 0, DK, lane);
+      if constexpr (WM == GDN_QDQ_NONE) wgemm<2, false, true, DK, 64>(dacc, WcL, row0, HcH, col0, 0, DK, lane);
+      if constexpr (SM == GDN_QDQ_NONE) wgemm<2, false, true, DK, 64>(dacc, WcH, row0, HcL, col0, 0, DK, lane);
+      const float sWH = (WM != GDN_QDQ_NONE ? sW : 1.f) * (SM != GDN_QDQ_NONE ? sH : 1.f);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) dacc[i][e] = 0.f;
-#pragma unroll
-    for (int ks = 0; ks < DK / 16; ++ks) {
-      uint32_t ah[4], al[4];
-      ldsm_x4(ah, a_frag_addr<DK>(WcH, row0, ks * 16, lane));
-      if constexpr (WM == GDN_QDQ_NONE) ldsm_x4(al, a_frag_addr<DK>(WcL, row0, ks * 16, lane));
-#pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        uint32_t bh[4], bl[4];
-        ldsm_x4_t(bh, bkn_frag_addr<64>(HcH, ks * 16, col0 + np * 16, lane));
-        if constexpr (SM == GDN_QDQ_NONE) ldsm_x4_t(bl, bkn_frag_addr<64>(HcL, ks * 16, col0 + np * 16, lane));
-        mma_bf16(dacc[2 * np], ah, bh[0], bh[1]);
-        mma_bf16(dacc[2 * np + 1], ah, bh[2], bh[3]);
-        if constexpr (WM == GDN_QDQ_NONE) {
-          mma_bf16(dacc[2 * np], al, bh[0], bh[1]);
-          mma_bf16(dacc[2 * np + 1], al, bh[2], bh[3]);
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
+          const float d0 = uacc[nt][2 * e2] - sWH * dacc[nt][2 * e2];
+          const float d1 = uacc[nt][2 * e2 + 1] - sWH * dacc[nt][2 * e2 + 1];
+          float h0v, l0v, h1v, l1v;
+          split_bf16(d0, h0v, l0v);
+          split_bf16(d1, h1v, l1v);
+          st_bf16x2(DH + swz<64>(i, j), h0v, h1v);
+          st_bf16x2(DL + swz<64>(i, j), l0v, l1v);
+          const float di = dec[i];
+          split_bf16(d0 * di, h0v, l0v);
+          split_bf16(d1 * di, h1v, l1v);
+          st_bf16x2(DpH + swz<64>(i, j), h0v, h1v);
+          st_bf16x2(DpL + swz<64>(i, j), l0v, l1v);
         }
-        if constexpr (SM == GDN_QDQ_NONE) {
-          mma_bf16(dacc[2 * np], ah, bl[0], bl[1]);
-          mma_bf16(dacc[2 * np + 1], ah, bl[2], bl[3]);
-        }
-      }
     }
-    const float sWH = (WM != GDN_QDQ_NONE ? sW : 1.f) * (SM != GDN_QDQ_NONE ? sH : 1.f);
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e2 = 0; e2 < 2; ++e2) {
-        const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-        const float d0 = uacc[nt][2 * e2] - sWH * dacc[nt][2 * e2];
-        const float d1 = uacc[nt][2 * e2 + 1] - sWH * dacc[nt][2 * e2 + 1];
-        float h0v, l0v, h1v, l1v;
-        split_bf16(d0, h0v, l0v);
-        split_bf16(d1, h1v, l1v);
-        st_bf16x2(DH + swz<64>(i, j), h0v, h1v);
-        st_bf16x2(DL + swz<64>(i, j), l0v, l1v);
-        const float di = dec[i];
-        split_bf16(d0 * di, h0v, l0v);
-        split_bf16(d1 * di, h1v, l1v);
-        st_bf16x2(DpH + swz<64>(i, j), h0v, h1v);
-        st_bf16x2(DpL + swz<64>(i, j), l0v, l1v);
-      }
     __syncthreads();  // Delta operands complete
 
     // ---- a8: O = scale (diag(e^gamma) Q H^ + P Delta) ----
     {
-      float o1[4][4], o2[4][4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) o1[i][e] = o2[i][e] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < DK / 16; ++ks) {
-        uint32_t aq[4];
-        ldsm_x4(aq, a_frag_addr<DK>(Qs, row0, ks * 16, lane));
-#pragma unroll
-        for (int np = 0; np < 2; ++np) {
-          uint32_t bh[4];
-          ldsm_x4_t(bh, bkn_frag_addr<64>(HcH, ks * 16, col0 + np * 16, lane));
-          mma_bf16(o1[2 * np], aq, bh[0], bh[1]);
-          mma_bf16(o1[2 * np + 1], aq, bh[2], bh[3]);
-          if constexpr (SM == GDN_QDQ_NONE) {
-            uint32_t bl[4];
-            ldsm_x4_t(bl, bkn_frag_addr<64>(HcL, ks * 16, col0 + np * 16, lane));
-            mma_bf16(o1[2 * np], aq, bl[0], bl[1]);
-            mma_bf16(o1[2 * np + 1], aq, bl[2], bl[3]);
-          }
-        }
-      }
-      for (int ks = 0; ks <= rt; ++ks) {
-        uint32_t ph[4], pl[4];
-        ldsm_x4(ph, a_frag_addr<64>(PH, row0, ks * 16, lane));
-        ldsm_x4(pl, a_frag_addr<64>(PL, row0, ks * 16, lane));
-#pragma unroll
-        for (int np = 0; np < 2; ++np) {
-          uint32_t bh[4], bl[4];
-          ldsm_x4_t(bh, bkn_frag_addr<64>(DH, ks * 16, col0 + np * 16, lane));
-          ldsm_x4_t(bl, bkn_frag_addr<64>(DL, ks * 16, col0 + np * 16, lane));
-          mma_bf16(o2[2 * np], ph, bh[0], bh[1]);
-          mma_bf16(o2[2 * np], ph, bl[0], bl[1]);
-          mma_bf16(o2[2 * np], pl, bh[0], bh[1]);
-          mma_bf16(o2[2 * np + 1], ph, bh[2], bh[3]);
-          mma_bf16(o2[2 * np + 1], ph, bl[2], bl[3]);
-          mma_bf16(o2[2 * np + 1], pl, bh[2], bh[3]);
-        }
-      }
+      float o1[2][4], o2[2][4];
+      zero_acc(o1);
+      zero_acc(o2);
+      wgemm<2, false, true, DK, 64>(o1, Qs, row0, HcH, col0, 0, DK, lane);
+      if constexpr (SM == GDN_QDQ_NONE) wgemm<2, false, true, DK, 64>(o1, Qs, row0, HcL, col0, 0, DK, lane);
+      const int kend = row0 + 16;   // P is lower triangular: columns j <= i only
+      wgemm<2, false, true, 64, 64>(o2, PH, row0, DH, col0, 0, kend, lane);
+      wgemm<2, false, true, 64, 64>(o2, PH, row0, DL, col0, 0, kend, lane);
+      wgemm<2, false, true, 64, 64>(o2, PL, row0, DH, col0, 0, kend, lane);
       const float sq = (SM != GDN_QDQ_NONE) ? sH : 1.f;
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -671,21 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_kernel(const FwdParams p)
       for (int nt = 0; nt < NTH; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) hreg[nt][e] *= egL;
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        uint32_t a[4];
-        ldsm_x4_t(a, at_frag_addr<DK>(Ks, h_row0, ks * 16, lane));
-#pragma unroll
-        for (int np = 0; np < NTH / 2; ++np) {
-          uint32_t bh[4], bl[4];
-          ldsm_x4_t(bh, bkn_frag_addr<64>(DpH, ks * 16, h_col0 + np * 16, lane));
-          ldsm_x4_t(bl, bkn_frag_addr<64>(DpL, ks * 16, h_col0 + np * 16, lane));
-          mma_bf16(hreg[2 * np], a, bh[0], bh[1]);
-          mma_bf16(hreg[2 * np], a, bl[0], bl[1]);
-          mma_bf16(hreg[2 * np + 1], a, bh[2], bh[3]);
-          mma_bf16(hreg[2 * np + 1], a, bl[2], bl[3]);
-        }
-      }
+      wgemm<NTH, true, true, DK, 64>(hreg, Ks, h_row0, DpH, h_col0, 0, 64, lane);
+      wgemm<NTH, true, true, DK, 64>(hreg, Ks, h_row0, DpL, h_col0, 0, 64, lane);
     }
     __syncthreads();  // O staged; all reads of K/Q(buf), Delta, P done
 
