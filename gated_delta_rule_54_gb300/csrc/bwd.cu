@@ -520,7 +520,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
   __nv_bfloat16* dKKb = dHp;
   float* As = reinterpret_cast<float*>(sm + S::AS);
   float* Ts = reinterpret_cast<float*>(sm + S::TS);
-  uint8_t* stage = reinterpret_cast<uint8_t*>(sm + S::AS);  // code staging, before A / T exist
   __nv_bfloat16* GKKb = reinterpret_cast<__nv_bfloat16*>(sm + S::GKK);
   __nv_bfloat16* Pb = reinterpret_cast<__nv_bfloat16*>(sm + S::PB);
   __nv_bfloat16* Tb = reinterpret_cast<__nv_bfloat16*>(sm + S::TB);
@@ -528,6 +527,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
   __nv_bfloat16* Gmb = Tub;                // after U
   __nv_bfloat16* Db = reinterpret_cast<__nv_bfloat16*>(sm + S::DB);
   __nv_bfloat16* dDb = reinterpret_cast<__nv_bfloat16*>(sm + S::DDB);
+  uint8_t* wst = reinterpret_cast<uint8_t*>(sm + S::DB);   // W codes [64][DK], until Delta
+  uint8_t* hst = reinterpret_cast<uint8_t*>(sm + S::DDB);  // H codes [DK][64], until dDelta
   float* gam = reinterpret_cast<float*>(sm + S::VEC);
   float* eg = gam + 64;
   float* dec = gam + 128;
@@ -538,13 +539,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
   float* racc = reinterpret_cast<float*>(sm + S::RACC);
   float* hd_part = racc + S::kSlots * 64;  // [kWarps] <H^, dH'> partials, then [2] sums of t_i
 
-  // ---- loads ----
+  // ---- loads: group 1 (needed first) and group 2 (needed after the solve) ----
   load_rows_bf16<DK>(Ks, p.k + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
   load_rows_bf16<DK>(Qs, p.q + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
   load_rows_bf16<64>(Vs, p.v + (ctok * p.Hv + h) * p.Dv + vb * 64, (int64_t)p.Hv * p.Dv, Lc);
   load_rows_bf16<64>(dOs, p.dO + (ctok * p.Hv + h) * p.Dv + vb * 64, (int64_t)p.Hv * p.Dv, Lc);
   load_col_f32(gs, p.g + ctok * p.Hv + h, p.Hv, Lc);
   load_col_f32(bsg, p.beta + ctok * p.Hv + h, p.Hv, Lc);
+  cp_async_commit();
   {  // dH' [DK][64] bf16 from the workspace (always a full tile)
     const __nv_bfloat16* src = p.ws_dh + ((slot * p.Hv + h) * DK) * p.Dv + vb * 64;
     for (int i = threadIdx.x; i < DK * 8; i += kThreads) {
@@ -557,12 +559,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
     for (int i = threadIdx.x; i < kChunk * CPR; i += kThreads) {
       const int r = i / CPR, cc = i % CPR;
       const bool ok = r < Lc;
-      cp_async16(smem_u32(stage + r * DK + cc * 16),
+      cp_async16(smem_u32(wst + r * DK + cc * 16),
                  p.w_codes + ((ctok + (ok ? r : 0)) * p.Hv + h) * DK + cc * 16, ok ? 16 : 0);
     }
   }
   if constexpr (SM != GDN_QDQ_NONE) {
-    uint8_t* hst = stage + kChunk * DK;
     const uint8_t* src = p.h_codes + ((slot * p.Hv + h) * DK) * p.Dv + vb * 64;
     for (int i = threadIdx.x; i < DK * 4; i += kThreads) {
       const int d = i >> 2, c16 = i & 3;
@@ -570,47 +571,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
     }
   }
   cp_async_commit();
-  cp_async_wait<0>();
+  cp_async_wait<1>();
   __syncthreads();
 
-  // ---- dequantized operands, chunk vectors ----
+  // ---- chunk vectors ----
   if (warp == 0) chunk_vectors(gs, bsg, gam, eg, dec, beg, lane);
   if (threadIdx.x < 64) bet[threadIdx.x] = bsg[threadIdx.x];
-  if constexpr (WM != GDN_QDQ_NONE) {
-    const float sW = p.w_scales[slot * p.Hv + h];
-    for (int e = threadIdx.x; e < kChunk * DK / 2; e += kThreads) {
-      const int r = (2 * e) / DK, col = (2 * e) % DK;
-      st_bf16x2(Wv + swz<DK>(r, col), code_val<WM>(stage[r * DK + col]) * sW,
-                code_val<WM>(stage[r * DK + col + 1]) * sW);
-    }
-  }
-  {
-    float hd = 0.f;
-    if constexpr (SM != GDN_QDQ_NONE) {
-      const float sH = p.h_scales[(slot * p.Hv + h) * (p.Dv / 64) + vb];
-      const uint8_t* hst = stage + kChunk * DK;
-      for (int e = threadIdx.x; e < DK * 32; e += kThreads) {
-        const int d = e >> 5, col = (e & 31) * 2;
-        const float x0 = code_val<SM>(hst[d * 64 + col]) * sH;
-        const float x1 = code_val<SM>(hst[d * 64 + col + 1]) * sH;
-        st_bf16x2(Hh + swz<64>(d, col), x0, x1);
-        const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162*>(dHp + swz<64>(d, col));
-        hd += x0 * __bfloat162float(y.x) + x1 * __bfloat162float(y.y);
-      }
-    } else {
-      const float* src = p.h_full + ((slot * p.Hv + h) * DK) * p.Dv + vb * 64;
-      for (int e = threadIdx.x; e < DK * 32; e += kThreads) {
-        const int d = e >> 5, col = (e & 31) * 2;
-        const float2 x = *reinterpret_cast<const float2*>(src + (int64_t)d * p.Dv + col);
-        st_bf16x2(Hh + swz<64>(d, col), x.x, x.y);
-        const __nv_bfloat162 y = *reinterpret_cast<const __nv_bfloat162*>(dHp + swz<64>(d, col));
-        hd += x.x * __bfloat162float(y.x) + x.y * __bfloat162float(y.y);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
-    if (lane == 0) hd_part[warp] = hd;
-  }
   __syncthreads();
 
   // ---- KK^T -> A (f32) and Gamma KK (bf16); QK^T -> P (bf16) ----
@@ -652,6 +618,48 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
 
   // ---- a3: T = (I + A)^-1 ----
   solve_unit_lower64<kThreads>(As, Ts);
+  cp_async_wait<0>();
+  __syncthreads();  // group 2 (dH', W codes, H codes) visible to all threads
+
+  // ---- dequantized operands (4 codes per step), <H^, dH'>, and T / Tu in bf16 ----
+  if constexpr (WM != GDN_QDQ_NONE) {
+    const float sW = p.w_scales[slot * p.Hv + h];
+    for (int e = threadIdx.x; e < kChunk * DK / 4; e += kThreads) {
+      const int r = (4 * e) / DK, col = (4 * e) % DK;
+      const float4 v = qdq_code4_values<WM>(*reinterpret_cast<const uint32_t*>(wst + r * DK + col));
+      uint2 pk;
+      pk.x = pack_bf16(v.x * sW, v.y * sW);
+      pk.y = pack_bf16(v.z * sW, v.w * sW);
+      *reinterpret_cast<uint2*>(Wv + swz<DK>(r, col)) = pk;
+    }
+  }
+  {
+    float hd = 0.f;
+    for (int e = threadIdx.x; e < DK * 16; e += kThreads) {
+      const int d = e >> 4, col = (e & 15) * 4;
+      float4 x;
+      if constexpr (SM != GDN_QDQ_NONE) {
+        const float sH = p.h_scales[(slot * p.Hv + h) * (p.Dv / 64) + vb];
+        x = qdq_code4_values<SM>(*reinterpret_cast<const uint32_t*>(hst + d * 64 + col));
+        x.x *= sH; x.y *= sH; x.z *= sH; x.w *= sH;
+      } else {
+        x = *reinterpret_cast<const float4*>(p.h_full + ((slot * p.Hv + h) * DK + d) * p.Dv +
+                                              vb * 64 + col);
+      }
+      uint2 pk;
+      pk.x = pack_bf16(x.x, x.y);
+      pk.y = pack_bf16(x.z, x.w);
+      *reinterpret_cast<uint2*>(Hh + swz<64>(d, col)) = pk;
+      const uint2 yb = *reinterpret_cast<const uint2*>(dHp + swz<64>(d, col));
+      const __nv_bfloat162 y0 = *reinterpret_cast<const __nv_bfloat162*>(&yb.x);
+      const __nv_bfloat162 y1 = *reinterpret_cast<const __nv_bfloat162*>(&yb.y);
+      hd += x.x * __bfloat162float(y0.x) + x.y * __bfloat162float(y0.y) +
+            x.z * __bfloat162float(y1.x) + x.w * __bfloat162float(y1.y);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
+    if (lane == 0) hd_part[warp] = hd;
+  }
   for (int e = threadIdx.x; e < 64 * 32; e += kThreads) {
     const int i = e >> 5, j = (e & 31) * 2;
     const float t0 = (j <= i) ? Ts[i * kSA + j] : 0.f;
@@ -994,21 +1002,31 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
   }
 
   // ---- dq, dk: two value-block contributions per element onto zero ----
+  // Lane pairs (tq, tq ^ 1) swap halves so each lane owns four consecutive
+  // columns of one row and adds them with one 16-byte atomic.
   float* dq_out = p.ws_dqk ? p.ws_dqk : p.dq;
   float* dk_out = p.ws_dqk ? p.ws_dqk + p.BT * p.Hv * DK : p.dk;
   const int hh = p.ws_dqk ? h : hk;
   const int HH = p.ws_dqk ? p.Hv : p.Hk;
+  const bool odd = tq & 1;
+  const int i_own = wrow0 + gq + (odd ? 8 : 0);
 #pragma unroll
-  for (int nt = 0; nt < NTW; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int i = wrow0 + gq + 8 * (e >> 1), d = wcol0 + nt * 8 + 2 * tq + (e & 1);
-      if (i < Lc) {
-        const int64_t off = ((ctok + i) * HH + hh) * DK + d;
-        atomicAdd(dq_out + off, dQ[nt][e]);
-        atomicAdd(dk_out + off, dK[nt][e]);
-      }
+  for (int nt = 0; nt < NTW; ++nt) {
+    const int c4 = wcol0 + nt * 8 + 2 * (tq & ~1);
+    const float sq0 = __shfl_xor_sync(0xffffffffu, odd ? dQ[nt][0] : dQ[nt][2], 1);
+    const float sq1 = __shfl_xor_sync(0xffffffffu, odd ? dQ[nt][1] : dQ[nt][3], 1);
+    const float sk0 = __shfl_xor_sync(0xffffffffu, odd ? dK[nt][0] : dK[nt][2], 1);
+    const float sk1 = __shfl_xor_sync(0xffffffffu, odd ? dK[nt][1] : dK[nt][3], 1);
+    const float4 vq = odd ? make_float4(sq0, sq1, dQ[nt][2], dQ[nt][3])
+                          : make_float4(dQ[nt][0], dQ[nt][1], sq0, sq1);
+    const float4 vk = odd ? make_float4(sk0, sk1, dK[nt][2], dK[nt][3])
+                          : make_float4(dK[nt][0], dK[nt][1], sk0, sk1);
+    if (i_own < Lc) {
+      const int64_t off = ((ctok + i_own) * HH + hh) * DK + c4;
+      atomicAdd(reinterpret_cast<float4*>(dq_out + off), vq);
+      atomicAdd(reinterpret_cast<float4*>(dk_out + off), vk);
     }
+  }
 }
 
 // dq[t][hk][d] = sum_{g < G} ws[t][hk*G + g][d] (fixed order), same for dk.

@@ -68,6 +68,20 @@ __device__ __forceinline__ float qdq_code_value(uint8_t c) {
   }
 }
 
+// Values of four code bytes packed little-endian in c4 (exact in fp32).
+template <int MODE>
+__device__ __forceinline__ float4 qdq_code4_values(uint32_t c4) {
+  if constexpr (MODE == GDN_QDQ_E4M3) {
+    const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(c4 & 0xffffu), __NV_E4M3);
+    const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(c4 >> 16), __NV_E4M3);
+    const float2 a = __half22float2(__half2(lo)), b = __half22float2(__half2(hi));
+    return make_float4(a.x, a.y, b.x, b.y);
+  } else {
+    return make_float4((float)(int8_t)(c4 & 0xffu), (float)(int8_t)((c4 >> 8) & 0xffu),
+                       (float)(int8_t)((c4 >> 16) & 0xffu), (float)(int8_t)(c4 >> 24));
+  }
+}
+
 // For amax == 0 a group passes through unchanged; its codes are signed zeros
 // for E4M3 and zeros for INT8.
 template <int MODE>
