@@ -5,7 +5,8 @@ One step = one pass of the hot path over one batch of the single-layer
 workload (B=4, T=4096, H=16, Dk=Dv=128, E4M3 state and W QDQ, h0 ~ N(0, 0.1^2)):
 the forward (saving the QDQ context) followed by the identity-STE backward
 (``--mode fwdbwd``, the default once the backward is present), or the
-forward alone (``--mode fwd``).  Inputs are synthetic (seeded) and resident
+forward alone (``--mode fwd``).  ``--mode decode`` times the decode QAT step
+instead (256 sequences, one token each, carried fp32 states of 256 MiB).  Inputs are synthetic (seeded) and resident
 in HBM when the timed region starts; per step the inputs (~350 MB) exceed
 the 129 MB L2, so no flush is needed between steps.
 
@@ -427,6 +428,145 @@ def cpu_baseline(w, cpu, bwd, budget_s=20.0):
 
 
 # ----------------------------------------------------------------------------
+# decode QAT step (--mode decode)
+# ----------------------------------------------------------------------------
+DECODE_METRIC = "GDN decode QAT tokens/s at B=256,H=16,D=128 (one token per sequence); % of roofline"
+DECODE_SOURCES = ["gated_delta_rule_54_gb300/csrc/decode.cu", "gated_delta_rule_54_gb300/csrc/common.cuh"]
+
+
+def decode_alg_bytes(w):
+    """Algorithmic HBM bytes of one decode launch: the carried state read and
+    written once, the token's q, k, v, beta, g read and o written."""
+    tok = w.B * w.T
+    b = w.B * w.Hv * w.Dk * w.Dv * 4 * 2
+    b += tok * (w.Hk * w.Dk * 2 * 2 + w.Hv * w.Dv * 2 + w.Hv * 4 * 2 + w.Hv * w.Dv * 4)
+    return b
+
+
+def run_decode(args, ws, rank, local):
+    from gated_delta_rule_54_gb300 import api, synth
+    from gated_delta_rule_54_gb300._lib import load
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    load()
+    w = synth.WORKLOADS[args.workload]
+    w = synth.Workload(**{**w.__dict__, "seed": w.seed + rank})
+    cpu = synth.make_inputs(w)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in cpu.items()}
+    q, k, v, beta, g = d["q"], d["k"], d["v"], d["beta"], d["g"]
+    # two state buffers used in turn: each step reads the state the last one wrote
+    states = [d["h0"], torch.empty_like(d["h0"])]
+    o = torch.empty(w.B, w.T, w.Hv, w.Dv, device=dev)
+    sm = w.state_mode
+    stream = torch.cuda.current_stream(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    it = [0]
+
+    def step():
+        i = it[0]
+        api.gdn_decode_qdq(q, k, v, beta, g, states[i % 2], state_mode=sm, state_out=states[1 - i % 2],
+                           out=o)
+        it[0] += 1
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    _barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk:
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(args.steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+    _barrier(ws)
+    ms_total = _max_over_ranks(a.elapsed_time(b), ws, dev)
+    ms_step = ms_total / args.steps
+    tokens = w.B * w.T
+    value = tokens * ws * args.steps / (ms_total / 1e3)
+    peak, peak_kind = _peaks()
+    alg = decode_alg_bytes(w)
+    achieved = alg / (ms_step / 1e3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "traffic": _traffic("gdn_decode_kernel_decode_step.md", DECODE_SOURCES, args.workload),
+            "kernel": "gdn_decode_kernel", "peak_source": peak_kind,
+            "alg_bytes_per_launch": alg, "launch_ms": round(ms_step, 4)}
+
+    # end to end: the token's inputs from pinned host memory, o back; the
+    # carried states stay resident on the device (a decode cache)
+    e2e = None
+    if not args.no_e2e:
+        names = ("q", "k", "v", "beta", "g")
+        host = {n: cpu[n].pin_memory() for n in names}
+        o_h = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+        d2h = o_h.numel() * o_h.element_size()
+
+        def e2e_step():
+            for n in names:
+                d[n].copy_(host[n], non_blocking=True)
+            step()
+            o_h.copy_(o, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        _barrier(ws)
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e_ms = _max_over_ranks(a.elapsed_time(b), ws, dev)
+        e2e = {"value": round(tokens * ws * args.steps / (e_ms / 1e3), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e_ms / args.steps, 4),
+               "note": "carried states resident on the device"}
+
+    cpu_base = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu_base = decode_cpu_baseline(w, cpu, budget_s=args.cpu_budget)
+    line = {
+        "metric": DECODE_METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), beta=sigmoid, "
+                "g=-softplus, states N(0, 0.1^2))",
+        "config": {"workload": w.name, "mode": "decode", "B": w.B, "T": w.T, "Hk": w.Hk,
+                   "Hv": w.Hv, "Dk": w.Dk, "Dv": w.Dv, "state_mode": sm, "block_v": 64,
+                   "readout": "pre",
+                   "l2": "states (2 x 256 MiB, read and written in turn) larger than L2"},
+        "clocks": clk.summary(), "e2e": e2e, "gpu_launches": args.steps, "roofline": roof,
+        "cpu_baseline": cpu_base,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def decode_cpu_baseline(w, cpu, budget_s=20.0, rows=None):
+    """The fp64 decode oracle, as it stands, on whole rows (all heads) until
+    the budget is used; tokens/s scaled from the sample."""
+    from oracle.decode import decode
+    t0 = time.time()
+    done = 0
+    for n in range(w.B if rows is None else rows):
+        sl = slice(n, n + 1)
+        decode(*[cpu[x][sl] for x in ("q", "k", "v", "beta", "g", "h0")], state_mode=w.state_mode)
+        done += 1
+        if time.time() - t0 > budget_s * 0.5:
+            break
+    dt = time.time() - t0
+    return {"value": round(done * w.T / dt, 2), "unit": "tokens/s", "cores": torch.get_num_threads(),
+            "kind": "oracle",
+            "sample": "%d of %d rows (one token, all %d heads), fp64 decode oracle" % (
+                done, w.B, w.Hv)}
+
+
+# ----------------------------------------------------------------------------
 # reference arm: the oracle on the host cores
 # ----------------------------------------------------------------------------
 def run_reference(args, ws, rank):
@@ -435,6 +575,28 @@ def run_reference(args, ws, rank):
     from gated_delta_rule_54_gb300 import synth
     from oracle.chunked import chunked
     w = synth.WORKLOADS[args.workload]
+    if args.mode == "decode":
+        cpu = synth.make_inputs(synth.Workload(**{**w.__dict__, "B": 16}))
+        for _ in range(args.warmup):
+            decode_cpu_baseline(w, cpu, budget_s=1e9, rows=1)
+        t0 = time.time()
+        for _ in range(args.steps):
+            decode_cpu_baseline(w, cpu, budget_s=1e9, rows=16)
+        dt = time.time() - t0
+        value = 16 * w.T * args.steps / dt
+        sample = "16 rows x one token, all %d heads per step (fp64 decode oracle)" % w.Hv
+        print(json.dumps({
+            "impl": "reference", "metric": DECODE_METRIC, "value": round(value, 2),
+            "unit": "tokens/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "mode": "decode", "B": w.B, "T": w.T, "Hk": w.Hk,
+                       "Hv": w.Hv, "Dk": w.Dk, "Dv": w.Dv, "state_mode": w.state_mode},
+            "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s",
+                             "cores": torch.get_num_threads(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}), flush=True)
+        return
     bwd = args.mode == "fwdbwd"
     T_s = 1024   # bounded sample per step: one sequence, all heads, 1024 tokens
     ws_ = synth.Workload(**{**w.__dict__, "B": 1, "T": T_s})
@@ -478,8 +640,8 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="layer")
-    ap.add_argument("--mode", default=None, choices=["fwd", "fwdbwd"])
+    ap.add_argument("--workload", default=None)
+    ap.add_argument("--mode", default=None, choices=["fwd", "fwdbwd", "decode"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
@@ -487,10 +649,14 @@ def main():
     args.warmup = max(args.warmup, 3)
     if args.mode is None:
         args.mode = "fwdbwd" if _backward_available() else "fwd"
+    if args.workload is None:
+        args.workload = "decode" if args.mode == "decode" else "layer"
     args.bwd_launches = BWD_LAUNCHES
     ws, rank, local = _dist()
     if args.impl == "reference":
         run_reference(args, ws, rank)
+    elif args.mode == "decode":
+        run_decode(args, ws, rank, local)
     else:
         run_ours(args, ws, rank, local)
     if ws > 1:

@@ -38,6 +38,20 @@ class GdnProblem(ctypes.Structure):
 
 
 _PP = ctypes.POINTER(GdnProblem)
+
+READOUTS = {"pre": 0, "post": 1}
+
+
+class GdnDecodeProblem(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int64), ("T", ctypes.c_int64),
+        ("Hk", ctypes.c_int32), ("Hv", ctypes.c_int32), ("Dk", ctypes.c_int32), ("Dv", ctypes.c_int32),
+        ("scale", ctypes.c_float), ("state_mode", ctypes.c_int32), ("block_v", ctypes.c_int32),
+        ("readout", ctypes.c_int32), ("dtype", ctypes.c_int32),
+    ]
+
+
+_DP = ctypes.POINTER(GdnDecodeProblem)
 SIGNATURES = {
     "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_abi_version": (ctypes.c_int, []),
@@ -52,6 +66,8 @@ SIGNATURES = {
                                                  _P, _P, _P, _P]),
     "fake_qdq_e4m3": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
     "fake_qdq_int8": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
+    "gdn_decode_validate": (ctypes.c_int, [_DP]),
+    "gdn_decode_qdq": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 
 _lock = threading.Lock()

@@ -11,7 +11,7 @@ from typing import Optional
 
 import torch
 
-from ._lib import DTYPES, QDQ_MODES, GdnError, GdnProblem, check, load
+from ._lib import DTYPES, QDQ_MODES, READOUTS, GdnDecodeProblem, GdnError, GdnProblem, check, load
 
 _DT = {torch.bfloat16: DTYPES["bf16"], torch.float16: DTYPES["fp16"], torch.float32: DTYPES["fp32"]}
 
@@ -135,6 +135,57 @@ def gdn_chunk_bwd_ste(q, k, v, beta, g, ctx, do, dht=None, cu_seqlens=None, scal
                                ctypes.c_size_t(workspace.numel()), _stream(dev))
     check("gdn_chunk_bwd_ste", st)
     return dq, dk, dv, dbeta, dg, dh0
+
+
+def make_decode_problem(q, k, v, scale=1.0, state_mode="e4m3", block_v=64,
+                        readout="pre") -> GdnDecodeProblem:
+    B, T, Hk, Dk = k.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    p = GdnDecodeProblem()
+    p.B, p.T, p.Hk, p.Hv, p.Dk, p.Dv = B, T, Hk, Hv, Dk, Dv
+    p.scale = float(scale)
+    p.state_mode = _mode(state_mode)
+    p.block_v = block_v
+    if readout not in READOUTS:
+        raise ValueError("readout must be one of %s, got %r" % (sorted(READOUTS), readout))
+    p.readout = READOUTS[readout]
+    p.dtype = _DT.get(q.dtype, 99)
+    return p
+
+
+def gdn_decode_qdq(q, k, v, beta, g, state_in=None, scale=1.0, state_mode="e4m3", block_v=64,
+                   readout="pre", record=False, state_out=None, out=None):
+    """Decode QAT step over T tokens per row.  q, k [B,T,Hk,Dk] bf16; v [B,T,Hv,Dv] bf16;
+    beta, g [B,T,Hv] f32; state_in [B,Hv,Dk,Dv] f32 or None (zeros).
+
+    Returns (o [B,T,Hv,Dv] f32, state_out [B,Hv,Dk,Dv] f32) and, with ``record``,
+    (codes u8 [B,T,Hv,Dk,Dv], scales f32 [B,T,Hv,Dv/block_v]) of the quantized
+    state each token read.  ``state_out`` may be ``state_in`` (in-place update);
+    ``out`` may pass a preallocated o.
+    """
+    lib = load()
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g),
+                    ("state_in", state_in), ("state_out", state_out)):
+        _check_dev(name, t, dev)
+    p = make_decode_problem(q, k, v, scale, state_mode, block_v, readout)
+    check("gdn_decode_validate", lib.gdn_decode_validate(ctypes.byref(p)))
+    B, T, Hv, Dv = v.shape
+    Dk = k.shape[3]
+    o = torch.empty(B, T, Hv, Dv, device=dev, dtype=torch.float32) if out is None else out
+    if state_out is None:
+        state_out = torch.empty(B, Hv, Dk, Dv, device=dev, dtype=torch.float32)
+    codes = scales = None
+    if record and p.state_mode != 0:
+        codes = torch.empty(B, T, Hv, Dk, Dv, device=dev, dtype=torch.uint8)
+        scales = torch.empty(B, T, Hv, Dv // block_v, device=dev, dtype=torch.float32)
+    st = lib.gdn_decode_qdq(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
+                            _ptr(state_in), _ptr(o), _ptr(state_out), _ptr(codes), _ptr(scales),
+                            _stream(dev))
+    check("gdn_decode_qdq", st)
+    if record:
+        return o, state_out, codes, scales
+    return o, state_out
 
 
 def _fake_qdq(fn_name, x, group_cols, with_codes=False, out=None):

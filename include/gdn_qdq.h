@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define GDN_QDQ_ABI_VERSION 1
+#define GDN_QDQ_ABI_VERSION 2
 
 typedef enum {
   GDN_QDQ_NONE = 0, /* site not quantized                                   */
@@ -201,6 +201,55 @@ gdn_status fake_qdq_e4m3(const float* x, float* y, float* scales, uint8_t* codes
                          int64_t rows, int64_t cols, int64_t group_cols, void* stream);
 gdn_status fake_qdq_int8(const float* x, float* y, float* scales, uint8_t* codes, int64_t batch,
                          int64_t rows, int64_t cols, int64_t group_cols, void* stream);
+
+/*
+ * Decode QAT step ("[2/4] GDN/KDA decode QAT with INT8 recurrent state",
+ * section "What does this PR do?": after an exact chunked prefill of an
+ * explicit prefix, every later token writes the recurrent state through the
+ * state quantizer; E4M3 or signed symmetric INT8 with per-head [Dk, block_v]
+ * scales; section "Testing": both readouts, split carry, all state scale
+ * widths).  The page prints no formula; the step is the chunked forward's
+ * chunk-boundary rule with one-token chunks.  Per row b, value head h and
+ * token t, with H = S^T (Dk x Dv) and S the carried state:
+ *     S^ = Q(S)                 (fake QDQ per [Dk, block_v] tile, exactly as
+ *                                fake_qdq_*; skipped when state_mode is NONE)
+ *     H  = exp(g) S^ + beta k (v - exp(g) S^^T k)^T
+ *     o  = scale H^T q          (readout PRE, as inside a forward chunk)
+ *        = scale Q(H)^T q       (readout POST: the state the next token reads)
+ *     S <- H                    (carried unquantized)
+ * so one call over T tokens equals T one-token calls chained through the
+ * state, and the split carry from a prefill is state_in = the forward's ht.
+ *   q, k   bf16 [B, T, Hk, Dk]        v bf16 [B, T, Hv, Dv]
+ *   beta   f32  [B, T, Hv]            g f32  [B, T, Hv] (log decay)
+ *   state_in  f32 [B, Hv, Dk, Dv] carried state, or NULL for zeros
+ *   o         f32 [B, T, Hv, Dv] (written)
+ *   state_out f32 [B, Hv, Dk, Dv] (written; may BE state_in for an in-place
+ *             update, any other overlap is GDN_ERR_INVALID_ARG)
+ *   codes     u8  [B, T, Hv, Dk, Dv] codes of S^ read by each token, or NULL
+ *   scales    f32 [B, T, Hv, Dv / block_v] scales of S^, or NULL
+ * B <= 65535 rows; all pointers 16-byte aligned (GDN_ERR_MISALIGNED).
+ * T == 0 copies state_in to state_out.  Host-validated like the forward.
+ */
+typedef enum { GDN_READOUT_PRE = 0, GDN_READOUT_POST = 1 } gdn_readout;
+
+typedef struct {
+  int64_t B;                  /* rows: one sequence and one state each          */
+  int64_t T;                  /* tokens per row in this call (>= 0)             */
+  int32_t Hk, Hv, Dk, Dv;     /* Dk, Dv in {64, 128}; Hv % Hk == 0              */
+  float scale;                /* output scale                                   */
+  int32_t state_mode;         /* gdn_qdq_mode of the state                      */
+  int32_t block_v;            /* state-scale tile width: 16, 32, 64 or 128, <= Dv */
+  int32_t readout;            /* gdn_readout                                    */
+  int32_t dtype;              /* gdn_dtype of q, k, v; must be BF16             */
+} gdn_decode_problem;
+
+/* Host-only validation of a decode problem (no CUDA call). */
+gdn_status gdn_decode_validate(const gdn_decode_problem* p);
+
+gdn_status gdn_decode_qdq(const gdn_decode_problem* p, const void* q, const void* k,
+                          const void* v, const float* beta, const float* g,
+                          const float* state_in, float* o, float* state_out, uint8_t* codes,
+                          float* scales, void* stream);
 
 #ifdef __cplusplus
 }

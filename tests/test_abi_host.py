@@ -136,4 +136,42 @@ def test_status_strings():
     for code in range(-7, 1):
         s = lib.gdn_status_string(code).decode()
         assert s.startswith("GDN_")
-    assert lib.gdn_abi_version() == 1
+    assert lib.gdn_abi_version() == 2
+
+
+def _dproblem(**kw):
+    p = _lib.GdnDecodeProblem()
+    p.B, p.T, p.Hk, p.Hv, p.Dk, p.Dv = 8, 1, 2, 4, 128, 128
+    p.scale, p.state_mode, p.block_v, p.readout, p.dtype = 1.0, 1, 64, 0, 0
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(), 0), (dict(block_v=16), 0), (dict(block_v=32, Dv=64), 0), (dict(block_v=128), 0),
+    (dict(state_mode=2, readout=1), 0), (dict(state_mode=0, T=0), 0), (dict(Dk=64, Dv=64), 0),
+    (dict(dtype=2), -2), (dict(dtype=9), -1), (dict(Dk=96), -3), (dict(Hv=3), -3),
+    (dict(block_v=128, Dv=64), -4), (dict(block_v=48), -4), (dict(block_v=8), -4),
+    (dict(readout=2), -1), (dict(state_mode=3), -1), (dict(B=-1), -1), (dict(T=-1), -1),
+    (dict(B=65536), -3), (dict(scale=float("nan")), -1),
+])
+def test_decode_validate(kw, code):
+    assert _lib.load().gdn_decode_validate(ctypes.byref(_dproblem(**kw))) == code
+
+
+def test_decode_entry_rejects_before_launch():
+    lib = _lib.load()
+    P = ctypes.c_void_p
+    f = P(4096)
+    ok = _dproblem()
+    call = lambda p, *a: lib.gdn_decode_qdq(ctypes.byref(p), *a)
+    assert call(_dproblem(dtype=2), f, f, f, f, f, f, f, f, None, None, None) == -2
+    assert call(ok, None, f, f, f, f, f, f, f, None, None, None) == -1          # null q
+    assert call(ok, f, f, f, f, f, f, f, None, None, None, None) == -1          # null state_out
+    assert call(ok, P(4100), f, f, f, f, f, f, f, None, None, None) == -7       # misaligned
+    # state_out overlapping state_in without being it
+    n = 8 * 4 * 128 * 128 * 4
+    assert call(ok, f, f, f, f, f, P(1 << 20), f, P((1 << 20) + n // 2), None, None, None) == -1
+    assert call(_dproblem(B=0), None, None, None, None, None, None, None, None, None, None,
+                None) == 0
