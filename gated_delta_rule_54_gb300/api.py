@@ -78,7 +78,9 @@ def gdn_chunk_fwd_qdq(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, sta
     h0 [N,Hv,Dk,Dv] f32 or None; cu_seqlens [N+1] int32 or None (B == 1).
 
     Returns (o [B,T,Hv,Dv] f32, ht [N,Hv,Dk,Dv] f32 or None, ctx uint8 or None).
-    ``out`` may pass preallocated (o, ht, ctx) buffers.
+    The forward always writes its context (quantized W and chunk states); it
+    is returned when ``save_ctx`` (for the backward).  ``out`` may pass
+    preallocated (o, ht, ctx) buffers; ctx is required there.
     """
     lib = load()
     dev = q.device
@@ -94,12 +96,11 @@ def gdn_chunk_fwd_qdq(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, sta
         o = torch.empty(B, T, Hv, Dv, device=dev, dtype=torch.float32)
         ht = (torch.empty(p.N, Hv, k.shape[3], Dv, device=dev, dtype=torch.float32)
               if output_final_state else None)
-        ctx = (torch.empty(int(lib.gdn_ctx_bytes(ctypes.byref(p))), device=dev, dtype=torch.uint8)
-               if save_ctx else None)
+        ctx = torch.empty(int(lib.gdn_ctx_bytes(ctypes.byref(p))), device=dev, dtype=torch.uint8)
     st = lib.gdn_chunk_fwd_qdq(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(g),
                                _ptr(h0), _ptr(o), _ptr(ht), _ptr(ctx), _stream(dev))
     check("gdn_chunk_fwd_qdq", st)
-    return o, ht, ctx
+    return o, ht, (ctx if save_ctx or out is not None else None)
 
 
 def gdn_chunk_bwd_ste(q, k, v, beta, g, ctx, do, dht=None, cu_seqlens=None, scale=1.0,
@@ -231,6 +232,10 @@ def split_ctx(ctx: torch.Tensor, p: GdnProblem):
         off = al(off + n)
         out["w_scales"] = ctx[off:off + 4 * ns * Hv].view(torch.float32).view(ns, Hv)
         off = al(off + 4 * ns * Hv)
+    else:
+        n = B * T * Hv * Dk
+        out["w_full"] = ctx[off:off + 4 * n].view(torch.float32).view(B, T, Hv, Dk)
+        off = al(off + 4 * n)
     if p.state_mode != 0:
         n = ns * Hv * Dk * Dv
         out["h_codes"] = ctx[off:off + n].view(ns, Hv, Dk, Dv)

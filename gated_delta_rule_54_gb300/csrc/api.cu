@@ -36,6 +36,9 @@ CtxLayout ctx_layout(const gdn_problem& p) {
     off = align256(off + tokens * d.Hv * d.Dk);
     L.w_scales = off;
     off = align256(off + sizeof(float) * (size_t)d.n_slots * d.Hv);
+  } else {
+    L.w_full = off;
+    off = align256(off + sizeof(float) * tokens * d.Hv * d.Dk);
   }
   const size_t per_slot = (size_t)d.n_slots * d.Hv * d.Dk * d.Dv;
   if (p.state_mode != GDN_QDQ_NONE) {
@@ -127,6 +130,7 @@ gdn_status gdn_chunk_fwd_qdq(const gdn_problem* p, const void* q, const void* k,
                           (const void*)o, (const void*)ht, (const void*)ctx,
                           (const void*)p->cu_seqlens})
     if (ptr && !aligned16(ptr)) return GDN_ERR_MISALIGNED;
+  if (d.B * d.T > 0 && !ctx) return GDN_ERR_INVALID_ARG;
   if (ctx && ((uintptr_t)ctx & 255)) return GDN_ERR_MISALIGNED;
   if (d.N == 0 || (d.B * d.T == 0 && !ht)) return GDN_OK;
   return launch_fwd(*p, d, q, k, v, beta, g, h0, o, ht, ctx, (cudaStream_t)stream);

@@ -1,4 +1,4 @@
-// Fused forward of the chunked gated delta rule with state / W fake QDQ.
+// Forward of the chunked gated delta rule with state / W fake QDQ.
 //
 // Method: GatedDeltaNet chunked training form with QDQ at the recurrent-state
 // and WY "W" sites ("[1/4] GDN state/W QAT foundation", "What does this PR
@@ -12,29 +12,32 @@
 //   O = scale (diag(e^gamma) Q H^ + (lower-incl(e^{gamma_i-gamma_j} q_i.k_j)) Delta);
 //   H <- e^{gamma_L} H^ + (diag(e^{gamma_L - gamma}) K)^T Delta.
 //
-// GB300 design: one CTA (8 warps) per (sequence, value head, 64-wide value
-// block) walks its chunks in order; the fp32 state tile [Dk x 64] never
-// leaves registers.  Everything chunk-local (KK^T, the solve, W, U, QK^T) is
-// recomputed per CTA, so HBM traffic is the algorithmic minimum: q, k, v,
-// beta, g in, o (+ final state, + optional saved context) out.  Contractions
-// run on tensor cores in bf16 with fp32 accumulation.  Operands that are not
-// exactly bf16 (T, Delta, the decayed Delta, P, and unquantized W / H) are
-// split into hi + lo bf16 halves so the state path keeps ~16 mantissa bits:
-// a plain bf16 rounding of these flips far more quantization codes than the
-// fp32 arithmetic of the definition would.  Quantized W and H are fed to the
-// tensor cores as their codes (E4M3 values and INT8 integers are exact in
-// bf16), with the fp32 scales applied in the epilogues.
-// K and Q chunks are double-buffered with cp.async; V is prefetched once U
-// has consumed it.
+// GB300 design: only H^ -> Delta -> H is a serial dependence between chunks,
+// so the forward is three launches.
+//   1. gdn_fwd_prep_kernel, one CTA per (chunk, value head), all chunks in
+//      parallel: KK^T, the exact solve, W (quantized: codes and scale go to the
+//      saved context) and U (fp32, parked in the output buffer o).
+//   2. gdn_fwd_state_kernel, one CTA per (sequence, value head, 64-wide value
+//      block) walks its chunks in order with the fp32 state tile in registers;
+//      per chunk only the state QDQ (codes to the context), Delta and the state
+//      update remain on the serial path, with the next chunk's operands
+//      prefetched by cp.async.
+//   3. gdn_fwd_output_kernel, one CTA per (chunk, value head, value block), all
+//      in parallel: QK^T, Delta = U - W^ H^ again from the saved codes, and O,
+//      written over U.
+// Contractions run on tensor cores (mma.sync bf16, fp32 accumulation).
+// Operands that are not exactly bf16 (T diag(.), Delta, the decayed Delta, P,
+// and unquantized W / H) are split into hi + lo bf16 halves so the state path
+// keeps ~16 mantissa bits: a plain bf16 rounding of these flips far more
+// quantization codes than the fp32 arithmetic of the definition would.
+// Quantized W and H enter the tensor cores as their codes (E4M3 values and
+// INT8 integers are exact in bf16) with the fp32 scales applied in epilogues.
 #include "common.cuh"
 #include "launch.h"
 
 namespace gdn {
 
 namespace {
-
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
 
 struct FwdParams {
   const __nv_bfloat16* q;
@@ -43,90 +46,369 @@ struct FwdParams {
   const float* beta;
   const float* g;
   const float* h0;
-  float* o;
+  float* o;  // also holds U between the prep and the output launches
   float* ht;
   uint8_t* w_codes;
   float* w_scales;
+  float* w_full;
   uint8_t* h_codes;
   float* h_scales;
   float* h_full;
   const int32_t* cu_seqlens;
   int64_t T;
-  int Hk, Hv, Dv, G;
+  int Hk, Hv, Dv, G, N;
   int64_t nt_fixed;
   float scale;
 };
 
-template <int DK, int SM, int WM>
-struct Smem {
-  static constexpr int kTileK = kChunk * DK * 2;      // bf16 [64][DK]
-  static constexpr int kTile64 = kChunk * 64 * 2;     // bf16 [64][64]
-  static constexpr int kF32 = kF32Tile;                // f32  [64][kSA]
-  static constexpr int K = 0;                          // 2 buffers
-  static constexpr int Q = K + 2 * kTileK;             // 2 buffers
-  static constexpr int V = Q + 2 * kTileK;
-  static constexpr int BG = V + kTile64;               // 2 x (beta[64], g[64])
-  static constexpr int VEC = BG + 2 * 2 * 64 * 4;      // gamma, e^g, beta e^g, beta, decay
-  static constexpr int A = VEC + 5 * 64 * 4 + 256;
-  static constexpr int TT = A + kF32;
-  static constexpr int TW = TT + kF32;                 // Tw hi/lo -> (H code staging) -> Delta' hi/lo
-  static constexpr int TU = TW + 2 * kTile64;          // Tu hi/lo -> Delta hi/lo
-  static constexpr int P = TU + 2 * kTile64;           // P hi/lo
-  static constexpr int WC = P + 2 * kTile64;           // W^ codes (or W hi [, lo])
-  static constexpr int WC_N = (WM == GDN_QDQ_NONE) ? 2 : 1;
-  static constexpr int HC = WC + WC_N * kTileK;        // H^ codes (or H hi [, lo]) [DK][64]
-  static constexpr int HC_N = (SM == GDN_QDQ_NONE) ? 2 : 1;
-  static constexpr int BYTES = HC + HC_N * DK * 64 * 2;
-  static_assert(BYTES <= 232448, "shared memory budget");
-  static_assert((A % 128) == 0 && (TW % 128) == 0 && (WC % 128) == 0 && (HC % 128) == 0,
-                "tile alignment");
+// The chunk stored at a chunk slot (see gdn_qdq.h); false for an unused
+// packed slot.  Uniform across a CTA.
+struct ChunkRef {
+  int64_t tok;  // first token
+  int L;        // valid rows (1..64)
 };
 
-// Issue the async loads of chunk rows [t0, t0 + 64) of one sequence
-// (rows >= L zero-filled) into the K / Q buffers and the beta/g staging.
-template <int DK>
-__device__ __forceinline__ void load_kq(const FwdParams& p, unsigned char* sm, int kOff,
-                                        int qOff, int bgOff, int64_t tok0, int L, int hk, int h) {
-  __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(sm + kOff);
-  __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(sm + qOff);
-  constexpr int CPR = DK / 8;  // 16-byte chunks per row
-  for (int i = threadIdx.x; i < kChunk * CPR; i += kThreads) {
+__device__ __forceinline__ bool chunk_of_slot(const FwdParams& p, int64_t slot, ChunkRef& r) {
+  if (!p.cu_seqlens) {
+    const int64_t n = slot / p.nt_fixed, c = slot % p.nt_fixed;
+    r.tok = n * p.T + c * kChunk;
+    r.L = (int)min((int64_t)kChunk, p.T - c * kChunk);
+    return r.L > 0;
+  }
+  // largest n with floor(cu[n] / 64) + n <= slot (strictly increasing in n)
+  int lo = 0, hi = p.N - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if ((int64_t)p.cu_seqlens[mid] / kChunk + mid <= slot)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  const int64_t a = p.cu_seqlens[lo], b = p.cu_seqlens[lo + 1];
+  const int64_t c = slot - (a / kChunk + lo);
+  if (c < 0 || c * kChunk >= b - a) return false;
+  r.tok = a + c * kChunk;
+  r.L = (int)min((int64_t)kChunk, b - a - c * kChunk);
+  return true;
+}
+
+// [64][DK] bf16 rows of q or k of one chunk (rows >= L zero-filled), swizzled.
+template <int DK, int NTHREADS>
+__device__ __forceinline__ void load_rows_bf16(__nv_bfloat16* dst, const __nv_bfloat16* src,
+                                               int64_t tok0, int L, int H, int hh) {
+  constexpr int CPR = DK / 8;
+  for (int i = threadIdx.x; i < kChunk * CPR; i += NTHREADS) {
     const int r = i / CPR, c = i % CPR;
     const bool ok = r < L;
     const int64_t tok = tok0 + (ok ? r : 0);
-    const __nv_bfloat16* ks = p.k + (tok * p.Hk + hk) * DK + c * 8;
-    const __nv_bfloat16* qs = p.q + (tok * p.Hk + hk) * DK + c * 8;
-    cp_async16(smem_u32(Ks + swz<DK>(r, c * 8)), ks, ok ? 16 : 0);
-    cp_async16(smem_u32(Qs + swz<DK>(r, c * 8)), qs, ok ? 16 : 0);
-  }
-  if (threadIdx.x < 2 * kChunk) {
-    const int r = threadIdx.x & 63;
-    const bool ok = r < L;
-    const int64_t tok = tok0 + (ok ? r : 0);
-    const float* src = (threadIdx.x < kChunk ? p.beta : p.g) + tok * p.Hv + h;
-    const uint32_t dst = smem_u32(sm + bgOff + threadIdx.x * 4);
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src),
-                 "r"(ok ? 4 : 0));
+    cp_async16(smem_u32(dst + swz<DK>(r, c * 8)), src + (tok * H + hh) * DK + c * 8, ok ? 16 : 0);
   }
 }
 
-__device__ __forceinline__ void load_v(const FwdParams& p, unsigned char* sm, int vOff,
-                                       int64_t tok0, int L, int h, int vb) {
-  __nv_bfloat16* Vs = reinterpret_cast<__nv_bfloat16*>(sm + vOff);
-  for (int i = threadIdx.x; i < kChunk * 8; i += kThreads) {
-    const int r = i >> 3, c = i & 7;
+// 64 floats of beta or g of one chunk (rows >= L zero-filled).
+__device__ __forceinline__ void load_vec64(float* dst, const float* src, int64_t tok0, int L,
+                                           int Hv, int h, int t) {
+  const bool ok = t < L;
+  const int64_t tok = tok0 + (ok ? t : 0);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_u32(dst + t)),
+               "l"(src + tok * Hv + h), "r"(ok ? 4 : 0));
+}
+
+// gamma = in-chunk cumsum of g (padded rows have g = 0, so gamma stays at the
+// last valid value there).  Warp-wide; lane l owns rows 2l, 2l+1.
+__device__ __forceinline__ void chunk_cumsum(const float* g, int lane, float& gam0, float& gam1,
+                                             float& gL) {
+  const float g0 = g[2 * lane], g1 = g[2 * lane + 1];
+  float s = g0 + g1;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, s, o);
+    if (lane >= o) s += y;
+  }
+  gam1 = s;
+  gam0 = s - g1;
+  gL = __shfl_sync(0xffffffffu, s, 31);
+}
+
+// ===========================================================================
+// 1. Chunk-local prep: A, T, W (+ QDQ), U.
+// ===========================================================================
+constexpr int kPrepThreads = 256;
+constexpr int kPrepWarps = kPrepThreads / 32;
+
+template <int DK>
+struct PrepSmem {
+  static constexpr int K = 0;                            // bf16 [64][DK]
+  static constexpr int V = K + kChunk * DK * 2;          // bf16 Dv/64 x [64][64]
+  static constexpr int BG = V + 2 * kChunk * 64 * 2;     // beta[64], g[64]
+  static constexpr int VEC = BG + 512;                   // gamma, e^gamma, beta e^gamma, beta
+  static constexpr int A = VEC + 4 * 64 * 4;             // f32 [64][kSA]; later U staging
+  static constexpr int TT = A + kF32Tile;                // f32 [64][kSA]
+  static constexpr int TW = TT + kF32Tile;               // Tw hi, lo
+  static constexpr int TU = TW + 2 * kChunk * 64 * 2;    // Tu hi, lo
+  static constexpr int WST = TU + 2 * kChunk * 64 * 2;   // u8 [64][DK] W codes
+  static constexpr int BYTES = WST + kChunk * DK;
+  static_assert((A % 128) == 0 && (TW % 128) == 0 && (WST % 16) == 0, "alignment");
+};
+
+template <int DK, int WM>
+__global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const FwdParams p) {
+  using S = PrepSmem<DK>;
+  extern __shared__ __align__(1024) unsigned char sm[];
+  __shared__ float red[kPrepWarps];
+
+  const int64_t slot = blockIdx.x / p.Hv;
+  const int h = blockIdx.x % p.Hv;
+  ChunkRef cr;
+  if (!chunk_of_slot(p, slot, cr)) return;
+  const int hk = h / p.G;
+  const int L = cr.L;
+  const int64_t tok0 = cr.tok;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int nvb = p.Dv / 64;
+
+  __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(sm + S::K);
+  __nv_bfloat16* Vs = reinterpret_cast<__nv_bfloat16*>(sm + S::V);
+  float* bsrc = reinterpret_cast<float*>(sm + S::BG);
+  float* gam = reinterpret_cast<float*>(sm + S::VEC);
+  float* eg = gam + 64;
+  float* beg = gam + 128;
+  float* bet = gam + 192;
+  float* As = reinterpret_cast<float*>(sm + S::A);
+  float* Ts = reinterpret_cast<float*>(sm + S::TT);
+  __nv_bfloat16* TwH = reinterpret_cast<__nv_bfloat16*>(sm + S::TW);
+  __nv_bfloat16* TwL = TwH + kChunk * 64;
+  __nv_bfloat16* TuH = reinterpret_cast<__nv_bfloat16*>(sm + S::TU);
+  __nv_bfloat16* TuL = TuH + kChunk * 64;
+  uint8_t* Wst = sm + S::WST;
+  float* Ust = As;
+
+  load_rows_bf16<DK, kPrepThreads>(Ks, p.k, tok0, L, p.Hk, hk);
+  for (int i = threadIdx.x; i < kChunk * nvb * 8; i += kPrepThreads) {
+    const int r = i / (nvb * 8), rem = i % (nvb * 8), vb = rem >> 3, c = rem & 7;
     const bool ok = r < L;
     const int64_t tok = tok0 + (ok ? r : 0);
-    const __nv_bfloat16* src = p.v + (tok * p.Hv + h) * p.Dv + vb * 64 + c * 8;
-    cp_async16(smem_u32(Vs + swz<64>(r, c * 8)), src, ok ? 16 : 0);
+    cp_async16(smem_u32(Vs + vb * kChunk * 64 + swz<64>(r, c * 8)),
+               p.v + (tok * p.Hv + h) * p.Dv + vb * 64 + c * 8, ok ? 16 : 0);
   }
+  if (threadIdx.x < 2 * kChunk) {
+    const int t = threadIdx.x & 63;
+    load_vec64(bsrc + (threadIdx.x < kChunk ? 0 : 64), threadIdx.x < kChunk ? p.beta : p.g,
+               tok0, L, p.Hv, h, t);
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+
+  if (warp == 0) {
+    float gam0, gam1, gL;
+    chunk_cumsum(bsrc + 64, lane, gam0, gam1, gL);
+    const float b0 = bsrc[2 * lane], b1 = bsrc[2 * lane + 1];
+    const float e0 = expf(gam0), e1 = expf(gam1);
+    gam[2 * lane] = gam0;
+    gam[2 * lane + 1] = gam1;
+    eg[2 * lane] = e0;
+    eg[2 * lane + 1] = e1;
+    beg[2 * lane] = b0 * e0;
+    beg[2 * lane + 1] = b1 * e1;
+    bet[2 * lane] = b0;
+    bet[2 * lane + 1] = b1;
+  }
+
+  // warp tile: rows 16 rt .. +15, columns 32 ch .. +31 of a [64 x 64] product
+  const int rt = warp & 3, ch = warp >> 2;
+  const int row0 = rt * 16, col0 = ch * 32;
+
+  // ---- a2: A = strict-lower(beta_i Gamma_ij k_i.k_j) (blocks above the diagonal skipped);
+  //      KK^T needs no gamma, so it runs before the barrier that publishes gamma ----
+  const bool a_tile = col0 <= row0 + 15;
+  float acc[4][4];
+  zero_acc(acc);
+  if (a_tile) wgemm<4, false, false, DK, DK>(acc, Ks, row0, Ks, col0, 0, DK, lane);
+  __syncthreads();
+  if (a_tile) {
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
+        const float gi = gam[i], bi = bet[i];
+        const float a0 = (j < i) ? bi * expf(gi - gam[j]) * acc[nt][2 * e2] : 0.f;
+        const float a1 = (j + 1 < i) ? bi * expf(gi - gam[j + 1]) * acc[nt][2 * e2 + 1] : 0.f;
+        *reinterpret_cast<float2*>(As + i * kSA + j) = make_float2(a0, a1);
+      }
+  }
+  __syncthreads();
+
+  // ---- a3: T = (I + A)^-1 ----
+  solve_unit_lower64<kPrepThreads>(As, Ts);
+
+  // ---- a4 operands: Tw = T diag(beta e^gamma), Tu = T diag(beta), split hi/lo ----
+  for (int e = threadIdx.x; e < 64 * 32; e += kPrepThreads) {
+    const int i = e >> 5, j = (e & 31) * 2;
+    const float2 tt = *reinterpret_cast<const float2*>(Ts + i * kSA + j);
+    const float t0 = (j <= i) ? tt.x : 0.f;
+    const float t1 = (j + 1 <= i) ? tt.y : 0.f;
+    float a0, a1, b0, b1;
+    split_bf16(t0 * beg[j], a0, b0);
+    split_bf16(t1 * beg[j + 1], a1, b1);
+    st_bf16x2(TwH + swz<64>(i, j), a0, a1);
+    st_bf16x2(TwL + swz<64>(i, j), b0, b1);
+    split_bf16(t0 * bet[j], a0, b0);
+    split_bf16(t1 * bet[j + 1], a1, b1);
+    st_bf16x2(TuH + swz<64>(i, j), a0, a1);
+    st_bf16x2(TuL + swz<64>(i, j), b0, b1);
+  }
+  __syncthreads();
+
+  // ---- a4: W = Tw K [64 x DK] (warp: 16 rows x DK/2 columns), hi and lo passes ----
+  constexpr int NTW = DK / 16;
+  const int wc0 = ch * (DK / 2);
+  float wacc[NTW][4];
+  zero_acc(wacc);
+  wgemm<NTW, false, true, 64, DK>(wacc, TwH, row0, Ks, wc0, 0, 64, lane);
+  wgemm<NTW, false, true, 64, DK>(wacc, TwL, row0, Ks, wc0, 0, 64, lane);
+
+  // ---- a5: W QDQ over the whole [L, DK] tile ----
+  if constexpr (WM != GDN_QDQ_NONE) {
+    float m = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(wacc[nt][e]));
+    m = warp_max(m);
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    float amax = red[0];
+#pragma unroll
+    for (int i = 1; i < kPrepWarps; ++i) amax = fmaxf(amax, red[i]);
+    float sW, rcp;
+    qdq_scale<WM>(amax, sW, rcp);
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int i = row0 + gq + 8 * e2, col = wc0 + nt * 8 + 2 * tq;
+        uint8_t c0, c1;
+        if (amax == 0.f) {
+          c0 = qdq_zero_code<WM>(wacc[nt][2 * e2]);
+          c1 = qdq_zero_code<WM>(wacc[nt][2 * e2 + 1]);
+        } else {
+          c0 = qdq_code<WM>(wacc[nt][2 * e2], rcp);
+          c1 = qdq_code<WM>(wacc[nt][2 * e2 + 1], rcp);
+        }
+        *reinterpret_cast<uint16_t*>(Wst + i * DK + col) = (uint16_t)(c0 | (c1 << 8));
+      }
+    __syncthreads();
+    constexpr int CPR = DK / 16;
+    for (int i = threadIdx.x; i < L * CPR; i += kPrepThreads) {
+      const int r = i / CPR, c16 = i % CPR;
+      *reinterpret_cast<uint4*>(p.w_codes + ((tok0 + r) * p.Hv + h) * DK + c16 * 16) =
+          *reinterpret_cast<const uint4*>(Wst + r * DK + c16 * 16);
+    }
+    if (threadIdx.x == 0) p.w_scales[slot * p.Hv + h] = (amax == 0.f) ? 0.f : sW;
+  } else {
+#pragma unroll
+    for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int i = row0 + gq + 8 * e2, col = wc0 + nt * 8 + 2 * tq;
+        if (i < L)
+          *reinterpret_cast<float2*>(p.w_full + ((tok0 + i) * p.Hv + h) * DK + col) =
+              make_float2(wacc[nt][2 * e2], wacc[nt][2 * e2 + 1]);
+      }
+  }
+
+  // ---- a4: U = Tu V, one 64-column block at a time, parked in o ----
+  for (int vb = 0; vb < nvb; ++vb) {
+    float uacc[4][4];
+    zero_acc(uacc);
+    const __nv_bfloat16* Vb = Vs + vb * kChunk * 64;
+    wgemm<4, false, true, 64, 64>(uacc, TuH, row0, Vb, col0, 0, 64, lane);
+    wgemm<4, false, true, 64, 64>(uacc, TuL, row0, Vb, col0, 0, 64, lane);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
+        *reinterpret_cast<float2*>(Ust + i * kSA + j) =
+            make_float2(uacc[nt][2 * e2], uacc[nt][2 * e2 + 1]);
+      }
+    __syncthreads();
+    for (int i = threadIdx.x; i < L * 16; i += kPrepThreads) {
+      const int r = i >> 4, c4 = i & 15;
+      *reinterpret_cast<float4*>(p.o + ((tok0 + r) * p.Hv + h) * p.Dv + vb * 64 + c4 * 4) =
+          *reinterpret_cast<const float4*>(Ust + r * kSA + c4 * 4);
+    }
+    __syncthreads();
+  }
+}
+
+// ===========================================================================
+// 2. Serial state scan: H^ = Q_S(H), Delta = U - W^ H^, H <- e^{gL} H^ + K~^T Delta.
+// ===========================================================================
+constexpr int kStateThreads = 512;
+constexpr int kStateWarps = kStateThreads / 32;
+
+template <int DK, int SM, int WM>
+struct StateSmem {
+  static constexpr int WRAW = (WM == GDN_QDQ_NONE) ? kChunk * DK * 4 : kChunk * DK;
+  static constexpr int K = 0;                                          // 2 x bf16 [64][DK]
+  static constexpr int WR = K + 2 * kChunk * DK * 2;                   // 2 x W codes / f32
+  static constexpr int U = WR + 2 * WRAW;                              // 2 x f32 [64][kSA]
+  static constexpr int G = U + 2 * kF32Tile;                           // 2 x g[64]
+  static constexpr int VEC = G + 512;                                  // decay[64], e^{gL}
+  static constexpr int WC = VEC + 512;                                 // W^ bf16 [64][DK] (hi, lo)
+  static constexpr int HC = WC + (WM == GDN_QDQ_NONE ? 2 : 1) * kChunk * DK * 2;  // H^ [DK][64]
+  static constexpr int DP = HC + (SM == GDN_QDQ_NONE ? 2 : 1) * DK * 64 * 2;      // Delta' hi, lo
+  static constexpr int HST = DP + 2 * kChunk * 64 * 2;                 // u8 [DK][64] codes
+  static constexpr int BYTES = HST + DK * 64;
+  static_assert(BYTES <= 232448, "shared memory budget");
+  static_assert((WR % 128) == 0 && (U % 128) == 0 && (WC % 128) == 0 && (HC % 128) == 0 &&
+                    (DP % 128) == 0 && (HST % 16) == 0,
+                "alignment");
+};
+
+template <int DK, int WM>
+__device__ __forceinline__ void load_state_chunk(const FwdParams& p, __nv_bfloat16* Ks, unsigned char* Wr, float* Us,
+                                                 float* Gs, int64_t tok0, int L, int hk, int h,
+                                                 int vb) {
+  load_rows_bf16<DK, kStateThreads>(Ks, p.k, tok0, L, p.Hk, hk);
+  if constexpr (WM != GDN_QDQ_NONE) {
+    constexpr int CPR = DK / 16;
+    for (int i = threadIdx.x; i < kChunk * CPR; i += kStateThreads) {
+      const int r = i / CPR, c = i % CPR;
+      const bool ok = r < L;
+      const int64_t tok = tok0 + (ok ? r : 0);
+      cp_async16(smem_u32(Wr + r * DK + c * 16), p.w_codes + (tok * p.Hv + h) * DK + c * 16,
+                 ok ? 16 : 0);
+    }
+  } else {
+    constexpr int CPR = DK / 4;
+    for (int i = threadIdx.x; i < kChunk * CPR; i += kStateThreads) {
+      const int r = i / CPR, c = i % CPR;
+      const bool ok = r < L;
+      const int64_t tok = tok0 + (ok ? r : 0);
+      cp_async16(smem_u32(Wr + (r * DK + c * 4) * 4), p.w_full + (tok * p.Hv + h) * DK + c * 4,
+                 ok ? 16 : 0);
+    }
+  }
+  for (int i = threadIdx.x; i < kChunk * 16; i += kStateThreads) {
+    const int r = i >> 4, c = i & 15;
+    const bool ok = r < L;
+    const int64_t tok = tok0 + (ok ? r : 0);
+    cp_async16(smem_u32(Us + r * kSA + c * 4), p.o + (tok * p.Hv + h) * p.Dv + vb * 64 + c * 4,
+               ok ? 16 : 0);
+  }
+  if (threadIdx.x < kChunk) load_vec64(Gs, p.g, tok0, L, p.Hv, h, threadIdx.x);
 }
 
 template <int DK, int SM, int WM>
-__global__ void __launch_bounds__(kThreads, 1) gdn_fwd_kernel(const FwdParams p) {
-  using S = Smem<DK, SM, WM>;
+__global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const FwdParams p) {
+  using S = StateSmem<DK, SM, WM>;
   extern __shared__ __align__(1024) unsigned char sm[];
-  __shared__ float red[2][kWarps];
+  __shared__ float red[kStateWarps];
 
   const int vb = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
   const int hk = h / p.G;
@@ -147,47 +429,30 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_kernel(const FwdParams p)
   }
   const int nchunks = (L + kChunk - 1) / kChunk;
 
-  __nv_bfloat16* Vs = reinterpret_cast<__nv_bfloat16*>(sm + S::V);
-  float* gam = reinterpret_cast<float*>(sm + S::VEC);
-  float* eg = gam + 64;
-  float* beg = gam + 128;
-  float* bet = gam + 192;
-  float* dec = gam + 256;
-  float* As = reinterpret_cast<float*>(sm + S::A);
-  float* Ts = reinterpret_cast<float*>(sm + S::TT);
-  __nv_bfloat16* TwH = reinterpret_cast<__nv_bfloat16*>(sm + S::TW);
-  __nv_bfloat16* TwL = TwH + kChunk * 64;
-  __nv_bfloat16* TuH = reinterpret_cast<__nv_bfloat16*>(sm + S::TU);
-  __nv_bfloat16* TuL = TuH + kChunk * 64;
-  __nv_bfloat16* PH = reinterpret_cast<__nv_bfloat16*>(sm + S::P);
-  __nv_bfloat16* PL = PH + kChunk * 64;
+  float* dec = reinterpret_cast<float*>(sm + S::VEC);  // e^{gamma_L - gamma_i}; [64] = e^{gamma_L}
   __nv_bfloat16* WcH = reinterpret_cast<__nv_bfloat16*>(sm + S::WC);
-  __nv_bfloat16* WcL = WcH + kChunk * DK;  // only with WM == NONE
+  __nv_bfloat16* WcL = WcH + kChunk * DK;  // WM == NONE only
   __nv_bfloat16* HcH = reinterpret_cast<__nv_bfloat16*>(sm + S::HC);
-  __nv_bfloat16* HcL = HcH + DK * 64;      // only with SM == NONE
-  __nv_bfloat16* DpH = TwH;                // Delta' = diag(e^{gL - gamma}) Delta
-  __nv_bfloat16* DpL = TwL;
-  __nv_bfloat16* DH = TuH;
-  __nv_bfloat16* DL = TuL;
-  uint8_t* Hstage = reinterpret_cast<uint8_t*>(sm + S::TW);  // [DK][64] codes
-  uint8_t* Wstage = reinterpret_cast<uint8_t*>(sm + S::TT);  // [64][DK] codes
-  float* Ostage = As;                                         // [64][kSA] f32
-  constexpr int OSTR = kSA;
+  __nv_bfloat16* HcL = HcH + DK * 64;      // SM == NONE only
+  __nv_bfloat16* DpH = reinterpret_cast<__nv_bfloat16*>(sm + S::DP);
+  __nv_bfloat16* DpL = DpH + kChunk * 64;
+  uint8_t* Hst = sm + S::HST;
+  auto Kbuf = [&](int b) { return reinterpret_cast<__nv_bfloat16*>(sm + S::K + b * kChunk * DK * 2); };
+  auto Wbuf = [&](int b) { return sm + S::WR + b * S::WRAW; };
+  auto Ubuf = [&](int b) { return reinterpret_cast<float*>(sm + S::U + b * kF32Tile); };
+  auto Gbuf = [&](int b) { return reinterpret_cast<float*>(sm + S::G + b * 256); };
 
-  // warp tiles: [64 x 64] outputs -> 16 x 16 per warp; [64 x DK] -> 16 x DK/4
-  const int rt = warp & 3, cq = warp >> 2;
-  const int row0 = rt * 16, col0 = cq * 16;
-  constexpr int NTW = DK / 32;
-  const int wcol0 = cq * (DK / 4);
-  // state tile [DK x 64]
-  constexpr int HM = DK / 16;            // row tiles
-  constexpr int HN = kWarps / HM;        // warps per row tile
-  constexpr int NTH = 8 / HN;            // 8-wide n tiles per warp
+  // Delta tile: [64 x 64] -> 16 x 16 per warp; state tile [DK x 64]
+  const int row0 = (warp & 3) * 16, col0 = (warp >> 2) * 16;
+  constexpr int HM = DK / 16;
+  constexpr int HN = kStateWarps / HM;
+  constexpr int NTH = 8 / HN;
   const int h_row0 = (warp % HM) * 16;
   const int h_col0 = (warp / HM) * (64 / HN);
   float hreg[NTH][4];
   {
     const float* src = p.h0 ? p.h0 + (((int64_t)n * p.Hv + h) * DK) * p.Dv + vb * 64 : nullptr;
+    float m = 0.f;
 #pragma unroll
     for (int nt = 0; nt < NTH; ++nt)
 #pragma unroll
@@ -197,111 +462,68 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_kernel(const FwdParams p)
         if (src) v2 = *reinterpret_cast<const float2*>(src + (int64_t)d * p.Dv + c);
         hreg[nt][2 * e2] = v2.x;
         hreg[nt][2 * e2 + 1] = v2.y;
+        m = fmaxf(m, fmaxf(fabsf(v2.x), fabsf(v2.y)));
       }
+    m = warp_max(m);
+    if (lane == 0) red[warp] = m;
   }
 
-  // Prologue: chunk 0 (K, Q, beta/g, V) and chunk 1 (K, Q, beta/g).
+  float sW_next = 1.f;
   if (nchunks > 0) {
-    load_kq<DK>(p, sm, S::K, S::Q, S::BG, tok0, min(L, kChunk), hk, h);
-    load_v(p, sm, S::V, tok0, min(L, kChunk), h, vb);
+    load_state_chunk<DK, WM>(p, Kbuf(0), Wbuf(0), Ubuf(0), Gbuf(0), tok0, min(L, kChunk), hk,
+                             h, vb);
+    if constexpr (WM != GDN_QDQ_NONE) sW_next = p.w_scales[slot0 * p.Hv + h];
   }
-  cp_async_commit();
-  if (nchunks > 1)
-    load_kq<DK>(p, sm, S::K + S::kTileK, S::Q + S::kTileK, S::BG + 512, tok0 + kChunk,
-                min(L - kChunk, kChunk), hk, h);
   cp_async_commit();
 
   for (int c = 0; c < nchunks; ++c) {
     const int buf = c & 1;
-    const int Lc = min(L - c * kChunk, kChunk);
-    const int64_t ctok = tok0 + (int64_t)c * kChunk;
     const int64_t slot = slot0 + c;
-    __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(sm + S::K + buf * S::kTileK);
-    __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(sm + S::Q + buf * S::kTileK);
-    const float* bsrc = reinterpret_cast<const float*>(sm + S::BG + buf * 512);
-    cp_async_wait<1>();
-    __syncthreads();
+    const float sW = sW_next;
+    cp_async_wait<0>();
+    __syncthreads();  // chunk c landed; amax partials of H visible; buffer buf^1 free
 
-    // ---- a1: in-chunk cumulative log decay (warp 0; padded rows have g = 0) ----
     if (warp == 0) {
-      const float g0 = bsrc[64 + 2 * lane], g1 = bsrc[64 + 2 * lane + 1];
-      float s = g0 + g1;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, s, o);
-        if (lane >= o) s += y;
-      }
-      const float gam1 = s, gam0 = s - g1;
-      const float gL = __shfl_sync(0xffffffffu, s, 31);
-      const float b0 = bsrc[2 * lane], b1 = bsrc[2 * lane + 1];
-      gam[2 * lane] = gam0;
-      gam[2 * lane + 1] = gam1;
-      const float e0 = expf(gam0), e1 = expf(gam1);
-      eg[2 * lane] = e0;
-      eg[2 * lane + 1] = e1;
-      beg[2 * lane] = b0 * e0;
-      beg[2 * lane + 1] = b1 * e1;
-      bet[2 * lane] = b0;
-      bet[2 * lane + 1] = b1;
+      float gam0, gam1, gL;
+      chunk_cumsum(Gbuf(buf), lane, gam0, gam1, gL);
       dec[2 * lane] = expf(gL - gam0);
       dec[2 * lane + 1] = expf(gL - gam1);
+      if (lane == 0) dec[64] = expf(gL);
     }
-    // state amax (a6), warp partials
-    {
-      float m = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < NTH; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(hreg[nt][e]));
-      m = warp_max(m);
-      if (lane == 0) red[0][warp] = m;
-    }
-    __syncthreads();
 
-    // ---- a2 (+ QK^T for a8): A = strict-lower(beta_i Gamma_ij KK^T), P = lower-incl(Gamma QK^T) ----
-    if (cq <= rt) {
-      float akk[2][4], aqk[2][4];
-      zero_acc(akk);
-      zero_acc(aqk);
-#pragma unroll
-      for (int ks = 0; ks < DK / 16; ++ks) {
-        uint32_t ak[4], aq[4], b[4];
-        ldsm_x4(ak, a_frag_addr<DK>(Ks, row0, ks * 16, lane));
-        ldsm_x4(aq, a_frag_addr<DK>(Qs, row0, ks * 16, lane));
-        ldsm_x4(b, bnk_frag_addr<DK>(Ks, col0, ks * 16, lane));
-        mma_bf16(akk[0], ak, b[0], b[1]);
-        mma_bf16(akk[1], ak, b[2], b[3]);
-        mma_bf16(aqk[0], aq, b[0], b[1]);
-        mma_bf16(aqk[1], aq, b[2], b[3]);
+    // W^ operand: codes -> bf16 values (exact), or the fp32 W split hi/lo
+    if constexpr (WM != GDN_QDQ_NONE) {
+      const uint8_t* Wr = Wbuf(buf);
+      constexpr int C4 = DK / 4;
+      for (int i = threadIdx.x; i < kChunk * C4; i += kStateThreads) {
+        const int r = i / C4, c4 = i % C4;
+        const float4 v = qdq_code4_values<WM>(*reinterpret_cast<const uint32_t*>(Wr + r * DK + c4 * 4));
+        const int e = swz<DK>(r, c4 * 4);
+        *reinterpret_cast<uint2*>(WcH + e) = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
       }
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int i = row0 + gq + 8 * e2;
-          const int j = col0 + nt * 8 + 2 * tq;
-          const float gi = gam[i];
-          const float x0 = (j <= i) ? expf(gi - gam[j]) : 0.f;
-          const float x1 = (j + 1 <= i) ? expf(gi - gam[j + 1]) : 0.f;
-          const float bi = bet[i];
-          *reinterpret_cast<float2*>(As + i * kSA + j) =
-              make_float2((j < i) ? bi * x0 * akk[nt][2 * e2] : 0.f,
-                          (j + 1 < i) ? bi * x1 * akk[nt][2 * e2 + 1] : 0.f);
-          const float p0 = x0 * aqk[nt][2 * e2], p1 = x1 * aqk[nt][2 * e2 + 1];
-          float h0v, l0v, h1v, l1v;
-          split_bf16(p0, h0v, l0v);
-          split_bf16(p1, h1v, l1v);
-          st_bf16x2(PH + swz<64>(i, j), h0v, h1v);
-          st_bf16x2(PL + swz<64>(i, j), l0v, l1v);
-        }
+    } else {
+      const float* Wr = reinterpret_cast<const float*>(Wbuf(buf));
+      constexpr int C4 = DK / 4;
+      for (int i = threadIdx.x; i < kChunk * C4; i += kStateThreads) {
+        const int r = i / C4, c4 = i % C4;
+        const float4 v = *reinterpret_cast<const float4*>(Wr + r * DK + c4 * 4);
+        float h0v, l0v, h1v, l1v, h2v, l2v, h3v, l3v;
+        split_bf16(v.x, h0v, l0v);
+        split_bf16(v.y, h1v, l1v);
+        split_bf16(v.z, h2v, l2v);
+        split_bf16(v.w, h3v, l3v);
+        const int e = swz<DK>(r, c4 * 4);
+        *reinterpret_cast<uint2*>(WcH + e) = make_uint2(pack_bf16(h0v, h1v), pack_bf16(h2v, h3v));
+        *reinterpret_cast<uint2*>(WcL + e) = make_uint2(pack_bf16(l0v, l1v), pack_bf16(l2v, l3v));
+      }
     }
 
-    // ---- a6: state QDQ (every thread holds a piece of the state tile) ----
+    // ---- a6: state QDQ over the [DK x 64] tile ----
     float sH = 1.f;
     {
-      float amax = red[0][0];
+      float amax = red[0];
 #pragma unroll
-      for (int i = 1; i < kWarps; ++i) amax = fmaxf(amax, red[0][i]);
+      for (int i = 1; i < kStateWarps; ++i) amax = fmaxf(amax, red[i]);
       if constexpr (SM != GDN_QDQ_NONE) {
         float rcp;
         qdq_scale<SM>(amax, sH, rcp);
@@ -312,12 +534,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_kernel(const FwdParams p)
             const int d = h_row0 + gq + 8 * e2, col = h_col0 + nt * 8 + 2 * tq;
             float* hv = &hreg[nt][2 * e2];
             uint8_t c0, c1;
-            float v0, v1;
+            float v0 = 0.f, v1 = 0.f;
             if (amax == 0.f) {
               c0 = qdq_zero_code<SM>(hv[0]);
               c1 = qdq_zero_code<SM>(hv[1]);
-              v0 = 0.f;
-              v1 = 0.f;
             } else {
               c0 = qdq_code<SM>(hv[0], rcp);
               c1 = qdq_code<SM>(hv[1], rcp);
@@ -327,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_kernel(const FwdParams p)
               hv[1] = __fmul_rn(v1, sH);
             }
             st_bf16x2(HcH + swz<64>(d, col), v0, v1);
-            *reinterpret_cast<uint16_t*>(Hstage + d * 64 + col) = (uint16_t)(c0 | (c1 << 8));
+            *reinterpret_cast<uint16_t*>(Hst + d * 64 + col) = (uint16_t)(c0 | (c1 << 8));
           }
         if (amax == 0.f) sH = 0.f;
       } else {
@@ -341,133 +561,32 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_kernel(const FwdParams p)
             split_bf16(hreg[nt][2 * e2 + 1], hi1, lo1);
             st_bf16x2(HcH + swz<64>(d, col), hi0, hi1);
             st_bf16x2(HcL + swz<64>(d, col), lo0, lo1);
-            if (p.h_full) {
-              float* dst = p.h_full + ((slot * p.Hv + h) * DK + d) * p.Dv + vb * 64 + col;
-              *reinterpret_cast<float2*>(dst) = make_float2(hreg[nt][2 * e2], hreg[nt][2 * e2 + 1]);
-            }
+            *reinterpret_cast<float2*>(p.h_full + ((slot * p.Hv + h) * DK + d) * p.Dv + vb * 64 +
+                                       col) = make_float2(hreg[nt][2 * e2], hreg[nt][2 * e2 + 1]);
           }
       }
     }
+    __syncthreads();  // W^, H^ operands, decay factors ready
 
-    __syncthreads();  // A, P, H codes complete
-
-    // saved context: state codes (coalesced 16-byte rows) and scale
-    if constexpr (SM != GDN_QDQ_NONE) {
-      if (p.h_codes) {
-        for (int i = threadIdx.x; i < DK * 4; i += kThreads) {
-          const int d = i >> 2, c16 = i & 3;
-          const uint4 val = *reinterpret_cast<const uint4*>(Hstage + d * 64 + c16 * 16);
-          *reinterpret_cast<uint4*>(p.h_codes + ((slot * p.Hv + h) * DK + d) * p.Dv + vb * 64 +
-                                    c16 * 16) = val;
-        }
-        if (threadIdx.x == 0) p.h_scales[(slot * p.Hv + h) * (p.Dv / 64) + vb] = sH;
-      }
+    // prefetch chunk c + 1 (buffer buf ^ 1 was last read before this iteration's first barrier)
+    if (c + 1 < nchunks) {
+      load_state_chunk<DK, WM>(p, Kbuf(buf ^ 1), Wbuf(buf ^ 1), Ubuf(buf ^ 1), Gbuf(buf ^ 1),
+                               tok0 + (int64_t)(c + 1) * kChunk,
+                               min(L - (c + 1) * kChunk, kChunk), hk, h, vb);
+      if constexpr (WM != GDN_QDQ_NONE) sW_next = p.w_scales[(slot + 1) * p.Hv + h];
     }
-
-    // ---- a3: T = (I + A)^-1 ----
-    solve_unit_lower64<kThreads>(As, Ts);
-
-    // ---- a4 operands: Tw = T diag(beta e^gamma), Tu = T diag(beta), split hi/lo ----
-    for (int e = threadIdx.x; e < 64 * 32; e += kThreads) {
-      const int i = e >> 5, j = (e & 31) * 2;
-      const float2 tt = *reinterpret_cast<const float2*>(Ts + i * kSA + j);
-      const float t0 = (j <= i) ? tt.x : 0.f;
-      const float t1 = (j + 1 <= i) ? tt.y : 0.f;
-      float a0, a1, b0, b1;
-      split_bf16(t0 * beg[j], a0, b0);
-      split_bf16(t1 * beg[j + 1], a1, b1);
-      st_bf16x2(TwH + swz<64>(i, j), a0, a1);
-      st_bf16x2(TwL + swz<64>(i, j), b0, b1);
-      split_bf16(t0 * bet[j], a0, b0);
-      split_bf16(t1 * bet[j + 1], a1, b1);
-      st_bf16x2(TuH + swz<64>(i, j), a0, a1);
-      st_bf16x2(TuL + swz<64>(i, j), b0, b1);
-    }
-    __syncthreads();
-
-    // ---- a4: W = Tw K  [64 x DK] and U = Tu V  [64 x 64] (hi and lo passes) ----
-    float wacc[NTW][4];
-    zero_acc(wacc);
-    float uacc[2][4];
-    zero_acc(uacc);
-    wgemm<NTW, false, true, 64, DK>(wacc, TwH, row0, Ks, wcol0, 0, 64, lane);
-    wgemm<2, false, true, 64, 64>(uacc, TuH, row0, Vs, col0, 0, 64, lane);
-    wgemm<NTW, false, true, 64, DK>(wacc, TwL, row0, Ks, wcol0, 0, 64, lane);
-    wgemm<2, false, true, 64, 64>(uacc, TuL, row0, Vs, col0, 0, 64, lane);
-    {
-      float m = 0.f;
-#pragma unroll
-      for (int nt = 0; nt < NTW; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(wacc[nt][e]));
-      m = warp_max(m);
-      if (lane == 0) red[1][warp] = m;
-    }
-    __syncthreads();  // W amax partials; Tw/Tu/V reads done
-
-    // V buffer is free: prefetch the next chunk's V.
-    if (c + 1 < nchunks) load_v(p, sm, S::V, ctok + kChunk, min(L - (c + 1) * kChunk, kChunk), h, vb);
     cp_async_commit();
 
-    // ---- a5: W QDQ over the whole [L, DK] tile ----
-    float sW = 1.f;
-    {
-      float amax = red[1][0];
-#pragma unroll
-      for (int i = 1; i < kWarps; ++i) amax = fmaxf(amax, red[1][i]);
-      if constexpr (WM != GDN_QDQ_NONE) {
-        float rcp;
-        qdq_scale<WM>(amax, sW, rcp);
-#pragma unroll
-        for (int nt = 0; nt < NTW; ++nt)
-#pragma unroll
-          for (int e2 = 0; e2 < 2; ++e2) {
-            const int i = row0 + gq + 8 * e2, col = wcol0 + nt * 8 + 2 * tq;
-            uint8_t c0, c1;
-            float v0, v1;
-            if (amax == 0.f) {
-              c0 = qdq_zero_code<WM>(wacc[nt][2 * e2]);
-              c1 = qdq_zero_code<WM>(wacc[nt][2 * e2 + 1]);
-              v0 = v1 = 0.f;
-            } else {
-              c0 = qdq_code<WM>(wacc[nt][2 * e2], rcp);
-              c1 = qdq_code<WM>(wacc[nt][2 * e2 + 1], rcp);
-              v0 = qdq_code_value<WM>(c0);
-              v1 = qdq_code_value<WM>(c1);
-            }
-            st_bf16x2(WcH + swz<DK>(i, col), v0, v1);
-            *reinterpret_cast<uint16_t*>(Wstage + i * DK + col) = (uint16_t)(c0 | (c1 << 8));
-          }
-        if (amax == 0.f) sW = 0.f;
-      } else {
-#pragma unroll
-        for (int nt = 0; nt < NTW; ++nt)
-#pragma unroll
-          for (int e2 = 0; e2 < 2; ++e2) {
-            const int i = row0 + gq + 8 * e2, col = wcol0 + nt * 8 + 2 * tq;
-            float hi0, lo0, hi1, lo1;
-            split_bf16(wacc[nt][2 * e2], hi0, lo0);
-            split_bf16(wacc[nt][2 * e2 + 1], hi1, lo1);
-            st_bf16x2(WcH + swz<DK>(i, col), hi0, hi1);
-            st_bf16x2(WcL + swz<DK>(i, col), lo0, lo1);
-          }
+    if constexpr (SM != GDN_QDQ_NONE) {
+      for (int i = threadIdx.x; i < DK * 4; i += kStateThreads) {
+        const int d = i >> 2, c16 = i & 3;
+        *reinterpret_cast<uint4*>(p.h_codes + ((slot * p.Hv + h) * DK + d) * p.Dv + vb * 64 +
+                                  c16 * 16) = *reinterpret_cast<const uint4*>(Hst + d * 64 + c16 * 16);
       }
-    }
-    __syncthreads();  // W^ operand complete
-
-    if constexpr (WM != GDN_QDQ_NONE) {
-      if (p.w_codes && vb == 0) {
-        constexpr int CPR = DK / 16;
-        for (int i = threadIdx.x; i < Lc * CPR; i += kThreads) {
-          const int r = i / CPR, c16 = i % CPR;
-          const uint4 val = *reinterpret_cast<const uint4*>(Wstage + r * DK + c16 * 16);
-          *reinterpret_cast<uint4*>(p.w_codes + ((ctok + r) * p.Hv + h) * DK + c16 * 16) = val;
-        }
-        if (threadIdx.x == 0) p.w_scales[slot * p.Hv + h] = sW;
-      }
+      if (threadIdx.x == 0) p.h_scales[(slot * p.Hv + h) * (p.Dv / 64) + vb] = sH;
     }
 
-    // ---- a7: Delta = U - W^ H^ ----
+    // ---- a7: Delta = U - W^ H^;  Delta' = diag(e^{gamma_L - gamma}) Delta ----
     {
       float dacc[2][4];
       zero_acc(dacc);
@@ -475,79 +594,44 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_kernel(const FwdParams p)
       if constexpr (WM == GDN_QDQ_NONE) wgemm<2, false, true, DK, 64>(dacc, WcL, row0, HcH, col0, 0, DK, lane);
       if constexpr (SM == GDN_QDQ_NONE) wgemm<2, false, true, DK, 64>(dacc, WcH, row0, HcL, col0, 0, DK, lane);
       const float sWH = (WM != GDN_QDQ_NONE ? sW : 1.f) * (SM != GDN_QDQ_NONE ? sH : 1.f);
+      const float* Us = Ubuf(buf);
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-          const float d0 = uacc[nt][2 * e2] - sWH * dacc[nt][2 * e2];
-          const float d1 = uacc[nt][2 * e2 + 1] - sWH * dacc[nt][2 * e2 + 1];
-          float h0v, l0v, h1v, l1v;
-          split_bf16(d0, h0v, l0v);
-          split_bf16(d1, h1v, l1v);
-          st_bf16x2(DH + swz<64>(i, j), h0v, h1v);
-          st_bf16x2(DL + swz<64>(i, j), l0v, l1v);
+          const float2 u = *reinterpret_cast<const float2*>(Us + i * kSA + j);
           const float di = dec[i];
-          split_bf16(d0 * di, h0v, l0v);
-          split_bf16(d1 * di, h1v, l1v);
+          float h0v, l0v, h1v, l1v;
+          split_bf16((u.x - sWH * dacc[nt][2 * e2]) * di, h0v, l0v);
+          split_bf16((u.y - sWH * dacc[nt][2 * e2 + 1]) * di, h1v, l1v);
           st_bf16x2(DpH + swz<64>(i, j), h0v, h1v);
           st_bf16x2(DpL + swz<64>(i, j), l0v, l1v);
         }
     }
-    __syncthreads();  // Delta operands complete
-
-    // ---- a8: O = scale (diag(e^gamma) Q H^ + P Delta) ----
-    {
-      float o1[2][4], o2[2][4];
-      zero_acc(o1);
-      zero_acc(o2);
-      wgemm<2, false, true, DK, 64>(o1, Qs, row0, HcH, col0, 0, DK, lane);
-      if constexpr (SM == GDN_QDQ_NONE) wgemm<2, false, true, DK, 64>(o1, Qs, row0, HcL, col0, 0, DK, lane);
-      const int kend = row0 + 16;   // P is lower triangular: columns j <= i only
-      wgemm<2, false, true, 64, 64>(o2, PH, row0, DH, col0, 0, kend, lane);
-      wgemm<2, false, true, 64, 64>(o2, PH, row0, DL, col0, 0, kend, lane);
-      wgemm<2, false, true, 64, 64>(o2, PL, row0, DH, col0, 0, kend, lane);
-      const float sq = (SM != GDN_QDQ_NONE) ? sH : 1.f;
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-          const float ei = eg[i] * sq;
-          float2 r;
-          r.x = p.scale * (ei * o1[nt][2 * e2] + o2[nt][2 * e2]);
-          r.y = p.scale * (ei * o1[nt][2 * e2 + 1] + o2[nt][2 * e2 + 1]);
-          *reinterpret_cast<float2*>(Ostage + i * OSTR + j) = r;
-        }
-    }
+    __syncthreads();  // Delta' ready
 
     // ---- a9: H <- e^{gamma_L} H^ + K^T Delta' ----
     {
-      const float egL = eg[63];
+      const float egL = dec[64];
+      float m = 0.f;
 #pragma unroll
       for (int nt = 0; nt < NTH; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) hreg[nt][e] *= egL;
+      const __nv_bfloat16* Ks = Kbuf(buf);
       wgemm<NTH, true, true, DK, 64>(hreg, Ks, h_row0, DpH, h_col0, 0, 64, lane);
       wgemm<NTH, true, true, DK, 64>(hreg, Ks, h_row0, DpL, h_col0, 0, 64, lane);
+#pragma unroll
+      for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(hreg[nt][e]));
+      m = warp_max(m);
+      if (lane == 0) red[warp] = m;
     }
-    __syncthreads();  // O staged; all reads of K/Q(buf), Delta, P done
-
-    // output rows of this chunk (coalesced 16-byte stores)
-    for (int i = threadIdx.x; i < Lc * 16; i += kThreads) {
-      const int r = i >> 4, c4 = i & 15;
-      const float4 val = *reinterpret_cast<const float4*>(Ostage + r * OSTR + c4 * 4);
-      *reinterpret_cast<float4*>(p.o + ((ctok + r) * p.Hv + h) * p.Dv + vb * 64 + c4 * 4) = val;
-    }
-    // prefetch chunk c + 2 into this buffer
-    if (c + 2 < nchunks)
-      load_kq<DK>(p, sm, S::K + buf * S::kTileK, S::Q + buf * S::kTileK, S::BG + buf * 512,
-                  ctok + 2 * kChunk, min(L - (c + 2) * kChunk, kChunk), hk, h);
-    cp_async_commit();
   }
   cp_async_wait<0>();
 
-  // final state (unquantized)
   if (p.ht) {
     float* dst = p.ht + (((int64_t)n * p.Hv + h) * DK) * p.Dv + vb * 64;
 #pragma unroll
@@ -561,16 +645,258 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_kernel(const FwdParams p)
   }
 }
 
+// ===========================================================================
+// 3. Output: O = scale (diag(e^gamma) Q H^ + P Delta), Delta = U - W^ H^.
+// ===========================================================================
+constexpr int kOutThreads = 256;
+
+template <int DK, int SM, int WM>
+struct OutSmem {
+  static constexpr int Q = 0;                                              // bf16 [64][DK]
+  static constexpr int K = Q + kChunk * DK * 2;                            // bf16 [64][DK]; later Delta hi, lo
+  static constexpr int WC = K + kChunk * DK * 2;                           // W^ [64][DK] (hi, lo)
+  static constexpr int HC = WC + (WM == GDN_QDQ_NONE ? 2 : 1) * kChunk * DK * 2;  // H^ [DK][64] (hi, lo)
+  static constexpr int U = HC + (SM == GDN_QDQ_NONE ? 2 : 1) * DK * 64 * 2;       // f32 [64][kSA]; later O
+  static constexpr int P = U + kF32Tile;                                   // P hi, lo [64][64]
+  static constexpr int G = P + 2 * kChunk * 64 * 2;                        // g[64], gamma[64], e^gamma[64]
+  // Delta hi, lo [64][64]: in the dead K tile when it is large enough
+  static constexpr bool D_IN_K = 2 * kChunk * 64 * 2 <= kChunk * DK * 2;
+  static constexpr int D = D_IN_K ? K : G + 3 * 64 * 4;
+  static constexpr int BYTES = D_IN_K ? G + 3 * 64 * 4 : D + 2 * kChunk * 64 * 2;
+  static_assert((K % 128) == 0 && (WC % 128) == 0 && (HC % 128) == 0 && (U % 128) == 0 &&
+                    (P % 128) == 0 && (D % 128) == 0,
+                "alignment");
+};
+
+template <int DK, int SM, int WM>
+__global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const FwdParams p) {
+  using S = OutSmem<DK, SM, WM>;
+  extern __shared__ __align__(1024) unsigned char sm[];
+
+  const int nvb = p.Dv / 64;
+  const int vb = blockIdx.x % nvb;
+  const int64_t sh = blockIdx.x / nvb;
+  const int64_t slot = sh / p.Hv;
+  const int h = (int)(sh % p.Hv);
+  ChunkRef cr;
+  if (!chunk_of_slot(p, slot, cr)) return;
+  const int hk = h / p.G;
+  const int L = cr.L;
+  const int64_t tok0 = cr.tok;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gq = lane >> 2, tq = lane & 3;
+
+  __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(sm + S::Q);
+  __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(sm + S::K);
+  __nv_bfloat16* WcH = reinterpret_cast<__nv_bfloat16*>(sm + S::WC);
+  __nv_bfloat16* WcL = WcH + kChunk * DK;
+  __nv_bfloat16* HcH = reinterpret_cast<__nv_bfloat16*>(sm + S::HC);
+  __nv_bfloat16* HcL = HcH + DK * 64;
+  float* Us = reinterpret_cast<float*>(sm + S::U);
+  float* Ost = Us;
+  __nv_bfloat16* PH = reinterpret_cast<__nv_bfloat16*>(sm + S::P);
+  __nv_bfloat16* PL = PH + kChunk * 64;
+  __nv_bfloat16* DH = reinterpret_cast<__nv_bfloat16*>(sm + S::D);
+  __nv_bfloat16* DL = DH + kChunk * 64;
+  float* Gs = reinterpret_cast<float*>(sm + S::G);
+  float* gam = Gs + 64;
+  float* eg = Gs + 128;
+
+  load_rows_bf16<DK, kOutThreads>(Qs, p.q, tok0, L, p.Hk, hk);
+  load_rows_bf16<DK, kOutThreads>(Ks, p.k, tok0, L, p.Hk, hk);
+  for (int i = threadIdx.x; i < kChunk * 16; i += kOutThreads) {
+    const int r = i >> 4, c = i & 15;
+    const bool ok = r < L;
+    const int64_t tok = tok0 + (ok ? r : 0);
+    cp_async16(smem_u32(Us + r * kSA + c * 4), p.o + (tok * p.Hv + h) * p.Dv + vb * 64 + c * 4,
+               ok ? 16 : 0);
+  }
+  if (threadIdx.x < kChunk) load_vec64(Gs, p.g, tok0, L, p.Hv, h, threadIdx.x);
+  cp_async_commit();
+
+  // W^ and H^ operands from the saved context (rows >= L of W are zero).  Codes
+  // land in the P tile (free until the P epilogue) and are widened after the wait.
+  uint8_t* Wraw = reinterpret_cast<uint8_t*>(PH);
+  uint8_t* Hraw = Wraw + kChunk * DK;
+  float sW = 1.f, sH = 1.f;
+  if constexpr (WM != GDN_QDQ_NONE) {
+    constexpr int C16 = DK / 16;
+    for (int i = threadIdx.x; i < kChunk * C16; i += kOutThreads) {
+      const int r = i / C16, c16 = i % C16;
+      const bool ok = r < L;
+      cp_async16(smem_u32(Wraw + r * DK + c16 * 16),
+                 p.w_codes + ((tok0 + (ok ? r : 0)) * p.Hv + h) * DK + c16 * 16, ok ? 16 : 0);
+    }
+    sW = p.w_scales[slot * p.Hv + h];
+  } else {
+    constexpr int C4 = DK / 4;
+    for (int i = threadIdx.x; i < kChunk * C4; i += kOutThreads) {
+      const int r = i / C4, c4 = i % C4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (r < L) v = *reinterpret_cast<const float4*>(p.w_full + ((tok0 + r) * p.Hv + h) * DK + c4 * 4);
+      float h0v, l0v, h1v, l1v, h2v, l2v, h3v, l3v;
+      split_bf16(v.x, h0v, l0v);
+      split_bf16(v.y, h1v, l1v);
+      split_bf16(v.z, h2v, l2v);
+      split_bf16(v.w, h3v, l3v);
+      const int e = swz<DK>(r, c4 * 4);
+      *reinterpret_cast<uint2*>(WcH + e) = make_uint2(pack_bf16(h0v, h1v), pack_bf16(h2v, h3v));
+      *reinterpret_cast<uint2*>(WcL + e) = make_uint2(pack_bf16(l0v, l1v), pack_bf16(l2v, l3v));
+    }
+  }
+  if constexpr (SM != GDN_QDQ_NONE) {
+    const uint8_t* src = p.h_codes + ((slot * p.Hv + h) * DK) * p.Dv + vb * 64;
+    for (int i = threadIdx.x; i < DK * 4; i += kOutThreads) {
+      const int d = i >> 2, c16 = i & 3;
+      cp_async16(smem_u32(Hraw + d * 64 + c16 * 16), src + (int64_t)d * p.Dv + c16 * 16, 16);
+    }
+    sH = p.h_scales[(slot * p.Hv + h) * nvb + vb];
+  } else {
+    const float* src = p.h_full + ((slot * p.Hv + h) * DK) * p.Dv + vb * 64;
+    for (int i = threadIdx.x; i < DK * 16; i += kOutThreads) {
+      const int d = i >> 4, c4 = i & 15;
+      const float4 v = *reinterpret_cast<const float4*>(src + (int64_t)d * p.Dv + c4 * 4);
+      float h0v, l0v, h1v, l1v, h2v, l2v, h3v, l3v;
+      split_bf16(v.x, h0v, l0v);
+      split_bf16(v.y, h1v, l1v);
+      split_bf16(v.z, h2v, l2v);
+      split_bf16(v.w, h3v, l3v);
+      const int e = swz<64>(d, c4 * 4);
+      *reinterpret_cast<uint2*>(HcH + e) = make_uint2(pack_bf16(h0v, h1v), pack_bf16(h2v, h3v));
+      *reinterpret_cast<uint2*>(HcL + e) = make_uint2(pack_bf16(l0v, l1v), pack_bf16(l2v, l3v));
+    }
+  }
+  cp_async_commit();
+  cp_async_wait<0>();
+  __syncthreads();
+
+  if constexpr (WM != GDN_QDQ_NONE) {
+    constexpr int C4 = DK / 4;
+    for (int i = threadIdx.x; i < kChunk * C4; i += kOutThreads) {
+      const int r = i / C4, c4 = i % C4;
+      const float4 v = qdq_code4_values<WM>(*reinterpret_cast<const uint32_t*>(Wraw + r * DK + c4 * 4));
+      *reinterpret_cast<uint2*>(WcH + swz<DK>(r, c4 * 4)) =
+          make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+    }
+  }
+  if constexpr (SM != GDN_QDQ_NONE) {
+    for (int i = threadIdx.x; i < DK * 16; i += kOutThreads) {
+      const int d = i >> 4, c4 = i & 15;
+      const float4 v = qdq_code4_values<SM>(*reinterpret_cast<const uint32_t*>(Hraw + d * 64 + c4 * 4));
+      *reinterpret_cast<uint2*>(HcH + swz<64>(d, c4 * 4)) =
+          make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+    }
+  }
+  __syncthreads();  // W^, H^ operands ready; the P tile is free again
+
+  if (warp == 0) {
+    float gam0, gam1, gL;
+    chunk_cumsum(Gs, lane, gam0, gam1, gL);
+    gam[2 * lane] = gam0;
+    gam[2 * lane + 1] = gam1;
+    eg[2 * lane] = expf(gam0);
+    eg[2 * lane + 1] = expf(gam1);
+  }
+
+  // warp tile: rows 16 rt .. +15, columns 32 ch .. +31
+  const int rt = warp & 3, ch = warp >> 2;
+  const int row0 = rt * 16, col0 = ch * 32;
+  const bool p_tile = col0 <= row0 + 15;
+  float pacc[4][4], dacc[4][4], qacc[4][4];
+  zero_acc(pacc);
+  zero_acc(dacc);
+  zero_acc(qacc);
+  if (p_tile) wgemm<4, false, false, DK, DK>(pacc, Qs, row0, Ks, col0, 0, DK, lane);
+  wgemm<4, false, true, DK, 64>(dacc, WcH, row0, HcH, col0, 0, DK, lane);
+  if constexpr (WM == GDN_QDQ_NONE) wgemm<4, false, true, DK, 64>(dacc, WcL, row0, HcH, col0, 0, DK, lane);
+  if constexpr (SM == GDN_QDQ_NONE) wgemm<4, false, true, DK, 64>(dacc, WcH, row0, HcL, col0, 0, DK, lane);
+  wgemm<4, false, true, DK, 64>(qacc, Qs, row0, HcH, col0, 0, DK, lane);
+  if constexpr (SM == GDN_QDQ_NONE) wgemm<4, false, true, DK, 64>(qacc, Qs, row0, HcL, col0, 0, DK, lane);
+  __syncthreads();  // K reads done (its tile becomes Delta); gamma ready
+
+  const float sWH = (WM != GDN_QDQ_NONE ? sW : 1.f) * (SM != GDN_QDQ_NONE ? sH : 1.f);
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int e2 = 0; e2 < 2; ++e2) {
+      const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
+      float h0v, l0v, h1v, l1v;
+      if (p_tile) {
+        const float gi = gam[i];
+        const float p0 = (j <= i) ? expf(gi - gam[j]) * pacc[nt][2 * e2] : 0.f;
+        const float p1 = (j + 1 <= i) ? expf(gi - gam[j + 1]) * pacc[nt][2 * e2 + 1] : 0.f;
+        split_bf16(p0, h0v, l0v);
+        split_bf16(p1, h1v, l1v);
+        st_bf16x2(PH + swz<64>(i, j), h0v, h1v);
+        st_bf16x2(PL + swz<64>(i, j), l0v, l1v);
+      }
+      const float2 u = *reinterpret_cast<const float2*>(Us + i * kSA + j);
+      split_bf16(u.x - sWH * dacc[nt][2 * e2], h0v, l0v);
+      split_bf16(u.y - sWH * dacc[nt][2 * e2 + 1], h1v, l1v);
+      st_bf16x2(DH + swz<64>(i, j), h0v, h1v);
+      st_bf16x2(DL + swz<64>(i, j), l0v, l1v);
+    }
+  __syncthreads();  // P, Delta ready; U reads done (its tile becomes the O staging)
+
+  {
+    float o2[4][4];
+    zero_acc(o2);
+    const int kend = row0 + 16;  // P is lower triangular: columns j <= i only
+    wgemm<4, false, true, 64, 64>(o2, PH, row0, DH, col0, 0, kend, lane);
+    wgemm<4, false, true, 64, 64>(o2, PH, row0, DL, col0, 0, kend, lane);
+    wgemm<4, false, true, 64, 64>(o2, PL, row0, DH, col0, 0, kend, lane);
+    const float sq = (SM != GDN_QDQ_NONE) ? sH : 1.f;
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
+        const float ei = eg[i] * sq;
+        *reinterpret_cast<float2*>(Ost + i * kSA + j) =
+            make_float2(p.scale * (ei * qacc[nt][2 * e2] + o2[nt][2 * e2]),
+                        p.scale * (ei * qacc[nt][2 * e2 + 1] + o2[nt][2 * e2 + 1]));
+      }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < L * 16; i += kOutThreads) {
+    const int r = i >> 4, c4 = i & 15;
+    *reinterpret_cast<float4*>(p.o + ((tok0 + r) * p.Hv + h) * p.Dv + vb * 64 + c4 * 4) =
+        *reinterpret_cast<const float4*>(Ost + r * kSA + c4 * 4);
+  }
+}
+
+// ===========================================================================
+// launch
+// ===========================================================================
+template <typename Kern>
+gdn_status set_smem(Kern kern, int bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) ==
+                 cudaSuccess
+             ? GDN_OK
+             : GDN_ERR_CUDA;
+}
+
 template <int DK, int SM, int WM>
 gdn_status launch_t(const FwdParams& prm, const Dims& d, cudaStream_t st) {
-  using S = Smem<DK, SM, WM>;
-  auto kern = gdn_fwd_kernel<DK, SM, WM>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::BYTES) !=
-      cudaSuccess)
-    return GDN_ERR_CUDA;
-  dim3 grid((unsigned)(d.Dv / 64), (unsigned)d.Hv, (unsigned)d.N);
-  kern<<<grid, kThreads, S::BYTES, st>>>(prm);
-  return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  const int nvb = d.Dv / 64;
+  if (d.B * d.T > 0 && d.n_slots > 0) {
+    auto k1 = gdn_fwd_prep_kernel<DK, WM>;
+    if (set_smem(k1, PrepSmem<DK>::BYTES) != GDN_OK) return GDN_ERR_CUDA;
+    k1<<<(unsigned)(d.n_slots * d.Hv), kPrepThreads, PrepSmem<DK>::BYTES, st>>>(prm);
+    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+  }
+  auto k2 = gdn_fwd_state_kernel<DK, SM, WM>;
+  if (set_smem(k2, StateSmem<DK, SM, WM>::BYTES) != GDN_OK) return GDN_ERR_CUDA;
+  k2<<<dim3((unsigned)nvb, (unsigned)d.Hv, (unsigned)d.N), kStateThreads,
+       StateSmem<DK, SM, WM>::BYTES, st>>>(prm);
+  if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+  if (d.B * d.T > 0 && d.n_slots > 0) {
+    auto k3 = gdn_fwd_output_kernel<DK, SM, WM>;
+    if (set_smem(k3, OutSmem<DK, SM, WM>::BYTES) != GDN_OK) return GDN_ERR_CUDA;
+    k3<<<(unsigned)(d.n_slots * d.Hv * nvb), kOutThreads, OutSmem<DK, SM, WM>::BYTES, st>>>(prm);
+    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+  }
+  return GDN_OK;
 }
 
 template <int DK>
@@ -596,6 +922,8 @@ gdn_status dispatch_modes(const gdn_problem& p, const FwdParams& prm, const Dims
 gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const void* k,
                       const void* v, const float* beta, const float* g, const float* h0,
                       float* o, float* ht, void* ctx, cudaStream_t st) {
+  // 32-bit grid limits of the two per-chunk launches
+  if (d.n_slots * d.Hv * (d.Dv / 64) > 0x7fffffffLL) return GDN_ERR_UNSUPPORTED_SHAPE;
   FwdParams prm{};
   prm.q = static_cast<const __nv_bfloat16*>(q);
   prm.k = static_cast<const __nv_bfloat16*>(k);
@@ -605,19 +933,19 @@ gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const 
   prm.h0 = h0;
   prm.o = o;
   prm.ht = ht;
-  if (ctx) {
-    const CtxLayout L = ctx_layout(p);
-    unsigned char* base = static_cast<unsigned char*>(ctx);
-    if (p.w_mode != GDN_QDQ_NONE) {
-      prm.w_codes = base + L.w_codes;
-      prm.w_scales = reinterpret_cast<float*>(base + L.w_scales);
-    }
-    if (p.state_mode != GDN_QDQ_NONE) {
-      prm.h_codes = base + L.h_codes;
-      prm.h_scales = reinterpret_cast<float*>(base + L.h_scales);
-    } else {
-      prm.h_full = reinterpret_cast<float*>(base + L.h_full);
-    }
+  const CtxLayout L = ctx_layout(p);
+  unsigned char* base = static_cast<unsigned char*>(ctx);
+  if (p.w_mode != GDN_QDQ_NONE) {
+    prm.w_codes = base + L.w_codes;
+    prm.w_scales = reinterpret_cast<float*>(base + L.w_scales);
+  } else {
+    prm.w_full = reinterpret_cast<float*>(base + L.w_full);
+  }
+  if (p.state_mode != GDN_QDQ_NONE) {
+    prm.h_codes = base + L.h_codes;
+    prm.h_scales = reinterpret_cast<float*>(base + L.h_scales);
+  } else {
+    prm.h_full = reinterpret_cast<float*>(base + L.h_full);
   }
   prm.cu_seqlens = p.cu_seqlens;
   prm.T = d.T;
@@ -625,6 +953,7 @@ gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const 
   prm.Hv = d.Hv;
   prm.Dv = d.Dv;
   prm.G = d.Hv / d.Hk;
+  prm.N = (int)d.N;
   prm.nt_fixed = d.nt_fixed;
   prm.scale = p.scale;
   if (d.Dk == 128) return dispatch_modes<128>(p, prm, d, st);

@@ -102,11 +102,13 @@ gdn_status gdn_validate(const gdn_problem* p);
 int64_t gdn_num_chunk_slots(const gdn_problem* p);
 
 /*
- * Bytes of the saved-for-backward context written by the forward when its
- * `ctx` argument is non-NULL, or 0 if p is invalid.  Layout (each segment
- * starts on a 256-byte boundary, in this order):
+ * Bytes of the forward's context (the quantized W and chunk states it
+ * writes, read back by its own output pass and by the backward), or 0 if p
+ * is invalid.  Layout (each segment starts on a 256-byte boundary, in this
+ * order):
  *   w_codes   u8  [B, T, Hv, Dk]        quantized W codes    (w_mode != NONE)
  *   w_scales  f32 [n_slots, Hv]         W scale per chunk    (w_mode != NONE)
+ *   w_full    f32 [B, T, Hv, Dk]        unquantized W        (w_mode == NONE)
  *   h_codes   u8  [n_slots, Hv, Dk, Dv] state codes entering each chunk (state_mode != NONE)
  *   h_scales  f32 [n_slots, Hv, Dv/64]  state scale per [Dk, 64] tile  (state_mode != NONE)
  *   h_full    f32 [n_slots, Hv, Dk, Dv] unquantized state entering each chunk (state_mode == NONE)
@@ -123,7 +125,8 @@ size_t gdn_ctx_bytes(const gdn_problem* p);
  *   h0    f32  [N, Hv, Dk, Dv] initial state H = S^T, or NULL for zeros
  *   o     f32  [B, T, Hv, Dv]      (written)
  *   ht    f32  [N, Hv, Dk, Dv] final state, unquantized, or NULL (written)
- *   ctx   gdn_ctx_bytes(p) bytes, 256-byte aligned, or NULL (written)
+ *   ctx   gdn_ctx_bytes(p) bytes, 256-byte aligned (written; required when
+ *         B * T > 0: the output pass reads the saved W and chunk states)
  * Per chunk (method of the first page; the pages print no equations, this is
  * the published WY form of the gated delta rule): gamma = in-chunk cumsum of
  * g; A = strictly-lower(beta_i exp(gamma_i - gamma_j) k_i.k_j); T = (I+A)^-1;
@@ -131,6 +134,9 @@ size_t gdn_ctx_bytes(const gdn_problem* p);
  * diag(beta) V; H^ = Q_S(H) per [Dk, 64] tile (h0 included); Delta = U - W^ H^;
  * o = scale (diag(exp(gamma)) Q H^ + (lower-incl(exp(gamma_i-gamma_j) q_i.k_j)) Delta);
  * H <- exp(gamma_L) H^ + (diag(exp(gamma_L - gamma)) K)^T Delta.
+ * Three launches: the chunk-local part (A, T, W with its QDQ, U) for all
+ * chunks at once, the serial state scan, then the outputs for all chunks at
+ * once; U is kept in `o` between the first and the last launch.
  * A sequence of length 0 returns ht = h0 (not quantized).
  * All pointers must be 16-byte aligned (GDN_ERR_MISALIGNED otherwise).
  */

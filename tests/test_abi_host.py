@@ -80,7 +80,7 @@ def test_sizes():
     exp = al(2 * 300 * 4 * 128) + al(4 * ns * 4) + al(ns * 4 * 128 * 128) + al(4 * ns * 4 * 2)
     assert lib.gdn_ctx_bytes(ctypes.byref(p)) == exp
     p0 = _problem(state_mode=0, w_mode=0)
-    assert lib.gdn_ctx_bytes(ctypes.byref(p0)) == al(4 * ns * 4 * 128 * 128)
+    assert lib.gdn_ctx_bytes(ctypes.byref(p0)) == al(4 * 2 * 300 * 4 * 128) + al(4 * ns * 4 * 128 * 128)
     pk = _problem(B=1, T=1000, N=7, cu_seqlens=4096)
     assert lib.gdn_num_chunk_slots(ctypes.byref(pk)) == 1000 // 64 + 7
     assert lib.gdn_ctx_bytes(ctypes.byref(_problem(Dk=96))) == 0
@@ -114,9 +114,11 @@ def test_entry_points_reject_before_launch():
     # misaligned pointer
     assert lib.gdn_chunk_fwd_qdq(ctypes.byref(ok), P(4097), fake, fake, fake, fake, None, fake,
                                  None, None, None) == -7
-    # ctx must be 256-byte aligned
+    # ctx must be 256-byte aligned, and is required
     assert lib.gdn_chunk_fwd_qdq(ctypes.byref(ok), fake, fake, fake, fake, fake, None, fake,
                                  None, P(4096 + 16), None) == -7
+    assert lib.gdn_chunk_fwd_qdq(ctypes.byref(ok), fake, fake, fake, fake, fake, None, fake,
+                                 None, None, None) == -1
     # backward: workspace too small
     need = lib.gdn_bwd_workspace_bytes(ctypes.byref(ok))
     if need > 0:
