@@ -55,6 +55,7 @@ _DP = ctypes.POINTER(GdnDecodeProblem)
 SIGNATURES = {
     "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_abi_version": (ctypes.c_int, []),
+    "gdn_device_error": (ctypes.c_int, [ctypes.c_int]),
     "gdn_validate": (ctypes.c_int, [_PP]),
     "gdn_num_chunk_slots": (ctypes.c_int64, [_PP]),
     "gdn_ctx_bytes": (_SZ, [_PP]),

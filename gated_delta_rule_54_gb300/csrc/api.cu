@@ -107,6 +107,8 @@ const char* gdn_status_string(int s) {
 
 int gdn_abi_version(void) { return GDN_QDQ_ABI_VERSION; }
 
+int gdn_device_error(int reset) { return fwd_device_error(reset != 0); }
+
 gdn_status gdn_validate(const gdn_problem* p) { return validate(p); }
 
 int64_t gdn_num_chunk_slots(const gdn_problem* p) {

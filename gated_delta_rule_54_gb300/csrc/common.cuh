@@ -130,14 +130,26 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 }
 
 // ---------------------------------------------------------------------------
-// bf16 tiles in shared memory: rows of RL elements (RL*2 bytes = 8 or 16
-// chunks of 16 bytes); chunk ch of row r is stored at chunk ch ^ (r & 7) so
-// that ldmatrix of 8 rows touches 8 distinct bank groups.
+// bf16 tiles in shared memory.  A tile of 64-element (128-byte) rows keeps
+// 16-byte chunk ch of row r at chunk ch ^ (r & 7), so that ldmatrix of 8 rows
+// touches 8 distinct bank groups; this is also the layout a TMA copy with
+// 128-byte swizzling writes into a 1024-byte aligned tile.  128-element rows
+// are stored as two such 64-column panels of 64 rows each (every 128-wide
+// tile here has 64 rows), one TMA box per panel.
 // ---------------------------------------------------------------------------
 template <int RL>
 __device__ __forceinline__ int swz(int row, int col) {
+  static_assert(RL == 64 || RL == 128, "row length");
   // element offset of (row, col)
-  return row * RL + ((((col >> 3) ^ (row & 7))) << 3) + (col & 7);
+  const int in_panel = row * 64 + (((((col >> 3) & 7) ^ (row & 7))) << 3) + (col & 7);
+  if constexpr (RL == 64) return in_panel;
+  return (col >> 6) * (64 * 64) + in_panel;
+}
+
+// fp32 tile of 64 rows x 64 columns as two 32-column panels (128-byte rows,
+// 16-byte chunks swizzled like swz): element offset of (row, col).
+__device__ __forceinline__ int swz_f32(int row, int col) {
+  return (col >> 5) * (64 * 32) + row * 32 + (((((col >> 2) & 7) ^ (row & 7))) << 2) + (col & 3);
 }
 
 // ldmatrix.x4 address of a 16x16 A fragment at (r0, c0) of a row-major tile.
@@ -208,6 +220,74 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// ---------------------------------------------------------------------------
+// Tensor memory access (TMA) and mbarriers.  One thread issues a copy of a
+// whole box; the copy signals the box's bytes on an mbarrier that every
+// consumer waits on.  Waits are bounded: after kMbarPolls polls a wait gives
+// up and reports it, so a lost transfer ends the kernel with an error status
+// instead of hanging the GPU.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kMbarPolls = 1u << 22;
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count));
+}
+// makes mbarrier initialisation visible to the asynchronous (TMA) proxy
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+// true once the phase with this parity has completed; false after kMbarPolls polls
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  const uint32_t a = smem_u32(bar);
+  for (uint32_t i = 0; i < kMbarPolls; ++i) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(a), "r"(parity)
+        : "memory");
+    if (done) return true;
+  }
+  return false;
+}
+// 2-D tiled load of one box at (x = inner element, y = row) into shared memory
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(smem_u32(dst)),
+      "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+// 2-D tiled store of one box from shared memory (bulk async-group completion)
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int x, int y, const void* src) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];\n" ::"l"(
+                   tmap),
+               "r"(x), "r"(y), "r"(smem_u32(src))
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_commit() {
+  asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
+}
+// the committed stores have finished reading shared memory
+__device__ __forceinline__ void tma_store_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;\n" ::: "memory");
+}
+// the committed stores are complete
+__device__ __forceinline__ void tma_store_wait_all() {
+  asm volatile("cp.async.bulk.wait_group 0;\n" ::: "memory");
+}
+// orders this thread's shared-memory writes before later TMA reads of them
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
 
 }  // namespace gdn

@@ -32,6 +32,11 @@
 // quantization codes than the fp32 arithmetic of the definition would.
 // Quantized W and H enter the tensor cores as their codes (E4M3 values and
 // INT8 integers are exact in bf16) with the fp32 scales applied in epilogues.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -39,7 +44,13 @@ namespace gdn {
 
 namespace {
 
+// set by a kernel whose bounded wait for a TMA transfer gave up
+__device__ int g_fwd_device_error;
+
 struct FwdParams {
+  // TMA descriptors (2-D): k [B*T, Hk*Dk] bf16, o/U [B*T, Hv*Dv] f32,
+  // W codes [B*T, Hv*Dk] u8, state codes [n_slots*Hv*Dk, Dv] u8
+  CUtensorMap tm_k, tm_u, tm_wc, tm_hc;
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
@@ -354,37 +365,45 @@ constexpr int kStateWarps = kStateThreads / 32;
 template <int DK, int SM, int WM>
 struct StateSmem {
   static constexpr int WRAW = (WM == GDN_QDQ_NONE) ? kChunk * DK * 4 : kChunk * DK;
-  static constexpr int K = 0;                                          // 2 x bf16 [64][DK]
-  static constexpr int WR = K + 2 * kChunk * DK * 2;                   // 2 x W codes / f32
-  static constexpr int U = WR + 2 * WRAW;                              // 2 x f32 [64][kSA]
-  static constexpr int G = U + 2 * kF32Tile;                           // 2 x g[64]
+  static constexpr int K = 0;                                          // 2 x bf16 [64][DK] (TMA)
+  static constexpr int U = K + 2 * kChunk * DK * 2;                    // 2 x f32 [64][64] (TMA, swz_f32)
+  static constexpr int WR = U + 2 * kChunk * 64 * 4;                   // 2 x W codes (TMA) / f32
+  static constexpr int G = WR + 2 * WRAW;                              // 2 x g[64]
   static constexpr int VEC = G + 512;                                  // decay[64], e^{gL}
   static constexpr int WC = VEC + 512;                                 // W^ bf16 [64][DK] (hi, lo)
   static constexpr int HC = WC + (WM == GDN_QDQ_NONE ? 2 : 1) * kChunk * DK * 2;  // H^ [DK][64]
   static constexpr int DP = HC + (SM == GDN_QDQ_NONE ? 2 : 1) * DK * 64 * 2;      // Delta' hi, lo
-  static constexpr int HST = DP + 2 * kChunk * 64 * 2;                 // u8 [DK][64] codes
-  static constexpr int BYTES = HST + DK * 64;
+  static constexpr int HST = DP + 2 * kChunk * 64 * 2;                 // u8 [DK][64] codes (TMA store)
+  static constexpr int BYTES = HST + DK * 64 + 1024;                   // + alignment slack
   static_assert(BYTES <= 232448, "shared memory budget");
-  static_assert((WR % 128) == 0 && (U % 128) == 0 && (WC % 128) == 0 && (HC % 128) == 0 &&
-                    (DP % 128) == 0 && (HST % 16) == 0,
+  static_assert((U % 1024) == 0 && (WR % 1024) == 0 && (WC % 128) == 0 && (HC % 128) == 0 &&
+                    (DP % 128) == 0 && (HST % 128) == 0,
                 "alignment");
 };
 
+// TMA boxes of one chunk: K (two 64-column panels), U (two 32-column fp32
+// panels) and, for quantized W, its codes; g (and an fp32 W) by cp.async.
 template <int DK, int WM>
-__device__ __forceinline__ void load_state_chunk(const FwdParams& p, __nv_bfloat16* Ks, unsigned char* Wr, float* Us,
-                                                 float* Gs, int64_t tok0, int L, int hk, int h,
-                                                 int vb) {
-  load_rows_bf16<DK, kStateThreads>(Ks, p.k, tok0, L, p.Hk, hk);
-  if constexpr (WM != GDN_QDQ_NONE) {
-    constexpr int CPR = DK / 16;
-    for (int i = threadIdx.x; i < kChunk * CPR; i += kStateThreads) {
-      const int r = i / CPR, c = i % CPR;
-      const bool ok = r < L;
-      const int64_t tok = tok0 + (ok ? r : 0);
-      cp_async16(smem_u32(Wr + r * DK + c * 16), p.w_codes + (tok * p.Hv + h) * DK + c * 16,
-                 ok ? 16 : 0);
-    }
-  } else {
+__device__ __forceinline__ uint32_t state_chunk_tx_bytes() {
+  return kChunk * DK * 2 + kChunk * 64 * 4 + (WM != GDN_QDQ_NONE ? kChunk * DK : 0);
+}
+
+template <int DK, int WM>
+__device__ __forceinline__ void issue_state_chunk(const FwdParams& p, __nv_bfloat16* Ks,
+                                                  unsigned char* Wr, float* Us, float* Gs,
+                                                  uint64_t* bar, int64_t tok0, int L, int hk,
+                                                  int h, int vb) {
+  if (threadIdx.x == 0) {
+    mbar_expect_tx(bar, state_chunk_tx_bytes<DK, WM>());
+#pragma unroll
+    for (int pn = 0; pn < DK / 64; ++pn)
+      tma_load_2d(Ks + pn * kChunk * 64, &p.tm_k, hk * DK + pn * 64, (int)tok0, bar);
+#pragma unroll
+    for (int pn = 0; pn < 2; ++pn)
+      tma_load_2d(Us + pn * kChunk * 32, &p.tm_u, h * p.Dv + vb * 64 + pn * 32, (int)tok0, bar);
+    if constexpr (WM != GDN_QDQ_NONE) tma_load_2d(Wr, &p.tm_wc, h * DK, (int)tok0, bar);
+  }
+  if constexpr (WM == GDN_QDQ_NONE) {
     constexpr int CPR = DK / 4;
     for (int i = threadIdx.x; i < kChunk * CPR; i += kStateThreads) {
       const int r = i / CPR, c = i % CPR;
@@ -394,21 +413,17 @@ __device__ __forceinline__ void load_state_chunk(const FwdParams& p, __nv_bfloat
                  ok ? 16 : 0);
     }
   }
-  for (int i = threadIdx.x; i < kChunk * 16; i += kStateThreads) {
-    const int r = i >> 4, c = i & 15;
-    const bool ok = r < L;
-    const int64_t tok = tok0 + (ok ? r : 0);
-    cp_async16(smem_u32(Us + r * kSA + c * 4), p.o + (tok * p.Hv + h) * p.Dv + vb * 64 + c * 4,
-               ok ? 16 : 0);
-  }
   if (threadIdx.x < kChunk) load_vec64(Gs, p.g, tok0, L, p.Hv, h, threadIdx.x);
+  cp_async_commit();
 }
 
 template <int DK, int SM, int WM>
-__global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const __grid_constant__ FwdParams p) {
   using S = StateSmem<DK, SM, WM>;
-  extern __shared__ __align__(1024) unsigned char sm[];
+  extern __shared__ __align__(1024) unsigned char sm_raw[];
+  unsigned char* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
   __shared__ float red[kStateWarps];
+  __shared__ __align__(8) uint64_t bars[2];
 
   const int vb = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
   const int hk = h / p.G;
@@ -439,7 +454,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const F
   uint8_t* Hst = sm + S::HST;
   auto Kbuf = [&](int b) { return reinterpret_cast<__nv_bfloat16*>(sm + S::K + b * kChunk * DK * 2); };
   auto Wbuf = [&](int b) { return sm + S::WR + b * S::WRAW; };
-  auto Ubuf = [&](int b) { return reinterpret_cast<float*>(sm + S::U + b * kF32Tile); };
+  auto Ubuf = [&](int b) { return reinterpret_cast<float*>(sm + S::U + b * kChunk * 64 * 4); };
   auto Gbuf = [&](int b) { return reinterpret_cast<float*>(sm + S::G + b * 256); };
 
   // Delta tile: [64 x 64] -> 16 x 16 per warp; state tile [DK x 64]
@@ -467,21 +482,37 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const F
     m = warp_max(m);
     if (lane == 0) red[warp] = m;
   }
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
 
   float sW_next = 1.f;
   if (nchunks > 0) {
-    load_state_chunk<DK, WM>(p, Kbuf(0), Wbuf(0), Ubuf(0), Gbuf(0), tok0, min(L, kChunk), hk,
-                             h, vb);
+    issue_state_chunk<DK, WM>(p, Kbuf(0), Wbuf(0), Ubuf(0), Gbuf(0), &bars[0], tok0,
+                              min(L, kChunk), hk, h, vb);
     if constexpr (WM != GDN_QDQ_NONE) sW_next = p.w_scales[slot0 * p.Hv + h];
   }
-  cp_async_commit();
 
   for (int c = 0; c < nchunks; ++c) {
     const int buf = c & 1;
+    const int Lc = min(L - c * kChunk, kChunk);
     const int64_t slot = slot0 + c;
     const float sW = sW_next;
+    const bool ok = mbar_wait(&bars[buf], (uint32_t)(c >> 1) & 1u);
     cp_async_wait<0>();
-    __syncthreads();  // chunk c landed; amax partials of H visible; buffer buf^1 free
+    if (threadIdx.x == 0) tma_store_wait_read();  // the codes store of chunk c - 1 has read Hst
+    // chunk c landed; amax partials of H visible; buffer buf ^ 1 free
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) {
+        atomicOr(&g_fwd_device_error, 1);
+        mbar_wait(&bars[buf], (uint32_t)(c >> 1) & 1u);  // once more, bounded, for the copies in flight
+        tma_store_wait_all();
+      }
+      return;
+    }
 
     if (warp == 0) {
       float gam0, gam1, gL;
@@ -491,15 +522,16 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const F
       if (lane == 0) dec[64] = expf(gL);
     }
 
-    // W^ operand: codes -> bf16 values (exact), or the fp32 W split hi/lo
+    // W^ operand: codes -> bf16 values (exact), or the fp32 W split hi/lo; rows >= Lc are zero
     if constexpr (WM != GDN_QDQ_NONE) {
       const uint8_t* Wr = Wbuf(buf);
       constexpr int C4 = DK / 4;
       for (int i = threadIdx.x; i < kChunk * C4; i += kStateThreads) {
         const int r = i / C4, c4 = i % C4;
-        const float4 v = qdq_code4_values<WM>(*reinterpret_cast<const uint32_t*>(Wr + r * DK + c4 * 4));
-        const int e = swz<DK>(r, c4 * 4);
-        *reinterpret_cast<uint2*>(WcH + e) = make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < Lc) v = qdq_code4_values<WM>(*reinterpret_cast<const uint32_t*>(Wr + r * DK + c4 * 4));
+        *reinterpret_cast<uint2*>(WcH + swz<DK>(r, c4 * 4)) =
+            make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
       }
     } else {
       const float* Wr = reinterpret_cast<const float*>(Wbuf(buf));
@@ -550,6 +582,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const F
             *reinterpret_cast<uint16_t*>(Hst + d * 64 + col) = (uint16_t)(c0 | (c1 << 8));
           }
         if (amax == 0.f) sH = 0.f;
+        fence_proxy_async();  // Hst is read by the TMA store below
       } else {
 #pragma unroll
         for (int nt = 0; nt < NTH; ++nt)
@@ -568,25 +601,22 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const F
     }
     __syncthreads();  // W^, H^ operands, decay factors ready
 
+    if (threadIdx.x == 0) {
+      if constexpr (SM != GDN_QDQ_NONE) {
+        tma_store_2d(&p.tm_hc, vb * 64, (int)((slot * p.Hv + h) * DK), Hst);
+        tma_store_commit();
+        p.h_scales[(slot * p.Hv + h) * (p.Dv / 64) + vb] = sH;
+      }
+    }
     // prefetch chunk c + 1 (buffer buf ^ 1 was last read before this iteration's first barrier)
     if (c + 1 < nchunks) {
-      load_state_chunk<DK, WM>(p, Kbuf(buf ^ 1), Wbuf(buf ^ 1), Ubuf(buf ^ 1), Gbuf(buf ^ 1),
-                               tok0 + (int64_t)(c + 1) * kChunk,
-                               min(L - (c + 1) * kChunk, kChunk), hk, h, vb);
+      issue_state_chunk<DK, WM>(p, Kbuf(buf ^ 1), Wbuf(buf ^ 1), Ubuf(buf ^ 1), Gbuf(buf ^ 1),
+                                &bars[buf ^ 1], tok0 + (int64_t)(c + 1) * kChunk,
+                                min(L - (c + 1) * kChunk, kChunk), hk, h, vb);
       if constexpr (WM != GDN_QDQ_NONE) sW_next = p.w_scales[(slot + 1) * p.Hv + h];
     }
-    cp_async_commit();
 
-    if constexpr (SM != GDN_QDQ_NONE) {
-      for (int i = threadIdx.x; i < DK * 4; i += kStateThreads) {
-        const int d = i >> 2, c16 = i & 3;
-        *reinterpret_cast<uint4*>(p.h_codes + ((slot * p.Hv + h) * DK + d) * p.Dv + vb * 64 +
-                                  c16 * 16) = *reinterpret_cast<const uint4*>(Hst + d * 64 + c16 * 16);
-      }
-      if (threadIdx.x == 0) p.h_scales[(slot * p.Hv + h) * (p.Dv / 64) + vb] = sH;
-    }
-
-    // ---- a7: Delta = U - W^ H^;  Delta' = diag(e^{gamma_L - gamma}) Delta ----
+    // ---- a7: Delta = U - W^ H^;  Delta' = diag(e^{gamma_L - gamma}) Delta (rows >= Lc zero) ----
     {
       float dacc[2][4];
       zero_acc(dacc);
@@ -600,7 +630,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const F
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-          const float2 u = *reinterpret_cast<const float2*>(Us + i * kSA + j);
+          float2 u = *reinterpret_cast<const float2*>(Us + swz_f32(i, j));
+          if (i >= Lc) u = make_float2(0.f, 0.f);
           const float di = dec[i];
           float h0v, l0v, h1v, l1v;
           split_bf16((u.x - sWH * dacc[nt][2 * e2]) * di, h0v, l0v);
@@ -611,7 +642,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const F
     }
     __syncthreads();  // Delta' ready
 
-    // ---- a9: H <- e^{gamma_L} H^ + K^T Delta' ----
+    // ---- a9: H <- e^{gamma_L} H^ + K^T Delta' (K rows >= Lc meet zero rows of Delta') ----
     {
       const float egL = dec[64];
       float m = 0.f;
@@ -631,6 +662,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const F
     }
   }
   cp_async_wait<0>();
+  if (threadIdx.x == 0) tma_store_wait_all();
 
   if (p.ht) {
     float* dst = p.ht + (((int64_t)n * p.Hv + h) * DK) * p.Dv + vb * 64;
@@ -917,7 +949,47 @@ gdn_status dispatch_modes(const gdn_problem& p, const FwdParams& prm, const Dims
   return GDN_ERR_UNSUPPORTED_MODE;
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2-D row-major map: `cols` elements per row (contiguous), `rows` rows of
+// `row_bytes` bytes; boxes of box_cols x box_rows elements.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols,
+              uint64_t rows, uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows,
+              CUtensorMapSwizzle sw) {
+  const PFN_cuTensorMapEncodeTiled_v12000 fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_cols, box_rows};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
+
+int fwd_device_error(bool reset) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fwd_device_error, sizeof(int)) != cudaSuccess) return -1;
+  if (reset && v) {
+    const int z = 0;
+    if (cudaMemcpyToSymbol(g_fwd_device_error, &z, sizeof(int)) != cudaSuccess) return -1;
+  }
+  return v;
+}
 
 gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const void* k,
                       const void* v, const float* beta, const float* g, const float* h0,
@@ -956,6 +1028,24 @@ gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const 
   prm.N = (int)d.N;
   prm.nt_fixed = d.nt_fixed;
   prm.scale = p.scale;
+  const uint64_t tok = (uint64_t)(d.B * d.T);
+  if (tok > 0) {
+    // 32-bit TMA coordinates: state-code rows of all slots must fit
+    if ((uint64_t)d.n_slots * d.Hv * d.Dk > 0x7fffffffULL) return GDN_ERR_UNSUPPORTED_SHAPE;
+    const int DK = d.Dk;
+    bool ok = make_map(&prm.tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k, (uint64_t)d.Hk * DK, tok,
+                       (uint64_t)d.Hk * DK * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              make_map(&prm.tm_u, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, o, (uint64_t)d.Hv * d.Dv, tok,
+                       (uint64_t)d.Hv * d.Dv * 4, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (ok && p.w_mode != GDN_QDQ_NONE)
+      ok = make_map(&prm.tm_wc, CU_TENSOR_MAP_DATA_TYPE_UINT8, prm.w_codes, (uint64_t)d.Hv * DK,
+                    tok, (uint64_t)d.Hv * DK, DK, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (ok && p.state_mode != GDN_QDQ_NONE)
+      ok = make_map(&prm.tm_hc, CU_TENSOR_MAP_DATA_TYPE_UINT8, prm.h_codes, (uint64_t)d.Dv,
+                    (uint64_t)d.n_slots * d.Hv * DK, (uint64_t)d.Dv, 64, DK,
+                    CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!ok) return GDN_ERR_CUDA;
+  }
   if (d.Dk == 128) return dispatch_modes<128>(p, prm, d, st);
   return dispatch_modes<64>(p, prm, d, st);
 }

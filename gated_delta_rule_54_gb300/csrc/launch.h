@@ -33,6 +33,10 @@ gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const 
                       const void* v, const float* beta, const float* g, const float* h0,
                       float* o, float* ht, void* ctx, cudaStream_t st);
 
+// nonzero if a forward kernel's bounded wait for a TMA transfer gave up
+// (cleared when reset); -1 if the flag could not be read
+int fwd_device_error(bool reset);
+
 size_t bwd_workspace_bytes(const gdn_problem& p, const Dims& d);
 
 gdn_status launch_bwd(const gdn_problem& p, const Dims& d, const void* q, const void* k,

@@ -89,6 +89,16 @@ typedef struct {
   int32_t dtype;              /* gdn_dtype of q, k, v (and dO); must be BF16    */
 } gdn_problem;
 
+/*
+ * Device-side error flag.  Kernels that wait for their own asynchronous
+ * copies (TMA transfers signalled on mbarriers) bound every wait; a wait that
+ * gives up ends the kernel early and sets this flag, so the outputs of the
+ * call that set it are invalid.  Returns the flag (nonzero = a wait gave up)
+ * and clears it when `reset` is nonzero; -1 if it cannot be read.  Unlike
+ * every other entry point this call synchronizes with the current device.
+ */
+int gdn_device_error(int reset);
+
 /* Human-readable name of a status code (static string). */
 const char* gdn_status_string(int status);
 

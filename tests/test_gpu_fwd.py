@@ -190,3 +190,9 @@ def test_full_packed_varlen_sampled():
     lens = synth.varlen_lengths(32768)
     picks = [(0, 0), (len(lens) - 1, 31), (int(np.argmax(lens)), 5), (int(np.argmin(lens)), 17)]
     _sample_check("varlen", picks)
+
+
+def test_no_bounded_wait_gave_up():
+    """No forward kernel of the runs above ended early on a TMA wait."""
+    from gated_delta_rule_54_gb300 import _lib
+    assert _lib.load().gdn_device_error(1) == 0
