@@ -48,9 +48,9 @@ namespace {
 __device__ int g_fwd_device_error;
 
 struct FwdParams {
-  // TMA descriptors (2-D): k [B*T, Hk*Dk] bf16, o/U [B*T, Hv*Dv] f32,
+  // TMA descriptors (2-D): k, q [B*T, Hk*Dk] bf16, v [B*T, Hv*Dv] bf16, o/U [B*T, Hv*Dv] f32,
   // W codes [B*T, Hv*Dk] u8, state codes [n_slots*Hv*Dk, Dv] u8
-  CUtensorMap tm_k, tm_u, tm_wc, tm_hc;
+  CUtensorMap tm_k, tm_q, tm_v, tm_u, tm_wc, tm_hc;
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
@@ -149,24 +149,27 @@ constexpr int kPrepWarps = kPrepThreads / 32;
 
 template <int DK>
 struct PrepSmem {
-  static constexpr int K = 0;                            // bf16 [64][DK]
-  static constexpr int V = K + kChunk * DK * 2;          // bf16 Dv/64 x [64][64]
-  static constexpr int BG = V + 2 * kChunk * 64 * 2;     // beta[64], g[64]
-  static constexpr int VEC = BG + 512;                   // gamma, e^gamma, beta e^gamma, beta
-  static constexpr int A = VEC + 4 * 64 * 4;             // f32 [64][kSA]; later U staging
+  static constexpr int K = 0;                            // bf16 [64][DK] (TMA)
+  static constexpr int V = K + kChunk * DK * 2;          // bf16 Dv/64 x [64][64] (TMA)
+  static constexpr int A = V + 2 * kChunk * 64 * 2;      // f32 [64][kSA]; later U staging (swz_f32)
   static constexpr int TT = A + kF32Tile;                // f32 [64][kSA]
   static constexpr int TW = TT + kF32Tile;               // Tw hi, lo
   static constexpr int TU = TW + 2 * kChunk * 64 * 2;    // Tu hi, lo
   static constexpr int WST = TU + 2 * kChunk * 64 * 2;   // u8 [64][DK] W codes
-  static constexpr int BYTES = WST + kChunk * DK;
-  static_assert((A % 128) == 0 && (TW % 128) == 0 && (WST % 16) == 0, "alignment");
+  static constexpr int BG = WST + kChunk * DK;           // beta[64], g[64]
+  static constexpr int VEC = BG + 512;                   // gamma, e^gamma, beta e^gamma, beta
+  static constexpr int BYTES = VEC + 4 * 64 * 4 + 1024;  // + alignment slack
+  static_assert((V % 1024) == 0 && (A % 1024) == 0 && (TW % 128) == 0 && (WST % 128) == 0,
+                "alignment");
 };
 
 template <int DK, int WM>
-__global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __grid_constant__ FwdParams p) {
   using S = PrepSmem<DK>;
-  extern __shared__ __align__(1024) unsigned char sm[];
+  extern __shared__ __align__(1024) unsigned char sm_raw[];
+  unsigned char* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
   __shared__ float red[kPrepWarps];
+  __shared__ __align__(8) uint64_t bar;
 
   const int64_t slot = blockIdx.x / p.Hv;
   const int h = blockIdx.x % p.Hv;
@@ -195,13 +198,17 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const Fwd
   uint8_t* Wst = sm + S::WST;
   float* Ust = As;
 
-  load_rows_bf16<DK, kPrepThreads>(Ks, p.k, tok0, L, p.Hk, hk);
-  for (int i = threadIdx.x; i < kChunk * nvb * 8; i += kPrepThreads) {
-    const int r = i / (nvb * 8), rem = i % (nvb * 8), vb = rem >> 3, c = rem & 7;
-    const bool ok = r < L;
-    const int64_t tok = tok0 + (ok ? r : 0);
-    cp_async16(smem_u32(Vs + vb * kChunk * 64 + swz<64>(r, c * 8)),
-               p.v + (tok * p.Hv + h) * p.Dv + vb * 64 + c * 8, ok ? 16 : 0);
+  // K and V as TMA boxes (rows >= L hold another sequence's tokens: they only
+  // meet zero beta, so they reach neither A, W nor U); beta and g zero-filled
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    mbar_expect_tx(&bar, kChunk * DK * 2 + nvb * kChunk * 64 * 2);
+#pragma unroll
+    for (int pn = 0; pn < DK / 64; ++pn)
+      tma_load_2d(Ks + pn * kChunk * 64, &p.tm_k, hk * DK + pn * 64, (int)tok0, &bar);
+    for (int vb = 0; vb < nvb; ++vb)
+      tma_load_2d(Vs + vb * kChunk * 64, &p.tm_v, h * p.Dv + vb * 64, (int)tok0, &bar);
   }
   if (threadIdx.x < 2 * kChunk) {
     const int t = threadIdx.x & 63;
@@ -209,8 +216,18 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const Fwd
                tok0, L, p.Hv, h, t);
   }
   cp_async_commit();
-  cp_async_wait<0>();
-  __syncthreads();
+  __syncthreads();  // the mbarrier is initialised before anyone waits on it
+  {
+    const bool ok = mbar_wait(&bar, 0);
+    cp_async_wait<0>();
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) {
+        atomicOr(&g_fwd_device_error, 1);
+        mbar_wait(&bar, 0);  // once more, bounded, for the copies in flight
+      }
+      return;
+    }
+  }
 
   if (warp == 0) {
     float gam0, gam1, gL;
@@ -311,12 +328,21 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const Fwd
         }
         *reinterpret_cast<uint16_t*>(Wst + i * DK + col) = (uint16_t)(c0 | (c1 << 8));
       }
-    __syncthreads();
-    constexpr int CPR = DK / 16;
-    for (int i = threadIdx.x; i < L * CPR; i += kPrepThreads) {
-      const int r = i / CPR, c16 = i % CPR;
-      *reinterpret_cast<uint4*>(p.w_codes + ((tok0 + r) * p.Hv + h) * DK + c16 * 16) =
-          *reinterpret_cast<const uint4*>(Wst + r * DK + c16 * 16);
+    if (L == kChunk) {
+      fence_proxy_async();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        tma_store_2d(&p.tm_wc, h * DK, (int)tok0, Wst);
+        tma_store_commit();
+      }
+    } else {
+      __syncthreads();
+      constexpr int CPR = DK / 16;
+      for (int i = threadIdx.x; i < L * CPR; i += kPrepThreads) {
+        const int r = i / CPR, c16 = i % CPR;
+        *reinterpret_cast<uint4*>(p.w_codes + ((tok0 + r) * p.Hv + h) * DK + c16 * 16) =
+            *reinterpret_cast<const uint4*>(Wst + r * DK + c16 * 16);
+      }
     }
     if (threadIdx.x == 0) p.w_scales[slot * p.Hv + h] = (amax == 0.f) ? 0.f : sW;
   } else {
@@ -338,22 +364,35 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const Fwd
     const __nv_bfloat16* Vb = Vs + vb * kChunk * 64;
     wgemm<4, false, true, 64, 64>(uacc, TuH, row0, Vb, col0, 0, 64, lane);
     wgemm<4, false, true, 64, 64>(uacc, TuL, row0, Vb, col0, 0, 64, lane);
+    if (vb > 0 && threadIdx.x == 0) tma_store_wait_read();  // previous block's U has left
+    __syncthreads();
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-        *reinterpret_cast<float2*>(Ust + i * kSA + j) =
+        *reinterpret_cast<float2*>(Ust + swz_f32(i, j)) =
             make_float2(uacc[nt][2 * e2], uacc[nt][2 * e2 + 1]);
       }
-    __syncthreads();
-    for (int i = threadIdx.x; i < L * 16; i += kPrepThreads) {
-      const int r = i >> 4, c4 = i & 15;
-      *reinterpret_cast<float4*>(p.o + ((tok0 + r) * p.Hv + h) * p.Dv + vb * 64 + c4 * 4) =
-          *reinterpret_cast<const float4*>(Ust + r * kSA + c4 * 4);
+    if (L == kChunk) {
+      fence_proxy_async();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+#pragma unroll
+        for (int pn = 0; pn < 2; ++pn)
+          tma_store_2d(&p.tm_u, h * p.Dv + vb * 64 + pn * 32, (int)tok0, Ust + pn * kChunk * 32);
+        tma_store_commit();
+      }
+    } else {
+      __syncthreads();
+      for (int i = threadIdx.x; i < L * 16; i += kPrepThreads) {
+        const int r = i >> 4, c4 = i & 15;
+        *reinterpret_cast<float4*>(p.o + ((tok0 + r) * p.Hv + h) * p.Dv + vb * 64 + c4 * 4) =
+            *reinterpret_cast<const float4*>(Ust + swz_f32(r, c4 * 4));
+      }
     }
-    __syncthreads();
   }
+  if (threadIdx.x == 0) tma_store_wait_all();
 }
 
 // ===========================================================================
@@ -684,26 +723,29 @@ constexpr int kOutThreads = 256;
 
 template <int DK, int SM, int WM>
 struct OutSmem {
-  static constexpr int Q = 0;                                              // bf16 [64][DK]
-  static constexpr int K = Q + kChunk * DK * 2;                            // bf16 [64][DK]; later Delta hi, lo
-  static constexpr int WC = K + kChunk * DK * 2;                           // W^ [64][DK] (hi, lo)
+  static constexpr int Q = 0;                                              // bf16 [64][DK] (TMA)
+  static constexpr int K = Q + kChunk * DK * 2;                            // bf16 [64][DK] (TMA); later Delta hi, lo
+  static constexpr int U = K + kChunk * DK * 2;                            // f32 [64][64] swz_f32 (TMA); later O
+  static constexpr int P = U + kChunk * 64 * 4;                            // P hi, lo; first W / H codes (TMA)
+  static constexpr int WC = P + 2 * kChunk * 64 * 2;                       // W^ [64][DK] (hi, lo)
   static constexpr int HC = WC + (WM == GDN_QDQ_NONE ? 2 : 1) * kChunk * DK * 2;  // H^ [DK][64] (hi, lo)
-  static constexpr int U = HC + (SM == GDN_QDQ_NONE ? 2 : 1) * DK * 64 * 2;       // f32 [64][kSA]; later O
-  static constexpr int P = U + kF32Tile;                                   // P hi, lo [64][64]
-  static constexpr int G = P + 2 * kChunk * 64 * 2;                        // g[64], gamma[64], e^gamma[64]
+  static constexpr int G = HC + (SM == GDN_QDQ_NONE ? 2 : 1) * DK * 64 * 2;       // g, gamma, e^gamma
   // Delta hi, lo [64][64]: in the dead K tile when it is large enough
   static constexpr bool D_IN_K = 2 * kChunk * 64 * 2 <= kChunk * DK * 2;
   static constexpr int D = D_IN_K ? K : G + 3 * 64 * 4;
-  static constexpr int BYTES = D_IN_K ? G + 3 * 64 * 4 : D + 2 * kChunk * 64 * 2;
-  static_assert((K % 128) == 0 && (WC % 128) == 0 && (HC % 128) == 0 && (U % 128) == 0 &&
-                    (P % 128) == 0 && (D % 128) == 0,
+  static constexpr int END = D_IN_K ? G + 3 * 64 * 4 : D + 2 * kChunk * 64 * 2;
+  static constexpr int BYTES = END + 1024;  // + alignment slack
+  static_assert((K % 1024) == 0 && (U % 1024) == 0 && (P % 1024) == 0 && (WC % 128) == 0 &&
+                    (HC % 128) == 0 && (D % 128) == 0,
                 "alignment");
 };
 
 template <int DK, int SM, int WM>
-__global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const FwdParams p) {
+__global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __grid_constant__ FwdParams p) {
   using S = OutSmem<DK, SM, WM>;
-  extern __shared__ __align__(1024) unsigned char sm[];
+  extern __shared__ __align__(1024) unsigned char sm_raw[];
+  unsigned char* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
+  __shared__ __align__(8) uint64_t bar;
 
   const int nvb = p.Dv / 64;
   const int vb = blockIdx.x % nvb;
@@ -733,32 +775,34 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const Fw
   float* Gs = reinterpret_cast<float*>(sm + S::G);
   float* gam = Gs + 64;
   float* eg = Gs + 128;
+  // W / H codes land in the P tile (free until the P epilogue)
+  uint8_t* Wraw = reinterpret_cast<uint8_t*>(PH);
+  uint8_t* Hraw = Wraw + kChunk * DK;
 
-  load_rows_bf16<DK, kOutThreads>(Qs, p.q, tok0, L, p.Hk, hk);
-  load_rows_bf16<DK, kOutThreads>(Ks, p.k, tok0, L, p.Hk, hk);
-  for (int i = threadIdx.x; i < kChunk * 16; i += kOutThreads) {
-    const int r = i >> 4, c = i & 15;
-    const bool ok = r < L;
-    const int64_t tok = tok0 + (ok ? r : 0);
-    cp_async16(smem_u32(Us + r * kSA + c * 4), p.o + (tok * p.Hv + h) * p.Dv + vb * 64 + c * 4,
-               ok ? 16 : 0);
+  // ---- loads: TMA boxes on one mbarrier; g (and fp32 W / H) by the threads ----
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    const uint32_t bytes = 2 * kChunk * DK * 2 + kChunk * 64 * 4 +
+                           (WM != GDN_QDQ_NONE ? kChunk * DK : 0) +
+                           (SM != GDN_QDQ_NONE ? DK * 64 : 0);
+    mbar_expect_tx(&bar, bytes);
+#pragma unroll
+    for (int pn = 0; pn < DK / 64; ++pn) {
+      tma_load_2d(Qs + pn * kChunk * 64, &p.tm_q, hk * DK + pn * 64, (int)tok0, &bar);
+      tma_load_2d(Ks + pn * kChunk * 64, &p.tm_k, hk * DK + pn * 64, (int)tok0, &bar);
+    }
+#pragma unroll
+    for (int pn = 0; pn < 2; ++pn)
+      tma_load_2d(Us + pn * kChunk * 32, &p.tm_u, h * p.Dv + vb * 64 + pn * 32, (int)tok0, &bar);
+    if constexpr (WM != GDN_QDQ_NONE) tma_load_2d(Wraw, &p.tm_wc, h * DK, (int)tok0, &bar);
+    if constexpr (SM != GDN_QDQ_NONE)
+      tma_load_2d(Hraw, &p.tm_hc, vb * 64, (int)((slot * p.Hv + h) * DK), &bar);
   }
   if (threadIdx.x < kChunk) load_vec64(Gs, p.g, tok0, L, p.Hv, h, threadIdx.x);
   cp_async_commit();
-
-  // W^ and H^ operands from the saved context (rows >= L of W are zero).  Codes
-  // land in the P tile (free until the P epilogue) and are widened after the wait.
-  uint8_t* Wraw = reinterpret_cast<uint8_t*>(PH);
-  uint8_t* Hraw = Wraw + kChunk * DK;
   float sW = 1.f, sH = 1.f;
   if constexpr (WM != GDN_QDQ_NONE) {
-    constexpr int C16 = DK / 16;
-    for (int i = threadIdx.x; i < kChunk * C16; i += kOutThreads) {
-      const int r = i / C16, c16 = i % C16;
-      const bool ok = r < L;
-      cp_async16(smem_u32(Wraw + r * DK + c16 * 16),
-                 p.w_codes + ((tok0 + (ok ? r : 0)) * p.Hv + h) * DK + c16 * 16, ok ? 16 : 0);
-    }
     sW = p.w_scales[slot * p.Hv + h];
   } else {
     constexpr int C4 = DK / 4;
@@ -777,11 +821,6 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const Fw
     }
   }
   if constexpr (SM != GDN_QDQ_NONE) {
-    const uint8_t* src = p.h_codes + ((slot * p.Hv + h) * DK) * p.Dv + vb * 64;
-    for (int i = threadIdx.x; i < DK * 4; i += kOutThreads) {
-      const int d = i >> 2, c16 = i & 3;
-      cp_async16(smem_u32(Hraw + d * 64 + c16 * 16), src + (int64_t)d * p.Dv + c16 * 16, 16);
-    }
     sH = p.h_scales[(slot * p.Hv + h) * nvb + vb];
   } else {
     const float* src = p.h_full + ((slot * p.Hv + h) * DK) * p.Dv + vb * 64;
@@ -798,15 +837,24 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const Fw
       *reinterpret_cast<uint2*>(HcL + e) = make_uint2(pack_bf16(l0v, l1v), pack_bf16(l2v, l3v));
     }
   }
-  cp_async_commit();
+  __syncthreads();  // the mbarrier is initialised before anyone waits on it
+  const bool ok = mbar_wait(&bar, 0);
   cp_async_wait<0>();
-  __syncthreads();
+  if (__syncthreads_or(!ok)) {
+    if (threadIdx.x == 0) {
+      atomicOr(&g_fwd_device_error, 1);
+      mbar_wait(&bar, 0);  // once more, bounded, for the copies in flight
+    }
+    return;
+  }
 
+  // codes -> bf16 values (exact); W rows >= L (another sequence's tokens) are zero
   if constexpr (WM != GDN_QDQ_NONE) {
     constexpr int C4 = DK / 4;
     for (int i = threadIdx.x; i < kChunk * C4; i += kOutThreads) {
       const int r = i / C4, c4 = i % C4;
-      const float4 v = qdq_code4_values<WM>(*reinterpret_cast<const uint32_t*>(Wraw + r * DK + c4 * 4));
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (r < L) v = qdq_code4_values<WM>(*reinterpret_cast<const uint32_t*>(Wraw + r * DK + c4 * 4));
       *reinterpret_cast<uint2*>(WcH + swz<DK>(r, c4 * 4)) =
           make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
     }
@@ -830,7 +878,9 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const Fw
     eg[2 * lane + 1] = expf(gam1);
   }
 
-  // warp tile: rows 16 rt .. +15, columns 32 ch .. +31
+  // warp tile: rows 16 rt .. +15, columns 32 ch .. +31.  Rows >= L of Q and K
+  // hold another sequence's tokens: they only reach P entries outside the
+  // causal mask or output rows that are not stored.
   const int rt = warp & 3, ch = warp >> 2;
   const int row0 = rt * 16, col0 = ch * 32;
   const bool p_tile = col0 <= row0 + 15;
@@ -862,7 +912,8 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const Fw
         st_bf16x2(PH + swz<64>(i, j), h0v, h1v);
         st_bf16x2(PL + swz<64>(i, j), l0v, l1v);
       }
-      const float2 u = *reinterpret_cast<const float2*>(Us + i * kSA + j);
+      float2 u = *reinterpret_cast<const float2*>(Us + swz_f32(i, j));
+      if (i >= L) u = make_float2(0.f, 0.f);
       split_bf16(u.x - sWH * dacc[nt][2 * e2], h0v, l0v);
       split_bf16(u.y - sWH * dacc[nt][2 * e2 + 1], h1v, l1v);
       st_bf16x2(DH + swz<64>(i, j), h0v, h1v);
@@ -884,16 +935,29 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const Fw
       for (int e2 = 0; e2 < 2; ++e2) {
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
         const float ei = eg[i] * sq;
-        *reinterpret_cast<float2*>(Ost + i * kSA + j) =
+        *reinterpret_cast<float2*>(Ost + swz_f32(i, j)) =
             make_float2(p.scale * (ei * qacc[nt][2 * e2] + o2[nt][2 * e2]),
                         p.scale * (ei * qacc[nt][2 * e2 + 1] + o2[nt][2 * e2 + 1]));
       }
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < L * 16; i += kOutThreads) {
-    const int r = i >> 4, c4 = i & 15;
-    *reinterpret_cast<float4*>(p.o + ((tok0 + r) * p.Hv + h) * p.Dv + vb * 64 + c4 * 4) =
-        *reinterpret_cast<const float4*>(Ost + r * kSA + c4 * 4);
+  if (L == kChunk) {
+    // a full chunk leaves as two TMA boxes (rows past the tensor end are clipped)
+    fence_proxy_async();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+#pragma unroll
+      for (int pn = 0; pn < 2; ++pn)
+        tma_store_2d(&p.tm_u, h * p.Dv + vb * 64 + pn * 32, (int)tok0, Ost + pn * kChunk * 32);
+      tma_store_commit();
+      tma_store_wait_all();
+    }
+  } else {
+    __syncthreads();
+    for (int i = threadIdx.x; i < L * 16; i += kOutThreads) {
+      const int r = i >> 4, c4 = i & 15;
+      *reinterpret_cast<float4*>(p.o + ((tok0 + r) * p.Hv + h) * p.Dv + vb * 64 + c4 * 4) =
+          *reinterpret_cast<const float4*>(Ost + swz_f32(r, c4 * 4));
+    }
   }
 }
 
@@ -1035,6 +1099,10 @@ gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const 
     const int DK = d.Dk;
     bool ok = make_map(&prm.tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k, (uint64_t)d.Hk * DK, tok,
                        (uint64_t)d.Hk * DK * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              make_map(&prm.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, (uint64_t)d.Hk * DK, tok,
+                       (uint64_t)d.Hk * DK * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              make_map(&prm.tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v, (uint64_t)d.Hv * d.Dv, tok,
+                       (uint64_t)d.Hv * d.Dv * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
               make_map(&prm.tm_u, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, o, (uint64_t)d.Hv * d.Dv, tok,
                        (uint64_t)d.Hv * d.Dv * 4, 32, 64, CU_TENSOR_MAP_SWIZZLE_128B);
     if (ok && p.w_mode != GDN_QDQ_NONE)
