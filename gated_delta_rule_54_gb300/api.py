@@ -236,6 +236,9 @@ def split_ctx(ctx: torch.Tensor, p: GdnProblem):
         n = B * T * Hv * Dk
         out["w_full"] = ctx[off:off + 4 * n].view(torch.float32).view(B, T, Hv, Dk)
         off = al(off + 4 * n)
+    n = ns * Hv * 5 * 64
+    out["chunk_vectors"] = ctx[off:off + 4 * n].view(torch.float32).view(ns, Hv, 5, 64)
+    off = al(off + 4 * n)
     if p.state_mode != 0:
         n = ns * Hv * Dk * Dv
         out["h_codes"] = ctx[off:off + n].view(ns, Hv, Dk, Dv)

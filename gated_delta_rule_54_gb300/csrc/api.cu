@@ -40,6 +40,8 @@ CtxLayout ctx_layout(const gdn_problem& p) {
     L.w_full = off;
     off = align256(off + sizeof(float) * tokens * d.Hv * d.Dk);
   }
+  L.cvec = off;
+  off = align256(off + sizeof(float) * (size_t)d.n_slots * d.Hv * kCvecFloats);
   const size_t per_slot = (size_t)d.n_slots * d.Hv * d.Dk * d.Dv;
   if (p.state_mode != GDN_QDQ_NONE) {
     L.h_codes = off;

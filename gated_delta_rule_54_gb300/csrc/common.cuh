@@ -12,6 +12,8 @@
 namespace gdn {
 
 constexpr int kChunk = 64;   // chunk length (first QAT page, "What does this PR do?")
+// offsets in the per (chunk, value head) vector record (kCvecFloats floats)
+constexpr int kCvGam = 0, kCvEg = 64, kCvDec = 128, kCvBet = 192, kCvBeg = 256;
 constexpr int kBlockV = 64;  // state-scale tile width (`state.block_v 64`)
 
 // ---------------------------------------------------------------------------
@@ -265,6 +267,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, 
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%2, %3}], [%4];\n" ::"r"(smem_u32(dst)),
       "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+// contiguous bulk copy of `bytes` (multiple of 16; both addresses 16-byte aligned)
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes,
+                                             uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
       : "memory");
 }
 // 2-D tiled store of one box from shared memory (bulk async-group completion)

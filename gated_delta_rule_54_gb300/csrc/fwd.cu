@@ -65,6 +65,7 @@ struct FwdParams {
   uint8_t* h_codes;
   float* h_scales;
   float* h_full;
+  float* cvec;  // [n_slots, Hv, kCvecFloats] chunk vectors
   const int32_t* cu_seqlens;
   int64_t T;
   int Hk, Hv, Dv, G, N;
@@ -242,6 +243,13 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __g
     beg[2 * lane + 1] = b1 * e1;
     bet[2 * lane] = b0;
     bet[2 * lane + 1] = b1;
+    // the chunk vectors the state scan, the output pass and the backward read
+    float* cv = p.cvec + (slot * p.Hv + h) * kCvecFloats;
+    *reinterpret_cast<float2*>(cv + kCvGam + 2 * lane) = make_float2(gam0, gam1);
+    *reinterpret_cast<float2*>(cv + kCvEg + 2 * lane) = make_float2(e0, e1);
+    *reinterpret_cast<float2*>(cv + kCvDec + 2 * lane) = make_float2(expf(gL - gam0), expf(gL - gam1));
+    *reinterpret_cast<float2*>(cv + kCvBet + 2 * lane) = make_float2(b0, b1);
+    *reinterpret_cast<float2*>(cv + kCvBeg + 2 * lane) = make_float2(b0 * e0, b1 * e1);
   }
 
   // warp tile: rows 16 rt .. +15, columns 32 ch .. +31 of a [64 x 64] product
@@ -407,9 +415,8 @@ struct StateSmem {
   static constexpr int K = 0;                                          // 2 x bf16 [64][DK] (TMA)
   static constexpr int U = K + 2 * kChunk * DK * 2;                    // 2 x f32 [64][64] (TMA, swz_f32)
   static constexpr int WR = U + 2 * kChunk * 64 * 4;                   // 2 x W codes (TMA) / f32
-  static constexpr int G = WR + 2 * WRAW;                              // 2 x g[64]
-  static constexpr int VEC = G + 512;                                  // decay[64], e^{gL}
-  static constexpr int WC = VEC + 512;                                 // W^ bf16 [64][DK] (hi, lo)
+  static constexpr int CV = WR + 2 * WRAW;                             // 2 x chunk vectors (bulk copy)
+  static constexpr int WC = CV + 2 * kCvecFloats * 4;                  // W^ bf16 [64][DK] (hi, lo)
   static constexpr int HC = WC + (WM == GDN_QDQ_NONE ? 2 : 1) * kChunk * DK * 2;  // H^ [DK][64]
   static constexpr int DP = HC + (SM == GDN_QDQ_NONE ? 2 : 1) * DK * 64 * 2;      // Delta' hi, lo
   static constexpr int HST = DP + 2 * kChunk * 64 * 2;                 // u8 [DK][64] codes (TMA store)
@@ -421,19 +428,22 @@ struct StateSmem {
 };
 
 // TMA boxes of one chunk: K (two 64-column panels), U (two 32-column fp32
-// panels) and, for quantized W, its codes; g (and an fp32 W) by cp.async.
+// panels), the chunk vectors and, for quantized W, its codes (an fp32 W by
+// cp.async).
 template <int DK, int WM>
 __device__ __forceinline__ uint32_t state_chunk_tx_bytes() {
-  return kChunk * DK * 2 + kChunk * 64 * 4 + (WM != GDN_QDQ_NONE ? kChunk * DK : 0);
+  return kChunk * DK * 2 + kChunk * 64 * 4 + kCvecFloats * 4 +
+         (WM != GDN_QDQ_NONE ? kChunk * DK : 0);
 }
 
 template <int DK, int WM>
 __device__ __forceinline__ void issue_state_chunk(const FwdParams& p, __nv_bfloat16* Ks,
-                                                  unsigned char* Wr, float* Us, float* Gs,
+                                                  unsigned char* Wr, float* Us, float* Cv,
                                                   uint64_t* bar, int64_t tok0, int L, int hk,
-                                                  int h, int vb) {
+                                                  int h, int vb, int64_t slot) {
   if (threadIdx.x == 0) {
     mbar_expect_tx(bar, state_chunk_tx_bytes<DK, WM>());
+    bulk_load_1d(Cv, p.cvec + (slot * p.Hv + h) * kCvecFloats, kCvecFloats * 4, bar);
 #pragma unroll
     for (int pn = 0; pn < DK / 64; ++pn)
       tma_load_2d(Ks + pn * kChunk * 64, &p.tm_k, hk * DK + pn * 64, (int)tok0, bar);
@@ -452,7 +462,6 @@ __device__ __forceinline__ void issue_state_chunk(const FwdParams& p, __nv_bfloa
                  ok ? 16 : 0);
     }
   }
-  if (threadIdx.x < kChunk) load_vec64(Gs, p.g, tok0, L, p.Hv, h, threadIdx.x);
   cp_async_commit();
 }
 
@@ -483,7 +492,6 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
   }
   const int nchunks = (L + kChunk - 1) / kChunk;
 
-  float* dec = reinterpret_cast<float*>(sm + S::VEC);  // e^{gamma_L - gamma_i}; [64] = e^{gamma_L}
   __nv_bfloat16* WcH = reinterpret_cast<__nv_bfloat16*>(sm + S::WC);
   __nv_bfloat16* WcL = WcH + kChunk * DK;  // WM == NONE only
   __nv_bfloat16* HcH = reinterpret_cast<__nv_bfloat16*>(sm + S::HC);
@@ -494,7 +502,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
   auto Kbuf = [&](int b) { return reinterpret_cast<__nv_bfloat16*>(sm + S::K + b * kChunk * DK * 2); };
   auto Wbuf = [&](int b) { return sm + S::WR + b * S::WRAW; };
   auto Ubuf = [&](int b) { return reinterpret_cast<float*>(sm + S::U + b * kChunk * 64 * 4); };
-  auto Gbuf = [&](int b) { return reinterpret_cast<float*>(sm + S::G + b * 256); };
+  auto Cbuf = [&](int b) { return reinterpret_cast<float*>(sm + S::CV + b * kCvecFloats * 4); };
 
   // Delta tile: [64 x 64] -> 16 x 16 per warp; state tile [DK x 64]
   const int row0 = (warp & 3) * 16, col0 = (warp >> 2) * 16;
@@ -530,8 +538,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
 
   float sW_next = 1.f;
   if (nchunks > 0) {
-    issue_state_chunk<DK, WM>(p, Kbuf(0), Wbuf(0), Ubuf(0), Gbuf(0), &bars[0], tok0,
-                              min(L, kChunk), hk, h, vb);
+    issue_state_chunk<DK, WM>(p, Kbuf(0), Wbuf(0), Ubuf(0), Cbuf(0), &bars[0], tok0,
+                              min(L, kChunk), hk, h, vb, slot0);
     if constexpr (WM != GDN_QDQ_NONE) sW_next = p.w_scales[slot0 * p.Hv + h];
   }
 
@@ -553,13 +561,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
       return;
     }
 
-    if (warp == 0) {
-      float gam0, gam1, gL;
-      chunk_cumsum(Gbuf(buf), lane, gam0, gam1, gL);
-      dec[2 * lane] = expf(gL - gam0);
-      dec[2 * lane + 1] = expf(gL - gam1);
-      if (lane == 0) dec[64] = expf(gL);
-    }
+    const float* dec = Cbuf(buf) + kCvDec;  // e^{gamma_L - gamma_i}
+    const float egL = Cbuf(buf)[kCvEg + 63];  // e^{gamma_L} (gamma is flat past the last row)
 
     // W^ operand: codes -> bf16 values (exact), or the fp32 W split hi/lo; rows >= Lc are zero
     if constexpr (WM != GDN_QDQ_NONE) {
@@ -638,7 +641,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
           }
       }
     }
-    __syncthreads();  // W^, H^ operands, decay factors ready
+    __syncthreads();  // W^, H^ operands ready
 
     if (threadIdx.x == 0) {
       if constexpr (SM != GDN_QDQ_NONE) {
@@ -649,9 +652,9 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
     }
     // prefetch chunk c + 1 (buffer buf ^ 1 was last read before this iteration's first barrier)
     if (c + 1 < nchunks) {
-      issue_state_chunk<DK, WM>(p, Kbuf(buf ^ 1), Wbuf(buf ^ 1), Ubuf(buf ^ 1), Gbuf(buf ^ 1),
+      issue_state_chunk<DK, WM>(p, Kbuf(buf ^ 1), Wbuf(buf ^ 1), Ubuf(buf ^ 1), Cbuf(buf ^ 1),
                                 &bars[buf ^ 1], tok0 + (int64_t)(c + 1) * kChunk,
-                                min(L - (c + 1) * kChunk, kChunk), hk, h, vb);
+                                min(L - (c + 1) * kChunk, kChunk), hk, h, vb, slot + 1);
       if constexpr (WM != GDN_QDQ_NONE) sW_next = p.w_scales[(slot + 1) * p.Hv + h];
     }
 
@@ -683,7 +686,6 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
 
     // ---- a9: H <- e^{gamma_L} H^ + K^T Delta' (K rows >= Lc meet zero rows of Delta') ----
     {
-      const float egL = dec[64];
       float m = 0.f;
 #pragma unroll
       for (int nt = 0; nt < NTH; ++nt)
@@ -729,11 +731,11 @@ struct OutSmem {
   static constexpr int P = U + kChunk * 64 * 4;                            // P hi, lo; first W / H codes (TMA)
   static constexpr int WC = P + 2 * kChunk * 64 * 2;                       // W^ [64][DK] (hi, lo)
   static constexpr int HC = WC + (WM == GDN_QDQ_NONE ? 2 : 1) * kChunk * DK * 2;  // H^ [DK][64] (hi, lo)
-  static constexpr int G = HC + (SM == GDN_QDQ_NONE ? 2 : 1) * DK * 64 * 2;       // g, gamma, e^gamma
+  static constexpr int CV = HC + (SM == GDN_QDQ_NONE ? 2 : 1) * DK * 64 * 2;      // chunk vectors
   // Delta hi, lo [64][64]: in the dead K tile when it is large enough
   static constexpr bool D_IN_K = 2 * kChunk * 64 * 2 <= kChunk * DK * 2;
-  static constexpr int D = D_IN_K ? K : G + 3 * 64 * 4;
-  static constexpr int END = D_IN_K ? G + 3 * 64 * 4 : D + 2 * kChunk * 64 * 2;
+  static constexpr int D = D_IN_K ? K : CV + kCvecFloats * 4;
+  static constexpr int END = D_IN_K ? CV + kCvecFloats * 4 : D + 2 * kChunk * 64 * 2;
   static constexpr int BYTES = END + 1024;  // + alignment slack
   static_assert((K % 1024) == 0 && (U % 1024) == 0 && (P % 1024) == 0 && (WC % 128) == 0 &&
                     (HC % 128) == 0 && (D % 128) == 0,
@@ -772,9 +774,9 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
   __nv_bfloat16* PL = PH + kChunk * 64;
   __nv_bfloat16* DH = reinterpret_cast<__nv_bfloat16*>(sm + S::D);
   __nv_bfloat16* DL = DH + kChunk * 64;
-  float* Gs = reinterpret_cast<float*>(sm + S::G);
-  float* gam = Gs + 64;
-  float* eg = Gs + 128;
+  float* Cv = reinterpret_cast<float*>(sm + S::CV);
+  const float* gam = Cv + kCvGam;
+  const float* eg = Cv + kCvEg;
   // W / H codes land in the P tile (free until the P epilogue)
   uint8_t* Wraw = reinterpret_cast<uint8_t*>(PH);
   uint8_t* Hraw = Wraw + kChunk * DK;
@@ -783,10 +785,11 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();
-    const uint32_t bytes = 2 * kChunk * DK * 2 + kChunk * 64 * 4 +
+    const uint32_t bytes = 2 * kChunk * DK * 2 + kChunk * 64 * 4 + kCvecFloats * 4 +
                            (WM != GDN_QDQ_NONE ? kChunk * DK : 0) +
                            (SM != GDN_QDQ_NONE ? DK * 64 : 0);
     mbar_expect_tx(&bar, bytes);
+    bulk_load_1d(Cv, p.cvec + (slot * p.Hv + h) * kCvecFloats, kCvecFloats * 4, &bar);
 #pragma unroll
     for (int pn = 0; pn < DK / 64; ++pn) {
       tma_load_2d(Qs + pn * kChunk * 64, &p.tm_q, hk * DK + pn * 64, (int)tok0, &bar);
@@ -799,8 +802,6 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
     if constexpr (SM != GDN_QDQ_NONE)
       tma_load_2d(Hraw, &p.tm_hc, vb * 64, (int)((slot * p.Hv + h) * DK), &bar);
   }
-  if (threadIdx.x < kChunk) load_vec64(Gs, p.g, tok0, L, p.Hv, h, threadIdx.x);
-  cp_async_commit();
   float sW = 1.f, sH = 1.f;
   if constexpr (WM != GDN_QDQ_NONE) {
     sW = p.w_scales[slot * p.Hv + h];
@@ -839,7 +840,6 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
   }
   __syncthreads();  // the mbarrier is initialised before anyone waits on it
   const bool ok = mbar_wait(&bar, 0);
-  cp_async_wait<0>();
   if (__syncthreads_or(!ok)) {
     if (threadIdx.x == 0) {
       atomicOr(&g_fwd_device_error, 1);
@@ -869,15 +869,6 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
   }
   __syncthreads();  // W^, H^ operands ready; the P tile is free again
 
-  if (warp == 0) {
-    float gam0, gam1, gL;
-    chunk_cumsum(Gs, lane, gam0, gam1, gL);
-    gam[2 * lane] = gam0;
-    gam[2 * lane + 1] = gam1;
-    eg[2 * lane] = expf(gam0);
-    eg[2 * lane + 1] = expf(gam1);
-  }
-
   // warp tile: rows 16 rt .. +15, columns 32 ch .. +31.  Rows >= L of Q and K
   // hold another sequence's tokens: they only reach P entries outside the
   // causal mask or output rows that are not stored.
@@ -894,7 +885,7 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
   if constexpr (SM == GDN_QDQ_NONE) wgemm<4, false, true, DK, 64>(dacc, WcH, row0, HcL, col0, 0, DK, lane);
   wgemm<4, false, true, DK, 64>(qacc, Qs, row0, HcH, col0, 0, DK, lane);
   if constexpr (SM == GDN_QDQ_NONE) wgemm<4, false, true, DK, 64>(qacc, Qs, row0, HcL, col0, 0, DK, lane);
-  __syncthreads();  // K reads done (its tile becomes Delta); gamma ready
+  __syncthreads();  // K reads done (its tile becomes Delta)
 
   const float sWH = (WM != GDN_QDQ_NONE ? sW : 1.f) * (SM != GDN_QDQ_NONE ? sH : 1.f);
 #pragma unroll
@@ -949,7 +940,7 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
       for (int pn = 0; pn < 2; ++pn)
         tma_store_2d(&p.tm_u, h * p.Dv + vb * 64 + pn * 32, (int)tok0, Ost + pn * kChunk * 32);
       tma_store_commit();
-      tma_store_wait_all();
+      tma_store_wait_read();
     }
   } else {
     __syncthreads();
@@ -1077,6 +1068,7 @@ gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const 
   } else {
     prm.w_full = reinterpret_cast<float*>(base + L.w_full);
   }
+  prm.cvec = reinterpret_cast<float*>(base + L.cvec);
   if (p.state_mode != GDN_QDQ_NONE) {
     prm.h_codes = base + L.h_codes;
     prm.h_scales = reinterpret_cast<float*>(base + L.h_scales);

@@ -9,6 +9,9 @@
 namespace gdn {
 
 constexpr int kChunkLen = 64;  // chunk length and state-scale tile width
+// per (chunk, value head) vectors the forward's chunk prep saves in the
+// context: gamma, e^gamma, e^{gamma_L - gamma}, beta, beta e^gamma (64 each)
+constexpr int kCvecFloats = 5 * 64;
 
 // Derived sizes of a validated problem.
 struct Dims {
@@ -19,7 +22,7 @@ struct Dims {
 
 // Byte offsets of the saved context segments (see gdn_ctx_bytes).
 struct CtxLayout {
-  size_t w_codes, w_scales, w_full, h_codes, h_scales, h_full, total;
+  size_t w_codes, w_scales, w_full, cvec, h_codes, h_scales, h_full, total;
 };
 
 Dims dims_of(const gdn_problem& p);

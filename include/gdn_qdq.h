@@ -119,6 +119,10 @@ int64_t gdn_num_chunk_slots(const gdn_problem* p);
  *   w_codes   u8  [B, T, Hv, Dk]        quantized W codes    (w_mode != NONE)
  *   w_scales  f32 [n_slots, Hv]         W scale per chunk    (w_mode != NONE)
  *   w_full    f32 [B, T, Hv, Dk]        unquantized W        (w_mode == NONE)
+ *   cvec      f32 [n_slots, Hv, 5, 64]  per chunk: gamma (in-chunk cumsum of
+ *                                       g), e^gamma, e^{gamma_L - gamma}, beta,
+ *                                       beta e^gamma (rows past the chunk end:
+ *                                       gamma flat, beta 0)
  *   h_codes   u8  [n_slots, Hv, Dk, Dv] state codes entering each chunk (state_mode != NONE)
  *   h_scales  f32 [n_slots, Hv, Dv/64]  state scale per [Dk, 64] tile  (state_mode != NONE)
  *   h_full    f32 [n_slots, Hv, Dk, Dv] unquantized state entering each chunk (state_mode == NONE)

@@ -77,10 +77,11 @@ def test_sizes():
     assert lib.gdn_num_chunk_slots(ctypes.byref(p)) == 2 * nt
     al = lambda x: (x + 255) // 256 * 256
     ns = 2 * nt
-    exp = al(2 * 300 * 4 * 128) + al(4 * ns * 4) + al(ns * 4 * 128 * 128) + al(4 * ns * 4 * 2)
+    cv = al(4 * ns * 4 * 5 * 64)
+    exp = al(2 * 300 * 4 * 128) + al(4 * ns * 4) + cv + al(ns * 4 * 128 * 128) + al(4 * ns * 4 * 2)
     assert lib.gdn_ctx_bytes(ctypes.byref(p)) == exp
     p0 = _problem(state_mode=0, w_mode=0)
-    assert lib.gdn_ctx_bytes(ctypes.byref(p0)) == al(4 * 2 * 300 * 4 * 128) + al(4 * ns * 4 * 128 * 128)
+    assert lib.gdn_ctx_bytes(ctypes.byref(p0)) == al(4 * 2 * 300 * 4 * 128) + cv + al(4 * ns * 4 * 128 * 128)
     pk = _problem(B=1, T=1000, N=7, cu_seqlens=4096)
     assert lib.gdn_num_chunk_slots(ctypes.byref(pk)) == 1000 // 64 + 7
     assert lib.gdn_ctx_bytes(ctypes.byref(_problem(Dk=96))) == 0

@@ -61,6 +61,24 @@ def _check_case(w, lengths=None, scale=1.0):
         diff = code_steps(wc, wref, wm).max(-1)
         for t, h in zip(*np.nonzero(diff)):
             flipped.add((int(tok_seq[t]), int(h)))
+    # chunk vectors: gamma, e^gamma, e^{gamma_L - gamma}, beta, beta e^gamma per (chunk, head)
+    cv = seg["chunk_vectors"].cpu().numpy()[smap]
+    g64 = d["g"].double().numpy().reshape(-1, w.Hv)
+    b64 = d["beta"].double().numpy().reshape(-1, w.Hv)
+    start = 0
+    ci = 0
+    for L in lens:
+        for c0 in range(0, L, 64):
+            Lc = min(64, L - c0)
+            gam = np.zeros((64, w.Hv))
+            gam[:Lc] = np.cumsum(g64[start + c0:start + c0 + Lc], 0)
+            gam[Lc:] = gam[Lc - 1]
+            bet = np.zeros((64, w.Hv))
+            bet[:Lc] = b64[start + c0:start + c0 + Lc]
+            ref = np.stack([gam, np.exp(gam), np.exp(gam[63] - gam), bet, bet * np.exp(gam)], 0)
+            assert np.allclose(cv[ci].transpose(1, 2, 0), ref, rtol=2e-5, atol=1e-6), "chunk vectors"
+            ci += 1
+        start += L
     Hv = w.Hv
     key = lambda n, h: n * Hv + h
     fl = {key(n, h) for n, h in flipped}
