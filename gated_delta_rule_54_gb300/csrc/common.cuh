@@ -115,6 +115,29 @@ __device__ __forceinline__ void mma_bf16(float (&c)[4], const uint32_t (&a)[4], 
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
+// mma.sync m16n8k32 with E4M3 operands (exact products of E4M3 codes), f32
+// accumulation.  Byte geometry of the fragments equals the bf16 m16n8k16
+// case with two codes per 16-bit element, so the same ldmatrix addressing
+// serves both (k offsets in units of two codes).
+__device__ __forceinline__ void mma_e4m3(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 "
+      "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// E4M3 codes of (x0, x1) * rcp (each product rounded to fp32 first, then RNE
+// with finite saturation), packed low byte = x0, and their exact values.
+__device__ __forceinline__ uint16_t e4m3_code2(float x0, float x1, float rcp, float2& val) {
+  const __nv_fp8x2_storage_t c = __nv_cvt_float2_to_fp8x2(
+      make_float2(__fmul_rn(x0, rcp), __fmul_rn(x1, rcp)), __NV_SATFINITE, __NV_E4M3);
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(c, __NV_E4M3);
+  val = __half22float2(__half2(h));
+  return (uint16_t)c;
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], uint32_t addr) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])

@@ -49,8 +49,9 @@ __device__ int g_fwd_device_error;
 
 struct FwdParams {
   // TMA descriptors (2-D): k, q [B*T, Hk*Dk] bf16, v [B*T, Hv*Dv] bf16, o/U [B*T, Hv*Dv] f32,
-  // W codes [B*T, Hv*Dk] u8, state codes [n_slots*Hv*Dk, Dv] u8
-  CUtensorMap tm_k, tm_q, tm_v, tm_u, tm_wc, tm_hc;
+  // W codes [B*T, Hv*Dk] u8 (plain rows, and with the 128-byte swizzle when
+  // Dk = 128), state codes [n_slots*Hv*Dk, Dv] u8
+  CUtensorMap tm_k, tm_q, tm_v, tm_u, tm_wc, tm_wc_sw, tm_hc;
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
@@ -436,7 +437,7 @@ __device__ __forceinline__ uint32_t state_chunk_tx_bytes() {
          (WM != GDN_QDQ_NONE ? kChunk * DK : 0);
 }
 
-template <int DK, int WM>
+template <int DK, int WM, bool F8>
 __device__ __forceinline__ void issue_state_chunk(const FwdParams& p, __nv_bfloat16* Ks,
                                                   unsigned char* Wr, float* Us, float* Cv,
                                                   uint64_t* bar, int64_t tok0, int L, int hk,
@@ -450,7 +451,8 @@ __device__ __forceinline__ void issue_state_chunk(const FwdParams& p, __nv_bfloa
 #pragma unroll
     for (int pn = 0; pn < 2; ++pn)
       tma_load_2d(Us + pn * kChunk * 32, &p.tm_u, h * p.Dv + vb * 64 + pn * 32, (int)tok0, bar);
-    if constexpr (WM != GDN_QDQ_NONE) tma_load_2d(Wr, &p.tm_wc, h * DK, (int)tok0, bar);
+    if constexpr (WM != GDN_QDQ_NONE)
+      tma_load_2d(Wr, F8 ? &p.tm_wc_sw : &p.tm_wc, h * DK, (int)tok0, bar);
   }
   if constexpr (WM == GDN_QDQ_NONE) {
     constexpr int CPR = DK / 4;
@@ -468,6 +470,9 @@ __device__ __forceinline__ void issue_state_chunk(const FwdParams& p, __nv_bfloa
 template <int DK, int SM, int WM>
 __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const __grid_constant__ FwdParams p) {
   using S = StateSmem<DK, SM, WM>;
+  // E4M3 W and state at Dk = 128: Delta = W^ H^ runs on E4M3 codes directly
+  // (W codes as TMA wrote them, H^ codes written [v][dk] as the B operand)
+  constexpr bool F8 = SM == GDN_QDQ_E4M3 && WM == GDN_QDQ_E4M3 && DK == 128;
   extern __shared__ __align__(1024) unsigned char sm_raw[];
   unsigned char* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
   __shared__ float red[kStateWarps];
@@ -499,6 +504,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
   __nv_bfloat16* DpH = reinterpret_cast<__nv_bfloat16*>(sm + S::DP);
   __nv_bfloat16* DpL = DpH + kChunk * 64;
   uint8_t* Hst = sm + S::HST;
+  uint8_t* Hb = sm + S::HC;  // F8: H^ codes [64 v][DK dk], swizzled like a bf16 [64][64] tile
   auto Kbuf = [&](int b) { return reinterpret_cast<__nv_bfloat16*>(sm + S::K + b * kChunk * DK * 2); };
   auto Wbuf = [&](int b) { return sm + S::WR + b * S::WRAW; };
   auto Ubuf = [&](int b) { return reinterpret_cast<float*>(sm + S::U + b * kChunk * 64 * 4); };
@@ -538,7 +544,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
 
   float sW_next = 1.f;
   if (nchunks > 0) {
-    issue_state_chunk<DK, WM>(p, Kbuf(0), Wbuf(0), Ubuf(0), Cbuf(0), &bars[0], tok0,
+    issue_state_chunk<DK, WM, F8>(p, Kbuf(0), Wbuf(0), Ubuf(0), Cbuf(0), &bars[0], tok0,
                               min(L, kChunk), hk, h, vb, slot0);
     if constexpr (WM != GDN_QDQ_NONE) sW_next = p.w_scales[slot0 * p.Hv + h];
   }
@@ -565,7 +571,9 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
     const float egL = Cbuf(buf)[kCvEg + 63];  // e^{gamma_L} (gamma is flat past the last row)
 
     // W^ operand: codes -> bf16 values (exact), or the fp32 W split hi/lo; rows >= Lc are zero
-    if constexpr (WM != GDN_QDQ_NONE) {
+    // (F8 reads the codes as they landed; rows >= Lc of Delta' are zeroed below)
+    if constexpr (F8) {
+    } else if constexpr (WM != GDN_QDQ_NONE) {
       const uint8_t* Wr = Wbuf(buf);
       constexpr int C4 = DK / 4;
       for (int i = threadIdx.x; i < kChunk * C4; i += kStateThreads) {
@@ -598,7 +606,31 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
       float amax = red[0];
 #pragma unroll
       for (int i = 1; i < kStateWarps; ++i) amax = fmaxf(amax, red[i]);
-      if constexpr (SM != GDN_QDQ_NONE) {
+      if constexpr (F8) {
+        float rcp;
+        qdq_scale<SM>(amax, sH, rcp);
+        const bool zero = amax == 0.f;
+#pragma unroll
+        for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int d = h_row0 + gq + 8 * e2, col = h_col0 + nt * 8 + 2 * tq;
+            float* hv = &hreg[nt][2 * e2];
+            float2 val;
+            // amax == 0: rcp == 0 gives signed-zero codes, and the values stay as they are
+            const uint16_t c2 = e4m3_code2(hv[0], hv[1], rcp, val);
+            if (!zero) {
+              hv[0] = __fmul_rn(val.x, sH);
+              hv[1] = __fmul_rn(val.y, sH);
+            }
+            *reinterpret_cast<uint16_t*>(Hst + d * 64 + col) = c2;
+            uint8_t* hb = Hb + 2 * swz<64>(col, d >> 1) + (d & 1);
+            hb[0] = (uint8_t)(c2 & 0xff);
+            hb[2 * swz<64>(col + 1, d >> 1) - 2 * swz<64>(col, d >> 1)] = (uint8_t)(c2 >> 8);
+          }
+        if (zero) sH = 0.f;
+        fence_proxy_async();  // Hst is read by the TMA store below
+      } else if constexpr (SM != GDN_QDQ_NONE) {
         float rcp;
         qdq_scale<SM>(amax, sH, rcp);
 #pragma unroll
@@ -652,7 +684,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
     }
     // prefetch chunk c + 1 (buffer buf ^ 1 was last read before this iteration's first barrier)
     if (c + 1 < nchunks) {
-      issue_state_chunk<DK, WM>(p, Kbuf(buf ^ 1), Wbuf(buf ^ 1), Ubuf(buf ^ 1), Cbuf(buf ^ 1),
+      issue_state_chunk<DK, WM, F8>(p, Kbuf(buf ^ 1), Wbuf(buf ^ 1), Ubuf(buf ^ 1), Cbuf(buf ^ 1),
                                 &bars[buf ^ 1], tok0 + (int64_t)(c + 1) * kChunk,
                                 min(L - (c + 1) * kChunk, kChunk), hk, h, vb, slot + 1);
       if constexpr (WM != GDN_QDQ_NONE) sW_next = p.w_scales[(slot + 1) * p.Hv + h];
@@ -662,9 +694,22 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
     {
       float dacc[2][4];
       zero_acc(dacc);
-      wgemm<2, false, true, DK, 64>(dacc, WcH, row0, HcH, col0, 0, DK, lane);
-      if constexpr (WM == GDN_QDQ_NONE) wgemm<2, false, true, DK, 64>(dacc, WcL, row0, HcH, col0, 0, DK, lane);
-      if constexpr (SM == GDN_QDQ_NONE) wgemm<2, false, true, DK, 64>(dacc, WcH, row0, HcL, col0, 0, DK, lane);
+      if constexpr (F8) {
+        const __nv_bfloat16* Wb = reinterpret_cast<const __nv_bfloat16*>(Wbuf(buf));
+        const __nv_bfloat16* Hbb = reinterpret_cast<const __nv_bfloat16*>(Hb);
+#pragma unroll
+        for (int k2 = 0; k2 < DK / 2; k2 += 16) {  // 32 codes per step
+          uint32_t a[4], b[4];
+          ldsm_x4(a, a_frag_addr<64>(Wb, row0, k2, lane));
+          ldsm_x4(b, bnk_frag_addr<64>(Hbb, col0, k2, lane));
+          mma_e4m3(dacc[0], a, b[0], b[1]);
+          mma_e4m3(dacc[1], a, b[2], b[3]);
+        }
+      } else {
+        wgemm<2, false, true, DK, 64>(dacc, WcH, row0, HcH, col0, 0, DK, lane);
+        if constexpr (WM == GDN_QDQ_NONE) wgemm<2, false, true, DK, 64>(dacc, WcL, row0, HcH, col0, 0, DK, lane);
+        if constexpr (SM == GDN_QDQ_NONE) wgemm<2, false, true, DK, 64>(dacc, WcH, row0, HcL, col0, 0, DK, lane);
+      }
       const float sWH = (WM != GDN_QDQ_NONE ? sW : 1.f) * (SM != GDN_QDQ_NONE ? sH : 1.f);
       const float* Us = Ubuf(buf);
 #pragma unroll
@@ -672,9 +717,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-          float2 u = *reinterpret_cast<const float2*>(Us + swz_f32(i, j));
-          if (i >= Lc) u = make_float2(0.f, 0.f);
-          const float di = dec[i];
+          const float2 u = *reinterpret_cast<const float2*>(Us + swz_f32(i, j));
+          const float di = i < Lc ? dec[i] : 0.f;  // rows past the chunk end contribute nothing
           float h0v, l0v, h1v, l1v;
           split_bf16((u.x - sWH * dacc[nt][2 * e2]) * di, h0v, l0v);
           split_bf16((u.y - sWH * dacc[nt][2 * e2 + 1]) * di, h1v, l1v);
@@ -1100,6 +1144,9 @@ gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const 
     if (ok && p.w_mode != GDN_QDQ_NONE)
       ok = make_map(&prm.tm_wc, CU_TENSOR_MAP_DATA_TYPE_UINT8, prm.w_codes, (uint64_t)d.Hv * DK,
                     tok, (uint64_t)d.Hv * DK, DK, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (ok && p.w_mode != GDN_QDQ_NONE && DK == 128)
+      ok = make_map(&prm.tm_wc_sw, CU_TENSOR_MAP_DATA_TYPE_UINT8, prm.w_codes, (uint64_t)d.Hv * DK,
+                    tok, (uint64_t)d.Hv * DK, DK, 64, CU_TENSOR_MAP_SWIZZLE_128B);
     if (ok && p.state_mode != GDN_QDQ_NONE)
       ok = make_map(&prm.tm_hc, CU_TENSOR_MAP_DATA_TYPE_UINT8, prm.h_codes, (uint64_t)d.Dv,
                     (uint64_t)d.n_slots * d.Hv * DK, (uint64_t)d.Dv, 64, DK,
