@@ -239,6 +239,10 @@ def split_ctx(ctx: torch.Tensor, p: GdnProblem):
     n = ns * Hv * 5 * 64
     out["chunk_vectors"] = ctx[off:off + 4 * n].view(torch.float32).view(ns, Hv, 5, 64)
     off = al(off + 4 * n)
+    for name in ("t_img", "gkk_img", "p_img"):   # bf16 64x64 tiles as swizzled images
+        n = ns * Hv * 64 * 64
+        out[name] = ctx[off:off + 2 * n].view(torch.bfloat16).view(ns, Hv, 64 * 64)
+        off = al(off + 2 * n)
     if p.state_mode != 0:
         n = ns * Hv * Dk * Dv
         out["h_codes"] = ctx[off:off + n].view(ns, Hv, Dk, Dv)

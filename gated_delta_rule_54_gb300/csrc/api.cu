@@ -42,6 +42,12 @@ CtxLayout ctx_layout(const gdn_problem& p) {
   }
   L.cvec = off;
   off = align256(off + sizeof(float) * (size_t)d.n_slots * d.Hv * kCvecFloats);
+  L.tb = off;
+  off = align256(off + (size_t)d.n_slots * d.Hv * kTileImgBytes);
+  L.gkk = off;
+  off = align256(off + (size_t)d.n_slots * d.Hv * kTileImgBytes);
+  L.pb = off;
+  off = align256(off + (size_t)d.n_slots * d.Hv * kTileImgBytes);
   const size_t per_slot = (size_t)d.n_slots * d.Hv * d.Dk * d.Dv;
   if (p.state_mode != GDN_QDQ_NONE) {
     L.h_codes = off;

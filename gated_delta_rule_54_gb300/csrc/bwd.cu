@@ -48,6 +48,9 @@ struct BwdParams {
   const uint8_t* h_codes;
   const float* h_scales;
   const float* h_full;
+  const float* w_full;                          // fp32 W (W site off)
+  const float* cvec;                            // [n_slots, Hv, kCvecFloats] chunk vectors
+  const __nv_bfloat16 *tb, *gkk, *pb;           // [n_slots, Hv] tile images of T, Gamma o KK^T, P
   float* dq;
   float* dk;
   float* dv;
@@ -96,39 +99,11 @@ __device__ __forceinline__ void load_rows_bf16(__nv_bfloat16* dst, const __nv_bf
   }
 }
 
-__device__ __forceinline__ void load_col_f32(float* dst, const float* src, int64_t stride, int L) {
-  if (threadIdx.x < kChunk) {
-    const int r = threadIdx.x;
-    const bool ok = r < L;
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(smem_u32(dst + r)),
-                 "l"(src + (ok ? r : 0) * stride), "r"(ok ? 4 : 0));
-  }
-}
-
-// gamma / decay vectors of a chunk from g (warp 0).  gam[i] = cumsum(g)[i];
-// eg = e^gamma; dec = e^{gamma_63 - gamma}; beg = beta e^gamma.
-__device__ __forceinline__ void chunk_vectors(const float* gs, const float* bs, float* gam,
-                                              float* eg, float* dec, float* beg, int lane) {
-  const float g0 = gs[2 * lane], g1 = gs[2 * lane + 1];
-  float s = g0 + g1;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const float y = __shfl_up_sync(0xffffffffu, s, o);
-    if (lane >= o) s += y;
-  }
-  const float gL = __shfl_sync(0xffffffffu, s, 31);
-  const float a0 = s - g1, a1 = s;
-  gam[2 * lane] = a0;
-  gam[2 * lane + 1] = a1;
-  const float e0 = expf(a0), e1 = expf(a1);
-  eg[2 * lane] = e0;
-  eg[2 * lane + 1] = e1;
-  dec[2 * lane] = expf(gL - a0);
-  dec[2 * lane + 1] = expf(gL - a1);
-  if (bs) {
-    beg[2 * lane] = bs[2 * lane] * e0;
-    beg[2 * lane + 1] = bs[2 * lane + 1] * e1;
-  }
+// a contiguous block of `bytes` (multiple of 16) into shared memory
+__device__ __forceinline__ void load_block(void* dst, const void* src, int bytes) {
+  for (int i = threadIdx.x; i < bytes / 16; i += kThreads)
+    cp_async16(smem_u32(static_cast<unsigned char*>(dst) + 16 * i),
+               static_cast<const unsigned char*>(src) + 16 * i, 16);
 }
 
 template <int MODE>
@@ -146,24 +121,21 @@ struct ScanSmem {
   static constexpr int K = 0;                            // 2 buffers
   static constexpr int Q = K + 2 * kTileK;               // 2 buffers
   static constexpr int DO = Q + 2 * kTileK;              // 2 buffers [64][64]
-  static constexpr int WU8 = DO + 2 * kTile64;           // 2 buffers u8 [64][DK]
-  static constexpr int BG = WU8 + 2 * kChunk * DK;       // 2 x (beta[64], g[64])
-  static constexpr int VEC = BG + 2 * 512;               // gam, eg, dec, beg
-  static constexpr int WV = VEC + 4 * 256;               // W^ codes (or W) bf16 [64][DK]
-  static constexpr int PB = WV + kTileK;                 // P bf16 [64][64]
-  static constexpr int EDO = PB + kTile64;               // e^gamma dO bf16
+  static constexpr int PB = DO + 2 * kTile64;            // 2 buffers: P tile images (forward)
+  static constexpr int WU8 = PB + 2 * kTile64;           // 2 buffers u8 [64][DK] (W site on)
+  static constexpr int CV = WU8 + 2 * kChunk * DK;       // 2 buffers: chunk vectors (forward)
+  static constexpr int WV = CV + 2 * kCvecFloats * 4;    // W^ codes (or W) bf16 [64][DK]
+  static constexpr int EDO = WV + kTileK;                // e^gamma dO bf16
   static constexpr int DD = EDO + kTile64;               // dDelta bf16
   static constexpr int DH = DD + kTile64;                // dH bf16 [DK][64]
-  static constexpr int AS = DH + DK * 64 * 2;            // f32 [64][64] (W recompute only)
-  static constexpr int TS = AS + (WM == GDN_QDQ_NONE ? kF32Tile : 0);
-  static constexpr int TW = TS + (WM == GDN_QDQ_NONE ? kF32Tile : 0);
-  static constexpr int BYTES = TW + (WM == GDN_QDQ_NONE ? kTile64 : 0);
+  static constexpr int BYTES = DH + DK * 64 * 2;
   static_assert(BYTES <= 232448, "shared memory budget");
 };
 
 template <int DK, int WM>
 __device__ __forceinline__ void scan_load(const BwdParams& p, unsigned char* sm, int buf,
-                                          int64_t ctok, int Lc, int hk, int h, int vb) {
+                                          int64_t ctok, int Lc, int hk, int h, int vb,
+                                          int64_t slot) {
   using S = ScanSmem<DK, WM>;
   load_rows_bf16<DK>(reinterpret_cast<__nv_bfloat16*>(sm + S::K + buf * S::kTileK),
                      p.k + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
@@ -171,8 +143,10 @@ __device__ __forceinline__ void scan_load(const BwdParams& p, unsigned char* sm,
                      p.q + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
   load_rows_bf16<64>(reinterpret_cast<__nv_bfloat16*>(sm + S::DO + buf * S::kTile64),
                      p.dO + (ctok * p.Hv + h) * p.Dv + vb * 64, (int64_t)p.Hv * p.Dv, Lc);
-  float* bg = reinterpret_cast<float*>(sm + S::BG + buf * 512);
-  load_col_f32(bg + 64, p.g + ctok * p.Hv + h, p.Hv, Lc);
+  load_block(sm + S::PB + buf * S::kTile64, p.pb + (slot * p.Hv + h) * (kTileImgBytes / 2),
+             kTileImgBytes);
+  load_block(sm + S::CV + buf * kCvecFloats * 4, p.cvec + (slot * p.Hv + h) * kCvecFloats,
+             kCvecFloats * 4);
   if constexpr (WM != GDN_QDQ_NONE) {
     uint8_t* wu = sm + S::WU8 + buf * kChunk * DK;
     constexpr int CPR = DK / 16;
@@ -182,8 +156,6 @@ __device__ __forceinline__ void scan_load(const BwdParams& p, unsigned char* sm,
       cp_async16(smem_u32(wu + r * DK + c * 16),
                  p.w_codes + ((ctok + (ok ? r : 0)) * p.Hv + h) * DK + c * 16, ok ? 16 : 0);
     }
-  } else {
-    load_col_f32(bg, p.beta + ctok * p.Hv + h, p.Hv, Lc);
   }
 }
 
@@ -198,12 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const BwdPara
   const SeqInfo si = seq_info(p, n);
   const int nch = (si.L + kChunk - 1) / kChunk;
 
-  float* gam = reinterpret_cast<float*>(sm + S::VEC);
-  float* eg = gam + 64;
-  float* dec = gam + 128;
-  float* beg = gam + 192;
   __nv_bfloat16* Wv = reinterpret_cast<__nv_bfloat16*>(sm + S::WV);
-  __nv_bfloat16* Pb = reinterpret_cast<__nv_bfloat16*>(sm + S::PB);
   __nv_bfloat16* EdO = reinterpret_cast<__nv_bfloat16*>(sm + S::EDO);
   __nv_bfloat16* dDb = reinterpret_cast<__nv_bfloat16*>(sm + S::DD);
   __nv_bfloat16* dHb = reinterpret_cast<__nv_bfloat16*>(sm + S::DH);
@@ -229,13 +196,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const BwdPara
 
   if (nch > 0) {
     const int c = nch - 1;
-    scan_load<DK, WM>(p, sm, 0, si.tok0 + (int64_t)c * kChunk, si.L - c * kChunk, hk, h, vb);
+    scan_load<DK, WM>(p, sm, 0, si.tok0 + (int64_t)c * kChunk, si.L - c * kChunk, hk, h, vb,
+                      si.slot0 + c);
   }
   cp_async_commit();
   if (nch > 1) {
     const int c = nch - 2;
     scan_load<DK, WM>(p, sm, 1, si.tok0 + (int64_t)c * kChunk, min(si.L - c * kChunk, kChunk), hk,
-                      h, vb);
+                      h, vb, si.slot0 + c);
   }
   cp_async_commit();
 
@@ -248,11 +216,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const BwdPara
     const __nv_bfloat16* Ks = reinterpret_cast<const __nv_bfloat16*>(sm + S::K + buf * S::kTileK);
     const __nv_bfloat16* Qs = reinterpret_cast<const __nv_bfloat16*>(sm + S::Q + buf * S::kTileK);
     const __nv_bfloat16* dOs = reinterpret_cast<const __nv_bfloat16*>(sm + S::DO + buf * S::kTile64);
-    const float* bg = reinterpret_cast<const float*>(sm + S::BG + buf * 512);
+    const __nv_bfloat16* Pb = reinterpret_cast<const __nv_bfloat16*>(sm + S::PB + buf * S::kTile64);
+    const float* cv = reinterpret_cast<const float*>(sm + S::CV + buf * kCvecFloats * 4);
+    const float* eg = cv + kCvEg;
+    const float* dec = cv + kCvDec;
+    const int Lc = min(si.L - c * kChunk, kChunk);
     cp_async_wait<1>();
     __syncthreads();
 
-    if (warp == 0) chunk_vectors(bg + 64, WM == GDN_QDQ_NONE ? bg : nullptr, gam, eg, dec, beg, lane);
     // current dH (gradient w.r.t. the state after this chunk) -> bf16 tile
 #pragma unroll
     for (int nt = 0; nt < NTH; ++nt)
@@ -264,12 +235,23 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const BwdPara
     float sW = 1.f;
     if constexpr (WM != GDN_QDQ_NONE) {
       const uint8_t* wu = sm + S::WU8 + buf * kChunk * DK;
-      for (int e = threadIdx.x; e < kChunk * DK / 2; e += kThreads) {
-        const int r = (2 * e) / DK, col = (2 * e) % DK;
-        st_bf16x2(Wv + swz<DK>(r, col), code_val<WM>(wu[r * DK + col]),
-                  code_val<WM>(wu[r * DK + col + 1]));
+      for (int e = threadIdx.x; e < kChunk * DK / 4; e += kThreads) {
+        const int r = (4 * e) / DK, col = (4 * e) % DK;
+        const float4 v = qdq_code4_values<WM>(*reinterpret_cast<const uint32_t*>(wu + r * DK + col));
+        *reinterpret_cast<uint2*>(Wv + swz<DK>(r, col)) =
+            make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
       }
       sW = p.w_scales[slot * p.Hv + h];
+    } else {
+      // W from the forward's fp32 copy (rows >= Lc zero)
+      const int64_t ctok = si.tok0 + (int64_t)c * kChunk;
+      for (int e = threadIdx.x; e < kChunk * DK / 4; e += kThreads) {
+        const int r = (4 * e) / DK, col = (4 * e) % DK;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (r < Lc) x = *reinterpret_cast<const float4*>(p.w_full + ((ctok + r) * p.Hv + h) * DK + col);
+        *reinterpret_cast<uint2*>(Wv + swz<DK>(r, col)) =
+            make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
+      }
     }
     __syncthreads();
 
@@ -279,68 +261,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const BwdPara
       const uint4 val = *reinterpret_cast<const uint4*>(dHb + d * 64 + ((c8 ^ (d & 7)) << 3));
       *reinterpret_cast<uint4*>(p.ws_dh + ((slot * p.Hv + h) * DK + d) * p.Dv + vb * 64 + c8 * 8) = val;
     }
-    // P = lower-incl(Gamma QK^T) and e^gamma dO
-    if (cq <= rt) {
-      float acc[2][4];
-      zero_acc(acc);
-      wgemm<2, false, false, DK, DK>(acc, Qs, row0, Ks, col0, 0, DK, lane);
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-          const float x0 = (j <= i) ? expf(gam[i] - gam[j]) * acc[nt][2 * e2] : 0.f;
-          const float x1 = (j + 1 <= i) ? expf(gam[i] - gam[j + 1]) * acc[nt][2 * e2 + 1] : 0.f;
-          st_bf16x2(Pb + swz<64>(i, j), x0, x1);
-        }
-    }
+    // e^gamma dO
     for (int e = threadIdx.x; e < kChunk * 32; e += kThreads) {
       const int r = e >> 5, col = (e & 31) * 2;
       const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(dOs + swz<64>(r, col));
       const float er = eg[r];
       st_bf16x2(EdO + swz<64>(r, col), er * __bfloat162float(v2.x), er * __bfloat162float(v2.y));
-    }
-    if constexpr (WM == GDN_QDQ_NONE) {
-      // recompute W = T diag(beta e^gamma) K (bf16 operands)
-      float* As = reinterpret_cast<float*>(sm + S::AS);
-      float* Ts = reinterpret_cast<float*>(sm + S::TS);
-      __nv_bfloat16* Tw = reinterpret_cast<__nv_bfloat16*>(sm + S::TW);
-      const float* bs = bg;
-      if (cq <= rt) {
-        float acc[2][4];
-        zero_acc(acc);
-        wgemm<2, false, false, DK, DK>(acc, Ks, row0, Ks, col0, 0, DK, lane);
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int i = row0 + gq + 8 * (e >> 1), j = col0 + nt * 8 + 2 * tq + (e & 1);
-            As[i * kSA + j] = (j < i) ? bs[i] * expf(gam[i] - gam[j]) * acc[nt][e] : 0.f;
-          }
-      }
-      __syncthreads();
-      solve_unit_lower64<kThreads>(As, Ts);
-      for (int e = threadIdx.x; e < 64 * 32; e += kThreads) {
-        const int i = e >> 5, j = (e & 31) * 2;
-        const float t0 = (j <= i) ? Ts[i * kSA + j] * beg[j] : 0.f;
-        const float t1 = (j + 1 <= i) ? Ts[i * kSA + j + 1] * beg[j + 1] : 0.f;
-        st_bf16x2(Tw + swz<64>(i, j), t0, t1);
-      }
-      __syncthreads();
-      {
-        constexpr int NTW = DK / 32;
-        const int wcol0 = cq * (DK / 4);
-        float acc[NTW][4];
-        zero_acc(acc);
-        wgemm<NTW, false, true, 64, DK>(acc, Tw, row0, Ks, wcol0, 0, 64, lane);
-#pragma unroll
-        for (int nt = 0; nt < NTW; ++nt)
-#pragma unroll
-          for (int e2 = 0; e2 < 2; ++e2) {
-            const int i = row0 + gq + 8 * e2, col = wcol0 + nt * 8 + 2 * tq;
-            st_bf16x2(Wv + swz<DK>(i, col), acc[nt][2 * e2], acc[nt][2 * e2 + 1]);
-          }
-      }
     }
     __syncthreads();
 
@@ -380,7 +306,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const BwdPara
     __syncthreads();
     if (it + 2 < nch) {
       const int c2 = c - 2;
-      scan_load<DK, WM>(p, sm, buf, si.tok0 + (int64_t)c2 * kChunk, kChunk, hk, h, vb);
+      scan_load<DK, WM>(p, sm, buf, si.tok0 + (int64_t)c2 * kChunk, kChunk, hk, h, vb,
+                        si.slot0 + c2);
     }
     cp_async_commit();
   }
@@ -413,20 +340,18 @@ struct ChunkSmem {
   static constexpr int WV = DO + kTile64;          // W^ values bf16 [64][DK] -> later dW
   static constexpr int HH = WV + kTileK;           // H^ values bf16 [DK][64] -> later dT, X, dKK
   static constexpr int DHP = HH + DK * 64 * 2;     // dH' bf16 [DK][64]
-  static constexpr int AS = DHP + DK * 64 * 2;     // f32 [64][kSA]: A (lower), solve scratch (upper)
-  static constexpr int TS = AS + kF32Tile;         // f32 [64][kSA]: T; u8 code staging before that
-  static constexpr int GKK = TS + kF32Tile;        // bf16 Gamma KK (strict lower)
-  static constexpr int PB = GKK + kTile64;         // bf16 P
-  static constexpr int TB = PB + kTile64;          // bf16 T
+  static constexpr int GKK = DHP + DK * 64 * 2;    // bf16 Gamma KK (strict lower; forward's image)
+  static constexpr int PB = GKK + kTile64;         // bf16 P (forward's image)
+  static constexpr int TB = PB + kTile64;          // bf16 T (forward's image)
   static constexpr int TU = TB + kTile64;          // bf16 T diag(beta) -> later Gm
   static constexpr int DB = TU + kTile64;          // bf16 Delta
   static constexpr int DDB = DB + kTile64;         // bf16 dDelta
-  static constexpr int VEC = DDB + kTile64;        // gam, eg, dec, bet, beg, bg staging (2 x 64)
-  static constexpr int RACC = VEC + 7 * 256;       // per-row partial sums [kSlots][64] + 8 scalars
+  static constexpr int VEC = DDB + kTile64;        // chunk vectors (forward)
+  static constexpr int RACC = VEC + kCvecFloats * 4;  // per-row partial sums [kSlots][64] + 8 scalars
   static constexpr int kSlots = 36;
   static constexpr int BYTES = RACC + kSlots * 256 + 4 * (16 + 2);
   static_assert(BYTES <= 232448, "shared memory budget");
-  static_assert(2 * kChunk * DK <= 32768, "code staging fits in As + Ts");
+  static_assert(kChunk * DK <= kTile64 && DK * 64 <= kTile64, "code staging fits in Delta, dDelta");
 };
 
 // racc slot indices (each a [64] row of partial sums; written exactly once)
@@ -518,8 +443,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
   __nv_bfloat16* dTb = Hh;                 // after the H^ / dH' products
   __nv_bfloat16* Xb = Hh + kChunk * 64;
   __nv_bfloat16* dKKb = dHp;
-  float* As = reinterpret_cast<float*>(sm + S::AS);
-  float* Ts = reinterpret_cast<float*>(sm + S::TS);
   __nv_bfloat16* GKKb = reinterpret_cast<__nv_bfloat16*>(sm + S::GKK);
   __nv_bfloat16* Pb = reinterpret_cast<__nv_bfloat16*>(sm + S::PB);
   __nv_bfloat16* Tb = reinterpret_cast<__nv_bfloat16*>(sm + S::TB);
@@ -529,23 +452,27 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
   __nv_bfloat16* dDb = reinterpret_cast<__nv_bfloat16*>(sm + S::DDB);
   uint8_t* wst = reinterpret_cast<uint8_t*>(sm + S::DB);   // W codes [64][DK], until Delta
   uint8_t* hst = reinterpret_cast<uint8_t*>(sm + S::DDB);  // H codes [DK][64], until dDelta
-  float* gam = reinterpret_cast<float*>(sm + S::VEC);
-  float* eg = gam + 64;
-  float* dec = gam + 128;
-  float* bet = gam + 192;
-  float* beg = gam + 256;
-  float* gs = gam + 320;   // g staging
-  float* bsg = gam + 384;  // beta staging
+  const float* cvs = reinterpret_cast<const float*>(sm + S::VEC);
+  const float* gam = cvs + kCvGam;
+  const float* eg = cvs + kCvEg;
+  const float* dec = cvs + kCvDec;
+  const float* bet = cvs + kCvBet;
+  const float* beg = cvs + kCvBeg;
   float* racc = reinterpret_cast<float*>(sm + S::RACC);
   float* hd_part = racc + S::kSlots * 64;  // [kWarps] <H^, dH'> partials, then [2] sums of t_i
 
-  // ---- loads: group 1 (needed first) and group 2 (needed after the solve) ----
+  // ---- loads (T, Gamma o KK^T, P and the chunk vectors come from the forward) ----
   load_rows_bf16<DK>(Ks, p.k + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
   load_rows_bf16<DK>(Qs, p.q + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
   load_rows_bf16<64>(Vs, p.v + (ctok * p.Hv + h) * p.Dv + vb * 64, (int64_t)p.Hv * p.Dv, Lc);
   load_rows_bf16<64>(dOs, p.dO + (ctok * p.Hv + h) * p.Dv + vb * 64, (int64_t)p.Hv * p.Dv, Lc);
-  load_col_f32(gs, p.g + ctok * p.Hv + h, p.Hv, Lc);
-  load_col_f32(bsg, p.beta + ctok * p.Hv + h, p.Hv, Lc);
+  {
+    const int64_t img = (slot * p.Hv + h) * (kTileImgBytes / 2);
+    load_block(Tb, p.tb + img, kTileImgBytes);
+    load_block(GKKb, p.gkk + img, kTileImgBytes);
+    load_block(Pb, p.pb + img, kTileImgBytes);
+    load_block(sm + S::VEC, p.cvec + (slot * p.Hv + h) * kCvecFloats, kCvecFloats * 4);
+  }
   cp_async_commit();
   {  // dH' [DK][64] bf16 from the workspace (always a full tile)
     const __nv_bfloat16* src = p.ws_dh + ((slot * p.Hv + h) * DK) * p.Dv + vb * 64;
@@ -571,55 +498,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
     }
   }
   cp_async_commit();
-  cp_async_wait<1>();
-  __syncthreads();
-
-  // ---- chunk vectors ----
-  if (warp == 0) chunk_vectors(gs, bsg, gam, eg, dec, beg, lane);
-  if (threadIdx.x < 64) bet[threadIdx.x] = bsg[threadIdx.x];
-  __syncthreads();
-
-  // ---- KK^T -> A (f32) and Gamma KK (bf16); QK^T -> P (bf16) ----
-  {
-    const int row0 = rt * 16, col0 = ch * 16;
-    if (ch <= rt) {
-      float akk[2][4], aqk[2][4];
-      zero_acc(akk);
-      zero_acc(aqk);
-      wgemm<2, false, false, DK, DK>(akk, Ks, row0, Ks, col0, 0, DK, lane);
-      wgemm<2, false, false, DK, DK>(aqk, Qs, row0, Ks, col0, 0, DK, lane);
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-          const float x0 = (j <= i) ? expf(gam[i] - gam[j]) : 0.f;
-          const float x1 = (j + 1 <= i) ? expf(gam[i] - gam[j + 1]) : 0.f;
-          const float gk0 = (j < i) ? x0 * akk[nt][2 * e2] : 0.f;
-          const float gk1 = (j + 1 < i) ? x1 * akk[nt][2 * e2 + 1] : 0.f;
-          As[i * kSA + j] = bet[i] * gk0;
-          As[i * kSA + j + 1] = bet[i] * gk1;
-          st_bf16x2(GKKb + swz<64>(i, j), gk0, gk1);
-          st_bf16x2(Pb + swz<64>(i, j), x0 * aqk[nt][2 * e2], x1 * aqk[nt][2 * e2 + 1]);
-        }
-    } else {
-      // strictly-upper tiles of GKK and P are read by the transposed products
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-          st_bf16x2(GKKb + swz<64>(i, j), 0.f, 0.f);
-          st_bf16x2(Pb + swz<64>(i, j), 0.f, 0.f);
-        }
-    }
-  }
-  __syncthreads();
-
-  // ---- a3: T = (I + A)^-1 ----
-  solve_unit_lower64<kThreads>(As, Ts);
   cp_async_wait<0>();
-  __syncthreads();  // group 2 (dH', W codes, H codes) visible to all threads
+  __syncthreads();  // every load visible to all threads
 
   // ---- dequantized operands (4 codes per step), <H^, dH'>, and T / Tu in bf16 ----
   if constexpr (WM != GDN_QDQ_NONE) {
@@ -660,41 +540,23 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
     for (int o = 16; o > 0; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
     if (lane == 0) hd_part[warp] = hd;
   }
+  if constexpr (WM == GDN_QDQ_NONE) {
+    // W from the forward's fp32 copy (rows >= Lc zero)
+    for (int e = threadIdx.x; e < kChunk * DK / 4; e += kThreads) {
+      const int r = (4 * e) / DK, col = (4 * e) % DK;
+      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (r < Lc) x = *reinterpret_cast<const float4*>(p.w_full + ((ctok + r) * p.Hv + h) * DK + col);
+      *reinterpret_cast<uint2*>(Wv + swz<DK>(r, col)) =
+          make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
+    }
+  }
   for (int e = threadIdx.x; e < 64 * 32; e += kThreads) {
     const int i = e >> 5, j = (e & 31) * 2;
-    const float t0 = (j <= i) ? Ts[i * kSA + j] : 0.f;
-    const float t1 = (j + 1 <= i) ? Ts[i * kSA + j + 1] : 0.f;
-    st_bf16x2(Tb + swz<64>(i, j), t0, t1);
-    if constexpr (WM == GDN_QDQ_NONE)
-      st_bf16x2(Tub + swz<64>(i, j), t0 * beg[j], t1 * beg[j + 1]);
-    else
-      st_bf16x2(Tub + swz<64>(i, j), t0 * bet[j], t1 * bet[j + 1]);
+    const __nv_bfloat162 t2 = *reinterpret_cast<const __nv_bfloat162*>(Tb + swz<64>(i, j));
+    st_bf16x2(Tub + swz<64>(i, j), __bfloat162float(t2.x) * bet[j],
+              __bfloat162float(t2.y) * bet[j + 1]);
   }
   __syncthreads();
-  if constexpr (WM == GDN_QDQ_NONE) {
-    // W = (T diag(beta e^gamma)) K, then Tu = T diag(beta) in the same buffer
-    constexpr int NTW = DK / 32;
-    const int row0 = rt * 16, col0 = ch * (DK / 4);
-    float acc[NTW][4];
-    zero_acc(acc);
-    wgemm<NTW, false, true, 64, DK>(acc, Tub, row0, Ks, col0, 0, 64, lane);
-#pragma unroll
-    for (int nt = 0; nt < NTW; ++nt)
-#pragma unroll
-      for (int e2 = 0; e2 < 2; ++e2) {
-        const int i = row0 + gq + 8 * e2, col = col0 + nt * 8 + 2 * tq;
-        st_bf16x2(Wv + swz<DK>(i, col), acc[nt][2 * e2], acc[nt][2 * e2 + 1]);
-      }
-    __syncthreads();
-    for (int e = threadIdx.x; e < 64 * 32; e += kThreads) {
-      const int i = e >> 5, j = (e & 31) * 2;
-      const float t0 = (j <= i) ? Ts[i * kSA + j] : 0.f;
-      const float t1 = (j + 1 <= i) ? Ts[i * kSA + j + 1] : 0.f;
-      st_bf16x2(Tub + swz<64>(i, j), t0 * bet[j], t1 * bet[j + 1]);
-    }
-    __syncthreads();
-  }
-
   // ---- Delta = Tu V - W^ H^;  dDelta = scale P^T dO + dec (K dH') ----
   {
     const int row0 = rt * 16, col0 = ch * 16;
@@ -926,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
           const float gkk = __bfloat162float(GKKb[swz<64>(i, jj)]);
           kk[e] = da * bet[i] * ((jj < i) ? expf(gam[i] - gam[jj]) : 0.f);
           ba[nt][2 * e2 + e] = da * gkk;
-          aa[nt][2 * e2 + e] = da * As[i * kSA + jj] * ((jj < i) ? 1.f : 0.f);
+          aa[nt][2 * e2 + e] = da * bet[i] * gkk;  // A = diag(beta) (Gamma o KK^T), strictly lower
         }
         st_bf16x2(dKKb + swz<64>(i, j), kk[0], kk[1]);
       }
@@ -1131,6 +993,11 @@ gdn_status launch_bwd(const gdn_problem& p, const Dims& d, const void* q, const 
   } else {
     prm.h_full = reinterpret_cast<const float*>(base + L.h_full);
   }
+  if (p.w_mode == GDN_QDQ_NONE) prm.w_full = reinterpret_cast<const float*>(base + L.w_full);
+  prm.cvec = reinterpret_cast<const float*>(base + L.cvec);
+  prm.tb = reinterpret_cast<const __nv_bfloat16*>(base + L.tb);
+  prm.gkk = reinterpret_cast<const __nv_bfloat16*>(base + L.gkk);
+  prm.pb = reinterpret_cast<const __nv_bfloat16*>(base + L.pb);
   prm.dq = dq;
   prm.dk = dk;
   prm.dv = dv;

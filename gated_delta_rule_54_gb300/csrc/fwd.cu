@@ -67,6 +67,7 @@ struct FwdParams {
   float* h_scales;
   float* h_full;
   float* cvec;  // [n_slots, Hv, kCvecFloats] chunk vectors
+  __nv_bfloat16 *tb, *gkk, *pb;  // [n_slots, Hv] 8 KiB tile images for the backward
   const int32_t* cu_seqlens;
   int64_t T;
   int Hk, Hv, Dv, G, N;
@@ -264,16 +265,26 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __g
   zero_acc(acc);
   if (a_tile) wgemm<4, false, false, DK, DK>(acc, Ks, row0, Ks, col0, 0, DK, lane);
   __syncthreads();
-  if (a_tile) {
+  {
+    // Gamma o KK^T (strictly lower; rows >= L hold another sequence's keys: zero)
+    // as the backward's tile image, and A = diag(beta) (Gamma o KK^T)
+    __nv_bfloat16* gimg = p.gkk + (slot * p.Hv + h) * (kTileImgBytes / 2);
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-        const float gi = gam[i], bi = bet[i];
-        const float a0 = (j < i) ? bi * expf(gi - gam[j]) * acc[nt][2 * e2] : 0.f;
-        const float a1 = (j + 1 < i) ? bi * expf(gi - gam[j + 1]) * acc[nt][2 * e2 + 1] : 0.f;
-        *reinterpret_cast<float2*>(As + i * kSA + j) = make_float2(a0, a1);
+        float k0 = 0.f, k1 = 0.f;
+        if (a_tile && i < L) {
+          const float gi = gam[i];
+          k0 = (j < i) ? expf(gi - gam[j]) * acc[nt][2 * e2] : 0.f;
+          k1 = (j + 1 < i) ? expf(gi - gam[j + 1]) * acc[nt][2 * e2 + 1] : 0.f;
+        }
+        st_bf16x2(gimg + swz<64>(i, j), k0, k1);
+        if (a_tile) {
+          const float bi = bet[i];
+          *reinterpret_cast<float2*>(As + i * kSA + j) = make_float2(bi * k0, bi * k1);
+        }
       }
   }
   __syncthreads();
@@ -281,12 +292,15 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __g
   // ---- a3: T = (I + A)^-1 ----
   solve_unit_lower64<kPrepThreads>(As, Ts);
 
-  // ---- a4 operands: Tw = T diag(beta e^gamma), Tu = T diag(beta), split hi/lo ----
+  // ---- a4 operands: Tw = T diag(beta e^gamma), Tu = T diag(beta), split hi/lo;
+  //      T itself as the backward's tile image ----
+  __nv_bfloat16* timg = p.tb + (slot * p.Hv + h) * (kTileImgBytes / 2);
   for (int e = threadIdx.x; e < 64 * 32; e += kPrepThreads) {
     const int i = e >> 5, j = (e & 31) * 2;
     const float2 tt = *reinterpret_cast<const float2*>(Ts + i * kSA + j);
     const float t0 = (j <= i) ? tt.x : 0.f;
     const float t1 = (j + 1 <= i) ? tt.y : 0.f;
+    st_bf16x2(timg + swz<64>(i, j), t0, t1);
     float a0, a1, b0, b1;
     split_bf16(t0 * beg[j], a0, b0);
     split_bf16(t1 * beg[j + 1], a1, b1);
@@ -932,6 +946,8 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
   __syncthreads();  // K reads done (its tile becomes Delta)
 
   const float sWH = (WM != GDN_QDQ_NONE ? sW : 1.f) * (SM != GDN_QDQ_NONE ? sH : 1.f);
+  // value block 0 also saves P (bf16; rows >= L zero) as the backward's tile image
+  __nv_bfloat16* pimg = vb == 0 ? p.pb + (slot * p.Hv + h) * (kTileImgBytes / 2) : nullptr;
 #pragma unroll
   for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
@@ -946,6 +962,9 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
         split_bf16(p1, h1v, l1v);
         st_bf16x2(PH + swz<64>(i, j), h0v, h1v);
         st_bf16x2(PL + swz<64>(i, j), l0v, l1v);
+        if (pimg) st_bf16x2(pimg + swz<64>(i, j), i < L ? p0 : 0.f, i < L ? p1 : 0.f);
+      } else if (pimg) {
+        st_bf16x2(pimg + swz<64>(i, j), 0.f, 0.f);
       }
       float2 u = *reinterpret_cast<const float2*>(Us + swz_f32(i, j));
       if (i >= L) u = make_float2(0.f, 0.f);
@@ -1113,6 +1132,9 @@ gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const 
     prm.w_full = reinterpret_cast<float*>(base + L.w_full);
   }
   prm.cvec = reinterpret_cast<float*>(base + L.cvec);
+  prm.tb = reinterpret_cast<__nv_bfloat16*>(base + L.tb);
+  prm.gkk = reinterpret_cast<__nv_bfloat16*>(base + L.gkk);
+  prm.pb = reinterpret_cast<__nv_bfloat16*>(base + L.pb);
   if (p.state_mode != GDN_QDQ_NONE) {
     prm.h_codes = base + L.h_codes;
     prm.h_scales = reinterpret_cast<float*>(base + L.h_scales);

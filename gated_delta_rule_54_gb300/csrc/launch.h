@@ -12,6 +12,10 @@ constexpr int kChunkLen = 64;  // chunk length and state-scale tile width
 // per (chunk, value head) vectors the forward's chunk prep saves in the
 // context: gamma, e^gamma, e^{gamma_L - gamma}, beta, beta e^gamma (64 each)
 constexpr int kCvecFloats = 5 * 64;
+// bf16 [64][64] chunk tiles the forward saves for the backward, each stored as
+// the 8 KiB shared-memory image (64-column swizzled rows): T = (I + A)^-1,
+// Gamma o KK^T (strictly lower), P = Gamma o QK^T (lower incl. diagonal)
+constexpr int kTileImgBytes = 64 * 64 * 2;
 
 // Derived sizes of a validated problem.
 struct Dims {
@@ -22,7 +26,7 @@ struct Dims {
 
 // Byte offsets of the saved context segments (see gdn_ctx_bytes).
 struct CtxLayout {
-  size_t w_codes, w_scales, w_full, cvec, h_codes, h_scales, h_full, total;
+  size_t w_codes, w_scales, w_full, cvec, tb, gkk, pb, h_codes, h_scales, h_full, total;
 };
 
 Dims dims_of(const gdn_problem& p);

@@ -123,6 +123,12 @@ int64_t gdn_num_chunk_slots(const gdn_problem* p);
  *                                       g), e^gamma, e^{gamma_L - gamma}, beta,
  *                                       beta e^gamma (rows past the chunk end:
  *                                       gamma flat, beta 0)
+ *   t_img     bf16 [n_slots, Hv, 4096]  T = (I + A)^-1 (lower incl. diagonal)
+ *   gkk_img   bf16 [n_slots, Hv, 4096]  Gamma o KK^T (strictly lower)
+ *   p_img     bf16 [n_slots, Hv, 4096]  P = Gamma o QK^T (lower incl. diagonal)
+ *             each 64 x 64 tile stored as its shared-memory image: element
+ *             (i, j) at i * 64 + 8 * ((j / 8) ^ (i % 8)) + j % 8; rows past
+ *             the chunk end are zero (T: identity rows)
  *   h_codes   u8  [n_slots, Hv, Dk, Dv] state codes entering each chunk (state_mode != NONE)
  *   h_scales  f32 [n_slots, Hv, Dv/64]  state scale per [Dk, 64] tile  (state_mode != NONE)
  *   h_full    f32 [n_slots, Hv, Dk, Dv] unquantized state entering each chunk (state_mode == NONE)

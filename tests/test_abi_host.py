@@ -77,7 +77,7 @@ def test_sizes():
     assert lib.gdn_num_chunk_slots(ctypes.byref(p)) == 2 * nt
     al = lambda x: (x + 255) // 256 * 256
     ns = 2 * nt
-    cv = al(4 * ns * 4 * 5 * 64)
+    cv = al(4 * ns * 4 * 5 * 64) + 3 * al(ns * 4 * 64 * 64 * 2)   # chunk vectors, T / GKK / P images
     exp = al(2 * 300 * 4 * 128) + al(4 * ns * 4) + cv + al(ns * 4 * 128 * 128) + al(4 * ns * 4 * 2)
     assert lib.gdn_ctx_bytes(ctypes.byref(p)) == exp
     p0 = _problem(state_mode=0, w_mode=0)

@@ -214,3 +214,42 @@ def test_no_bounded_wait_gave_up():
     """No forward kernel of the runs above ended early on a TMA wait."""
     from gated_delta_rule_54_gb300 import _lib
     assert _lib.load().gdn_device_error(1) == 0
+
+
+def _unswizzle(img):
+    """[..., 4096] bf16 tile images -> [..., 64, 64]."""
+    i = np.arange(64)[:, None]
+    j = np.arange(64)[None, :]
+    idx = i * 64 + 8 * ((j // 8) ^ (i % 8)) + j % 8
+    return img[..., idx]
+
+
+def test_fwd_saved_backward_tiles():
+    """T, Gamma o KK^T and P saved for the backward, against the oracle's T and
+    their definitions (bf16 storage: 2^-8 relative)."""
+    from oracle.chunked import chunked
+    w = synth.small(B=1, T=150, Hk=1, Hv=2, Dk=64, Dv=64, h0=True, seed=31)
+    d = synth.make_inputs(w)
+    dd, o, ht, ctx = _gpu_fwd(d, "e4m3", "e4m3")
+    p = make_problem(dd["q"], dd["k"], dd["v"], None, 1.0, "e4m3", "e4m3")
+    seg = split_ctx(ctx, p)
+    imgs = {k: _unswizzle(seg[k].float().cpu().numpy()) for k in ("t_img", "gkk_img", "p_img")}
+    _, _, inter = chunked(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"],
+                          state_mode="e4m3", w_mode="e4m3", intermediates=True)
+    q = d["q"].double().numpy()[0, :, 0]
+    k = d["k"].double().numpy()[0, :, 0]
+    for c, st in enumerate(inter[0]):
+        L = st["T"].shape[-1]
+        sl = slice(64 * c, 64 * c + L)
+        for h in range(2):
+            gam = st["gamma"][h].numpy()
+            G = np.exp(gam[:, None] - gam[None, :])
+            kk = np.tril(G * (k[sl] @ k[sl].T), -1)
+            pp = np.tril(G * (q[sl] @ k[sl].T))
+            T = st["T"][h].numpy()
+            for name, ref in (("t_img", T), ("gkk_img", kk), ("p_img", pp)):
+                x = imgs[name][c, h]
+                assert np.abs(x[:L, :L] - ref).max() <= 2 ** -7 * np.abs(ref).max(), (name, c, h)
+                if name != "t_img":
+                    assert not x[L:].any(), (name, c, h)   # rows past the chunk end are zero
+            assert np.array_equal(imgs["t_img"][c, h, L:, L:], np.eye(64 - L))
