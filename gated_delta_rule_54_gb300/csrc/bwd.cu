@@ -461,19 +461,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
   float* racc = reinterpret_cast<float*>(sm + S::RACC);
   float* hd_part = racc + S::kSlots * 64;  // [kWarps] <H^, dH'> partials, then [2] sums of t_i
 
-  // ---- loads (T, Gamma o KK^T, P and the chunk vectors come from the forward) ----
-  load_rows_bf16<DK>(Ks, p.k + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
-  load_rows_bf16<DK>(Qs, p.q + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
-  load_rows_bf16<64>(Vs, p.v + (ctok * p.Hv + h) * p.Dv + vb * 64, (int64_t)p.Hv * p.Dv, Lc);
-  load_rows_bf16<64>(dOs, p.dO + (ctok * p.Hv + h) * p.Dv + vb * 64, (int64_t)p.Hv * p.Dv, Lc);
+  // ---- loads: group A feeds the dequantization below, group B (K, Q, V, dO,
+  //      Gamma o KK^T, P) lands meanwhile; T, Gamma o KK^T, P and the chunk
+  //      vectors come from the forward ----
   {
     const int64_t img = (slot * p.Hv + h) * (kTileImgBytes / 2);
-    load_block(Tb, p.tb + img, kTileImgBytes);
-    load_block(GKKb, p.gkk + img, kTileImgBytes);
-    load_block(Pb, p.pb + img, kTileImgBytes);
     load_block(sm + S::VEC, p.cvec + (slot * p.Hv + h) * kCvecFloats, kCvecFloats * 4);
+    load_block(Tb, p.tb + img, kTileImgBytes);
   }
-  cp_async_commit();
   {  // dH' [DK][64] bf16 from the workspace (always a full tile)
     const __nv_bfloat16* src = p.ws_dh + ((slot * p.Hv + h) * DK) * p.Dv + vb * 64;
     for (int i = threadIdx.x; i < DK * 8; i += kThreads) {
@@ -498,8 +493,18 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
     }
   }
   cp_async_commit();
-  cp_async_wait<0>();
-  __syncthreads();  // every load visible to all threads
+  load_rows_bf16<DK>(Ks, p.k + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
+  load_rows_bf16<DK>(Qs, p.q + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
+  load_rows_bf16<64>(Vs, p.v + (ctok * p.Hv + h) * p.Dv + vb * 64, (int64_t)p.Hv * p.Dv, Lc);
+  load_rows_bf16<64>(dOs, p.dO + (ctok * p.Hv + h) * p.Dv + vb * 64, (int64_t)p.Hv * p.Dv, Lc);
+  {
+    const int64_t img = (slot * p.Hv + h) * (kTileImgBytes / 2);
+    load_block(GKKb, p.gkk + img, kTileImgBytes);
+    load_block(Pb, p.pb + img, kTileImgBytes);
+  }
+  cp_async_commit();
+  cp_async_wait<1>();
+  __syncthreads();  // group A visible to all threads
 
   // ---- dequantized operands (4 codes per step), <H^, dH'>, and T / Tu in bf16 ----
   if constexpr (WM != GDN_QDQ_NONE) {
@@ -556,7 +561,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
     st_bf16x2(Tub + swz<64>(i, j), __bfloat162float(t2.x) * bet[j],
               __bfloat162float(t2.y) * bet[j + 1]);
   }
-  __syncthreads();
+  cp_async_wait<0>();
+  __syncthreads();  // group B visible; operands above complete
   // ---- Delta = Tu V - W^ H^;  dDelta = scale P^T dO + dec (K dH') ----
   {
     const int row0 = rt * 16, col0 = ch * 16;
