@@ -567,6 +567,90 @@ def decode_cpu_baseline(w, cpu, budget_s=20.0, rows=None):
 
 
 # ----------------------------------------------------------------------------
+# KDA recurrence (--mode kda)
+# ----------------------------------------------------------------------------
+KDA_METRIC = "KDA recurrent fwd tokens/s at B=4,T=4096,H=16,D=128 (state QDQ every 64 tokens); % of roofline"
+
+
+def kda_alg_bytes(w):
+    """Algorithmic HBM bytes of one KDA launch: inputs read once (g per key
+    channel), o written once, h0 read and ht written."""
+    tok = w.B * w.T
+    b = tok * (w.Hk * w.Dk * 2 * 2 + w.Hv * w.Dv * 2 + w.Hv * 4 + w.Hv * w.Dk * 4 + w.Hv * w.Dv * 4)
+    return b + w.B * w.Hv * w.Dk * w.Dv * 4 * 2
+
+
+def run_kda(args, ws, rank, local):
+    from gated_delta_rule_54_gb300 import api, synth
+    from gated_delta_rule_54_gb300._lib import load
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    load()
+    w = synth.WORKLOADS[args.workload]
+    w = synth.Workload(**{**w.__dict__, "seed": w.seed + rank})
+    cpu = synth.make_kda_inputs(w)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in cpu.items()}
+    stream = torch.cuda.current_stream(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def step():
+        api.kda_recurrent_fwd_qdq(d["q"], d["k"], d["v"], d["beta"], d["g_k"], d["h0"],
+                                  state_mode=w.state_mode)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    _barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk:
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(args.steps):
+            step()
+        b.record(stream)
+        torch.cuda.synchronize()
+    _barrier(ws)
+    ms_total = _max_over_ranks(a.elapsed_time(b), ws, dev)
+    ms_step = ms_total / args.steps
+    tokens = w.B * w.T
+    value = tokens * ws * args.steps / (ms_total / 1e3)
+    peak, peak_kind = _peaks()
+    alg = kda_alg_bytes(w)
+    achieved = alg / (ms_step / 1e3) / 1e9
+    cpu_base = None
+    if rank == 0 and not args.no_cpu_baseline:
+        from oracle.kda import kda_recurrent
+        t0 = time.time()
+        Ts = 256
+        sl = lambda x: x[:1, :Ts]
+        kda_recurrent(sl(cpu["q"]), sl(cpu["k"]), sl(cpu["v"]), sl(cpu["beta"]), sl(cpu["g_k"]),
+                      cpu["h0"][:1], state_mode=w.state_mode)
+        dt = time.time() - t0
+        cpu_base = {"value": round(Ts / dt, 2), "unit": "tokens/s", "cores": torch.get_num_threads(),
+                    "kind": "oracle",
+                    "sample": "1 sequence x %d tokens, all %d heads, fp64 KDA oracle" % (Ts, w.Hv)}
+    line = {
+        "metric": KDA_METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), beta=sigmoid, "
+                "g per key channel=-softplus(N(0,1)), h0 N(0, 0.1^2))",
+        "config": {"workload": w.name, "mode": "kda", "B": w.B, "T": w.T, "Hk": w.Hk, "Hv": w.Hv,
+                   "Dk": w.Dk, "Dv": w.Dv, "state_mode": w.state_mode, "chunk": 64, "block_v": 64,
+                   "l2": "inputs larger than L2 (no flush needed)"},
+        "clocks": clk.summary(), "e2e": None, "gpu_launches": args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "kda_recurrent_kernel", "peak_source": peak_kind,
+                     "alg_bytes_per_launch": alg, "launch_ms": round(ms_step, 4)},
+        "cpu_baseline": cpu_base,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
 # reference arm: the oracle on the host cores
 # ----------------------------------------------------------------------------
 def run_reference(args, ws, rank):
@@ -641,7 +725,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=None)
-    ap.add_argument("--mode", default=None, choices=["fwd", "fwdbwd", "decode"])
+    ap.add_argument("--mode", default=None, choices=["fwd", "fwdbwd", "decode", "kda"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
@@ -650,13 +734,15 @@ def main():
     if args.mode is None:
         args.mode = "fwdbwd" if _backward_available() else "fwd"
     if args.workload is None:
-        args.workload = "decode" if args.mode == "decode" else "layer"
+        args.workload = {"decode": "decode", "kda": "kda"}.get(args.mode, "layer")
     args.bwd_launches = BWD_LAUNCHES
     ws, rank, local = _dist()
     if args.impl == "reference":
         run_reference(args, ws, rank)
     elif args.mode == "decode":
         run_decode(args, ws, rank, local)
+    elif args.mode == "kda":
+        run_kda(args, ws, rank, local)
     else:
         run_ours(args, ws, rank, local)
     if ws > 1:

@@ -67,6 +67,7 @@ SIGNATURES = {
                                                  _P, _P, _P, _P]),
     "fake_qdq_e4m3": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
     "fake_qdq_int8": (ctypes.c_int, [_P, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
+    "kda_recurrent_fwd_qdq": (ctypes.c_int, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "gdn_decode_validate": (ctypes.c_int, [_DP]),
     "gdn_decode_qdq": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }

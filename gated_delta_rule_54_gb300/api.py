@@ -138,6 +138,27 @@ def gdn_chunk_bwd_ste(q, k, v, beta, g, ctx, do, dht=None, cu_seqlens=None, scal
     return dq, dk, dv, dbeta, dg, dh0
 
 
+def kda_recurrent_fwd_qdq(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0,
+                          state_mode="e4m3", block_v=64, chunk=64, output_final_state=True):
+    """KDA recurrence with per-key-channel decay g [B,T,Hv,Dk] f32 and the state QDQ every
+    ``chunk`` tokens.  q, k [B,T,Hk,Dk] bf16; v [B,T,Hv,Dv] bf16; beta [B,T,Hv] f32;
+    h0 [N,Hv,Dk,Dv] f32 or None.  Returns (o [B,T,Hv,Dv] f32, ht [N,Hv,Dk,Dv] f32 or None)."""
+    lib = load()
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g), ("h0", h0),
+                    ("cu_seqlens", cu_seqlens)):
+        _check_dev(name, t, dev)
+    p = make_problem(q, k, v, cu_seqlens, scale, state_mode, "none", block_v=block_v, chunk=chunk)
+    B, T, Hv, Dv = v.shape
+    o = torch.empty(B, T, Hv, Dv, device=dev, dtype=torch.float32)
+    ht = (torch.empty(p.N, Hv, k.shape[3], Dv, device=dev, dtype=torch.float32)
+          if output_final_state else None)
+    st = lib.kda_recurrent_fwd_qdq(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                   _ptr(g), _ptr(h0), _ptr(o), _ptr(ht), _stream(dev))
+    check("kda_recurrent_fwd_qdq", st)
+    return o, ht
+
+
 def make_decode_problem(q, k, v, scale=1.0, state_mode="e4m3", block_v=64,
                         readout="pre") -> GdnDecodeProblem:
     B, T, Hk, Dk = k.shape

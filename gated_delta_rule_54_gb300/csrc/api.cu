@@ -93,6 +93,22 @@ static gdn_status validate(const gdn_problem* p) {
 
 static bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15) == 0; }
 
+// The KDA recurrence shares the problem description; its own rules: no W site,
+// any QDQ period (`chunk` >= 1), state scale widths 16, 32 or 64.
+static gdn_status validate_kda(const gdn_problem* p) {
+  if (!p) return GDN_ERR_INVALID_ARG;
+  gdn_problem c = *p;
+  if (c.w_mode != GDN_QDQ_NONE) return GDN_ERR_UNSUPPORTED_MODE;
+  if (c.chunk < 1) return GDN_ERR_INVALID_ARG;
+  if (c.block_v != 16 && c.block_v != 32 && c.block_v != 64) return GDN_ERR_UNSUPPORTED_MODE;
+  c.chunk = kChunkLen;
+  c.block_v = kChunkLen;
+  const gdn_status s = validate(&c);
+  if (s != GDN_OK) return s;
+  if (c.N > 65535) return GDN_ERR_UNSUPPORTED_SHAPE;  // grid z
+  return GDN_OK;
+}
+
 }  // namespace gdn
 
 using namespace gdn;
@@ -144,6 +160,23 @@ gdn_status gdn_chunk_fwd_qdq(const gdn_problem* p, const void* q, const void* k,
   if (ctx && ((uintptr_t)ctx & 255)) return GDN_ERR_MISALIGNED;
   if (d.N == 0 || (d.B * d.T == 0 && !ht)) return GDN_OK;
   return launch_fwd(*p, d, q, k, v, beta, g, h0, o, ht, ctx, (cudaStream_t)stream);
+}
+
+gdn_status kda_recurrent_fwd_qdq(const gdn_problem* p, const void* q, const void* k,
+                                 const void* v, const float* beta, const float* g,
+                                 const float* h0, float* o, float* ht, void* stream) {
+  const gdn_status s = validate_kda(p);
+  if (s != GDN_OK) return s;
+  gdn_problem c = *p;
+  c.chunk = kChunkLen;
+  c.block_v = kChunkLen;
+  const Dims d = dims_of(c);
+  if (d.B * d.T > 0 && (!q || !k || !v || !beta || !g || !o)) return GDN_ERR_INVALID_ARG;
+  for (const void* ptr : {q, k, v, (const void*)beta, (const void*)g, (const void*)h0,
+                          (const void*)o, (const void*)ht, (const void*)p->cu_seqlens})
+    if (ptr && !aligned16(ptr)) return GDN_ERR_MISALIGNED;
+  if (d.N == 0 || (d.B * d.T == 0 && !ht)) return GDN_OK;
+  return launch_kda(*p, d, q, k, v, beta, g, h0, o, ht, (cudaStream_t)stream);
 }
 
 size_t gdn_bwd_workspace_bytes(const gdn_problem* p) {

@@ -44,6 +44,10 @@ gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const 
 // (cleared when reset); -1 if the flag could not be read
 int fwd_device_error(bool reset);
 
+gdn_status launch_kda(const gdn_problem& p, const Dims& d, const void* q, const void* k,
+                      const void* v, const float* beta, const float* g, const float* h0,
+                      float* o, float* ht, cudaStream_t st);
+
 size_t bwd_workspace_bytes(const gdn_problem& p, const Dims& d);
 
 gdn_status launch_bwd(const gdn_problem& p, const Dims& d, const void* q, const void* k,

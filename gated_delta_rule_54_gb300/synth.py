@@ -61,6 +61,9 @@ WORKLOADS = {
     # (256 x 16 x 128 x 128 fp32 = 256 MiB) exceed L2
     "decode": Workload("decode step B256 T1 H16 D128 e4m3-state", B=256, T=1, Hk=16, Hv=16,
                        Dk=128, Dv=128, h0=True, seed=5),
+    # KDA recurrence (per-key-channel decay), state QDQ every 64 tokens
+    "kda": Workload("KDA recurrent B4 T4096 H16 D128 e4m3-state", B=4, T=4096, Hk=16, Hv=16,
+                    Dk=128, Dv=128, w_mode="none", h0=True, seed=6),
 }
 
 
@@ -108,6 +111,21 @@ def make_inputs(w: Workload, lengths=None, device="cpu"):
     if w.backward:
         d["do"] = rn(B, T, w.Hv, w.Dv).to(torch.bfloat16)
         d["dht"] = rn(N, w.Hv, w.Dk, w.Dv) * 0.01
+    if device != "cpu":
+        for key, val in list(d.items()):
+            if isinstance(val, torch.Tensor):
+                d[key] = val.to(device)
+    return d
+
+
+def make_kda_inputs(w: Workload, lengths=None, device="cpu"):
+    """make_inputs plus the per-key-channel log decay g_k [B, T, Hv, Dk] of the
+    KDA recurrence, -softplus(N(0, 1)) per channel (its own seeded stream)."""
+    d = make_inputs(w, lengths=lengths)
+    gen = torch.Generator().manual_seed(w.seed + 7919)
+    B, T = d["B"], d["T"]
+    d["g_k"] = -torch.nn.functional.softplus(
+        torch.randn(B, T, w.Hv, w.Dk, generator=gen, dtype=torch.float32))
     if device != "cpu":
         for key, val in list(d.items()):
             if isinstance(val, torch.Tensor):

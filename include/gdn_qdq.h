@@ -229,6 +229,31 @@ gdn_status fake_qdq_int8(const float* x, float* y, float* scales, uint8_t* codes
                          int64_t rows, int64_t cols, int64_t group_cols, void* stream);
 
 /*
+ * KDA recurrent forward with the state fake QDQ ("[1/4] GDN state/W QAT
+ * foundation", "What does this PR do?": KDA has a recurrent reference only;
+ * "[2/4] GDN/KDA decode QAT with INT8 recurrent state": the same E4M3 / INT8
+ * state quantizer).  The pages print no formula; this is the published Kimi
+ * Delta Attention recurrence, i.e. the gated delta rule with one decay per
+ * key channel.  Per sequence and value head, with H = S^T (Dk x Dv) starting
+ * at h0 and t counted from the sequence start:
+ *     if t % p->chunk == 0:  H <- Q(H)   (per [Dk, block_v] tile, as fake_qdq_*)
+ *     H <- diag(exp(g_t)) H;  H <- H + beta_t k_t (v_t - H^T k_t)^T;  o_t = scale H^T q_t
+ * and ht is the final H, unquantized.
+ *   q, k  bf16 [B, T, Hk, Dk]      v  bf16 [B, T, Hv, Dv]     beta f32 [B, T, Hv]
+ *   g     f32  [B, T, Hv, Dk]  log decay per key channel
+ *   h0    f32  [N, Hv, Dk, Dv] or NULL (zeros)
+ *   o     f32  [B, T, Hv, Dv] (written)    ht f32 [N, Hv, Dk, Dv] or NULL (written)
+ * The problem description is the chunked forward's, read with these rules:
+ * w_mode must be NONE (no W site; GDN_ERR_UNSUPPORTED_MODE), `chunk` is the
+ * QDQ period (>= 1; 64 is the chunk-boundary rule, 1 quantizes before every
+ * token), block_v is 16, 32 or 64, N <= 65535.  Packed sequences, grouped
+ * heads and all alignment rules as for the forward.
+ */
+gdn_status kda_recurrent_fwd_qdq(const gdn_problem* p, const void* q, const void* k,
+                                 const void* v, const float* beta, const float* g,
+                                 const float* h0, float* o, float* ht, void* stream);
+
+/*
  * Decode QAT step ("[2/4] GDN/KDA decode QAT with INT8 recurrent state",
  * section "What does this PR do?": after an exact chunked prefill of an
  * explicit prefix, every later token writes the recurrent state through the
