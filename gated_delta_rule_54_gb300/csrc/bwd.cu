@@ -335,28 +335,31 @@ struct ChunkSmem {
   static constexpr int kTile64 = kChunk * 64 * 2; // bf16 [64][64]
   static constexpr int K = 0;
   static constexpr int Q = K + kTileK;
-  static constexpr int V = Q + kTileK;             // [64][64] (this value block)
-  static constexpr int DO = V + kTile64;
-  static constexpr int WV = DO + kTile64;          // W^ values bf16 [64][DK] -> later dW
-  static constexpr int HH = WV + kTileK;           // H^ values bf16 [DK][64] -> later dT, X, dKK
-  static constexpr int DHP = HH + DK * 64 * 2;     // dH' bf16 [DK][64]
-  static constexpr int GKK = DHP + DK * 64 * 2;    // bf16 Gamma KK (strict lower; forward's image)
-  static constexpr int PB = GKK + kTile64;         // bf16 P (forward's image)
+  static constexpr int V = Q + kTileK;             // 2 x [64][64] (value blocks 0, 1)
+  static constexpr int DO = V + 2 * kTile64;       // 2 x [64][64]
+  static constexpr int DHP = DO + 2 * kTile64;     // 2 x dH' bf16 [DK][64]; later dKK
+  static constexpr int WV = DHP + 2 * DK * 64 * 2; // W^ values bf16 [64][DK]; later dW
+  static constexpr int HH = WV + kTileK;           // H^ values of one block [DK][64]; later dT
+  static constexpr int GKK = HH + DK * 64 * 2;     // bf16 Gamma KK (strict lower; forward's image)
+  static constexpr int PB = GKK + kTile64;         // bf16 P (forward's image); later X
   static constexpr int TB = PB + kTile64;          // bf16 T (forward's image)
-  static constexpr int TU = TB + kTile64;          // bf16 T diag(beta) -> later Gm
-  static constexpr int DB = TU + kTile64;          // bf16 Delta
-  static constexpr int DDB = DB + kTile64;         // bf16 dDelta
-  static constexpr int VEC = DDB + kTile64;        // chunk vectors (forward)
-  static constexpr int RACC = VEC + kCvecFloats * 4;  // per-row partial sums [kSlots][64] + 8 scalars
+  static constexpr int TU = TB + kTile64;          // bf16 T diag(beta); later Gm
+  static constexpr int DB = TU + kTile64;          // bf16 Delta; W codes before that
+  static constexpr int DDB = DB + kTile64;         // bf16 dDelta; block-0 state codes before that
+  static constexpr int HC1 = DDB + kTile64;        // u8 [DK][64] block-1 state codes
+  static constexpr int VEC = HC1 + DK * 64;        // chunk vectors (forward)
+  static constexpr int RACC = VEC + kCvecFloats * 4;  // per-row partial sums [kSlots][64] + scalars
   static constexpr int kSlots = 36;
-  static constexpr int BYTES = RACC + kSlots * 256 + 4 * (16 + 2);
+  static constexpr int BYTES = RACC + kSlots * 256 + 4 * (kWarps + 2);
   static_assert(BYTES <= 232448, "shared memory budget");
   static_assert(kChunk * DK <= kTile64 && DK * 64 <= kTile64, "code staging fits in Delta, dDelta");
+  static_assert(DK * 64 * 2 >= kTile64, "dT fits in the H^ tile");
 };
 
-// racc slot indices (each a [64] row of partial sums; written exactly once)
-// (four slots per kind: one per column quarter for row sums, one per row
-// quarter for column sums)
+// racc slot indices (each a [64] row of partial sums; four slots per kind: one
+// per column quarter for row sums, one per row quarter for column sums).  Each
+// slot entry is owned by one thread, which adds the contributions of both
+// value blocks in a fixed order.
 enum : int {
   R_PPR = 0,   // row sums of dP * P
   R_PPC = 4,   // column sums of dP * P
@@ -402,13 +405,28 @@ __device__ __forceinline__ void col_sums(const float (&x)[NT][4], float (&c)[NT]
     }
 }
 
+// row sums r0 (row gq), r1 (row gq + 8) of a warp tile added into a racc slot
+__device__ __forceinline__ void racc_add_rows(float* racc, int slot, int row0, int gq, int tq,
+                                              float r0, float r1) {
+  if (tq == 0) {
+    racc[slot * 64 + row0 + gq] += r0;
+    racc[slot * 64 + row0 + gq + 8] += r1;
+  }
+}
+
+// Phase 2: all gradients of one (chunk slot, value head), both 64-column value
+// blocks in one CTA: the value-block terms (Delta, dDelta, dP, dV, the parts
+// of dW, dT, Gm, dq, dk and the row sums) run per block and are summed on
+// chip; T^T dW, Gm K, Gm^T Q, X = T^T dT, dA and dKK run once; every output
+// element has one writer.
 template <int DK, int SM, int WM>
 __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdParams p) {
   using S = ChunkSmem<DK>;
   extern __shared__ __align__(1024) unsigned char sm[];
-  const int vb = blockIdx.x, h = blockIdx.y;
-  const int64_t slot = blockIdx.z;
+  const int64_t slot = blockIdx.x;
+  const int h = blockIdx.y;
   const int hk = h / p.G;
+  const int nvb = p.Dv / 64;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
   const int rt = warp & 3, ch = warp >> 2;   // row quarter, column quarter
@@ -434,24 +452,24 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
 
   __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(sm + S::K);
   __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(sm + S::Q);
-  __nv_bfloat16* Vs = reinterpret_cast<__nv_bfloat16*>(sm + S::V);
-  __nv_bfloat16* dOs = reinterpret_cast<__nv_bfloat16*>(sm + S::DO);
   __nv_bfloat16* Wv = reinterpret_cast<__nv_bfloat16*>(sm + S::WV);
-  __nv_bfloat16* dWb = Wv;  // after Delta
+  __nv_bfloat16* dWb = Wv;                 // after the value blocks
   __nv_bfloat16* Hh = reinterpret_cast<__nv_bfloat16*>(sm + S::HH);
-  __nv_bfloat16* dHp = reinterpret_cast<__nv_bfloat16*>(sm + S::DHP);
-  __nv_bfloat16* dTb = Hh;                 // after the H^ / dH' products
-  __nv_bfloat16* Xb = Hh + kChunk * 64;
-  __nv_bfloat16* dKKb = dHp;
+  __nv_bfloat16* dTb = Hh;                 // after the value blocks
+  __nv_bfloat16* dKKb = reinterpret_cast<__nv_bfloat16*>(sm + S::DHP);  // after the value blocks
   __nv_bfloat16* GKKb = reinterpret_cast<__nv_bfloat16*>(sm + S::GKK);
   __nv_bfloat16* Pb = reinterpret_cast<__nv_bfloat16*>(sm + S::PB);
+  __nv_bfloat16* Xb = Pb;                  // after the value blocks
   __nv_bfloat16* Tb = reinterpret_cast<__nv_bfloat16*>(sm + S::TB);
   __nv_bfloat16* Tub = reinterpret_cast<__nv_bfloat16*>(sm + S::TU);
-  __nv_bfloat16* Gmb = Tub;                // after U
+  __nv_bfloat16* Gmb = Tub;                // after the value blocks
   __nv_bfloat16* Db = reinterpret_cast<__nv_bfloat16*>(sm + S::DB);
   __nv_bfloat16* dDb = reinterpret_cast<__nv_bfloat16*>(sm + S::DDB);
   uint8_t* wst = reinterpret_cast<uint8_t*>(sm + S::DB);   // W codes [64][DK], until Delta
-  uint8_t* hst = reinterpret_cast<uint8_t*>(sm + S::DDB);  // H codes [DK][64], until dDelta
+  auto Vb = [&](int b) { return reinterpret_cast<__nv_bfloat16*>(sm + S::V + b * S::kTile64); };
+  auto dOb = [&](int b) { return reinterpret_cast<__nv_bfloat16*>(sm + S::DO + b * S::kTile64); };
+  auto dHpb = [&](int b) { return reinterpret_cast<__nv_bfloat16*>(sm + S::DHP + b * DK * 64 * 2); };
+  auto hcb = [&](int b) { return reinterpret_cast<uint8_t*>(sm + (b == 0 ? S::DDB : S::HC1)); };
   const float* cvs = reinterpret_cast<const float*>(sm + S::VEC);
   const float* gam = cvs + kCvGam;
   const float* eg = cvs + kCvEg;
@@ -461,91 +479,70 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
   float* racc = reinterpret_cast<float*>(sm + S::RACC);
   float* hd_part = racc + S::kSlots * 64;  // [kWarps] <H^, dH'> partials, then [2] sums of t_i
 
-  // ---- loads: group A feeds the dequantization below, group B (K, Q, V, dO,
-  //      Gamma o KK^T, P) lands meanwhile; T, Gamma o KK^T, P and the chunk
-  //      vectors come from the forward ----
+  // ---- loads.  Group A feeds the W / block-0 dequantization, group B the
+  //      block-0 products, group C is block 1; T, Gamma o KK^T, P and the
+  //      chunk vectors come from the forward ----
+  auto load_block_vb = [&](int b) {
+    const __nv_bfloat16* src = p.ws_dh + ((slot * p.Hv + h) * DK) * p.Dv + b * 64;
+    __nv_bfloat16* dst = dHpb(b);
+    for (int i = threadIdx.x; i < DK * 8; i += kThreads) {
+      const int d = i >> 3, c8 = i & 7;
+      cp_async16(smem_u32(dst + swz<64>(d, c8 * 8)), src + (int64_t)d * p.Dv + c8 * 8, 16);
+    }
+    if constexpr (SM != GDN_QDQ_NONE) {
+      const uint8_t* hs = p.h_codes + ((slot * p.Hv + h) * DK) * p.Dv + b * 64;
+      uint8_t* hd = hcb(b);
+      for (int i = threadIdx.x; i < DK * 4; i += kThreads) {
+        const int d = i >> 2, c16 = i & 3;
+        cp_async16(smem_u32(hd + d * 64 + c16 * 16), hs + (int64_t)d * p.Dv + c16 * 16, 16);
+      }
+    }
+  };
+  auto load_vo = [&](int b) {
+    load_rows_bf16<64>(Vb(b), p.v + (ctok * p.Hv + h) * p.Dv + b * 64, (int64_t)p.Hv * p.Dv, Lc);
+    load_rows_bf16<64>(dOb(b), p.dO + (ctok * p.Hv + h) * p.Dv + b * 64, (int64_t)p.Hv * p.Dv, Lc);
+  };
   {
     const int64_t img = (slot * p.Hv + h) * (kTileImgBytes / 2);
     load_block(sm + S::VEC, p.cvec + (slot * p.Hv + h) * kCvecFloats, kCvecFloats * 4);
     load_block(Tb, p.tb + img, kTileImgBytes);
-  }
-  {  // dH' [DK][64] bf16 from the workspace (always a full tile)
-    const __nv_bfloat16* src = p.ws_dh + ((slot * p.Hv + h) * DK) * p.Dv + vb * 64;
-    for (int i = threadIdx.x; i < DK * 8; i += kThreads) {
-      const int d = i >> 3, c8 = i & 7;
-      cp_async16(smem_u32(dHp + swz<64>(d, c8 * 8)), src + (int64_t)d * p.Dv + c8 * 8, 16);
+    if constexpr (WM != GDN_QDQ_NONE) {
+      constexpr int CPR = DK / 16;
+      for (int i = threadIdx.x; i < kChunk * CPR; i += kThreads) {
+        const int r = i / CPR, cc = i % CPR;
+        const bool ok = r < Lc;
+        cp_async16(smem_u32(wst + r * DK + cc * 16),
+                   p.w_codes + ((ctok + (ok ? r : 0)) * p.Hv + h) * DK + cc * 16, ok ? 16 : 0);
+      }
     }
-  }
-  if constexpr (WM != GDN_QDQ_NONE) {
-    constexpr int CPR = DK / 16;
-    for (int i = threadIdx.x; i < kChunk * CPR; i += kThreads) {
-      const int r = i / CPR, cc = i % CPR;
-      const bool ok = r < Lc;
-      cp_async16(smem_u32(wst + r * DK + cc * 16),
-                 p.w_codes + ((ctok + (ok ? r : 0)) * p.Hv + h) * DK + cc * 16, ok ? 16 : 0);
-    }
-  }
-  if constexpr (SM != GDN_QDQ_NONE) {
-    const uint8_t* src = p.h_codes + ((slot * p.Hv + h) * DK) * p.Dv + vb * 64;
-    for (int i = threadIdx.x; i < DK * 4; i += kThreads) {
-      const int d = i >> 2, c16 = i & 3;
-      cp_async16(smem_u32(hst + d * 64 + c16 * 16), src + (int64_t)d * p.Dv + c16 * 16, 16);
-    }
-  }
-  cp_async_commit();
-  load_rows_bf16<DK>(Ks, p.k + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
-  load_rows_bf16<DK>(Qs, p.q + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
-  load_rows_bf16<64>(Vs, p.v + (ctok * p.Hv + h) * p.Dv + vb * 64, (int64_t)p.Hv * p.Dv, Lc);
-  load_rows_bf16<64>(dOs, p.dO + (ctok * p.Hv + h) * p.Dv + vb * 64, (int64_t)p.Hv * p.Dv, Lc);
-  {
-    const int64_t img = (slot * p.Hv + h) * (kTileImgBytes / 2);
+    load_block_vb(0);
+    cp_async_commit();  // group A
+    load_rows_bf16<DK>(Ks, p.k + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
+    load_rows_bf16<DK>(Qs, p.q + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
+    load_vo(0);
     load_block(GKKb, p.gkk + img, kTileImgBytes);
     load_block(Pb, p.pb + img, kTileImgBytes);
+    cp_async_commit();  // group B
+    if (nvb > 1) {
+      load_block_vb(1);
+      load_vo(1);
+    }
+    cp_async_commit();  // group C
   }
-  cp_async_commit();
-  cp_async_wait<1>();
-  __syncthreads();  // group A visible to all threads
+  for (int i = threadIdx.x; i < S::kSlots * 64 + kWarps + 2; i += kThreads) racc[i] = 0.f;
+  cp_async_wait<2>();
+  __syncthreads();  // group A and the zeroed partial sums visible to all threads
 
-  // ---- dequantized operands (4 codes per step), <H^, dH'>, and T / Tu in bf16 ----
+  // ---- W^ (dequantized, bf16) and T diag(beta), once ----
   if constexpr (WM != GDN_QDQ_NONE) {
     const float sW = p.w_scales[slot * p.Hv + h];
     for (int e = threadIdx.x; e < kChunk * DK / 4; e += kThreads) {
       const int r = (4 * e) / DK, col = (4 * e) % DK;
       const float4 v = qdq_code4_values<WM>(*reinterpret_cast<const uint32_t*>(wst + r * DK + col));
-      uint2 pk;
-      pk.x = pack_bf16(v.x * sW, v.y * sW);
-      pk.y = pack_bf16(v.z * sW, v.w * sW);
-      *reinterpret_cast<uint2*>(Wv + swz<DK>(r, col)) = pk;
+      *reinterpret_cast<uint2*>(Wv + swz<DK>(r, col)) =
+          make_uint2(pack_bf16(v.x * sW, v.y * sW), pack_bf16(v.z * sW, v.w * sW));
     }
-  }
-  {
-    float hd = 0.f;
-    for (int e = threadIdx.x; e < DK * 16; e += kThreads) {
-      const int d = e >> 4, col = (e & 15) * 4;
-      float4 x;
-      if constexpr (SM != GDN_QDQ_NONE) {
-        const float sH = p.h_scales[(slot * p.Hv + h) * (p.Dv / 64) + vb];
-        x = qdq_code4_values<SM>(*reinterpret_cast<const uint32_t*>(hst + d * 64 + col));
-        x.x *= sH; x.y *= sH; x.z *= sH; x.w *= sH;
-      } else {
-        x = *reinterpret_cast<const float4*>(p.h_full + ((slot * p.Hv + h) * DK + d) * p.Dv +
-                                              vb * 64 + col);
-      }
-      uint2 pk;
-      pk.x = pack_bf16(x.x, x.y);
-      pk.y = pack_bf16(x.z, x.w);
-      *reinterpret_cast<uint2*>(Hh + swz<64>(d, col)) = pk;
-      const uint2 yb = *reinterpret_cast<const uint2*>(dHp + swz<64>(d, col));
-      const __nv_bfloat162 y0 = *reinterpret_cast<const __nv_bfloat162*>(&yb.x);
-      const __nv_bfloat162 y1 = *reinterpret_cast<const __nv_bfloat162*>(&yb.y);
-      hd += x.x * __bfloat162float(y0.x) + x.y * __bfloat162float(y0.y) +
-            x.z * __bfloat162float(y1.x) + x.w * __bfloat162float(y1.y);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
-    if (lane == 0) hd_part[warp] = hd;
-  }
-  if constexpr (WM == GDN_QDQ_NONE) {
+  } else {
     // W from the forward's fp32 copy (rows >= Lc zero)
     for (int e = threadIdx.x; e < kChunk * DK / 4; e += kThreads) {
       const int r = (4 * e) / DK, col = (4 * e) % DK;
@@ -561,178 +558,205 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
     st_bf16x2(Tub + swz<64>(i, j), __bfloat162float(t2.x) * bet[j],
               __bfloat162float(t2.y) * bet[j + 1]);
   }
-  cp_async_wait<0>();
-  __syncthreads();  // group B visible; operands above complete
-  // ---- Delta = Tu V - W^ H^;  dDelta = scale P^T dO + dec (K dH') ----
-  {
-    const int row0 = rt * 16, col0 = ch * 16;
-    float u[2][4], wh[2][4];
-    zero_acc(u);
-    zero_acc(wh);
-    wgemm<2, false, true, 64, 64>(u, Tub, row0, Vs, col0, 0, 64, lane);
-    wgemm<2, false, true, DK, 64>(wh, Wv, row0, Hh, col0, 0, DK, lane);
-    float a1[2][4], a2[2][4];
-    zero_acc(a1);
-    zero_acc(a2);
-    wgemm<2, true, true, 64, 64>(a1, Pb, row0, dOs, col0, row0, 64, lane);
-    wgemm<2, false, true, DK, 64>(a2, Ks, row0, dHp, col0, 0, DK, lane);
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e2 = 0; e2 < 2; ++e2) {
-        const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-        st_bf16x2(Db + swz<64>(i, j), u[nt][2 * e2] - wh[nt][2 * e2],
-                  u[nt][2 * e2 + 1] - wh[nt][2 * e2 + 1]);
-        const float di = dec[i];
-        st_bf16x2(dDb + swz<64>(i, j), p.scale * a1[nt][2 * e2] + di * a2[nt][2 * e2],
-                  p.scale * a1[nt][2 * e2 + 1] + di * a2[nt][2 * e2 + 1]);
-      }
-  }
-  __syncthreads();
 
   constexpr int NTW = DK / 32;
   const int wrow0 = rt * 16, wcol0 = ch * (DK / 4);
-  float dQ[NTW][4], dK[NTW][4];
+  const int row0 = rt * 16, col0 = ch * 16;
+  float dQ[NTW][4], dK[NTW][4], dWa[NTW][4], gma[2][4], dta[2][4];
   zero_acc(dQ);
   zero_acc(dK);
+  zero_acc(dWa);
+  zero_acc(gma);
+  zero_acc(dta);
 
-  // ---- output-side products ----
-  {
-    // dP = lower-incl(scale dO Delta^T); Gm = dP Gamma (into Tu's buffer); PP = dP P
-    const int row0 = rt * 16, col0 = ch * 16;
-    float dp[2][4];
-    zero_acc(dp);
-    wgemm<2, false, false, 64, 64>(dp, dOs, row0, Db, col0, 0, 64, lane);
-    float pp[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e2 = 0; e2 < 2; ++e2) {
-        const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-        float gm[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const int jj = j + e;
-          const float d = (jj <= i) ? p.scale * dp[nt][2 * e2 + e] : 0.f;
-          gm[e] = (jj <= i) ? d * expf(gam[i] - gam[jj]) : 0.f;
-          const __nv_bfloat16 pv = Pb[swz<64>(i, jj)];
-          pp[nt][2 * e2 + e] = d * __bfloat162float(pv);
+  for (int vb = 0; vb < nvb; ++vb) {
+    const __nv_bfloat16* Vs = Vb(vb);
+    const __nv_bfloat16* dOs = dOb(vb);
+    const __nv_bfloat16* dHp = dHpb(vb);
+    // ---- H^ of this block (bf16) and <H^, dH'> ----
+    {
+      const uint8_t* hst = hcb(vb);
+      float hd = 0.f;
+      for (int e = threadIdx.x; e < DK * 16; e += kThreads) {
+        const int d = e >> 4, col = (e & 15) * 4;
+        float4 x;
+        if constexpr (SM != GDN_QDQ_NONE) {
+          const float sH = p.h_scales[(slot * p.Hv + h) * nvb + vb];
+          x = qdq_code4_values<SM>(*reinterpret_cast<const uint32_t*>(hst + d * 64 + col));
+          x.x *= sH; x.y *= sH; x.z *= sH; x.w *= sH;
+        } else {
+          x = *reinterpret_cast<const float4*>(p.h_full + ((slot * p.Hv + h) * DK + d) * p.Dv +
+                                                vb * 64 + col);
         }
-        st_bf16x2(Gmb + swz<64>(i, j), gm[0], gm[1]);
+        *reinterpret_cast<uint2*>(Hh + swz<64>(d, col)) =
+            make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
+        const uint2 yb = *reinterpret_cast<const uint2*>(dHp + swz<64>(d, col));
+        const __nv_bfloat162 y0 = *reinterpret_cast<const __nv_bfloat162*>(&yb.x);
+        const __nv_bfloat162 y1 = *reinterpret_cast<const __nv_bfloat162*>(&yb.y);
+        hd += x.x * __bfloat162float(y0.x) + x.y * __bfloat162float(y0.y) +
+              x.z * __bfloat162float(y1.x) + x.w * __bfloat162float(y1.y);
       }
-    float r0, r1;
-    row_sums<2>(pp, r0, r1);
-    if (tq == 0) {
-      racc[(R_PPR + ch) * 64 + row0 + gq] = r0;
-      racc[(R_PPR + ch) * 64 + row0 + gq + 8] = r1;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
+      if (lane == 0) hd_part[warp] += hd;
     }
-    float cs[2][2];
-    col_sums<2>(pp, cs);
-    if (gq == 0)
+    if (vb == 0) cp_async_wait<1>();  // block 1's group was waited for before its H^
+    __syncthreads();  // H^, this block's loads (and W^, T diag(beta)) ready
+
+    // ---- Delta = Tu V - W^ H^;  dDelta = scale P^T dO + dec (K dH') ----
+    {
+      float u[2][4], wh[2][4];
+      zero_acc(u);
+      zero_acc(wh);
+      wgemm<2, false, true, 64, 64>(u, Tub, row0, Vs, col0, 0, 64, lane);
+      wgemm<2, false, true, DK, 64>(wh, Wv, row0, Hh, col0, 0, DK, lane);
+      float a1[2][4], a2[2][4];
+      zero_acc(a1);
+      zero_acc(a2);
+      wgemm<2, true, true, 64, 64>(a1, Pb, row0, dOs, col0, row0, 64, lane);
+      wgemm<2, false, true, DK, 64>(a2, Ks, row0, dHp, col0, 0, DK, lane);
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) racc[(R_PPC + rt) * 64 + col0 + nt * 8 + 2 * tq + e] = cs[nt][e];
-  }
-  {
-    // dQ_inter = scale e^gamma (dO H^T); row sums of q * dQ_inter
-    float acc[NTW][4];
-    zero_acc(acc);
-    wgemm<NTW, false, false, 64, 64>(acc, dOs, wrow0, Hh, wcol0, 0, 64, lane);
-    float qd[NTW][4];
-#pragma unroll
-    for (int nt = 0; nt < NTW; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = wrow0 + gq + 8 * (e >> 1), d = wcol0 + nt * 8 + 2 * tq + (e & 1);
-        const float v = p.scale * eg[i] * acc[nt][e];
-        dQ[nt][e] = v;
-        qd[nt][e] = v * __bfloat162float(Qs[swz<DK>(i, d)]);
-      }
-    float r0, r1;
-    row_sums<NTW>(qd, r0, r1);
-    if (tq == 0) {
-      racc[(R_OH + ch) * 64 + wrow0 + gq] = r0;
-      racc[(R_OH + ch) * 64 + wrow0 + gq + 8] = r1;
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
+          st_bf16x2(Db + swz<64>(i, j), u[nt][2 * e2] - wh[nt][2 * e2],
+                    u[nt][2 * e2 + 1] - wh[nt][2 * e2 + 1]);
+          const float di = dec[i];
+          st_bf16x2(dDb + swz<64>(i, j), p.scale * a1[nt][2 * e2] + di * a2[nt][2 * e2],
+                    p.scale * a1[nt][2 * e2 + 1] + di * a2[nt][2 * e2 + 1]);
+        }
     }
-  }
-  {
-    // Delta dH'^T: dK += dec_i (Delta dH'^T); t_i = dec_i sum_d k_id (Delta dH'^T)_id
-    float acc[NTW][4];
-    zero_acc(acc);
-    wgemm<NTW, false, false, 64, 64>(acc, Db, wrow0, dHp, wcol0, 0, 64, lane);
-    float kd[NTW][4];
+    __syncthreads();
+
+    // ---- output-side products of this block ----
+    {
+      // dP = lower-incl(scale dO Delta^T); Gm += dP Gamma; PP = dP P
+      float dp[2][4];
+      zero_acc(dp);
+      wgemm<2, false, false, 64, 64>(dp, dOs, row0, Db, col0, 0, 64, lane);
+      float pp[2][4];
 #pragma unroll
-    for (int nt = 0; nt < NTW; ++nt)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = wrow0 + gq + 8 * (e >> 1), d = wcol0 + nt * 8 + 2 * tq + (e & 1);
-        const float v = dec[i] * acc[nt][e];
-        dK[nt][e] += v;
-        kd[nt][e] = v * __bfloat162float(Ks[swz<DK>(i, d)]);
-      }
-    float r0, r1;
-    row_sums<NTW>(kd, r0, r1);
-    if (tq == 0) {
-      racc[(R_TT + ch) * 64 + wrow0 + gq] = r0;
-      racc[(R_TT + ch) * 64 + wrow0 + gq + 8] = r1;
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int jj = j + e;
+            const float d = (jj <= i) ? p.scale * dp[nt][2 * e2 + e] : 0.f;
+            gma[nt][2 * e2 + e] += (jj <= i) ? d * expf(gam[i] - gam[jj]) : 0.f;
+            pp[nt][2 * e2 + e] = d * __bfloat162float(Pb[swz<64>(i, jj)]);
+          }
+        }
+      float r0, r1;
+      row_sums<2>(pp, r0, r1);
+      racc_add_rows(racc, R_PPR + ch, row0, gq, tq, r0, r1);
+      float cs[2][2];
+      col_sums<2>(pp, cs);
+      if (gq == 0)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) racc[(R_PPC + rt) * 64 + col0 + nt * 8 + 2 * tq + e] += cs[nt][e];
     }
-  }
-  {
-    // dW = -dDelta H^T (STE: = dW^) into W^'s buffer (W^ no longer needed)
-    float acc[NTW][4];
-    zero_acc(acc);
-    wgemm<NTW, false, false, 64, 64>(acc, dDb, wrow0, Hh, wcol0, 0, 64, lane);
-    __syncthreads();  // every warp is done reading W^ (Delta products above)
+    {
+      // dQ_inter = scale e^gamma (dO H^T); row sums of q * dQ_inter
+      float acc[NTW][4];
+      zero_acc(acc);
+      wgemm<NTW, false, false, 64, 64>(acc, dOs, wrow0, Hh, wcol0, 0, 64, lane);
+      float qd[NTW][4];
 #pragma unroll
-    for (int nt = 0; nt < NTW; ++nt)
+      for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
-      for (int e2 = 0; e2 < 2; ++e2) {
-        const int i = wrow0 + gq + 8 * e2, d = wcol0 + nt * 8 + 2 * tq;
-        st_bf16x2(dWb + swz<DK>(i, d), -acc[nt][2 * e2], -acc[nt][2 * e2 + 1]);
-      }
+        for (int e = 0; e < 4; ++e) {
+          const int i = wrow0 + gq + 8 * (e >> 1), d = wcol0 + nt * 8 + 2 * tq + (e & 1);
+          const float v = p.scale * eg[i] * acc[nt][e];
+          dQ[nt][e] += v;
+          qd[nt][e] = v * __bfloat162float(Qs[swz<DK>(i, d)]);
+        }
+      float r0, r1;
+      row_sums<NTW>(qd, r0, r1);
+      racc_add_rows(racc, R_OH + ch, wrow0, gq, tq, r0, r1);
+    }
+    {
+      // Delta dH'^T: dK += dec_i (Delta dH'^T); t_i = dec_i sum_d k_id (Delta dH'^T)_id
+      float acc[NTW][4];
+      zero_acc(acc);
+      wgemm<NTW, false, false, 64, 64>(acc, Db, wrow0, dHp, wcol0, 0, 64, lane);
+      float kd[NTW][4];
+#pragma unroll
+      for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int i = wrow0 + gq + 8 * (e >> 1), d = wcol0 + nt * 8 + 2 * tq + (e & 1);
+          const float v = dec[i] * acc[nt][e];
+          dK[nt][e] += v;
+          kd[nt][e] = v * __bfloat162float(Ks[swz<DK>(i, d)]);
+        }
+      float r0, r1;
+      row_sums<NTW>(kd, r0, r1);
+      racc_add_rows(racc, R_TT + ch, wrow0, gq, tq, r0, r1);
+    }
+    // dW += -dDelta H^T (STE: = dW^)
+    wgemm<NTW, false, false, 64, 64>(dWa, dDb, wrow0, Hh, wcol0, 0, 64, lane);
+    {
+      // dT part (dDelta V^T), summed over the blocks; T^T dDelta -> dV and its row sums
+      wgemm<2, false, false, 64, 64>(dta, dDb, row0, Vs, col0, 0, 64, lane);
+      float tu[2][4];
+      zero_acc(tu);
+      wgemm<2, true, true, 64, 64>(tu, Tb, row0, dDb, col0, 0, 64, lane);
+      float bv[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
+          const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(Vs + swz<64>(i, j));
+          bv[nt][2 * e2] = tu[nt][2 * e2] * __bfloat162float(v2.x);
+          bv[nt][2 * e2 + 1] = tu[nt][2 * e2 + 1] * __bfloat162float(v2.y);
+          if (i < Lc)
+            *reinterpret_cast<float2*>(p.dv + ((ctok + i) * p.Hv + h) * p.Dv + vb * 64 + j) =
+                make_float2(bet[i] * tu[nt][2 * e2], bet[i] * tu[nt][2 * e2 + 1]);
+        }
+      float r0, r1;
+      row_sums<2>(bv, r0, r1);
+      racc_add_rows(racc, R_BU + ch, row0, gq, tq, r0, r1);
+    }
+    if (vb + 1 < nvb) cp_async_wait<0>();  // the next block's loads (group C)
+    __syncthreads();  // this block's H^, Delta, dDelta are no longer read
   }
-  __syncthreads();  // Gm, dW complete; H^ and dH' free
+
+  // ---- summed block terms to shared memory: dW (into W^'s tile), Gm (into Tu's) ----
+#pragma unroll
+  for (int nt = 0; nt < NTW; ++nt)
+#pragma unroll
+    for (int e2 = 0; e2 < 2; ++e2) {
+      const int i = wrow0 + gq + 8 * e2, d = wcol0 + nt * 8 + 2 * tq;
+      st_bf16x2(dWb + swz<DK>(i, d), -dWa[nt][2 * e2], -dWa[nt][2 * e2 + 1]);
+    }
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e2 = 0; e2 < 2; ++e2) {
+      const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
+      st_bf16x2(Gmb + swz<64>(i, j), gma[nt][2 * e2], gma[nt][2 * e2 + 1]);
+    }
+  __syncthreads();  // dW, Gm complete
 
   {
     // dT = (dDelta V^T) diag(beta) + (dW K^T) diag(beta e^gamma)  -> dTb
-    const int row0 = rt * 16, col0 = ch * 16;
-    float a1[2][4], a2[2][4];
-    zero_acc(a1);
+    float a2[2][4];
     zero_acc(a2);
-    wgemm<2, false, false, 64, 64>(a1, dDb, row0, Vs, col0, 0, 64, lane);
     wgemm<2, false, false, DK, DK>(a2, dWb, row0, Ks, col0, 0, DK, lane);
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-        st_bf16x2(dTb + swz<64>(i, j), a1[nt][2 * e2] * bet[j] + a2[nt][2 * e2] * beg[j],
-                  a1[nt][2 * e2 + 1] * bet[j + 1] + a2[nt][2 * e2 + 1] * beg[j + 1]);
+        st_bf16x2(dTb + swz<64>(i, j), dta[nt][2 * e2] * bet[j] + a2[nt][2 * e2] * beg[j],
+                  dta[nt][2 * e2 + 1] * bet[j + 1] + a2[nt][2 * e2 + 1] * beg[j + 1]);
       }
-    // T^T dU: dV = beta (T^T dDelta); row sums of v * (T^T dDelta)
-    float tu[2][4];
-    zero_acc(tu);
-    wgemm<2, true, true, 64, 64>(tu, Tb, row0, dDb, col0, 0, 64, lane);
-    float bv[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int e2 = 0; e2 < 2; ++e2) {
-        const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-        const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(Vs + swz<64>(i, j));
-        bv[nt][2 * e2] = tu[nt][2 * e2] * __bfloat162float(v2.x);
-        bv[nt][2 * e2 + 1] = tu[nt][2 * e2 + 1] * __bfloat162float(v2.y);
-        if (i < Lc)
-          *reinterpret_cast<float2*>(p.dv + ((ctok + i) * p.Hv + h) * p.Dv + vb * 64 + j) =
-              make_float2(bet[i] * tu[nt][2 * e2], bet[i] * tu[nt][2 * e2 + 1]);
-      }
-    float r0, r1;
-    row_sums<2>(bv, r0, r1);
-    if (tq == 0) {
-      racc[(R_BU + ch) * 64 + row0 + gq] = r0;
-      racc[(R_BU + ch) * 64 + row0 + gq + 8] = r1;
-    }
   }
   {
     // T^T dW: dK += beta e^gamma (T^T dW); row sums of k * (T^T dW)
@@ -750,18 +774,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
       }
     float r0, r1;
     row_sums<NTW>(kw, r0, r1);
-    if (tq == 0) {
-      racc[(R_KW + ch) * 64 + wrow0 + gq] = r0;
-      racc[(R_KW + ch) * 64 + wrow0 + gq + 8] = r1;
-    }
-    // attention-side: dQ += Gm K, dK += Gm^T Q
+    racc_add_rows(racc, R_KW + ch, wrow0, gq, tq, r0, r1);
+    // attention side: dQ += Gm K, dK += Gm^T Q
     wgemm<NTW, false, true, 64, DK>(dQ, Gmb, wrow0, Ks, wcol0, 0, 64, lane);
     wgemm<NTW, true, true, 64, DK>(dK, Gmb, wrow0, Qs, wcol0, 0, 64, lane);
   }
-  __syncthreads();  // dT complete
+  __syncthreads();  // dT complete; P no longer read (its tile becomes X)
   {
     // X = T^T dT
-    const int row0 = rt * 16, col0 = ch * 16;
     float acc[2][4];
     zero_acc(acc);
     wgemm<2, true, true, 64, 64>(acc, Tb, row0, dTb, col0, 0, 64, lane);
@@ -776,7 +796,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
   __syncthreads();
   {
     // dA = -X T^T (strictly lower): dKK = dA beta_i Gamma_ij; dbeta += dA GKK; AA = dA A
-    const int row0 = rt * 16, col0 = ch * 16;
     float acc[2][4];
     zero_acc(acc);
     wgemm<2, false, false, 64, 64>(acc, Xb, row0, Tb, col0, 0, 64, lane);
@@ -800,22 +819,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
       }
     float r0, r1;
     row_sums<2>(ba, r0, r1);
-    if (tq == 0) {
-      racc[(R_BA + ch) * 64 + row0 + gq] = r0;
-      racc[(R_BA + ch) * 64 + row0 + gq + 8] = r1;
-    }
+    racc_add_rows(racc, R_BA + ch, row0, gq, tq, r0, r1);
     row_sums<2>(aa, r0, r1);
-    if (tq == 0) {
-      racc[(R_AAR + ch) * 64 + row0 + gq] = r0;
-      racc[(R_AAR + ch) * 64 + row0 + gq + 8] = r1;
-    }
+    racc_add_rows(racc, R_AAR + ch, row0, gq, tq, r0, r1);
     float cs[2][2];
     col_sums<2>(aa, cs);
     if (gq == 0)
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int e = 0; e < 2; ++e) racc[(R_AAC + rt) * 64 + col0 + nt * 8 + 2 * tq + e] = cs[nt][e];
+        for (int e = 0; e < 2; ++e) racc[(R_AAC + rt) * 64 + col0 + nt * 8 + 2 * tq + e] += cs[nt][e];
   }
   __syncthreads();
   // dK += dKK K + dKK^T K
@@ -825,19 +838,20 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
   // ---- dgamma -> dg (reverse cumsum), dbeta (warps 0-1, fixed-order sums) ----
   if (warp < 2) {
     const int i = threadIdx.x;  // row 0..63
-    auto sum4 = [&](int slot) {
-      return (racc[slot * 64 + i] + racc[(slot + 1) * 64 + i]) +
-             (racc[(slot + 2) * 64 + i] + racc[(slot + 3) * 64 + i]);
+    auto sum4 = [&](int s0) {
+      return (racc[s0 * 64 + i] + racc[(s0 + 1) * 64 + i]) +
+             (racc[(s0 + 2) * 64 + i] + racc[(s0 + 3) * 64 + i]);
     };
     const float rr = sum4(R_PPR), cc = sum4(R_PPC), ar = sum4(R_AAR), ac = sum4(R_AAC);
     const float oh = sum4(R_OH), tt = sum4(R_TT), kw = sum4(R_KW), bu = sum4(R_BU);
     const float ba = sum4(R_BA);
-    float dgam = (rr - cc) + (ar - ac) + oh - tt + beg[i] * kw;
+    const float dgam = (rr - cc) + (ar - ac) + oh - tt + beg[i] * kw;
     const float dbeta = bu + eg[i] * kw + ba;
     // gamma_L (row 63) collects e^{gL} <H^, dH'> + sum_i t_i
     float tsum = tt;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) tsum += __shfl_xor_sync(0xffffffffu, tsum, o);
+    __syncwarp();
     racc[i] = dgam;           // reuse slot 0 (fully consumed above by this thread only)
     racc[64 + i] = dbeta;
     if (lane == 0) hd_part[kWarps + warp] = tsum;
@@ -860,18 +874,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
     const float dg1 = s - x0, dg0 = s;
     const int64_t base = (ctok + 2 * lane) * p.Hv + h;
     if (2 * lane < Lc) {
-      atomicAdd(p.dg + base, dg0);
-      atomicAdd(p.dbeta + base, racc[64 + 2 * lane]);
+      p.dg[base] = dg0;
+      p.dbeta[base] = racc[64 + 2 * lane];
     }
     if (2 * lane + 1 < Lc) {
-      atomicAdd(p.dg + base + p.Hv, dg1);
-      atomicAdd(p.dbeta + base + p.Hv, racc[64 + 2 * lane + 1]);
+      p.dg[base + p.Hv] = dg1;
+      p.dbeta[base + p.Hv] = racc[64 + 2 * lane + 1];
     }
   }
 
-  // ---- dq, dk: two value-block contributions per element onto zero ----
-  // Lane pairs (tq, tq ^ 1) swap halves so each lane owns four consecutive
-  // columns of one row and adds them with one 16-byte atomic.
+  // ---- dq, dk: one writer per element.  Lane pairs (tq, tq ^ 1) swap halves
+  //      so each lane stores four consecutive columns of one row ----
   float* dq_out = p.ws_dqk ? p.ws_dqk : p.dq;
   float* dk_out = p.ws_dqk ? p.ws_dqk + p.BT * p.Hv * DK : p.dk;
   const int hh = p.ws_dqk ? h : hk;
@@ -891,8 +904,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
                           : make_float4(dK[nt][0], dK[nt][1], sk0, sk1);
     if (i_own < Lc) {
       const int64_t off = ((ctok + i_own) * HH + hh) * DK + c4;
-      atomicAdd(reinterpret_cast<float4*>(dq_out + off), vq);
-      atomicAdd(reinterpret_cast<float4*>(dk_out + off), vk);
+      *reinterpret_cast<float4*>(dq_out + off) = vq;
+      *reinterpret_cast<float4*>(dk_out + off) = vk;
     }
   }
 }
@@ -936,8 +949,7 @@ gdn_status launch_bwd_t(const BwdParams& prm, const Dims& d, cudaStream_t st) {
   if (set_smem(k1, SS::BYTES) != GDN_OK || set_smem(k2, CS::BYTES) != GDN_OK) return GDN_ERR_CUDA;
   k1<<<dim3((unsigned)(d.Dv / 64), (unsigned)d.Hv, (unsigned)d.N), kThreads, SS::BYTES, st>>>(prm);
   if (d.B * d.T > 0 && d.n_slots > 0)
-    k2<<<dim3((unsigned)(d.Dv / 64), (unsigned)d.Hv, (unsigned)d.n_slots), kThreads, CS::BYTES, st>>>(
-        prm);
+    k2<<<dim3((unsigned)d.n_slots, (unsigned)d.Hv), kThreads, CS::BYTES, st>>>(prm);
   if (prm.ws_dqk && d.B * d.T > 0) {
     const int64_t total = d.B * d.T * d.Hk * d.Dk;
     const int blocks = (int)((total + 255) / 256 < 152 * 16 ? (total + 255) / 256 : 152 * 16);
@@ -1024,21 +1036,6 @@ gdn_status launch_bwd(const gdn_problem& p, const Dims& d, const void* q, const 
   prm.N = (int)d.N;
   prm.nt_fixed = d.nt_fixed;
   prm.scale = p.scale;
-  const size_t tok = (size_t)(d.B * d.T);
-  // accumulated outputs start at zero (the library never allocates; memset is stream-ordered)
-  if (tok > 0) {
-    if (prm.ws_dqk) {
-      if (cudaMemsetAsync(prm.ws_dqk, 0, 2 * tok * d.Hv * d.Dk * sizeof(float), st) != cudaSuccess)
-        return GDN_ERR_CUDA;
-    } else {
-      if (cudaMemsetAsync(dq, 0, tok * d.Hk * d.Dk * sizeof(float), st) != cudaSuccess ||
-          cudaMemsetAsync(dk, 0, tok * d.Hk * d.Dk * sizeof(float), st) != cudaSuccess)
-        return GDN_ERR_CUDA;
-    }
-    if (cudaMemsetAsync(dbeta, 0, tok * d.Hv * sizeof(float), st) != cudaSuccess ||
-        cudaMemsetAsync(dg, 0, tok * d.Hv * sizeof(float), st) != cudaSuccess)
-      return GDN_ERR_CUDA;
-  }
   if (d.Dk == 128) return dispatch_bwd<128>(p, prm, d, st);
   return dispatch_bwd<64>(p, prm, d, st);
 }
