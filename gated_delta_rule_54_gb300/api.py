@@ -73,7 +73,8 @@ def gdn_bwd_workspace_bytes(p: GdnProblem) -> int:
 
 
 def gdn_chunk_fwd_qdq(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, state_mode="e4m3",
-                      w_mode="e4m3", output_final_state=True, save_ctx=False, out=None):
+                      w_mode="e4m3", output_final_state=True, save_ctx=False, out=None,
+                      block_v=64):
     """Forward.  q, k [B,T,Hk,Dk] bf16; v [B,T,Hv,Dv] bf16; beta, g [B,T,Hv] f32;
     h0 [N,Hv,Dk,Dv] f32 or None; cu_seqlens [N+1] int32 or None (B == 1).
 
@@ -87,7 +88,7 @@ def gdn_chunk_fwd_qdq(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, sta
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g), ("h0", h0),
                     ("cu_seqlens", cu_seqlens)):
         _check_dev(name, t, dev)
-    p = make_problem(q, k, v, cu_seqlens, scale, state_mode, w_mode)
+    p = make_problem(q, k, v, cu_seqlens, scale, state_mode, w_mode, block_v=block_v)
     check("gdn_validate", lib.gdn_validate(ctypes.byref(p)))
     B, T, Hv, Dv = v.shape
     if out is not None:
@@ -104,7 +105,8 @@ def gdn_chunk_fwd_qdq(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, sta
 
 
 def gdn_chunk_bwd_ste(q, k, v, beta, g, ctx, do, dht=None, cu_seqlens=None, scale=1.0,
-                      state_mode="e4m3", w_mode="e4m3", need_dh0=True, workspace=None, out=None):
+                      state_mode="e4m3", w_mode="e4m3", need_dh0=True, workspace=None, out=None,
+                      block_v=64):
     """Identity-STE backward.  Returns (dq, dk, dv, dbeta, dg, dh0 or None).
 
     ``out`` may pass preallocated (dq, dk, dv, dbeta, dg, dh0) buffers."""
@@ -115,7 +117,7 @@ def gdn_chunk_bwd_ste(q, k, v, beta, g, ctx, do, dht=None, cu_seqlens=None, scal
         _check_dev(name, t, dev)
     if do.dtype != torch.bfloat16:
         raise GdnError("gdn_chunk_bwd_ste", -2)
-    p = make_problem(q, k, v, cu_seqlens, scale, state_mode, w_mode)
+    p = make_problem(q, k, v, cu_seqlens, scale, state_mode, w_mode, block_v=block_v)
     check("gdn_validate", lib.gdn_validate(ctypes.byref(p)))
     f32 = dict(device=dev, dtype=torch.float32)
     if out is not None:
@@ -268,8 +270,8 @@ def split_ctx(ctx: torch.Tensor, p: GdnProblem):
         n = ns * Hv * Dk * Dv
         out["h_codes"] = ctx[off:off + n].view(ns, Hv, Dk, Dv)
         off = al(off + n)
-        m = ns * Hv * (Dv // 64)
-        out["h_scales"] = ctx[off:off + 4 * m].view(torch.float32).view(ns, Hv, Dv // 64)
+        m = ns * Hv * (Dv // p.block_v)
+        out["h_scales"] = ctx[off:off + 4 * m].view(torch.float32).view(ns, Hv, Dv // p.block_v)
     else:
         n = ns * Hv * Dk * Dv
         out["h_full"] = ctx[off:off + 4 * n].view(torch.float32).view(ns, Hv, Dk, Dv)

@@ -53,7 +53,7 @@ CtxLayout ctx_layout(const gdn_problem& p) {
     L.h_codes = off;
     off = align256(off + per_slot);
     L.h_scales = off;
-    off = align256(off + sizeof(float) * (size_t)d.n_slots * d.Hv * (d.Dv / kChunkLen));
+    off = align256(off + sizeof(float) * (size_t)d.n_slots * d.Hv * (d.Dv / p.block_v));
   } else {
     L.h_full = off;
     off = align256(off + sizeof(float) * per_slot);
@@ -76,9 +76,11 @@ static gdn_status validate(const gdn_problem* p) {
     return GDN_ERR_INVALID_ARG;
   }
   if (p->chunk != kChunkLen) return GDN_ERR_UNSUPPORTED_SHAPE;
-  if (p->block_v != kChunkLen) return GDN_ERR_UNSUPPORTED_MODE;
+  if (p->block_v != 16 && p->block_v != 32 && p->block_v != 64 && p->block_v != 128)
+    return GDN_ERR_UNSUPPORTED_MODE;
   if ((p->Dk != 64 && p->Dk != 128) || (p->Dv != 64 && p->Dv != 128))
     return GDN_ERR_UNSUPPORTED_SHAPE;
+  if (p->block_v > p->Dv) return GDN_ERR_UNSUPPORTED_MODE;
   if (p->Hv % p->Hk != 0) return GDN_ERR_UNSUPPORTED_SHAPE;
   if (p->cu_seqlens) {
     if (p->B != 1 || p->N < 1) return GDN_ERR_INVALID_ARG;
@@ -102,7 +104,6 @@ static gdn_status validate_kda(const gdn_problem* p) {
   if (c.chunk < 1) return GDN_ERR_INVALID_ARG;
   if (c.block_v != 16 && c.block_v != 32 && c.block_v != 64) return GDN_ERR_UNSUPPORTED_MODE;
   c.chunk = kChunkLen;
-  c.block_v = kChunkLen;
   const gdn_status s = validate(&c);
   if (s != GDN_OK) return s;
   if (c.N > 65535) return GDN_ERR_UNSUPPORTED_SHAPE;  // grid z

@@ -62,6 +62,8 @@ struct BwdParams {
   const int32_t* cu_seqlens;
   int64_t T, BT;
   int Hk, Hv, Dv, G, N;
+  int block_v;  // state-scale tile width
+  int bv_log2;  // log2(block_v)
   int64_t nt_fixed;
   float scale;
 };
@@ -581,7 +583,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
         const int d = e >> 4, col = (e & 15) * 4;
         float4 x;
         if constexpr (SM != GDN_QDQ_NONE) {
-          const float sH = p.h_scales[(slot * p.Hv + h) * nvb + vb];
+          const float sH = p.h_scales[(slot * p.Hv + h) * (p.Dv >> p.bv_log2) +
+                                      ((vb * 64 + col) >> p.bv_log2)];
           x = qdq_code4_values<SM>(*reinterpret_cast<const uint32_t*>(hst + d * 64 + col));
           x.x *= sH; x.y *= sH; x.z *= sH; x.w *= sH;
         } else {
@@ -1036,6 +1039,8 @@ gdn_status launch_bwd(const gdn_problem& p, const Dims& d, const void* q, const 
   prm.N = (int)d.N;
   prm.nt_fixed = d.nt_fixed;
   prm.scale = p.scale;
+  prm.block_v = p.block_v;
+  prm.bv_log2 = p.block_v == 16 ? 4 : (p.block_v == 32 ? 5 : (p.block_v == 64 ? 6 : 7));
   if (d.Dk == 128) return dispatch_bwd<128>(p, prm, d, st);
   return dispatch_bwd<64>(p, prm, d, st);
 }

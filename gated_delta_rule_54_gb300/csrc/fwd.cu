@@ -37,6 +37,8 @@
 
 #include <mutex>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -71,9 +73,19 @@ struct FwdParams {
   const int32_t* cu_seqlens;
   int64_t T;
   int Hk, Hv, Dv, G, N;
+  int block_v;  // state-scale tile width: 16, 32, 64, or 128 (two value blocks)
+  int bv_log2;  // log2(block_v)
   int64_t nt_fixed;
   float scale;
 };
+
+// state-scale tile of local column c of a 64-column value block
+__device__ __forceinline__ int tile_of(int c, const FwdParams& p) {
+  return p.block_v >= 64 ? 0 : c >> p.bv_log2;
+}
+__device__ __forceinline__ float pick4(const float (&x)[4], int i) {
+  return i == 0 ? x[0] : (i == 1 ? x[1] : (i == 2 ? x[2] : x[3]));
+}
 
 // The chunk stored at a chunk slot (see gdn_qdq.h); false for an unused
 // packed slot.  Uniform across a CTA.
@@ -489,10 +501,13 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
   constexpr bool F8 = SM == GDN_QDQ_E4M3 && WM == GDN_QDQ_E4M3 && DK == 128;
   extern __shared__ __align__(1024) unsigned char sm_raw[];
   unsigned char* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
-  __shared__ float red[kStateWarps];
+  __shared__ float red[kStateWarps][4];  // per-warp partial amax of each state-scale tile
+  __shared__ float xchg[2][2];           // block_v 128: (fail, amax) from the peer value block
   __shared__ __align__(8) uint64_t bars[2];
 
   const int vb = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+  const int bvl = p.block_v < 64 ? p.block_v : 64;  // tile width inside this block
+  const int ntiles = 64 / bvl;
   const int hk = h / p.G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
@@ -532,9 +547,38 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
   const int h_row0 = (warp % HM) * 16;
   const int h_col0 = (warp / HM) * (64 / HN);
   float hreg[NTH][4];
+  // per-warp partial amax of every state-scale tile of the block -> red
+  auto tile_partials = [&]() {
+    if (ntiles == 1) {
+      float m = 0.f;
+#pragma unroll
+      for (int nt = 0; nt < NTH; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(hreg[nt][e]));
+      m = warp_max(m);
+      if (lane == 0) red[warp][0] = m;
+      return;
+    }
+    float mt[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int nt = 0; nt < NTH; ++nt) {
+      float m = 0.f;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(hreg[nt][e]));
+      const int t = tile_of(h_col0 + nt * 8, p);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mt[i] = (i == t) ? fmaxf(mt[i], m) : mt[i];
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (i < ntiles) {
+        const float m = warp_max(mt[i]);
+        if (lane == 0) red[warp][i] = m;
+      }
+    }
+  };
   {
     const float* src = p.h0 ? p.h0 + (((int64_t)n * p.Hv + h) * DK) * p.Dv + vb * 64 : nullptr;
-    float m = 0.f;
 #pragma unroll
     for (int nt = 0; nt < NTH; ++nt)
 #pragma unroll
@@ -544,10 +588,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
         if (src) v2 = *reinterpret_cast<const float2*>(src + (int64_t)d * p.Dv + c);
         hreg[nt][2 * e2] = v2.x;
         hreg[nt][2 * e2 + 1] = v2.y;
-        m = fmaxf(m, fmaxf(fabsf(v2.x), fabsf(v2.y)));
       }
-    m = warp_max(m);
-    if (lane == 0) red[warp] = m;
+    tile_partials();
   }
   if (threadIdx.x == 0) {
     mbar_init(&bars[0], 1);
@@ -572,7 +614,33 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
     cp_async_wait<0>();
     if (threadIdx.x == 0) tma_store_wait_read();  // the codes store of chunk c - 1 has read Hst
     // chunk c landed; amax partials of H visible; buffer buf ^ 1 free
-    if (__syncthreads_or(!ok)) {
+    bool fail = __syncthreads_or(!ok);
+    // tile amax of the state entering chunk c
+    float amx[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (i < ntiles) {
+        float a = red[0][i];
+#pragma unroll
+        for (int w = 1; w < kStateWarps; ++w) a = fmaxf(a, red[w][i]);
+        amx[i] = a;
+      }
+    }
+    if (p.block_v == 128) {
+      // one scale across both value blocks: the pair of CTAs (a cluster) swaps
+      // its block amax, and its failure flag so that both leave together
+      namespace cg = cooperative_groups;
+      cg::cluster_group cl = cg::this_cluster();
+      if (threadIdx.x == 0) {
+        float* peer = cl.map_shared_rank(&xchg[c & 1][0], (int)(cl.block_rank() ^ 1));
+        peer[0] = fail ? 1.f : 0.f;
+        peer[1] = amx[0];
+      }
+      cl.sync();
+      fail = fail || xchg[c & 1][0] != 0.f;
+      amx[0] = fmaxf(amx[0], xchg[c & 1][1]);
+    }
+    if (fail) {
       if (threadIdx.x == 0) {
         atomicOr(&g_fwd_device_error, 1);
         mbar_wait(&bars[buf], (uint32_t)(c >> 1) & 1u);  // once more, bounded, for the copies in flight
@@ -614,18 +682,24 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
       }
     }
 
-    // ---- a6: state QDQ over the [DK x 64] tile ----
-    float sH = 1.f;
+    // ---- a6: state QDQ per [DK x block_v] tile ----
+    float sHt[4] = {1.f, 1.f, 1.f, 1.f}, rct[4] = {0.f, 0.f, 0.f, 0.f};
+    if constexpr (SM != GDN_QDQ_NONE) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (i < ntiles) {
+          qdq_scale<SM>(amx[i], sHt[i], rct[i]);
+          if (amx[i] == 0.f) sHt[i] = 0.f;
+        }
+      }
+    }
     {
-      float amax = red[0];
-#pragma unroll
-      for (int i = 1; i < kStateWarps; ++i) amax = fmaxf(amax, red[i]);
       if constexpr (F8) {
-        float rcp;
-        qdq_scale<SM>(amax, sH, rcp);
-        const bool zero = amax == 0.f;
 #pragma unroll
-        for (int nt = 0; nt < NTH; ++nt)
+        for (int nt = 0; nt < NTH; ++nt) {
+          const int t = tile_of(h_col0 + nt * 8, p);
+          const float sH = pick4(sHt, t), rcp = pick4(rct, t);
+          const bool zero = pick4(amx, t) == 0.f;
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             const int d = h_row0 + gq + 8 * e2, col = h_col0 + nt * 8 + 2 * tq;
@@ -642,13 +716,14 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
             hb[0] = (uint8_t)(c2 & 0xff);
             hb[2 * swz<64>(col + 1, d >> 1) - 2 * swz<64>(col, d >> 1)] = (uint8_t)(c2 >> 8);
           }
-        if (zero) sH = 0.f;
+        }
         fence_proxy_async();  // Hst is read by the TMA store below
       } else if constexpr (SM != GDN_QDQ_NONE) {
-        float rcp;
-        qdq_scale<SM>(amax, sH, rcp);
 #pragma unroll
-        for (int nt = 0; nt < NTH; ++nt)
+        for (int nt = 0; nt < NTH; ++nt) {
+          const int t = tile_of(h_col0 + nt * 8, p);
+          const float sH = pick4(sHt, t), rcp = pick4(rct, t);
+          const float amax = pick4(amx, t);
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             const int d = h_row0 + gq + 8 * e2, col = h_col0 + nt * 8 + 2 * tq;
@@ -669,7 +744,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
             st_bf16x2(HcH + swz<64>(d, col), v0, v1);
             *reinterpret_cast<uint16_t*>(Hst + d * 64 + col) = (uint16_t)(c0 | (c1 << 8));
           }
-        if (amax == 0.f) sH = 0.f;
+        }
         fence_proxy_async();  // Hst is read by the TMA store below
       } else {
 #pragma unroll
@@ -693,7 +768,14 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
       if constexpr (SM != GDN_QDQ_NONE) {
         tma_store_2d(&p.tm_hc, vb * 64, (int)((slot * p.Hv + h) * DK), Hst);
         tma_store_commit();
-        p.h_scales[(slot * p.Hv + h) * (p.Dv / 64) + vb] = sH;
+        // scales [slot, Hv, Dv / block_v]
+        if (p.block_v == 128) {
+          if (vb == 0) p.h_scales[slot * p.Hv + h] = sHt[0];
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            if (i < ntiles) p.h_scales[(slot * p.Hv + h) * (p.Dv / bvl) + vb * ntiles + i] = sHt[i];
+        }
       }
     }
     // prefetch chunk c + 1 (buffer buf ^ 1 was last read before this iteration's first barrier)
@@ -724,10 +806,11 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
         if constexpr (WM == GDN_QDQ_NONE) wgemm<2, false, true, DK, 64>(dacc, WcL, row0, HcH, col0, 0, DK, lane);
         if constexpr (SM == GDN_QDQ_NONE) wgemm<2, false, true, DK, 64>(dacc, WcH, row0, HcL, col0, 0, DK, lane);
       }
-      const float sWH = (WM != GDN_QDQ_NONE ? sW : 1.f) * (SM != GDN_QDQ_NONE ? sH : 1.f);
       const float* Us = Ubuf(buf);
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 2; ++nt) {
+        const float sWH = (WM != GDN_QDQ_NONE ? sW : 1.f) *
+                          (SM != GDN_QDQ_NONE ? pick4(sHt, tile_of(col0 + nt * 8, p)) : 1.f);
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -739,12 +822,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
           st_bf16x2(DpH + swz<64>(i, j), h0v, h1v);
           st_bf16x2(DpL + swz<64>(i, j), l0v, l1v);
         }
+      }
     }
     __syncthreads();  // Delta' ready
 
     // ---- a9: H <- e^{gamma_L} H^ + K^T Delta' (K rows >= Lc meet zero rows of Delta') ----
     {
-      float m = 0.f;
 #pragma unroll
       for (int nt = 0; nt < NTH; ++nt)
 #pragma unroll
@@ -752,12 +835,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
       const __nv_bfloat16* Ks = Kbuf(buf);
       wgemm<NTH, true, true, DK, 64>(hreg, Ks, h_row0, DpH, h_col0, 0, 64, lane);
       wgemm<NTH, true, true, DK, 64>(hreg, Ks, h_row0, DpL, h_col0, 0, 64, lane);
-#pragma unroll
-      for (int nt = 0; nt < NTH; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(hreg[nt][e]));
-      m = warp_max(m);
-      if (lane == 0) red[warp] = m;
+      tile_partials();
     }
   }
   cp_async_wait<0>();
@@ -860,7 +938,7 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
     if constexpr (SM != GDN_QDQ_NONE)
       tma_load_2d(Hraw, &p.tm_hc, vb * 64, (int)((slot * p.Hv + h) * DK), &bar);
   }
-  float sW = 1.f, sH = 1.f;
+  float sW = 1.f;
   if constexpr (WM != GDN_QDQ_NONE) {
     sW = p.w_scales[slot * p.Hv + h];
   } else {
@@ -879,8 +957,16 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
       *reinterpret_cast<uint2*>(WcL + e) = make_uint2(pack_bf16(l0v, l1v), pack_bf16(l2v, l3v));
     }
   }
+  float sHt[4] = {1.f, 1.f, 1.f, 1.f};  // scale of each state-scale tile of this block
   if constexpr (SM != GDN_QDQ_NONE) {
-    sH = p.h_scales[(slot * p.Hv + h) * nvb + vb];
+    if (p.block_v == 128) {
+      sHt[0] = p.h_scales[slot * p.Hv + h];
+    } else {
+      const int nt_b = 64 / p.block_v;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (i < nt_b) sHt[i] = p.h_scales[(slot * p.Hv + h) * (p.Dv / p.block_v) + vb * nt_b + i];
+    }
   } else {
     const float* src = p.h_full + ((slot * p.Hv + h) * DK) * p.Dv + vb * 64;
     for (int i = threadIdx.x; i < DK * 16; i += kOutThreads) {
@@ -945,11 +1031,12 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
   if constexpr (SM == GDN_QDQ_NONE) wgemm<4, false, true, DK, 64>(qacc, Qs, row0, HcL, col0, 0, DK, lane);
   __syncthreads();  // K reads done (its tile becomes Delta)
 
-  const float sWH = (WM != GDN_QDQ_NONE ? sW : 1.f) * (SM != GDN_QDQ_NONE ? sH : 1.f);
   // value block 0 also saves P (bf16; rows >= L zero) as the backward's tile image
   __nv_bfloat16* pimg = vb == 0 ? p.pb + (slot * p.Hv + h) * (kTileImgBytes / 2) : nullptr;
 #pragma unroll
-  for (int nt = 0; nt < 4; ++nt)
+  for (int nt = 0; nt < 4; ++nt) {
+    const float sWH = (WM != GDN_QDQ_NONE ? sW : 1.f) *
+                      (SM != GDN_QDQ_NONE ? pick4(sHt, tile_of(col0 + nt * 8, p)) : 1.f);
 #pragma unroll
     for (int e2 = 0; e2 < 2; ++e2) {
       const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -973,6 +1060,7 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
       st_bf16x2(DH + swz<64>(i, j), h0v, h1v);
       st_bf16x2(DL + swz<64>(i, j), l0v, l1v);
     }
+  }
   __syncthreads();  // P, Delta ready; U reads done (its tile becomes the O staging)
 
   {
@@ -982,12 +1070,12 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
     wgemm<4, false, true, 64, 64>(o2, PH, row0, DH, col0, 0, kend, lane);
     wgemm<4, false, true, 64, 64>(o2, PH, row0, DL, col0, 0, kend, lane);
     wgemm<4, false, true, 64, 64>(o2, PL, row0, DH, col0, 0, kend, lane);
-    const float sq = (SM != GDN_QDQ_NONE) ? sH : 1.f;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
+        const float sq = (SM != GDN_QDQ_NONE) ? pick4(sHt, tile_of(col0 + nt * 8, p)) : 1.f;
         const float ei = eg[i] * sq;
         *reinterpret_cast<float2*>(Ost + swz_f32(i, j)) =
             make_float2(p.scale * (ei * qacc[nt][2 * e2] + o2[nt][2 * e2]),
@@ -1037,9 +1125,29 @@ gdn_status launch_t(const FwdParams& prm, const Dims& d, cudaStream_t st) {
   }
   auto k2 = gdn_fwd_state_kernel<DK, SM, WM>;
   if (set_smem(k2, StateSmem<DK, SM, WM>::BYTES) != GDN_OK) return GDN_ERR_CUDA;
-  k2<<<dim3((unsigned)nvb, (unsigned)d.Hv, (unsigned)d.N), kStateThreads,
-       StateSmem<DK, SM, WM>::BYTES, st>>>(prm);
-  if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+  {
+    // block_v 128: the two value blocks of a (sequence, head) share a state
+    // scale and run as a 2-CTA cluster that swaps the block amax every chunk
+    const dim3 grid((unsigned)nvb, (unsigned)d.Hv, (unsigned)d.N);
+    if (prm.block_v == 128) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = grid;
+      cfg.blockDim = dim3(kStateThreads);
+      cfg.dynamicSmemBytes = StateSmem<DK, SM, WM>::BYTES;
+      cfg.stream = st;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaLaunchKernelEx(&cfg, k2, prm) != cudaSuccess) return GDN_ERR_CUDA;
+    } else {
+      k2<<<grid, kStateThreads, StateSmem<DK, SM, WM>::BYTES, st>>>(prm);
+      if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+    }
+  }
   if (d.B * d.T > 0 && d.n_slots > 0) {
     auto k3 = gdn_fwd_output_kernel<DK, SM, WM>;
     if (set_smem(k3, OutSmem<DK, SM, WM>::BYTES) != GDN_OK) return GDN_ERR_CUDA;
@@ -1150,6 +1258,9 @@ gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const 
   prm.N = (int)d.N;
   prm.nt_fixed = d.nt_fixed;
   prm.scale = p.scale;
+  prm.block_v = p.block_v;
+  prm.bv_log2 = p.block_v == 16 ? 4 : (p.block_v == 32 ? 5 : (p.block_v == 64 ? 6 : 7));
+  if (p.block_v == 128 && d.Dv != 128) return GDN_ERR_UNSUPPORTED_MODE;
   const uint64_t tok = (uint64_t)(d.B * d.T);
   if (tok > 0) {
     // 32-bit TMA coordinates: state-code rows of all slots must fit

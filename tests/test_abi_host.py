@@ -50,6 +50,8 @@ def test_validate_accepts_supported_problems():
     assert _validate(_problem(state_mode=0, w_mode=0)) == 0
     assert _validate(_problem(B=1, N=5, cu_seqlens=4096)) == 0
     assert _validate(_problem(T=0)) == 0
+    for bv in (16, 32, 128):
+        assert _validate(_problem(block_v=bv)) == 0
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -59,7 +61,7 @@ def test_validate_accepts_supported_problems():
     (dict(Dk=96), -3), (dict(Dv=256), -3),
     (dict(Hv=3), -3),                    # Hv % Hk
     (dict(chunk=32), -3),
-    (dict(block_v=32), -4),
+    (dict(block_v=48), -4), (dict(block_v=128, Dv=64), -4),
     (dict(state_mode=3), -1), (dict(w_mode=-1), -1),
     (dict(B=-1), -1), (dict(Hk=0), -1),
     (dict(N=3), -1),                     # N != B without cu_seqlens

@@ -18,24 +18,24 @@ pytestmark = pytest.mark.gpu
 NAMES = ("dq", "dk", "dv", "dbeta", "dg", "dh0")
 
 
-def _grads_gpu(d, sm, wm, do, dht, scale=1.0):
+def _grads_gpu(d, sm, wm, do, dht, scale=1.0, block_v=64):
     dd = to_dev(d)
     cu = dd["cu_seqlens"]
     o, ht, ctx = gdn_chunk_fwd_qdq(dd["q"], dd["k"], dd["v"], dd["beta"], dd["g"], dd["h0"],
                                    cu_seqlens=cu, scale=scale, state_mode=sm, w_mode=wm,
-                                   save_ctx=True)
+                                   save_ctx=True, block_v=block_v)
     gr = gdn_chunk_bwd_ste(dd["q"], dd["k"], dd["v"], dd["beta"], dd["g"], ctx, do.cuda(),
                            dht.cuda() if dht is not None else None, cu_seqlens=cu, scale=scale,
-                           state_mode=sm, w_mode=wm)
+                           state_mode=sm, w_mode=wm, block_v=block_v)
     torch.cuda.synchronize()
     return [x.cpu().double().numpy() for x in gr]
 
 
-def _grads_oracle(d, sm, wm, do, dht, scale=1.0, cu=None):
+def _grads_oracle(d, sm, wm, do, dht, scale=1.0, cu=None, block_v=64):
     N, Hv = d["N"], d["v"].shape[2]
     h0 = d["h0"] if d["h0"] is not None else torch.zeros(N, Hv, d["k"].shape[3], d["v"].shape[3])
     xs = [t.double().requires_grad_(True) for t in (d["q"], d["k"], d["v"], d["beta"], d["g"], h0)]
-    o, ht = chunked(*xs, cu_seqlens=cu, scale=scale, state_mode=sm, w_mode=wm)
+    o, ht = chunked(*xs, cu_seqlens=cu, scale=scale, state_mode=sm, w_mode=wm, block_v=block_v)
     loss = (o * do.double()).sum() + ((ht * dht.double()).sum() if dht is not None else 0.0)
     return [g.numpy() for g in torch.autograd.grad(loss, xs)]
 
@@ -48,11 +48,11 @@ def _dO(w, d, seed=11, with_dht=True):
     return do, dht
 
 
-def _check(w, lengths=None, scale=1.0, with_dht=True):
+def _check(w, lengths=None, scale=1.0, with_dht=True, block_v=64):
     d = synth.make_inputs(w, lengths=lengths)
     do, dht = _dO(w, d, with_dht=with_dht)
-    g = _grads_gpu(d, w.state_mode, w.w_mode, do, dht, scale)
-    r = _grads_oracle(d, w.state_mode, w.w_mode, do, dht, scale, d["cu_seqlens"])
+    g = _grads_gpu(d, w.state_mode, w.w_mode, do, dht, scale, block_v=block_v)
+    r = _grads_oracle(d, w.state_mode, w.w_mode, do, dht, scale, d["cu_seqlens"], block_v=block_v)
     errs = {}
     for name, a, b in zip(NAMES, g, r):
         assert np.isfinite(a).all(), name
@@ -71,6 +71,13 @@ def test_bwd_modes(sm, wm):
     w = synth.small(B=2, T=200, Hk=2, Hv=2, Dk=128, Dv=128, state_mode=sm, w_mode=wm, h0=True,
                     seed=21)
     _check(w)
+
+
+@pytest.mark.parametrize("block_v", [16, 32, 128])
+def test_bwd_state_scale_widths(block_v):
+    w = synth.small(B=2, T=150, Hk=1, Hv=2, Dk=128, Dv=128, state_mode="int8", h0=True,
+                    seed=40 + block_v)
+    _check(w, block_v=block_v)
 
 
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 130])

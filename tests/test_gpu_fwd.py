@@ -18,21 +18,21 @@ from _parity import (assert_close, assert_close_units, assert_codes, code_steps,
 pytestmark = pytest.mark.gpu
 
 
-def _gpu_fwd(d, sm, wm, scale=1.0, save_ctx=True):
+def _gpu_fwd(d, sm, wm, scale=1.0, save_ctx=True, block_v=64):
     dd = to_dev(d)
     o, ht, ctx = gdn_chunk_fwd_qdq(dd["q"], dd["k"], dd["v"], dd["beta"], dd["g"], dd["h0"],
                                    cu_seqlens=dd["cu_seqlens"], scale=scale, state_mode=sm,
-                                   w_mode=wm, save_ctx=save_ctx)
+                                   w_mode=wm, save_ctx=save_ctx, block_v=block_v)
     torch.cuda.synchronize()
     return dd, o, ht, ctx
 
 
-def _check_case(w, lengths=None, scale=1.0):
+def _check_case(w, lengths=None, scale=1.0, block_v=64):
     d = synth.make_inputs(w, lengths=lengths)
     sm, wm = w.state_mode, w.w_mode
-    dd, o, ht, ctx = _gpu_fwd(d, sm, wm, scale)
-    o_ref, ht_ref, rec = run_oracle(d, sm, wm, scale=scale, record=True)
-    p = make_problem(dd["q"], dd["k"], dd["v"], dd["cu_seqlens"], scale, sm, wm)
+    dd, o, ht, ctx = _gpu_fwd(d, sm, wm, scale, block_v=block_v)
+    o_ref, ht_ref, rec = run_oracle(d, sm, wm, scale=scale, record=True, block_v=block_v)
+    p = make_problem(dd["q"], dd["k"], dd["v"], dd["cu_seqlens"], scale, sm, wm, block_v=block_v)
     seg = split_ctx(ctx, p)
     packed = lengths is not None
     lens = list(lengths) if packed else [w.T] * w.B
@@ -108,6 +108,20 @@ def test_fwd_modes(sm, wm):
     w = synth.small(B=2, T=200, Hk=2, Hv=4, Dk=128, Dv=128, state_mode=sm, w_mode=wm, h0=True,
                     seed=3)
     _check_case(w)
+
+
+@pytest.mark.parametrize("block_v", [16, 32, 128])
+@pytest.mark.parametrize("sm,wm", [("e4m3", "e4m3"), ("int8", "e4m3"), ("int8", "int8")])
+def test_fwd_state_scale_widths(sm, wm, block_v):
+    """[Dk, block_v] state-scale tiles other than 64 ("[2/4] GDN/KDA decode QAT
+    with INT8 recurrent state", "Testing": all state scale widths); 128 spans
+    both value blocks."""
+    w = synth.small(B=2, T=150, Hk=2, Hv=2, Dk=128, Dv=128, state_mode=sm, w_mode=wm, h0=True,
+                    seed=block_v)
+    _check_case(w, block_v=block_v)
+    w = synth.small(B=1, T=0, Hk=1, Hv=2, Dk=64, Dv=128, state_mode=sm, w_mode=wm, h0=True,
+                    seed=block_v + 1)
+    _check_case(w, lengths=[70, 1, 129], block_v=block_v)
 
 
 @pytest.mark.parametrize("T", [1, 3, 63, 64, 65, 127, 128, 257])
