@@ -53,7 +53,22 @@ def qdq_ste(x: torch.Tensor, mode: str, group_cols: int, record=None):
     return x + (y - x).detach()
 
 
-def _chunk_step(Qc, Kc, Vc, bc, gc, H, scale, state_mode, w_mode, block_v, rec, inter):
+def neumann_inverse(A, degree):
+    """T = sum_{i=0..degree} (-A)^i, the Neumann polynomial for (I + A)^-1 of a
+    strictly lower-triangular A ("[7/7] Experimental GDN/KDA approximate-inverse
+    QAT", "What does this PR do?": an explicit polynomial degree, the backward
+    differentiating the actual polynomial).  Exact once degree >= L - 1."""
+    L = A.shape[-1]
+    eye = torch.eye(L, dtype=A.dtype).expand(A.shape)
+    T, Xp = eye, eye
+    for _ in range(degree):
+        Xp = Xp @ (-A)
+        T = T + Xp
+    return T
+
+
+def _chunk_step(Qc, Kc, Vc, bc, gc, H, scale, state_mode, w_mode, block_v, rec, inter,
+                neumann_degree=None):
     """One chunk for a batch of value-head problems. Qc,Kc [S,L,Dk]; Vc [S,L,Dv];
     bc,gc [S,L]; H [S,Dk,Dv].  Returns (O [S,L,Dv], H_next)."""
     S, L, Dk = Kc.shape
@@ -67,7 +82,10 @@ def _chunk_step(Qc, Kc, Vc, bc, gc, H, scale, state_mode, w_mode, block_v, rec, 
     KK = Kc @ Kc.transpose(-1, -2)
     A = torch.where(strict, bc[:, :, None] * Gam * KK, torch.zeros((), dtype=dt))  # a2
     eye = torch.eye(L, dtype=dt).expand(S, L, L)
-    T = torch.linalg.solve_triangular(eye + A, eye, upper=False, unitriangular=True)  # a3
+    if neumann_degree is None:
+        T = torch.linalg.solve_triangular(eye + A, eye, upper=False, unitriangular=True)  # a3
+    else:
+        T = neumann_inverse(A, neumann_degree)
     W = T @ ((bc * torch.exp(gam))[:, :, None] * Kc)                  # a4
     U = T @ (bc[:, :, None] * Vc)
     Wh = qdq_ste(W, w_mode, Dk, rec["w"] if rec is not None else None)      # a5
@@ -84,7 +102,8 @@ def _chunk_step(Qc, Kc, Vc, bc, gc, H, scale, state_mode, w_mode, block_v, rec, 
     return O, Hn
 
 
-def _run_equal(q, k, v, beta, g, h0, scale, state_mode, w_mode, chunk, block_v, rec, inter):
+def _run_equal(q, k, v, beta, g, h0, scale, state_mode, w_mode, chunk, block_v, rec, inter,
+               neumann_degree=None):
     """Equal-length batch. q,k [S,L,Hk,Dk]; v [S,L,Hv,Dv]; beta,g [S,L,Hv]; h0 [S,Hv,Dk,Dv]."""
     S, L, Hk, Dk = k.shape
     Hv, Dv = v.shape[2], v.shape[3]
@@ -101,7 +120,8 @@ def _run_equal(q, k, v, beta, g, h0, scale, state_mode, w_mode, chunk, block_v, 
     for c0 in range(0, L, chunk):
         c1 = min(L, c0 + chunk)
         O, H = _chunk_step(qv[:, c0:c1], kv[:, c0:c1], vv[:, c0:c1], bv[:, c0:c1],
-                           gv[:, c0:c1], H, scale, state_mode, w_mode, block_v, rec, inter)
+                           gv[:, c0:c1], H, scale, state_mode, w_mode, block_v, rec, inter,
+                           neumann_degree)
         outs.append(O)
     o = torch.cat(outs, dim=1) if outs else vv.new_zeros(S * Hv, 0, Dv)
     o = o.reshape(S, Hv, L, Dv).permute(0, 2, 1, 3)
@@ -109,8 +129,11 @@ def _run_equal(q, k, v, beta, g, h0, scale, state_mode, w_mode, chunk, block_v, 
 
 
 def chunked(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, state_mode="none",
-            w_mode="none", chunk=64, block_v=64, record=False, intermediates=False):
+            w_mode="none", chunk=64, block_v=64, record=False, intermediates=False,
+            neumann_degree=None):
     """O2.  Tensors are torch CPU; they are used in fp64 (bf16 widens exactly).
+    ``neumann_degree`` replaces the exact solve by the Neumann polynomial of that
+    degree (see neumann_inverse).
 
     q, k [B,T,Hk,Dk]; v [B,T,Hv,Dv]; beta, g [B,T,Hv]; h0 [N,Hv,Dk,Dv] or None;
     cu_seqlens [N+1] (B == 1) or None.  Differentiable in every float input.
@@ -139,7 +162,7 @@ def chunked(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, state_mode="n
         rec = {"w": [], "s": []} if record else None
         inter = [] if intermediates else None
         o, ht = _run_equal(q, k, v, beta, g, h0, scale, state_mode, w_mode, chunk, block_v,
-                           rec, inter)
+                           rec, inter, neumann_degree)
         recs.append((rec, B, T))
         inters.append(inter)
     else:
@@ -150,7 +173,7 @@ def chunked(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, state_mode="n
             inter = [] if intermediates else None
             o_n, h_n = _run_equal(q[:, sl], k[:, sl], v[:, sl], beta[:, sl], g[:, sl],
                                   h0[n:n + 1], scale, state_mode, w_mode, chunk, block_v,
-                                  rec, inter)
+                                  rec, inter, neumann_degree)
             os_.append(o_n)
             hts.append(h_n)
             recs.append((rec, 1, L))

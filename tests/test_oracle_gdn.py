@@ -261,3 +261,53 @@ def test_qdq_ste_backward_is_identity():
         assert torch.equal(gx, wgt)
         ref, _ = oracle.qdq_groups(x.detach().float().numpy(), 8, mode)
         assert np.array_equal(y.detach().float().numpy(), ref)
+
+
+# ---- Neumann approximate inverse ("[7/7] Experimental GDN/KDA approximate-inverse QAT") ----
+from oracle.chunked import neumann_inverse
+
+
+def test_neumann_inverse_identities():
+    """(I + A) T_d = I - (-A)^{d+1} (the residual identity of the polynomial);
+    degree 0 is I; the product form prod_j (I + X^{2^j}) equals the sum for
+    d = 2^m - 1; degree >= L - 1 is the exact inverse (A is nilpotent)."""
+    rng = np.random.default_rng(5)
+    L = 24
+    A = torch.from_numpy(np.tril(rng.standard_normal((2, L, L)) * 0.3, -1))
+    I = torch.eye(L, dtype=torch.float64)
+    for d in (0, 1, 3, 7, 10):
+        T = neumann_inverse(A, d)
+        Xd1 = torch.linalg.matrix_power(-A, d + 1)
+        assert ((I + A) @ T - (I - Xd1)).abs().max() <= 1e-12 * max(1.0, Xd1.abs().max().item())
+    assert torch.equal(neumann_inverse(A, 0), I.expand(2, L, L))
+    X = -A
+    prod = (I + X) @ (I + X @ X) @ (I + torch.linalg.matrix_power(X, 4))
+    assert (prod - neumann_inverse(A, 7)).abs().max() <= 1e-12 * prod.abs().max()
+    exact = torch.linalg.solve_triangular(I + A, I.expand(2, L, L), upper=False, unitriangular=True)
+    assert (neumann_inverse(A, L - 1) - exact).abs().max() <= 1e-10 * exact.abs().max()
+
+
+def test_chunked_neumann_degree_63_is_the_exact_solve():
+    w = synth.small(B=1, T=150, Hk=1, Hv=2, Dk=32, Dv=64, h0=True, seed=12)
+    d = synth.make_inputs(w)
+    o1, h1 = chunked(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], state_mode="e4m3",
+                     w_mode="e4m3")
+    o2, h2 = chunked(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], state_mode="e4m3",
+                     w_mode="e4m3", neumann_degree=63)
+    assert (o1 - o2).abs().max() <= 1e-9 * o1.abs().max()
+    assert (h1 - h2).abs().max() <= 1e-9 * h1.abs().max()
+    o3, _ = chunked(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], state_mode="e4m3",
+                    w_mode="e4m3", neumann_degree=3)
+    assert (o1 - o3).abs().max() > 1e-6 * o1.abs().max()   # a low degree is not the inverse
+
+
+def test_gradcheck_chunked_neumann():
+    """The backward differentiates the actual polynomial."""
+    w = synth.small(B=1, T=20, Hk=1, Hv=1, Dk=4, Dv=3, h0=True, seed=13)
+    d = synth.make_inputs(w)
+    xs = [d[n].double().requires_grad_(True) for n in ("q", "k", "v", "beta", "g", "h0")]
+
+    def f(*a):
+        o, ht = chunked(*a, chunk=8, neumann_degree=3)
+        return o.sum() + (ht * ht).sum()
+    assert torch.autograd.gradcheck(f, xs, eps=1e-6, atol=1e-7, rtol=1e-6)
