@@ -261,7 +261,8 @@ def run_ours(args, ws, rank, local):
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in cpu.items()}
     q, k, v, beta, g, h0 = d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"]
     sm, wm = w.state_mode, w.w_mode
-    p = api.make_problem(q, k, v, None, 1.0, sm, wm)
+    bv, nd = args.block_v, args.neumann_degree
+    p = api.make_problem(q, k, v, None, 1.0, sm, wm, block_v=bv, neumann_degree=nd)
     o = torch.empty(w.B, w.T, w.Hv, w.Dv, device=dev)
     ht = torch.empty(w.B, w.Hv, w.Dk, w.Dv, device=dev)
     ctx = torch.empty(api.gdn_ctx_bytes(p), device=dev, dtype=torch.uint8)
@@ -279,14 +280,15 @@ def run_ours(args, ws, rank, local):
         e0 = ev() if record else None
         if record:
             e0.record(stream)
-        api.gdn_chunk_fwd_qdq(q, k, v, beta, g, h0, state_mode=sm, w_mode=wm, out=(o, ht, ctx))
+        api.gdn_chunk_fwd_qdq(q, k, v, beta, g, h0, state_mode=sm, w_mode=wm, out=(o, ht, ctx),
+                              block_v=bv, neumann_degree=nd)
         if record:
             e1 = ev()
             e1.record(stream)
             fwd_times.append((e0, e1))
         if bwd:
             api.gdn_chunk_bwd_ste(q, k, v, beta, g, ctx, do, dht, state_mode=sm, w_mode=wm,
-                                  workspace=wsb)
+                                  workspace=wsb, block_v=bv, neumann_degree=nd)
             if record:
                 e2 = ev()
                 e2.record(stream)
@@ -356,10 +358,11 @@ def run_ours(args, ws, rank, local):
             for n, t in bufs.items():
                 if t is not None:
                     t.copy_(host[n], non_blocking=True)
-            api.gdn_chunk_fwd_qdq(q, k, v, beta, g, h0, state_mode=sm, w_mode=wm, out=(o, ht, ctx))
+            api.gdn_chunk_fwd_qdq(q, k, v, beta, g, h0, state_mode=sm, w_mode=wm, out=(o, ht, ctx),
+                                  block_v=bv, neumann_degree=nd)
             if bwd:
                 api.gdn_chunk_bwd_ste(q, k, v, beta, g, ctx, do, dht, state_mode=sm, w_mode=wm,
-                                      workspace=wsb, out=grads)
+                                      workspace=wsb, out=grads, block_v=bv, neumann_degree=nd)
             for dst, src in zip(res_h, results):
                 dst.copy_(src, non_blocking=True)
 
@@ -389,7 +392,9 @@ def run_ours(args, ws, rank, local):
         "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), beta=sigmoid, g=-softplus)",
         "config": {"workload": w.name, "mode": args.mode, "B": w.B, "T": w.T, "Hk": w.Hk,
                    "Hv": w.Hv, "Dk": w.Dk, "Dv": w.Dv, "state_mode": sm, "w_mode": wm,
-                   "chunk": 64, "block_v": 64, "global_batch_tokens": w.B * w.T * ws,
+                   "chunk": 64, "block_v": bv,
+                   "solve": "exact" if nd is None else "neumann degree %d" % nd,
+                   "global_batch_tokens": w.B * w.T * ws,
                    "l2": "inputs larger than L2 (no flush needed)",
                    "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(bwd_ms, 4) if bwd else None,
                    "fwd_tflops_alg": round(fwd_alg_flops(w) / (fwd_ms / 1e3) / 1e12, 2)},
@@ -729,6 +734,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--block-v", type=int, default=64, help="state-scale tile width")
+    ap.add_argument("--neumann-degree", type=int, default=None,
+                    help="Neumann approximate inverse of this degree instead of the exact solve")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.mode is None:

@@ -33,7 +33,8 @@ class GdnProblem(ctypes.Structure):
         ("Hk", ctypes.c_int32), ("Hv", ctypes.c_int32), ("Dk", ctypes.c_int32), ("Dv", ctypes.c_int32),
         ("N", ctypes.c_int32), ("cu_seqlens", ctypes.c_void_p), ("scale", ctypes.c_float),
         ("state_mode", ctypes.c_int32), ("w_mode", ctypes.c_int32), ("block_v", ctypes.c_int32),
-        ("chunk", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("chunk", ctypes.c_int32), ("dtype", ctypes.c_int32), ("solve", ctypes.c_int32),
+        ("solve_degree", ctypes.c_int32),
     ]
 
 

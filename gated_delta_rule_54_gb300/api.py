@@ -33,7 +33,7 @@ def _mode(m) -> int:
 
 
 def make_problem(q, k, v, cu_seqlens=None, scale=1.0, state_mode="e4m3", w_mode="e4m3",
-                 block_v=64, chunk=64, N=None) -> GdnProblem:
+                 block_v=64, chunk=64, N=None, neumann_degree=None) -> GdnProblem:
     B, T, Hk, Dk = k.shape
     Hv, Dv = v.shape[2], v.shape[3]
     p = GdnProblem()
@@ -44,6 +44,8 @@ def make_problem(q, k, v, cu_seqlens=None, scale=1.0, state_mode="e4m3", w_mode=
     p.state_mode, p.w_mode = _mode(state_mode), _mode(w_mode)
     p.block_v, p.chunk = block_v, chunk
     p.dtype = _DT.get(q.dtype, 99)
+    p.solve = 0 if neumann_degree is None else 1
+    p.solve_degree = 0 if neumann_degree is None else int(neumann_degree)
     return p
 
 
@@ -74,7 +76,7 @@ def gdn_bwd_workspace_bytes(p: GdnProblem) -> int:
 
 def gdn_chunk_fwd_qdq(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, state_mode="e4m3",
                       w_mode="e4m3", output_final_state=True, save_ctx=False, out=None,
-                      block_v=64):
+                      block_v=64, neumann_degree=None):
     """Forward.  q, k [B,T,Hk,Dk] bf16; v [B,T,Hv,Dv] bf16; beta, g [B,T,Hv] f32;
     h0 [N,Hv,Dk,Dv] f32 or None; cu_seqlens [N+1] int32 or None (B == 1).
 
@@ -88,7 +90,8 @@ def gdn_chunk_fwd_qdq(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, sta
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g), ("h0", h0),
                     ("cu_seqlens", cu_seqlens)):
         _check_dev(name, t, dev)
-    p = make_problem(q, k, v, cu_seqlens, scale, state_mode, w_mode, block_v=block_v)
+    p = make_problem(q, k, v, cu_seqlens, scale, state_mode, w_mode, block_v=block_v,
+                     neumann_degree=neumann_degree)
     check("gdn_validate", lib.gdn_validate(ctypes.byref(p)))
     B, T, Hv, Dv = v.shape
     if out is not None:
@@ -106,7 +109,7 @@ def gdn_chunk_fwd_qdq(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, sta
 
 def gdn_chunk_bwd_ste(q, k, v, beta, g, ctx, do, dht=None, cu_seqlens=None, scale=1.0,
                       state_mode="e4m3", w_mode="e4m3", need_dh0=True, workspace=None, out=None,
-                      block_v=64):
+                      block_v=64, neumann_degree=None):
     """Identity-STE backward.  Returns (dq, dk, dv, dbeta, dg, dh0 or None).
 
     ``out`` may pass preallocated (dq, dk, dv, dbeta, dg, dh0) buffers."""
@@ -117,7 +120,8 @@ def gdn_chunk_bwd_ste(q, k, v, beta, g, ctx, do, dht=None, cu_seqlens=None, scal
         _check_dev(name, t, dev)
     if do.dtype != torch.bfloat16:
         raise GdnError("gdn_chunk_bwd_ste", -2)
-    p = make_problem(q, k, v, cu_seqlens, scale, state_mode, w_mode, block_v=block_v)
+    p = make_problem(q, k, v, cu_seqlens, scale, state_mode, w_mode, block_v=block_v,
+                     neumann_degree=neumann_degree)
     check("gdn_validate", lib.gdn_validate(ctypes.byref(p)))
     f32 = dict(device=dev, dtype=torch.float32)
     if out is not None:

@@ -78,6 +78,9 @@ static gdn_status validate(const gdn_problem* p) {
   if (p->chunk != kChunkLen) return GDN_ERR_UNSUPPORTED_SHAPE;
   if (p->block_v != 16 && p->block_v != 32 && p->block_v != 64 && p->block_v != 128)
     return GDN_ERR_UNSUPPORTED_MODE;
+  if (p->solve != GDN_SOLVE_EXACT && p->solve != GDN_SOLVE_NEUMANN) return GDN_ERR_INVALID_ARG;
+  if (p->solve == GDN_SOLVE_NEUMANN && (p->solve_degree < 0 || p->solve_degree > 63))
+    return GDN_ERR_UNSUPPORTED_MODE;  // degree 63 is already the exact inverse
   if ((p->Dk != 64 && p->Dk != 128) || (p->Dv != 64 && p->Dv != 128))
     return GDN_ERR_UNSUPPORTED_SHAPE;
   if (p->block_v > p->Dv) return GDN_ERR_UNSUPPORTED_MODE;

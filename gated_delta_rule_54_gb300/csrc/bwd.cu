@@ -64,6 +64,7 @@ struct BwdParams {
   int Hk, Hv, Dv, G, N;
   int block_v;  // state-scale tile width
   int bv_log2;  // log2(block_v)
+  int neumann;  // -1: exact solve; d >= 0: T is the Neumann polynomial of degree d
   int64_t nt_fixed;
   float scale;
 };
@@ -783,10 +784,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
     wgemm<NTW, true, true, 64, DK>(dK, Gmb, wrow0, Qs, wcol0, 0, 64, lane);
   }
   __syncthreads();  // dT complete; P no longer read (its tile becomes X)
-  {
+  // acc <- the gradient of the loss w.r.t. -A: T^T dT T^T for the exact inverse,
+  // or, for the Neumann polynomial T = sum_{i<=d} Xn^i (Xn = -A), Z_{d-1} of
+  //   S_0 = I, Z_0 = dT;  S_m = I + Xn S_{m-1},  Z_m = dT S_m^T + Xn^T Z_{m-1}
+  // (= sum_{a+b<=d-1} (Xn^T)^a dT (Xn^T)^b, the derivative of the polynomial).
+  float acc[2][4];
+  zero_acc(acc);
+  if (p.neumann < 0) {
     // X = T^T dT
-    float acc[2][4];
-    zero_acc(acc);
     wgemm<2, true, true, 64, 64>(acc, Tb, row0, dTb, col0, 0, 64, lane);
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
@@ -795,13 +800,70 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
         st_bf16x2(Xb + swz<64>(i, j), acc[nt][2 * e2], acc[nt][2 * e2 + 1]);
       }
-  }
-  __syncthreads();
-  {
-    // dA = -X T^T (strictly lower): dKK = dA beta_i Gamma_ij; dbeta += dA GKK; AA = dA A
-    float acc[2][4];
+    __syncthreads();
     zero_acc(acc);
     wgemm<2, false, false, 64, 64>(acc, Xb, row0, Tb, col0, 0, 64, lane);
+  } else if (p.neumann >= 1) {
+    // bf16 tiles in space the value blocks no longer need: Xn (P's tile), S and
+    // Z in turn (Delta / dDelta, and the two V tiles); Z_0 is dT itself
+    __nv_bfloat16* Xn = Xb;
+    __nv_bfloat16* Sbuf[2] = {Db, dDb};
+    __nv_bfloat16* Zbuf[2] = {Vb(0), Vb(1)};
+    for (int e = threadIdx.x; e < 64 * 32; e += kThreads) {
+      const int i = e >> 5, j = (e & 31) * 2;
+      const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(GKKb + swz<64>(i, j));
+      st_bf16x2(Xn + swz<64>(i, j), -bet[i] * __bfloat162float(g2.x), -bet[i] * __bfloat162float(g2.y));
+      st_bf16x2(Sbuf[0] + swz<64>(i, j), i == j ? 1.f : 0.f, i == j + 1 ? 1.f : 0.f);
+    }
+    __syncthreads();
+    const __nv_bfloat16* Z = dTb;
+    const __nv_bfloat16* Sp = Sbuf[0];
+    for (int m = 1; m < p.neumann; ++m) {
+      __nv_bfloat16* Sn = Sbuf[m & 1];
+      __nv_bfloat16* Zn = Zbuf[m & 1];
+      {
+        float sa[2][4];
+        zero_acc(sa);
+        wgemm<2, false, true, 64, 64>(sa, Xn, row0, Sp, col0, 0, 64, lane);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
+            st_bf16x2(Sn + swz<64>(i, j), sa[nt][2 * e2] + (i == j ? 1.f : 0.f),
+                      sa[nt][2 * e2 + 1] + (i == j + 1 ? 1.f : 0.f));
+          }
+      }
+      __syncthreads();
+      {
+        float za[2][4];
+        zero_acc(za);
+        wgemm<2, false, false, 64, 64>(za, dTb, row0, Sn, col0, 0, 64, lane);  // dT S^T
+        wgemm<2, true, true, 64, 64>(za, Xn, row0, Z, col0, 0, 64, lane);      // Xn^T Z
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
+            st_bf16x2(Zn + swz<64>(i, j), za[nt][2 * e2], za[nt][2 * e2 + 1]);
+          }
+      }
+      __syncthreads();
+      Z = Zn;
+      Sp = Sn;
+    }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
+        const __nv_bfloat162 z2 = *reinterpret_cast<const __nv_bfloat162*>(Z + swz<64>(i, j));
+        acc[nt][2 * e2] = __bfloat162float(z2.x);
+        acc[nt][2 * e2 + 1] = __bfloat162float(z2.y);
+      }
+  }
+  {
+    // dA = -acc (strictly lower): dKK = dA beta_i Gamma_ij; dbeta += dA GKK; AA = dA A
     float ba[2][4], aa[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
@@ -1041,6 +1103,7 @@ gdn_status launch_bwd(const gdn_problem& p, const Dims& d, const void* q, const 
   prm.scale = p.scale;
   prm.block_v = p.block_v;
   prm.bv_log2 = p.block_v == 16 ? 4 : (p.block_v == 32 ? 5 : (p.block_v == 64 ? 6 : 7));
+  prm.neumann = p.solve == GDN_SOLVE_NEUMANN ? p.solve_degree : -1;
   if (d.Dk == 128) return dispatch_bwd<128>(p, prm, d, st);
   return dispatch_bwd<64>(p, prm, d, st);
 }

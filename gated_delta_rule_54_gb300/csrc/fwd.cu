@@ -75,6 +75,7 @@ struct FwdParams {
   int Hk, Hv, Dv, G, N;
   int block_v;  // state-scale tile width: 16, 32, 64, or 128 (two value blocks)
   int bv_log2;  // log2(block_v)
+  int neumann;  // -1: exact solve; d >= 0: Neumann polynomial of degree d
   int64_t nt_fixed;
   float scale;
 };
@@ -156,6 +157,50 @@ __device__ __forceinline__ void chunk_cumsum(const float* g, int lane, float& ga
   gL = __shfl_sync(0xffffffffu, s, 31);
 }
 
+// T = sum_{i<=degree} X^i with X = -A ("[7/7] Experimental GDN/KDA
+// approximate-inverse QAT", "What does this PR do?": the Neumann polynomial of
+// an explicit degree, in fp32), by Horner's rule T <- I + X T from T = I.  A is
+// the strictly lower fp32 [64][kSA] tile (zero elsewhere); T ping-pongs between
+// Tmp and Ts and ends in Ts.  256 threads, each a 4 x 4 block of the product.
+__device__ __forceinline__ void neumann_lower64(const float* As, float* Ts, float* Tmp, int degree) {
+  const int tid = threadIdx.x;
+  const int r0 = (tid >> 4) * 4, c0 = (tid & 15) * 4;
+  float* cur = (degree % 2 == 0) ? Ts : Tmp;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    *reinterpret_cast<float4*>(cur + (r0 + i) * kSA + c0) =
+        make_float4(r0 + i == c0 ? 1.f : 0.f, r0 + i == c0 + 1 ? 1.f : 0.f,
+                    r0 + i == c0 + 2 ? 1.f : 0.f, r0 + i == c0 + 3 ? 1.f : 0.f);
+  __syncthreads();
+  for (int step = 0; step < degree; ++step) {
+    float* nxt = (cur == Ts) ? Tmp : Ts;
+    float4 acc[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+    for (int k = 0; k < 64; ++k) {
+      const float4 b = *reinterpret_cast<const float4*>(cur + k * kSA + c0);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float a = -As[(r0 + i) * kSA + k];
+        acc[i].x = fmaf(a, b.x, acc[i].x);
+        acc[i].y = fmaf(a, b.y, acc[i].y);
+        acc[i].z = fmaf(a, b.z, acc[i].z);
+        acc[i].w = fmaf(a, b.w, acc[i].w);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int r = r0 + i;
+      *reinterpret_cast<float4*>(nxt + r * kSA + c0) =
+          make_float4(acc[i].x + (r == c0 ? 1.f : 0.f), acc[i].y + (r == c0 + 1 ? 1.f : 0.f),
+                      acc[i].z + (r == c0 + 2 ? 1.f : 0.f), acc[i].w + (r == c0 + 3 ? 1.f : 0.f));
+    }
+    __syncthreads();
+    cur = nxt;
+  }
+}
+
 // ===========================================================================
 // 1. Chunk-local prep: A, T, W (+ QDQ), U.
 // ===========================================================================
@@ -176,6 +221,7 @@ struct PrepSmem {
   static constexpr int BYTES = VEC + 4 * 64 * 4 + 1024;  // + alignment slack
   static_assert((V % 1024) == 0 && (A % 1024) == 0 && (TW % 128) == 0 && (WST % 128) == 0,
                 "alignment");
+  static_assert(WST - TW >= kF32Tile, "Tw, Tu hold a second fp32 tile for the Neumann products");
 };
 
 template <int DK, int WM>
@@ -293,16 +339,17 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __g
           k1 = (j + 1 < i) ? expf(gi - gam[j + 1]) * acc[nt][2 * e2 + 1] : 0.f;
         }
         st_bf16x2(gimg + swz<64>(i, j), k0, k1);
-        if (a_tile) {
-          const float bi = bet[i];
-          *reinterpret_cast<float2*>(As + i * kSA + j) = make_float2(bi * k0, bi * k1);
-        }
+        // (tiles above the diagonal hold zeros: the Neumann products read all of A)
+        *reinterpret_cast<float2*>(As + i * kSA + j) = make_float2(bet[i] * k0, bet[i] * k1);
       }
   }
   __syncthreads();
 
-  // ---- a3: T = (I + A)^-1 ----
-  solve_unit_lower64<kPrepThreads>(As, Ts);
+  // ---- a3: T = (I + A)^-1, or its Neumann polynomial ----
+  if (p.neumann < 0)
+    solve_unit_lower64<kPrepThreads>(As, Ts);
+  else
+    neumann_lower64(As, Ts, reinterpret_cast<float*>(sm + S::TW), p.neumann);
 
   // ---- a4 operands: Tw = T diag(beta e^gamma), Tu = T diag(beta), split hi/lo;
   //      T itself as the backward's tile image ----
@@ -1260,6 +1307,7 @@ gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const 
   prm.scale = p.scale;
   prm.block_v = p.block_v;
   prm.bv_log2 = p.block_v == 16 ? 4 : (p.block_v == 32 ? 5 : (p.block_v == 64 ? 6 : 7));
+  prm.neumann = p.solve == GDN_SOLVE_NEUMANN ? p.solve_degree : -1;
   if (p.block_v == 128 && d.Dv != 128) return GDN_ERR_UNSUPPORTED_MODE;
   const uint64_t tok = (uint64_t)(d.B * d.T);
   if (tok > 0) {

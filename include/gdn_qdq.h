@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define GDN_QDQ_ABI_VERSION 2
+#define GDN_QDQ_ABI_VERSION 3
 
 typedef enum {
   GDN_QDQ_NONE = 0, /* site not quantized                                   */
@@ -84,10 +84,18 @@ typedef struct {
   float scale;                /* output scale (1.0 for o_t = S_t q_t)           */
   int32_t state_mode;         /* gdn_qdq_mode at the state site                 */
   int32_t w_mode;             /* gdn_qdq_mode at the W site                     */
-  int32_t block_v;            /* state-scale tile width; must be 64            */
+  int32_t block_v;            /* state-scale tile width: 16, 32, 64 or 128 (<= Dv) */
   int32_t chunk;              /* chunk length; must be 64                      */
   int32_t dtype;              /* gdn_dtype of q, k, v (and dO); must be BF16    */
+  int32_t solve;              /* GDN_SOLVE_EXACT (0): T = (I + A)^-1;
+                                 GDN_SOLVE_NEUMANN (1): T = sum_{i<=solve_degree} (-A)^i
+                                 ("[7/7] Experimental GDN/KDA approximate-inverse
+                                 QAT", "What does this PR do?"), the backward
+                                 through that polynomial                       */
+  int32_t solve_degree;       /* Neumann degree, 0..63 (63 is already exact)    */
 } gdn_problem;
+
+typedef enum { GDN_SOLVE_EXACT = 0, GDN_SOLVE_NEUMANN = 1 } gdn_solve;
 
 /*
  * Device-side error flag.  Kernels that wait for their own asynchronous

@@ -114,11 +114,11 @@ def slot_map(lengths, packed, T):
     return np.array(out, dtype=np.int64)
 
 
-def run_oracle(d, state_mode, w_mode, scale=1.0, record=False, block_v=64):
+def run_oracle(d, state_mode, w_mode, scale=1.0, record=False, block_v=64, neumann_degree=None):
     """O2 (chunked, fp64) on CPU inputs dict from synth.make_inputs."""
     return chunked(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"],
                    cu_seqlens=d.get("cu_seqlens"), scale=scale, state_mode=state_mode,
-                   w_mode=w_mode, record=record, block_v=block_v)
+                   w_mode=w_mode, record=record, block_v=block_v, neumann_degree=neumann_degree)
 
 
 def to_dev(d, device="cuda"):

@@ -34,6 +34,7 @@ def _problem(**kw):
     p.cu_seqlens = None
     p.scale = 1.0
     p.state_mode, p.w_mode, p.block_v, p.chunk, p.dtype = 1, 1, 64, 64, 0
+    p.solve, p.solve_degree = 0, 0
     for k, v in kw.items():
         setattr(p, k, v)
     return p
@@ -52,6 +53,8 @@ def test_validate_accepts_supported_problems():
     assert _validate(_problem(T=0)) == 0
     for bv in (16, 32, 128):
         assert _validate(_problem(block_v=bv)) == 0
+    for deg in (0, 3, 63):
+        assert _validate(_problem(solve=1, solve_degree=deg)) == 0
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -62,6 +65,7 @@ def test_validate_accepts_supported_problems():
     (dict(Hv=3), -3),                    # Hv % Hk
     (dict(chunk=32), -3),
     (dict(block_v=48), -4), (dict(block_v=128, Dv=64), -4),
+    (dict(solve=2), -1), (dict(solve=1, solve_degree=64), -4), (dict(solve=1, solve_degree=-1), -4),
     (dict(state_mode=3), -1), (dict(w_mode=-1), -1),
     (dict(B=-1), -1), (dict(Hk=0), -1),
     (dict(N=3), -1),                     # N != B without cu_seqlens
@@ -141,7 +145,7 @@ def test_status_strings():
     for code in range(-7, 1):
         s = lib.gdn_status_string(code).decode()
         assert s.startswith("GDN_")
-    assert lib.gdn_abi_version() == 2
+    assert lib.gdn_abi_version() == 3
 
 
 def _dproblem(**kw):

@@ -18,24 +18,26 @@ pytestmark = pytest.mark.gpu
 NAMES = ("dq", "dk", "dv", "dbeta", "dg", "dh0")
 
 
-def _grads_gpu(d, sm, wm, do, dht, scale=1.0, block_v=64):
+def _grads_gpu(d, sm, wm, do, dht, scale=1.0, block_v=64, neumann_degree=None):
     dd = to_dev(d)
     cu = dd["cu_seqlens"]
     o, ht, ctx = gdn_chunk_fwd_qdq(dd["q"], dd["k"], dd["v"], dd["beta"], dd["g"], dd["h0"],
                                    cu_seqlens=cu, scale=scale, state_mode=sm, w_mode=wm,
-                                   save_ctx=True, block_v=block_v)
+                                   save_ctx=True, block_v=block_v, neumann_degree=neumann_degree)
     gr = gdn_chunk_bwd_ste(dd["q"], dd["k"], dd["v"], dd["beta"], dd["g"], ctx, do.cuda(),
                            dht.cuda() if dht is not None else None, cu_seqlens=cu, scale=scale,
-                           state_mode=sm, w_mode=wm, block_v=block_v)
+                           state_mode=sm, w_mode=wm, block_v=block_v,
+                           neumann_degree=neumann_degree)
     torch.cuda.synchronize()
     return [x.cpu().double().numpy() for x in gr]
 
 
-def _grads_oracle(d, sm, wm, do, dht, scale=1.0, cu=None, block_v=64):
+def _grads_oracle(d, sm, wm, do, dht, scale=1.0, cu=None, block_v=64, neumann_degree=None):
     N, Hv = d["N"], d["v"].shape[2]
     h0 = d["h0"] if d["h0"] is not None else torch.zeros(N, Hv, d["k"].shape[3], d["v"].shape[3])
     xs = [t.double().requires_grad_(True) for t in (d["q"], d["k"], d["v"], d["beta"], d["g"], h0)]
-    o, ht = chunked(*xs, cu_seqlens=cu, scale=scale, state_mode=sm, w_mode=wm, block_v=block_v)
+    o, ht = chunked(*xs, cu_seqlens=cu, scale=scale, state_mode=sm, w_mode=wm, block_v=block_v,
+                    neumann_degree=neumann_degree)
     loss = (o * do.double()).sum() + ((ht * dht.double()).sum() if dht is not None else 0.0)
     return [g.numpy() for g in torch.autograd.grad(loss, xs)]
 
@@ -48,11 +50,13 @@ def _dO(w, d, seed=11, with_dht=True):
     return do, dht
 
 
-def _check(w, lengths=None, scale=1.0, with_dht=True, block_v=64):
+def _check(w, lengths=None, scale=1.0, with_dht=True, block_v=64, neumann_degree=None):
     d = synth.make_inputs(w, lengths=lengths)
     do, dht = _dO(w, d, with_dht=with_dht)
-    g = _grads_gpu(d, w.state_mode, w.w_mode, do, dht, scale, block_v=block_v)
-    r = _grads_oracle(d, w.state_mode, w.w_mode, do, dht, scale, d["cu_seqlens"], block_v=block_v)
+    g = _grads_gpu(d, w.state_mode, w.w_mode, do, dht, scale, block_v=block_v,
+                   neumann_degree=neumann_degree)
+    r = _grads_oracle(d, w.state_mode, w.w_mode, do, dht, scale, d["cu_seqlens"], block_v=block_v,
+                      neumann_degree=neumann_degree)
     errs = {}
     for name, a, b in zip(NAMES, g, r):
         assert np.isfinite(a).all(), name
@@ -78,6 +82,13 @@ def test_bwd_state_scale_widths(block_v):
     w = synth.small(B=2, T=150, Hk=1, Hv=2, Dk=128, Dv=128, state_mode="int8", h0=True,
                     seed=40 + block_v)
     _check(w, block_v=block_v)
+
+
+@pytest.mark.parametrize("degree", [1, 3, 7])
+def test_bwd_neumann_solve(degree):
+    """The backward differentiates the actual Neumann polynomial."""
+    w = synth.small(B=2, T=150, Hk=1, Hv=2, Dk=128, Dv=128, h0=True, seed=50 + degree)
+    _check(w, neumann_degree=degree)
 
 
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 130])

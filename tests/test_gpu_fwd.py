@@ -18,20 +18,22 @@ from _parity import (assert_close, assert_close_units, assert_codes, code_steps,
 pytestmark = pytest.mark.gpu
 
 
-def _gpu_fwd(d, sm, wm, scale=1.0, save_ctx=True, block_v=64):
+def _gpu_fwd(d, sm, wm, scale=1.0, save_ctx=True, block_v=64, neumann_degree=None):
     dd = to_dev(d)
     o, ht, ctx = gdn_chunk_fwd_qdq(dd["q"], dd["k"], dd["v"], dd["beta"], dd["g"], dd["h0"],
                                    cu_seqlens=dd["cu_seqlens"], scale=scale, state_mode=sm,
-                                   w_mode=wm, save_ctx=save_ctx, block_v=block_v)
+                                   w_mode=wm, save_ctx=save_ctx, block_v=block_v,
+                                   neumann_degree=neumann_degree)
     torch.cuda.synchronize()
     return dd, o, ht, ctx
 
 
-def _check_case(w, lengths=None, scale=1.0, block_v=64):
+def _check_case(w, lengths=None, scale=1.0, block_v=64, neumann_degree=None):
     d = synth.make_inputs(w, lengths=lengths)
     sm, wm = w.state_mode, w.w_mode
-    dd, o, ht, ctx = _gpu_fwd(d, sm, wm, scale, block_v=block_v)
-    o_ref, ht_ref, rec = run_oracle(d, sm, wm, scale=scale, record=True, block_v=block_v)
+    dd, o, ht, ctx = _gpu_fwd(d, sm, wm, scale, block_v=block_v, neumann_degree=neumann_degree)
+    o_ref, ht_ref, rec = run_oracle(d, sm, wm, scale=scale, record=True, block_v=block_v,
+                                    neumann_degree=neumann_degree)
     p = make_problem(dd["q"], dd["k"], dd["v"], dd["cu_seqlens"], scale, sm, wm, block_v=block_v)
     seg = split_ctx(ctx, p)
     packed = lengths is not None
@@ -122,6 +124,23 @@ def test_fwd_state_scale_widths(sm, wm, block_v):
     w = synth.small(B=1, T=0, Hk=1, Hv=2, Dk=64, Dv=128, state_mode=sm, w_mode=wm, h0=True,
                     seed=block_v + 1)
     _check_case(w, lengths=[70, 1, 129], block_v=block_v)
+
+
+@pytest.mark.parametrize("degree", [0, 3, 7])
+def test_fwd_neumann_solve(degree):
+    """Neumann approximate inverse of an explicit degree ("[7/7] Experimental
+    GDN/KDA approximate-inverse QAT")."""
+    w = synth.small(B=2, T=150, Hk=2, Hv=2, Dk=128, Dv=128, h0=True, seed=60 + degree)
+    _check_case(w, neumann_degree=degree)
+
+
+def test_fwd_neumann_degree_63_is_the_exact_solve():
+    w = synth.small(B=1, T=130, Hk=1, Hv=2, Dk=128, Dv=128, h0=True, seed=70)
+    d = synth.make_inputs(w)
+    _, o1, h1, _ = _gpu_fwd(d, "none", "none")
+    _, o2, h2, _ = _gpu_fwd(d, "none", "none", neumann_degree=63)
+    assert_close(o2.cpu().numpy(), o1.cpu().numpy(), "degree 63 o")
+    assert_close(h2.cpu().numpy(), h1.cpu().numpy(), "degree 63 ht")
 
 
 @pytest.mark.parametrize("T", [1, 3, 63, 64, 65, 127, 128, 257])
