@@ -80,12 +80,13 @@ struct FwdParams {
   float scale;
 };
 
-// state-scale tile of local column c of a 64-column value block
-__device__ __forceinline__ int tile_of(int c, const FwdParams& p) {
-  return p.block_v >= 64 ? 0 : c >> p.bv_log2;
-}
-__device__ __forceinline__ float pick4(const float (&x)[4], int i) {
-  return i == 0 ? x[0] : (i == 1 ? x[1] : (i == 2 ? x[2] : x[3]));
+// x[i] of a short register array without a local-memory copy (i < N)
+template <int N>
+__device__ __forceinline__ float pick(const float (&x)[N], int i) {
+  float r = x[0];
+#pragma unroll
+  for (int j = 1; j < N; ++j) r = (i == j) ? x[j] : r;
+  return r;
 }
 
 // The chunk stored at a chunk slot (see gdn_qdq.h); false for an unused
@@ -540,21 +541,25 @@ __device__ __forceinline__ void issue_state_chunk(const FwdParams& p, __nv_bfloa
   cp_async_commit();
 }
 
-template <int DK, int SM, int WM>
+// BV is the state-scale tile width: 16 or 32 (two or four tiles in the 64-column
+// block), 64 (the block), or 128 (two blocks: the pair of CTAs is a cluster
+// that swaps its block amax every chunk).  The tile bookkeeping is resolved at
+// compile time, so the common one-tile case carries none of it.
+template <int DK, int SM, int WM, int BV>
 __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const __grid_constant__ FwdParams p) {
   using S = StateSmem<DK, SM, WM>;
   // E4M3 W and state at Dk = 128: Delta = W^ H^ runs on E4M3 codes directly
   // (W codes as TMA wrote them, H^ codes written [v][dk] as the B operand)
   constexpr bool F8 = SM == GDN_QDQ_E4M3 && WM == GDN_QDQ_E4M3 && DK == 128;
+  constexpr int NTL = BV < 64 ? 64 / BV : 1;  // state-scale tiles in this block
+  constexpr bool PAIR = BV == 128;
   extern __shared__ __align__(1024) unsigned char sm_raw[];
   unsigned char* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
-  __shared__ float red[kStateWarps][4];  // per-warp partial amax of each state-scale tile
-  __shared__ float xchg[2][2];           // block_v 128: (fail, amax) from the peer value block
+  __shared__ float red[kStateWarps][NTL];  // per-warp partial amax of each state-scale tile
+  __shared__ float xchg[2][2];             // PAIR: (fail, amax) from the peer value block
   __shared__ __align__(8) uint64_t bars[2];
 
   const int vb = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
-  const int bvl = p.block_v < 64 ? p.block_v : 64;  // tile width inside this block
-  const int ntiles = 64 / bvl;
   const int hk = h / p.G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
@@ -594,33 +599,31 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
   const int h_row0 = (warp % HM) * 16;
   const int h_col0 = (warp / HM) * (64 / HN);
   float hreg[NTH][4];
+  // Every warp's column range starts on a multiple of 16 and every tile is at
+  // least 16 wide, so a thread's state columns fall in two tiles at most:
+  // ta (n-tiles 0, 1) and tb (n-tiles 2, 3); its Delta columns in tile td.
+  const int ta = NTL == 1 ? 0 : h_col0 / BV;
+  const int tb = NTL == 1 ? 0 : (h_col0 + 16) / BV;
+  const int td = NTL == 1 ? 0 : col0 / BV;
   // per-warp partial amax of every state-scale tile of the block -> red
   auto tile_partials = [&]() {
-    if (ntiles == 1) {
-      float m = 0.f;
+    float ma = 0.f, mb = 0.f;
 #pragma unroll
-      for (int nt = 0; nt < NTH; ++nt)
+    for (int nt = 0; nt < NTH; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(hreg[nt][e]));
-      m = warp_max(m);
+      for (int e = 0; e < 4; ++e) {
+        if (nt < 2) ma = fmaxf(ma, fabsf(hreg[nt][e]));
+        else mb = fmaxf(mb, fabsf(hreg[nt][e]));
+      }
+    if constexpr (NTL == 1) {
+      const float m = warp_max(fmaxf(ma, mb));
       if (lane == 0) red[warp][0] = m;
-      return;
-    }
-    float mt[4] = {0.f, 0.f, 0.f, 0.f};
+    } else {
+      ma = warp_max(ma);
+      if constexpr (NTH > 2) mb = warp_max(mb);
+      if (lane == 0) {
 #pragma unroll
-    for (int nt = 0; nt < NTH; ++nt) {
-      float m = 0.f;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) m = fmaxf(m, fabsf(hreg[nt][e]));
-      const int t = tile_of(h_col0 + nt * 8, p);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) mt[i] = (i == t) ? fmaxf(mt[i], m) : mt[i];
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (i < ntiles) {
-        const float m = warp_max(mt[i]);
-        if (lane == 0) red[warp][i] = m;
+        for (int i = 0; i < NTL; ++i) red[warp][i] = fmaxf(i == ta ? ma : 0.f, i == tb ? mb : 0.f);
       }
     }
   };
@@ -662,18 +665,16 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
     if (threadIdx.x == 0) tma_store_wait_read();  // the codes store of chunk c - 1 has read Hst
     // chunk c landed; amax partials of H visible; buffer buf ^ 1 free
     bool fail = __syncthreads_or(!ok);
-    // tile amax of the state entering chunk c
-    float amx[4] = {0.f, 0.f, 0.f, 0.f};
+    // amax of each state-scale tile of the state entering chunk c
+    float amx[NTL];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (i < ntiles) {
-        float a = red[0][i];
+    for (int i = 0; i < NTL; ++i) {
+      float a = red[0][i];
 #pragma unroll
-        for (int w = 1; w < kStateWarps; ++w) a = fmaxf(a, red[w][i]);
-        amx[i] = a;
-      }
+      for (int w = 1; w < kStateWarps; ++w) a = fmaxf(a, red[w][i]);
+      amx[i] = a;
     }
-    if (p.block_v == 128) {
+    if constexpr (PAIR) {
       // one scale across both value blocks: the pair of CTAs (a cluster) swaps
       // its block amax, and its failure flag so that both leave together
       namespace cg = cooperative_groups;
@@ -729,24 +730,26 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
       }
     }
 
-    // ---- a6: state QDQ per [DK x block_v] tile ----
-    float sHt[4] = {1.f, 1.f, 1.f, 1.f}, rct[4] = {0.f, 0.f, 0.f, 0.f};
-    if constexpr (SM != GDN_QDQ_NONE) {
+    // ---- a6: state QDQ per [DK x BV] tile ----
+    // scale and reciprocal of each tile (the scale of an all-zero tile is 0)
+    float sHt[NTL], rct[NTL];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (i < ntiles) {
-          qdq_scale<SM>(amx[i], sHt[i], rct[i]);
-          if (amx[i] == 0.f) sHt[i] = 0.f;
-        }
+    for (int i = 0; i < NTL; ++i) {
+      sHt[i] = 1.f;
+      rct[i] = 0.f;
+      if constexpr (SM != GDN_QDQ_NONE) {
+        qdq_scale<SM>(amx[i], sHt[i], rct[i]);
+        if (amx[i] == 0.f) sHt[i] = 0.f;
       }
     }
+    const float sHa = pick(sHt, ta), rca = pick(rct, ta), ama = pick(amx, ta);
+    const float sHb = pick(sHt, tb), rcb = pick(rct, tb), amb = pick(amx, tb);
     {
       if constexpr (F8) {
 #pragma unroll
         for (int nt = 0; nt < NTH; ++nt) {
-          const int t = tile_of(h_col0 + nt * 8, p);
-          const float sH = pick4(sHt, t), rcp = pick4(rct, t);
-          const bool zero = pick4(amx, t) == 0.f;
+          const float sH = nt < 2 ? sHa : sHb, rcp = nt < 2 ? rca : rcb;
+          const bool zero = (nt < 2 ? ama : amb) == 0.f;
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             const int d = h_row0 + gq + 8 * e2, col = h_col0 + nt * 8 + 2 * tq;
@@ -768,9 +771,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
       } else if constexpr (SM != GDN_QDQ_NONE) {
 #pragma unroll
         for (int nt = 0; nt < NTH; ++nt) {
-          const int t = tile_of(h_col0 + nt * 8, p);
-          const float sH = pick4(sHt, t), rcp = pick4(rct, t);
-          const float amax = pick4(amx, t);
+          const float sH = nt < 2 ? sHa : sHb, rcp = nt < 2 ? rca : rcb;
+          const float amax = nt < 2 ? ama : amb;
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             const int d = h_row0 + gq + 8 * e2, col = h_col0 + nt * 8 + 2 * tq;
@@ -815,13 +817,12 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
       if constexpr (SM != GDN_QDQ_NONE) {
         tma_store_2d(&p.tm_hc, vb * 64, (int)((slot * p.Hv + h) * DK), Hst);
         tma_store_commit();
-        // scales [slot, Hv, Dv / block_v]
-        if (p.block_v == 128) {
+        // scales [slot, Hv, Dv / BV]
+        if constexpr (PAIR) {
           if (vb == 0) p.h_scales[slot * p.Hv + h] = sHt[0];
         } else {
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            if (i < ntiles) p.h_scales[(slot * p.Hv + h) * (p.Dv / bvl) + vb * ntiles + i] = sHt[i];
+          for (int i = 0; i < NTL; ++i) p.h_scales[(slot * p.Hv + h) * (p.Dv / (64 / NTL)) + vb * NTL + i] = sHt[i];
         }
       }
     }
@@ -854,10 +855,9 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
         if constexpr (SM == GDN_QDQ_NONE) wgemm<2, false, true, DK, 64>(dacc, WcH, row0, HcL, col0, 0, DK, lane);
       }
       const float* Us = Ubuf(buf);
+      const float sWH = (WM != GDN_QDQ_NONE ? sW : 1.f) * (SM != GDN_QDQ_NONE ? pick(sHt, td) : 1.f);
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        const float sWH = (WM != GDN_QDQ_NONE ? sW : 1.f) *
-                          (SM != GDN_QDQ_NONE ? pick4(sHt, tile_of(col0 + nt * 8, p)) : 1.f);
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -1004,16 +1004,15 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
       *reinterpret_cast<uint2*>(WcL + e) = make_uint2(pack_bf16(l0v, l1v), pack_bf16(l2v, l3v));
     }
   }
-  float sHt[4] = {1.f, 1.f, 1.f, 1.f};  // scale of each state-scale tile of this block
+  // state scales of this warp's two 16-column groups (each inside one
+  // state-scale tile: tiles are 16-aligned and at least 16 wide); scales are
+  // [slot, Hv, Dv / block_v]
+  float sHa = 1.f, sHb = 1.f;
   if constexpr (SM != GDN_QDQ_NONE) {
-    if (p.block_v == 128) {
-      sHt[0] = p.h_scales[slot * p.Hv + h];
-    } else {
-      const int nt_b = 64 / p.block_v;
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (i < nt_b) sHt[i] = p.h_scales[(slot * p.Hv + h) * (p.Dv / p.block_v) + vb * nt_b + i];
-    }
+    const int64_t sb = (slot * p.Hv + h) * (p.Dv >> p.bv_log2);
+    const int c = vb * 64 + (warp >> 2) * 32;
+    sHa = p.h_scales[sb + (c >> p.bv_log2)];
+    sHb = p.h_scales[sb + ((c + 16) >> p.bv_log2)];
   } else {
     const float* src = p.h_full + ((slot * p.Hv + h) * DK) * p.Dv + vb * 64;
     for (int i = threadIdx.x; i < DK * 16; i += kOutThreads) {
@@ -1082,8 +1081,7 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
   __nv_bfloat16* pimg = vb == 0 ? p.pb + (slot * p.Hv + h) * (kTileImgBytes / 2) : nullptr;
 #pragma unroll
   for (int nt = 0; nt < 4; ++nt) {
-    const float sWH = (WM != GDN_QDQ_NONE ? sW : 1.f) *
-                      (SM != GDN_QDQ_NONE ? pick4(sHt, tile_of(col0 + nt * 8, p)) : 1.f);
+    const float sWH = (WM != GDN_QDQ_NONE ? sW : 1.f) * (nt < 2 ? sHa : sHb);
 #pragma unroll
     for (int e2 = 0; e2 < 2; ++e2) {
       const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -1122,7 +1120,7 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-        const float sq = (SM != GDN_QDQ_NONE) ? pick4(sHt, tile_of(col0 + nt * 8, p)) : 1.f;
+        const float sq = nt < 2 ? sHa : sHb;
         const float ei = eg[i] * sq;
         *reinterpret_cast<float2*>(Ost + swz_f32(i, j)) =
             make_float2(p.scale * (ei * qacc[nt][2 * e2] + o2[nt][2 * e2]),
@@ -1161,6 +1159,33 @@ gdn_status set_smem(Kern kern, int bytes) {
              : GDN_ERR_CUDA;
 }
 
+template <int DK, int SM, int WM, int BV>
+gdn_status launch_state(const FwdParams& prm, dim3 grid, cudaStream_t st) {
+  // the none-state kernel is built for BV 64 only
+  constexpr int B = SM == GDN_QDQ_NONE ? 64 : BV;
+  auto k2 = gdn_fwd_state_kernel<DK, SM, WM, B>;
+  if (set_smem(k2, StateSmem<DK, SM, WM>::BYTES) != GDN_OK) return GDN_ERR_CUDA;
+  if constexpr (B == 128) {
+    // the two value blocks of a (sequence, head) share a state scale: a 2-CTA cluster
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kStateThreads);
+    cfg.dynamicSmemBytes = StateSmem<DK, SM, WM>::BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k2, prm) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  } else {
+    k2<<<grid, kStateThreads, StateSmem<DK, SM, WM>::BYTES, st>>>(prm);
+    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+  }
+}
+
 template <int DK, int SM, int WM>
 gdn_status launch_t(const FwdParams& prm, const Dims& d, cudaStream_t st) {
   const int nvb = d.Dv / 64;
@@ -1170,30 +1195,14 @@ gdn_status launch_t(const FwdParams& prm, const Dims& d, cudaStream_t st) {
     k1<<<(unsigned)(d.n_slots * d.Hv), kPrepThreads, PrepSmem<DK>::BYTES, st>>>(prm);
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
   }
-  auto k2 = gdn_fwd_state_kernel<DK, SM, WM>;
-  if (set_smem(k2, StateSmem<DK, SM, WM>::BYTES) != GDN_OK) return GDN_ERR_CUDA;
   {
-    // block_v 128: the two value blocks of a (sequence, head) share a state
-    // scale and run as a 2-CTA cluster that swaps the block amax every chunk
     const dim3 grid((unsigned)nvb, (unsigned)d.Hv, (unsigned)d.N);
-    if (prm.block_v == 128) {
-      cudaLaunchConfig_t cfg = {};
-      cfg.gridDim = grid;
-      cfg.blockDim = dim3(kStateThreads);
-      cfg.dynamicSmemBytes = StateSmem<DK, SM, WM>::BYTES;
-      cfg.stream = st;
-      cudaLaunchAttribute attr[1];
-      attr[0].id = cudaLaunchAttributeClusterDimension;
-      attr[0].val.clusterDim.x = 2;
-      attr[0].val.clusterDim.y = 1;
-      attr[0].val.clusterDim.z = 1;
-      cfg.attrs = attr;
-      cfg.numAttrs = 1;
-      if (cudaLaunchKernelEx(&cfg, k2, prm) != cudaSuccess) return GDN_ERR_CUDA;
-    } else {
-      k2<<<grid, kStateThreads, StateSmem<DK, SM, WM>::BYTES, st>>>(prm);
-      if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
-    }
+    const int bv = SM == GDN_QDQ_NONE ? 64 : prm.block_v;  // no state scales without a state QDQ
+    const gdn_status s = bv == 16    ? launch_state<DK, SM, WM, 16>(prm, grid, st)
+                         : bv == 32  ? launch_state<DK, SM, WM, 32>(prm, grid, st)
+                         : bv == 128 ? launch_state<DK, SM, WM, 128>(prm, grid, st)
+                                     : launch_state<DK, SM, WM, 64>(prm, grid, st);
+    if (s != GDN_OK) return s;
   }
   if (d.B * d.T > 0 && d.n_slots > 0) {
     auto k3 = gdn_fwd_output_kernel<DK, SM, WM>;
