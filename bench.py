@@ -577,6 +577,9 @@ def decode_cpu_baseline(w, cpu, budget_s=20.0, rows=None):
 KDA_METRIC = "KDA recurrent fwd tokens/s at B=4,T=4096,H=16,D=128 (state QDQ every 64 tokens); % of roofline"
 
 
+KDA_SOURCES = ["gated_delta_rule_54_gb300/csrc/kda.cu", "gated_delta_rule_54_gb300/csrc/common.cuh"]
+
+
 def kda_alg_bytes(w):
     """Algorithmic HBM bytes of one KDA launch: inputs read once (g per key
     channel), o written once, h0 read and ht written."""
@@ -646,7 +649,8 @@ def run_kda(args, ws, rank, local):
                    "l2": "inputs larger than L2 (no flush needed)"},
         "clocks": clk.summary(), "e2e": None, "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": _traffic("kda_recurrent_kernel_kda_layer.md", KDA_SOURCES, args.workload),
                      "kernel": "kda_recurrent_kernel", "peak_source": peak_kind,
                      "alg_bytes_per_launch": alg, "launch_ms": round(ms_step, 4)},
         "cpu_baseline": cpu_base,

@@ -580,12 +580,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
     {
       const uint8_t* hst = hcb(vb);
       float hd = 0.f;
+      // this thread's four columns (fixed: kThreads is a multiple of 16) lie in one state-scale tile
+      static_assert(kThreads % 16 == 0, "column of a thread");
+      float sH = 1.f;
+      if constexpr (SM != GDN_QDQ_NONE)
+        sH = p.h_scales[(slot * p.Hv + h) * (p.Dv >> p.bv_log2) +
+                        ((vb * 64 + (threadIdx.x & 15) * 4) >> p.bv_log2)];
       for (int e = threadIdx.x; e < DK * 16; e += kThreads) {
         const int d = e >> 4, col = (e & 15) * 4;
         float4 x;
         if constexpr (SM != GDN_QDQ_NONE) {
-          const float sH = p.h_scales[(slot * p.Hv + h) * (p.Dv >> p.bv_log2) +
-                                      ((vb * 64 + col) >> p.bv_log2)];
           x = qdq_code4_values<SM>(*reinterpret_cast<const uint32_t*>(hst + d * 64 + col));
           x.x *= sH; x.y *= sH; x.z *= sH; x.w *= sH;
         } else {
