@@ -10,6 +10,9 @@ Contents
   recurrent.c    O1: fp64 token-by-token recurrence with state QDQ, plain C + OpenMP
   chunked.py     O2: fp64 chunked (WY) form with state and W QDQ, torch CPU + autograd
   recurrent_torch.py  small-case fp64 recurrence in torch (autograd), for gradient pins
+  decode.py      decode QAT step (state QDQ before every token), numpy fp64
+  kda.py         KDA recurrence (decay per key channel) with state QDQ, numpy fp64
+  two_precision.py  two-precision GDN profile: fp32 anchor + E4M3 read copy, numpy fp64
 
 The C part is compiled with gcc into ``oracle/liboracle.so`` by ``build()``.
 """
