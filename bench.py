@@ -6,7 +6,9 @@ workload (B=4, T=4096, H=16, Dk=Dv=128, E4M3 state and W QDQ, h0 ~ N(0, 0.1^2)):
 the forward (saving the QDQ context) followed by the identity-STE backward
 (``--mode fwdbwd``, the default once the backward is present), or the
 forward alone (``--mode fwd``).  ``--mode decode`` times the decode QAT step
-instead (256 sequences, one token each, carried fp32 states of 256 MiB).  Inputs are synthetic (seeded) and resident
+instead (256 sequences, one token each, carried fp32 states of 256 MiB);
+``--mode kda`` the KDA recurrence and ``--mode two_precision`` the
+two-precision profile (fp32 anchor, E4M3 read copy), both B=4, T=4096, H=16.  Inputs are synthetic (seeded) and resident
 in HBM when the timed region starts; per step the inputs (~350 MB) exceed
 the 129 MB L2, so no flush is needed between steps.
 
@@ -572,42 +574,104 @@ def decode_cpu_baseline(w, cpu, budget_s=20.0, rows=None):
 
 
 # ----------------------------------------------------------------------------
-# KDA recurrence (--mode kda)
+# token-serial recurrences: KDA (--mode kda) and the two-precision profile
+# (--mode two_precision)
 # ----------------------------------------------------------------------------
 KDA_METRIC = "KDA recurrent fwd tokens/s at B=4,T=4096,H=16,D=128 (state QDQ every 64 tokens); % of roofline"
-
-
+TP_METRIC = ("two-precision GDN fwd tokens/s at B=4,T=4096,H=16,D=128 (fp32 anchor, E4M3 read copy, "
+             "16-token flush); % of roofline")
 KDA_SOURCES = ["gated_delta_rule_54_gb300/csrc/kda.cu", "gated_delta_rule_54_gb300/csrc/common.cuh"]
+TP_SOURCES = ["gated_delta_rule_54_gb300/csrc/two_precision.cu",
+              "gated_delta_rule_54_gb300/csrc/common.cuh"]
+TP_FLUSH = 16
 
 
-def kda_alg_bytes(w):
-    """Algorithmic HBM bytes of one KDA launch: inputs read once (g per key
-    channel), o written once, h0 read and ht written."""
+def token_serial_alg_bytes(w, g_per_channel):
+    """Algorithmic HBM bytes of one launch: q, k, v, beta, g read once (g per key
+    channel for KDA, per head otherwise), o written once, h0 read and ht written."""
     tok = w.B * w.T
-    b = tok * (w.Hk * w.Dk * 2 * 2 + w.Hv * w.Dv * 2 + w.Hv * 4 + w.Hv * w.Dk * 4 + w.Hv * w.Dv * 4)
+    g = w.Hv * w.Dk * 4 if g_per_channel else w.Hv * 4
+    b = tok * (w.Hk * w.Dk * 2 * 2 + w.Hv * w.Dv * 2 + w.Hv * 4 + g + w.Hv * w.Dv * 4)
     return b + w.B * w.Hv * w.Dk * w.Dv * 4 * 2
 
 
-def run_kda(args, ws, rank, local):
-    from gated_delta_rule_54_gb300 import api, synth
+def kda_alg_bytes(w):
+    return token_serial_alg_bytes(w, True)
+
+
+class _TokenSerial:
+    """What differs between the two token-serial benchmarks."""
+
+    def __init__(self, mode):
+        from gated_delta_rule_54_gb300 import api, synth
+        self.mode = mode
+        self.kda = mode == "kda"
+        self.metric = KDA_METRIC if self.kda else TP_METRIC
+        self.kernel = "kda_recurrent_kernel" if self.kda else "gdn_two_precision_kernel"
+        self.profile = ("kda_recurrent_kernel_kda_layer.md" if self.kda
+                        else "gdn_two_precision_kernel_two_precision_layer.md")
+        self.sources = KDA_SOURCES if self.kda else TP_SOURCES
+        self.make = synth.make_kda_inputs if self.kda else synth.make_inputs
+        self.gname = "g_k" if self.kda else "g"
+        self.api = api
+
+    def call(self, w, x, out=None):
+        if self.kda:
+            return self.api.kda_recurrent_fwd_qdq(x["q"], x["k"], x["v"], x["beta"], x["g_k"],
+                                                  x["h0"], state_mode=w.state_mode)
+        return self.api.gdn_two_precision_fwd(x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"],
+                                              read_mode=w.state_mode, flush=TP_FLUSH, out=out)
+
+    def oracle(self, w, x):
+        if self.kda:
+            from oracle.kda import kda_recurrent
+            return kda_recurrent(x["q"], x["k"], x["v"], x["beta"], x["g_k"], x["h0"],
+                                 state_mode=w.state_mode)
+        from oracle.two_precision import two_precision
+        return two_precision(x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"],
+                             read_mode=w.state_mode, flush=TP_FLUSH)
+
+    def config(self, w):
+        c = {"workload": w.name, "mode": self.mode, "B": w.B, "T": w.T, "Hk": w.Hk, "Hv": w.Hv,
+             "Dk": w.Dk, "Dv": w.Dv}
+        if self.kda:
+            c.update(state_mode=w.state_mode, chunk=64, block_v=64)
+        else:
+            c.update(read_mode=w.state_mode, flush=TP_FLUSH, read_group="per value row, 128 key channels")
+        c["l2"] = "inputs larger than L2 (no flush needed)"
+        return c
+
+    def data(self):
+        g = "g per key channel" if self.kda else "g"
+        return ("synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), beta=sigmoid, "
+                "%s=-softplus(N(0,1)), h0 N(0, 0.1^2))" % g)
+
+    def cpu_sample(self, w, cpu, Ts=256):
+        sl = lambda t: t[:1, :Ts] if t is not None else None
+        x = {n: sl(cpu[n]) for n in ("q", "k", "v", "beta", self.gname)}
+        x["h0"] = cpu["h0"][:1] if cpu["h0"] is not None else None
+        t0 = time.time()
+        self.oracle(w, x)
+        return Ts, time.time() - t0
+
+
+def run_token_serial(args, ws, rank, local):
+    from gated_delta_rule_54_gb300 import synth
     from gated_delta_rule_54_gb300._lib import load
 
+    ts = _TokenSerial(args.mode)
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     load()
     w = synth.WORKLOADS[args.workload]
     w = synth.Workload(**{**w.__dict__, "seed": w.seed + rank})
-    cpu = synth.make_kda_inputs(w)
+    cpu = ts.make(w)
     d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in cpu.items()}
     stream = torch.cuda.current_stream(dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
-    def step():
-        api.kda_recurrent_fwd_qdq(d["q"], d["k"], d["v"], d["beta"], d["g_k"], d["h0"],
-                                  state_mode=w.state_mode)
-
     for _ in range(args.warmup):
-        step()
+        ts.call(w, d)
     torch.cuda.synchronize()
     _barrier(ws)
     torch.cuda.synchronize()
@@ -615,7 +679,7 @@ def run_kda(args, ws, rank, local):
         a, b = ev(), ev()
         a.record(stream)
         for _ in range(args.steps):
-            step()
+            ts.call(w, d)
         b.record(stream)
         torch.cuda.synchronize()
     _barrier(ws)
@@ -624,34 +688,60 @@ def run_kda(args, ws, rank, local):
     tokens = w.B * w.T
     value = tokens * ws * args.steps / (ms_total / 1e3)
     peak, peak_kind = _peaks()
-    alg = kda_alg_bytes(w)
+    alg = token_serial_alg_bytes(w, ts.kda)
     achieved = alg / (ms_step / 1e3) / 1e9
+
+    # end to end through the public API from pinned host buffers (two-precision only)
+    e2e = None
+    if not args.no_e2e and not ts.kda:
+        names = ("q", "k", "v", "beta", "g", "h0")
+        host = {n: cpu[n].pin_memory() for n in names}
+        o_h = torch.empty(w.B, w.T, w.Hv, w.Dv).pin_memory()
+        ht_h = torch.empty(w.B, w.Hv, w.Dk, w.Dv).pin_memory()
+        o_d = torch.empty(w.B, w.T, w.Hv, w.Dv, device=dev)
+        ht_d = torch.empty(w.B, w.Hv, w.Dk, w.Dv, device=dev)
+        h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+        d2h = o_h.numel() * 4 + ht_h.numel() * 4
+
+        def e2e_step():
+            for n in names:
+                d[n].copy_(host[n], non_blocking=True)
+            ts.call(w, d, out=(o_d, ht_d))
+            o_h.copy_(o_d, non_blocking=True)
+            ht_h.copy_(ht_d, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        _barrier(ws)
+        e0, e1 = ev(), ev()
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = _max_over_ranks(e0.elapsed_time(e1), ws, dev) / args.steps
+        e2e = {"value": round(tokens * ws / (ms_e2e / 1e3), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(ms_e2e, 4)}
+
     cpu_base = None
     if rank == 0 and not args.no_cpu_baseline:
-        from oracle.kda import kda_recurrent
-        t0 = time.time()
-        Ts = 256
-        sl = lambda x: x[:1, :Ts]
-        kda_recurrent(sl(cpu["q"]), sl(cpu["k"]), sl(cpu["v"]), sl(cpu["beta"]), sl(cpu["g_k"]),
-                      cpu["h0"][:1], state_mode=w.state_mode)
-        dt = time.time() - t0
+        Ts, dt = ts.cpu_sample(w, cpu)
         cpu_base = {"value": round(Ts / dt, 2), "unit": "tokens/s", "cores": torch.get_num_threads(),
                     "kind": "oracle",
-                    "sample": "1 sequence x %d tokens, all %d heads, fp64 KDA oracle" % (Ts, w.Hv)}
+                    "sample": "1 sequence x %d tokens, all %d heads, fp64 %s oracle" % (
+                        Ts, w.Hv, "KDA" if ts.kda else "two-precision")}
     line = {
-        "metric": KDA_METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
+        "metric": ts.metric, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), beta=sigmoid, "
-                "g per key channel=-softplus(N(0,1)), h0 N(0, 0.1^2))",
-        "config": {"workload": w.name, "mode": "kda", "B": w.B, "T": w.T, "Hk": w.Hk, "Hv": w.Hv,
-                   "Dk": w.Dk, "Dv": w.Dv, "state_mode": w.state_mode, "chunk": 64, "block_v": 64,
-                   "l2": "inputs larger than L2 (no flush needed)"},
-        "clocks": clk.summary(), "e2e": None, "gpu_launches": args.steps,
+        "data": ts.data(), "config": ts.config(w),
+        "clocks": clk.summary(), "e2e": e2e, "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": _traffic("kda_recurrent_kernel_kda_layer.md", KDA_SOURCES, args.workload),
-                     "kernel": "kda_recurrent_kernel", "peak_source": peak_kind,
+                     "traffic": _traffic(ts.profile, ts.sources, args.workload),
+                     "kernel": ts.kernel, "peak_source": peak_kind,
                      "alg_bytes_per_launch": alg, "launch_ms": round(ms_step, 4)},
         "cpu_baseline": cpu_base,
     }
@@ -685,6 +775,30 @@ def run_reference(args, ws, rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": w.name, "mode": "decode", "B": w.B, "T": w.T, "Hk": w.Hk,
                        "Hv": w.Hv, "Dk": w.Dk, "Dv": w.Dv, "state_mode": w.state_mode},
+            "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s",
+                             "cores": torch.get_num_threads(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    if args.mode in ("kda", "two_precision"):
+        ts = _TokenSerial(args.mode)
+        cpu = ts.make(w)
+        for _ in range(args.warmup):
+            ts.cpu_sample(w, cpu, Ts=64)
+        done = el = 0.0
+        for _ in range(args.steps):
+            n, dt = ts.cpu_sample(w, cpu, Ts=256)
+            done += n
+            el += dt
+        value = done / el
+        sample = "1 sequence x 256 tokens, all %d heads per step (fp64 %s oracle)" % (
+            w.Hv, "KDA" if ts.kda else "two-precision")
+        print(json.dumps({
+            "impl": "reference", "metric": ts.metric, "value": round(value, 2), "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el * 1e3 / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": ts.config(w),
             "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s",
                              "cores": torch.get_num_threads(), "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -734,7 +848,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=None)
-    ap.add_argument("--mode", default=None, choices=["fwd", "fwdbwd", "decode", "kda"])
+    ap.add_argument("--mode", default=None,
+                    choices=["fwd", "fwdbwd", "decode", "kda", "two_precision"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
@@ -746,15 +861,16 @@ def main():
     if args.mode is None:
         args.mode = "fwdbwd" if _backward_available() else "fwd"
     if args.workload is None:
-        args.workload = {"decode": "decode", "kda": "kda"}.get(args.mode, "layer")
+        args.workload = {"decode": "decode", "kda": "kda",
+                         "two_precision": "two_precision"}.get(args.mode, "layer")
     args.bwd_launches = BWD_LAUNCHES
     ws, rank, local = _dist()
     if args.impl == "reference":
         run_reference(args, ws, rank)
     elif args.mode == "decode":
         run_decode(args, ws, rank, local)
-    elif args.mode == "kda":
-        run_kda(args, ws, rank, local)
+    elif args.mode in ("kda", "two_precision"):
+        run_token_serial(args, ws, rank, local)
     else:
         run_ours(args, ws, rank, local)
     if ws > 1:

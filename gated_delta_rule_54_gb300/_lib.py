@@ -53,6 +53,18 @@ class GdnDecodeProblem(ctypes.Structure):
 
 
 _DP = ctypes.POINTER(GdnDecodeProblem)
+
+
+class GdnTwoPrecisionProblem(ctypes.Structure):
+    _fields_ = [
+        ("B", ctypes.c_int64), ("T", ctypes.c_int64),
+        ("Hk", ctypes.c_int32), ("Hv", ctypes.c_int32), ("Dk", ctypes.c_int32), ("Dv", ctypes.c_int32),
+        ("N", ctypes.c_int32), ("cu_seqlens", ctypes.c_void_p), ("scale", ctypes.c_float),
+        ("read_mode", ctypes.c_int32), ("flush", ctypes.c_int32), ("dtype", ctypes.c_int32),
+    ]
+
+
+_TP = ctypes.POINTER(GdnTwoPrecisionProblem)
 SIGNATURES = {
     "gdn_status_string": (ctypes.c_char_p, [ctypes.c_int]),
     "gdn_abi_version": (ctypes.c_int, []),
@@ -71,6 +83,8 @@ SIGNATURES = {
     "kda_recurrent_fwd_qdq": (ctypes.c_int, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "gdn_decode_validate": (ctypes.c_int, [_DP]),
     "gdn_decode_qdq": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "gdn_two_precision_validate": (ctypes.c_int, [_TP]),
+    "gdn_two_precision_fwd": (ctypes.c_int, [_TP, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 
 _lock = threading.Lock()

@@ -11,7 +11,8 @@ from typing import Optional
 
 import torch
 
-from ._lib import DTYPES, QDQ_MODES, READOUTS, GdnDecodeProblem, GdnError, GdnProblem, check, load
+from ._lib import (DTYPES, QDQ_MODES, READOUTS, GdnDecodeProblem, GdnError, GdnProblem,  # noqa: F401
+                   GdnTwoPrecisionProblem, check, load)
 
 _DT = {torch.bfloat16: DTYPES["bf16"], torch.float16: DTYPES["fp16"], torch.float32: DTYPES["fp32"]}
 
@@ -162,6 +163,48 @@ def kda_recurrent_fwd_qdq(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0,
     st = lib.kda_recurrent_fwd_qdq(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
                                    _ptr(g), _ptr(h0), _ptr(o), _ptr(ht), _stream(dev))
     check("kda_recurrent_fwd_qdq", st)
+    return o, ht
+
+
+def make_two_precision_problem(q, k, v, cu_seqlens=None, scale=1.0, read_mode="e4m3",
+                               flush=16) -> GdnTwoPrecisionProblem:
+    B, T, Hk, Dk = k.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    p = GdnTwoPrecisionProblem()
+    p.B, p.T, p.Hk, p.Hv, p.Dk, p.Dv = B, T, Hk, Hv, Dk, Dv
+    p.N = B if cu_seqlens is None else cu_seqlens.numel() - 1
+    p.cu_seqlens = _ptr(cu_seqlens)
+    p.scale = float(scale)
+    p.read_mode = _mode(read_mode)
+    p.flush = int(flush)
+    p.dtype = _DT.get(q.dtype, 99)
+    return p
+
+
+def gdn_two_precision_fwd(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0,
+                          read_mode="e4m3", flush=16, output_final_state=True, out=None):
+    """Two-precision GDN forward: fp32 recurrence anchor, E4M3 read copy (one scale per
+    value row over the 128 key channels) re-derived from the anchor every ``flush`` tokens
+    and read by the outputs only.  q, k [B,T,Hk,128] bf16; v [B,T,Hv,Dv] bf16; beta, g
+    [B,T,Hv] f32; h0 [N,Hv,128,Dv] f32 or None.  Returns (o [B,T,Hv,Dv] f32,
+    ht [N,Hv,128,Dv] f32 = the anchor, or None); ``out`` may pass preallocated (o, ht)."""
+    lib = load()
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g), ("h0", h0),
+                    ("cu_seqlens", cu_seqlens)):
+        _check_dev(name, t, dev)
+    p = make_two_precision_problem(q, k, v, cu_seqlens, scale, read_mode, flush)
+    check("gdn_two_precision_validate", lib.gdn_two_precision_validate(ctypes.byref(p)))
+    B, T, Hv, Dv = v.shape
+    if out is not None:
+        o, ht = out
+    else:
+        o = torch.empty(B, T, Hv, Dv, device=dev, dtype=torch.float32)
+        ht = (torch.empty(p.N, Hv, k.shape[3], Dv, device=dev, dtype=torch.float32)
+              if output_final_state else None)
+    st = lib.gdn_two_precision_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                   _ptr(g), _ptr(h0), _ptr(o), _ptr(ht), _stream(dev))
+    check("gdn_two_precision_fwd", st)
     return o, ht
 
 

@@ -64,6 +64,10 @@ WORKLOADS = {
     # KDA recurrence (per-key-channel decay), state QDQ every 64 tokens
     "kda": Workload("KDA recurrent B4 T4096 H16 D128 e4m3-state", B=4, T=4096, Hk=16, Hv=16,
                     Dk=128, Dv=128, w_mode="none", h0=True, seed=6),
+    # two-precision profile: fp32 anchor, E4M3 read copy (state_mode names the
+    # read quantizer), 16-token flushes
+    "two_precision": Workload("two-precision B4 T4096 H16 D128 e4m3-read flush16", B=4, T=4096,
+                              Hk=16, Hv=16, Dk=128, Dv=128, w_mode="none", h0=True, seed=7),
 }
 
 

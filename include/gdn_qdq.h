@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define GDN_QDQ_ABI_VERSION 3
+#define GDN_QDQ_ABI_VERSION 4
 
 typedef enum {
   GDN_QDQ_NONE = 0, /* site not quantized                                   */
@@ -309,6 +309,52 @@ gdn_status gdn_decode_qdq(const gdn_decode_problem* p, const void* q, const void
                           const void* v, const float* beta, const float* g,
                           const float* state_in, float* o, float* state_out, uint8_t* codes,
                           float* scales, void* stream);
+
+/*
+ * Two-precision GDN forward ("[5/8] ReplaySSM state QAT and two-precision
+ * GDN", section "What does this PR do?": an FP32 recurrence anchor and a
+ * dynamic FP8 E4M3 read copy grouped by the 128 key channels of each value
+ * row; every 16-token flush recomputes the recurrence from the raw inputs and
+ * the anchor; read-side quantization errors never overwrite the anchor; GDN
+ * with K = 128, FP8 or disabled read quantization).  The page prints no
+ * formula; the reading implemented here, per sequence and value head with
+ * H = S^T (Dk x Dv), t counted from the sequence start and W = p->flush:
+ *     A <- h0 (the anchor), and for each token:
+ *     if t % W == 0:  R <- Q_read(A)   (E4M3 fake QDQ, one scale per column of H
+ *                                       over all Dk key rows, as fake_qdq_e4m3
+ *                                       with rows = Dk, group_cols = 1)
+ *     A <- exp(g_t) A;  A <- A + beta_t k_t (v_t - A^T k_t)^T
+ *     R <- exp(g_t) R;  R <- R + beta_t k_t (v_t - R^T k_t)^T
+ *     o_t = scale R^T q_t
+ * and ht = A, the unquantized recurrence.  read_mode NONE makes R = A: the
+ * plain gated delta rule token recurrence.
+ *   q, k  bf16 [B, T, Hk, 128]     v bf16 [B, T, Hv, Dv]   beta, g f32 [B, T, Hv]
+ *   h0    f32  [N, Hv, 128, Dv] or NULL (zeros)
+ *   o     f32  [B, T, Hv, Dv] (written)     ht f32 [N, Hv, 128, Dv] or NULL (written)
+ * Dk must be 128 (GDN_ERR_UNSUPPORTED_SHAPE), Dv 64 or 128; read_mode NONE or
+ * E4M3 (INT8: GDN_ERR_UNSUPPORTED_MODE); flush >= 1; N <= 65535; packed
+ * sequences and grouped heads as for the chunked forward; all pointers 16-byte
+ * aligned (GDN_ERR_MISALIGNED).
+ */
+typedef struct {
+  int64_t B;                  /* batch rows (1 when packed)                     */
+  int64_t T;                  /* tokens per row (total tokens when packed)      */
+  int32_t Hk, Hv, Dk, Dv;     /* Dk == 128; Dv in {64, 128}; Hv % Hk == 0       */
+  int32_t N;                  /* sequences: == B, or packed count (>= 1)        */
+  const int32_t* cu_seqlens;  /* device [N + 1] int32, or NULL                  */
+  float scale;                /* output scale                                   */
+  int32_t read_mode;          /* gdn_qdq_mode of the read copy: NONE or E4M3    */
+  int32_t flush;              /* flush period W in tokens (16 on the page)      */
+  int32_t dtype;              /* gdn_dtype of q, k, v; must be BF16             */
+} gdn_two_precision_problem;
+
+/* Host-only validation of a two-precision problem (no CUDA call). */
+gdn_status gdn_two_precision_validate(const gdn_two_precision_problem* p);
+
+gdn_status gdn_two_precision_fwd(const gdn_two_precision_problem* p, const void* q,
+                                 const void* k, const void* v, const float* beta,
+                                 const float* g, const float* h0, float* o, float* ht,
+                                 void* stream);
 
 #ifdef __cplusplus
 }

@@ -145,7 +145,7 @@ def test_status_strings():
     for code in range(-7, 1):
         s = lib.gdn_status_string(code).decode()
         assert s.startswith("GDN_")
-    assert lib.gdn_abi_version() == 3
+    assert lib.gdn_abi_version() == 4
 
 
 def _dproblem(**kw):
@@ -184,3 +184,40 @@ def test_decode_entry_rejects_before_launch():
     assert call(ok, f, f, f, f, f, P(1 << 20), f, P((1 << 20) + n // 2), None, None, None) == -1
     assert call(_dproblem(B=0), None, None, None, None, None, None, None, None, None, None,
                 None) == 0
+
+
+def _tproblem(**kw):
+    p = _lib.GdnTwoPrecisionProblem()
+    p.B, p.T, p.Hk, p.Hv, p.Dk, p.Dv, p.N = 2, 100, 2, 4, 128, 128, 2
+    p.scale, p.read_mode, p.flush, p.dtype = 1.0, 1, 16, 0
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(), 0), (dict(read_mode=0), 0), (dict(Dv=64), 0), (dict(flush=1), 0), (dict(T=0), 0),
+    (dict(flush=100000), 0), (dict(read_mode=2), -4), (dict(read_mode=7), -1), (dict(flush=0), -1),
+    (dict(Dk=64), -3), (dict(Dv=96), -3), (dict(Hv=3), -3), (dict(dtype=2), -2), (dict(dtype=1), -2),
+    (dict(N=3), -1), (dict(B=-1), -1), (dict(scale=float("nan")), -1),
+    (dict(B=70000, N=70000), -3),
+])
+def test_two_precision_validate(kw, code):
+    assert _lib.load().gdn_two_precision_validate(ctypes.byref(_tproblem(**kw))) == code
+
+
+def test_two_precision_entry_rejects_before_launch():
+    lib = _lib.load()
+    P = ctypes.c_void_p
+    f = P(4096)
+    call = lambda p, *a: lib.gdn_two_precision_fwd(ctypes.byref(p), *a)
+    assert call(_tproblem(read_mode=2), f, f, f, f, f, None, f, f, None) == -4
+    assert call(_tproblem(), None, f, f, f, f, None, f, f, None) == -1          # null q
+    assert call(_tproblem(), f, f, f, f, f, None, None, f, None) == -1          # null o
+    assert call(_tproblem(), f, f, f, f, f, P(4104), f, f, None) == -7          # misaligned h0
+    # packed sequences: B == 1 and N >= 1
+    assert lib.gdn_two_precision_validate(ctypes.byref(_tproblem(B=2, N=3, cu_seqlens=f))) == -1
+    assert lib.gdn_two_precision_validate(ctypes.byref(_tproblem(B=1, N=3, cu_seqlens=f))) == 0
+    # nothing to do: no sequences, or no tokens and no final state
+    assert call(_tproblem(B=0, N=0), None, None, None, None, None, None, None, None, None) == 0
+    assert call(_tproblem(T=0), None, None, None, None, None, None, None, None, None) == 0
