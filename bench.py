@@ -172,6 +172,69 @@ class ClockSampler:
                 "samples": len(self.samples), "source": "nvml" if self.nvml else "nvidia-smi"}
 
 
+def e2e_pipelined(dev, ws, steps, warmup, host_in, dev_in, run, res_h):
+    """End-to-end timing through the public API from pinned host memory.
+
+    Every step copies its inputs host -> device (``host_in[name]`` into
+    ``dev_in[set][name]``), runs ``run(set)`` (the library calls; returns the
+    device result tensors) and copies every result back into ``res_h[set]``.
+    Three streams and two device buffer sets let step i's compute overlap the
+    upload of step i+1 and the download of step i-1, as a pipelined user loop
+    would; events order each buffer set's reuse.  Returns (pipelined ms per
+    step, serial ms per step), both max over ranks; the serial figure runs the
+    same steps on one stream, copies and compute back to back."""
+    s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_cmp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def step(i):
+        st = i % 2
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_cmp[st])          # step i-2 no longer reads this input set
+            for n, t in dev_in[st].items():
+                t.copy_(host_in[n], non_blocking=True)
+            ev_in[st].record(s_in)
+        with torch.cuda.stream(s_cmp):
+            s_cmp.wait_event(ev_in[st])
+            s_cmp.wait_event(ev_out[st])         # step i-2's results have left this set
+            outs = run(st)
+            ev_cmp[st].record(s_cmp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_cmp[st])
+            for dst, src in zip(res_h[st], outs):
+                dst.copy_(src, non_blocking=True)
+            ev_out[st].record(s_out)
+
+    def serial_step():
+        for n, t in dev_in[0].items():
+            t.copy_(host_in[n], non_blocking=True)
+        for dst, src in zip(res_h[0], run(0)):
+            dst.copy_(src, non_blocking=True)
+
+    t = {}
+    for kind in ("pipelined", "serial"):
+        for i in range(max(2, warmup)):
+            step(i) if kind == "pipelined" else serial_step()
+        torch.cuda.synchronize()
+        _barrier(ws)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        if kind == "pipelined":
+            a.record(s_in)
+            for i in range(steps):
+                step(i)
+            s_in.wait_stream(s_out)
+            b.record(s_in)
+        else:
+            a.record()
+            for _ in range(steps):
+                serial_step()
+            b.record()
+        torch.cuda.synchronize()
+        t[kind] = _max_over_ranks(a.elapsed_time(b), ws, dev) / steps
+    return t["pipelined"], t["serial"]
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -340,48 +403,45 @@ def run_ours(args, ws, rank, local):
     # end to end through the public API from pinned host buffers
     e2e = None
     if not args.no_e2e:
-        host = {kk: (vv.pin_memory() if isinstance(vv, torch.Tensor) else vv) for kk, vv in cpu.items()}
-        bufs = dict(q=q, k=k, v=v, beta=beta, g=g, h0=h0)
+        names = [n for n in ("q", "k", "v", "beta", "g", "h0") if cpu[n] is not None]
+        host_in = {n: cpu[n].pin_memory() for n in names}
         if bwd:
-            host["do"] = do.cpu().pin_memory()
-            host["dht"] = dht.cpu().pin_memory()
-            bufs.update(do=do, dht=dht)
-            grads = (torch.empty_like(q, dtype=torch.float32), torch.empty_like(k, dtype=torch.float32),
-                     torch.empty_like(v, dtype=torch.float32), torch.empty_like(beta),
-                     torch.empty_like(g), torch.empty_like(ht))
-            results = (o, ht) + grads
-        else:
-            results = (o, ht)
-        res_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in results]
-        h2d = sum(host[n].numel() * host[n].element_size() for n in bufs if host[n] is not None)
-        d2h = sum(t.numel() * t.element_size() for t in res_h)
+            host_in["do"] = do.cpu().pin_memory()
+            host_in["dht"] = dht.cpu().pin_memory()
+        dev_in = [{n: torch.empty_like(t, device=dev) for n, t in host_in.items()} for _ in range(2)]
 
-        def e2e_step():
-            for n, t in bufs.items():
-                if t is not None:
-                    t.copy_(host[n], non_blocking=True)
-            api.gdn_chunk_fwd_qdq(q, k, v, beta, g, h0, state_mode=sm, w_mode=wm, out=(o, ht, ctx),
+        def result_set():
+            r = [torch.empty_like(o), torch.empty_like(ht)]
+            if bwd:
+                r += [torch.empty_like(q, dtype=torch.float32), torch.empty_like(k, dtype=torch.float32),
+                      torch.empty_like(v, dtype=torch.float32), torch.empty_like(beta),
+                      torch.empty_like(g), torch.empty_like(ht)]
+            return r
+
+        res_d = [result_set(), result_set()]
+        res_h = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in r] for r in res_d]
+
+        def run(st):
+            x, r = dev_in[st], res_d[st]
+            api.gdn_chunk_fwd_qdq(x["q"], x["k"], x["v"], x["beta"], x["g"], x.get("h0"),
+                                  state_mode=sm, w_mode=wm, out=(r[0], r[1], ctx),
                                   block_v=bv, neumann_degree=nd)
             if bwd:
-                api.gdn_chunk_bwd_ste(q, k, v, beta, g, ctx, do, dht, state_mode=sm, w_mode=wm,
-                                      workspace=wsb, out=grads, block_v=bv, neumann_degree=nd)
-            for dst, src in zip(res_h, results):
-                dst.copy_(src, non_blocking=True)
+                api.gdn_chunk_bwd_ste(x["q"], x["k"], x["v"], x["beta"], x["g"], ctx, x["do"],
+                                      x["dht"], state_mode=sm, w_mode=wm, workspace=wsb,
+                                      out=tuple(r[2:]), block_v=bv, neumann_degree=nd)
+            return r
 
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
-        torch.cuda.synchronize()
-        _barrier(ws)
-        a, b = ev(), ev()
-        a.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        b.record(stream)
-        torch.cuda.synchronize()
-        e_ms = _max_over_ranks(a.elapsed_time(b), ws, dev)
-        e2e = {"value": round(tokens * ws * args.steps / (e_ms / 1e3), 1), "unit": "tokens/s",
+        e_ms, s_ms = e2e_pipelined(dev, ws, args.steps, args.warmup, host_in, dev_in, run, res_h)
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in res_h[0])
+        e2e = {"value": round(tokens * ws / (e_ms / 1e3), 1), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": round(e_ms / args.steps, 4)}
+               "ms_per_step": round(e_ms, 4),
+               "schedule": "pipelined: step i+1's upload and step i-1's download overlap step i's "
+                           "compute (three streams, two device buffer sets)",
+               "serial_value": round(tokens * ws / (s_ms / 1e3), 1),
+               "serial_ms_per_step": round(s_ms, 4)}
 
     cpu_base = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -695,35 +755,25 @@ def run_token_serial(args, ws, rank, local):
     e2e = None
     if not args.no_e2e and not ts.kda:
         names = ("q", "k", "v", "beta", "g", "h0")
-        host = {n: cpu[n].pin_memory() for n in names}
-        o_h = torch.empty(w.B, w.T, w.Hv, w.Dv).pin_memory()
-        ht_h = torch.empty(w.B, w.Hv, w.Dk, w.Dv).pin_memory()
-        o_d = torch.empty(w.B, w.T, w.Hv, w.Dv, device=dev)
-        ht_d = torch.empty(w.B, w.Hv, w.Dk, w.Dv, device=dev)
-        h2d = sum(host[n].numel() * host[n].element_size() for n in names)
-        d2h = o_h.numel() * 4 + ht_h.numel() * 4
+        host_in = {n: cpu[n].pin_memory() for n in names}
+        dev_in = [{n: torch.empty_like(t, device=dev) for n, t in host_in.items()} for _ in range(2)]
+        res_d = [[torch.empty(w.B, w.T, w.Hv, w.Dv, device=dev),
+                  torch.empty(w.B, w.Hv, w.Dk, w.Dv, device=dev)] for _ in range(2)]
+        res_h = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in r] for r in res_d]
 
-        def e2e_step():
-            for n in names:
-                d[n].copy_(host[n], non_blocking=True)
-            ts.call(w, d, out=(o_d, ht_d))
-            o_h.copy_(o_d, non_blocking=True)
-            ht_h.copy_(ht_d, non_blocking=True)
+        def run(st):
+            ts.call(w, dev_in[st], out=tuple(res_d[st]))
+            return res_d[st]
 
-        for _ in range(2):
-            e2e_step()
-        torch.cuda.synchronize()
-        _barrier(ws)
-        e0, e1 = ev(), ev()
-        e0.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        e1.record(stream)
-        torch.cuda.synchronize()
-        ms_e2e = _max_over_ranks(e0.elapsed_time(e1), ws, dev) / args.steps
-        e2e = {"value": round(tokens * ws / (ms_e2e / 1e3), 1), "unit": "tokens/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": round(ms_e2e, 4)}
+        e_ms, s_ms = e2e_pipelined(dev, ws, args.steps, args.warmup, host_in, dev_in, run, res_h)
+        e2e = {"value": round(tokens * ws / (e_ms / 1e3), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in.values()),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in res_h[0]),
+               "ms_per_step": round(e_ms, 4),
+               "schedule": "pipelined: step i+1's upload and step i-1's download overlap step i's "
+                           "compute (three streams, two device buffer sets)",
+               "serial_value": round(tokens * ws / (s_ms / 1e3), 1),
+               "serial_ms_per_step": round(s_ms, 4)}
 
     cpu_base = None
     if rank == 0 and not args.no_cpu_baseline:

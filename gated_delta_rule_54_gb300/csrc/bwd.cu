@@ -25,6 +25,7 @@
 //     is order independent, so results are deterministic.
 // Gradients tolerate bf16 operands (no hi/lo splits): the backward has no
 // quantization decision to preserve.
+#define GDN_WGEMM_UNROLL2  // see wgemm
 #include "common.cuh"
 #include "launch.h"
 
