@@ -335,19 +335,23 @@ namespace gdn {
 // (AT = true); B is stored [k][n] (BKN = true) or [n][k] (BKN = false).
 // RLA / RLB are the row lengths (elements) of the swizzled tiles.
 // ---------------------------------------------------------------------------
-// A translation unit that defines GDN_WGEMM_UNROLL2 before including this
-// header gets the k loop unrolled by two (the next step's fragment loads then
-// issue ahead of the current step's MMAs).  The backward kernels, with 16
-// warps and one CTA per SM, run 7 % faster that way; the forward kernels run
-// slower, so it is a per-file choice.
-template <int NT, bool AT, bool BKN, int RLA, int RLB>
+// UNROLL = 2 unrolls the k loop by two (the next step's fragment loads then
+// issue ahead of the current step's MMAs).  The default is 1, or 2 in a
+// translation unit that defines GDN_WGEMM_UNROLL2 before including this
+// header: the backward kernels (16 warps, one CTA per SM) run 7 % faster
+// unrolled, the forward kernels choose per call site.
+#ifdef GDN_WGEMM_UNROLL2
+constexpr int kWgemmUnroll = 2;
+#else
+constexpr int kWgemmUnroll = 1;
+#endif
+
+template <int NT, bool AT, bool BKN, int RLA, int RLB, int UNROLL = kWgemmUnroll>
 __device__ __forceinline__ void wgemm(float (&acc)[NT][4], const __nv_bfloat16* A, int m0,
                                       const __nv_bfloat16* B, int n0, int k0, int k1, int lane) {
   static_assert(NT % 2 == 0, "n tiles come in pairs");
-#ifdef GDN_WGEMM_UNROLL2
-#pragma unroll 2
-#endif
-  for (int k = k0; k < k1; k += 16) {
+  static_assert(UNROLL == 1 || UNROLL == 2, "unroll factor");
+  auto step = [&](int k) {
     uint32_t a[4];
     if constexpr (AT)
       ldsm_x4_t(a, at_frag_addr<RLA>(A, m0, k, lane));
@@ -363,6 +367,12 @@ __device__ __forceinline__ void wgemm(float (&acc)[NT][4], const __nv_bfloat16* 
       mma_bf16(acc[2 * np], a, b[0], b[1]);
       mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
     }
+  };
+  if constexpr (UNROLL == 2) {
+#pragma unroll 2
+    for (int k = k0; k < k1; k += 16) step(k);
+  } else {
+    for (int k = k0; k < k1; k += 16) step(k);
   }
 }
 
