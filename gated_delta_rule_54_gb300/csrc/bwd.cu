@@ -650,12 +650,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
+          const float2 pv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(Pb + swz<64>(i, j)));
+          const float gi = gam[i];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int jj = j + e;
             const float d = (jj <= i) ? p.scale * dp[nt][2 * e2 + e] : 0.f;
-            gma[nt][2 * e2 + e] += (jj <= i) ? d * expf(gam[i] - gam[jj]) : 0.f;
-            pp[nt][2 * e2 + e] = d * __bfloat162float(Pb[swz<64>(i, jj)]);
+            gma[nt][2 * e2 + e] += (jj <= i) ? d * __expf(gi - gam[jj]) : 0.f;
+            pp[nt][2 * e2 + e] = d * (e == 0 ? pv.x : pv.y);
           }
         }
       float r0, r1;
@@ -678,11 +680,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
 #pragma unroll
       for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = wrow0 + gq + 8 * (e >> 1), d = wcol0 + nt * 8 + 2 * tq + (e & 1);
-          const float v = p.scale * eg[i] * acc[nt][e];
-          dQ[nt][e] += v;
-          qd[nt][e] = v * __bfloat162float(Qs[swz<DK>(i, d)]);
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int i = wrow0 + gq + 8 * e2, d = wcol0 + nt * 8 + 2 * tq;
+          const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(Qs + swz<DK>(i, d)));
+          const float si = p.scale * eg[i];
+          const float v0 = si * acc[nt][2 * e2], v1 = si * acc[nt][2 * e2 + 1];
+          dQ[nt][2 * e2] += v0;
+          dQ[nt][2 * e2 + 1] += v1;
+          qd[nt][2 * e2] = v0 * qv.x;
+          qd[nt][2 * e2 + 1] = v1 * qv.y;
         }
       float r0, r1;
       row_sums<NTW>(qd, r0, r1);
@@ -697,11 +703,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
 #pragma unroll
       for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = wrow0 + gq + 8 * (e >> 1), d = wcol0 + nt * 8 + 2 * tq + (e & 1);
-          const float v = dec[i] * acc[nt][e];
-          dK[nt][e] += v;
-          kd[nt][e] = v * __bfloat162float(Ks[swz<DK>(i, d)]);
+        for (int e2 = 0; e2 < 2; ++e2) {
+          const int i = wrow0 + gq + 8 * e2, d = wcol0 + nt * 8 + 2 * tq;
+          const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(Ks + swz<DK>(i, d)));
+          const float di = dec[i];
+          const float v0 = di * acc[nt][2 * e2], v1 = di * acc[nt][2 * e2 + 1];
+          dK[nt][2 * e2] += v0;
+          dK[nt][2 * e2 + 1] += v1;
+          kd[nt][2 * e2] = v0 * kv.x;
+          kd[nt][2 * e2 + 1] = v1 * kv.y;
         }
       float r0, r1;
       row_sums<NTW>(kd, r0, r1);
@@ -776,10 +786,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
 #pragma unroll
     for (int nt = 0; nt < NTW; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int i = wrow0 + gq + 8 * (e >> 1), d = wcol0 + nt * 8 + 2 * tq + (e & 1);
-        dK[nt][e] += beg[i] * acc[nt][e];
-        kw[nt][e] = acc[nt][e] * __bfloat162float(Ks[swz<DK>(i, d)]);
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int i = wrow0 + gq + 8 * e2, d = wcol0 + nt * 8 + 2 * tq;
+        const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(Ks + swz<DK>(i, d)));
+        dK[nt][2 * e2] += beg[i] * acc[nt][2 * e2];
+        dK[nt][2 * e2 + 1] += beg[i] * acc[nt][2 * e2 + 1];
+        kw[nt][2 * e2] = acc[nt][2 * e2] * kv.x;
+        kw[nt][2 * e2 + 1] = acc[nt][2 * e2 + 1] * kv.y;
       }
     float r0, r1;
     row_sums<NTW>(kw, r0, r1);
@@ -876,12 +889,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdPar
       for (int e2 = 0; e2 < 2; ++e2) {
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
         float kk[2];
+        const float2 gv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(GKKb + swz<64>(i, j)));
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int jj = j + e;
           const float da = (jj < i) ? -acc[nt][2 * e2 + e] : 0.f;
-          const float gkk = __bfloat162float(GKKb[swz<64>(i, jj)]);
-          kk[e] = da * bet[i] * ((jj < i) ? expf(gam[i] - gam[jj]) : 0.f);
+          const float gkk = e == 0 ? gv.x : gv.y;
+          kk[e] = da * bet[i] * ((jj < i) ? __expf(gam[i] - gam[jj]) : 0.f);
           ba[nt][2 * e2 + e] = da * gkk;
           aa[nt][2 * e2 + e] = da * bet[i] * gkk;  // A = diag(beta) (Gamma o KK^T), strictly lower
         }
