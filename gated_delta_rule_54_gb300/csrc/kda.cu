@@ -7,13 +7,17 @@
 //     if t % chunk == 0:  H <- Q(H)                  (t from the sequence start)
 //     H <- diag(exp(g_t)) H;  H <- H + beta_t k_t (v_t - H^T k_t)^T;  o_t = scale H^T q_t
 //
-// The columns of H evolve independently given the token vectors, so one CTA
-// owns a [Dk x 64] column block of one (sequence, value head) and walks its
-// tokens in order with the block in registers: 256 threads, thread (rg, cq)
-// holds columns 4cq..4cq+3 of rows rg, rg + 16, ...  Per token two block
-// barriers: the column sums H^T k (after the decay) and H^T q reduce across
-// the 16 row groups in shared memory.  The next token's vectors are fetched
-// into registers while the current token computes.
+// The columns of H evolve independently given the token vectors, so a warp
+// owns four value columns over all Dk key rows (lane l: rows RPL l .. RPL l +
+// RPL - 1, RPL = Dk / 32) and walks the tokens with its part of H in
+// registers; a CTA of 16 warps covers one 64-column value block, which holds
+// every [Dk, block_v] scale tile whole.  No block barrier is on the token
+// path: per token one warp reduction (halving exchanges, 9 shuffles) serves
+// this token's readout H^T q and the next token's H^T (e^{g'} o k'), whose
+// four sums are gathered back to every lane (4 shuffles).  The state QDQ
+// (every `chunk` tokens) takes the tile amax through shared memory with one
+// block barrier (its buffer alternates, so no second barrier is needed).
+// Token vectors are fetched four tokens ahead into a register ring.
 #include "common.cuh"
 #include "launch.h"
 
@@ -21,10 +25,10 @@ namespace gdn {
 
 namespace {
 
-constexpr int kKdaThreads = 256;
-constexpr int kKdaWarps = kKdaThreads / 32;
-constexpr int kKdaC4 = 16;                         // column quads of the 64-column block
-constexpr int kKdaRG = kKdaThreads / kKdaC4;       // row groups
+constexpr int kKdaWarps = 16;                  // one 64-column value block
+constexpr int kKdaThreads = kKdaWarps * 32;
+constexpr int kKdaCols = 4;                    // value columns per warp
+constexpr int kKdaRing = 4;                    // tokens in flight per warp
 
 struct KdaParams {
   const __nv_bfloat16 *q, *k, *v;
@@ -36,53 +40,34 @@ struct KdaParams {
   float scale;
 };
 
-__device__ __forceinline__ float4 fma4s(float a, float4 x, float4 y) {
-  return make_float4(fmaf(a, x.x, y.x), fmaf(a, x.y, y.y), fmaf(a, x.z, y.z), fmaf(a, x.w, y.w));
-}
+// one token's inputs as a lane needs them: k, q and g at its RPL key rows,
+// v at the warp's four value columns, beta
+template <int RPL>
+struct KdaTok {
+  uint32_t k[RPL / 2], q[RPL / 2];
+  float g[RPL];
+  uint2 v;
+  float b;
+};
 
-template <int MODE>
-__device__ __forceinline__ float4 qdq4v(float4 x, float s, float r, bool zero) {
-  if (zero) return x;
-  return make_float4(__fmul_rn(qdq_code_value<MODE>(qdq_code<MODE>(x.x, r)), s),
-                     __fmul_rn(qdq_code_value<MODE>(qdq_code<MODE>(x.y, r)), s),
-                     __fmul_rn(qdq_code_value<MODE>(qdq_code<MODE>(x.z, r)), s),
-                     __fmul_rn(qdq_code_value<MODE>(qdq_code<MODE>(x.w, r)), s));
-}
-
-// column sums over the 16 row groups of per-thread partials (4 columns);
-// red: shared [kKdaWarps][64].  Valid for every thread after the barrier.
-__device__ __forceinline__ float4 kda_colsum(float4 p, int lane, int warp, float (*red)[64]) {
-  p.x += __shfl_xor_sync(0xffffffffu, p.x, 16);
-  p.y += __shfl_xor_sync(0xffffffffu, p.y, 16);
-  p.z += __shfl_xor_sync(0xffffffffu, p.z, 16);
-  p.w += __shfl_xor_sync(0xffffffffu, p.w, 16);
-  if (lane < 16) *reinterpret_cast<float4*>(&red[warp][lane * 4]) = p;
-  __syncthreads();
-  float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-  const int cq = lane & 15;
-#pragma unroll
-  for (int w = 0; w < kKdaWarps; ++w) {
-    const float4 x = *reinterpret_cast<const float4*>(&red[w][cq * 4]);
-    s.x += x.x;
-    s.y += x.y;
-    s.z += x.z;
-    s.w += x.w;
+template <int RPL>
+__device__ __forceinline__ void unpack_rows(const uint32_t (&u)[RPL / 2], float (&x)[RPL]) {
+  if constexpr (RPL == 4) {
+    bf16x4(make_uint2(u[0], u[1]), x);
+  } else {
+    bf16x2(u[0], x);
   }
-  return s;
 }
 
 template <int DK, int MODE>
 __global__ void __launch_bounds__(kKdaThreads, 1) kda_recurrent_kernel(const KdaParams p) {
-  constexpr int RPT = DK / kKdaRG;  // rows per thread
+  constexpr int RPL = DK / 32;  // key rows per lane
   constexpr bool QUANT = MODE != GDN_QDQ_NONE;
-  __shared__ __align__(16) float red[2][kKdaWarps][64];
-  __shared__ float amx[kKdaWarps][4];
-  __shared__ __align__(16) float tv[2][3][DK];    // k, q, e^g of a token (two tokens in turn)
-  __shared__ __align__(16) float tvv[2][64 + 4];  // v block and beta
+  __shared__ float amx[2][kKdaWarps];  // per-warp amax, alternate buffers
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int cq = tid % kKdaC4, rg = tid / kKdaC4;
-  const int vb = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c0 = blockIdx.x * 64 + warp * kKdaCols;
+  const int h = blockIdx.y, n = blockIdx.z;
   const int hk = h / (p.Hv / p.Hk);
   int64_t tok0;
   int L;
@@ -93,108 +78,164 @@ __global__ void __launch_bounds__(kKdaThreads, 1) kda_recurrent_kernel(const Kda
     tok0 = (int64_t)n * p.T;
     L = (int)p.T;
   }
-  const int tile = (cq * 4) / p.block_v;
-  const int64_t sbase = ((int64_t)n * p.Hv + h) * DK * p.Dv + vb * 64 + cq * 4;
 
-  float4 S[RPT];
+  float H[RPL][kKdaCols];
+  const int64_t sbase = (((int64_t)n * p.Hv + h) * DK + RPL * lane) * p.Dv + c0;
 #pragma unroll
-  for (int i = 0; i < RPT; ++i)
-    S[i] = p.h0 ? *reinterpret_cast<const float4*>(p.h0 + sbase + (int64_t)(rg + kKdaRG * i) * p.Dv)
-                : make_float4(0.f, 0.f, 0.f, 0.f);
-
-  // the next token's vectors in registers: threads < DK hold k, q, g of one
-  // key channel; threads < 64 one value; thread 64 (or 0 when DK == 64) beta
-  float k_nx = 0.f, q_nx = 0.f, g_nx = 0.f, v_nx = 0.f, b_nx = 0.f;
-  auto fetch = [&](int lt) {
-    const int64_t t = tok0 + lt;
-    if (tid < DK) {
-      k_nx = __bfloat162float(p.k[(t * p.Hk + hk) * DK + tid]);
-      q_nx = __bfloat162float(p.q[(t * p.Hk + hk) * DK + tid]);
-      g_nx = p.g[(t * p.Hv + h) * DK + tid];
-    }
-    if (tid < 64) v_nx = __bfloat162float(p.v[(t * p.Hv + h) * p.Dv + vb * 64 + tid]);
-    if (tid == 64 % DK) b_nx = p.beta[t * p.Hv + h];
-  };
-  auto publish = [&](int buf) {
-    if (tid < DK) {
-      tv[buf][0][tid] = k_nx;
-      tv[buf][1][tid] = q_nx;
-      tv[buf][2][tid] = expf(g_nx);
-    }
-    if (tid < 64) tvv[buf][tid] = v_nx;
-    if (tid == 64 % DK) tvv[buf][64] = b_nx;
-  };
-  if (L > 0) {
-    fetch(0);
-    publish(0);
+  for (int r = 0; r < RPL; ++r) {
+    const float4 x = p.h0 ? *reinterpret_cast<const float4*>(p.h0 + sbase + (int64_t)r * p.Dv)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    H[r][0] = x.x;
+    H[r][1] = x.y;
+    H[r][2] = x.z;
+    H[r][3] = x.w;
   }
-  __syncthreads();
 
-  for (int lt = 0; lt < L; ++lt) {
-    const int buf = lt & 1;
-    const int64_t t = tok0 + lt;
-    if (lt + 1 < L) fetch(lt + 1);
+  auto load = [&](int lt) {
+    KdaTok<RPL> tv;
+    if (lt < L) {
+      const int64_t t = tok0 + lt;
+      const int64_t kq = (t * p.Hk + hk) * DK + RPL * lane;
+      const int64_t gr = (t * p.Hv + h) * DK + RPL * lane;
+      if constexpr (RPL == 4) {
+        const uint2 kk = __ldg(reinterpret_cast<const uint2*>(p.k + kq));
+        const uint2 qq = __ldg(reinterpret_cast<const uint2*>(p.q + kq));
+        const float4 gg = __ldg(reinterpret_cast<const float4*>(p.g + gr));
+        tv.k[0] = kk.x; tv.k[1] = kk.y;
+        tv.q[0] = qq.x; tv.q[1] = qq.y;
+        tv.g[0] = gg.x; tv.g[1] = gg.y; tv.g[2] = gg.z; tv.g[3] = gg.w;
+      } else {
+        tv.k[0] = __ldg(reinterpret_cast<const uint32_t*>(p.k + kq));
+        tv.q[0] = __ldg(reinterpret_cast<const uint32_t*>(p.q + kq));
+        const float2 gg = __ldg(reinterpret_cast<const float2*>(p.g + gr));
+        tv.g[0] = gg.x; tv.g[1] = gg.y;
+      }
+      tv.v = __ldg(reinterpret_cast<const uint2*>(p.v + (t * p.Hv + h) * p.Dv + c0));
+      tv.b = __ldg(p.beta + t * p.Hv + h);
+    } else {
+#pragma unroll
+      for (int i = 0; i < RPL / 2; ++i) tv.k[i] = tv.q[i] = 0u;
+#pragma unroll
+      for (int i = 0; i < RPL; ++i) tv.g[i] = 0.f;
+      tv.v = make_uint2(0u, 0u);
+      tv.b = 0.f;
+    }
+    return tv;
+  };
 
-    // ---- state QDQ at chunk boundaries, per [Dk, block_v] tile ----
+  // H <- Q(H) per [Dk, block_v] tile: the warp's four columns lie in one tile
+  // of block_v / 4 warps; their amax meet in shared memory
+  int par = 0;
+  auto qdq = [&]() {
     if constexpr (QUANT) {
-      if (lt % p.chunk == 0) {
-        float m = 0.f;
+      float m = 0.f;
 #pragma unroll
-        for (int i = 0; i < RPT; ++i)
-          m = fmaxf(m, fmaxf(fmaxf(fabsf(S[i].x), fabsf(S[i].y)), fmaxf(fabsf(S[i].z), fabsf(S[i].w))));
-        for (int o = 1; o < p.block_v / 4; o <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 16));
-        if (lane < 16 && (cq * 4) % p.block_v == 0) amx[warp][tile] = m;
-        __syncthreads();
-        float a = amx[0][tile];
+      for (int r = 0; r < RPL; ++r)
 #pragma unroll
-        for (int w = 1; w < kKdaWarps; ++w) a = fmaxf(a, amx[w][tile]);
-        float s, r;
-        qdq_scale<MODE>(a, s, r);
+        for (int c = 0; c < kKdaCols; ++c) m = fmaxf(m, fabsf(H[r][c]));
+      m = warp_max(m);
+      if (lane == 0) amx[par][warp] = m;
+      __syncthreads();
+      const int wpt = p.block_v / kKdaCols;  // warps per tile
+      const int w0 = warp - warp % wpt;
+      float a = 0.f;
+      for (int w = w0; w < w0 + wpt; ++w) a = fmaxf(a, amx[par][w]);
+      par ^= 1;
+      float s, rcp;
+      qdq_scale<MODE>(a, s, rcp);
+      if (a != 0.f) {
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) S[i] = qdq4v<MODE>(S[i], s, r, a == 0.f);
+        for (int r = 0; r < RPL; ++r)
+#pragma unroll
+          for (int c = 0; c < kKdaCols; ++c)
+            H[r][c] = __fmul_rn(qdq_code_value<MODE>(qdq_code<MODE>(H[r][c], rcp)), s);
       }
     }
+  };
 
-    // ---- decay per key channel, then H^T k ----
-    const float* kv = tv[buf][0];
-    const float* qv = tv[buf][1];
-    const float* ev = tv[buf][2];
-    float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+  KdaTok<RPL> ring[kKdaRing];
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-      const int row = rg + kKdaRG * i;
-      const float e = ev[row];
-      S[i] = make_float4(S[i].x * e, S[i].y * e, S[i].z * e, S[i].w * e);
-      part = fma4s(kv[row], S[i], part);
-    }
-    const float4 kS = kda_colsum(part, lane, warp, red[0]);
-    const float4 vv = *reinterpret_cast<const float4*>(&tvv[buf][cq * 4]);
-    const float bt = tvv[buf][64];
-    const float4 u = make_float4(vv.x - kS.x, vv.y - kS.y, vv.z - kS.z, vv.w - kS.w);
+  for (int i = 0; i < kKdaRing; ++i) ring[i] = load(i);
 
-    // ---- write, then the readout H^T q ----
-    part = make_float4(0.f, 0.f, 0.f, 0.f);
+  // the first token: QDQ at t = 0, its decays and its column sums H^T (e^g o k)
+  float kS[kKdaCols], dec[RPL];
+  if (L > 0) {
+    qdq();
+    float kr[RPL];
+    unpack_rows<RPL>(ring[0].k, kr);
+    float x[8];
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-      const int row = rg + kKdaRG * i;
-      S[i] = fma4s(bt * kv[row], u, S[i]);
-      part = fma4s(qv[row], S[i], part);
+    for (int j = 0; j < 8; ++j) x[j] = 0.f;
+#pragma unroll
+    for (int r = 0; r < RPL; ++r) {
+      dec[r] = expf(ring[0].g[r]);
+      const float kd = dec[r] * kr[r];
+#pragma unroll
+      for (int c = 0; c < kKdaCols; ++c) x[c] = fmaf(kd, H[r][c], x[c]);
     }
-    // the next token's vectors go to the other buffer before the barrier below
-    if (lt + 1 < L) publish(buf ^ 1);
-    const float4 os = kda_colsum(part, lane, warp, red[1]);
-    if (tid < kKdaC4) {
-      const float sc = p.scale;
-      *reinterpret_cast<float4*>(p.o + (t * p.Hv + h) * p.Dv + vb * 64 + cq * 4) =
-          make_float4(sc * os.x, sc * os.y, sc * os.z, sc * os.w);
+    const float s = warp_reduce_scatter<8>(x, lane);
+#pragma unroll
+    for (int c = 0; c < kKdaCols; ++c) kS[c] = __shfl_sync(0xffffffffu, s, c * 4);
+  }
+
+  int left = p.chunk;  // tokens of the current QDQ period not yet written
+  for (int base = 0; base < L; base += kKdaRing) {
+#pragma unroll
+    for (int i = 0; i < kKdaRing; ++i) {
+      const int lt = base + i;
+      if (lt >= L) break;
+      const KdaTok<RPL> cur = ring[i];
+      float kr[RPL], qr[RPL], vv[kKdaCols];
+      unpack_rows<RPL>(cur.k, kr);
+      unpack_rows<RPL>(cur.q, qr);
+      bf16x4(cur.v, vv);
+      // ---- the token's write: H <- diag(e^g) H + beta k (v - (diag(e^g) H)^T k)^T ----
+#pragma unroll
+      for (int c = 0; c < kKdaCols; ++c) {
+        const float u = vv[c] - kS[c];
+#pragma unroll
+        for (int r = 0; r < RPL; ++r) H[r][c] = fmaf(cur.b * kr[r], u, dec[r] * H[r][c]);
+      }
+      // ---- this token's readout, then the next token's column sums ----
+      float x[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) x[j] = 0.f;
+#pragma unroll
+      for (int c = 0; c < kKdaCols; ++c)
+#pragma unroll
+        for (int r = 0; r < RPL; ++r) x[4 + c] = fmaf(qr[r], H[r][c], x[4 + c]);
+      const bool more = lt + 1 < L;
+      if (more && --left == 0) {  // the next token starts a QDQ period
+        qdq();
+        left = p.chunk;
+      }
+      if (more) {
+        const KdaTok<RPL>& nx = ring[(i + 1) % kKdaRing];
+        float nk[RPL];
+        unpack_rows<RPL>(nx.k, nk);
+#pragma unroll
+        for (int r = 0; r < RPL; ++r) {
+          dec[r] = expf(nx.g[r]);
+          const float kd = dec[r] * nk[r];
+#pragma unroll
+          for (int c = 0; c < kKdaCols; ++c) x[c] = fmaf(kd, H[r][c], x[c]);
+        }
+      }
+      const float s = warp_reduce_scatter<8>(x, lane);
+#pragma unroll
+      for (int c = 0; c < kKdaCols; ++c) kS[c] = __shfl_sync(0xffffffffu, s, c * 4);
+      // lanes 16, 20, 24, 28 hold the readouts of the four columns
+      if (lane >= 16 && (lane & 3) == 0)
+        p.o[((tok0 + lt) * p.Hv + h) * p.Dv + c0 + ((lane >> 2) - 4)] = p.scale * s;
+      ring[i] = load(lt + kKdaRing);
     }
   }
 
   if (p.ht) {
 #pragma unroll
-    for (int i = 0; i < RPT; ++i)
-      *reinterpret_cast<float4*>(p.ht + sbase + (int64_t)(rg + kKdaRG * i) * p.Dv) = S[i];
+    for (int r = 0; r < RPL; ++r)
+      *reinterpret_cast<float4*>(p.ht + sbase + (int64_t)r * p.Dv) =
+          make_float4(H[r][0], H[r][1], H[r][2], H[r][3]);
   }
 }
 

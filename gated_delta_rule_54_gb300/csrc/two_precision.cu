@@ -50,41 +50,6 @@ struct TokVec {
   float b, g;
 };
 
-__device__ __forceinline__ void bf16x4(uint2 u, float (&x)[4]) {
-  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
-  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
-  x[0] = a.x;
-  x[1] = a.y;
-  x[2] = b.x;
-  x[3] = b.y;
-}
-
-// Sum over the 32 lanes of each of NV values (NV = 8 or 16) by halving
-// exchanges: at offset o a lane keeps the upper half of its values when its
-// bit o is set.  Returns value j = lane / (32 / NV) summed over all lanes.
-template <int NV>
-__device__ __forceinline__ float warp_reduce_scatter(float (&x)[NV], int lane) {
-  int n = NV;
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    if (n > 1) {
-      const bool up = (lane & o) != 0;
-#pragma unroll
-      for (int i = 0; i < NV / 2; ++i) {
-        if (i < n / 2) {
-          const float send = up ? x[i] : x[i + n / 2];
-          const float keep = up ? x[i + n / 2] : x[i];
-          x[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
-      }
-      n >>= 1;
-    } else {
-      x[0] += __shfl_xor_sync(0xffffffffu, x[0], o);
-    }
-  }
-  return x[0];
-}
-
 template <int RM>
 __global__ void __launch_bounds__(kTpWarps * 32) gdn_two_precision_kernel(const TpParams p) {
   constexpr bool READQ = RM != GDN_QDQ_NONE;
