@@ -135,7 +135,10 @@ const char* gdn_status_string(int s) {
 
 int gdn_abi_version(void) { return GDN_QDQ_ABI_VERSION; }
 
-int gdn_device_error(int reset) { return fwd_device_error(reset != 0); }
+int gdn_device_error(int reset) {
+  const int f = fwd_device_error(reset != 0), b = bwd_device_error(reset != 0);
+  return (f < 0 || b < 0) ? -1 : (f | b);
+}
 
 gdn_status gdn_validate(const gdn_problem* p) { return validate(p); }
 

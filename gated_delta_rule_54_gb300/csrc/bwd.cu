@@ -37,6 +37,7 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 
 struct BwdParams {
+  CUtensorMap tm_k, tm_q, tm_do, tm_wc;  // the scan's per-chunk operands (TMA)
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
@@ -69,6 +70,9 @@ struct BwdParams {
   int64_t nt_fixed;
   float scale;
 };
+
+// set when a bounded wait for a TMA transfer gave up (the call's results are invalid)
+__device__ int g_bwd_device_error;
 
 struct SeqInfo {
   int64_t tok0, slot0;
@@ -132,41 +136,51 @@ struct ScanSmem {
   static constexpr int EDO = WV + kTileK;                // e^gamma dO bf16
   static constexpr int DD = EDO + kTile64;               // dDelta bf16
   static constexpr int DH = DD + kTile64;                // dH bf16 [DK][64]
-  static constexpr int BYTES = DH + DK * 64 * 2;
+  static constexpr int BYTES = DH + DK * 64 * 2 + 1024;  // + alignment slack
+  static_assert((Q % 1024) == 0 && (DO % 1024) == 0 && (WU8 % 128) == 0 && (CV % 16) == 0,
+                "TMA destinations");
   static_assert(BYTES <= 232448, "shared memory budget");
 };
 
 template <int DK, int WM>
+constexpr uint32_t scan_tx_bytes() {
+  return 2 * kChunk * DK * 2 + kChunk * 64 * 2 + kTileImgBytes + kCvecFloats * 4 +
+         (WM != GDN_QDQ_NONE ? kChunk * DK : 0);
+}
+
+// One chunk's operands into buffer `buf` by TMA and bulk copies on `bar`
+// (issued by thread 0): K, Q, dO boxes of 64 rows (rows past the chunk end
+// hold the next tokens or zeros; the scan zeroes their contributions), the
+// forward's P image and chunk vectors, the W codes.
+template <int DK, int WM>
 __device__ __forceinline__ void scan_load(const BwdParams& p, unsigned char* sm, int buf,
-                                          int64_t ctok, int Lc, int hk, int h, int vb,
+                                          uint64_t* bar, int64_t ctok, int hk, int h, int vb,
                                           int64_t slot) {
   using S = ScanSmem<DK, WM>;
-  load_rows_bf16<DK>(reinterpret_cast<__nv_bfloat16*>(sm + S::K + buf * S::kTileK),
-                     p.k + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
-  load_rows_bf16<DK>(reinterpret_cast<__nv_bfloat16*>(sm + S::Q + buf * S::kTileK),
-                     p.q + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
-  load_rows_bf16<64>(reinterpret_cast<__nv_bfloat16*>(sm + S::DO + buf * S::kTile64),
-                     p.dO + (ctok * p.Hv + h) * p.Dv + vb * 64, (int64_t)p.Hv * p.Dv, Lc);
-  load_block(sm + S::PB + buf * S::kTile64, p.pb + (slot * p.Hv + h) * (kTileImgBytes / 2),
-             kTileImgBytes);
-  load_block(sm + S::CV + buf * kCvecFloats * 4, p.cvec + (slot * p.Hv + h) * kCvecFloats,
-             kCvecFloats * 4);
-  if constexpr (WM != GDN_QDQ_NONE) {
-    uint8_t* wu = sm + S::WU8 + buf * kChunk * DK;
-    constexpr int CPR = DK / 16;
-    for (int i = threadIdx.x; i < kChunk * CPR; i += kThreads) {
-      const int r = i / CPR, c = i % CPR;
-      const bool ok = r < Lc;
-      cp_async16(smem_u32(wu + r * DK + c * 16),
-                 p.w_codes + ((ctok + (ok ? r : 0)) * p.Hv + h) * DK + c * 16, ok ? 16 : 0);
-    }
+  if (threadIdx.x != 0) return;
+  mbar_expect_tx(bar, scan_tx_bytes<DK, WM>());
+  __nv_bfloat16* Kd = reinterpret_cast<__nv_bfloat16*>(sm + S::K + buf * S::kTileK);
+  __nv_bfloat16* Qd = reinterpret_cast<__nv_bfloat16*>(sm + S::Q + buf * S::kTileK);
+#pragma unroll
+  for (int pn = 0; pn < DK / 64; ++pn) {
+    tma_load_2d(Kd + pn * kChunk * 64, &p.tm_k, hk * DK + pn * 64, (int)ctok, bar);
+    tma_load_2d(Qd + pn * kChunk * 64, &p.tm_q, hk * DK + pn * 64, (int)ctok, bar);
   }
+  tma_load_2d(sm + S::DO + buf * S::kTile64, &p.tm_do, h * p.Dv + vb * 64, (int)ctok, bar);
+  bulk_load_1d(sm + S::PB + buf * S::kTile64, p.pb + (slot * p.Hv + h) * (kTileImgBytes / 2),
+               kTileImgBytes, bar);
+  bulk_load_1d(sm + S::CV + buf * kCvecFloats * 4, p.cvec + (slot * p.Hv + h) * kCvecFloats,
+               kCvecFloats * 4, bar);
+  if constexpr (WM != GDN_QDQ_NONE)
+    tma_load_2d(sm + S::WU8 + buf * kChunk * DK, &p.tm_wc, h * DK, (int)ctok, bar);
 }
 
 template <int DK, int WM>
-__global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const __grid_constant__ BwdParams p) {
   using S = ScanSmem<DK, WM>;
-  extern __shared__ __align__(1024) unsigned char sm[];
+  extern __shared__ __align__(1024) unsigned char sm_raw[];
+  unsigned char* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
+  __shared__ __align__(8) uint64_t bars[2];
   const int vb = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
   const int hk = h / p.G;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -198,18 +212,18 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const BwdPara
       }
   }
 
-  if (nch > 0) {
-    const int c = nch - 1;
-    scan_load<DK, WM>(p, sm, 0, si.tok0 + (int64_t)c * kChunk, si.L - c * kChunk, hk, h, vb,
-                      si.slot0 + c);
+  if (threadIdx.x == 0) {
+    mbar_init(&bars[0], 1);
+    mbar_init(&bars[1], 1);
+    fence_mbar_init();
   }
-  cp_async_commit();
-  if (nch > 1) {
-    const int c = nch - 2;
-    scan_load<DK, WM>(p, sm, 1, si.tok0 + (int64_t)c * kChunk, min(si.L - c * kChunk, kChunk), hk,
-                      h, vb, si.slot0 + c);
-  }
-  cp_async_commit();
+  __syncthreads();
+  if (nch > 0)
+    scan_load<DK, WM>(p, sm, 0, &bars[0], si.tok0 + (int64_t)(nch - 1) * kChunk, hk, h, vb,
+                      si.slot0 + nch - 1);
+  if (nch > 1)
+    scan_load<DK, WM>(p, sm, 1, &bars[1], si.tok0 + (int64_t)(nch - 2) * kChunk, hk, h, vb,
+                      si.slot0 + nch - 2);
 
   const int rt = warp & 3, cq = warp >> 2;
   const int row0 = rt * 16, col0 = cq * 16;
@@ -225,8 +239,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const BwdPara
     const float* eg = cv + kCvEg;
     const float* dec = cv + kCvDec;
     const int Lc = min(si.L - c * kChunk, kChunk);
-    cp_async_wait<1>();
-    __syncthreads();
+    const bool ok = mbar_wait(&bars[buf], (uint32_t)(it >> 1) & 1u);
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) {
+        atomicOr(&g_bwd_device_error, 1);
+        mbar_wait(&bars[buf], (uint32_t)(it >> 1) & 1u);  // once more, bounded, for the copies in flight
+      }
+      return;
+    }
 
     // current dH (gradient w.r.t. the state after this chunk) -> bf16 tile
 #pragma unroll
@@ -269,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const BwdPara
     for (int e = threadIdx.x; e < kChunk * 32; e += kThreads) {
       const int r = e >> 5, col = (e & 31) * 2;
       const __nv_bfloat162 v2 = *reinterpret_cast<const __nv_bfloat162*>(dOs + swz<64>(r, col));
-      const float er = eg[r];
+      const float er = r < Lc ? eg[r] : 0.f;  // rows past the chunk end contribute nothing
       st_bf16x2(EdO + swz<64>(r, col), er * __bfloat162float(v2.x), er * __bfloat162float(v2.y));
     }
     __syncthreads();
@@ -286,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const BwdPara
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-          const float di = dec[i];
+          const float di = i < Lc ? dec[i] : 0.f;  // rows past the chunk end are zero
           st_bf16x2(dDb + swz<64>(i, j), p.scale * a1[nt][2 * e2] + di * a2[nt][2 * e2],
                     p.scale * a1[nt][2 * e2 + 1] + di * a2[nt][2 * e2 + 1]);
         }
@@ -307,15 +327,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const BwdPara
         for (int e = 0; e < 4; ++e)
           dH[nt][e] = p.scale * a1[nt][e] + egL * dH[nt][e] - sW * a2[nt][e];
     }
-    __syncthreads();
-    if (it + 2 < nch) {
-      const int c2 = c - 2;
-      scan_load<DK, WM>(p, sm, buf, si.tok0 + (int64_t)c2 * kChunk, kChunk, hk, h, vb,
-                        si.slot0 + c2);
-    }
-    cp_async_commit();
+    __syncthreads();  // buffer buf is no longer read
+    if (it + 2 < nch)
+      scan_load<DK, WM>(p, sm, buf, &bars[buf], si.tok0 + (int64_t)(c - 2) * kChunk, hk, h, vb,
+                        si.slot0 + c - 2);
   }
-  cp_async_wait<0>();
   if (p.dh0) {
     float* dst = p.dh0 + (((int64_t)n * p.Hv + h) * DK) * p.Dv + vb * 64;
 #pragma unroll
@@ -424,7 +440,7 @@ __device__ __forceinline__ void racc_add_rows(float* racc, int slot, int row0, i
 // chip; T^T dW, Gm K, Gm^T Q, X = T^T dT, dA and dKK run once; every output
 // element has one writer.
 template <int DK, int SM, int WM>
-__global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const BwdParams p) {
+__global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid_constant__ BwdParams p) {
   using S = ChunkSmem<DK>;
   extern __shared__ __align__(1024) unsigned char sm[];
   const int64_t slot = blockIdx.x;
@@ -1065,6 +1081,16 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 }  // namespace
 
+int bwd_device_error(bool reset) {
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_bwd_device_error, sizeof(int)) != cudaSuccess) return -1;
+  if (reset && v) {
+    const int z = 0;
+    if (cudaMemcpyToSymbol(g_bwd_device_error, &z, sizeof(int)) != cudaSuccess) return -1;
+  }
+  return v;
+}
+
 size_t bwd_workspace_bytes(const gdn_problem& p, const Dims& d) {
   size_t b = align256((size_t)d.n_slots * d.Hv * d.Dk * d.Dv * 2);
   if (d.Hv != d.Hk) b += align256((size_t)2 * d.B * d.T * d.Hv * d.Dk * 4);
@@ -1123,6 +1149,22 @@ gdn_status launch_bwd(const gdn_problem& p, const Dims& d, const void* q, const 
   prm.block_v = p.block_v;
   prm.bv_log2 = p.block_v == 16 ? 4 : (p.block_v == 32 ? 5 : (p.block_v == 64 ? 6 : 7));
   prm.neumann = p.solve == GDN_SOLVE_NEUMANN ? p.solve_degree : -1;
+  const uint64_t tok = (uint64_t)(d.B * d.T);
+  if (tok > 0) {
+    // TMA row coordinates are 32-bit
+    if (tok > 0x7fffffffULL) return GDN_ERR_UNSUPPORTED_SHAPE;
+    const int DK = d.Dk;
+    bool ok = make_map(&prm.tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, k, (uint64_t)d.Hk * DK, tok,
+                       (uint64_t)d.Hk * DK * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              make_map(&prm.tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, q, (uint64_t)d.Hk * DK, tok,
+                       (uint64_t)d.Hk * DK * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B) &&
+              make_map(&prm.tm_do, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dO, (uint64_t)d.Hv * d.Dv, tok,
+                       (uint64_t)d.Hv * d.Dv * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (ok && p.w_mode != GDN_QDQ_NONE)
+      ok = make_map(&prm.tm_wc, CU_TENSOR_MAP_DATA_TYPE_UINT8, prm.w_codes, (uint64_t)d.Hv * DK, tok,
+                    (uint64_t)d.Hv * DK, DK, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (!ok) return GDN_ERR_CUDA;
+  }
   if (d.Dk == 128) return dispatch_bwd<128>(p, prm, d, st);
   return dispatch_bwd<64>(p, prm, d, st);
 }

@@ -1231,6 +1231,8 @@ gdn_status dispatch_modes(const gdn_problem& p, const FwdParams& prm, const Dims
   return GDN_ERR_UNSUPPORTED_MODE;
 }
 
+}  // namespace
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -1260,8 +1262,6 @@ bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t
             CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 int fwd_device_error(bool reset) {
   int v = 0;

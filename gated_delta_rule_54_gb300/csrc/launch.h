@@ -1,6 +1,7 @@
 // Internal launchers behind the C ABI (host side; arguments already validated).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -40,9 +41,16 @@ gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const 
                       const void* v, const float* beta, const float* g, const float* h0,
                       float* o, float* ht, void* ctx, cudaStream_t st);
 
-// nonzero if a forward kernel's bounded wait for a TMA transfer gave up
-// (cleared when reset); -1 if the flag could not be read
+// nonzero if a forward (backward) kernel's bounded wait for a TMA transfer
+// gave up (cleared when reset); -1 if the flag could not be read
 int fwd_device_error(bool reset);
+int bwd_device_error(bool reset);
+
+// 2-D row-major TMA map: `cols` elements per row (contiguous), `rows` rows of
+// `row_bytes` bytes; boxes of box_cols x box_rows elements; false on failure
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t cols,
+              uint64_t rows, uint64_t row_bytes, uint32_t box_cols, uint32_t box_rows,
+              CUtensorMapSwizzle sw);
 
 gdn_status launch_kda(const gdn_problem& p, const Dims& d, const void* q, const void* k,
                       const void* v, const float* beta, const float* g, const float* h0,
