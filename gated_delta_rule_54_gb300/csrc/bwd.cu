@@ -655,11 +655,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
     __syncthreads();
 
     // ---- output-side products of this block ----
+    // dO Delta^T (for dP) and dO H^T (for dQ_inter) share their dO fragments
+    float dp[2][4], ohq[NTW][4];
+    zero_acc(dp);
+    zero_acc(ohq);
+    static_assert(NTW == 2 || NTW == 4, "warp tile");
+    wgemm_shared_a<2, NTW, false, false, false, 64, 64, 64>(dp, ohq, dOs, row0, Db, col0, Hh, wcol0,
+                                                            0, 64, lane);
     {
       // dP = lower-incl(scale dO Delta^T); Gm += dP Gamma; PP = dP P
-      float dp[2][4];
-      zero_acc(dp);
-      wgemm<2, false, false, 64, 64>(dp, dOs, row0, Db, col0, 0, 64, lane);
       float pp[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
@@ -689,9 +693,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
     }
     {
       // dQ_inter = scale e^gamma (dO H^T); row sums of q * dQ_inter
-      float acc[NTW][4];
-      zero_acc(acc);
-      wgemm<NTW, false, false, 64, 64>(acc, dOs, wrow0, Hh, wcol0, 0, 64, lane);
+      const float (&acc)[NTW][4] = ohq;
       float qd[NTW][4];
 #pragma unroll
       for (int nt = 0; nt < NTW; ++nt)
@@ -733,11 +735,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
       row_sums<NTW>(kd, r0, r1);
       racc_add_rows(racc, R_TT + ch, wrow0, gq, tq, r0, r1);
     }
-    // dW += -dDelta H^T (STE: = dW^)
-    wgemm<NTW, false, false, 64, 64>(dWa, dDb, wrow0, Hh, wcol0, 0, 64, lane);
+    // dW += -dDelta H^T (STE: = dW^) and the dT part dDelta V^T (summed over the
+    // blocks) share their dDelta fragments
+    wgemm_shared_a<NTW, 2, false, false, false, 64, 64, 64>(dWa, dta, dDb, wrow0, Hh, wcol0, Vs,
+                                                            col0, 0, 64, lane);
     {
-      // dT part (dDelta V^T), summed over the blocks; T^T dDelta -> dV and its row sums
-      wgemm<2, false, false, 64, 64>(dta, dDb, row0, Vs, col0, 0, 64, lane);
+      // T^T dDelta -> dV and its row sums
       float tu[2][4];
       zero_acc(tu);
       wgemm<2, true, true, 64, 64>(tu, Tb, row0, dDb, col0, 0, 64, lane);

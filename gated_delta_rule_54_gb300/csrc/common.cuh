@@ -418,6 +418,52 @@ __device__ __forceinline__ void wgemm(float (&acc)[NT][4], const __nv_bfloat16* 
   }
 }
 
+// Two warp-tile GEMMs that share their A fragments (same A tile, rows m0..,
+// k range): acc1 += A * B1[.., n1 : n1 + 8 NT1], acc2 += A * B2[.., n2 : n2 + 8 NT2].
+// One A ldmatrix per k step serves both, easing the shared-memory pipe.
+template <int NT1, int NT2, bool AT, bool BKN1, bool BKN2, int RLA, int RLB1, int RLB2,
+          int UNROLL = kWgemmUnroll>
+__device__ __forceinline__ void wgemm_shared_a(float (&acc1)[NT1][4], float (&acc2)[NT2][4],
+                                               const __nv_bfloat16* A, int m0,
+                                               const __nv_bfloat16* B1, int n1,
+                                               const __nv_bfloat16* B2, int n2, int k0, int k1,
+                                               int lane) {
+  static_assert(NT1 % 2 == 0 && NT2 % 2 == 0, "n tiles come in pairs");
+  auto step = [&](int k) {
+    uint32_t a[4];
+    if constexpr (AT)
+      ldsm_x4_t(a, at_frag_addr<RLA>(A, m0, k, lane));
+    else
+      ldsm_x4(a, a_frag_addr<RLA>(A, m0, k, lane));
+#pragma unroll
+    for (int np = 0; np < NT1 / 2; ++np) {
+      uint32_t b[4];
+      if constexpr (BKN1)
+        ldsm_x4_t(b, bkn_frag_addr<RLB1>(B1, k, n1 + 16 * np, lane));
+      else
+        ldsm_x4(b, bnk_frag_addr<RLB1>(B1, n1 + 16 * np, k, lane));
+      mma_bf16(acc1[2 * np], a, b[0], b[1]);
+      mma_bf16(acc1[2 * np + 1], a, b[2], b[3]);
+    }
+#pragma unroll
+    for (int np = 0; np < NT2 / 2; ++np) {
+      uint32_t b[4];
+      if constexpr (BKN2)
+        ldsm_x4_t(b, bkn_frag_addr<RLB2>(B2, k, n2 + 16 * np, lane));
+      else
+        ldsm_x4(b, bnk_frag_addr<RLB2>(B2, n2 + 16 * np, k, lane));
+      mma_bf16(acc2[2 * np], a, b[0], b[1]);
+      mma_bf16(acc2[2 * np + 1], a, b[2], b[3]);
+    }
+  };
+  if constexpr (UNROLL == 2) {
+#pragma unroll 2
+    for (int k = k0; k < k1; k += 16) step(k);
+  } else {
+    for (int k = k0; k < k1; k += 16) step(k);
+  }
+}
+
 template <int NT>
 __device__ __forceinline__ void zero_acc(float (&acc)[NT][4]) {
 #pragma unroll
