@@ -464,6 +464,89 @@ __device__ __forceinline__ void wgemm_shared_a(float (&acc1)[NT1][4], float (&ac
   }
 }
 
+// Two warp-tile GEMMs that share their B fragments (same B tile, columns
+// n0.., k range) and read A1, A2 (same layout, rows m0..):
+// acc1 += A1 * B, acc2 += A2 * B.  acc1 and acc2 may be the same array (the
+// hi and lo halves of a split A into one accumulator).
+template <int NT, bool AT, bool BKN, int RLA, int RLB, int UNROLL = kWgemmUnroll>
+__device__ __forceinline__ void wgemm_shared_b(float (&acc1)[NT][4], float (&acc2)[NT][4],
+                                               const __nv_bfloat16* A1, const __nv_bfloat16* A2,
+                                               int m0, const __nv_bfloat16* B, int n0, int k0,
+                                               int k1, int lane) {
+  static_assert(NT % 2 == 0, "n tiles come in pairs");
+  auto step = [&](int k) {
+    uint32_t a1[4], a2[4];
+    if constexpr (AT) {
+      ldsm_x4_t(a1, at_frag_addr<RLA>(A1, m0, k, lane));
+      ldsm_x4_t(a2, at_frag_addr<RLA>(A2, m0, k, lane));
+    } else {
+      ldsm_x4(a1, a_frag_addr<RLA>(A1, m0, k, lane));
+      ldsm_x4(a2, a_frag_addr<RLA>(A2, m0, k, lane));
+    }
+#pragma unroll
+    for (int np = 0; np < NT / 2; ++np) {
+      uint32_t b[4];
+      if constexpr (BKN)
+        ldsm_x4_t(b, bkn_frag_addr<RLB>(B, k, n0 + 16 * np, lane));
+      else
+        ldsm_x4(b, bnk_frag_addr<RLB>(B, n0 + 16 * np, k, lane));
+      mma_bf16(acc1[2 * np], a1, b[0], b[1]);
+      mma_bf16(acc1[2 * np + 1], a1, b[2], b[3]);
+      mma_bf16(acc2[2 * np], a2, b[0], b[1]);
+      mma_bf16(acc2[2 * np + 1], a2, b[2], b[3]);
+    }
+  };
+  if constexpr (UNROLL == 2) {
+#pragma unroll 2
+    for (int k = k0; k < k1; k += 16) step(k);
+  } else {
+    for (int k = k0; k < k1; k += 16) step(k);
+  }
+}
+
+// acc += Ah Bh + Ah Bl + Al Bh: the product of two hi + lo split operands to
+// ~16 mantissa bits, each fragment loaded once per k step.
+template <int NT, bool AT, bool BKN, int RLA, int RLB, int UNROLL = kWgemmUnroll>
+__device__ __forceinline__ void wgemm_split3(float (&acc)[NT][4], const __nv_bfloat16* Ah,
+                                             const __nv_bfloat16* Al, int m0,
+                                             const __nv_bfloat16* Bh, const __nv_bfloat16* Bl,
+                                             int n0, int k0, int k1, int lane) {
+  static_assert(NT % 2 == 0, "n tiles come in pairs");
+  auto step = [&](int k) {
+    uint32_t ah[4], al[4];
+    if constexpr (AT) {
+      ldsm_x4_t(ah, at_frag_addr<RLA>(Ah, m0, k, lane));
+      ldsm_x4_t(al, at_frag_addr<RLA>(Al, m0, k, lane));
+    } else {
+      ldsm_x4(ah, a_frag_addr<RLA>(Ah, m0, k, lane));
+      ldsm_x4(al, a_frag_addr<RLA>(Al, m0, k, lane));
+    }
+#pragma unroll
+    for (int np = 0; np < NT / 2; ++np) {
+      uint32_t bh[4], bl[4];
+      if constexpr (BKN) {
+        ldsm_x4_t(bh, bkn_frag_addr<RLB>(Bh, k, n0 + 16 * np, lane));
+        ldsm_x4_t(bl, bkn_frag_addr<RLB>(Bl, k, n0 + 16 * np, lane));
+      } else {
+        ldsm_x4(bh, bnk_frag_addr<RLB>(Bh, n0 + 16 * np, k, lane));
+        ldsm_x4(bl, bnk_frag_addr<RLB>(Bl, n0 + 16 * np, k, lane));
+      }
+      mma_bf16(acc[2 * np], ah, bh[0], bh[1]);
+      mma_bf16(acc[2 * np + 1], ah, bh[2], bh[3]);
+      mma_bf16(acc[2 * np], ah, bl[0], bl[1]);
+      mma_bf16(acc[2 * np + 1], ah, bl[2], bl[3]);
+      mma_bf16(acc[2 * np], al, bh[0], bh[1]);
+      mma_bf16(acc[2 * np + 1], al, bh[2], bh[3]);
+    }
+  };
+  if constexpr (UNROLL == 2) {
+#pragma unroll 2
+    for (int k = k0; k < k1; k += 16) step(k);
+  } else {
+    for (int k = k0; k < k1; k += 16) step(k);
+  }
+}
+
 template <int NT>
 __device__ __forceinline__ void zero_acc(float (&acc)[NT][4]) {
 #pragma unroll

@@ -378,8 +378,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __g
   const int wc0 = ch * (DK / 2);
   float wacc[NTW][4];
   zero_acc(wacc);
-  wgemm<NTW, false, true, 64, DK>(wacc, TwH, row0, Ks, wc0, 0, 64, lane);
-  wgemm<NTW, false, true, 64, DK>(wacc, TwL, row0, Ks, wc0, 0, 64, lane);
+  wgemm_shared_b<NTW, false, true, 64, DK>(wacc, wacc, TwH, TwL, row0, Ks, wc0, 0, 64, lane);
 
   // ---- a5: W QDQ over the whole [L, DK] tile ----
   if constexpr (WM != GDN_QDQ_NONE) {
@@ -445,8 +444,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __g
     float uacc[4][4];
     zero_acc(uacc);
     const __nv_bfloat16* Vb = Vs + vb * kChunk * 64;
-    wgemm<4, false, true, 64, 64>(uacc, TuH, row0, Vb, col0, 0, 64, lane);
-    wgemm<4, false, true, 64, 64>(uacc, TuL, row0, Vb, col0, 0, 64, lane);
+    wgemm_shared_b<4, false, true, 64, 64>(uacc, uacc, TuH, TuL, row0, Vb, col0, 0, 64, lane);
     if (vb > 0 && threadIdx.x == 0) tma_store_wait_read();  // previous block's U has left
     __syncthreads();
 #pragma unroll
@@ -880,8 +878,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
 #pragma unroll
         for (int e = 0; e < 4; ++e) hreg[nt][e] *= egL;
       const __nv_bfloat16* Ks = Kbuf(buf);
-      wgemm<NTH, true, true, DK, 64>(hreg, Ks, h_row0, DpH, h_col0, 0, 64, lane);
-      wgemm<NTH, true, true, DK, 64>(hreg, Ks, h_row0, DpL, h_col0, 0, 64, lane);
+      wgemm_shared_a<NTH, NTH, true, true, true, DK, 64, 64>(hreg, hreg, Ks, h_row0, DpH, h_col0, DpL,
+                                                              h_col0, 0, 64, lane);
       tile_partials();
     }
   }
@@ -1070,11 +1068,16 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
   zero_acc(dacc);
   zero_acc(qacc);
   if (p_tile) wgemm<4, false, false, DK, DK>(pacc, Qs, row0, Ks, col0, 0, DK, lane);
-  wgemm<4, false, true, DK, 64>(dacc, WcH, row0, HcH, col0, 0, DK, lane);
-  if constexpr (WM == GDN_QDQ_NONE) wgemm<4, false, true, DK, 64>(dacc, WcL, row0, HcH, col0, 0, DK, lane);
-  if constexpr (SM == GDN_QDQ_NONE) wgemm<4, false, true, DK, 64>(dacc, WcH, row0, HcL, col0, 0, DK, lane);
-  wgemm<4, false, true, DK, 64>(qacc, Qs, row0, HcH, col0, 0, DK, lane);
-  if constexpr (SM == GDN_QDQ_NONE) wgemm<4, false, true, DK, 64>(qacc, Qs, row0, HcL, col0, 0, DK, lane);
+  if constexpr (WM != GDN_QDQ_NONE && SM != GDN_QDQ_NONE) {
+    // W^ H^ and Q H^ share their H^ fragments
+    wgemm_shared_b<4, false, true, DK, 64>(dacc, qacc, WcH, Qs, row0, HcH, col0, 0, DK, lane);
+  } else {
+    wgemm<4, false, true, DK, 64>(dacc, WcH, row0, HcH, col0, 0, DK, lane);
+    if constexpr (WM == GDN_QDQ_NONE) wgemm<4, false, true, DK, 64>(dacc, WcL, row0, HcH, col0, 0, DK, lane);
+    if constexpr (SM == GDN_QDQ_NONE) wgemm<4, false, true, DK, 64>(dacc, WcH, row0, HcL, col0, 0, DK, lane);
+    wgemm<4, false, true, DK, 64>(qacc, Qs, row0, HcH, col0, 0, DK, lane);
+    if constexpr (SM == GDN_QDQ_NONE) wgemm<4, false, true, DK, 64>(qacc, Qs, row0, HcL, col0, 0, DK, lane);
+  }
   __syncthreads();  // K reads done (its tile becomes Delta)
 
   // value block 0 also saves P (bf16; rows >= L zero) as the backward's tile image
@@ -1112,9 +1115,7 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
     float o2[4][4];
     zero_acc(o2);
     const int kend = row0 + 16;  // P is lower triangular: columns j <= i only
-    wgemm<4, false, true, 64, 64>(o2, PH, row0, DH, col0, 0, kend, lane);
-    wgemm<4, false, true, 64, 64>(o2, PH, row0, DL, col0, 0, kend, lane);
-    wgemm<4, false, true, 64, 64>(o2, PL, row0, DH, col0, 0, kend, lane);
+    wgemm_split3<4, false, true, 64, 64>(o2, PH, PL, row0, DH, DL, col0, 0, kend, lane);
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
