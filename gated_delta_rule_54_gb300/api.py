@@ -313,6 +313,9 @@ def split_ctx(ctx: torch.Tensor, p: GdnProblem):
         n = ns * Hv * 64 * 64
         out[name] = ctx[off:off + 2 * n].view(torch.bfloat16).view(ns, Hv, 64 * 64)
         off = al(off + 2 * n)
+    n = ns * Hv * (Dv // 64) * 64 * 64               # Delta of each value block, same images
+    out["d_img"] = ctx[off:off + 2 * n].view(torch.bfloat16).view(ns, Hv, Dv // 64, 64 * 64)
+    off = al(off + 2 * n)
     if p.state_mode != 0:
         n = ns * Hv * Dk * Dv
         out["h_codes"] = ctx[off:off + n].view(ns, Hv, Dk, Dv)

@@ -48,6 +48,8 @@ CtxLayout ctx_layout(const gdn_problem& p) {
   off = align256(off + (size_t)d.n_slots * d.Hv * kTileImgBytes);
   L.pb = off;
   off = align256(off + (size_t)d.n_slots * d.Hv * kTileImgBytes);
+  L.db = off;
+  off = align256(off + (size_t)d.n_slots * d.Hv * (d.Dv / 64) * kTileImgBytes);
   const size_t per_slot = (size_t)d.n_slots * d.Hv * d.Dk * d.Dv;
   if (p.state_mode != GDN_QDQ_NONE) {
     L.h_codes = off;

@@ -53,6 +53,7 @@ struct BwdParams {
   const float* w_full;                          // fp32 W (W site off)
   const float* cvec;                            // [n_slots, Hv, kCvecFloats] chunk vectors
   const __nv_bfloat16 *tb, *gkk, *pb;           // [n_slots, Hv] tile images of T, Gamma o KK^T, P
+  const __nv_bfloat16* db;                      // [n_slots, Hv, Dv / 64] tile images of Delta
   float* dq;
   float* dk;
   float* dv;
@@ -358,21 +359,21 @@ struct ChunkSmem {
   static constexpr int V = Q + kTileK;             // 2 x [64][64] (value blocks 0, 1)
   static constexpr int DO = V + 2 * kTile64;       // 2 x [64][64]
   static constexpr int DHP = DO + 2 * kTile64;     // 2 x dH' bf16 [DK][64]; later dKK
-  static constexpr int WV = DHP + 2 * DK * 64 * 2; // W^ values bf16 [64][DK]; later dW
+  static constexpr int WV = DHP + 2 * DK * 64 * 2; // dW bf16 [64][DK] (after the value blocks)
   static constexpr int HH = WV + kTileK;           // H^ values of one block [DK][64]; later dT
   static constexpr int GKK = HH + DK * 64 * 2;     // bf16 Gamma KK (strict lower; forward's image)
   static constexpr int PB = GKK + kTile64;         // bf16 P (forward's image); later X
   static constexpr int TB = PB + kTile64;          // bf16 T (forward's image)
-  static constexpr int TU = TB + kTile64;          // bf16 T diag(beta); later Gm
-  static constexpr int DB = TU + kTile64;          // bf16 Delta; W codes before that
-  static constexpr int DDB = DB + kTile64;         // bf16 dDelta; block-0 state codes before that
+  static constexpr int TU = TB + kTile64;          // Gm (after the value blocks)
+  static constexpr int DB = TU + kTile64;          // 2 x bf16 Delta of the value blocks (forward's images)
+  static constexpr int DDB = DB + 2 * kTile64;     // bf16 dDelta; block-0 state codes before that
   static constexpr int HC1 = DDB + kTile64;        // u8 [DK][64] block-1 state codes
   static constexpr int VEC = HC1 + DK * 64;        // chunk vectors (forward)
   static constexpr int RACC = VEC + kCvecFloats * 4;  // per-row partial sums [kSlots][64] + scalars
   static constexpr int kSlots = 36;
   static constexpr int BYTES = RACC + kSlots * 256 + 4 * (kWarps + 2);
   static_assert(BYTES <= 232448, "shared memory budget");
-  static_assert(kChunk * DK <= kTile64 && DK * 64 <= kTile64, "code staging fits in Delta, dDelta");
+  static_assert(DK * 64 <= kTile64, "block-0 state codes fit in dDelta");
   static_assert(DK * 64 * 2 >= kTile64, "dT fits in the H^ tile");
 };
 
@@ -472,8 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
 
   __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(sm + S::K);
   __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(sm + S::Q);
-  __nv_bfloat16* Wv = reinterpret_cast<__nv_bfloat16*>(sm + S::WV);
-  __nv_bfloat16* dWb = Wv;                 // after the value blocks
+  __nv_bfloat16* dWb = reinterpret_cast<__nv_bfloat16*>(sm + S::WV);
   __nv_bfloat16* Hh = reinterpret_cast<__nv_bfloat16*>(sm + S::HH);
   __nv_bfloat16* dTb = Hh;                 // after the value blocks
   __nv_bfloat16* dKKb = reinterpret_cast<__nv_bfloat16*>(sm + S::DHP);  // after the value blocks
@@ -481,11 +481,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
   __nv_bfloat16* Pb = reinterpret_cast<__nv_bfloat16*>(sm + S::PB);
   __nv_bfloat16* Xb = Pb;                  // after the value blocks
   __nv_bfloat16* Tb = reinterpret_cast<__nv_bfloat16*>(sm + S::TB);
-  __nv_bfloat16* Tub = reinterpret_cast<__nv_bfloat16*>(sm + S::TU);
-  __nv_bfloat16* Gmb = Tub;                // after the value blocks
-  __nv_bfloat16* Db = reinterpret_cast<__nv_bfloat16*>(sm + S::DB);
+  __nv_bfloat16* Gmb = reinterpret_cast<__nv_bfloat16*>(sm + S::TU);
+  auto DbOf = [&](int b) { return reinterpret_cast<__nv_bfloat16*>(sm + S::DB + b * S::kTile64); };
+  __nv_bfloat16* Db = DbOf(0);             // the Neumann scratch after the value blocks
   __nv_bfloat16* dDb = reinterpret_cast<__nv_bfloat16*>(sm + S::DDB);
-  uint8_t* wst = reinterpret_cast<uint8_t*>(sm + S::DB);   // W codes [64][DK], until Delta
   auto Vb = [&](int b) { return reinterpret_cast<__nv_bfloat16*>(sm + S::V + b * S::kTile64); };
   auto dOb = [&](int b) { return reinterpret_cast<__nv_bfloat16*>(sm + S::DO + b * S::kTile64); };
   auto dHpb = [&](int b) { return reinterpret_cast<__nv_bfloat16*>(sm + S::DHP + b * DK * 64 * 2); };
@@ -499,9 +498,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
   float* racc = reinterpret_cast<float*>(sm + S::RACC);
   float* hd_part = racc + S::kSlots * 64;  // [kWarps] <H^, dH'> partials, then [2] sums of t_i
 
-  // ---- loads.  Group A feeds the W / block-0 dequantization, group B the
-  //      block-0 products, group C is block 1; T, Gamma o KK^T, P and the
-  //      chunk vectors come from the forward ----
+  // ---- loads.  Group A feeds the block-0 dequantization, group B the
+  //      block-0 products, group C is block 1; T, Gamma o KK^T, P, each
+  //      block's Delta and the chunk vectors come from the forward ----
   auto load_block_vb = [&](int b) {
     const __nv_bfloat16* src = p.ws_dh + ((slot * p.Hv + h) * DK) * p.Dv + b * 64;
     __nv_bfloat16* dst = dHpb(b);
@@ -521,20 +520,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
   auto load_vo = [&](int b) {
     load_rows_bf16<64>(Vb(b), p.v + (ctok * p.Hv + h) * p.Dv + b * 64, (int64_t)p.Hv * p.Dv, Lc);
     load_rows_bf16<64>(dOb(b), p.dO + (ctok * p.Hv + h) * p.Dv + b * 64, (int64_t)p.Hv * p.Dv, Lc);
+    load_block(DbOf(b), p.db + ((slot * p.Hv + h) * nvb + b) * (kTileImgBytes / 2), kTileImgBytes);
   };
   {
     const int64_t img = (slot * p.Hv + h) * (kTileImgBytes / 2);
     load_block(sm + S::VEC, p.cvec + (slot * p.Hv + h) * kCvecFloats, kCvecFloats * 4);
     load_block(Tb, p.tb + img, kTileImgBytes);
-    if constexpr (WM != GDN_QDQ_NONE) {
-      constexpr int CPR = DK / 16;
-      for (int i = threadIdx.x; i < kChunk * CPR; i += kThreads) {
-        const int r = i / CPR, cc = i % CPR;
-        const bool ok = r < Lc;
-        cp_async16(smem_u32(wst + r * DK + cc * 16),
-                   p.w_codes + ((ctok + (ok ? r : 0)) * p.Hv + h) * DK + cc * 16, ok ? 16 : 0);
-      }
-    }
     load_block_vb(0);
     cp_async_commit();  // group A
     load_rows_bf16<DK>(Ks, p.k + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
@@ -553,32 +544,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
   cp_async_wait<2>();
   __syncthreads();  // group A and the zeroed partial sums visible to all threads
 
-  // ---- W^ (dequantized, bf16) and T diag(beta), once ----
-  if constexpr (WM != GDN_QDQ_NONE) {
-    const float sW = p.w_scales[slot * p.Hv + h];
-    for (int e = threadIdx.x; e < kChunk * DK / 4; e += kThreads) {
-      const int r = (4 * e) / DK, col = (4 * e) % DK;
-      const float4 v = qdq_code4_values<WM>(*reinterpret_cast<const uint32_t*>(wst + r * DK + col));
-      *reinterpret_cast<uint2*>(Wv + swz<DK>(r, col)) =
-          make_uint2(pack_bf16(v.x * sW, v.y * sW), pack_bf16(v.z * sW, v.w * sW));
-    }
-  } else {
-    // W from the forward's fp32 copy (rows >= Lc zero)
-    for (int e = threadIdx.x; e < kChunk * DK / 4; e += kThreads) {
-      const int r = (4 * e) / DK, col = (4 * e) % DK;
-      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (r < Lc) x = *reinterpret_cast<const float4*>(p.w_full + ((ctok + r) * p.Hv + h) * DK + col);
-      *reinterpret_cast<uint2*>(Wv + swz<DK>(r, col)) =
-          make_uint2(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w));
-    }
-  }
-  for (int e = threadIdx.x; e < 64 * 32; e += kThreads) {
-    const int i = e >> 5, j = (e & 31) * 2;
-    const __nv_bfloat162 t2 = *reinterpret_cast<const __nv_bfloat162*>(Tb + swz<64>(i, j));
-    st_bf16x2(Tub + swz<64>(i, j), __bfloat162float(t2.x) * bet[j],
-              __bfloat162float(t2.y) * bet[j + 1]);
-  }
-
   constexpr int NTW = DK / 32;
   const int wrow0 = rt * 16, wcol0 = ch * (DK / 4);
   const int row0 = rt * 16, col0 = ch * 16;
@@ -593,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
     const __nv_bfloat16* Vs = Vb(vb);
     const __nv_bfloat16* dOs = dOb(vb);
     const __nv_bfloat16* dHp = dHpb(vb);
+    const __nv_bfloat16* Dv = DbOf(vb);  // this block's Delta, as the forward formed it
     // ---- H^ of this block (bf16) and <H^, dH'> ----
     {
       const uint8_t* hst = hcb(vb);
@@ -628,13 +594,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
     if (vb == 0) cp_async_wait<1>();  // block 1's group was waited for before its H^
     __syncthreads();  // H^, this block's loads (and W^, T diag(beta)) ready
 
-    // ---- Delta = Tu V - W^ H^;  dDelta = scale P^T dO + dec (K dH') ----
+    // ---- dDelta = scale P^T dO + dec (K dH') ----
     {
-      float u[2][4], wh[2][4];
-      zero_acc(u);
-      zero_acc(wh);
-      wgemm<2, false, true, 64, 64>(u, Tub, row0, Vs, col0, 0, 64, lane);
-      wgemm<2, false, true, DK, 64>(wh, Wv, row0, Hh, col0, 0, DK, lane);
       float a1[2][4], a2[2][4];
       zero_acc(a1);
       zero_acc(a2);
@@ -645,8 +606,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-          st_bf16x2(Db + swz<64>(i, j), u[nt][2 * e2] - wh[nt][2 * e2],
-                    u[nt][2 * e2 + 1] - wh[nt][2 * e2 + 1]);
           const float di = dec[i];
           st_bf16x2(dDb + swz<64>(i, j), p.scale * a1[nt][2 * e2] + di * a2[nt][2 * e2],
                     p.scale * a1[nt][2 * e2 + 1] + di * a2[nt][2 * e2 + 1]);
@@ -660,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
     zero_acc(dp);
     zero_acc(ohq);
     static_assert(NTW == 2 || NTW == 4, "warp tile");
-    wgemm_shared_a<2, NTW, false, false, false, 64, 64, 64>(dp, ohq, dOs, row0, Db, col0, Hh, wcol0,
+    wgemm_shared_a<2, NTW, false, false, false, 64, 64, 64>(dp, ohq, dOs, row0, Dv, col0, Hh, wcol0,
                                                             0, 64, lane);
     {
       // dP = lower-incl(scale dO Delta^T); Gm += dP Gamma; PP = dP P
@@ -716,7 +675,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
       // Delta dH'^T: dK += dec_i (Delta dH'^T); t_i = dec_i sum_d k_id (Delta dH'^T)_id
       float acc[NTW][4];
       zero_acc(acc);
-      wgemm<NTW, false, false, 64, 64>(acc, Db, wrow0, dHp, wcol0, 0, 64, lane);
+      wgemm<NTW, false, false, 64, 64>(acc, Dv, wrow0, dHp, wcol0, 0, 64, lane);
       float kd[NTW][4];
 #pragma unroll
       for (int nt = 0; nt < NTW; ++nt)
@@ -1129,6 +1088,7 @@ gdn_status launch_bwd(const gdn_problem& p, const Dims& d, const void* q, const 
   prm.tb = reinterpret_cast<const __nv_bfloat16*>(base + L.tb);
   prm.gkk = reinterpret_cast<const __nv_bfloat16*>(base + L.gkk);
   prm.pb = reinterpret_cast<const __nv_bfloat16*>(base + L.pb);
+  prm.db = reinterpret_cast<const __nv_bfloat16*>(base + L.db);
   prm.dq = dq;
   prm.dk = dk;
   prm.dv = dv;

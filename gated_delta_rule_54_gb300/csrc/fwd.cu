@@ -70,6 +70,7 @@ struct FwdParams {
   float* h_full;
   float* cvec;  // [n_slots, Hv, kCvecFloats] chunk vectors
   __nv_bfloat16 *tb, *gkk, *pb;  // [n_slots, Hv] 8 KiB tile images for the backward
+  __nv_bfloat16* db;             // [n_slots, Hv, Dv / 64] Delta tile images for the backward
   const int32_t* cu_seqlens;
   int64_t T;
   int Hk, Hv, Dv, G, N;
@@ -1080,8 +1081,10 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
   }
   __syncthreads();  // K reads done (its tile becomes Delta)
 
-  // value block 0 also saves P (bf16; rows >= L zero) as the backward's tile image
+  // value block 0 also saves P (bf16; rows >= L zero) as the backward's tile
+  // image, and every block its Delta (the hi half: Delta rounded to bf16)
   __nv_bfloat16* pimg = vb == 0 ? p.pb + (slot * p.Hv + h) * (kTileImgBytes / 2) : nullptr;
+  __nv_bfloat16* dimg = p.db + ((slot * p.Hv + h) * nvb + vb) * (kTileImgBytes / 2);
 #pragma unroll
   for (int nt = 0; nt < 4; ++nt) {
     const float sWH = (WM != GDN_QDQ_NONE ? sW : 1.f) * (nt < 2 ? sHa : sHb);
@@ -1107,6 +1110,7 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
       split_bf16(u.y - sWH * dacc[nt][2 * e2 + 1], h1v, l1v);
       st_bf16x2(DH + swz<64>(i, j), h0v, h1v);
       st_bf16x2(DL + swz<64>(i, j), l0v, l1v);
+      st_bf16x2(dimg + swz<64>(i, j), h0v, h1v);
     }
   }
   __syncthreads();  // P, Delta ready; U reads done (its tile becomes the O staging)
@@ -1300,6 +1304,7 @@ gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const 
   prm.tb = reinterpret_cast<__nv_bfloat16*>(base + L.tb);
   prm.gkk = reinterpret_cast<__nv_bfloat16*>(base + L.gkk);
   prm.pb = reinterpret_cast<__nv_bfloat16*>(base + L.pb);
+  prm.db = reinterpret_cast<__nv_bfloat16*>(base + L.db);
   if (p.state_mode != GDN_QDQ_NONE) {
     prm.h_codes = base + L.h_codes;
     prm.h_scales = reinterpret_cast<float*>(base + L.h_scales);

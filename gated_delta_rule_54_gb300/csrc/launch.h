@@ -27,7 +27,7 @@ struct Dims {
 
 // Byte offsets of the saved context segments (see gdn_ctx_bytes).
 struct CtxLayout {
-  size_t w_codes, w_scales, w_full, cvec, tb, gkk, pb, h_codes, h_scales, h_full, total;
+  size_t w_codes, w_scales, w_full, cvec, tb, gkk, pb, db, h_codes, h_scales, h_full, total;
 };
 
 Dims dims_of(const gdn_problem& p);

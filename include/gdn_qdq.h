@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define GDN_QDQ_ABI_VERSION 4
+#define GDN_QDQ_ABI_VERSION 5
 
 typedef enum {
   GDN_QDQ_NONE = 0, /* site not quantized                                   */
@@ -134,6 +134,8 @@ int64_t gdn_num_chunk_slots(const gdn_problem* p);
  *   t_img     bf16 [n_slots, Hv, 4096]  T = (I + A)^-1 (lower incl. diagonal)
  *   gkk_img   bf16 [n_slots, Hv, 4096]  Gamma o KK^T (strictly lower)
  *   p_img     bf16 [n_slots, Hv, 4096]  P = Gamma o QK^T (lower incl. diagonal)
+ *   d_img     bf16 [n_slots, Hv, Dv/64, 4096]  Delta = U - W^ H^ of each
+ *                                       64-column value block
  *             each 64 x 64 tile stored as its shared-memory image: element
  *             (i, j) at i * 64 + 8 * ((j / 8) ^ (i % 8)) + j % 8; rows past
  *             the chunk end are zero (T: identity rows)

@@ -84,6 +84,7 @@ def test_sizes():
     al = lambda x: (x + 255) // 256 * 256
     ns = 2 * nt
     cv = al(4 * ns * 4 * 5 * 64) + 3 * al(ns * 4 * 64 * 64 * 2)   # chunk vectors, T / GKK / P images
+    cv += al(ns * 4 * 2 * 64 * 64 * 2)                              # Delta images of both value blocks
     exp = al(2 * 300 * 4 * 128) + al(4 * ns * 4) + cv + al(ns * 4 * 128 * 128) + al(4 * ns * 4 * 2)
     assert lib.gdn_ctx_bytes(ctypes.byref(p)) == exp
     p0 = _problem(state_mode=0, w_mode=0)
@@ -145,7 +146,7 @@ def test_status_strings():
     for code in range(-7, 1):
         s = lib.gdn_status_string(code).decode()
         assert s.startswith("GDN_")
-    assert lib.gdn_abi_version() == 4
+    assert lib.gdn_abi_version() == 5
 
 
 def _dproblem(**kw):

@@ -258,8 +258,8 @@ def _unswizzle(img):
 
 
 def test_fwd_saved_backward_tiles():
-    """T, Gamma o KK^T and P saved for the backward, against the oracle's T and
-    their definitions (bf16 storage: 2^-8 relative)."""
+    """T, Gamma o KK^T, P and Delta saved for the backward, against the oracle's
+    intermediates and their definitions (bf16 storage: 2^-8 relative)."""
     from oracle.chunked import chunked
     w = synth.small(B=1, T=150, Hk=1, Hv=2, Dk=64, Dv=64, h0=True, seed=31)
     d = synth.make_inputs(w)
@@ -286,3 +286,8 @@ def test_fwd_saved_backward_tiles():
                 if name != "t_img":
                     assert not x[L:].any(), (name, c, h)   # rows past the chunk end are zero
             assert np.array_equal(imgs["t_img"][c, h, L:, L:], np.eye(64 - L))
+            # Delta = U - W^ H^ of the (single, Dv = 64) value block, rounded to bf16
+            dimg = _unswizzle(seg["d_img"][:, :, 0].float().cpu().numpy())[c, h]
+            dref = st["Delta"][h].numpy()
+            assert np.abs(dimg[:L] - dref).max() <= 2 ** -7 * np.abs(dref).max(), ("d_img", c, h)
+            assert not dimg[L:].any(), ("d_img", c, h)
