@@ -833,7 +833,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
       if constexpr (WM != GDN_QDQ_NONE) sW_next = p.w_scales[(slot + 1) * p.Hv + h];
     }
 
-    // ---- a7: Delta = U - W^ H^;  Delta' = diag(e^{gamma_L - gamma}) Delta (rows >= Lc zero) ----
+    // ---- a7: Delta = U - W^ H^ (written over U, for the output pass);
+    //      Delta' = diag(e^{gamma_L - gamma}) Delta (rows >= Lc zero) ----
     {
       float dacc[2][4];
       zero_acc(dacc);
@@ -853,24 +854,48 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
         if constexpr (WM == GDN_QDQ_NONE) wgemm<2, false, true, DK, 64>(dacc, WcL, row0, HcH, col0, 0, DK, lane);
         if constexpr (SM == GDN_QDQ_NONE) wgemm<2, false, true, DK, 64>(dacc, WcH, row0, HcL, col0, 0, DK, lane);
       }
-      const float* Us = Ubuf(buf);
+      float* Us = Ubuf(buf);
       const float sWH = (WM != GDN_QDQ_NONE ? sW : 1.f) * (SM != GDN_QDQ_NONE ? pick(sHt, td) : 1.f);
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-          const float2 u = *reinterpret_cast<const float2*>(Us + swz_f32(i, j));
+          float2* up = reinterpret_cast<float2*>(Us + swz_f32(i, j));
+          const float2 u = *up;
+          const float2 dl = make_float2(u.x - sWH * dacc[nt][2 * e2], u.y - sWH * dacc[nt][2 * e2 + 1]);
+          *up = dl;
           const float di = i < Lc ? dec[i] : 0.f;  // rows past the chunk end contribute nothing
           float h0v, l0v, h1v, l1v;
-          split_bf16((u.x - sWH * dacc[nt][2 * e2]) * di, h0v, l0v);
-          split_bf16((u.y - sWH * dacc[nt][2 * e2 + 1]) * di, h1v, l1v);
+          split_bf16(dl.x * di, h0v, l0v);
+          split_bf16(dl.y * di, h1v, l1v);
           st_bf16x2(DpH + swz<64>(i, j), h0v, h1v);
           st_bf16x2(DpL + swz<64>(i, j), l0v, l1v);
         }
       }
+      fence_proxy_async();  // the Delta tile is read by the TMA store below
     }
-    __syncthreads();  // Delta' ready
+    __syncthreads();  // Delta' ready; Delta over U in its tile
+    if (Lc == kChunk) {
+      // Delta replaces U in o (rows past the tensor end are clipped); the store
+      // has read the tile before the buffer is refilled (next iteration's wait)
+      if (threadIdx.x == 0) {
+#pragma unroll
+        for (int pn = 0; pn < 2; ++pn)
+          tma_store_2d(&p.tm_u, h * p.Dv + vb * 64 + pn * 32, (int)(tok0 + (int64_t)c * kChunk),
+                       Ubuf(buf) + pn * kChunk * 32);
+        tma_store_commit();
+      }
+    } else {
+      // a sequence's last, partial chunk: its rows only (the next rows are another sequence's U)
+      const float* Us = Ubuf(buf);
+      const int64_t t0 = tok0 + (int64_t)c * kChunk;
+      for (int i = threadIdx.x; i < Lc * 16; i += kStateThreads) {
+        const int r = i >> 4, c4 = i & 15;
+        *reinterpret_cast<float4*>(p.o + ((t0 + r) * p.Hv + h) * p.Dv + vb * 64 + c4 * 4) =
+            *reinterpret_cast<const float4*>(Us + swz_f32(r, c4 * 4));
+      }
+    }
 
     // ---- a9: H <- e^{gamma_L} H^ + K^T Delta' (K rows >= Lc meet zero rows of Delta') ----
     {
@@ -901,7 +926,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
 }
 
 // ===========================================================================
-// 3. Output: O = scale (diag(e^gamma) Q H^ + P Delta), Delta = U - W^ H^.
+// 3. Output: O = scale (diag(e^gamma) Q H^ + P Delta); Delta = U - W^ H^ as the
+//    state scan left it in o.
 // ===========================================================================
 constexpr int kOutThreads = 256;
 
@@ -909,17 +935,16 @@ template <int DK, int SM, int WM>
 struct OutSmem {
   static constexpr int Q = 0;                                              // bf16 [64][DK] (TMA)
   static constexpr int K = Q + kChunk * DK * 2;                            // bf16 [64][DK] (TMA); later Delta hi, lo
-  static constexpr int U = K + kChunk * DK * 2;                            // f32 [64][64] swz_f32 (TMA); later O
-  static constexpr int P = U + kChunk * 64 * 4;                            // P hi, lo; first W / H codes (TMA)
-  static constexpr int WC = P + 2 * kChunk * 64 * 2;                       // W^ [64][DK] (hi, lo)
-  static constexpr int HC = WC + (WM == GDN_QDQ_NONE ? 2 : 1) * kChunk * DK * 2;  // H^ [DK][64] (hi, lo)
+  static constexpr int U = K + kChunk * DK * 2;                            // f32 Delta [64][64] swz_f32 (TMA); later O
+  static constexpr int P = U + kChunk * 64 * 4;                            // P hi, lo; first the H codes (TMA)
+  static constexpr int HC = P + 2 * kChunk * 64 * 2;                       // H^ [DK][64] (hi, lo)
   static constexpr int CV = HC + (SM == GDN_QDQ_NONE ? 2 : 1) * DK * 64 * 2;      // chunk vectors
   // Delta hi, lo [64][64]: in the dead K tile when it is large enough
   static constexpr bool D_IN_K = 2 * kChunk * 64 * 2 <= kChunk * DK * 2;
   static constexpr int D = D_IN_K ? K : CV + kCvecFloats * 4;
   static constexpr int END = D_IN_K ? CV + kCvecFloats * 4 : D + 2 * kChunk * 64 * 2;
   static constexpr int BYTES = END + 1024;  // + alignment slack
-  static_assert((K % 1024) == 0 && (U % 1024) == 0 && (P % 1024) == 0 && (WC % 128) == 0 &&
+  static_assert((K % 1024) == 0 && (U % 1024) == 0 && (P % 1024) == 0 &&
                     (HC % 128) == 0 && (D % 128) == 0,
                 "alignment");
 };
@@ -946,8 +971,6 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
 
   __nv_bfloat16* Qs = reinterpret_cast<__nv_bfloat16*>(sm + S::Q);
   __nv_bfloat16* Ks = reinterpret_cast<__nv_bfloat16*>(sm + S::K);
-  __nv_bfloat16* WcH = reinterpret_cast<__nv_bfloat16*>(sm + S::WC);
-  __nv_bfloat16* WcL = WcH + kChunk * DK;
   __nv_bfloat16* HcH = reinterpret_cast<__nv_bfloat16*>(sm + S::HC);
   __nv_bfloat16* HcL = HcH + DK * 64;
   float* Us = reinterpret_cast<float*>(sm + S::U);
@@ -959,16 +982,14 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
   float* Cv = reinterpret_cast<float*>(sm + S::CV);
   const float* gam = Cv + kCvGam;
   const float* eg = Cv + kCvEg;
-  // W / H codes land in the P tile (free until the P epilogue)
-  uint8_t* Wraw = reinterpret_cast<uint8_t*>(PH);
-  uint8_t* Hraw = Wraw + kChunk * DK;
+  // H codes land in the P tile (free until the P epilogue)
+  uint8_t* Hraw = reinterpret_cast<uint8_t*>(PH);
 
-  // ---- loads: TMA boxes on one mbarrier; g (and fp32 W / H) by the threads ----
+  // ---- loads: TMA boxes on one mbarrier; fp32 H (state site off) by the threads ----
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();
     const uint32_t bytes = 2 * kChunk * DK * 2 + kChunk * 64 * 4 + kCvecFloats * 4 +
-                           (WM != GDN_QDQ_NONE ? kChunk * DK : 0) +
                            (SM != GDN_QDQ_NONE ? DK * 64 : 0);
     mbar_expect_tx(&bar, bytes);
     bulk_load_1d(Cv, p.cvec + (slot * p.Hv + h) * kCvecFloats, kCvecFloats * 4, &bar);
@@ -980,28 +1001,8 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
 #pragma unroll
     for (int pn = 0; pn < 2; ++pn)
       tma_load_2d(Us + pn * kChunk * 32, &p.tm_u, h * p.Dv + vb * 64 + pn * 32, (int)tok0, &bar);
-    if constexpr (WM != GDN_QDQ_NONE) tma_load_2d(Wraw, &p.tm_wc, h * DK, (int)tok0, &bar);
     if constexpr (SM != GDN_QDQ_NONE)
       tma_load_2d(Hraw, &p.tm_hc, vb * 64, (int)((slot * p.Hv + h) * DK), &bar);
-  }
-  float sW = 1.f;
-  if constexpr (WM != GDN_QDQ_NONE) {
-    sW = p.w_scales[slot * p.Hv + h];
-  } else {
-    constexpr int C4 = DK / 4;
-    for (int i = threadIdx.x; i < kChunk * C4; i += kOutThreads) {
-      const int r = i / C4, c4 = i % C4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (r < L) v = *reinterpret_cast<const float4*>(p.w_full + ((tok0 + r) * p.Hv + h) * DK + c4 * 4);
-      float h0v, l0v, h1v, l1v, h2v, l2v, h3v, l3v;
-      split_bf16(v.x, h0v, l0v);
-      split_bf16(v.y, h1v, l1v);
-      split_bf16(v.z, h2v, l2v);
-      split_bf16(v.w, h3v, l3v);
-      const int e = swz<DK>(r, c4 * 4);
-      *reinterpret_cast<uint2*>(WcH + e) = make_uint2(pack_bf16(h0v, h1v), pack_bf16(h2v, h3v));
-      *reinterpret_cast<uint2*>(WcL + e) = make_uint2(pack_bf16(l0v, l1v), pack_bf16(l2v, l3v));
-    }
   }
   // state scales of this warp's two 16-column groups (each inside one
   // state-scale tile: tiles are 16-aligned and at least 16 wide); scales are
@@ -1037,17 +1038,7 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
     return;
   }
 
-  // codes -> bf16 values (exact); W rows >= L (another sequence's tokens) are zero
-  if constexpr (WM != GDN_QDQ_NONE) {
-    constexpr int C4 = DK / 4;
-    for (int i = threadIdx.x; i < kChunk * C4; i += kOutThreads) {
-      const int r = i / C4, c4 = i % C4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (r < L) v = qdq_code4_values<WM>(*reinterpret_cast<const uint32_t*>(Wraw + r * DK + c4 * 4));
-      *reinterpret_cast<uint2*>(WcH + swz<DK>(r, c4 * 4)) =
-          make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
-    }
-  }
+  // codes -> bf16 values (exact)
   if constexpr (SM != GDN_QDQ_NONE) {
     for (int i = threadIdx.x; i < DK * 16; i += kOutThreads) {
       const int d = i >> 4, c4 = i & 15;
@@ -1056,7 +1047,7 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
           make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
     }
   }
-  __syncthreads();  // W^, H^ operands ready; the P tile is free again
+  __syncthreads();  // H^ operand ready; the P tile is free again
 
   // warp tile: rows 16 rt .. +15, columns 32 ch .. +31.  Rows >= L of Q and K
   // hold another sequence's tokens: they only reach P entries outside the
@@ -1064,21 +1055,12 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
   const int rt = warp & 3, ch = warp >> 2;
   const int row0 = rt * 16, col0 = ch * 32;
   const bool p_tile = col0 <= row0 + 15;
-  float pacc[4][4], dacc[4][4], qacc[4][4];
+  float pacc[4][4], qacc[4][4];
   zero_acc(pacc);
-  zero_acc(dacc);
   zero_acc(qacc);
   if (p_tile) wgemm<4, false, false, DK, DK>(pacc, Qs, row0, Ks, col0, 0, DK, lane);
-  if constexpr (WM != GDN_QDQ_NONE && SM != GDN_QDQ_NONE) {
-    // W^ H^ and Q H^ share their H^ fragments
-    wgemm_shared_b<4, false, true, DK, 64>(dacc, qacc, WcH, Qs, row0, HcH, col0, 0, DK, lane);
-  } else {
-    wgemm<4, false, true, DK, 64>(dacc, WcH, row0, HcH, col0, 0, DK, lane);
-    if constexpr (WM == GDN_QDQ_NONE) wgemm<4, false, true, DK, 64>(dacc, WcL, row0, HcH, col0, 0, DK, lane);
-    if constexpr (SM == GDN_QDQ_NONE) wgemm<4, false, true, DK, 64>(dacc, WcH, row0, HcL, col0, 0, DK, lane);
-    wgemm<4, false, true, DK, 64>(qacc, Qs, row0, HcH, col0, 0, DK, lane);
-    if constexpr (SM == GDN_QDQ_NONE) wgemm<4, false, true, DK, 64>(qacc, Qs, row0, HcL, col0, 0, DK, lane);
-  }
+  wgemm<4, false, true, DK, 64>(qacc, Qs, row0, HcH, col0, 0, DK, lane);
+  if constexpr (SM == GDN_QDQ_NONE) wgemm<4, false, true, DK, 64>(qacc, Qs, row0, HcL, col0, 0, DK, lane);
   __syncthreads();  // K reads done (its tile becomes Delta)
 
   // value block 0 also saves P (bf16; rows >= L zero) as the backward's tile
@@ -1087,7 +1069,6 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
   __nv_bfloat16* dimg = p.db + ((slot * p.Hv + h) * nvb + vb) * (kTileImgBytes / 2);
 #pragma unroll
   for (int nt = 0; nt < 4; ++nt) {
-    const float sWH = (WM != GDN_QDQ_NONE ? sW : 1.f) * (nt < 2 ? sHa : sHb);
 #pragma unroll
     for (int e2 = 0; e2 < 2; ++e2) {
       const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -1104,10 +1085,10 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
       } else if (pimg) {
         st_bf16x2(pimg + swz<64>(i, j), 0.f, 0.f);
       }
-      float2 u = *reinterpret_cast<const float2*>(Us + swz_f32(i, j));
-      if (i >= L) u = make_float2(0.f, 0.f);
-      split_bf16(u.x - sWH * dacc[nt][2 * e2], h0v, l0v);
-      split_bf16(u.y - sWH * dacc[nt][2 * e2 + 1], h1v, l1v);
+      float2 dl = *reinterpret_cast<const float2*>(Us + swz_f32(i, j));
+      if (i >= L) dl = make_float2(0.f, 0.f);  // rows of another sequence
+      split_bf16(dl.x, h0v, l0v);
+      split_bf16(dl.y, h1v, l1v);
       st_bf16x2(DH + swz<64>(i, j), h0v, h1v);
       st_bf16x2(DL + swz<64>(i, j), l0v, l1v);
       st_bf16x2(dimg + swz<64>(i, j), h0v, h1v);

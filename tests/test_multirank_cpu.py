@@ -3,7 +3,7 @@ sequences across ranks needs no exchange — per-rank oracle results gathered
 from both ranks equal the unsharded result — and the benchmark's barrier and
 max-over-ranks timing work across processes."""
 import os
-import socket
+import tempfile
 
 import numpy as np
 import pytest
@@ -14,16 +14,11 @@ import torch.multiprocessing as mp
 from gated_delta_rule_54_gb300 import shard, synth
 
 
-def _free_port():
-    with socket.socket() as s:
-        s.bind(("127.0.0.1", 0))
-        return s.getsockname()[1]
-
-
-def _worker(rank, world, port, out):
-    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
-                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
-    dist.init_process_group("gloo", rank=rank, world_size=world)
+def _worker(rank, world, store_file, out):
+    # a file store: no port to race for
+    os.environ.update(RANK=str(rank), WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    dist.init_process_group("gloo", init_method="file://" + store_file, rank=rank,
+                            world_size=world)
     try:
         from oracle.chunked import chunked
         import bench
@@ -55,8 +50,9 @@ def _worker(rank, world, port, out):
             h_all = torch.cat([g[:s[1]] for g, s in zip(gh, sizes)], 0)
             o_ref, h_ref = chunked(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"],
                                    cu_seqlens=d["cu_seqlens"], state_mode="e4m3", w_mode="e4m3")
-            out.put((bool(torch.equal(o_all, o_ref)), bool(torch.equal(h_all, h_ref)), mx,
-                     [s for s in sizes]))
+            # the same per-sequence arithmetic; only the BLAS batch grouping differs
+            close = lambda a, b: float((a - b).abs().max()) <= 1e-12 * float(b.abs().max())
+            out.put((close(o_all, o_ref), close(h_all, h_ref), mx, [s for s in sizes]))
     finally:
         dist.destroy_process_group()
 
@@ -64,8 +60,8 @@ def _worker(rank, world, port, out):
 def test_two_ranks_shard_without_exchange():
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
-    port = _free_port()
-    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    store = os.path.join(tempfile.mkdtemp(prefix="gdn_gloo_"), "store")
+    procs = [ctx.Process(target=_worker, args=(r, 2, store, q)) for r in range(2)]
     for p in procs:
         p.start()
     res = q.get(timeout=300)
