@@ -166,7 +166,8 @@ size_t gdn_ctx_bytes(const gdn_problem* p);
  * H <- exp(gamma_L) H^ + (diag(exp(gamma_L - gamma)) K)^T Delta.
  * Three launches: the chunk-local part (A, T, W with its QDQ, U) for all
  * chunks at once, the serial state scan, then the outputs for all chunks at
- * once; U is kept in `o` between the first and the last launch.
+ * once; `o` holds U after the first launch and Delta (which the scan writes
+ * over U) until the last launch writes the outputs over it.
  * A sequence of length 0 returns ht = h0 (not quantized).
  * All pointers must be 16-byte aligned (GDN_ERR_MISALIGNED otherwise).
  */
