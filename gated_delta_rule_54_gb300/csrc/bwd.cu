@@ -436,10 +436,10 @@ __device__ __forceinline__ void racc_add_rows(float* racc, int slot, int row0, i
 }
 
 // Phase 2: all gradients of one (chunk slot, value head), both 64-column value
-// blocks in one CTA: the value-block terms (Delta, dDelta, dP, dV, the parts
-// of dW, dT, Gm, dq, dk and the row sums) run per block and are summed on
-// chip; T^T dW, Gm K, Gm^T Q, X = T^T dT, dA and dKK run once; every output
-// element has one writer.
+// blocks in one CTA: the value-block terms (dDelta, dP, dV, the parts of dW,
+// dT, Gm, dq, dk and the row sums; Delta itself is the forward's image) run
+// per block and are summed on chip; T^T dW, Gm K, Gm^T Q, X = T^T dT, dA and
+// dKK run once; every output element has one writer.
 template <int DK, int SM, int WM>
 __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid_constant__ BwdParams p) {
   using S = ChunkSmem<DK>;
@@ -592,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
       if (lane == 0) hd_part[warp] += hd;
     }
     if (vb == 0) cp_async_wait<1>();  // block 1's group was waited for before its H^
-    __syncthreads();  // H^, this block's loads (and W^, T diag(beta)) ready
+    __syncthreads();  // H^ and this block's loads ready
 
     // ---- dDelta = scale P^T dO + dec (K dH') ----
     {

@@ -1094,7 +1094,7 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
       st_bf16x2(dimg + swz<64>(i, j), h0v, h1v);
     }
   }
-  __syncthreads();  // P, Delta ready; U reads done (its tile becomes the O staging)
+  __syncthreads();  // P, Delta ready; the Delta tile from o is read (it becomes the O staging)
 
   {
     float o2[4][4];
