@@ -833,7 +833,7 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
       if constexpr (WM != GDN_QDQ_NONE) sW_next = p.w_scales[(slot + 1) * p.Hv + h];
     }
 
-    // ---- a7: Delta = U - W^ H^ (written over U, for the output pass);
+    // ---- a7: Delta = U - W^ H^ (stored over U in o, for the output pass);
     //      Delta' = diag(e^{gamma_L - gamma}) Delta (rows >= Lc zero) ----
     {
       float dacc[2][4];
@@ -854,17 +854,18 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
         if constexpr (WM == GDN_QDQ_NONE) wgemm<2, false, true, DK, 64>(dacc, WcL, row0, HcH, col0, 0, DK, lane);
         if constexpr (SM == GDN_QDQ_NONE) wgemm<2, false, true, DK, 64>(dacc, WcH, row0, HcL, col0, 0, DK, lane);
       }
-      float* Us = Ubuf(buf);
+      const float* Us = Ubuf(buf);
       const float sWH = (WM != GDN_QDQ_NONE ? sW : 1.f) * (SM != GDN_QDQ_NONE ? pick(sHt, td) : 1.f);
+      float* dst = p.o + ((tok0 + (int64_t)c * kChunk) * p.Hv + h) * p.Dv + vb * 64;
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-          float2* up = reinterpret_cast<float2*>(Us + swz_f32(i, j));
-          const float2 u = *up;
+          const float2 u = *reinterpret_cast<const float2*>(Us + swz_f32(i, j));
           const float2 dl = make_float2(u.x - sWH * dacc[nt][2 * e2], u.y - sWH * dacc[nt][2 * e2 + 1]);
-          *up = dl;
+          // Delta replaces U in o (this sequence's rows only)
+          if (i < Lc) *reinterpret_cast<float2*>(dst + (int64_t)i * p.Hv * p.Dv + j) = dl;
           const float di = i < Lc ? dec[i] : 0.f;  // rows past the chunk end contribute nothing
           float h0v, l0v, h1v, l1v;
           split_bf16(dl.x * di, h0v, l0v);
@@ -873,29 +874,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
           st_bf16x2(DpL + swz<64>(i, j), l0v, l1v);
         }
       }
-      fence_proxy_async();  // the Delta tile is read by the TMA store below
     }
-    __syncthreads();  // Delta' ready; Delta over U in its tile
-    if (Lc == kChunk) {
-      // Delta replaces U in o (rows past the tensor end are clipped); the store
-      // has read the tile before the buffer is refilled (next iteration's wait)
-      if (threadIdx.x == 0) {
-#pragma unroll
-        for (int pn = 0; pn < 2; ++pn)
-          tma_store_2d(&p.tm_u, h * p.Dv + vb * 64 + pn * 32, (int)(tok0 + (int64_t)c * kChunk),
-                       Ubuf(buf) + pn * kChunk * 32);
-        tma_store_commit();
-      }
-    } else {
-      // a sequence's last, partial chunk: its rows only (the next rows are another sequence's U)
-      const float* Us = Ubuf(buf);
-      const int64_t t0 = tok0 + (int64_t)c * kChunk;
-      for (int i = threadIdx.x; i < Lc * 16; i += kStateThreads) {
-        const int r = i >> 4, c4 = i & 15;
-        *reinterpret_cast<float4*>(p.o + ((t0 + r) * p.Hv + h) * p.Dv + vb * 64 + c4 * 4) =
-            *reinterpret_cast<const float4*>(Us + swz_f32(r, c4 * 4));
-      }
-    }
+    __syncthreads();  // Delta' ready
 
     // ---- a9: H <- e^{gamma_L} H^ + K^T Delta' (K rows >= Lc meet zero rows of Delta') ----
     {
