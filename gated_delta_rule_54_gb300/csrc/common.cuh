@@ -33,16 +33,19 @@ struct QdqMax<GDN_QDQ_INT8> {
   static constexpr float value = 127.0f;
 };
 
-// Scale and its reciprocal from the group amax.  amax == 0 gives s = 0 and
-// rcp = 0 (the caller keeps the inputs, which are all zero).
+// Scale and its reciprocal from the group amax.  When fl(1/s) is not finite
+// (amax == 0, or an amax so small that s = fl(amax / M) is at most 2^-128) the
+// group has no usable scale: s = 0 and rcp = 0, so every code is a signed zero
+// and every dequantized value is a zero of the input's sign (codes x scale
+// still reproduce the values).  Without this, a zero element of such a group
+// would give 0 * inf = NaN.
 template <int MODE>
 __device__ __forceinline__ void qdq_scale(float amax, float& s, float& rcp) {
-  if (amax == 0.0f) {
+  s = __fdiv_rn(amax, QdqMax<MODE>::value);
+  rcp = __frcp_rn(s);
+  if (isinf(rcp)) {
     s = 0.0f;
     rcp = 0.0f;
-  } else {
-    s = __fdiv_rn(amax, QdqMax<MODE>::value);
-    rcp = __frcp_rn(s);
   }
 }
 

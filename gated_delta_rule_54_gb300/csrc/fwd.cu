@@ -427,7 +427,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __g
             *reinterpret_cast<const uint4*>(Wst + r * DK + c16 * 16);
       }
     }
-    if (threadIdx.x == 0) p.w_scales[slot * p.Hv + h] = (amax == 0.f) ? 0.f : sW;
+    if (threadIdx.x == 0) p.w_scales[slot * p.Hv + h] = sW;
   } else {
 #pragma unroll
     for (int nt = 0; nt < NTW; ++nt)
@@ -738,7 +738,6 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
       rct[i] = 0.f;
       if constexpr (SM != GDN_QDQ_NONE) {
         qdq_scale<SM>(amx[i], sHt[i], rct[i]);
-        if (amx[i] == 0.f) sHt[i] = 0.f;
       }
     }
     const float sHa = pick(sHt, ta), rca = pick(rct, ta), ama = pick(amx, ta);
@@ -754,7 +753,8 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
             const int d = h_row0 + gq + 8 * e2, col = h_col0 + nt * 8 + 2 * tq;
             float* hv = &hreg[nt][2 * e2];
             float2 val;
-            // amax == 0: rcp == 0 gives signed-zero codes, and the values stay as they are
+            // no usable scale (rcp == 0): signed-zero codes; with amax == 0 the values
+            // (all zeros) stay, and a tiny amax turns them into zeros of their sign
             const uint16_t c2 = e4m3_code2(hv[0], hv[1], rcp, val);
             if (!zero) {
               hv[0] = __fmul_rn(val.x, sH);

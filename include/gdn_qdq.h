@@ -232,7 +232,12 @@ gdn_status gdn_chunk_bwd_ste_noalloc(const gdn_problem* p, const void* q, const 
  * Bit-exact definition: a = max|x|; a == 0 gives s = 0, y = x, signed-zero
  * codes; else s = fl(a/M), r = fl(1/s), u = fl(x*r), code = RNE onto the
  * E4M3FN grid with finite saturation (M = 448) or nearest-even integer
- * clamped to [-127, 127] (M = 127), y = fl(code * s).
+ * clamped to [-127, 127] (M = 127), y = fl(code * s).  A nonzero a so small
+ * that r overflows (s <= 2^-128, i.e. a up to about M * 2^-128: 1.3e-36 for
+ * E4M3, 3.7e-37 for INT8) has no usable scale and is taken like a zero group scaled to zero: s = 0, r = 0,
+ * so the codes are signed zeros (INT8: 0) and y = fl(code * 0), a zero of
+ * x's sign for E4M3 and +0 for INT8.  The same rule holds at every QDQ site
+ * of every entry point.
  */
 gdn_status fake_qdq_e4m3(const float* x, float* y, float* scales, uint8_t* codes, int64_t batch,
                          int64_t rows, int64_t cols, int64_t group_cols, void* stream);

@@ -20,6 +20,11 @@
  *   if a == 0: scale = 0, y = x, codes are signed zeros
  *   s   = fl(a / M)      M = 448 (E4M3) or 127 (INT8), correctly rounded
  *   r   = fl(1 / s)      correctly rounded
+ *   if r is not finite (a tiny nonzero a: s at most 2^-128, where binary32
+ *       cannot hold 1/s), the pages give no scale to use; this oracle reads
+ *       it as a group scaled to zero: s = 0 and r = 0, and the steps below
+ *       then give signed-zero codes and y = fl(decode(c) * 0).  Taking r = inf
+ *       literally would turn a zero element into 0 * inf = NaN.
  *   u_i = fl(x_i * r)
  *   c_i = E4M3: round-to-nearest-even onto the OCP E4M3FN grid, finite
  *               values beyond 448 saturate to +-448 (sign kept, -0 kept)
@@ -123,6 +128,10 @@ static float qdq_group(const float* x, float* y, uint8_t* codes, int64_t rows,
   const float M = (mode == ORACLE_QDQ_E4M3) ? 448.0f : 127.0f;
   volatile float s = a / M;     /* one correctly rounded binary32 division */
   volatile float rcp = 1.0f / s;
+  if (isinf(rcp)) {
+    s = 0.0f;
+    rcp = 0.0f;
+  }
   for (int64_t r = 0; r < rows; ++r)
     for (int64_t j = 0; j < row_len; ++j) {
       int64_t i = r * row_stride + j;

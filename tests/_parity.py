@@ -5,9 +5,13 @@ Tolerances (stated once, used everywhere):
       elements satisfy |x - r| <= 1e-2 * |r| + 1e-3 * max|r| (relative error,
       with an absolute floor ten times below the max-abs bound for elements
       of r near zero);
-  state / W codes: every differing code is one quantization step away, and at
+  state / W codes: every differing code is one quantization step away (E4M3:
+      or within 2^-5 in code units, where the grid steps by 2^-9), and at
       most 0.1% of the codes differ (at least one flip is always allowed: a
       single flip in a few hundred codes is consistent with a 1e-5 flip rate);
+      state codes are compared in each (sequence, value head) up to and
+      including its first chunk with a flip, as the flipped state feeds the
+      later ones;
   units with a permitted flip: a (sequence, value head) whose state or W codes
       contain a one-step flip may deviate by the consequences of that flip —
       one E4M3 step is at most 2^-3 of the flipped element, so its outputs and
@@ -82,6 +86,15 @@ def code_steps(a, b, mode):
 
 def assert_codes(a, b, mode, what="codes"):
     d = code_steps(a, b, mode)
+    if mode == "e4m3" and d.size:
+        # Below 2^-5 the E4M3 grid steps by 2^-9 (subnormals and the lowest
+        # normal binade), finer than the kernel's fp32 / split-bf16 error
+        # relative to the group amax (448 in code units): near-zero elements
+        # may land a few codes apart.  Differences within 2^-5 in code units
+        # (2^-5 s, about 7e-5 of the amax) count as one step.
+        near = np.abs(oracle.e4m3_decode(np.ravel(a)).astype(np.float64) -
+                      oracle.e4m3_decode(np.ravel(b)).astype(np.float64)) <= 2.0 ** -5
+        d = np.where(near.reshape(d.shape) & (d > 1), 1, d)
     nflip = int((d > 0).sum())
     frac = nflip / d.size if d.size else 0.0
     assert d.max(initial=0) <= 1, "%s: a code differs by %d steps" % (what, int(d.max()))

@@ -28,8 +28,12 @@ def _gpu_fwd(d, sm, wm, scale=1.0, save_ctx=True, block_v=64, neumann_degree=Non
     return dd, o, ht, ctx
 
 
-def _check_case(w, lengths=None, scale=1.0, block_v=64, neumann_degree=None):
-    d = synth.make_inputs(w, lengths=lengths)
+def _check_case(w, lengths=None, scale=1.0, block_v=64, neumann_degree=None, d=None):
+    """Forward of workload w (or of the given inputs d, made for w) against the
+    oracle: state / W codes and scales, chunk vectors, o and ht, the last two
+    with the looser bound on (sequence, head) units whose codes flipped."""
+    if d is None:
+        d = synth.make_inputs(w, lengths=lengths)
     sm, wm = w.state_mode, w.w_mode
     dd, o, ht, ctx = _gpu_fwd(d, sm, wm, scale, block_v=block_v, neumann_degree=neumann_degree)
     o_ref, ht_ref, rec = run_oracle(d, sm, wm, scale=scale, record=True, block_v=block_v,
@@ -44,12 +48,19 @@ def _check_case(w, lengths=None, scale=1.0, block_v=64, neumann_degree=None):
     flipped = set()
     if sm != "none":
         codes = seg["h_codes"].cpu().numpy()[smap]
-        assert_codes(codes, rec["state_codes"], sm, "state codes")
-        sc = seg["h_scales"].cpu().numpy()[smap]
-        assert np.allclose(sc, rec["state_scales"], rtol=1e-2, atol=0)
         diff = code_steps(codes, rec["state_codes"], sm).reshape(len(smap), w.Hv, -1).max(-1)
+        # A flipped state code changes H^ by one step, and H^ feeds every later
+        # state of the same (sequence, head): the codes of that unit's later
+        # chunks carry the flip's consequences and are no independent check
+        # (the unit's o and ht are held to the flip bound instead).
+        indep = np.ones(diff.shape, bool)
         for ci, h in zip(*np.nonzero(diff)):
+            later = (chunk_seq == chunk_seq[ci]) & (np.arange(len(smap)) > ci)
+            indep[later, h] = False
             flipped.add((int(chunk_seq[ci]), int(h)))
+        assert_codes(codes[indep], np.asarray(rec["state_codes"])[indep], sm, "state codes")
+        sc = seg["h_scales"].cpu().numpy()[smap]
+        assert np.allclose(sc[indep], np.asarray(rec["state_scales"])[indep], rtol=1e-2, atol=0)
     else:
         hf = seg["h_full"].cpu().numpy()[smap]
         assert hf.shape[0] == len(smap)

@@ -45,6 +45,27 @@ def test_fake_qdq_zero_group_and_in_place(mode):
     assert s.cpu().numpy()[0, 0] == 0.0
 
 
+@pytest.mark.parametrize("mode", ["e4m3", "int8"])
+def test_fake_qdq_tiny_amax_groups(mode):
+    """Groups whose amax sits around the point where fl(1/s) overflows, with
+    zeros inside: bit-exact with the oracle, and finite."""
+    M = 448.0 if mode == "e4m3" else 127.0
+    amax = [M * 2.0 ** -126, M * 2.0 ** -127, M * 2.0 ** -128, M * 2.0 ** -129, 1e-40, 2.0 ** -149]
+    rng = np.random.default_rng(12)
+    x = rng.uniform(-1, 1, (len(amax), 16, 64)).astype(np.float32)
+    for b, a in enumerate(amax):
+        x[b] *= np.float32(a) / np.abs(x[b]).max()
+        x[b, 0, 0] = np.float32(a)
+        x[b, 3, :4] = [0.0, -0.0, 0.0, -0.0]
+    y_ref, s_ref, c_ref = oracle.qdq_groups(x, 64, mode, with_codes=True)
+    y, s, c = FN[mode](torch.from_numpy(x).cuda(), 64, with_codes=True)
+    y = y.cpu().numpy()
+    assert np.isfinite(y).all()
+    assert np.array_equal(_bits(s.cpu().numpy()), _bits(s_ref))
+    assert np.array_equal(c.cpu().numpy(), c_ref)
+    assert np.array_equal(_bits(y), _bits(y_ref))
+
+
 def test_fake_qdq_large_group_many_blocks():
     rng = np.random.default_rng(11)
     x = rng.standard_normal((1, 2048, 2048)).astype(np.float32)   # one 4M-element group

@@ -178,6 +178,32 @@ def test_qdq_zero_group_and_signed_zero():
     assert list(cd[0, 0]) == [0x7E, 0x80, 0x00, 0x00]
 
 
+@pytest.mark.parametrize("mode,M", [("e4m3", 448.0), ("int8", 127.0)])
+def test_qdq_tiny_amax_threshold(mode, M):
+    """Where fl(1/s) stops being finite.  a = M 2^-127 gives s = 2^-127 exactly
+    and r = 2^127, finite: the group quantizes normally and its largest element
+    is reproduced exactly (code M, M * 2^-127 = a).  a = M 2^-129 gives
+    s = 2^-129 and 1/s = 2^129, beyond binary32: the group has no usable scale
+    and every value becomes a zero of its sign (E4M3) or +0 (INT8), with scale 0
+    -- in particular no NaN from 0 * inf at the zero elements."""
+    lo = np.float32(M * 2.0 ** -127)
+    x = np.array([[[lo, -lo / 4, 0.0, -0.0]]], np.float32)
+    y, sc, cd = oracle.qdq_groups(x, 4, mode, with_codes=True)
+    assert sc[0, 0] == np.float32(2.0 ** -127)
+    assert y[0, 0, 0] == lo and np.isfinite(y).all()
+    assert y[0, 0, 1] < 0
+    for a in (np.float32(M * 2.0 ** -129), np.float32(1e-40), np.float32(2.0 ** -149)):
+        x = np.array([[[a, -a / 2, 0.0, -0.0]]], np.float32)
+        y, sc, cd = oracle.qdq_groups(x, 4, mode, with_codes=True)
+        assert sc[0, 0] == 0.0
+        assert not y.any() and np.isfinite(y).all()
+        if mode == "e4m3":
+            assert list(cd[0, 0]) == [0x00, 0x80, 0x00, 0x80]
+            assert list(np.signbit(y[0, 0])) == [False, True, False, True]
+        else:
+            assert not cd.any()
+
+
 @pytest.mark.gpu
 def test_reciprocal_reading_matches_torch_cuda_scalar_division():
     """The pages' 'rounded reciprocal multiplication as Torch scalar division':
