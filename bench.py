@@ -244,11 +244,38 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _strip_comments(src):
+    """C/C++/CUDA source without its comments and blank lines (string and
+    character literals kept), so that a comment edit leaves the hash alone."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    lines = [ln.rstrip() for ln in "".join(out).splitlines()]
+    return "\n".join(ln for ln in lines if ln)
+
+
 def _source_hash(files):
+    """Hash of the kernel sources' code (comments excluded) that a committed
+    ncu summary was taken on."""
     h = hashlib.sha256()
     for f in files:
-        with open(os.path.join(ROOT, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, f), encoding="utf-8") as fh:
+            h.update(_strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -18,11 +18,11 @@
 //     carries the fp32 state gradient dH in registers through the chunks and
 //     stores the dH' entering every chunk (bf16) in the workspace.  It needs no
 //     solve: only P, K, Q, dO and the saved W^.
-//  2. a chunk-parallel kernel, one CTA per (chunk, value head, value block),
-//     recomputes the chunk-local quantities and produces every gradient; the
-//     two value-block halves add their (disjoint-column) contributions to
-//     dq/dk/dbeta/dg with exactly two atomic adds per element onto zero, which
-//     is order independent, so results are deterministic.
+//  2. a chunk-parallel kernel, one CTA per (chunk, value head) covering both
+//     64-wide value blocks, reads the tile images the forward saved (T,
+//     Gamma o KK^T, P, each block's Delta) and produces every gradient; the
+//     value blocks' contributions are summed on chip, so each output element
+//     has one writer and a fixed summation order (deterministic, no atomics).
 // Gradients tolerate bf16 operands (no hi/lo splits): the backward has no
 // quantization decision to preserve.
 #define GDN_WGEMM_UNROLL2  // see wgemm
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const __grid_
 
 
 // ===========================================================================
-// Phase 2: all gradients of one chunk, per (chunk slot, value head, value block).
+// Phase 2: all gradients of one chunk, per (chunk slot, value head).
 // ===========================================================================
 template <int DK>
 struct ChunkSmem {

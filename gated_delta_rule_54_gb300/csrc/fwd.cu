@@ -19,12 +19,13 @@
 //      saved context) and U (fp32, parked in the output buffer o).
 //   2. gdn_fwd_state_kernel, one CTA per (sequence, value head, 64-wide value
 //      block) walks its chunks in order with the fp32 state tile in registers;
-//      per chunk only the state QDQ (codes to the context), Delta and the state
-//      update remain on the serial path, with the next chunk's operands
-//      prefetched by cp.async.
+//      per chunk only the state QDQ (codes to the context), Delta = U - W^ H^
+//      (stored over U in o) and the state update remain on the serial path,
+//      with the next chunk's operands prefetched by TMA on an mbarrier.
 //   3. gdn_fwd_output_kernel, one CTA per (chunk, value head, value block), all
-//      in parallel: QK^T, Delta = U - W^ H^ again from the saved codes, and O,
-//      written over U.
+//      in parallel: QK^T, then O from H^ (the saved codes) and Delta (read
+//      from o), written over Delta; it also saves P and Delta as bf16 tile
+//      images for the backward.
 // Contractions run on tensor cores (mma.sync bf16, fp32 accumulation).
 // Operands that are not exactly bf16 (T diag(.), Delta, the decayed Delta, P,
 // and unquantized W / H) are split into hi + lo bf16 halves so the state path
