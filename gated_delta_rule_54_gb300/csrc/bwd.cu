@@ -775,8 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
     float r0, r1;
     row_sums<NTW>(kw, r0, r1);
     racc_add_rows(racc, R_KW + ch, wrow0, gq, tq, r0, r1);
-    // attention side: dQ += Gm K, dK += Gm^T Q
-    wgemm<NTW, false, true, 64, DK>(dQ, Gmb, wrow0, Ks, wcol0, 0, 64, lane);
+    // attention side: dK += Gm^T Q (dQ += Gm K runs with the dKK product at the end)
     wgemm<NTW, true, true, 64, DK>(dK, Gmb, wrow0, Qs, wcol0, 0, 64, lane);
   }
   __syncthreads();  // dT complete; P no longer read (its tile becomes X)
@@ -859,25 +858,31 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
       }
   }
   {
-    // dA = -acc (strictly lower): dKK = dA beta_i Gamma_ij; dbeta += dA GKK; AA = dA A
+    // dA = -acc (strictly lower): dKK = dA beta_i Gamma_ij; dbeta += dA GKK; AA = dA A.
+    // dK takes dKK K + dKK^T K = (dKK + dKK^T) K: the strictly lower dKK and its
+    // transpose fill disjoint halves of one symmetric tile, written once each.
     float ba[2][4], aa[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-        float kk[2];
         const float2 gv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(GKKb + swz<64>(i, j)));
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
           const int jj = j + e;
           const float da = (jj < i) ? -acc[nt][2 * e2 + e] : 0.f;
           const float gkk = e == 0 ? gv.x : gv.y;
-          kk[e] = da * bet[i] * ((jj < i) ? __expf(gam[i] - gam[jj]) : 0.f);
           ba[nt][2 * e2 + e] = da * gkk;
           aa[nt][2 * e2 + e] = da * bet[i] * gkk;  // A = diag(beta) (Gamma o KK^T), strictly lower
+          if (jj < i) {
+            const __nv_bfloat16 kk = __float2bfloat16(da * bet[i] * __expf(gam[i] - gam[jj]));
+            dKKb[swz<64>(i, jj)] = kk;
+            dKKb[swz<64>(jj, i)] = kk;
+          } else if (jj == i) {
+            dKKb[swz<64>(i, i)] = __float2bfloat16(0.f);
+          }
         }
-        st_bf16x2(dKKb + swz<64>(i, j), kk[0], kk[1]);
       }
     float r0, r1;
     row_sums<2>(ba, r0, r1);
@@ -893,9 +898,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
         for (int e = 0; e < 2; ++e) racc[(R_AAC + rt) * 64 + col0 + nt * 8 + 2 * tq + e] += cs[nt][e];
   }
   __syncthreads();
-  // dK += dKK K + dKK^T K
-  wgemm<NTW, false, true, 64, DK>(dK, dKKb, wrow0, Ks, wcol0, 0, 64, lane);
-  wgemm<NTW, true, true, 64, DK>(dK, dKKb, wrow0, Ks, wcol0, 0, 64, lane);
+  // dQ += Gm K and dK += (dKK + dKK^T) K share their K fragments
+  wgemm_shared_b<NTW, false, true, 64, DK>(dQ, dK, Gmb, dKKb, wrow0, Ks, wcol0, 0, 64, lane);
 
   // ---- dgamma -> dg (reverse cumsum), dbeta (warps 0-1, fixed-order sums) ----
   if (warp < 2) {
