@@ -22,10 +22,10 @@
 //      per chunk only the state QDQ (codes to the context), Delta = U - W^ H^
 //      (stored over U in o) and the state update remain on the serial path,
 //      with the next chunk's operands prefetched by TMA on an mbarrier.
-//   3. gdn_fwd_output_kernel, one CTA per (chunk, value head, value block), all
-//      in parallel: QK^T, then O from H^ (the saved codes) and Delta (read
-//      from o), written over Delta; it also saves P and Delta as bf16 tile
-//      images for the backward.
+//   3. gdn_fwd_output_kernel, one CTA per (chunk, value head), all in
+//      parallel: QK^T once, then per value block O from H^ (the saved codes)
+//      and Delta (read from o), written over Delta; it also saves P and Delta
+//      as bf16 tile images for the backward.
 // Contractions run on tensor cores (mma.sync bf16, fp32 accumulation).
 // Operands that are not exactly bf16 (T diag(.), Delta, the decayed Delta, P,
 // and unquantized W / H) are split into hi + lo bf16 halves so the state path
@@ -908,26 +908,31 @@ __global__ void __launch_bounds__(kStateThreads, 1) gdn_fwd_state_kernel(const _
 
 // ===========================================================================
 // 3. Output: O = scale (diag(e^gamma) Q H^ + P Delta); Delta = U - W^ H^ as the
-//    state scan left it in o.
+//    state scan left it in o.  One CTA per (chunk, value head): P = QK^T once,
+//    then the value blocks in turn, the next block's Delta arriving by TMA
+//    while the current one is multiplied.
 // ===========================================================================
 constexpr int kOutThreads = 256;
 
 template <int DK, int SM, int WM>
 struct OutSmem {
-  static constexpr int Q = 0;                                              // bf16 [64][DK] (TMA)
-  static constexpr int K = Q + kChunk * DK * 2;                            // bf16 [64][DK] (TMA); later Delta hi, lo
-  static constexpr int U = K + kChunk * DK * 2;                            // f32 Delta [64][64] swz_f32 (TMA); later O
-  static constexpr int P = U + kChunk * 64 * 4;                            // P hi, lo; first the H codes (TMA)
-  static constexpr int HC = P + 2 * kChunk * 64 * 2;                       // H^ [DK][64] (hi, lo)
-  static constexpr int CV = HC + (SM == GDN_QDQ_NONE ? 2 : 1) * DK * 64 * 2;      // chunk vectors
+  static constexpr bool QUANT = SM != GDN_QDQ_NONE;
+  static constexpr int Q = 0;                                  // bf16 [64][DK] (TMA)
+  static constexpr int K = Q + kChunk * DK * 2;                // bf16 [64][DK] (TMA); later Delta hi, lo
+  static constexpr int U = K + kChunk * DK * 2;                // f32 Delta [64][64] swz_f32 (TMA), per block
+  static constexpr int P = U + kChunk * 64 * 4;                // P hi, lo
+  static constexpr int HC = P + 2 * kChunk * 64 * 2;           // H^ of one block [DK][64] (hi, lo)
+  static constexpr int HR = HC + (QUANT ? 1 : 2) * DK * 64 * 2;  // u8 H codes, both blocks (TMA)
+  static constexpr int CV = HR + (QUANT ? 2 * DK * 64 : 0);    // chunk vectors
   // Delta hi, lo [64][64]: in the dead K tile when it is large enough
   static constexpr bool D_IN_K = 2 * kChunk * 64 * 2 <= kChunk * DK * 2;
   static constexpr int D = D_IN_K ? K : CV + kCvecFloats * 4;
   static constexpr int END = D_IN_K ? CV + kCvecFloats * 4 : D + 2 * kChunk * 64 * 2;
   static constexpr int BYTES = END + 1024;  // + alignment slack
   static_assert((K % 1024) == 0 && (U % 1024) == 0 && (P % 1024) == 0 &&
-                    (HC % 128) == 0 && (D % 128) == 0,
+                    (HC % 128) == 0 && (HR % 128) == 0 && (CV % 16) == 0 && (D % 128) == 0,
                 "alignment");
+  static_assert(2 * (BYTES + 2048) <= 233472, "two CTAs per SM (with static and reserved shared memory)");
 };
 
 template <int DK, int SM, int WM>
@@ -938,10 +943,8 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
   __shared__ __align__(8) uint64_t bar;
 
   const int nvb = p.Dv / 64;
-  const int vb = blockIdx.x % nvb;
-  const int64_t sh = blockIdx.x / nvb;
-  const int64_t slot = sh / p.Hv;
-  const int h = (int)(sh % p.Hv);
+  const int64_t slot = blockIdx.x / p.Hv;
+  const int h = (int)(blockIdx.x % p.Hv);
   ChunkRef cr;
   if (!chunk_of_slot(p, slot, cr)) return;
   const int hk = h / p.G;
@@ -955,46 +958,22 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
   __nv_bfloat16* HcH = reinterpret_cast<__nv_bfloat16*>(sm + S::HC);
   __nv_bfloat16* HcL = HcH + DK * 64;
   float* Us = reinterpret_cast<float*>(sm + S::U);
-  float* Ost = Us;
   __nv_bfloat16* PH = reinterpret_cast<__nv_bfloat16*>(sm + S::P);
   __nv_bfloat16* PL = PH + kChunk * 64;
   __nv_bfloat16* DH = reinterpret_cast<__nv_bfloat16*>(sm + S::D);
   __nv_bfloat16* DL = DH + kChunk * 64;
+  uint8_t* Hraw = sm + S::HR;  // [nvb][DK][64] state codes
   float* Cv = reinterpret_cast<float*>(sm + S::CV);
   const float* gam = Cv + kCvGam;
   const float* eg = Cv + kCvEg;
-  // H codes land in the P tile (free until the P epilogue)
-  uint8_t* Hraw = reinterpret_cast<uint8_t*>(PH);
 
-  // ---- loads: TMA boxes on one mbarrier; fp32 H (state site off) by the threads ----
-  if (threadIdx.x == 0) {
-    mbar_init(&bar, 1);
-    fence_mbar_init();
-    const uint32_t bytes = 2 * kChunk * DK * 2 + kChunk * 64 * 4 + kCvecFloats * 4 +
-                           (SM != GDN_QDQ_NONE ? DK * 64 : 0);
-    mbar_expect_tx(&bar, bytes);
-    bulk_load_1d(Cv, p.cvec + (slot * p.Hv + h) * kCvecFloats, kCvecFloats * 4, &bar);
-#pragma unroll
-    for (int pn = 0; pn < DK / 64; ++pn) {
-      tma_load_2d(Qs + pn * kChunk * 64, &p.tm_q, hk * DK + pn * 64, (int)tok0, &bar);
-      tma_load_2d(Ks + pn * kChunk * 64, &p.tm_k, hk * DK + pn * 64, (int)tok0, &bar);
-    }
+  auto load_u = [&](int vb) {  // by thread 0
 #pragma unroll
     for (int pn = 0; pn < 2; ++pn)
       tma_load_2d(Us + pn * kChunk * 32, &p.tm_u, h * p.Dv + vb * 64 + pn * 32, (int)tok0, &bar);
-    if constexpr (SM != GDN_QDQ_NONE)
-      tma_load_2d(Hraw, &p.tm_hc, vb * 64, (int)((slot * p.Hv + h) * DK), &bar);
-  }
-  // state scales of this warp's two 16-column groups (each inside one
-  // state-scale tile: tiles are 16-aligned and at least 16 wide); scales are
-  // [slot, Hv, Dv / block_v]
-  float sHa = 1.f, sHb = 1.f;
-  if constexpr (SM != GDN_QDQ_NONE) {
-    const int64_t sb = (slot * p.Hv + h) * (p.Dv >> p.bv_log2);
-    const int c = vb * 64 + (warp >> 2) * 32;
-    sHa = p.h_scales[sb + (c >> p.bv_log2)];
-    sHb = p.h_scales[sb + ((c + 16) >> p.bv_log2)];
-  } else {
+  };
+  // fp32 H of one block (state site off) -> hi, lo bf16 halves
+  auto split_h_full = [&](int vb) {
     const float* src = p.h_full + ((slot * p.Hv + h) * DK) * p.Dv + vb * 64;
     for (int i = threadIdx.x; i < DK * 16; i += kOutThreads) {
       const int d = i >> 4, c4 = i & 15;
@@ -1008,7 +987,28 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
       *reinterpret_cast<uint2*>(HcH + e) = make_uint2(pack_bf16(h0v, h1v), pack_bf16(h2v, h3v));
       *reinterpret_cast<uint2*>(HcL + e) = make_uint2(pack_bf16(l0v, l1v), pack_bf16(l2v, l3v));
     }
+  };
+
+  // ---- loads: TMA boxes on one mbarrier (phase 0: everything but the later
+  //      blocks' Delta; phase vb: block vb's Delta) ----
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+    const uint32_t bytes = 2 * kChunk * DK * 2 + kChunk * 64 * 4 + kCvecFloats * 4 +
+                           (S::QUANT ? nvb * DK * 64 : 0);
+    mbar_expect_tx(&bar, bytes);
+    bulk_load_1d(Cv, p.cvec + (slot * p.Hv + h) * kCvecFloats, kCvecFloats * 4, &bar);
+#pragma unroll
+    for (int pn = 0; pn < DK / 64; ++pn) {
+      tma_load_2d(Qs + pn * kChunk * 64, &p.tm_q, hk * DK + pn * 64, (int)tok0, &bar);
+      tma_load_2d(Ks + pn * kChunk * 64, &p.tm_k, hk * DK + pn * 64, (int)tok0, &bar);
+    }
+    load_u(0);
+    if constexpr (S::QUANT)
+      for (int b = 0; b < nvb; ++b)
+        tma_load_2d(Hraw + b * DK * 64, &p.tm_hc, b * 64, (int)((slot * p.Hv + h) * DK), &bar);
   }
+  if constexpr (!S::QUANT) split_h_full(0);
   __syncthreads();  // the mbarrier is initialised before anyone waits on it
   const bool ok = mbar_wait(&bar, 0);
   if (__syncthreads_or(!ok)) {
@@ -1019,69 +1019,103 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
     return;
   }
 
-  // codes -> bf16 values (exact)
-  if constexpr (SM != GDN_QDQ_NONE) {
-    for (int i = threadIdx.x; i < DK * 16; i += kOutThreads) {
-      const int d = i >> 4, c4 = i & 15;
-      const float4 v = qdq_code4_values<SM>(*reinterpret_cast<const uint32_t*>(Hraw + d * 64 + c4 * 4));
-      *reinterpret_cast<uint2*>(HcH + swz<64>(d, c4 * 4)) =
-          make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
-    }
-  }
-  __syncthreads();  // H^ operand ready; the P tile is free again
-
   // warp tile: rows 16 rt .. +15, columns 32 ch .. +31.  Rows >= L of Q and K
   // hold another sequence's tokens: they only reach P entries outside the
   // causal mask or output rows that are not stored.
   const int rt = warp & 3, ch = warp >> 2;
   const int row0 = rt * 16, col0 = ch * 32;
   const bool p_tile = col0 <= row0 + 15;
-  float pacc[4][4], qacc[4][4];
+  float pacc[4][4];
   zero_acc(pacc);
-  zero_acc(qacc);
   if (p_tile) wgemm<4, false, false, DK, DK>(pacc, Qs, row0, Ks, col0, 0, DK, lane);
-  wgemm<4, false, true, DK, 64>(qacc, Qs, row0, HcH, col0, 0, DK, lane);
-  if constexpr (SM == GDN_QDQ_NONE) wgemm<4, false, true, DK, 64>(qacc, Qs, row0, HcL, col0, 0, DK, lane);
-  __syncthreads();  // K reads done (its tile becomes Delta)
 
-  // value block 0 also saves P (bf16; rows >= L zero) as the backward's tile
-  // image, and every block its Delta (the hi half: Delta rounded to bf16)
-  __nv_bfloat16* pimg = vb == 0 ? p.pb + (slot * p.Hv + h) * (kTileImgBytes / 2) : nullptr;
-  __nv_bfloat16* dimg = p.db + ((slot * p.Hv + h) * nvb + vb) * (kTileImgBytes / 2);
-#pragma unroll
-  for (int nt = 0; nt < 4; ++nt) {
-#pragma unroll
-    for (int e2 = 0; e2 < 2; ++e2) {
-      const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
-      float h0v, l0v, h1v, l1v;
-      if (p_tile) {
-        const float gi = gam[i];
-        const float p0 = (j <= i) ? expf(gi - gam[j]) * pacc[nt][2 * e2] : 0.f;
-        const float p1 = (j + 1 <= i) ? expf(gi - gam[j + 1]) * pacc[nt][2 * e2 + 1] : 0.f;
-        split_bf16(p0, h0v, l0v);
-        split_bf16(p1, h1v, l1v);
-        st_bf16x2(PH + swz<64>(i, j), h0v, h1v);
-        st_bf16x2(PL + swz<64>(i, j), l0v, l1v);
-        if (pimg) st_bf16x2(pimg + swz<64>(i, j), i < L ? p0 : 0.f, i < L ? p1 : 0.f);
-      } else if (pimg) {
-        st_bf16x2(pimg + swz<64>(i, j), 0.f, 0.f);
+  for (int vb = 0; vb < nvb; ++vb) {
+    if (vb > 0) {
+      const bool okb = mbar_wait(&bar, (uint32_t)vb & 1u);
+      if (__syncthreads_or(!okb)) {
+        if (threadIdx.x == 0) {
+          atomicOr(&g_fwd_device_error, 1);
+          mbar_wait(&bar, (uint32_t)vb & 1u);
+        }
+        return;
       }
-      float2 dl = *reinterpret_cast<const float2*>(Us + swz_f32(i, j));
-      if (i >= L) dl = make_float2(0.f, 0.f);  // rows of another sequence
-      split_bf16(dl.x, h0v, l0v);
-      split_bf16(dl.y, h1v, l1v);
-      st_bf16x2(DH + swz<64>(i, j), h0v, h1v);
-      st_bf16x2(DL + swz<64>(i, j), l0v, l1v);
-      st_bf16x2(dimg + swz<64>(i, j), h0v, h1v);
     }
-  }
-  __syncthreads();  // P, Delta ready; the Delta tile from o is read (it becomes the O staging)
+    // codes -> bf16 values (exact); fp32 H split (state site off)
+    if constexpr (S::QUANT) {
+      const uint8_t* hr = Hraw + vb * DK * 64;
+      for (int i = threadIdx.x; i < DK * 16; i += kOutThreads) {
+        const int d = i >> 4, c4 = i & 15;
+        const float4 v = qdq_code4_values<SM>(*reinterpret_cast<const uint32_t*>(hr + d * 64 + c4 * 4));
+        *reinterpret_cast<uint2*>(HcH + swz<64>(d, c4 * 4)) =
+            make_uint2(pack_bf16(v.x, v.y), pack_bf16(v.z, v.w));
+      }
+    } else if (vb > 0) {
+      split_h_full(vb);
+    }
+    __syncthreads();  // H^ operand ready; the P product has read K (its tile becomes Delta)
 
-  {
+    // state scales of this warp's two 16-column groups (each inside one
+    // state-scale tile: tiles are 16-aligned and at least 16 wide); scales are
+    // [slot, Hv, Dv / block_v]
+    float sHa = 1.f, sHb = 1.f;
+    if constexpr (S::QUANT) {
+      const int64_t sb = (slot * p.Hv + h) * (p.Dv >> p.bv_log2);
+      const int c = vb * 64 + col0;
+      sHa = p.h_scales[sb + (c >> p.bv_log2)];
+      sHb = p.h_scales[sb + ((c + 16) >> p.bv_log2)];
+    }
+    float qacc[4][4];
+    zero_acc(qacc);
+    wgemm<4, false, true, DK, 64>(qacc, Qs, row0, HcH, col0, 0, DK, lane);
+    if constexpr (!S::QUANT) wgemm<4, false, true, DK, 64>(qacc, Qs, row0, HcL, col0, 0, DK, lane);
+
+    // block 0 saves P (bf16; rows >= L zero) as the backward's tile image, and
+    // every block its Delta (the hi half: Delta rounded to bf16)
+    __nv_bfloat16* pimg = vb == 0 ? p.pb + (slot * p.Hv + h) * (kTileImgBytes / 2) : nullptr;
+    __nv_bfloat16* dimg = p.db + ((slot * p.Hv + h) * nvb + vb) * (kTileImgBytes / 2);
+#pragma unroll
+    for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+      for (int e2 = 0; e2 < 2; ++e2) {
+        const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
+        float h0v, l0v, h1v, l1v;
+        if (vb == 0) {
+          if (p_tile) {
+            const float gi = gam[i];
+            const float p0 = (j <= i) ? expf(gi - gam[j]) * pacc[nt][2 * e2] : 0.f;
+            const float p1 = (j + 1 <= i) ? expf(gi - gam[j + 1]) * pacc[nt][2 * e2 + 1] : 0.f;
+            split_bf16(p0, h0v, l0v);
+            split_bf16(p1, h1v, l1v);
+            st_bf16x2(PH + swz<64>(i, j), h0v, h1v);
+            st_bf16x2(PL + swz<64>(i, j), l0v, l1v);
+            st_bf16x2(pimg + swz<64>(i, j), i < L ? p0 : 0.f, i < L ? p1 : 0.f);
+          } else {
+            st_bf16x2(pimg + swz<64>(i, j), 0.f, 0.f);
+          }
+        }
+        float2 dl = *reinterpret_cast<const float2*>(Us + swz_f32(i, j));
+        if (i >= L) dl = make_float2(0.f, 0.f);  // rows of another sequence
+        split_bf16(dl.x, h0v, l0v);
+        split_bf16(dl.y, h1v, l1v);
+        st_bf16x2(DH + swz<64>(i, j), h0v, h1v);
+        st_bf16x2(DL + swz<64>(i, j), l0v, l1v);
+        st_bf16x2(dimg + swz<64>(i, j), h0v, h1v);
+      }
+    }
+    // P, Delta ready; this block's Delta tile and H^ are read: the next block's
+    // Delta may land in the Delta tile (reads by the generic proxy, then TMA)
+    fence_proxy_async();
+    __syncthreads();
+    if (threadIdx.x == 0 && vb + 1 < nvb) {
+      mbar_expect_tx(&bar, kChunk * 64 * 4);
+      load_u(vb + 1);
+    }
+
     float o2[4][4];
     zero_acc(o2);
     const int kend = row0 + 16;  // P is lower triangular: columns j <= i only
     wgemm_split3<4, false, true, 64, 64>(o2, PH, PL, row0, DH, DL, col0, 0, kend, lane);
+    // O straight from the accumulators: each lane quad covers 32 contiguous bytes of a row
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
@@ -1089,29 +1123,13 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
         const float sq = nt < 2 ? sHa : sHb;
         const float ei = eg[i] * sq;
-        *reinterpret_cast<float2*>(Ost + swz_f32(i, j)) =
-            make_float2(p.scale * (ei * qacc[nt][2 * e2] + o2[nt][2 * e2]),
-                        p.scale * (ei * qacc[nt][2 * e2 + 1] + o2[nt][2 * e2 + 1]));
+        if (i < L)
+          *reinterpret_cast<float2*>(p.o + ((tok0 + i) * p.Hv + h) * p.Dv + vb * 64 + j) =
+              make_float2(p.scale * (ei * qacc[nt][2 * e2] + o2[nt][2 * e2]),
+                          p.scale * (ei * qacc[nt][2 * e2 + 1] + o2[nt][2 * e2 + 1]));
       }
-  }
-  if (L == kChunk) {
-    // a full chunk leaves as two TMA boxes (rows past the tensor end are clipped)
-    fence_proxy_async();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-#pragma unroll
-      for (int pn = 0; pn < 2; ++pn)
-        tma_store_2d(&p.tm_u, h * p.Dv + vb * 64 + pn * 32, (int)tok0, Ost + pn * kChunk * 32);
-      tma_store_commit();
-      tma_store_wait_read();
-    }
-  } else {
-    __syncthreads();
-    for (int i = threadIdx.x; i < L * 16; i += kOutThreads) {
-      const int r = i >> 4, c4 = i & 15;
-      *reinterpret_cast<float4*>(p.o + ((tok0 + r) * p.Hv + h) * p.Dv + vb * 64 + c4 * 4) =
-          *reinterpret_cast<const float4*>(Ost + swz_f32(r, c4 * 4));
-    }
+    // the next block's H^ conversion and Delta split wait at its first barrier
+    // for every warp to finish this block's products (they read H^, Delta hi/lo)
   }
 }
 
@@ -1174,7 +1192,7 @@ gdn_status launch_t(const FwdParams& prm, const Dims& d, cudaStream_t st) {
   if (d.B * d.T > 0 && d.n_slots > 0) {
     auto k3 = gdn_fwd_output_kernel<DK, SM, WM>;
     if (set_smem(k3, OutSmem<DK, SM, WM>::BYTES) != GDN_OK) return GDN_ERR_CUDA;
-    k3<<<(unsigned)(d.n_slots * d.Hv * nvb), kOutThreads, OutSmem<DK, SM, WM>::BYTES, st>>>(prm);
+    k3<<<(unsigned)(d.n_slots * d.Hv), kOutThreads, OutSmem<DK, SM, WM>::BYTES, st>>>(prm);
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
   }
   return GDN_OK;
