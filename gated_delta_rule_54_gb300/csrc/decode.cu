@@ -6,21 +6,23 @@
 //     S^ = Q(S);  H = exp(g) S^ + beta k (v - exp(g) S^^T k)^T;
 //     o = scale H^T q (pre) or scale Q(H)^T q (post);  S <- H.
 //
-// One CTA owns one (row, value head) state, Dk x Dv fp32 (<= 64 KB), held in
-// registers for all the call's tokens: the state is read from HBM once and
-// written once per call, so the step is bound by HBM traffic.  512 threads;
-// thread (rg, cq) holds columns 4cq..4cq+3 of rows rg, rg + RG, ... (a warp
-// load covers whole 512-byte rows, coalesced).  Column dot products reduce
-// across the RG row groups through shared memory; tile maxima reduce with
-// shuffles inside a warp and shared memory across warps.
+// One CTA owns the W columns of one (row, value head) state, Dk x W fp32 (<=
+// 64 KB), held in registers for all the call's tokens: the state is read from
+// HBM once and written once per call, so the step is bound by HBM traffic.
+// Every column's update and readout involve only that column (and the
+// [Dk, block_v] tile it belongs to), so with block_v <= 64 a 128-wide state is
+// split into two 64-column CTAs of 256 threads: four CTAs per SM keep more
+// state loads in flight while others compute.  Thread (rg, cq) holds columns
+// 4cq..4cq+3 of rows rg, rg + RG, ... (a warp load covers whole rows of the
+// block, coalesced).  Column dot products reduce across the RG row groups
+// through shared memory; tile maxima reduce with shuffles inside a warp and
+// shared memory across warps.
 #include "common.cuh"
 
 namespace gdn {
 
 namespace {
 
-constexpr int kDecThreads = 512;
-constexpr int kDecWarps = kDecThreads / 32;
 
 struct DecodeParams {
   const __nv_bfloat16 *q, *k, *v;
@@ -63,8 +65,8 @@ __device__ __forceinline__ float4 qdq4(float4 x, float s, float r, bool zero, ui
 }
 
 // Per-tile amax of the CTA's state.  Every thread returns the amax of the
-// [Dk, block_v] tile its columns fall in.  amx: shared [kDecWarps][8].
-template <int C4>
+// [Dk, block_v] tile its columns fall in.  amx: shared [NW][8].
+template <int C4, int NW>
 __device__ __forceinline__ float tile_amax(float m, int block_v, int lane, int warp, int tile,
                                            float (*amx)[8]) {
   // lanes of one tile and one row group differ in the low log2(block_v/4) bits
@@ -76,14 +78,14 @@ __device__ __forceinline__ float tile_amax(float m, int block_v, int lane, int w
   __syncthreads();
   float a = amx[0][tile];
 #pragma unroll
-  for (int w = 1; w < kDecWarps; ++w) a = fmaxf(a, amx[w][tile]);
+  for (int w = 1; w < NW; ++w) a = fmaxf(a, amx[w][tile]);
   return a;
 }
 
 // Column sums over all rows of per-thread partials p (4 columns), returned
-// to every thread for its own columns.  red: shared [kDecWarps][DV].
-template <int C4, int DV>
-__device__ __forceinline__ float4 column_sum(float4 p, int lane, int warp, float (*red)[DV],
+// to every thread for its own columns.  red: shared [NW][W].
+template <int C4, int W, int NW>
+__device__ __forceinline__ float4 column_sum(float4 p, int lane, int warp, float (*red)[W],
                                              bool all_threads) {
   if constexpr (C4 < 32) {
     p.x += __shfl_xor_sync(0xffffffffu, p.x, C4);
@@ -97,7 +99,7 @@ __device__ __forceinline__ float4 column_sum(float4 p, int lane, int warp, float
   float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
   if (all_threads) {
 #pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) {
+    for (int w = 0; w < NW; ++w) {
       const float4 x = *reinterpret_cast<const float4*>(&red[w][cq * 4]);
       s.x += x.x;
       s.y += x.y;
@@ -108,30 +110,34 @@ __device__ __forceinline__ float4 column_sum(float4 p, int lane, int warp, float
   return s;
 }
 
-template <int DK, int DV, int MODE, bool POST>
-__global__ void __launch_bounds__(kDecThreads, 2) gdn_decode_kernel(const DecodeParams p) {
-  constexpr int C4 = DV / 4;              // column quads
-  constexpr int RG = kDecThreads / C4;    // row groups
+// DV: the state's value width (row stride); W: the CTA's columns (DV, or 64
+// with blockIdx.z the 64-column block); NT: threads.
+template <int DK, int DV, int W, int NT, int MODE, bool POST>
+__global__ void __launch_bounds__(NT, 1024 / NT) gdn_decode_kernel(const DecodeParams p) {
+  constexpr int NW = NT / 32;             // warps
+  constexpr int C4 = W / 4;               // column quads
+  constexpr int RG = NT / C4;             // row groups
   constexpr int RPT = DK / RG;            // rows per thread
   constexpr bool QUANT = MODE != GDN_QDQ_NONE;
-  static_assert(RPT >= 1 && DK % RG == 0, "layout");
+  static_assert(RPT >= 1 && DK % RG == 0 && DK <= NT, "layout");
 
-  __shared__ __align__(16) float red[2][kDecWarps][DV];
-  __shared__ float amx[2][kDecWarps][8];
+  __shared__ __align__(16) float red[2][NW][W];
+  __shared__ float amx[2][NW][8];
   __shared__ float ks[DK], qs[DK];
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int cq = tid % C4, rg = tid / C4;
   const int h = blockIdx.x;
   const int64_t b = blockIdx.y;
+  const int c0 = (int)blockIdx.z * W + cq * 4;  // this thread's first column
   const int hk = h / (p.Hv / p.Hk);
-  const int tile = (cq * 4) / p.block_v;
+  const int tile = c0 / p.block_v;
   const int64_t sbase = (b * p.Hv + h) * (int64_t)DK * DV;
 
   float4 S[RPT];
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
-    const int64_t e = sbase + (int64_t)(rg + RG * i) * DV + cq * 4;
+    const int64_t e = sbase + (int64_t)(rg + RG * i) * DV + c0;
     S[i] = p.state_in ? __ldg(reinterpret_cast<const float4*>(p.state_in + e))
                       : make_float4(0.f, 0.f, 0.f, 0.f);
   }
@@ -147,7 +153,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) gdn_decode_kernel(const Decode
       k_nx = p.k[(tk * p.Hk + hk) * DK + tid];
       q_nx = p.q[(tk * p.Hk + hk) * DK + tid];
     }
-    v_nx = *reinterpret_cast<const uint2*>(p.v + (tk * p.Hv + h) * DV + cq * 4);
+    v_nx = *reinterpret_cast<const uint2*>(p.v + (tk * p.Hv + h) * DV + c0);
     beta_nx = p.beta[tk * p.Hv + h];
     g_nx = p.g[tk * p.Hv + h];
   };
@@ -172,7 +178,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) gdn_decode_kernel(const Decode
         float m = 0.f;
 #pragma unroll
         for (int i = 0; i < RPT; ++i) m = fmaxf(m, max_abs4(S[i]));
-        a_c = tile_amax<C4>(m, p.block_v, lane, warp, tile, amx[0]);
+        a_c = tile_amax<C4, NW>(m, p.block_v, lane, warp, tile, amx[0]);
         qdq_scale<MODE>(a_c, s_c, r_c);
       }
       const bool zero = a_c == 0.f;
@@ -181,11 +187,11 @@ __global__ void __launch_bounds__(kDecThreads, 2) gdn_decode_kernel(const Decode
         uint32_t c4;
         S[i] = qdq4<MODE>(S[i], s_c, r_c, zero, c4);
         if (p.codes) {
-          const int64_t e = ((tk * p.Hv + h) * DK + rg + RG * i) * DV + cq * 4;
+          const int64_t e = ((tk * p.Hv + h) * DK + rg + RG * i) * DV + c0;
           *reinterpret_cast<uint32_t*>(p.codes + e) = c4;
         }
       }
-      if (p.scales && rg == 0 && (cq * 4) % p.block_v == 0)
+      if (p.scales && rg == 0 && c0 % p.block_v == 0)
         p.scales[(tk * p.Hv + h) * (DV / p.block_v) + tile] = s_c;
     }
     __syncthreads();  // ks, qs visible; amx[0] reads done
@@ -201,7 +207,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) gdn_decode_kernel(const Decode
       S[i].w *= a;
       part = f4_fma(ks[rg + RG * i], S[i], part);
     }
-    const float4 kS = column_sum<C4, DV>(part, lane, warp, red[0], true);
+    const float4 kS = column_sum<C4, W, NW>(part, lane, warp, red[0], true);
     const float2 v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vraw.x));
     const float2 v23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vraw.y));
     const float4 u = make_float4(v01.x - kS.x, v01.y - kS.y, v23.x - kS.z, v23.y - kS.w);
@@ -214,7 +220,7 @@ __global__ void __launch_bounds__(kDecThreads, 2) gdn_decode_kernel(const Decode
       float m = 0.f;
 #pragma unroll
       for (int i = 0; i < RPT; ++i) m = fmaxf(m, max_abs4(S[i]));
-      a_c = tile_amax<C4>(m, p.block_v, lane, warp, tile, amx[1]);
+      a_c = tile_amax<C4, NW>(m, p.block_v, lane, warp, tile, amx[1]);
       qdq_scale<MODE>(a_c, s_c, r_c);
       cached = true;
       const bool zero = a_c == 0.f;
@@ -227,25 +233,33 @@ __global__ void __launch_bounds__(kDecThreads, 2) gdn_decode_kernel(const Decode
 #pragma unroll
       for (int i = 0; i < RPT; ++i) part = f4_fma(qs[rg + RG * i], S[i], part);
     }
-    const float4 os = column_sum<C4, DV>(part, lane, warp, red[1], rg == 0);
+    const float4 os = column_sum<C4, W, NW>(part, lane, warp, red[1], rg == 0);
     if (rg == 0) {
       const float sc = p.scale;
-      *reinterpret_cast<float4*>(p.o + (tk * p.Hv + h) * DV + cq * 4) =
+      *reinterpret_cast<float4*>(p.o + (tk * p.Hv + h) * DV + c0) =
           make_float4(sc * os.x, sc * os.y, sc * os.z, sc * os.w);
     }
   }
 
 #pragma unroll
   for (int i = 0; i < RPT; ++i) {
-    const int64_t e = sbase + (int64_t)(rg + RG * i) * DV + cq * 4;
+    const int64_t e = sbase + (int64_t)(rg + RG * i) * DV + c0;
     *reinterpret_cast<float4*>(p.state_out + e) = S[i];
   }
 }
 
 template <int DK, int DV, int MODE, bool POST>
 gdn_status launch_t(const DecodeParams& prm, cudaStream_t st) {
-  const dim3 grid((unsigned)prm.Hv, (unsigned)prm.B);
-  gdn_decode_kernel<DK, DV, MODE, POST><<<grid, kDecThreads, 0, st>>>(prm);
+  if constexpr (DV == 128) {
+    if (prm.block_v <= 64) {
+      // two 64-column CTAs of 256 threads per state (every scale tile inside one)
+      const dim3 grid((unsigned)prm.Hv, (unsigned)prm.B, 2u);
+      gdn_decode_kernel<DK, DV, 64, 256, MODE, POST><<<grid, 256, 0, st>>>(prm);
+      return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    }
+  }
+  const dim3 grid((unsigned)prm.Hv, (unsigned)prm.B, 1u);
+  gdn_decode_kernel<DK, DV, DV, 512, MODE, POST><<<grid, 512, 0, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
