@@ -244,10 +244,18 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const __grid_
     if (__syncthreads_or(!ok)) {
       if (threadIdx.x == 0) {
         atomicOr(&g_bwd_device_error, 1);
-        mbar_wait(&bars[buf], (uint32_t)(it >> 1) & 1u);  // once more, bounded, for the copies in flight
+        // once more, bounded, for the copies in flight: this chunk's, and at the
+        // first chunk the second one's (every later prefetch follows this barrier)
+        mbar_wait(&bars[buf], (uint32_t)(it >> 1) & 1u);
+        if (it == 0 && nch > 1) mbar_wait(&bars[1], 0u);
       }
       return;
     }
+    // every thread has left the previous chunk's buffer (the barrier above):
+    // the next chunk's operands go there
+    if (it >= 1 && it + 1 < nch)
+      scan_load<DK, WM>(p, sm, buf ^ 1, &bars[buf ^ 1], si.tok0 + (int64_t)(c - 1) * kChunk, hk,
+                        h, vb, si.slot0 + c - 1);
 
     // current dH (gradient w.r.t. the state after this chunk) -> bf16 tile
 #pragma unroll
@@ -293,7 +301,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const __grid_
       const float er = r < Lc ? eg[r] : 0.f;  // rows past the chunk end contribute nothing
       st_bf16x2(EdO + swz<64>(r, col), er * __bfloat162float(v2.x), er * __bfloat162float(v2.y));
     }
-    __syncthreads();
+    // (no barrier: the dDelta products read dH, K, P and dO, none written above;
+    // e^gamma dO is read after the next barrier)
 
     // dDelta = scale P^T dO + dec_i (K dH)
     {
@@ -328,10 +337,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const __grid_
         for (int e = 0; e < 4; ++e)
           dH[nt][e] = p.scale * a1[nt][e] + egL * dH[nt][e] - sW * a2[nt][e];
     }
-    __syncthreads();  // buffer buf is no longer read
-    if (it + 2 < nch)
-      scan_load<DK, WM>(p, sm, buf, &bars[buf], si.tok0 + (int64_t)(c - 2) * kChunk, hk, h, vb,
-                        si.slot0 + c - 2);
+    // the next chunk's first barrier orders these reads of dDelta, W^, e^gamma dO
+    // and this buffer before their next writes
   }
   if (p.dh0) {
     float* dst = p.dh0 + (((int64_t)n * p.Hv + h) * DK) * p.Dv + vb * 64;
