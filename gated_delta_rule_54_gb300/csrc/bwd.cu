@@ -33,8 +33,9 @@ namespace gdn {
 
 namespace {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 512;  // the reverse scan
 constexpr int kWarps = kThreads / 32;
+constexpr int kChunkWarps = 8;   // the chunk kernel (8 measured a little faster than 16)
 
 struct BwdParams {
   CUtensorMap tm_k, tm_q, tm_do, tm_wc;  // the scan's per-chunk operands (TMA)
@@ -97,11 +98,11 @@ __device__ __forceinline__ SeqInfo seq_info(const BwdParams& p, int n) {
 
 // rows [0, L) of a [64][RL] bf16 tile from a token-major tensor with row
 // stride `stride` elements; rows >= L zero-filled.
-template <int RL>
+template <int RL, int NTHR>
 __device__ __forceinline__ void load_rows_bf16(__nv_bfloat16* dst, const __nv_bfloat16* src,
                                                int64_t stride, int L) {
   constexpr int CPR = RL / 8;
-  for (int i = threadIdx.x; i < kChunk * CPR; i += kThreads) {
+  for (int i = threadIdx.x; i < kChunk * CPR; i += NTHR) {
     const int r = i / CPR, c = i % CPR;
     const bool ok = r < L;
     cp_async16(smem_u32(dst + swz<RL>(r, c * 8)), src + (ok ? r : 0) * stride + c * 8, ok ? 16 : 0);
@@ -109,8 +110,9 @@ __device__ __forceinline__ void load_rows_bf16(__nv_bfloat16* dst, const __nv_bf
 }
 
 // a contiguous block of `bytes` (multiple of 16) into shared memory
+template <int NTHR>
 __device__ __forceinline__ void load_block(void* dst, const void* src, int bytes) {
-  for (int i = threadIdx.x; i < bytes / 16; i += kThreads)
+  for (int i = threadIdx.x; i < bytes / 16; i += NTHR)
     cp_async16(smem_u32(static_cast<unsigned char*>(dst) + 16 * i),
                static_cast<const unsigned char*>(src) + 16 * i, 16);
 }
@@ -448,8 +450,15 @@ __device__ __forceinline__ void racc_add_rows(float* racc, int slot, int row0, i
 // per block and are summed on chip; T^T dW, Gm K, Gm^T Q, X = T^T dT, dA and
 // dKK run once; every output element has one writer.
 template <int DK, int SM, int WM>
-__global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid_constant__ BwdParams p) {
+__global__ void __launch_bounds__(kChunkWarps * 32, 1) gdn_bwd_chunk_kernel(const __grid_constant__ BwdParams p) {
   using S = ChunkSmem<DK>;
+  constexpr int kCT = kChunkWarps * 32, kCW = kChunkWarps;
+  // warp tiles: 16 rows (four row quarters) by 64 / CG columns of a [64 x 64]
+  // product (NT n-tiles) or DK / CG of a [64 x DK] one (NTW n-tiles)
+  constexpr int CG = kCW / 4;
+  constexpr int NT = 8 / CG;
+  constexpr int NTW = DK / (8 * CG);
+  static_assert(kCW == 8 || kCW == 16, "warp count");
   extern __shared__ __align__(1024) unsigned char sm[];
   const int64_t slot = blockIdx.x;
   const int h = blockIdx.y;
@@ -457,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
   const int nvb = p.Dv / 64;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
-  const int rt = warp & 3, ch = warp >> 2;   // row quarter, column quarter
+  const int rt = warp & 3, ch = warp >> 2;   // row quarter, column group
 
   // chunk slot -> (sequence, chunk)
   int n, c;
@@ -503,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
   const float* bet = cvs + kCvBet;
   const float* beg = cvs + kCvBeg;
   float* racc = reinterpret_cast<float*>(sm + S::RACC);
-  float* hd_part = racc + S::kSlots * 64;  // [kWarps] <H^, dH'> partials, then [2] sums of t_i
+  float* hd_part = racc + S::kSlots * 64;  // [kCW] <H^, dH'> partials, then [2] sums of t_i
 
   // ---- loads.  Group A feeds the block-0 dequantization, group B the
   //      block-0 products, group C is block 1; T, Gamma o KK^T, P, each
@@ -511,35 +520,35 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
   auto load_block_vb = [&](int b) {
     const __nv_bfloat16* src = p.ws_dh + ((slot * p.Hv + h) * DK) * p.Dv + b * 64;
     __nv_bfloat16* dst = dHpb(b);
-    for (int i = threadIdx.x; i < DK * 8; i += kThreads) {
+    for (int i = threadIdx.x; i < DK * 8; i += kCT) {
       const int d = i >> 3, c8 = i & 7;
       cp_async16(smem_u32(dst + swz<64>(d, c8 * 8)), src + (int64_t)d * p.Dv + c8 * 8, 16);
     }
     if constexpr (SM != GDN_QDQ_NONE) {
       const uint8_t* hs = p.h_codes + ((slot * p.Hv + h) * DK) * p.Dv + b * 64;
       uint8_t* hd = hcb(b);
-      for (int i = threadIdx.x; i < DK * 4; i += kThreads) {
+      for (int i = threadIdx.x; i < DK * 4; i += kCT) {
         const int d = i >> 2, c16 = i & 3;
         cp_async16(smem_u32(hd + d * 64 + c16 * 16), hs + (int64_t)d * p.Dv + c16 * 16, 16);
       }
     }
   };
   auto load_vo = [&](int b) {
-    load_rows_bf16<64>(Vb(b), p.v + (ctok * p.Hv + h) * p.Dv + b * 64, (int64_t)p.Hv * p.Dv, Lc);
-    load_rows_bf16<64>(dOb(b), p.dO + (ctok * p.Hv + h) * p.Dv + b * 64, (int64_t)p.Hv * p.Dv, Lc);
-    load_block(DbOf(b), p.db + ((slot * p.Hv + h) * nvb + b) * (kTileImgBytes / 2), kTileImgBytes);
+    load_rows_bf16<64, kCT>(Vb(b), p.v + (ctok * p.Hv + h) * p.Dv + b * 64, (int64_t)p.Hv * p.Dv, Lc);
+    load_rows_bf16<64, kCT>(dOb(b), p.dO + (ctok * p.Hv + h) * p.Dv + b * 64, (int64_t)p.Hv * p.Dv, Lc);
+    load_block<kCT>(DbOf(b), p.db + ((slot * p.Hv + h) * nvb + b) * (kTileImgBytes / 2), kTileImgBytes);
   };
   {
     const int64_t img = (slot * p.Hv + h) * (kTileImgBytes / 2);
-    load_block(sm + S::VEC, p.cvec + (slot * p.Hv + h) * kCvecFloats, kCvecFloats * 4);
-    load_block(Tb, p.tb + img, kTileImgBytes);
+    load_block<kCT>(sm + S::VEC, p.cvec + (slot * p.Hv + h) * kCvecFloats, kCvecFloats * 4);
+    load_block<kCT>(Tb, p.tb + img, kTileImgBytes);
     load_block_vb(0);
     cp_async_commit();  // group A
-    load_rows_bf16<DK>(Ks, p.k + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
-    load_rows_bf16<DK>(Qs, p.q + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
+    load_rows_bf16<DK, kCT>(Ks, p.k + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
+    load_rows_bf16<DK, kCT>(Qs, p.q + (ctok * p.Hk + hk) * DK, (int64_t)p.Hk * DK, Lc);
     load_vo(0);
-    load_block(GKKb, p.gkk + img, kTileImgBytes);
-    load_block(Pb, p.pb + img, kTileImgBytes);
+    load_block<kCT>(GKKb, p.gkk + img, kTileImgBytes);
+    load_block<kCT>(Pb, p.pb + img, kTileImgBytes);
     cp_async_commit();  // group B
     if (nvb > 1) {
       load_block_vb(1);
@@ -547,14 +556,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
     }
     cp_async_commit();  // group C
   }
-  for (int i = threadIdx.x; i < S::kSlots * 64 + kWarps + 2; i += kThreads) racc[i] = 0.f;
+  for (int i = threadIdx.x; i < S::kSlots * 64 + kCW + 2; i += kCT) racc[i] = 0.f;
   cp_async_wait<2>();
   __syncthreads();  // group A and the zeroed partial sums visible to all threads
 
-  constexpr int NTW = DK / 32;
-  const int wrow0 = rt * 16, wcol0 = ch * (DK / 4);
-  const int row0 = rt * 16, col0 = ch * 16;
-  float dQ[NTW][4], dK[NTW][4], dWa[NTW][4], gma[2][4], dta[2][4];
+  const int wrow0 = rt * 16, wcol0 = ch * (DK / CG);
+  const int row0 = rt * 16, col0 = ch * (64 / CG);
+  float dQ[NTW][4], dK[NTW][4], dWa[NTW][4], gma[NT][4], dta[NT][4];
   zero_acc(dQ);
   zero_acc(dK);
   zero_acc(dWa);
@@ -570,13 +578,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
     {
       const uint8_t* hst = hcb(vb);
       float hd = 0.f;
-      // this thread's four columns (fixed: kThreads is a multiple of 16) lie in one state-scale tile
-      static_assert(kThreads % 16 == 0, "column of a thread");
+      // this thread's four columns (fixed: kCT is a multiple of 16) lie in one state-scale tile
+      static_assert(kCT % 16 == 0, "column of a thread");
       float sH = 1.f;
       if constexpr (SM != GDN_QDQ_NONE)
         sH = p.h_scales[(slot * p.Hv + h) * (p.Dv >> p.bv_log2) +
                         ((vb * 64 + (threadIdx.x & 15) * 4) >> p.bv_log2)];
-      for (int e = threadIdx.x; e < DK * 16; e += kThreads) {
+      for (int e = threadIdx.x; e < DK * 16; e += kCT) {
         const int d = e >> 4, col = (e & 15) * 4;
         float4 x;
         if constexpr (SM != GDN_QDQ_NONE) {
@@ -603,13 +611,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
 
     // ---- dDelta = scale P^T dO + dec (K dH') ----
     {
-      float a1[2][4], a2[2][4];
+      float a1[NT][4], a2[NT][4];
       zero_acc(a1);
       zero_acc(a2);
-      wgemm<2, true, true, 64, 64>(a1, Pb, row0, dOs, col0, row0, 64, lane);
-      wgemm<2, false, true, DK, 64>(a2, Ks, row0, dHp, col0, 0, DK, lane);
+      wgemm<NT, true, true, 64, 64>(a1, Pb, row0, dOs, col0, row0, 64, lane);
+      wgemm<NT, false, true, DK, 64>(a2, Ks, row0, dHp, col0, 0, DK, lane);
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -622,17 +630,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
 
     // ---- output-side products of this block ----
     // dO Delta^T (for dP) and dO H^T (for dQ_inter) share their dO fragments
-    float dp[2][4], ohq[NTW][4];
+    float dp[NT][4], ohq[NTW][4];
     zero_acc(dp);
     zero_acc(ohq);
-    static_assert(NTW == 2 || NTW == 4, "warp tile");
-    wgemm_shared_a<2, NTW, false, false, false, 64, 64, 64>(dp, ohq, dOs, row0, Dv, col0, Hh, wcol0,
+    static_assert(NT % 2 == 0 && NTW % 2 == 0, "n tiles come in pairs");
+    wgemm_shared_a<NT, NTW, false, false, false, 64, 64, 64>(dp, ohq, dOs, row0, Dv, col0, Hh, wcol0,
                                                             0, 64, lane);
     {
       // dP = lower-incl(scale dO Delta^T); Gm += dP Gamma; PP = dP P
-      float pp[2][4];
+      float pp[NT][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -647,13 +655,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
           }
         }
       float r0, r1;
-      row_sums<2>(pp, r0, r1);
+      row_sums<NT>(pp, r0, r1);
       racc_add_rows(racc, R_PPR + ch, row0, gq, tq, r0, r1);
-      float cs[2][2];
-      col_sums<2>(pp, cs);
+      float cs[NT][2];
+      col_sums<NT>(pp, cs);
       if (gq == 0)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e = 0; e < 2; ++e) racc[(R_PPC + rt) * 64 + col0 + nt * 8 + 2 * tq + e] += cs[nt][e];
     }
@@ -703,16 +711,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
     }
     // dW += -dDelta H^T (STE: = dW^) and the dT part dDelta V^T (summed over the
     // blocks) share their dDelta fragments
-    wgemm_shared_a<NTW, 2, false, false, false, 64, 64, 64>(dWa, dta, dDb, wrow0, Hh, wcol0, Vs,
+    wgemm_shared_a<NTW, NT, false, false, false, 64, 64, 64>(dWa, dta, dDb, wrow0, Hh, wcol0, Vs,
                                                             col0, 0, 64, lane);
     {
       // T^T dDelta -> dV and its row sums
-      float tu[2][4];
+      float tu[NT][4];
       zero_acc(tu);
-      wgemm<2, true, true, 64, 64>(tu, Tb, row0, dDb, col0, 0, 64, lane);
-      float bv[2][4];
+      wgemm<NT, true, true, 64, 64>(tu, Tb, row0, dDb, col0, 0, 64, lane);
+      float bv[NT][4];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e2 = 0; e2 < 2; ++e2) {
           const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -724,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
                 make_float2(bet[i] * tu[nt][2 * e2], bet[i] * tu[nt][2 * e2 + 1]);
         }
       float r0, r1;
-      row_sums<2>(bv, r0, r1);
+      row_sums<NT>(bv, r0, r1);
       racc_add_rows(racc, R_BU + ch, row0, gq, tq, r0, r1);
     }
     if (vb + 1 < nvb) cp_async_wait<0>();  // the next block's loads (group C)
@@ -740,7 +748,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
       st_bf16x2(dWb + swz<DK>(i, d), -dWa[nt][2 * e2], -dWa[nt][2 * e2 + 1]);
     }
 #pragma unroll
-  for (int nt = 0; nt < 2; ++nt)
+  for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
     for (int e2 = 0; e2 < 2; ++e2) {
       const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -750,11 +758,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
 
   {
     // dT = (dDelta V^T) diag(beta) + (dW K^T) diag(beta e^gamma)  -> dTb
-    float a2[2][4];
+    float a2[NT][4];
     zero_acc(a2);
-    wgemm<2, false, false, DK, DK>(a2, dWb, row0, Ks, col0, 0, DK, lane);
+    wgemm<NT, false, false, DK, DK>(a2, dWb, row0, Ks, col0, 0, DK, lane);
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -790,13 +798,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
   // or, for the Neumann polynomial T = sum_{i<=d} Xn^i (Xn = -A), Z_{d-1} of
   //   S_0 = I, Z_0 = dT;  S_m = I + Xn S_{m-1},  Z_m = dT S_m^T + Xn^T Z_{m-1}
   // (= sum_{a+b<=d-1} (Xn^T)^a dT (Xn^T)^b, the derivative of the polynomial).
-  float acc[2][4];
+  float acc[NT][4];
   zero_acc(acc);
   if (p.neumann < 0) {
     // X = T^T dT
-    wgemm<2, true, true, 64, 64>(acc, Tb, row0, dTb, col0, 0, 64, lane);
+    wgemm<NT, true, true, 64, 64>(acc, Tb, row0, dTb, col0, 0, 64, lane);
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -804,14 +812,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
       }
     __syncthreads();
     zero_acc(acc);
-    wgemm<2, false, false, 64, 64>(acc, Xb, row0, Tb, col0, 0, 64, lane);
+    wgemm<NT, false, false, 64, 64>(acc, Xb, row0, Tb, col0, 0, 64, lane);
   } else if (p.neumann >= 1) {
     // bf16 tiles in space the value blocks no longer need: Xn (P's tile), S and
     // Z in turn (Delta / dDelta, and the two V tiles); Z_0 is dT itself
     __nv_bfloat16* Xn = Xb;
     __nv_bfloat16* Sbuf[2] = {Db, dDb};
     __nv_bfloat16* Zbuf[2] = {Vb(0), Vb(1)};
-    for (int e = threadIdx.x; e < 64 * 32; e += kThreads) {
+    for (int e = threadIdx.x; e < 64 * 32; e += kCT) {
       const int i = e >> 5, j = (e & 31) * 2;
       const __nv_bfloat162 g2 = *reinterpret_cast<const __nv_bfloat162*>(GKKb + swz<64>(i, j));
       st_bf16x2(Xn + swz<64>(i, j), -bet[i] * __bfloat162float(g2.x), -bet[i] * __bfloat162float(g2.y));
@@ -824,11 +832,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
       __nv_bfloat16* Sn = Sbuf[m & 1];
       __nv_bfloat16* Zn = Zbuf[m & 1];
       {
-        float sa[2][4];
+        float sa[NT][4];
         zero_acc(sa);
-        wgemm<2, false, true, 64, 64>(sa, Xn, row0, Sp, col0, 0, 64, lane);
+        wgemm<NT, false, true, 64, 64>(sa, Xn, row0, Sp, col0, 0, 64, lane);
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -838,12 +846,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
       }
       __syncthreads();
       {
-        float za[2][4];
+        float za[NT][4];
         zero_acc(za);
-        wgemm<2, false, false, 64, 64>(za, dTb, row0, Sn, col0, 0, 64, lane);  // dT S^T
-        wgemm<2, true, true, 64, 64>(za, Xn, row0, Z, col0, 0, 64, lane);      // Xn^T Z
+        wgemm<NT, false, false, 64, 64>(za, dTb, row0, Sn, col0, 0, 64, lane);  // dT S^T
+        wgemm<NT, true, true, 64, 64>(za, Xn, row0, Z, col0, 0, 64, lane);      // Xn^T Z
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -855,7 +863,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
       Sp = Sn;
     }
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -868,9 +876,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
     // dA = -acc (strictly lower): dKK = dA beta_i Gamma_ij; dbeta += dA GKK; AA = dA A.
     // dK takes dKK K + dKK^T K = (dKK + dKK^T) K: the strictly lower dKK and its
     // transpose fill disjoint halves of one symmetric tile, written once each.
-    float ba[2][4], aa[2][4];
+    float ba[NT][4], aa[NT][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
@@ -892,15 +900,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
         }
       }
     float r0, r1;
-    row_sums<2>(ba, r0, r1);
+    row_sums<NT>(ba, r0, r1);
     racc_add_rows(racc, R_BA + ch, row0, gq, tq, r0, r1);
-    row_sums<2>(aa, r0, r1);
+    row_sums<NT>(aa, r0, r1);
     racc_add_rows(racc, R_AAR + ch, row0, gq, tq, r0, r1);
-    float cs[2][2];
-    col_sums<2>(aa, cs);
+    float cs[NT][2];
+    col_sums<NT>(aa, cs);
     if (gq == 0)
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e = 0; e < 2; ++e) racc[(R_AAC + rt) * 64 + col0 + nt * 8 + 2 * tq + e] += cs[nt][e];
   }
@@ -927,14 +935,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_kernel(const __grid
     __syncwarp();
     racc[i] = dgam;           // reuse slot 0 (fully consumed above by this thread only)
     racc[64 + i] = dbeta;
-    if (lane == 0) hd_part[kWarps + warp] = tsum;
+    if (lane == 0) hd_part[kCW + warp] = tsum;
   }
   __syncthreads();
   if (warp == 0) {
     float hd = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) hd += hd_part[w];
-    const float extra = eg[63] * hd + hd_part[kWarps] + hd_part[kWarps + 1];
+    for (int w = 0; w < kCW; ++w) hd += hd_part[w];
+    const float extra = eg[63] * hd + hd_part[kCW] + hd_part[kCW + 1];
     // reverse cumsum over rows 63..0 of dgamma (row 63 gets the gamma_L terms)
     const float x1 = racc[2 * lane + 1] + (lane == 31 ? extra : 0.f);
     const float x0 = racc[2 * lane];
@@ -1022,7 +1030,7 @@ gdn_status launch_bwd_t(const BwdParams& prm, const Dims& d, cudaStream_t st) {
   if (set_smem(k1, SS::BYTES) != GDN_OK || set_smem(k2, CS::BYTES) != GDN_OK) return GDN_ERR_CUDA;
   k1<<<dim3((unsigned)(d.Dv / 64), (unsigned)d.Hv, (unsigned)d.N), kThreads, SS::BYTES, st>>>(prm);
   if (d.B * d.T > 0 && d.n_slots > 0)
-    k2<<<dim3((unsigned)d.n_slots, (unsigned)d.Hv), kThreads, CS::BYTES, st>>>(prm);
+    k2<<<dim3((unsigned)d.n_slots, (unsigned)d.Hv), kChunkWarps * 32, CS::BYTES, st>>>(prm);
   if (prm.ws_dqk && d.B * d.T > 0) {
     const int64_t total = d.B * d.T * d.Hk * d.Dk;
     const int blocks = (int)((total + 255) / 256 < 152 * 16 ? (total + 255) / 256 : 152 * 16);
