@@ -25,7 +25,7 @@
 //     has one writer and a fixed summation order (deterministic, no atomics).
 // Gradients tolerate bf16 operands (no hi/lo splits): the backward has no
 // quantization decision to preserve.
-#define GDN_WGEMM_UNROLL2  // see wgemm
+#define GDN_WGEMM_UNROLL 4  // see wgemm
 #include "common.cuh"
 #include "launch.h"
 

@@ -380,13 +380,13 @@ namespace gdn {
 // (AT = true); B is stored [k][n] (BKN = true) or [n][k] (BKN = false).
 // RLA / RLB are the row lengths (elements) of the swizzled tiles.
 // ---------------------------------------------------------------------------
-// UNROLL = 2 unrolls the k loop by two (the next step's fragment loads then
-// issue ahead of the current step's MMAs).  The default is 1, or 2 in a
-// translation unit that defines GDN_WGEMM_UNROLL2 before including this
-// header: the backward kernels (16 warps, one CTA per SM) run 7 % faster
-// unrolled, the forward kernels choose per call site.
-#ifdef GDN_WGEMM_UNROLL2
-constexpr int kWgemmUnroll = 2;
+// UNROLL = 2 or 4 unrolls the k loop (the next steps' fragment loads then
+// issue ahead of the current step's MMAs).  The default is 1, or the value of
+// GDN_WGEMM_UNROLL in a translation unit that defines it before including this
+// header: the backward kernels run 7 % faster unrolled by two than not, and
+// 1 % faster again by four; the forward kernels choose per call site.
+#ifdef GDN_WGEMM_UNROLL
+constexpr int kWgemmUnroll = GDN_WGEMM_UNROLL;
 #else
 constexpr int kWgemmUnroll = 1;
 #endif
@@ -395,7 +395,7 @@ template <int NT, bool AT, bool BKN, int RLA, int RLB, int UNROLL = kWgemmUnroll
 __device__ __forceinline__ void wgemm(float (&acc)[NT][4], const __nv_bfloat16* A, int m0,
                                       const __nv_bfloat16* B, int n0, int k0, int k1, int lane) {
   static_assert(NT % 2 == 0, "n tiles come in pairs");
-  static_assert(UNROLL == 1 || UNROLL == 2, "unroll factor");
+  static_assert(UNROLL == 1 || UNROLL == 2 || UNROLL == 4, "unroll factor");
   auto step = [&](int k) {
     uint32_t a[4];
     if constexpr (AT)
@@ -413,7 +413,10 @@ __device__ __forceinline__ void wgemm(float (&acc)[NT][4], const __nv_bfloat16* 
       mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
     }
   };
-  if constexpr (UNROLL == 2) {
+  if constexpr (UNROLL == 4) {
+#pragma unroll 4
+    for (int k = k0; k < k1; k += 16) step(k);
+  } else if constexpr (UNROLL == 2) {
 #pragma unroll 2
     for (int k = k0; k < k1; k += 16) step(k);
   } else {
@@ -459,7 +462,10 @@ __device__ __forceinline__ void wgemm_shared_a(float (&acc1)[NT1][4], float (&ac
       mma_bf16(acc2[2 * np + 1], a, b[2], b[3]);
     }
   };
-  if constexpr (UNROLL == 2) {
+  if constexpr (UNROLL == 4) {
+#pragma unroll 4
+    for (int k = k0; k < k1; k += 16) step(k);
+  } else if constexpr (UNROLL == 2) {
 #pragma unroll 2
     for (int k = k0; k < k1; k += 16) step(k);
   } else {
@@ -499,7 +505,10 @@ __device__ __forceinline__ void wgemm_shared_b(float (&acc1)[NT][4], float (&acc
       mma_bf16(acc2[2 * np + 1], a2, b[2], b[3]);
     }
   };
-  if constexpr (UNROLL == 2) {
+  if constexpr (UNROLL == 4) {
+#pragma unroll 4
+    for (int k = k0; k < k1; k += 16) step(k);
+  } else if constexpr (UNROLL == 2) {
 #pragma unroll 2
     for (int k = k0; k < k1; k += 16) step(k);
   } else {
@@ -542,7 +551,10 @@ __device__ __forceinline__ void wgemm_split3(float (&acc)[NT][4], const __nv_bfl
       mma_bf16(acc[2 * np + 1], al, bh[2], bh[3]);
     }
   };
-  if constexpr (UNROLL == 2) {
+  if constexpr (UNROLL == 4) {
+#pragma unroll 4
+    for (int k = k0; k < k1; k += 16) step(k);
+  } else if constexpr (UNROLL == 2) {
 #pragma unroll 2
     for (int k = k0; k < k1; k += 16) step(k);
   } else {
