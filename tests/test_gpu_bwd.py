@@ -113,6 +113,8 @@ def test_bwd_dims_scale_and_no_dht():
     _check(w, scale=64 ** -0.5, with_dht=False)
     w = synth.small(B=1, T=140, Hk=1, Hv=1, Dk=128, Dv=64, h0=False, seed=25)
     _check(w)
+    w = synth.small(B=2, T=100, Hk=2, Hv=2, Dk=64, Dv=64, h0=True, seed=27)
+    _check(w)
 
 
 def test_bwd_deterministic():
