@@ -5,6 +5,7 @@ import os
 import re
 
 import pytest
+import torch
 
 from gated_delta_rule_54_gb300 import _lib
 from gated_delta_rule_54_gb300._lib import GdnProblem
@@ -222,3 +223,22 @@ def test_two_precision_entry_rejects_before_launch():
     # nothing to do: no sequences, or no tokens and no final state
     assert call(_tproblem(B=0, N=0), None, None, None, None, None, None, None, None, None) == 0
     assert call(_tproblem(T=0), None, None, None, None, None, None, None, None, None) == 0
+
+
+def test_no_host_fallback_for_cpu_tensors():
+    """Every compute entry point of the binding refuses host tensors: there is no
+    CPU path behind the library."""
+    from gated_delta_rule_54_gb300 import (gdn_chunk_fwd_qdq, gdn_decode_qdq, gdn_two_precision_fwd,
+                                           kda_recurrent_fwd_qdq, fake_qdq_e4m3, synth)
+    d = synth.make_inputs(synth.small(B=1, T=8, Hk=1, Hv=1, Dk=64, Dv=64, h0=True, seed=1))
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        gdn_chunk_fwd_qdq(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"])
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        gdn_decode_qdq(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"])
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        gdn_two_precision_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"])
+    gk = d["g"][..., None].expand(*d["g"].shape, 64).contiguous()
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        kda_recurrent_fwd_qdq(d["q"], d["k"], d["v"], d["beta"], gk, d["h0"])
+    with pytest.raises(ValueError, match="CUDA float32 tensor"):
+        fake_qdq_e4m3(torch.zeros(1, 4, 64), 64)
