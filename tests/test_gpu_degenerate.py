@@ -137,3 +137,32 @@ def test_two_precision_pure_decay_through_the_scale_threshold():
     late = o[:, 64:]
     assert not late.any() and not np.asarray(ro)[:, 64:].any()
     assert_close(o, ro, "two-precision o")
+
+
+@pytest.mark.parametrize("k", [-7, 3])
+def test_paths_scale_exactly_with_values_and_state(k):
+    """Every path is linear in (v, h0), its QDQ is equivariant under powers of
+    two (the scale and its reciprocal absorb them exactly), and W does not
+    involve v: scaling v and h0 by 2^k must scale every output by exactly 2^k,
+    bit for bit, in the kernels' own arithmetic."""
+    from gated_delta_rule_54_gb300 import (gdn_decode_qdq, gdn_two_precision_fwd,
+                                           kda_recurrent_fwd_qdq)
+    f = 2.0 ** k
+    w = synth.small(B=2, T=150, Hk=1, Hv=2, Dk=128, Dv=128, h0=True, seed=51)
+    d = to_dev(synth.make_kda_inputs(w))
+    q, kk, v, beta, g, gk, h0 = d["q"], d["k"], d["v"], d["beta"], d["g"], d["g_k"], d["h0"]
+    v2 = (v.float() * f).to(torch.bfloat16)
+    assert torch.equal(v2.float(), v.float() * f)
+    runs = [
+        lambda vv, hh: gdn_chunk_fwd_qdq(q, kk, vv, beta, g, hh, state_mode="e4m3", w_mode="e4m3")[:2],
+        lambda vv, hh: gdn_chunk_fwd_qdq(q, kk, vv, beta, g, hh, state_mode="int8", w_mode="e4m3")[:2],
+        lambda vv, hh: gdn_decode_qdq(q, kk, vv, beta, g, hh, state_mode="e4m3", readout="post"),
+        lambda vv, hh: kda_recurrent_fwd_qdq(q, kk, vv, beta, gk, hh, state_mode="e4m3"),
+        lambda vv, hh: gdn_two_precision_fwd(q, kk, vv, beta, g, hh, read_mode="e4m3", flush=16),
+    ]
+    for i, run in enumerate(runs):
+        a = run(v, h0)
+        b = run(v2, h0 * f)
+        torch.cuda.synchronize()
+        for x, y in zip(a, b):
+            assert torch.equal(y, x * f), (i, float((y - x * f).abs().max()))

@@ -311,3 +311,20 @@ def test_gradcheck_chunked_neumann():
         o, ht = chunked(*a, chunk=8, neumann_degree=3)
         return o.sum() + (ht * ht).sum()
     assert torch.autograd.gradcheck(f, xs, eps=1e-6, atol=1e-7, rtol=1e-6)
+
+
+@pytest.mark.parametrize("sm,wm", [("e4m3", "e4m3"), ("int8", "e4m3"), ("none", "none")])
+def test_chunked_scales_exactly_with_values_and_state(sm, wm):
+    """o and ht are linear in (v, h0) and the QDQ is equivariant under powers
+    of two (s and 1/s absorb them exactly), while W does not involve v: scaling
+    v and h0 by 2^k scales o and ht by exactly 2^k, bit for bit in fp64."""
+    w = synth.small(B=2, T=150, Hk=1, Hv=2, Dk=64, Dv=64, h0=True, seed=41)
+    d = synth.make_inputs(w)
+    o, ht = chunked(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], state_mode=sm, w_mode=wm)
+    for k in (-7, 3):
+        f = 2.0 ** k
+        v2 = (d["v"].float() * f).to(torch.bfloat16)
+        assert torch.equal(v2.float(), d["v"].float() * f)     # exact in bf16
+        o2, ht2 = chunked(d["q"], d["k"], v2, d["beta"], d["g"], d["h0"] * f, state_mode=sm,
+                          w_mode=wm)
+        assert torch.equal(o2, o * f) and torch.equal(ht2, ht * f)

@@ -204,6 +204,40 @@ def test_qdq_tiny_amax_threshold(mode, M):
             assert not cd.any()
 
 
+@pytest.mark.parametrize("mode", ["e4m3", "int8"])
+def test_qdq_odd_symmetry_and_monotone_within_a_group(mode):
+    """Both grids and their rounding are symmetric about zero and order
+    preserving: within a group (one scale) Q(-x) = -Q(x), and x <= y implies
+    Q(x) <= Q(y).  A rounding that leans one way, or a wrong sign or exponent
+    path, breaks one of the two."""
+    rng = np.random.default_rng(8)
+    x = (rng.standard_normal((6, 8, 64)) * np.exp(rng.uniform(-6, 6, (6, 1, 1)))).astype(np.float32)
+    y, sc = oracle.qdq_groups(x, 64, mode)
+    yn, scn = oracle.qdq_groups(-x, 64, mode)
+    assert np.array_equal(sc, scn)
+    assert np.array_equal(np.abs(yn), np.abs(y)) and np.all((yn == -y) | ((yn == 0) & (y == 0)))
+    for b in range(x.shape[0]):
+        order = np.argsort(x[b].ravel(), kind="stable")
+        assert np.all(np.diff(y[b].ravel()[order].astype(np.float64)) >= 0)
+
+
+@pytest.mark.parametrize("mode", ["e4m3", "int8"])
+def test_qdq_scale_invariance_by_powers_of_two(mode):
+    """Scaling a group by 2^k (inside the normal range of s) scales its scale
+    and every dequantized value by exactly 2^k: the codes depend on x / amax
+    only, and powers of two pass through fl(a / M), fl(1 / s) and the products
+    without rounding."""
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((4, 16, 32)).astype(np.float32)
+    y, sc, cd = oracle.qdq_groups(x, 32, mode, with_codes=True)
+    for k in (-20, -3, 5, 17):
+        xs = (x * np.float32(2.0 ** k)).astype(np.float32)
+        ys, scs, cds = oracle.qdq_groups(xs, 32, mode, with_codes=True)
+        assert np.array_equal(cds, cd)
+        assert np.array_equal(scs, (sc * np.float32(2.0 ** k)).astype(np.float32))
+        assert np.array_equal(ys, (y * np.float32(2.0 ** k)).astype(np.float32))
+
+
 @pytest.mark.gpu
 def test_reciprocal_reading_matches_torch_cuda_scalar_division():
     """The pages' 'rounded reciprocal multiplication as Torch scalar division':
