@@ -166,3 +166,26 @@ def test_paths_scale_exactly_with_values_and_state(k):
         torch.cuda.synchronize()
         for x, y in zip(a, b):
             assert torch.equal(y, x * f), (i, float((y - x * f).abs().max()))
+
+
+@pytest.mark.parametrize("sm,wm,hv", [("e4m3", "e4m3", 2), ("int8", "e4m3", 4)])
+def test_backward_scales_exactly_with_the_cotangents(sm, wm, hv):
+    """The STE backward is linear in the incoming gradients (dO, dht) and reuses
+    the forward's saved values: scaling both by 2^k scales every gradient by
+    exactly 2^k, bit for bit (grouped heads included)."""
+    from gated_delta_rule_54_gb300 import gdn_chunk_bwd_ste
+    w = synth.small(B=2, T=150, Hk=2, Hv=hv, Dk=128, Dv=128, h0=True, seed=52)
+    d = synth.make_inputs(w)
+    do, dht = _dO(w, d)
+    dd = to_dev(d)
+    o, ht, ctx = gdn_chunk_fwd_qdq(dd["q"], dd["k"], dd["v"], dd["beta"], dd["g"], dd["h0"],
+                                   state_mode=sm, w_mode=wm, save_ctx=True)
+    f = 2.0 ** -5
+    do2 = (do.float() * f).to(torch.bfloat16)
+    assert torch.equal(do2.float(), do.float() * f)
+    args = (dd["q"], dd["k"], dd["v"], dd["beta"], dd["g"], ctx)
+    a = gdn_chunk_bwd_ste(*args, do.cuda(), dht.cuda(), state_mode=sm, w_mode=wm)
+    b = gdn_chunk_bwd_ste(*args, do2.cuda(), (dht * f).cuda(), state_mode=sm, w_mode=wm)
+    torch.cuda.synchronize()
+    for name, x, y in zip(NAMES, a, b):
+        assert torch.equal(y, x * f), (name, float((y - x * f).abs().max()))
