@@ -189,3 +189,38 @@ def test_backward_scales_exactly_with_the_cotangents(sm, wm, hv):
     torch.cuda.synchronize()
     for name, x, y in zip(NAMES, a, b):
         assert torch.equal(y, x * f), (name, float((y - x * f).abs().max()))
+
+
+def test_packed_sequences_equal_separate_calls_bit_for_bit():
+    """Packing changes only where a sequence's rows sit: a packed batch must give
+    every sequence exactly the outputs, final state and gradients that a call on
+    that sequence alone gives (rows past a chunk's end hold the next sequence's
+    tokens in the packed call and nothing in the single one; both must be
+    masked out)."""
+    from gated_delta_rule_54_gb300 import gdn_chunk_bwd_ste
+    lengths = [70, 130, 64, 1]
+    w = synth.small(B=1, T=0, Hk=2, Hv=4, Dk=128, Dv=128, h0=True, seed=53)
+    d = synth.make_inputs(w, lengths=lengths)
+    dd = to_dev(d)
+    gen = torch.Generator().manual_seed(54)
+    do = torch.randn(d["v"].shape, generator=gen).to(torch.bfloat16).cuda()
+    dht = (torch.randn(d["h0"].shape, generator=gen) * 0.01).cuda()
+    o, ht, ctx = gdn_chunk_fwd_qdq(dd["q"], dd["k"], dd["v"], dd["beta"], dd["g"], dd["h0"],
+                                   cu_seqlens=dd["cu_seqlens"], save_ctx=True)
+    grads = gdn_chunk_bwd_ste(dd["q"], dd["k"], dd["v"], dd["beta"], dd["g"], ctx, do, dht,
+                              cu_seqlens=dd["cu_seqlens"])
+    torch.cuda.synchronize()
+    start = 0
+    for n, L in enumerate(lengths):
+        sl = lambda x: x[:, start:start + L].contiguous()
+        q, k, v, beta, g = (sl(dd[key]) for key in ("q", "k", "v", "beta", "g"))
+        h0 = dd["h0"][n:n + 1].contiguous()
+        o1, ht1, ctx1 = gdn_chunk_fwd_qdq(q, k, v, beta, g, h0, save_ctx=True)
+        g1 = gdn_chunk_bwd_ste(q, k, v, beta, g, ctx1, sl(do), dht[n:n + 1].contiguous())
+        torch.cuda.synchronize()
+        assert torch.equal(o1, o[:, start:start + L]), ("o", n)
+        assert torch.equal(ht1, ht[n:n + 1]), ("ht", n)
+        for name, a, b in zip(NAMES, g1, grads):
+            ref = b[n:n + 1] if name == "dh0" else b[:, start:start + L]
+            assert torch.equal(a, ref), (name, n, float((a - ref).abs().max()))
+        start += L
