@@ -156,3 +156,20 @@ def test_split_carry_prefill_then_decode(P, sm):
     o_d, S = decode(*post, ht.numpy(), state_mode=sm)
     assert _rel(o_d, ref_o[:, P:].numpy()) <= 1e-9
     assert _rel(S, ref_h.numpy()) <= 1e-9
+
+
+@pytest.mark.parametrize("sm,readout", [("e4m3", "post"), ("int8", "pre"), ("none", "pre")])
+def test_decode_scales_exactly_with_values_and_state(sm, readout):
+    """o and the carried state are linear in (v, state) and the QDQ absorbs
+    powers of two in s and 1/s: scaling both by 2^k scales o and the state by
+    exactly 2^k in fp64."""
+    d = _inputs(seed=61)
+    S0 = torch.randn(2, 2, 32, 128, generator=torch.Generator().manual_seed(62)) * 0.3
+    o, S = decode(d["q"], d["k"], d["v"], d["beta"], d["g"], S0, state_mode=sm, readout=readout)
+    for k in (-9, 4):
+        f = 2.0 ** k
+        v2 = (d["v"].float() * f).to(torch.bfloat16)
+        assert torch.equal(v2.float(), d["v"].float() * f)
+        o2, S2 = decode(d["q"], d["k"], v2, d["beta"], d["g"], S0 * f, state_mode=sm,
+                        readout=readout)
+        assert np.array_equal(o2, o * f) and np.array_equal(S2, S * f)

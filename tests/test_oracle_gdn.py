@@ -328,3 +328,22 @@ def test_chunked_scales_exactly_with_values_and_state(sm, wm):
         o2, ht2 = chunked(d["q"], d["k"], v2, d["beta"], d["g"], d["h0"] * f, state_mode=sm,
                           w_mode=wm)
         assert torch.equal(o2, o * f) and torch.equal(ht2, ht * f)
+
+
+@pytest.mark.parametrize("sm,wm", [("e4m3", "e4m3"), ("int8", "none")])
+def test_chunked_packed_equals_separate_calls(sm, wm):
+    """cu_seqlens only says where each sequence's rows sit: the packed call gives
+    every sequence exactly the outputs and final state of a call on that
+    sequence alone (chunks restart at every sequence start)."""
+    lengths = [70, 130, 64, 1]
+    w = synth.small(B=1, T=0, Hk=1, Hv=2, Dk=64, Dv=64, h0=True, seed=65)
+    d = synth.make_inputs(w, lengths=lengths)
+    o, ht = chunked(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"],
+                    cu_seqlens=d["cu_seqlens"], state_mode=sm, w_mode=wm)
+    start = 0
+    for n, L in enumerate(lengths):
+        sl = lambda x: x[:, start:start + L]
+        o1, ht1 = chunked(sl(d["q"]), sl(d["k"]), sl(d["v"]), sl(d["beta"]), sl(d["g"]),
+                          d["h0"][n:n + 1], state_mode=sm, w_mode=wm)
+        assert torch.equal(o1, o[:, start:start + L]) and torch.equal(ht1, ht[n:n + 1])
+        start += L

@@ -89,3 +89,20 @@ def test_zero_beta_is_per_channel_decay():
         ref = (np.exp(cum[t])[:, None] * H0).T @ q[0, t, 0].astype(np.float64)
         assert np.allclose(o[0, t, 0], ref, rtol=1e-12, atol=1e-13)
     assert np.allclose(ht[0, 0], np.exp(cum[-1])[:, None] * H0, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("sm", ["e4m3", "int8", "none"])
+def test_kda_scales_exactly_with_values_and_state(sm):
+    """Linear in (v, h0), with a QDQ that absorbs powers of two: scaling both by
+    2^k scales o and ht by exactly 2^k in fp64."""
+    w = synth.small(B=2, T=150, Hk=1, Hv=2, Dk=64, Dv=64, w_mode="none", h0=True, seed=63)
+    d = synth.make_kda_inputs(w)
+    o, ht = kda_recurrent(d["q"], d["k"], d["v"], d["beta"], d["g_k"], d["h0"], state_mode=sm)
+    for k in (-9, 4):
+        f = 2.0 ** k
+        v2 = (d["v"].float() * f).to(torch.bfloat16)
+        assert torch.equal(v2.float(), d["v"].float() * f)
+        o2, ht2 = kda_recurrent(d["q"], d["k"], v2, d["beta"], d["g_k"], d["h0"] * f,
+                                state_mode=sm)
+        assert np.array_equal(np.asarray(o2), np.asarray(o) * f)
+        assert np.array_equal(np.asarray(ht2), np.asarray(ht) * f)

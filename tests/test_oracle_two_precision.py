@@ -120,3 +120,20 @@ def test_packed_sequences_flush_from_their_own_start():
                                d["h0"][n:n + 1], flush=4)
         assert np.array_equal(o[:, a:b], on)
         assert np.array_equal(ht[n], hn[0])
+
+
+@pytest.mark.parametrize("rm", ["e4m3", "none"])
+def test_two_precision_scales_exactly_with_values_and_state(rm):
+    """Anchor and read copy are linear in (v, h0), and the read QDQ absorbs
+    powers of two: scaling both by 2^k scales o and ht by exactly 2^k in fp64."""
+    import torch
+    w = synth.small(B=2, T=70, Hk=1, Hv=2, Dk=128, Dv=64, w_mode="none", h0=True, seed=64)
+    d = synth.make_inputs(w)
+    o, ht = two_precision(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], read_mode=rm)
+    for k in (-9, 4):
+        f = 2.0 ** k
+        v2 = (d["v"].float() * f).to(torch.bfloat16)
+        assert torch.equal(v2.float(), d["v"].float() * f)
+        o2, ht2 = two_precision(d["q"], d["k"], v2, d["beta"], d["g"], d["h0"] * f, read_mode=rm)
+        assert np.array_equal(np.asarray(o2), np.asarray(o) * f)
+        assert np.array_equal(np.asarray(ht2), np.asarray(ht) * f)
