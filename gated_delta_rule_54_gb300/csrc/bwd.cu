@@ -387,7 +387,8 @@ struct ChunkSmem {
 };
 
 // racc slot indices (each a [64] row of partial sums; four slots per kind: one
-// per column quarter for row sums, one per row quarter for column sums).  Each
+// per warp column group for row sums (two or four in use, by the warp count),
+// one per row quarter for column sums).  Each
 // slot entry is owned by one thread, which adds the contributions of both
 // value blocks in a fixed order.
 enum : int {
