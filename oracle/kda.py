@@ -30,11 +30,13 @@ from . import _np, qdq_groups
 
 
 def kda_recurrent(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, state_mode="none",
-                  block_v=64, chunk=64):
+                  block_v=64, chunk=64, record=None):
     """q, k [B, T, Hk, Dk]; v [B, T, Hv, Dv]; beta [B, T, Hv]; g [B, T, Hv, Dk] (log decay per
     key channel); h0 [N, Hv, Dk, Dv] or None; cu_seqlens [N + 1] or None (then B rows).
 
-    Returns (o fp64 [B, T, Hv, Dv], ht fp64 [N, Hv, Dk, Dv])."""
+    Returns (o fp64 [B, T, Hv, Dv], ht fp64 [N, Hv, Dk, Dv]).  With a list as
+    ``record``, (sequence, token offset, state [Hv, Dk, Dv] before the
+    quantizer) is appended at every state QDQ; nothing else changes."""
     f64 = lambda x: np.asarray(_np(x), dtype=np.float32).astype(np.float64)
     q, k, v, beta, g = f64(q), f64(k), f64(v), f64(beta), f64(g)
     B, T, Hk, Dk = k.shape
@@ -53,6 +55,8 @@ def kda_recurrent(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, state_m
         H = h0[n].copy()                                            # [Hv, Dk, Dv]
         for t in range(t0, t1):
             if state_mode != "none" and (t - t0) % chunk == 0:
+                if record is not None:
+                    record.append((n, t - t0, H.copy()))
                 H = qdq_groups(H.astype(np.float32), block_v, state_mode)[0].astype(np.float64)
             kt = k[b, t][np.arange(Hv) // G]                         # [Hv, Dk]
             qt = q[b, t][np.arange(Hv) // G]

@@ -46,11 +46,13 @@ def read_copy(A, read_mode):
 
 
 def two_precision(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, read_mode="e4m3",
-                  flush=16):
+                  flush=16, record=None):
     """q, k [B, T, Hk, Dk]; v [B, T, Hv, Dv]; beta, g [B, T, Hv]; h0 [N, Hv, Dk, Dv] or None;
     cu_seqlens [N + 1] or None (then B rows).
 
-    Returns (o fp64 [B, T, Hv, Dv], ht fp64 [N, Hv, Dk, Dv])."""
+    Returns (o fp64 [B, T, Hv, Dv], ht fp64 [N, Hv, Dk, Dv]).  With a list as
+    ``record``, (sequence, token offset, anchor [Hv, Dk, Dv]) is appended at
+    every flush, before the read copy is taken; nothing else changes."""
     if flush < 1:
         raise ValueError("flush period must be >= 1")
     f64 = lambda x: np.asarray(_np(x), dtype=np.float32).astype(np.float64)
@@ -79,6 +81,8 @@ def two_precision(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, read_mo
         R = A
         for t in range(t0, t1):
             if (t - t0) % flush == 0:
+                if record is not None:
+                    record.append((n, t - t0, A.copy()))
                 R = read_copy(A, read_mode)
             kt, qt = k[b, t][heads], q[b, t][heads]
             a = np.exp(g[b, t])
