@@ -25,3 +25,16 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    try:
+        from _parity import ALLOWANCE_LOG
+    except Exception:  # pragma: no cover
+        return
+    if not ALLOWANCE_LOG:
+        return
+    tr = terminalreporter
+    tr.section("derived flip allowances (units with an allowance / units, max allowance / max|ref|)")
+    for test, what, n, total, mx in ALLOWANCE_LOG:
+        tr.write_line("%s  %-16s %5d / %-6d %.2e" % (test, what, n, total, mx))

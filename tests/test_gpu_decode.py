@@ -1,9 +1,10 @@
 """GPU parity of the decode QAT step (gdn_decode_qdq, through the C ABI)
 against the fp64 decode oracle, with the tolerances of the forward parity
-tests: codes within one step and at most 0.1% of them flipped, (row, head)
-units holding a flip held to 2^-3 of their max, all other units to 1e-2
-relative.  Scales agree to 1e-4 relative (the tile amax is computed from
-fp32 instead of fp64 state values)."""
+tests: codes within one step and at most 0.1% of them flipped; o and the
+carried state within 1e-2 relative, each element widened by its derived flip
+allowance (a differing code's step times its tile scale, carried through the
+token updates; tests/_parity.py).  Scales agree to 1e-4 relative (the tile
+amax is computed from fp32 instead of fp64 state values)."""
 import numpy as np
 import pytest
 import torch
@@ -12,7 +13,8 @@ from gated_delta_rule_54_gb300 import gdn_chunk_fwd_qdq, gdn_decode_qdq, synth
 from oracle.decode import decode
 from oracle.recurrent_torch import recurrent_torch
 
-from _parity import assert_close, assert_close_units, assert_codes, code_steps, to_dev
+from _parity import (assert_close, assert_codes, code_steps, decode_flip_allowance, log_allowance,
+                     to_dev)
 
 pytestmark = pytest.mark.gpu
 
@@ -31,25 +33,24 @@ def _check(d, sm, bv, readout, scale=1.0):
     s0 = d["h0"] if d["h0"] is not None else torch.zeros(S.shape)
     ro, rS, rc, rs = decode(d["q"], d["k"], d["v"], d["beta"], d["g"], s0, scale=scale,
                             state_mode=sm, block_v=bv, readout=readout, record=True)
-    B, T, Hv = d["B"], d["T"], d["v"].shape[2]
-    flipped = set()
+    T = d["T"]
+    flip = None
     if sm != "none" and T > 0:
         c = codes.cpu().numpy()
         assert_codes(c, rc, sm, "decode state codes")
-        assert np.allclose(scales.cpu().numpy(), rs, rtol=1e-4, atol=0)
-        diff = code_steps(c, rc, sm).reshape(B, T, Hv, -1).max(-1).max(1)      # [B, Hv]
-        flipped = {(int(b), int(h)) for b, h in zip(*np.nonzero(diff))}
+        flip = code_steps(c, rc, sm) > 0
+        # scales of states that no earlier flip reached
+        reached = np.cumsum(flip.any(axis=(3, 4)), axis=1) > 0
+        ok = ~np.concatenate([np.zeros_like(reached[:, :1]), reached[:, :-1]], 1)
+        assert np.allclose(scales.cpu().numpy()[ok], rs[ok], rtol=1e-4, atol=0)
     else:
         assert codes is None or codes.numel() == 0
-    key = lambda b, h: b * Hv + h
-    fl = {key(b, h) for b, h in flipped}
-    o_units = lambda shape: (np.arange(shape[0])[:, None, None, None] * Hv +
-                             np.arange(shape[2])[None, None, :, None]) + np.zeros(shape, int)
-    s_units = lambda shape: (np.arange(shape[0])[:, None, None, None] * Hv +
-                             np.arange(shape[1])[None, :, None, None]) + np.zeros(shape, int)
+    o_al, s_al = decode_flip_allowance(d, rc, rs, flip, rS, scale, bv, sm, readout)
     if o.numel():
-        assert_close_units(o.cpu().numpy(), ro, o_units, fl, "decode o")
-    assert_close_units(S.cpu().numpy(), rS, s_units, fl, "decode state")
+        log_allowance("decode o", o_al, ro, unit_axes=(0, 2))
+        assert_close(o.cpu().numpy(), ro, "decode o", allow=o_al)
+    log_allowance("decode state", s_al, rS, unit_axes=(0, 1))
+    assert_close(S.cpu().numpy(), rS, "decode state", allow=s_al)
     return o, S
 
 

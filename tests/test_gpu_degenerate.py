@@ -15,7 +15,7 @@ import torch
 
 from gated_delta_rule_54_gb300 import gdn_chunk_fwd_qdq, synth
 
-from _parity import GRAD_L2, assert_close, grad_rel_l2, to_dev
+from _parity import GRAD_L2, assert_close, grad_rel_l2, sequence_allowances, to_dev
 from test_gpu_bwd import NAMES, _dO, _grads_gpu, _grads_oracle
 from test_gpu_fwd import _check_case
 
@@ -111,10 +111,12 @@ def test_kda_pure_decay_through_the_scale_threshold(sm):
     o, ht = kda_recurrent_fwd_qdq(dd["q"], dd["k"], dd["v"], dd["beta"], dd["g_k"], dd["h0"],
                                   state_mode=sm)
     torch.cuda.synchronize()
-    ro, rh = kda_recurrent(d["q"], d["k"], d["v"], d["beta"], d["g_k"], d["h0"], state_mode=sm)
+    rec = []
+    ro, rh = kda_recurrent(d["q"], d["k"], d["v"], d["beta"], d["g_k"], d["h0"], state_mode=sm,
+                           record=rec)
     o, ht = o.cpu().numpy(), ht.cpu().numpy()
     assert np.isfinite(o).all() and not ht.any() and not np.asarray(rh).any()
-    kda_check(o, ht, ro, rh, sm)
+    kda_check(o, ht, ro, rh, sequence_allowances(d, rec, sm, 64, 1.0, g_key="g_k"))
 
 
 def test_two_precision_pure_decay_through_the_scale_threshold():

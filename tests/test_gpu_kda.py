@@ -1,11 +1,12 @@
 """GPU parity of the KDA recurrence (kda_recurrent_fwd_qdq, through the C ABI)
 against the fp64 KDA oracle.
 
-Without QDQ the kernel's fp32 recurrence is held to the forward's bounds
-(max |err| <= 1e-2 max|ref|, 99.9% of elements within 1e-2 relative).  With
-QDQ the kernel quantizes its own fp32 state, so a code can land one step away
-from the oracle's; as for the forward, a (sequence, head) unit is then held
-to 2^-3 of its max, and the 99.9% rule still covers the whole output."""
+The kernel's fp32 recurrence is held to the forward's bounds (max |err| <=
+1e-2 max|ref|, 99.9% of elements within 1e-2 relative), each element widened
+by its derived flip allowance: with QDQ the kernel quantizes its own fp32
+state, so a code whose oracle value lies within the kernels' error of a
+rounding boundary may land one step away; that step, times its tile scale, is
+carried through the recurrence (tests/_parity.py)."""
 import numpy as np
 import pytest
 import torch
@@ -13,7 +14,7 @@ import torch
 from gated_delta_rule_54_gb300 import kda_recurrent_fwd_qdq, synth
 from oracle.kda import kda_recurrent
 
-from _parity import FLIP_REL, assert_close, close_report, to_dev
+from _parity import assert_close, log_allowance, sequence_allowances, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -27,50 +28,41 @@ def _run(w, lengths=None, sm="e4m3", block_v=64, chunk=64, scale=1.0, h0=True):
                                   cu_seqlens=dd["cu_seqlens"], scale=scale, state_mode=sm,
                                   block_v=block_v, chunk=chunk)
     torch.cuda.synchronize()
+    rec = []
     ro, rh = kda_recurrent(d["q"], d["k"], d["v"], d["beta"], d["g_k"], d["h0"],
                            cu_seqlens=d["cu_seqlens"], scale=scale, state_mode=sm,
-                           block_v=block_v, chunk=chunk)
-    return d, o.cpu().numpy(), ht.cpu().numpy(), ro, rh
+                           block_v=block_v, chunk=chunk, record=rec)
+    al = sequence_allowances(d, rec, sm, block_v, scale, g_key="g_k")
+    return d, o.cpu().numpy(), ht.cpu().numpy(), ro, rh, al
 
 
-def _check(o, ht, ro, rh, sm):
-    if sm == "none":
-        assert_close(o, ro, "kda o")
-        assert_close(ht, rh, "kda ht")
-        return
-    r = close_report(o, ro)
-    assert r["finite"] and r["frac_bad"] <= 1e-3, r
-    for x, ref, what in ((o, ro, "o"), (ht, rh, "ht")):
-        # units: (token rows, value head) for o; (sequence, value head) for ht
-        if what == "o":
-            x = x.transpose(2, 0, 1, 3).reshape(x.shape[2], -1)
-            ref = ref.transpose(2, 0, 1, 3).reshape(ref.shape[2], -1)
-        else:
-            x = x.reshape(x.shape[0] * x.shape[1], -1)
-            ref = ref.reshape(ref.shape[0] * ref.shape[1], -1)
-        err = np.abs(x - ref).max(axis=1)
-        mx = np.abs(ref).max(axis=1)
-        assert np.all(err <= FLIP_REL * mx + 1e-30), (what, float((err / np.maximum(mx, 1e-30)).max()))
+def _check(o, ht, ro, rh, al):
+    o_al, ht_al = al
+    if o.size:
+        log_allowance("kda o", o_al, ro, unit_axes=(0, 2))
+        assert_close(o, ro, "kda o", allow=o_al)
+    log_allowance("kda ht", ht_al, rh, unit_axes=(0, 1))
+    assert_close(ht, rh, "kda ht", allow=ht_al)
 
 
 @pytest.mark.parametrize("sm", ["e4m3", "int8", "none"])
 @pytest.mark.parametrize("block_v", [16, 32, 64])
 def test_kda_modes_and_scale_widths(sm, block_v):
     w = synth.small(B=2, T=150, Hk=2, Hv=4, Dk=128, Dv=128, w_mode="none", h0=True, seed=block_v)
-    _check(*_run(w, sm=sm, block_v=block_v)[1:], sm)
+    _check(*_run(w, sm=sm, block_v=block_v)[1:])
 
 
 @pytest.mark.parametrize("T", [1, 63, 64, 65, 257])
 def test_kda_lengths(T):
     w = synth.small(B=2, T=T, Hk=1, Hv=2, Dk=64, Dv=64, w_mode="none", h0=True, seed=T)
-    _check(*_run(w, sm="int8")[1:], "int8")
+    _check(*_run(w, sm="int8")[1:])
 
 
 def test_kda_packed_grouped_no_h0_and_every_token_qdq():
     w = synth.small(B=1, T=0, Hk=2, Hv=4, Dk=128, Dv=64, w_mode="none", h0=True, seed=9)
-    _check(*_run(w, lengths=[0, 5, 130, 64, 77], sm="e4m3", scale=0.125)[1:], "e4m3")
+    _check(*_run(w, lengths=[0, 5, 130, 64, 77], sm="e4m3", scale=0.125)[1:])
     w = synth.small(B=2, T=40, Hk=1, Hv=1, Dk=64, Dv=128, w_mode="none", seed=10)
-    _check(*_run(w, sm="e4m3", chunk=1, h0=False)[1:], "e4m3")
+    _check(*_run(w, sm="e4m3", chunk=1, h0=False)[1:])
 
 
 def test_kda_channel_constant_decay_matches_gdn_forward():
@@ -101,6 +93,10 @@ def test_kda_full_workload_sampled():
     o, ht = o.cpu().numpy(), ht.cpu().numpy()
     for n, h in [(0, 0), (3, 15)]:
         sl = lambda x: x[n:n + 1, :, h:h + 1]
-        ro, rh = kda_recurrent(sl(d["q"]), sl(d["k"]), sl(d["v"]), sl(d["beta"]), sl(d["g_k"]),
-                               d["h0"][n:n + 1, h:h + 1], state_mode=w.state_mode)
-        _check(o[n:n + 1, :, h:h + 1], ht[n:n + 1, h:h + 1], ro, rh, w.state_mode)
+        sub = dict(q=sl(d["q"]), k=sl(d["k"]), v=sl(d["v"]), beta=sl(d["beta"]), g_k=sl(d["g_k"]),
+                   h0=d["h0"][n:n + 1, h:h + 1], cu_seqlens=None)
+        rec = []
+        ro, rh = kda_recurrent(sub["q"], sub["k"], sub["v"], sub["beta"], sub["g_k"], sub["h0"],
+                               state_mode=w.state_mode, record=rec)
+        al = sequence_allowances(sub, rec, w.state_mode, 64, 1.0, g_key="g_k")
+        _check(o[n:n + 1, :, h:h + 1], ht[n:n + 1, h:h + 1], ro, rh, al)
