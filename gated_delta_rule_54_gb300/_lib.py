@@ -34,7 +34,7 @@ class GdnProblem(ctypes.Structure):
         ("N", ctypes.c_int32), ("cu_seqlens", ctypes.c_void_p), ("scale", ctypes.c_float),
         ("state_mode", ctypes.c_int32), ("w_mode", ctypes.c_int32), ("block_v", ctypes.c_int32),
         ("chunk", ctypes.c_int32), ("dtype", ctypes.c_int32), ("solve", ctypes.c_int32),
-        ("solve_degree", ctypes.c_int32),
+        ("solve_degree", ctypes.c_int32), ("save_ctx", ctypes.c_int32),
     ]
 
 
@@ -72,6 +72,7 @@ SIGNATURES = {
     "gdn_validate": (ctypes.c_int, [_PP]),
     "gdn_num_chunk_slots": (ctypes.c_int64, [_PP]),
     "gdn_ctx_bytes": (_SZ, [_PP]),
+    "gdn_ctx_offset": (_I64, [_PP, ctypes.c_int]),
     "gdn_chunk_fwd_qdq": (ctypes.c_int, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "gdn_bwd_workspace_bytes": (_SZ, [_PP]),
     "gdn_chunk_bwd_ste": (ctypes.c_int, [_PP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,

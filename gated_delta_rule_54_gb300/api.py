@@ -34,7 +34,7 @@ def _mode(m) -> int:
 
 
 def make_problem(q, k, v, cu_seqlens=None, scale=1.0, state_mode="e4m3", w_mode="e4m3",
-                 block_v=64, chunk=64, N=None, neumann_degree=None) -> GdnProblem:
+                 block_v=64, chunk=64, N=None, neumann_degree=None, save_ctx=True) -> GdnProblem:
     B, T, Hk, Dk = k.shape
     Hv, Dv = v.shape[2], v.shape[3]
     p = GdnProblem()
@@ -47,6 +47,7 @@ def make_problem(q, k, v, cu_seqlens=None, scale=1.0, state_mode="e4m3", w_mode=
     p.dtype = _DT.get(q.dtype, 99)
     p.solve = 0 if neumann_degree is None else 1
     p.solve_degree = 0 if neumann_degree is None else int(neumann_degree)
+    p.save_ctx = 1 if save_ctx else 0
     return p
 
 
@@ -82,9 +83,10 @@ def gdn_chunk_fwd_qdq(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, sta
     h0 [N,Hv,Dk,Dv] f32 or None; cu_seqlens [N+1] int32 or None (B == 1).
 
     Returns (o [B,T,Hv,Dv] f32, ht [N,Hv,Dk,Dv] f32 or None, ctx uint8 or None).
-    The forward always writes its context (quantized W and chunk states); it
-    is returned when ``save_ctx`` (for the backward).  ``out`` may pass
-    preallocated (o, ht, ctx) buffers; ctx is required there.
+    With ``save_ctx`` the forward writes the backward's context and returns
+    it; without, it runs forward only with a smaller scratch context (not
+    returned).  ``out`` may pass preallocated (o, ht, ctx) buffers (ctx of
+    gdn_ctx_bytes for the same save_ctx; returned then).
     """
     lib = load()
     dev = q.device
@@ -92,7 +94,7 @@ def gdn_chunk_fwd_qdq(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, sta
                     ("cu_seqlens", cu_seqlens)):
         _check_dev(name, t, dev)
     p = make_problem(q, k, v, cu_seqlens, scale, state_mode, w_mode, block_v=block_v,
-                     neumann_degree=neumann_degree)
+                     neumann_degree=neumann_degree, save_ctx=save_ctx)
     check("gdn_validate", lib.gdn_validate(ctypes.byref(p)))
     B, T, Hv, Dv = v.shape
     if out is not None:
@@ -290,39 +292,34 @@ def fake_qdq_int8(x, group_cols, with_codes=False, out=None):
 
 
 def split_ctx(ctx: torch.Tensor, p: GdnProblem):
-    """Views of the forward's saved context segments (layout of gdn_ctx_bytes)."""
+    """Views of the forward's context segments present for problem p (offsets
+    from gdn_ctx_offset)."""
+    lib = load()
     B, T, Hv, Dk, Dv = p.B, p.T, p.Hv, p.Dk, p.Dv
     ns = gdn_num_chunk_slots(p)
-    al = lambda x: (x + 255) // 256 * 256
-    off = 0
+    f32, bf16 = torch.float32, torch.bfloat16
+    segs = [  # name, segment id, dtype, shape
+        ("w_codes", 0, torch.uint8, (B, T, Hv, Dk)),
+        ("w_scales", 1, f32, (ns, Hv)),
+        ("w_full", 2, f32, (B, T, Hv, Dk)),
+        ("chunk_vectors", 3, f32, (ns, Hv, 5, 64)),
+        ("t_img", 4, bf16, (ns, Hv, 64 * 64)),      # bf16 64x64 tiles as swizzled images
+        ("gkk_img", 5, bf16, (ns, Hv, 64 * 64)),
+        ("p_img", 6, bf16, (ns, Hv, 64 * 64)),
+        ("d_img", 7, bf16, (ns, Hv, Dv // 64, 64 * 64)),   # Delta of each value block
+        ("t_f32", 8, f32, (ns, Hv, 64, 64)),
+        ("h_codes", 9, torch.uint8, (ns, Hv, Dk, Dv)),
+        ("h_scales", 10, f32, (ns, Hv, Dv // p.block_v)),
+        ("h_full", 11, f32, (ns, Hv, Dk, Dv)),
+    ]
     out = {}
-    if p.w_mode != 0:
-        n = B * T * Hv * Dk
-        out["w_codes"] = ctx[off:off + n].view(B, T, Hv, Dk)
-        off = al(off + n)
-        out["w_scales"] = ctx[off:off + 4 * ns * Hv].view(torch.float32).view(ns, Hv)
-        off = al(off + 4 * ns * Hv)
-    else:
-        n = B * T * Hv * Dk
-        out["w_full"] = ctx[off:off + 4 * n].view(torch.float32).view(B, T, Hv, Dk)
-        off = al(off + 4 * n)
-    n = ns * Hv * 5 * 64
-    out["chunk_vectors"] = ctx[off:off + 4 * n].view(torch.float32).view(ns, Hv, 5, 64)
-    off = al(off + 4 * n)
-    for name in ("t_img", "gkk_img", "p_img"):   # bf16 64x64 tiles as swizzled images
-        n = ns * Hv * 64 * 64
-        out[name] = ctx[off:off + 2 * n].view(torch.bfloat16).view(ns, Hv, 64 * 64)
-        off = al(off + 2 * n)
-    n = ns * Hv * (Dv // 64) * 64 * 64               # Delta of each value block, same images
-    out["d_img"] = ctx[off:off + 2 * n].view(torch.bfloat16).view(ns, Hv, Dv // 64, 64 * 64)
-    off = al(off + 2 * n)
-    if p.state_mode != 0:
-        n = ns * Hv * Dk * Dv
-        out["h_codes"] = ctx[off:off + n].view(ns, Hv, Dk, Dv)
-        off = al(off + n)
-        m = ns * Hv * (Dv // p.block_v)
-        out["h_scales"] = ctx[off:off + 4 * m].view(torch.float32).view(ns, Hv, Dv // p.block_v)
-    else:
-        n = ns * Hv * Dk * Dv
-        out["h_full"] = ctx[off:off + 4 * n].view(torch.float32).view(ns, Hv, Dk, Dv)
+    for name, sid, dt, shape in segs:
+        off = int(lib.gdn_ctx_offset(ctypes.byref(p), sid))
+        if off < 0:
+            continue
+        n = 1
+        for s in shape:
+            n *= s
+        nbytes = n * torch.tensor([], dtype=dt).element_size()
+        out[name] = ctx[off:off + nbytes].view(dt).view(*shape)
     return out

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/gdn_qdq.h"
+#include "fused.h"
 #include "launch.h"
 
 namespace gdn {
@@ -26,39 +27,44 @@ Dims dims_of(const gdn_problem& p) {
   return d;
 }
 
+bool fused_fwd(const gdn_problem& p) {
+  return p.Dk == 128 && p.Dv == 128 && p.state_mode != GDN_QDQ_NONE &&
+         p.w_mode != GDN_QDQ_NONE && p.block_v == 64 && p.solve == GDN_SOLVE_EXACT;
+}
+
 CtxLayout ctx_layout(const gdn_problem& p) {
   const Dims d = dims_of(p);
-  CtxLayout L{};
+  CtxLayout L;
   size_t off = 0;
   const size_t tokens = (size_t)(d.B * d.T);
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align256(off + bytes);
+    return (int64_t)at;
+  };
   if (p.w_mode != GDN_QDQ_NONE) {
-    L.w_codes = off;
-    off = align256(off + tokens * d.Hv * d.Dk);
-    L.w_scales = off;
-    off = align256(off + sizeof(float) * (size_t)d.n_slots * d.Hv);
+    L.w_codes = take(tokens * d.Hv * d.Dk);
+    L.w_scales = take(sizeof(float) * (size_t)d.n_slots * d.Hv);
   } else {
-    L.w_full = off;
-    off = align256(off + sizeof(float) * tokens * d.Hv * d.Dk);
+    L.w_full = take(sizeof(float) * tokens * d.Hv * d.Dk);
   }
-  L.cvec = off;
-  off = align256(off + sizeof(float) * (size_t)d.n_slots * d.Hv * kCvecFloats);
-  L.tb = off;
-  off = align256(off + (size_t)d.n_slots * d.Hv * kTileImgBytes);
-  L.gkk = off;
-  off = align256(off + (size_t)d.n_slots * d.Hv * kTileImgBytes);
-  L.pb = off;
-  off = align256(off + (size_t)d.n_slots * d.Hv * kTileImgBytes);
-  L.db = off;
-  off = align256(off + (size_t)d.n_slots * d.Hv * (d.Dv / 64) * kTileImgBytes);
+  L.cvec = take(sizeof(float) * (size_t)d.n_slots * d.Hv * kCvecFloats);
+  if (p.save_ctx) {
+    L.tb = take((size_t)d.n_slots * d.Hv * kTileImgBytes);
+    L.gkk = take((size_t)d.n_slots * d.Hv * kTileImgBytes);
+    L.pb = take((size_t)d.n_slots * d.Hv * kTileImgBytes);
+    L.db = take((size_t)d.n_slots * d.Hv * (d.Dv / 64) * kTileImgBytes);
+  }
+  const bool fused = fused_fwd(p);
+  if (fused) L.t_f32 = take(sizeof(float) * (size_t)d.n_slots * d.Hv * kChunkLen * kChunkLen);
   const size_t per_slot = (size_t)d.n_slots * d.Hv * d.Dk * d.Dv;
   if (p.state_mode != GDN_QDQ_NONE) {
-    L.h_codes = off;
-    off = align256(off + per_slot);
-    L.h_scales = off;
-    off = align256(off + sizeof(float) * (size_t)d.n_slots * d.Hv * (d.Dv / p.block_v));
+    if (p.save_ctx || !fused) {
+      L.h_codes = take(per_slot);
+      L.h_scales = take(sizeof(float) * (size_t)d.n_slots * d.Hv * (d.Dv / p.block_v));
+    }
   } else {
-    L.h_full = off;
-    off = align256(off + sizeof(float) * per_slot);
+    L.h_full = take(sizeof(float) * per_slot);
   }
   L.total = off;
   return L;
@@ -95,6 +101,7 @@ static gdn_status validate(const gdn_problem* p) {
   if (p->T > ((int64_t)1 << 31) - 1 || p->B * p->T > ((int64_t)1 << 31) - 1)
     return GDN_ERR_UNSUPPORTED_SHAPE;  // token indices are int32 on the device
   if (!(p->scale == p->scale)) return GDN_ERR_INVALID_ARG;  // NaN scale
+  if (p->save_ctx != 0 && p->save_ctx != 1) return GDN_ERR_INVALID_ARG;
   return GDN_OK;
 }
 
@@ -139,7 +146,8 @@ int gdn_abi_version(void) { return GDN_QDQ_ABI_VERSION; }
 
 int gdn_device_error(int reset) {
   const int f = fwd_device_error(reset != 0), b = bwd_device_error(reset != 0);
-  return (f < 0 || b < 0) ? -1 : (f | b);
+  const int u = fused_device_error(reset != 0);
+  return (f < 0 || b < 0 || u < 0) ? -1 : (f | b | u);
 }
 
 gdn_status gdn_validate(const gdn_problem* p) { return validate(p); }
@@ -152,6 +160,26 @@ int64_t gdn_num_chunk_slots(const gdn_problem* p) {
 size_t gdn_ctx_bytes(const gdn_problem* p) {
   if (validate(p) != GDN_OK) return 0;
   return ctx_layout(*p).total;
+}
+
+int64_t gdn_ctx_offset(const gdn_problem* p, int segment) {
+  if (validate(p) != GDN_OK) return -1;
+  const CtxLayout L = ctx_layout(*p);
+  switch (segment) {
+    case GDN_CTX_W_CODES: return L.w_codes;
+    case GDN_CTX_W_SCALES: return L.w_scales;
+    case GDN_CTX_W_FULL: return L.w_full;
+    case GDN_CTX_CVEC: return L.cvec;
+    case GDN_CTX_T_IMG: return L.tb;
+    case GDN_CTX_GKK_IMG: return L.gkk;
+    case GDN_CTX_P_IMG: return L.pb;
+    case GDN_CTX_D_IMG: return L.db;
+    case GDN_CTX_T_F32: return L.t_f32;
+    case GDN_CTX_H_CODES: return L.h_codes;
+    case GDN_CTX_H_SCALES: return L.h_scales;
+    case GDN_CTX_H_FULL: return L.h_full;
+    default: return -1;
+  }
 }
 
 gdn_status gdn_chunk_fwd_qdq(const gdn_problem* p, const void* q, const void* k, const void* v,
@@ -200,6 +228,7 @@ gdn_status gdn_chunk_bwd_ste(const gdn_problem* p, const void* q, const void* k,
                              void* stream) {
   gdn_status s = validate(p);
   if (s != GDN_OK) return s;
+  if (!p->save_ctx) return GDN_ERR_INVALID_ARG;  // a forward-only context has no backward data
   const Dims d = dims_of(*p);
   const bool any_tokens = d.B * d.T > 0;
   if (any_tokens && (!q || !k || !v || !beta || !g || !ctx || !dO || !dq || !dk || !dv ||

@@ -12,11 +12,16 @@
 // The array below is a file-scope __device__ variable: every GPU that loads
 // this library holds GDN_NOALLOC_SCRATCH_BYTES of device memory for it until
 // the process exits.  In host code its name is only a host-side stand-in, so
-// the device address is looked up with cudaGetSymbolAddress once per device
-// (with that device current) on the first call made on that device; make that
-// first call before any stream capture.  All calls share the one array, and it
-// keeps the last call's contents: the launch path clears what must start at
-// zero, and calls that overlap on the GPU (e.g. on two streams) race.
+// the device address is looked up with cudaGetSymbolAddress (with the device
+// current) on the first call made in each CUDA context, and kept per context:
+// a context created later on the same device (e.g. after cudaDeviceReset) gets
+// its own lookup.  Make the first call on a device before any stream capture.
+// All calls share the one array, and it keeps the last call's contents: every
+// scratch byte a call reads it has written first (each state-gradient slot and
+// each dq/dk partial row is stored before it is loaded), so nothing needs
+// clearing; calls that overlap on the GPU (e.g. on two streams) race.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "../../include/gdn_qdq.h"
@@ -26,21 +31,57 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_bwd_scratch[GDN_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_addr[kMaxDevices];  // device address of g_bwd_scratch, per device
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
 
-// Device address of the scratch array on the current device (looked up once).
+// cuCtxGetCurrent through the runtime's driver entry-point query (no link-time
+// dependency on the driver library)
+CtxGetCurrentFn ctx_get_current() {
+  static CtxGetCurrentFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<CtxGetCurrentFn>(f);
+  });
+  return fn;
+}
+
+constexpr int kMaxContexts = 64;
+std::mutex g_mu;
+CUcontext g_ctx[kMaxContexts];  // contexts seen so far ...
+void* g_addr[kMaxContexts];     // ... and the scratch array's device address in each
+int g_n = 0;
+
+// Device address of the scratch array in the current context (looked up once
+// per context).
 gdn_status scratch_address(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return GDN_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_addr[dev]) {
+  const CtxGetCurrentFn get = ctx_get_current();
+  CUcontext ctx = nullptr;
+  if (!get || get(&ctx) != CUDA_SUCCESS) return GDN_ERR_CUDA;
+  if (!ctx) {
+    // no context is current yet: the runtime makes the device's primary
+    // context current on its first call, here the symbol lookup
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || !p) return GDN_ERR_CUDA;
-    g_addr[dev] = p;
+    if (get(&ctx) != CUDA_SUCCESS || !ctx) return GDN_ERR_CUDA;
   }
-  *out = g_addr[dev];
+  std::lock_guard<std::mutex> lock(g_mu);
+  for (int i = 0; i < g_n; ++i)
+    if (g_ctx[i] == ctx) {
+      *out = g_addr[i];
+      return GDN_OK;
+    }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || !p) return GDN_ERR_CUDA;
+  if (g_n < kMaxContexts) {
+    g_ctx[g_n] = ctx;
+    g_addr[g_n] = p;
+    ++g_n;
+  }
+  *out = p;
   return GDN_OK;
 }
 

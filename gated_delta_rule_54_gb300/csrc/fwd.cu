@@ -41,6 +41,7 @@
 #include <cooperative_groups.h>
 
 #include "common.cuh"
+#include "fused.h"
 #include "launch.h"
 
 namespace gdn {
@@ -70,8 +71,9 @@ struct FwdParams {
   float* h_scales;
   float* h_full;
   float* cvec;  // [n_slots, Hv, kCvecFloats] chunk vectors
-  __nv_bfloat16 *tb, *gkk, *pb;  // [n_slots, Hv] 8 KiB tile images for the backward
-  __nv_bfloat16* db;             // [n_slots, Hv, Dv / 64] Delta tile images for the backward
+  __nv_bfloat16 *tb, *gkk, *pb;  // [n_slots, Hv] 8 KiB tile images for the backward (or null)
+  __nv_bfloat16* db;             // [n_slots, Hv, Dv / 64] Delta tile images for the backward (or null)
+  float* t_f32;                  // [n_slots, Hv, 64, 64] T = (I + A)^-1 for the fused scan
   const int32_t* cu_seqlens;
   int64_t T;
   int Hk, Hv, Dv, G, N;
@@ -227,7 +229,9 @@ struct PrepSmem {
   static_assert(WST - TW >= kF32Tile, "Tw, Tu hold a second fp32 tile for the Neumann products");
 };
 
-template <int DK, int WM>
+// TOUT: the variant for the fused scan, which forms U itself: T is written in
+// fp32 to p.t_f32 and U is not computed.
+template <int DK, int WM, bool TOUT>
 __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __grid_constant__ FwdParams p) {
   using S = PrepSmem<DK>;
   extern __shared__ __align__(1024) unsigned char sm_raw[];
@@ -267,11 +271,11 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __g
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();
-    mbar_expect_tx(&bar, kChunk * DK * 2 + nvb * kChunk * 64 * 2);
+    mbar_expect_tx(&bar, kChunk * DK * 2 + (TOUT ? 0 : nvb * kChunk * 64 * 2));
 #pragma unroll
     for (int pn = 0; pn < DK / 64; ++pn)
       tma_load_2d(Ks + pn * kChunk * 64, &p.tm_k, hk * DK + pn * 64, (int)tok0, &bar);
-    for (int vb = 0; vb < nvb; ++vb)
+    for (int vb = 0; vb < (TOUT ? 0 : nvb); ++vb)
       tma_load_2d(Vs + vb * kChunk * 64, &p.tm_v, h * p.Dv + vb * 64, (int)tok0, &bar);
   }
   if (threadIdx.x < 2 * kChunk) {
@@ -329,7 +333,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __g
   {
     // Gamma o KK^T (strictly lower; rows >= L hold another sequence's keys: zero)
     // as the backward's tile image, and A = diag(beta) (Gamma o KK^T)
-    __nv_bfloat16* gimg = p.gkk + (slot * p.Hv + h) * (kTileImgBytes / 2);
+    __nv_bfloat16* gimg = p.gkk ? p.gkk + (slot * p.Hv + h) * (kTileImgBytes / 2) : nullptr;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
@@ -341,7 +345,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __g
           k0 = (j < i) ? expf(gi - gam[j]) * acc[nt][2 * e2] : 0.f;
           k1 = (j + 1 < i) ? expf(gi - gam[j + 1]) * acc[nt][2 * e2 + 1] : 0.f;
         }
-        st_bf16x2(gimg + swz<64>(i, j), k0, k1);
+        if (gimg) st_bf16x2(gimg + swz<64>(i, j), k0, k1);
         // (tiles above the diagonal hold zeros: the Neumann products read all of A)
         *reinterpret_cast<float2*>(As + i * kSA + j) = make_float2(bet[i] * k0, bet[i] * k1);
       }
@@ -356,22 +360,26 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __g
 
   // ---- a4 operands: Tw = T diag(beta e^gamma), Tu = T diag(beta), split hi/lo;
   //      T itself as the backward's tile image ----
-  __nv_bfloat16* timg = p.tb + (slot * p.Hv + h) * (kTileImgBytes / 2);
+  __nv_bfloat16* timg = p.tb ? p.tb + (slot * p.Hv + h) * (kTileImgBytes / 2) : nullptr;
+  float* tf = TOUT ? p.t_f32 + (slot * p.Hv + h) * (kChunk * kChunk) : nullptr;
   for (int e = threadIdx.x; e < 64 * 32; e += kPrepThreads) {
     const int i = e >> 5, j = (e & 31) * 2;
     const float2 tt = *reinterpret_cast<const float2*>(Ts + i * kSA + j);
     const float t0 = (j <= i) ? tt.x : 0.f;
     const float t1 = (j + 1 <= i) ? tt.y : 0.f;
-    st_bf16x2(timg + swz<64>(i, j), t0, t1);
+    if (timg) st_bf16x2(timg + swz<64>(i, j), t0, t1);
+    if constexpr (TOUT) *reinterpret_cast<float2*>(tf + i * kChunk + j) = make_float2(t0, t1);
     float a0, a1, b0, b1;
     split_bf16(t0 * beg[j], a0, b0);
     split_bf16(t1 * beg[j + 1], a1, b1);
     st_bf16x2(TwH + swz<64>(i, j), a0, a1);
     st_bf16x2(TwL + swz<64>(i, j), b0, b1);
-    split_bf16(t0 * bet[j], a0, b0);
-    split_bf16(t1 * bet[j + 1], a1, b1);
-    st_bf16x2(TuH + swz<64>(i, j), a0, a1);
-    st_bf16x2(TuL + swz<64>(i, j), b0, b1);
+    if constexpr (!TOUT) {
+      split_bf16(t0 * bet[j], a0, b0);
+      split_bf16(t1 * bet[j + 1], a1, b1);
+      st_bf16x2(TuH + swz<64>(i, j), a0, a1);
+      st_bf16x2(TuL + swz<64>(i, j), b0, b1);
+    }
   }
   __syncthreads();
 
@@ -442,7 +450,7 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __g
   }
 
   // ---- a4: U = Tu V, one 64-column block at a time, parked in o ----
-  for (int vb = 0; vb < nvb; ++vb) {
+  for (int vb = 0; vb < (TOUT ? 0 : nvb); ++vb) {
     float uacc[4][4];
     zero_acc(uacc);
     const __nv_bfloat16* Vb = Vs + vb * kChunk * 64;
@@ -1071,8 +1079,8 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
 
     // block 0 saves P (bf16; rows >= L zero) as the backward's tile image, and
     // every block its Delta (the hi half: Delta rounded to bf16)
-    __nv_bfloat16* pimg = vb == 0 ? p.pb + (slot * p.Hv + h) * (kTileImgBytes / 2) : nullptr;
-    __nv_bfloat16* dimg = p.db + ((slot * p.Hv + h) * nvb + vb) * (kTileImgBytes / 2);
+    __nv_bfloat16* pimg = (vb == 0 && p.pb) ? p.pb + (slot * p.Hv + h) * (kTileImgBytes / 2) : nullptr;
+    __nv_bfloat16* dimg = p.db ? p.db + ((slot * p.Hv + h) * nvb + vb) * (kTileImgBytes / 2) : nullptr;
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt) {
 #pragma unroll
@@ -1088,8 +1096,8 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
             split_bf16(p1, h1v, l1v);
             st_bf16x2(PH + swz<64>(i, j), h0v, h1v);
             st_bf16x2(PL + swz<64>(i, j), l0v, l1v);
-            st_bf16x2(pimg + swz<64>(i, j), i < L ? p0 : 0.f, i < L ? p1 : 0.f);
-          } else {
+            if (pimg) st_bf16x2(pimg + swz<64>(i, j), i < L ? p0 : 0.f, i < L ? p1 : 0.f);
+          } else if (pimg) {
             st_bf16x2(pimg + swz<64>(i, j), 0.f, 0.f);
           }
         }
@@ -1099,7 +1107,7 @@ __global__ void __launch_bounds__(kOutThreads, 2) gdn_fwd_output_kernel(const __
         split_bf16(dl.y, h1v, l1v);
         st_bf16x2(DH + swz<64>(i, j), h0v, h1v);
         st_bf16x2(DL + swz<64>(i, j), l0v, l1v);
-        st_bf16x2(dimg + swz<64>(i, j), h0v, h1v);
+        if (dimg) st_bf16x2(dimg + swz<64>(i, j), h0v, h1v);
       }
     }
     // P, Delta ready; this block's Delta tile and H^ are read: the next block's
@@ -1175,7 +1183,7 @@ template <int DK, int SM, int WM>
 gdn_status launch_t(const FwdParams& prm, const Dims& d, cudaStream_t st) {
   const int nvb = d.Dv / 64;
   if (d.B * d.T > 0 && d.n_slots > 0) {
-    auto k1 = gdn_fwd_prep_kernel<DK, WM>;
+    auto k1 = gdn_fwd_prep_kernel<DK, WM, false>;
     if (set_smem(k1, PrepSmem<DK>::BYTES) != GDN_OK) return GDN_ERR_CUDA;
     k1<<<(unsigned)(d.n_slots * d.Hv), kPrepThreads, PrepSmem<DK>::BYTES, st>>>(prm);
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
@@ -1214,6 +1222,46 @@ gdn_status dispatch_modes(const gdn_problem& p, const FwdParams& prm, const Dims
   GDN_CASE(GDN_QDQ_NONE, GDN_QDQ_INT8)
 #undef GDN_CASE
   return GDN_ERR_UNSUPPORTED_MODE;
+}
+
+// Dk = Dv = 128, both sites quantized, block_v 64, exact solve: the chunk
+// prep (T kept in fp32, no U) and the fused scan + outputs.
+gdn_status launch_fused(const gdn_problem& p, const FwdParams& prm, const Dims& d,
+                        cudaStream_t st) {
+  if (d.B * d.T > 0 && d.n_slots > 0) {
+    gdn_status s = GDN_OK;
+    auto prep = [&](auto kern) {
+      if (set_smem(kern, PrepSmem<128>::BYTES) != GDN_OK) return GDN_ERR_CUDA;
+      kern<<<(unsigned)(d.n_slots * d.Hv), kPrepThreads, PrepSmem<128>::BYTES, st>>>(prm);
+      return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    };
+    s = p.w_mode == GDN_QDQ_E4M3 ? prep(gdn_fwd_prep_kernel<128, GDN_QDQ_E4M3, true>)
+                                 : prep(gdn_fwd_prep_kernel<128, GDN_QDQ_INT8, true>);
+    if (s != GDN_OK) return s;
+  }
+  FusedParams f{};
+  f.tm_k = prm.tm_k;
+  f.tm_q = prm.tm_q;
+  f.tm_v = prm.tm_v;
+  f.tm_wc = prm.tm_wc;
+  f.t_f32 = prm.t_f32;
+  f.cvec = prm.cvec;
+  f.w_scales = prm.w_scales;
+  f.h0 = prm.h0;
+  f.o = prm.o;
+  f.ht = prm.ht;
+  f.h_codes = prm.h_codes;
+  f.h_scales = prm.h_scales;
+  f.pb = prm.pb;
+  f.db = prm.db;
+  f.cu_seqlens = prm.cu_seqlens;
+  f.T = prm.T;
+  f.nt_fixed = prm.nt_fixed;
+  f.Hv = prm.Hv;
+  f.G = prm.G;
+  f.N = prm.N;
+  f.scale = prm.scale;
+  return launch_fused_scan(f, p.state_mode, p.w_mode, st);
 }
 
 }  // namespace
@@ -1274,23 +1322,20 @@ gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const 
   prm.ht = ht;
   const CtxLayout L = ctx_layout(p);
   unsigned char* base = static_cast<unsigned char*>(ctx);
-  if (p.w_mode != GDN_QDQ_NONE) {
-    prm.w_codes = base + L.w_codes;
-    prm.w_scales = reinterpret_cast<float*>(base + L.w_scales);
-  } else {
-    prm.w_full = reinterpret_cast<float*>(base + L.w_full);
-  }
-  prm.cvec = reinterpret_cast<float*>(base + L.cvec);
-  prm.tb = reinterpret_cast<__nv_bfloat16*>(base + L.tb);
-  prm.gkk = reinterpret_cast<__nv_bfloat16*>(base + L.gkk);
-  prm.pb = reinterpret_cast<__nv_bfloat16*>(base + L.pb);
-  prm.db = reinterpret_cast<__nv_bfloat16*>(base + L.db);
-  if (p.state_mode != GDN_QDQ_NONE) {
-    prm.h_codes = base + L.h_codes;
-    prm.h_scales = reinterpret_cast<float*>(base + L.h_scales);
-  } else {
-    prm.h_full = reinterpret_cast<float*>(base + L.h_full);
-  }
+  // segments absent from this problem's layout stay null (nothing writes them)
+  auto at = [&](int64_t off) -> unsigned char* { return off < 0 ? nullptr : base + off; };
+  prm.w_codes = at(L.w_codes);
+  prm.w_scales = reinterpret_cast<float*>(at(L.w_scales));
+  prm.w_full = reinterpret_cast<float*>(at(L.w_full));
+  prm.cvec = reinterpret_cast<float*>(at(L.cvec));
+  prm.tb = reinterpret_cast<__nv_bfloat16*>(at(L.tb));
+  prm.gkk = reinterpret_cast<__nv_bfloat16*>(at(L.gkk));
+  prm.pb = reinterpret_cast<__nv_bfloat16*>(at(L.pb));
+  prm.db = reinterpret_cast<__nv_bfloat16*>(at(L.db));
+  prm.t_f32 = reinterpret_cast<float*>(at(L.t_f32));
+  prm.h_codes = at(L.h_codes);
+  prm.h_scales = reinterpret_cast<float*>(at(L.h_scales));
+  prm.h_full = reinterpret_cast<float*>(at(L.h_full));
   prm.cu_seqlens = p.cu_seqlens;
   prm.T = d.T;
   prm.Hk = d.Hk;
@@ -1329,6 +1374,7 @@ gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const 
                     CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!ok) return GDN_ERR_CUDA;
   }
+  if (fused_fwd(p)) return launch_fused(p, prm, d, st);
   if (d.Dk == 128) return dispatch_modes<128>(p, prm, d, st);
   return dispatch_modes<64>(p, prm, d, st);
 }

@@ -25,13 +25,18 @@ struct Dims {
   bool packed;
 };
 
-// Byte offsets of the saved context segments (see gdn_ctx_bytes).
+// Byte offsets of the context segments (see gdn_ctx_bytes); -1 where absent.
 struct CtxLayout {
-  size_t w_codes, w_scales, w_full, cvec, tb, gkk, pb, db, h_codes, h_scales, h_full, total;
+  int64_t w_codes = -1, w_scales = -1, w_full = -1, cvec = -1, tb = -1, gkk = -1, pb = -1,
+          db = -1, t_f32 = -1, h_codes = -1, h_scales = -1, h_full = -1;
+  size_t total = 0;
 };
 
 Dims dims_of(const gdn_problem& p);
 CtxLayout ctx_layout(const gdn_problem& p);
+// the fused two-launch forward applies (Dk = Dv = 128, both sites quantized,
+// block_v 64, exact solve)
+bool fused_fwd(const gdn_problem& p);
 
 gdn_status launch_fake_qdq(int mode, const float* x, float* y, float* scales, uint8_t* codes,
                            int64_t batch, int64_t rows, int64_t cols, int64_t group_cols,

@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define GDN_QDQ_ABI_VERSION 5
+#define GDN_QDQ_ABI_VERSION 6
 
 typedef enum {
   GDN_QDQ_NONE = 0, /* site not quantized                                   */
@@ -93,6 +93,10 @@ typedef struct {
                                  QAT", "What does this PR do?"), the backward
                                  through that polynomial                       */
   int32_t solve_degree;       /* Neumann degree, 0..63 (63 is already exact)    */
+  int32_t save_ctx;           /* 1: the forward writes the context the backward
+                                 reads (training); 0: forward only (inference):
+                                 `ctx` is scratch for the forward's own launches
+                                 and gdn_ctx_bytes() is smaller               */
 } gdn_problem;
 
 typedef enum { GDN_SOLVE_EXACT = 0, GDN_SOLVE_NEUMANN = 1 } gdn_solve;
@@ -120,10 +124,11 @@ gdn_status gdn_validate(const gdn_problem* p);
 int64_t gdn_num_chunk_slots(const gdn_problem* p);
 
 /*
- * Bytes of the forward's context (the quantized W and chunk states it
- * writes, read back by its own output pass and by the backward), or 0 if p
- * is invalid.  Layout (each segment starts on a 256-byte boundary, in this
- * order):
+ * Bytes of the forward's context, or 0 if p is invalid.  With save_ctx = 1
+ * it holds what the backward reads (the quantized W and chunk states and the
+ * chunk tiles below); with save_ctx = 0 only what the forward's own launches
+ * hand to each other.  Segments (each starts on a 256-byte boundary, in this
+ * order; gdn_ctx_offset() gives each one's offset, or -1 where absent):
  *   w_codes   u8  [B, T, Hv, Dk]        quantized W codes    (w_mode != NONE)
  *   w_scales  f32 [n_slots, Hv]         W scale per chunk    (w_mode != NONE)
  *   w_full    f32 [B, T, Hv, Dk]        unquantized W        (w_mode == NONE)
@@ -131,22 +136,36 @@ int64_t gdn_num_chunk_slots(const gdn_problem* p);
  *                                       g), e^gamma, e^{gamma_L - gamma}, beta,
  *                                       beta e^gamma (rows past the chunk end:
  *                                       gamma flat, beta 0)
- *   t_img     bf16 [n_slots, Hv, 4096]  T = (I + A)^-1 (lower incl. diagonal)
- *   gkk_img   bf16 [n_slots, Hv, 4096]  Gamma o KK^T (strictly lower)
- *   p_img     bf16 [n_slots, Hv, 4096]  P = Gamma o QK^T (lower incl. diagonal)
+ *   t_img     bf16 [n_slots, Hv, 4096]  T = (I + A)^-1 (lower incl. diagonal)   (save_ctx)
+ *   gkk_img   bf16 [n_slots, Hv, 4096]  Gamma o KK^T (strictly lower)           (save_ctx)
+ *   p_img     bf16 [n_slots, Hv, 4096]  P = Gamma o QK^T (lower incl. diagonal) (save_ctx)
  *   d_img     bf16 [n_slots, Hv, Dv/64, 4096]  Delta = U - W^ H^ of each
- *                                       64-column value block
+ *                                       64-column value block                  (save_ctx)
  *             each 64 x 64 tile stored as its shared-memory image: element
  *             (i, j) at i * 64 + 8 * ((j / 8) ^ (i % 8)) + j % 8; rows past
  *             the chunk end are zero (T: identity rows)
- *   h_codes   u8  [n_slots, Hv, Dk, Dv] state codes entering each chunk (state_mode != NONE)
- *   h_scales  f32 [n_slots, Hv, Dv/64]  state scale per [Dk, 64] tile  (state_mode != NONE)
+ *   t_f32     f32 [n_slots, Hv, 64, 64] T row-major (fused forward only: Dk =
+ *                                       Dv = 128, both sites quantized,
+ *                                       block_v 64, exact solve)
+ *   h_codes   u8  [n_slots, Hv, Dk, Dv] state codes entering each chunk (state_mode != NONE;
+ *                                       absent for a forward-only fused call)
+ *   h_scales  f32 [n_slots, Hv, Dv/block_v] state scale per [Dk, block_v] tile (as h_codes)
  *   h_full    f32 [n_slots, Hv, Dk, Dv] unquantized state entering each chunk (state_mode == NONE)
  * E4M3 codes are OCP E4M3FN bytes; INT8 codes are two's-complement bytes.
  * Code times scale (fp32 multiply) is the dequantized value; the context
  * therefore holds the quantized W and states exactly.
  */
 size_t gdn_ctx_bytes(const gdn_problem* p);
+
+typedef enum {
+  GDN_CTX_W_CODES = 0, GDN_CTX_W_SCALES, GDN_CTX_W_FULL, GDN_CTX_CVEC, GDN_CTX_T_IMG,
+  GDN_CTX_GKK_IMG, GDN_CTX_P_IMG, GDN_CTX_D_IMG, GDN_CTX_T_F32, GDN_CTX_H_CODES,
+  GDN_CTX_H_SCALES, GDN_CTX_H_FULL
+} gdn_ctx_segment;
+
+/* Byte offset of one context segment (gdn_ctx_segment), or -1 if p is invalid
+ * or the segment is absent for this problem. */
+int64_t gdn_ctx_offset(const gdn_problem* p, int segment);
 
 /*
  * Forward: o = chunked gated delta rule with state/W fake QDQ.
@@ -156,7 +175,9 @@ size_t gdn_ctx_bytes(const gdn_problem* p);
  *   o     f32  [B, T, Hv, Dv]      (written)
  *   ht    f32  [N, Hv, Dk, Dv] final state, unquantized, or NULL (written)
  *   ctx   gdn_ctx_bytes(p) bytes, 256-byte aligned (written; required when
- *         B * T > 0: the output pass reads the saved W and chunk states)
+ *         B * T > 0: the forward's launches hand W and the chunk states to
+ *         each other through it; with save_ctx = 1 it is also the backward's
+ *         context)
  * Per chunk (method of the first page; the pages print no equations, this is
  * the published WY form of the gated delta rule): gamma = in-chunk cumsum of
  * g; A = strictly-lower(beta_i exp(gamma_i - gamma_j) k_i.k_j); T = (I+A)^-1;
@@ -170,6 +191,12 @@ size_t gdn_ctx_bytes(const gdn_problem* p);
  * over U) until the last launch writes the outputs over it.
  * A sequence of length 0 returns ht = h0 (not quantized).
  * All pointers must be 16-byte aligned (GDN_ERR_MISALIGNED otherwise).
+ * Launches: for Dk = Dv = 128 with both sites quantized, block_v 64 and the
+ * exact solve, two: the chunk-local A, T, W (with its QDQ) for all chunks at
+ * once, then one fused kernel per (sequence, value head, 64-column value
+ * block) that walks the chunks forming U, the state QDQ, Delta, the state
+ * update and the outputs on the tensor cores (tcgen05, accumulators in
+ * tensor memory).  Otherwise the three launches described above.
  */
 gdn_status gdn_chunk_fwd_qdq(const gdn_problem* p, const void* q, const void* k,
                              const void* v, const float* beta, const float* g,
@@ -185,7 +212,8 @@ size_t gdn_bwd_workspace_bytes(const gdn_problem* p);
  * Backward with identity STE through both QDQ sites (first page, "What":
  * identity straight-through; the quantized W saved by the forward is reused,
  * no second quantizer call).  `ctx` is the forward's context for the same
- * inputs.  Gradients of L = <dO, o> + <dht, ht>:
+ * inputs, written with save_ctx = 1 (a problem with save_ctx = 0 is
+ * GDN_ERR_INVALID_ARG).  Gradients of L = <dO, o> + <dht, ht>:
  *   dO    bf16 [B, T, Hv, Dv]          dht f32 [N, Hv, Dk, Dv] or NULL (zeros)
  *   dq,dk f32  [B, T, Hk, Dk]  (summed over the value heads sharing a key head)
  *   dv    f32  [B, T, Hv, Dv]          dbeta, dg f32 [B, T, Hv]
@@ -209,10 +237,12 @@ gdn_status gdn_chunk_bwd_ste(const gdn_problem* p, const void* q, const void* k,
  * of GDN_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
  * the library holds until the process exits.  Problems whose
  * gdn_bwd_workspace_bytes(p) exceeds that size are rejected before any launch
- * with GDN_ERR_WORKSPACE_TOO_SMALL.  The first call on a device looks up the
- * array's device address (once per device, that device current) — make it
- * before any stream capture.  Calls share the array: calls that overlap on the
- * GPU race; the call clears what must start at zero.  Allocates nothing.
+ * with GDN_ERR_WORKSPACE_TOO_SMALL.  The first call in a CUDA context (on a
+ * device, with that device current) looks up the array's device address and
+ * keeps it for that context — make it before any stream capture.  Calls share
+ * the array, which keeps the last call's contents: every scratch byte a call
+ * reads it writes first, so nothing needs clearing; calls that overlap on the
+ * GPU race.  Allocates nothing.
  */
 #define GDN_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 gdn_status gdn_chunk_bwd_ste_noalloc(const gdn_problem* p, const void* q, const void* k,

@@ -14,7 +14,9 @@ Tolerances (stated once, used everywhere):
       or within 2^-5 in code units, where the grid steps by 2^-9), and at
       most 0.1% of the codes differ (at least one flip is always allowed: a
       single flip in a few hundred codes is consistent with a 1e-5 flip rate);
-      all chunks are compared;
+      state codes are compared this way in each (sequence, head) up to and
+      including its first chunk (token) with a flip; the later ones carry that
+      flip's perturbation, which the allowance bounds;
   flip allowance: a code one step away from the oracle's changes that
       quantized element by (the code's grid gap) x (its tile scale), both
       taken from the oracle.  That perturbation is pushed through the exact
@@ -25,10 +27,10 @@ Tolerances (stated once, used everywhere):
       only its own flips and a scale change of at most max|dH| / amax.  Token
       recurrences use (I - beta k k^T) (spectral norm <= 1) and the decay.
       Where the kernel does not report its codes (KDA, two-precision, the
-      decode post readout of the last token) every element whose oracle value
-      lies within 2^-16 of the tile amax (plus any perturbation already
-      propagated) of a rounding boundary counts as possibly flipped.  Elements
-      before a unit's first flip get no allowance;
+      decode post readout of the last token; fp32 recurrences) every element
+      whose oracle value lies within 2^-20 of the tile amax (plus any
+      perturbation already propagated) of a rounding boundary counts as
+      possibly flipped.  Elements before a unit's first flip get no allowance;
   gradients: relative L2 error ||x - r|| / ||r|| <= 2e-2 per tensor.
 Every test that applies an allowance records how many (sequence, head) units
 carried one; the session summary prints the counts.
@@ -46,7 +48,7 @@ FLOOR = 1e-4
 FRAC = 1e-3
 CODE_FRAC = 1e-3
 GRAD_L2 = 2e-2
-FP_MARGIN = 2.0 ** -16   # kernels' error at a quantization input, relative to the tile amax
+FP_MARGIN = 2.0 ** -20   # fp32 kernels' error at a quantization input, relative to the tile amax
 DEQ_SLACK = 1.0 + 2.0 ** -20   # a dequantized value is code x scale rounded to binary32
 
 # (test name, what, units with an allowance, units, max allowance / max|ref|),
@@ -168,8 +170,9 @@ def fwd_flip_allowance(d, inters, rec, state_flip, w_flip, lens, packed, scale, 
     """Per-element allowances for o [B, T, Hv, Dv] and ht [N, Hv, Dk, Dv].
 
     state_flip: bool [n_chunks, Hv, Dk, Dv] where the kernel's state code
-    differs from the oracle's (dense chunk order); w_flip: bool [B*T, Hv, Dk]
-    likewise for W codes.  Everything else comes from the oracle's
+    differs from the oracle's (dense chunk order; after a unit's first flip its
+    later codes may differ by more than one step: the carried perturbation
+    bounds them); w_flip: bool [B*T, Hv, Dk] likewise for W codes.  Everything else comes from the oracle's
     intermediates (chunked(..., intermediates=True)) and its record."""
     q = d["q"].double().numpy()
     k = d["k"].double().numpy()
@@ -181,6 +184,8 @@ def fwd_flip_allowance(d, inters, rec, state_flip, w_flip, lens, packed, scale, 
     N = len(lens)
     o_al = np.zeros((B * T, Hv, Dv))
     ht_al = np.zeros((N, Hv, Dk, Dv))
+    # W codes by token (empty sequences have none), in the tokens' order
+    wref = np.concatenate(rec["w_codes"], 0) if wm != "none" and rec.get("w_codes") else None
     cbase = np.concatenate([[0], np.cumsum([-(-L // 64) for L in lens])]).astype(int)
     tbase = np.concatenate([[0], np.cumsum(lens)]).astype(int) if packed else \
         np.arange(N + 1) * T
@@ -209,9 +214,13 @@ def fwd_flip_allowance(d, inters, rec, state_flip, w_flip, lens, packed, scale, 
                 if sm != "none":
                     codes = rec["state_codes"][cbase[n] + c, h]
                     sc = np.repeat(rec["state_scales"][cbase[n] + c, h].astype(np.float64), block_v)
-                    E = np.where(sf[c], code_gap(codes, sm) * sc[None, :], 0.0)
+                    # a differing code: one step (the first flip), or, once a perturbation
+                    # of column norm prop reaches the quantizer, |Q(x + d) - Q(x)| <=
+                    # |d| + half a grid gap on each side (at most two of the oracle's gaps)
+                    E = np.where(sf[c], (2.0 if prop.any() else 1.0) * code_gap(codes, sm) *
+                                 sc[None, :] + prop[None, :], 0.0)
                     if prop.any():
-                        # the quantizer keeps its codes; its scale moves with the amax
+                        # elsewhere the quantizer keeps its codes; its scale moves with the amax
                         E = E + np.abs(Hh) * _scale_shift(Hh, prop, block_v)[None, :]
                     Ecol = np.zeros(Dv)
                 else:
@@ -219,7 +228,7 @@ def fwd_flip_allowance(d, inters, rec, state_flip, w_flip, lens, packed, scale, 
                     Ecol = prop
                 sW = np.zeros((Lc, Dk))
                 if wf is not None and wf[64 * c:64 * c + Lc].any():
-                    wcodes = rec["w_codes"][n][64 * c:64 * c + Lc, h]
+                    wcodes = wref[t0:t0 + Lc, h]
                     sW = np.where(wf[64 * c:64 * c + Lc],
                                   code_gap(wcodes, wm) * float(rec["w_scales"][cbase[n] + c, h]), 0.0)
                 le = np.tril(np.ones((Lc, Lc), bool))
@@ -344,7 +353,8 @@ def decode_flip_allowance(d, rec_codes, rec_scales, gpu_flip, state_out, scale, 
             Es = []
             for t in range(T):
                 sc = np.repeat(rec_scales[b, t, h].astype(np.float64), block_v)
-                E = np.where(gpu_flip[b, t, h], code_gap(rec_codes[b, t, h], sm) * sc[None, :], 0.0)
+                E = np.where(gpu_flip[b, t, h], (2.0 if prop.any() else 1.0) *
+                             code_gap(rec_codes[b, t, h], sm) * sc[None, :] + prop[None, :], 0.0)
                 if prop.any():
                     Sh = decode_values(rec_codes[b, t, h], sm) * sc[None, :]
                     E = E + np.abs(Sh) * _scale_shift(Sh, prop, block_v)[None, :]
@@ -398,8 +408,9 @@ def recurrence_flip_allowance(events, steps, Dk, Dv, mode, group_cols, scale, ca
             if not carried:
                 prop = np.zeros(Dv)
             pt = np.repeat(prop.reshape(-1, group_cols).max(-1), group_cols)
-            y, sig = flip_candidates(x, group_cols, mode, FP_MARGIN * amax + pt[None, :])
-            E = sig[0] + np.abs(y[0]) * _scale_shift(y[0], prop, group_cols)[None, :]
+            y, sig = flip_candidates(x, group_cols, mode, FP_MARGIN * amax + 2 * pt[None, :])
+            E = sig[0] + np.maximum(np.abs(y[0]) * _scale_shift(y[0], prop, group_cols)[None, :],
+                                    np.where(amax[0] > 0, 0.0, pt)[None, :])
             prop = np.linalg.norm(E, axis=0)
         prop = float(np.max(eg)) * token_step_norm(bt, kt) * prop
         o_al[t] = abs(scale) * np.linalg.norm(qt) * prop
@@ -440,11 +451,16 @@ def sequence_allowances(d, rec, mode, group_cols, scale, g_key="g", carried=True
 
 
 def _scale_shift(Hq, prop, group_cols):
-    """Bound on the relative change of each column tile's scale when the state
-    it quantizes moves by at most prop (column 2-norms >= the element change):
-    the amax moves by at most that much."""
+    """Bound on the change of each element of a quantized tile whose codes stay
+    while the state it quantizes moves by at most prop (column 2-norms, which
+    bound every element's change): the tile amax moves by at most that much, so
+    the scale by at most pt / amax relative, and code x scale by |value| pt / amax
+    (never more than pt).  Returned per column as the factor on |value|; a
+    column whose tile amax is zero gets the factor 1 (the values there are zero
+    and the allowance comes from pt)."""
     Dv = Hq.shape[-1]
     amax = np.repeat(np.abs(Hq).reshape(-1, Dv // group_cols, group_cols).max(axis=(0, 2)), group_cols)
     pt = np.repeat(np.asarray(prop).reshape(-1, group_cols).max(-1), group_cols)
     with np.errstate(divide="ignore", invalid="ignore"):
-        return np.where(amax > pt, pt / np.maximum(amax - pt, 1e-300), np.where(pt > 0, 1.0, 0.0))
+        return np.where(amax > 0, np.minimum(pt / np.where(amax > 0, amax, 1.0), 1.0),
+                        np.where(pt > 0, 1.0, 0.0))

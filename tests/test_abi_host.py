@@ -35,7 +35,7 @@ def _problem(**kw):
     p.cu_seqlens = None
     p.scale = 1.0
     p.state_mode, p.w_mode, p.block_v, p.chunk, p.dtype = 1, 1, 64, 64, 0
-    p.solve, p.solve_degree = 0, 0
+    p.solve, p.solve_degree, p.save_ctx = 0, 0, 1
     for k, v in kw.items():
         setattr(p, k, v)
     return p
@@ -84,16 +84,34 @@ def test_sizes():
     assert lib.gdn_num_chunk_slots(ctypes.byref(p)) == 2 * nt
     al = lambda x: (x + 255) // 256 * 256
     ns = 2 * nt
-    cv = al(4 * ns * 4 * 5 * 64) + 3 * al(ns * 4 * 64 * 64 * 2)   # chunk vectors, T / GKK / P images
-    cv += al(ns * 4 * 2 * 64 * 64 * 2)                              # Delta images of both value blocks
-    exp = al(2 * 300 * 4 * 128) + al(4 * ns * 4) + cv + al(ns * 4 * 128 * 128) + al(4 * ns * 4 * 2)
-    assert lib.gdn_ctx_bytes(ctypes.byref(p)) == exp
+    cv = al(4 * ns * 4 * 5 * 64)                                    # chunk vectors
+    imgs = 3 * al(ns * 4 * 64 * 64 * 2) + al(ns * 4 * 2 * 64 * 64 * 2)  # T / GKK / P, Delta images
+    tf = al(4 * ns * 4 * 64 * 64)                                   # fp32 T of the fused forward
+    w = al(2 * 300 * 4 * 128) + al(4 * ns * 4)                      # W codes and scales
+    h = al(ns * 4 * 128 * 128) + al(4 * ns * 4 * 2)                 # state codes and scales
+    # Dk = Dv = 128, both sites quantized, block_v 64: the fused forward
+    assert lib.gdn_ctx_bytes(ctypes.byref(p)) == w + cv + imgs + tf + h
+    # forward only: no backward tiles; the fused forward keeps the states on chip
+    assert lib.gdn_ctx_bytes(ctypes.byref(_problem(save_ctx=0))) == w + cv + tf
+    # the three-launch path (here block_v 32) hands the state codes to its output pass
+    h32 = al(ns * 4 * 128 * 128) + al(4 * ns * 4 * 4)
+    assert lib.gdn_ctx_bytes(ctypes.byref(_problem(block_v=32, save_ctx=0))) == w + cv + h32
     p0 = _problem(state_mode=0, w_mode=0)
-    assert lib.gdn_ctx_bytes(ctypes.byref(p0)) == al(4 * 2 * 300 * 4 * 128) + cv + al(4 * ns * 4 * 128 * 128)
+    assert lib.gdn_ctx_bytes(ctypes.byref(p0)) == al(4 * 2 * 300 * 4 * 128) + cv + imgs + al(4 * ns * 4 * 128 * 128)
+    # segment offsets: the first is at 0, absent ones are -1, and they are increasing
+    offs = [lib.gdn_ctx_offset(ctypes.byref(p), s) for s in range(12)]
+    assert offs[0] == 0 and offs[2] == -1 and offs[11] == -1
+    present = [o for o in offs if o >= 0]
+    assert present == sorted(present) and len(present) == 10
+    po = _problem(save_ctx=0)
+    assert [lib.gdn_ctx_offset(ctypes.byref(po), s) >= 0 for s in range(12)] == \
+        [True, True, False, True, False, False, False, False, True, False, False, False]
     pk = _problem(B=1, T=1000, N=7, cu_seqlens=4096)
     assert lib.gdn_num_chunk_slots(ctypes.byref(pk)) == 1000 // 64 + 7
     assert lib.gdn_ctx_bytes(ctypes.byref(_problem(Dk=96))) == 0
     assert lib.gdn_num_chunk_slots(ctypes.byref(_problem(Dk=96))) == -1
+    assert lib.gdn_ctx_offset(ctypes.byref(_problem(Dk=96)), 0) == -1
+    assert _validate(_problem(save_ctx=2)) == -1
 
 
 def test_packed_slot_formula_is_injective():
@@ -147,7 +165,7 @@ def test_status_strings():
     for code in range(-7, 1):
         s = lib.gdn_status_string(code).decode()
         assert s.startswith("GDN_")
-    assert lib.gdn_abi_version() == 5
+    assert lib.gdn_abi_version() == 6
 
 
 def _dproblem(**kw):

@@ -37,11 +37,11 @@ def _check(d, sm, bv, readout, scale=1.0):
     flip = None
     if sm != "none" and T > 0:
         c = codes.cpu().numpy()
-        assert_codes(c, rc, sm, "decode state codes")
         flip = code_steps(c, rc, sm) > 0
-        # scales of states that no earlier flip reached
+        # codes and scales of states that no earlier flip of their (row, head) reached
         reached = np.cumsum(flip.any(axis=(3, 4)), axis=1) > 0
         ok = ~np.concatenate([np.zeros_like(reached[:, :1]), reached[:, :-1]], 1)
+        assert_codes(c[ok], rc[ok], sm, "decode state codes")
         assert np.allclose(scales.cpu().numpy()[ok], rs[ok], rtol=1e-4, atol=0)
     else:
         assert codes is None or codes.numel() == 0

@@ -15,7 +15,7 @@ import oracle.chunked as oc
 import oracle.decode as od
 from gated_delta_rule_54_gb300 import synth
 
-from _parity import (code_gap, decode_flip_allowance, flip_candidates, fwd_flip_allowance,
+from _parity import (FP_MARGIN, code_gap, decode_flip_allowance, flip_candidates, fwd_flip_allowance,
                      sequence_allowances)
 
 
@@ -154,7 +154,7 @@ def test_kda_allowance_covers_a_planted_flip(monkeypatch):
     ro, rh = ok.kda_recurrent(*args, state_mode="int8", record=rec)
     H = rec[1][2].astype(np.float32)            # [Hv, Dk, Dv] entering token 64
     amax = np.abs(H).reshape(1, 64, 1, 64).max()
-    _, sig = flip_candidates(H, 64, "int8", 2.0 ** -16 * amax)
+    _, sig = flip_candidates(H, 64, "int8", FP_MARGIN * amax)
     assert sig.any()
     h, dk, v = np.unravel_index(np.argmax(sig), sig.shape)
     hook = _FlipHook(1, (h, dk, v))
