@@ -307,7 +307,7 @@ def split_ctx(ctx: torch.Tensor, p: GdnProblem):
         ("gkk_img", 5, bf16, (ns, Hv, 64 * 64)),
         ("p_img", 6, bf16, (ns, Hv, 64 * 64)),
         ("d_img", 7, bf16, (ns, Hv, Dv // 64, 64 * 64)),   # Delta of each value block
-        ("t_f32", 8, f32, (ns, Hv, 64, 64)),
+        ("tu_img", 8, bf16, (ns, Hv, 2, 64 * 64)),
         ("h_codes", 9, torch.uint8, (ns, Hv, Dk, Dv)),
         ("h_scales", 10, f32, (ns, Hv, Dv // p.block_v)),
         ("h_full", 11, f32, (ns, Hv, Dk, Dv)),

@@ -56,7 +56,7 @@ CtxLayout ctx_layout(const gdn_problem& p) {
     L.db = take((size_t)d.n_slots * d.Hv * (d.Dv / 64) * kTileImgBytes);
   }
   const bool fused = fused_fwd(p);
-  if (fused) L.t_f32 = take(sizeof(float) * (size_t)d.n_slots * d.Hv * kChunkLen * kChunkLen);
+  if (fused) L.tu_img = take((size_t)d.n_slots * d.Hv * 2 * kTileImgBytes);
   const size_t per_slot = (size_t)d.n_slots * d.Hv * d.Dk * d.Dv;
   if (p.state_mode != GDN_QDQ_NONE) {
     if (p.save_ctx || !fused) {
@@ -174,7 +174,7 @@ int64_t gdn_ctx_offset(const gdn_problem* p, int segment) {
     case GDN_CTX_GKK_IMG: return L.gkk;
     case GDN_CTX_P_IMG: return L.pb;
     case GDN_CTX_D_IMG: return L.db;
-    case GDN_CTX_T_F32: return L.t_f32;
+    case GDN_CTX_TU_IMG: return L.tu_img;
     case GDN_CTX_H_CODES: return L.h_codes;
     case GDN_CTX_H_SCALES: return L.h_scales;
     case GDN_CTX_H_FULL: return L.h_full;

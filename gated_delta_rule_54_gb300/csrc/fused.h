@@ -2,7 +2,8 @@
 //
 // For Dk = Dv = 128 with both QDQ sites on, block_v 64 and the exact solve,
 // the forward runs as two launches: the chunk-local prep (A, T, W and its QDQ,
-// the chunk vectors; T kept in fp32) and one fused kernel per (sequence, value
+// the chunk vectors; T diag(beta) as hi + lo bf16 tiles) and one fused kernel
+// per (sequence, value
 // head, 64-column value block) that walks the chunks and, per chunk, forms
 // U = T diag(beta) V, quantizes the state, forms Delta = U - W^ H^, the state
 // update and the outputs, all on the tensor cores with accumulators in tensor
@@ -22,7 +23,7 @@ struct FusedParams {
   // 2-D TMA maps: k, q [tokens, Hk*128] bf16, v [tokens, Hv*128] bf16 (64 x 64
   // boxes, 128-byte swizzle); W codes [tokens, Hv*128] u8 (64 rows x 128 bytes)
   CUtensorMap tm_k, tm_q, tm_v, tm_wc;
-  const float* t_f32;     // [n_slots, Hv, 64, 64] T = (I + A)^-1 (row-major)
+  const void* tu_img;     // [n_slots, Hv, 2, 4096] bf16 T diag(beta) hi, lo tile images
   const float* cvec;      // [n_slots, Hv, 5 * 64] chunk vectors
   const float* w_scales;  // [n_slots, Hv]
   const float* h0;        // [N, Hv, 128, 128] or null

@@ -73,7 +73,7 @@ struct FwdParams {
   float* cvec;  // [n_slots, Hv, kCvecFloats] chunk vectors
   __nv_bfloat16 *tb, *gkk, *pb;  // [n_slots, Hv] 8 KiB tile images for the backward (or null)
   __nv_bfloat16* db;             // [n_slots, Hv, Dv / 64] Delta tile images for the backward (or null)
-  float* t_f32;                  // [n_slots, Hv, 64, 64] T = (I + A)^-1 for the fused scan
+  __nv_bfloat16* tu_img;         // [n_slots, Hv, 2, 4096] T diag(beta) hi, lo images (fused scan)
   const int32_t* cu_seqlens;
   int64_t T;
   int Hk, Hv, Dv, G, N;
@@ -229,8 +229,9 @@ struct PrepSmem {
   static_assert(WST - TW >= kF32Tile, "Tw, Tu hold a second fp32 tile for the Neumann products");
 };
 
-// TOUT: the variant for the fused scan, which forms U itself: T is written in
-// fp32 to p.t_f32 and U is not computed.
+// TOUT: the variant for the fused scan, which forms U itself: T diag(beta),
+// split into hi and lo bf16 halves, is written as two tile images to
+// p.tu_img, and U is not computed.
 template <int DK, int WM, bool TOUT>
 __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __grid_constant__ FwdParams p) {
   using S = PrepSmem<DK>;
@@ -361,27 +362,29 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __g
   // ---- a4 operands: Tw = T diag(beta e^gamma), Tu = T diag(beta), split hi/lo;
   //      T itself as the backward's tile image ----
   __nv_bfloat16* timg = p.tb ? p.tb + (slot * p.Hv + h) * (kTileImgBytes / 2) : nullptr;
-  float* tf = TOUT ? p.t_f32 + (slot * p.Hv + h) * (kChunk * kChunk) : nullptr;
   for (int e = threadIdx.x; e < 64 * 32; e += kPrepThreads) {
     const int i = e >> 5, j = (e & 31) * 2;
     const float2 tt = *reinterpret_cast<const float2*>(Ts + i * kSA + j);
     const float t0 = (j <= i) ? tt.x : 0.f;
     const float t1 = (j + 1 <= i) ? tt.y : 0.f;
     if (timg) st_bf16x2(timg + swz<64>(i, j), t0, t1);
-    if constexpr (TOUT) *reinterpret_cast<float2*>(tf + i * kChunk + j) = make_float2(t0, t1);
     float a0, a1, b0, b1;
     split_bf16(t0 * beg[j], a0, b0);
     split_bf16(t1 * beg[j + 1], a1, b1);
     st_bf16x2(TwH + swz<64>(i, j), a0, a1);
     st_bf16x2(TwL + swz<64>(i, j), b0, b1);
-    if constexpr (!TOUT) {
-      split_bf16(t0 * bet[j], a0, b0);
-      split_bf16(t1 * bet[j + 1], a1, b1);
-      st_bf16x2(TuH + swz<64>(i, j), a0, a1);
-      st_bf16x2(TuL + swz<64>(i, j), b0, b1);
-    }
+    split_bf16(t0 * bet[j], a0, b0);
+    split_bf16(t1 * bet[j + 1], a1, b1);
+    st_bf16x2(TuH + swz<64>(i, j), a0, a1);
+    st_bf16x2(TuL + swz<64>(i, j), b0, b1);
   }
   __syncthreads();
+  if constexpr (TOUT) {
+    // the Tu hi and lo images (contiguous in shared memory) for the fused scan
+    uint4* dst = reinterpret_cast<uint4*>(p.tu_img + (slot * p.Hv + h) * (2 * kChunk * kChunk));
+    const uint4* src = reinterpret_cast<const uint4*>(TuH);
+    for (int e = threadIdx.x; e < 2 * kChunk * kChunk * 2 / 16; e += kPrepThreads) dst[e] = src[e];
+  }
 
   // ---- a4: W = Tw K [64 x DK] (warp: 16 rows x DK/2 columns), hi and lo passes ----
   constexpr int NTW = DK / 16;
@@ -1244,7 +1247,7 @@ gdn_status launch_fused(const gdn_problem& p, const FwdParams& prm, const Dims& 
   f.tm_q = prm.tm_q;
   f.tm_v = prm.tm_v;
   f.tm_wc = prm.tm_wc;
-  f.t_f32 = prm.t_f32;
+  f.tu_img = prm.tu_img;
   f.cvec = prm.cvec;
   f.w_scales = prm.w_scales;
   f.h0 = prm.h0;
@@ -1332,7 +1335,7 @@ gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const 
   prm.gkk = reinterpret_cast<__nv_bfloat16*>(at(L.gkk));
   prm.pb = reinterpret_cast<__nv_bfloat16*>(at(L.pb));
   prm.db = reinterpret_cast<__nv_bfloat16*>(at(L.db));
-  prm.t_f32 = reinterpret_cast<float*>(at(L.t_f32));
+  prm.tu_img = reinterpret_cast<__nv_bfloat16*>(at(L.tu_img));
   prm.h_codes = at(L.h_codes);
   prm.h_scales = reinterpret_cast<float*>(at(L.h_scales));
   prm.h_full = reinterpret_cast<float*>(at(L.h_full));

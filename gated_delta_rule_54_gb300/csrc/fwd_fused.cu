@@ -42,31 +42,30 @@ namespace {
 
 __device__ int g_fused_device_error;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 
 // shared memory (bytes from a 1024-aligned base)
 struct FSmem {
-  static constexpr int AQW = 0;                    // [W^ ; Q]: 2 dk panels x 128 rows x 128 B
-  static constexpr int KT = AQW + 2 * 16384;       // 2 buffers x K (2 panels x 64 rows x 128 B)
+  static constexpr int AQW = 0;                    // 2 buffers x [W^ ; Q]: 2 dk panels x 128 rows x 128 B
+  static constexpr int KT = AQW + 2 * 32768;       // 2 buffers x K (2 panels x 64 rows x 128 B)
   static constexpr int VT = KT + 2 * 16384;        // V block [64 tok][64 v] bf16 (TMA, swizzled)
-  static constexpr int TF = VT + 8192;             // T fp32 [64][64] (bulk copy)
-  static constexpr int WC = TF + 16384;            // W codes [64][128] u8 (TMA)
-  static constexpr int ATU = WC + 8192;            // Tu hi rows, Tu lo rows (8 KB each) ...
-  static constexpr int AP = ATU + 16384;           // ... then P hi, P lo: [Tu_lo ; P_hi] is contiguous
-  static constexpr int HB = AP + 16384;            // H^ codes as bf16 [128 dk][64 v]
+  static constexpr int WC = VT + 8192;             // W codes [64][128] u8 (TMA)
+  static constexpr int ATU = WC + 8192;            // Tu hi, Tu lo images (bulk copy) ...
+  static constexpr int AP = ATU + 16384;           // ... then P lo, P hi, P lo
+  static constexpr int HB = AP + 24576;            // H^ codes as bf16 [128 dk][64 v]
   static constexpr int DP = HB + 16384;            // decayed Delta hi, lo [64 tok][64 v]
   static constexpr int DD = DP + 16384;            // Delta hi, lo
   static constexpr int CV = DD + 16384;            // 2 buffers x chunk vectors (1280 B)
   static constexpr int BYTES = CV + 2 * kCvecFloats * 4 + 1024;  // + alignment slack
   static_assert(BYTES <= 232448, "shared memory budget");
-  static_assert(AP == ATU + 16384, "[Tu_lo ; P_hi] must be contiguous");
+  static_assert(AP == ATU + 16384, "[Tu_lo ; P_lo] read contiguously by the U product");
 };
 
 // TMEM accumulator columns
 constexpr uint32_t kD1 = 0, kD2 = 64, kD3 = 128, kD4 = 192, kD5 = 256, kTmemCols = 512;
 
-// bytes of one chunk's inputs: K, Q (2 boxes each), V, W codes, T, chunk vectors
+// bytes of one chunk's inputs: K, Q (2 boxes each), V, W codes, Tu images, chunk vectors
 constexpr uint32_t kChunkTx = 2 * 8192 + 2 * 8192 + 8192 + 8192 + 16384 + kCvecFloats * 4;
 
 // ---------------------------------------------------------------------------
@@ -104,21 +103,34 @@ __device__ __forceinline__ void tc_fence_before() {
 __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
 }
-// 32 consecutive fp32 columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
+// 16 consecutive fp32 columns of this thread's TMEM lane
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
+      "%15}, [%16];\n"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        "=r"(r[14]), "=r"(r[15])
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// 2^x by the hardware approximation (relative error about 2^-22; subnormal
+// results flush to zero)
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// (hi, lo) bf16 pairs of (x0, x1): hi = bf16(x), lo = bf16(x - hi), packed
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf16(x0, x1);
+  const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
+  lo = pack_bf16(x0 - h0, x1 - h1);
 }
 
 // byte offset of element (row, col) in a tile of 128-byte rows (64 bf16),
@@ -134,6 +146,54 @@ __device__ __forceinline__ void st8_bf16(unsigned char* tile, int row, int c8, c
   u.z = pack_bf16(x[4], x[5]);
   u.w = pack_bf16(x[6], x[7]);
   *reinterpret_cast<uint4*>(tile + sw_off(row, 8 * c8)) = u;
+}
+// sixteen values at (row, 16 c16 ..) split into hi and lo tiles
+__device__ __forceinline__ void st16_split(unsigned char* hi_tile, unsigned char* lo_tile, int row,
+                                           int col, const float* x) {
+  uint32_t h[8], l[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) split2(x[2 * i], x[2 * i + 1], h[i], l[i]);
+  *reinterpret_cast<uint4*>(hi_tile + sw_off(row, col)) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(hi_tile + sw_off(row, col + 8)) = make_uint4(h[4], h[5], h[6], h[7]);
+  *reinterpret_cast<uint4*>(lo_tile + sw_off(row, col)) = make_uint4(l[0], l[1], l[2], l[3]);
+  *reinterpret_cast<uint4*>(lo_tile + sw_off(row, col + 8)) = make_uint4(l[4], l[5], l[6], l[7]);
+}
+
+// Sixteen state values quantized with scale reciprocal rcp: codes (packed
+// little-endian in c4), dequantized values x <- code * s, and the codes' values
+// (exact in bf16) in v.  zero: the tile's amax is 0 (signed-zero codes, values
+// kept, which are zeros).
+template <int SM>
+__device__ __forceinline__ void quant16(float (&x)[16], float rcp, float s, bool zero,
+                                        float (&v)[16], uint32_t (&c4)[4]) {
+  if constexpr (SM == GDN_QDQ_E4M3) {
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+      float2 val;
+      const uint16_t c2 = e4m3_code2(x[j], x[j + 1], rcp, val);
+      v[j] = val.x;
+      v[j + 1] = val.y;
+      if (!zero) {
+        x[j] = __fmul_rn(val.x, s);
+        x[j + 1] = __fmul_rn(val.y, s);
+      }
+      if (j % 4 == 0)
+        c4[j / 4] = c2;
+      else
+        c4[j / 4] |= (uint32_t)c2 << 16;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint8_t cd = zero ? qdq_zero_code<SM>(x[j]) : qdq_code<SM>(x[j], rcp);
+      v[j] = zero ? 0.f : qdq_code_value<SM>(cd);
+      if (!zero) x[j] = __fmul_rn(v[j], s);
+      if (j % 4 == 0)
+        c4[j / 4] = cd;
+      else
+        c4[j / 4] |= (uint32_t)cd << (8 * (j % 4));
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -151,9 +211,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
   const int vb = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
   const int hk = h / p.G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quad = warp & 3, half = warp >> 2;
-  const int row = 32 * quad + lane;  // TMEM lane: accumulator row
-  const int col0 = 32 * half;        // this thread's 32 columns of the 64
+  const int quad = warp & 3;         // TMEM lane quadrant of this warp
+  const int row = 32 * quad + lane;  // accumulator row (TMEM lane)
+  const int col0 = 16 * (warp >> 2); // this thread's 16 columns of the 64
   const bool lo_rows = quad < 2;     // rows 0-63 (tokens of the W^ / U / Delta products)
   const int t_row = row & 63;        // token of this row in the chunk
 
@@ -171,15 +231,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
   }
   const int nch = (L + kChunk - 1) / kChunk;
 
-  unsigned char* AQW = sm + FSmem::AQW;
   unsigned char* VT = sm + FSmem::VT;
-  const float* TF = reinterpret_cast<const float*>(sm + FSmem::TF);
   const uint8_t* WCs = sm + FSmem::WC;
   unsigned char* ATU = sm + FSmem::ATU;
   unsigned char* AP = sm + FSmem::AP;
   unsigned char* HB = sm + FSmem::HB;
   unsigned char* DP = sm + FSmem::DP;
   unsigned char* DD = sm + FSmem::DD;
+  auto AQWb = [&](int b) { return sm + FSmem::AQW + b * 32768; };
   auto KTb = [&](int b) { return sm + FSmem::KT + b * 16384; };
   auto CVb = [&](int b) { return reinterpret_cast<float*>(sm + FSmem::CV + b * kCvecFloats * 4); };
 
@@ -201,44 +260,39 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
     fence_mbar_init();
   }
 
-  // TMA of chunk c's inputs, in the order the chunk frees their buffers
-  auto load_kc = [&](int c) {  // K and chunk vectors (double buffered); opens the chunk's tx
+  // TMA of chunk c's inputs, each issued once the buffer it fills is free
+  auto load_kqc = [&](int c) {  // K, Q, chunk vectors (double buffered); opens the chunk's tx
     const int b = c & 1;
     const int64_t tok = tok0 + (int64_t)c * kChunk;
     mbar_expect_tx(&bar_in[b], kChunkTx);
     bulk_load_1d(CVb(b), p.cvec + ((slot0 + c) * p.Hv + h) * kCvecFloats, kCvecFloats * 4,
                  &bar_in[b]);
 #pragma unroll
-    for (int pn = 0; pn < 2; ++pn)
+    for (int pn = 0; pn < 2; ++pn) {
       tma_load_2d(KTb(b) + pn * 8192, &p.tm_k, hk * 128 + pn * 64, (int)tok, &bar_in[b]);
+      tma_load_2d(AQWb(b) + pn * 16384 + 8192, &p.tm_q, hk * 128 + pn * 64, (int)tok, &bar_in[b]);
+    }
   };
-  auto load_tw = [&](int c) {  // T and W codes (single buffered)
-    const int b = c & 1;
+  auto load_w = [&](int c) {  // W codes
     const int64_t tok = tok0 + (int64_t)c * kChunk;
-    bulk_load_1d(sm + FSmem::TF, p.t_f32 + ((slot0 + c) * p.Hv + h) * (kChunk * kChunk),
-                 kChunk * kChunk * 4, &bar_in[b]);
-    tma_load_2d(sm + FSmem::WC, &p.tm_wc, h * 128, (int)tok, &bar_in[b]);
+    tma_load_2d(sm + FSmem::WC, &p.tm_wc, h * 128, (int)tok, &bar_in[c & 1]);
   };
-  auto load_v = [&](int c) {
+  auto load_vt = [&](int c) {  // V block and the Tu images
     const int b = c & 1;
     const int64_t tok = tok0 + (int64_t)c * kChunk;
     tma_load_2d(VT, &p.tm_v, h * 128 + vb * 64, (int)tok, &bar_in[b]);
-  };
-  auto load_q = [&](int c) {  // Q into rows 64-127 of both panels of [W^ ; Q]
-    const int b = c & 1;
-    const int64_t tok = tok0 + (int64_t)c * kChunk;
-#pragma unroll
-    for (int pn = 0; pn < 2; ++pn)
-      tma_load_2d(AQW + pn * 16384 + 8192, &p.tm_q, hk * 128 + pn * 64, (int)tok, &bar_in[b]);
+    bulk_load_1d(ATU,
+                 reinterpret_cast<const unsigned char*>(p.tu_img) + ((slot0 + c) * p.Hv + h) * 16384,
+                 16384, &bar_in[b]);
   };
 
-  // ---- the state: thread (row dk, col0) holds H[dk][col0 .. col0 + 31] ----
-  float hv[32];
+  // ---- the state: thread (row dk, col0) holds H[dk][col0 .. col0 + 15] ----
+  float hv[16];
   {
     const float* src = p.h0 ? p.h0 + (((int64_t)n * p.Hv + h) * 128 + row) * 128 + vb * 64 + col0
                             : nullptr;
 #pragma unroll
-    for (int j = 0; j < 32; j += 4) {
+    for (int j = 0; j < 16; j += 4) {
       float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
       if (src) x = *reinterpret_cast<const float4*>(src + j);
       hv[j] = x.x;
@@ -250,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
   auto amax_partial = [&]() {
     float m = 0.f;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) m = fmaxf(m, fabsf(hv[j]));
+    for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(hv[j]));
     m = warp_max(m);
     if (lane == 0) red[warp] = m;
   };
@@ -263,10 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
   const uint32_t tl = tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)col0;  // this thread's lane
 
   if (tid == 0 && nch > 0) {
-    load_kc(0);
-    load_tw(0);
-    load_v(0);
-    load_q(0);
+    load_kqc(0);
+    load_w(0);
+    load_vt(0);
   }
 
   bool bad = false;
@@ -278,6 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
     const int Lc = min(L - c * kChunk, kChunk);
     const uint32_t ph = (uint32_t)c & 1u;
     const float sW = p.w_scales[slot * p.Hv + h];
+    unsigned char* AQW = AQWb(b);
 
     // ---- a6: state QDQ of the state entering chunk c ----
     bad |= !mbar_wait(&bar_in[b], (uint32_t)(c >> 1) & 1u);
@@ -288,81 +342,47 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
     float sH, rcp;
     qdq_scale<SM>(amax, sH, rcp);
     {
-      uint32_t cw[8];  // the 32 codes, packed
-#pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) {
-        float vals[8];
-#pragma unroll
-        for (int e = 0; e < 8; e += 4) {
-          uint32_t w4 = 0;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int j = 8 * q8 + e + i;
-            uint8_t cd;
-            float val = 0.f;
-            if (amax == 0.f) {
-              cd = qdq_zero_code<SM>(hv[j]);  // zeros pass through; the operand holds zeros
-            } else {
-              cd = qdq_code<SM>(hv[j], rcp);
-              val = qdq_code_value<SM>(cd);
-              hv[j] = __fmul_rn(val, sH);
-            }
-            vals[e + i] = val;
-            w4 |= (uint32_t)cd << (8 * i);
-          }
-          cw[2 * q8 + e / 4] = w4;
-        }
-        // H^ codes as bf16 values: the MN-major B operand [dk][v]
-        st8_bf16(HB, row, (col0 >> 3) + q8, vals);
-      }
+      float vals[16];
+      uint32_t c4[4];
+      quant16<SM>(hv, rcp, sH, amax == 0.f, vals, c4);
+      // H^ codes as bf16 values: the MN-major B operand [dk][v]
+      st8_bf16(HB, row, col0 >> 3, vals);
+      st8_bf16(HB, row, (col0 >> 3) + 1, vals + 8);
       if (p.h_codes) {
         uint8_t* dst = p.h_codes + ((slot * p.Hv + h) * 128 + row) * 128 + vb * 64 + col0;
-        *reinterpret_cast<uint4*>(dst) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-        *reinterpret_cast<uint4*>(dst + 16) = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+        *reinterpret_cast<uint4*>(dst) = make_uint4(c4[0], c4[1], c4[2], c4[3]);
         if (tid == 0) p.h_scales[(slot * p.Hv + h) * 2 + vb] = sH;
       }
     }
-    if (tid == 0 && c + 1 < nch) load_kc(c + 1);  // buffers of chunk c - 1: free
+    if (tid == 0 && c + 1 < nch) load_kqc(c + 1);  // buffers of chunk c - 1: free
 
-    // ---- operands: W^ codes -> bf16 rows 0-63 of [W^ ; Q]; Tu = T diag(beta) hi / lo ----
+    // ---- W^ codes -> bf16 values in rows 0-63 of [W^ ; Q] ----
     const float* cv = CVb(b);
     {
-      // W^: thread -> row tid / 4, 32 codes from dk 32 (tid % 4)
-      const int r = tid >> 2, d0 = (tid & 3) * 32;
-      const uint4 c16a = *reinterpret_cast<const uint4*>(WCs + r * 128 + d0);
-      const uint4 c16b = *reinterpret_cast<const uint4*>(WCs + r * 128 + d0 + 16);
-      const uint32_t cw[8] = {c16a.x, c16a.y, c16a.z, c16a.w, c16b.x, c16b.y, c16b.z, c16b.w};
+      const int r = tid >> 3, d0 = (tid & 7) * 16;  // row, first of 16 codes
+      const uint4 cw = *reinterpret_cast<const uint4*>(WCs + r * 128 + d0);
+      const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
+      float x[16];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float4 a = qdq_code4_values<WM>(w4[i]);
+        x[4 * i] = a.x;
+        x[4 * i + 1] = a.y;
+        x[4 * i + 2] = a.z;
+        x[4 * i + 3] = a.w;
+      }
       unsigned char* panel = AQW + (d0 >> 6) * 16384;
-#pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) {
-        float x[8];
-        const float4 a = qdq_code4_values<WM>(cw[2 * q8]);
-        const float4 bq = qdq_code4_values<WM>(cw[2 * q8 + 1]);
-        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-        x[4] = bq.x; x[5] = bq.y; x[6] = bq.z; x[7] = bq.w;
-        st8_bf16(panel, r, ((d0 & 63) >> 3) + q8, x);
-      }
-      // Tu: warp -> rows 8 warp .. 8 warp + 7, lane -> columns 2 lane, 2 lane + 1
-      const float b0 = cv[kCvBet + 2 * lane], b1 = cv[kCvBet + 2 * lane + 1];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int ri = 8 * warp + i;
-        const float2 t2 = *reinterpret_cast<const float2*>(TF + ri * 64 + 2 * lane);
-        float h0v, l0v, h1v, l1v;
-        split_bf16(t2.x * b0, h0v, l0v);
-        split_bf16(t2.y * b1, h1v, l1v);
-        *reinterpret_cast<uint32_t*>(ATU + sw_off(ri, 2 * lane)) = pack_bf16(h0v, h1v);
-        *reinterpret_cast<uint32_t*>(ATU + 8192 + sw_off(ri, 2 * lane)) = pack_bf16(l0v, l1v);
-      }
+      st8_bf16(panel, r, (d0 & 63) >> 3, x);
+      st8_bf16(panel, r, ((d0 & 63) >> 3) + 1, x + 8);
     }
-    fence_proxy_async();  // generic-proxy writes of HB, AQW, ATU before the MMAs read them
+    fence_proxy_async();  // generic-proxy writes of HB and AQW before the MMAs read them
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
 
     // ---- the chunk's first products ----
     if (tid == 0) {
-      if (c + 1 < nch) load_tw(c + 1);  // T and W codes of this chunk are consumed
+      if (c + 1 < nch) load_w(c + 1);  // W codes of this chunk are converted
       const uint32_t aq = smem_u32(AQW), atu = smem_u32(ATU), vt = smem_u32(VT);
       const uint32_t kt = smem_u32(KTb(b)), hb = smem_u32(HB);
       // D3 = [Tu_hi ; *] V + [Tu_lo ; *] V  (U in rows 0-63)
@@ -391,65 +411,61 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
     // ---- U (rows 0-63) and P (rows 64-127) ----
     bad |= !mbar_wait(&bar_u, ph);
     tc_fence_after();
-    if (tid == 0 && c + 1 < nch) load_v(c + 1);  // D3 has read V
-    float u[32];
+    if (tid == 0 && c + 1 < nch) load_vt(c + 1);  // D3 has read V and Tu
+    float u[16];
     if (lo_rows) {
-      tmem_ld32(tl + kD3, u);
+      tmem_ld16(tl + kD3, u);
     } else {
-      // P_ij = e^{gamma_i - gamma_j} q_i.k_j for j <= i (i = t_row, j = col0 + jj)
-      float x[32];
-      tmem_ld32(tl + kD4, x);
+      // P_ij = 2^{(gamma_i - gamma_j) log2 e} q_i.k_j for j <= i (i = t_row, j = col0 + jj)
+      float x[16];
+      tmem_ld16(tl + kD4, x);
+      constexpr float kLog2e = 1.4426950408889634f;
       const float gi = cv[kCvGam + t_row];
-      float ph_[8], pl_[8];
-      __nv_bfloat16* pimg = p.pb ? reinterpret_cast<__nv_bfloat16*>(p.pb) + (slot * p.Hv + h) * 4096
-                                 : nullptr;
 #pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) {
+      for (int jj = 0; jj < 16; ++jj) {
+        const int j = col0 + jj;
+        x[jj] = (j <= t_row) ? ex2_approx((gi - cv[kCvGam + j]) * kLog2e) * x[jj] : 0.f;
+      }
+      // [P_lo | P_hi | P_lo]: hi at +8 KB, lo at 0 and +16 KB
+      st16_split(AP + 8192, AP, t_row, col0, x);
+      *reinterpret_cast<uint4*>(AP + 16384 + sw_off(t_row, col0)) =
+          *reinterpret_cast<const uint4*>(AP + sw_off(t_row, col0));
+      *reinterpret_cast<uint4*>(AP + 16384 + sw_off(t_row, col0 + 8)) =
+          *reinterpret_cast<const uint4*>(AP + sw_off(t_row, col0 + 8));
+      if (p.pb && vb == 0) {
+        unsigned char* pimg = reinterpret_cast<unsigned char*>(p.pb) + (slot * p.Hv + h) * 8192;
+        float z[16];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int j = col0 + 8 * q8 + e;
-          const float pv = (j <= t_row) ? expf(gi - cv[kCvGam + j]) * x[8 * q8 + e] : 0.f;
-          split_bf16(pv, ph_[e], pl_[e]);
-          x[8 * q8 + e] = pv;
-        }
-        st8_bf16(AP, t_row, (col0 >> 3) + q8, ph_);
-        st8_bf16(AP + 8192, t_row, (col0 >> 3) + q8, pl_);
-        if (pimg && vb == 0) {
-          float z[8];
-#pragma unroll
-          for (int e = 0; e < 8; ++e) z[e] = t_row < Lc ? x[8 * q8 + e] : 0.f;
-          st8_bf16(reinterpret_cast<unsigned char*>(pimg), t_row, (col0 >> 3) + q8, z);
-        }
+        for (int jj = 0; jj < 16; ++jj) z[jj] = t_row < Lc ? x[jj] : 0.f;
+        st8_bf16(pimg, t_row, col0 >> 3, z);
+        st8_bf16(pimg, t_row, (col0 >> 3) + 1, z + 8);
       }
     }
 
     // ---- a7: Delta = U - sW sH W^ H^ (rows 0-63); decayed Delta' for the state update ----
     bad |= !mbar_wait(&bar_a, ph);
     tc_fence_after();
-    if (tid == 0 && c + 1 < nch) load_q(c + 1);  // D1 and D4 have read Q and W^
     if (lo_rows) {
-      float y[32];
-      tmem_ld32(tl + kD1, y);
+      float y[16];
+      tmem_ld16(tl + kD1, y);
       const float sWH = sW * sH;
       const bool valid = t_row < Lc;
       const float di = valid ? cv[kCvDec + t_row] : 0.f;
-      __nv_bfloat16* dimg =
-          p.db ? reinterpret_cast<__nv_bfloat16*>(p.db) + ((slot * p.Hv + h) * 2 + vb) * 4096 : nullptr;
+      float dl[16], dd[16];
 #pragma unroll
-      for (int q8 = 0; q8 < 4; ++q8) {
-        float dh[8], dl[8], eh[8], el[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int j = 8 * q8 + e;
-          const float dlt = valid ? u[j] - sWH * y[j] : 0.f;
-          split_bf16(dlt, dh[e], dl[e]);
-          split_bf16(dlt * di, eh[e], el[e]);
-        }
-        st8_bf16(DD, t_row, (col0 >> 3) + q8, dh);
-        st8_bf16(DD + 8192, t_row, (col0 >> 3) + q8, dl);
-        st8_bf16(DP, t_row, (col0 >> 3) + q8, eh);
-        st8_bf16(DP + 8192, t_row, (col0 >> 3) + q8, el);
-        if (dimg) st8_bf16(reinterpret_cast<unsigned char*>(dimg), t_row, (col0 >> 3) + q8, dh);
+      for (int j = 0; j < 16; ++j) {
+        dl[j] = valid ? u[j] - sWH * y[j] : 0.f;
+        dd[j] = dl[j] * di;
+      }
+      st16_split(DD, DD + 8192, t_row, col0, dl);
+      st16_split(DP, DP + 8192, t_row, col0, dd);
+      if (p.db) {
+        // the Delta image: the hi half (Delta rounded to bf16), as stored in DD
+        unsigned char* dimg = reinterpret_cast<unsigned char*>(p.db) + ((slot * p.Hv + h) * 2 + vb) * 8192;
+        *reinterpret_cast<uint4*>(dimg + sw_off(t_row, col0)) =
+            *reinterpret_cast<const uint4*>(DD + sw_off(t_row, col0));
+        *reinterpret_cast<uint4*>(dimg + sw_off(t_row, col0 + 8)) =
+            *reinterpret_cast<const uint4*>(DD + sw_off(t_row, col0 + 8));
       }
     }
     fence_proxy_async();
@@ -471,19 +487,20 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
         umma(tmem + kD2, sdesc(kt + ks * 2048, 8192, 1024), sdesc(dp + 8192 + ks * 2048, 8192, 1024),
              kIdMM, true);
       umma_commit(&bar_s);
-      // D5 = [* ; P_hi] Delta_hi + [* ; P_hi] Delta_lo + [* ; P_lo] Delta_hi  (rows 64-127)
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        umma(tmem + kD5, sdesc(ap - 8192 + ks * 32, 16, 1024), sdesc(dd + ks * 2048, 8192, 1024),
-             kIdKM, ks > 0);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        umma(tmem + kD5, sdesc(ap - 8192 + ks * 32, 16, 1024),
-             sdesc(dd + 8192 + ks * 2048, 8192, 1024), kIdKM, true);
+      // D5 = [P_lo ; P_hi] Delta_hi + [P_lo ; P_hi] Delta_lo + [P_hi ; P_lo] Delta_hi
+      //      (rows 64-127: P Delta to ~16 bits)
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks)
         umma(tmem + kD5, sdesc(ap + ks * 32, 16, 1024), sdesc(dd + ks * 2048, 8192, 1024), kIdKM,
-             true);
+             ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        umma(tmem + kD5, sdesc(ap + ks * 32, 16, 1024), sdesc(dd + 8192 + ks * 2048, 8192, 1024),
+             kIdKM, true);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        umma(tmem + kD5, sdesc(ap + 8192 + ks * 32, 16, 1024), sdesc(dd + ks * 2048, 8192, 1024),
+             kIdKM, true);
       umma_commit(&bar_o);
     }
 
@@ -491,26 +508,26 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
     bad |= !mbar_wait(&bar_s, ph);
     tc_fence_after();
     {
-      float z[32];
-      tmem_ld32(tl + kD2, z);
+      float z[16];
+      tmem_ld16(tl + kD2, z);
       const float egL = cv[kCvEg + 63];  // gamma is flat past the last valid row
 #pragma unroll
-      for (int j = 0; j < 32; ++j) hv[j] = hv[j] * egL + z[j];
+      for (int j = 0; j < 16; ++j) hv[j] = hv[j] * egL + z[j];
       amax_partial();
     }
 
     // ---- a8: O = scale (e^gamma sH Q H^ + P Delta) (rows 64-127) ----
-    bad |= !mbar_wait(&bar_o, ph);
-    tc_fence_after();
     if (!lo_rows) {
-      float qh[32], pd[32];
-      tmem_ld32(tl + kD1, qh);
-      tmem_ld32(tl + kD5, pd);
+      bad |= !mbar_wait(&bar_o, ph);
+      tc_fence_after();
+      float qh[16], pd[16];
+      tmem_ld16(tl + kD1, qh);
+      tmem_ld16(tl + kD5, pd);
       if (t_row < Lc) {
         const float ei = cv[kCvEg + t_row] * sH;
         float* dst = p.o + ((tok + t_row) * p.Hv + h) * 128 + vb * 64 + col0;
 #pragma unroll
-        for (int j = 0; j < 32; j += 4)
+        for (int j = 0; j < 16; j += 4)
           *reinterpret_cast<float4*>(dst + j) =
               make_float4(p.scale * (ei * qh[j] + pd[j]), p.scale * (ei * qh[j + 1] + pd[j + 1]),
                           p.scale * (ei * qh[j + 2] + pd[j + 2]), p.scale * (ei * qh[j + 3] + pd[j + 3]));
@@ -523,7 +540,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
   if (!bad && p.ht) {
     float* dst = p.ht + (((int64_t)n * p.Hv + h) * 128 + row) * 128 + vb * 64 + col0;
 #pragma unroll
-    for (int j = 0; j < 32; j += 4)
+    for (int j = 0; j < 16; j += 4)
       *reinterpret_cast<float4*>(dst + j) = make_float4(hv[j], hv[j + 1], hv[j + 2], hv[j + 3]);
   }
 

@@ -28,7 +28,7 @@ struct Dims {
 // Byte offsets of the context segments (see gdn_ctx_bytes); -1 where absent.
 struct CtxLayout {
   int64_t w_codes = -1, w_scales = -1, w_full = -1, cvec = -1, tb = -1, gkk = -1, pb = -1,
-          db = -1, t_f32 = -1, h_codes = -1, h_scales = -1, h_full = -1;
+          db = -1, tu_img = -1, h_codes = -1, h_scales = -1, h_full = -1;
   size_t total = 0;
 };
 

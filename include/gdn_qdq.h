@@ -144,9 +144,11 @@ int64_t gdn_num_chunk_slots(const gdn_problem* p);
  *             each 64 x 64 tile stored as its shared-memory image: element
  *             (i, j) at i * 64 + 8 * ((j / 8) ^ (i % 8)) + j % 8; rows past
  *             the chunk end are zero (T: identity rows)
- *   t_f32     f32 [n_slots, Hv, 64, 64] T row-major (fused forward only: Dk =
- *                                       Dv = 128, both sites quantized,
- *                                       block_v 64, exact solve)
+ *   tu_img    bf16 [n_slots, Hv, 2, 4096] T diag(beta) split into hi + lo bf16
+ *                                       halves (hi = bf16(x), lo = bf16(x - hi)),
+ *                                       as images like the tiles above (fused
+ *                                       forward only: Dk = Dv = 128, both sites
+ *                                       quantized, block_v 64, exact solve)
  *   h_codes   u8  [n_slots, Hv, Dk, Dv] state codes entering each chunk (state_mode != NONE;
  *                                       absent for a forward-only fused call)
  *   h_scales  f32 [n_slots, Hv, Dv/block_v] state scale per [Dk, block_v] tile (as h_codes)
@@ -159,7 +161,7 @@ size_t gdn_ctx_bytes(const gdn_problem* p);
 
 typedef enum {
   GDN_CTX_W_CODES = 0, GDN_CTX_W_SCALES, GDN_CTX_W_FULL, GDN_CTX_CVEC, GDN_CTX_T_IMG,
-  GDN_CTX_GKK_IMG, GDN_CTX_P_IMG, GDN_CTX_D_IMG, GDN_CTX_T_F32, GDN_CTX_H_CODES,
+  GDN_CTX_GKK_IMG, GDN_CTX_P_IMG, GDN_CTX_D_IMG, GDN_CTX_TU_IMG, GDN_CTX_H_CODES,
   GDN_CTX_H_SCALES, GDN_CTX_H_FULL
 } gdn_ctx_segment;
 
