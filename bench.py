@@ -1,16 +1,23 @@
 #!/usr/bin/env python
 """Benchmark of the chunked gated delta rule with state / W fake QDQ on GB300.
 
-One step = one pass of the hot path over one batch of the single-layer
-workload (B=4, T=4096, H=16, Dk=Dv=128, E4M3 state and W QDQ, h0 ~ N(0, 0.1^2)):
-the forward (saving the QDQ context) followed by the identity-STE backward
-(``--mode fwdbwd``, the default once the backward is present), or the
-forward alone (``--mode fwd``).  ``--mode decode`` times the decode QAT step
-instead (256 sequences, one token each, carried fp32 states of 256 MiB);
+Default (``--mode fwdbwd``): one step = one pass of the hot path over one
+global batch made of micro-batches of the forward+backward workload (B=8,
+T=4096, H=16, Dk=Dv=128, E4M3 state and W QDQ, h0 ~ N(0, 0.1^2), dO and
+dht as upstream gradients): per micro-batch the forward (saving the
+backward's context) and the identity-STE backward.  The number of
+micro-batches is chosen during warm-up so that a step lasts about 50 ms of
+device time (stated in ``config``).  After the timed steps the forward alone
+(no backward context) is timed on the single-layer workload (B=4, T=4096,
+H=16, D=128): the configuration the forward's roofline target is set on,
+reported as ``roofline``; the backward's roofline is ``roofline_bwd``.
+``--mode fwd`` times the forward alone; ``--mode decode`` the decode QAT step
+(256 sequences, one token each, carried fp32 states of 256 MiB);
 ``--mode kda`` the KDA recurrence and ``--mode two_precision`` the
-two-precision profile (fp32 anchor, E4M3 read copy), both B=4, T=4096, H=16.  Inputs are synthetic (seeded) and resident
-in HBM when the timed region starts; per step the inputs (~350 MB) exceed
-the 129 MB L2, so no flush is needed between steps.
+two-precision profile (fp32 anchor, E4M3 read copy), both B=4, T=4096,
+H=16.  Inputs are synthetic (seeded) and resident in HBM when the timed
+region starts; every micro-batch's inputs exceed the 129 MB L2, so no flush
+is needed between them.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the CPU oracle
 (fp64 chunked reference) on a bounded sample of the same workload instead.
@@ -235,13 +242,15 @@ def e2e_pipelined(dev, ws, steps, warmup, host_in, dev_in, run, res_h):
     return t["pipelined"], t["serial"]
 
 
-def _peaks():
+def _peaks(tensor_key="bf16_tflops"):
+    """(HBM GB/s, dense bf16 TFLOP/s, source): the driver's measured peaks, else
+    the fallback figures (6.8 TB/s, 1.9 PFLOP/s burst, 1.7 sustained)."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             pk = json.load(f)
-        return float(pk["hbm_gbs"]), "measured"
+        return float(pk["hbm_gbs"]), float(pk[tensor_key]), "measured"
     except (OSError, KeyError, ValueError):
-        return 6800.0, "fallback"
+        return 6800.0, (1900.0 if tensor_key == "bf16_tflops" else 1700.0), "fallback"
 
 
 def _strip_comments(src):
@@ -336,9 +345,64 @@ def fwd_alg_flops(w):
     return per_chunk / C * w.B * w.T * w.Hv
 
 
+def bwd_alg_flops(w):
+    """Algorithmic STE-backward FLOPs: six Dk x Dv products (dH and dDelta
+    paths, 2 C Dk Dv each), ten C x C x D products (the gated attention and WY
+    gradients) and the solve's gradient, per 64-token chunk-head: 18.6 MFLOP
+    at Dk = Dv = 128 (291 kFLOP per token-head)."""
+    C, Dk, Dv = 64, w.Dk, w.Dv
+    per_chunk = 6 * 2 * C * Dk * Dv + 10 * C * C * (Dk + Dv) / 2 + 2 * C ** 3 / 3
+    return per_chunk / C * w.B * w.T * w.Hv
+
+
+def roofline_entry(alg_bytes, alg_flops, dur_ms, kernel, traffic, tensor_peak_key):
+    """Roofline record of one call: the bound is the larger of bytes / HBM peak
+    and FLOPs / bf16 tensor peak (measured peaks); achieved is in that bound's
+    unit."""
+    hbm, tensor, kind = _peaks(tensor_peak_key)
+    t_mem = alg_bytes / (hbm * 1e9)
+    t_tc = alg_flops / (tensor * 1e12)
+    if t_mem >= t_tc:
+        achieved = alg_bytes / (dur_ms / 1e3) / 1e9
+        rec = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+               "frac": round(achieved / hbm, 4)}
+    else:
+        achieved = alg_flops / (dur_ms / 1e3) / 1e12
+        rec = {"bound": "tensor", "achieved": round(achieved, 2), "peak": tensor, "unit": "TFLOP/s",
+               "frac": round(achieved / tensor, 4)}
+    rec.update({"traffic": traffic, "kernel": kernel, "peak_source": kind,
+                "alg_bytes_per_launch": int(alg_bytes), "alg_flops_per_launch": int(alg_flops),
+                "t_roof_us": round(max(t_mem, t_tc) * 1e6, 2), "launch_ms": round(dur_ms, 4)})
+    return rec
+
+
 # ----------------------------------------------------------------------------
 # our arm
 # ----------------------------------------------------------------------------
+STEP_TARGET_MS = 50.0   # micro-batches per step are chosen so that a step lasts about this long
+
+
+def _gdn_buffers(w, dev, rank, bwd, save_ctx):
+    from gated_delta_rule_54_gb300 import api, synth
+    cpu = synth.make_inputs(w)
+    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in cpu.items()}
+    p = api.make_problem(d["q"], d["k"], d["v"], None, 1.0, w.state_mode, w.w_mode,
+                         save_ctx=save_ctx)
+    d["o"] = torch.empty(w.B, w.T, w.Hv, w.Dv, device=dev)
+    d["ht"] = torch.empty(w.B, w.Hv, w.Dk, w.Dv, device=dev)
+    d["ctx"] = torch.empty(api.gdn_ctx_bytes(p), device=dev, dtype=torch.uint8)
+    if bwd:
+        gen = torch.Generator().manual_seed(1000 + rank)
+        d["do"] = torch.randn(w.B, w.T, w.Hv, w.Dv, generator=gen).to(torch.bfloat16).to(dev)
+        d["dht"] = (torch.randn(w.B, w.Hv, w.Dk, w.Dv, generator=gen) * 0.01).to(dev)
+        d["ws"] = torch.empty(max(api.gdn_bwd_workspace_bytes(p), 1), device=dev, dtype=torch.uint8)
+        f32 = dict(device=dev, dtype=torch.float32)
+        d["grads"] = (torch.empty(d["q"].shape, **f32), torch.empty(d["k"].shape, **f32),
+                      torch.empty(d["v"].shape, **f32), torch.empty(d["beta"].shape, **f32),
+                      torch.empty(d["g"].shape, **f32), torch.empty(d["ht"].shape, **f32))
+    return cpu, d
+
+
 def run_ours(args, ws, rank, local):
     from gated_delta_rule_54_gb300 import api, synth
     from gated_delta_rule_54_gb300._lib import load
@@ -349,45 +413,58 @@ def run_ours(args, ws, rank, local):
     w = synth.WORKLOADS[args.workload]
     w = synth.Workload(**{**w.__dict__, "seed": w.seed + rank})
     bwd = args.mode == "fwdbwd"
-    cpu = synth.make_inputs(w)
-    d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in cpu.items()}
-    q, k, v, beta, g, h0 = d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"]
     sm, wm = w.state_mode, w.w_mode
     bv, nd = args.block_v, args.neumann_degree
-    p = api.make_problem(q, k, v, None, 1.0, sm, wm, block_v=bv, neumann_degree=nd)
-    o = torch.empty(w.B, w.T, w.Hv, w.Dv, device=dev)
-    ht = torch.empty(w.B, w.Hv, w.Dk, w.Dv, device=dev)
-    ctx = torch.empty(api.gdn_ctx_bytes(p), device=dev, dtype=torch.uint8)
-    if bwd:
-        gen = torch.Generator().manual_seed(1000 + rank)
-        do = torch.randn(w.B, w.T, w.Hv, w.Dv, generator=gen).to(torch.bfloat16).to(dev)
-        dht = (torch.randn(w.B, w.Hv, w.Dk, w.Dv, generator=gen) * 0.01).to(dev)
-        wsb = torch.empty(max(api.gdn_bwd_workspace_bytes(p), 1), device=dev, dtype=torch.uint8)
+    # two buffer sets, used by alternate micro-batches
+    sets = [_gdn_buffers(w, dev, rank, bwd, save_ctx=bwd) for _ in range(2)]
+    cpu = sets[0][0]
     stream = torch.cuda.current_stream(dev)
     ev = lambda: torch.cuda.Event(enable_timing=True)
-
     fwd_times, bwd_times = [], []
 
-    def step(record=False):
-        e0 = ev() if record else None
-        if record:
-            e0.record(stream)
-        api.gdn_chunk_fwd_qdq(q, k, v, beta, g, h0, state_mode=sm, w_mode=wm, out=(o, ht, ctx),
+    def fwd(d):
+        api.gdn_chunk_fwd_qdq(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"], state_mode=sm,
+                              w_mode=wm, out=(d["o"], d["ht"], d["ctx"]), save_ctx=bwd,
                               block_v=bv, neumann_degree=nd)
-        if record:
-            e1 = ev()
-            e1.record(stream)
-            fwd_times.append((e0, e1))
-        if bwd:
-            api.gdn_chunk_bwd_ste(q, k, v, beta, g, ctx, do, dht, state_mode=sm, w_mode=wm,
-                                  workspace=wsb, block_v=bv, neumann_degree=nd)
-            if record:
-                e2 = ev()
-                e2.record(stream)
-                bwd_times.append((e1, e2))
 
+    def bwd_call(d):
+        api.gdn_chunk_bwd_ste(d["q"], d["k"], d["v"], d["beta"], d["g"], d["ctx"], d["do"],
+                              d["dht"], state_mode=sm, w_mode=wm, workspace=d["ws"],
+                              out=d["grads"], block_v=bv, neumann_degree=nd)
+
+    def step(micro, record=False):
+        for m in range(micro):
+            d = sets[m % 2][1]
+            e0 = ev() if record else None
+            if record:
+                e0.record(stream)
+            fwd(d)
+            if record:
+                e1 = ev()
+                e1.record(stream)
+                fwd_times.append((e0, e1))
+            if bwd:
+                bwd_call(d)
+                if record:
+                    e2 = ev()
+                    e2.record(stream)
+                    bwd_times.append((e1, e2))
+
+    # warm-up, which also sizes the step: micro-batches of the workload until a
+    # step lasts about STEP_TARGET_MS of device time (the clock sampler then
+    # sees the GPU under load for the whole timed region)
     for _ in range(args.warmup):
-        step()
+        step(1)
+    torch.cuda.synchronize()
+    a, b = ev(), ev()
+    a.record(stream)
+    step(2)
+    b.record(stream)
+    torch.cuda.synchronize()
+    one = a.elapsed_time(b) / 2
+    micro = args.micro_batches or max(1, min(64, int(round(STEP_TARGET_MS / max(one, 1e-3)))))
+    micro = int(_max_over_ranks(micro, ws, dev))
+    step(micro)
     torch.cuda.synchronize()
     _barrier(ws)
     torch.cuda.synchronize()
@@ -395,54 +472,80 @@ def run_ours(args, ws, rank, local):
         t_start, t_end = ev(), ev()
         t_start.record(stream)
         for _ in range(args.steps):
-            step(record=True)
+            step(micro, record=True)
         t_end.record(stream)
         torch.cuda.synchronize()
     _barrier(ws)
     ms_total = t_start.elapsed_time(t_end)
     ms_total = _max_over_ranks(ms_total, ws, dev)
     ms_step = ms_total / args.steps
-    tokens = w.B * w.T
+    tokens = w.B * w.T * micro
     value = tokens * ws * args.steps / (ms_total / 1e3)
-    fwd_ms = statistics.mean(a.elapsed_time(b) for a, b in fwd_times)
-    bwd_ms = statistics.mean(a.elapsed_time(b) for a, b in bwd_times) if bwd else None
-    launches_per_step = FWD_LAUNCHES + (args.bwd_launches if bwd else 0)
+    fwd_ms = statistics.mean(x.elapsed_time(y) for x, y in fwd_times)
+    bwd_ms = statistics.mean(x.elapsed_time(y) for x, y in bwd_times) if bwd else None
+    launches_per_step = micro * (_fwd_launches(w, bv, nd) + (args.bwd_launches if bwd else 0))
 
-    # roofline of the dominant kernel
-    peak, peak_kind = _peaks()
-    if bwd and bwd_ms > fwd_ms:
-        alg = bwd_alg_bytes(w)
-        dur = bwd_ms
-        kernel = "gdn backward (all launches of one call)"
-        traffic = _traffic("gdn_bwd_kernels_single_layer.md", BWD_SOURCES, args.workload)
-    else:
-        alg = fwd_alg_bytes(w, bwd)
-        dur = fwd_ms
-        kernel = "gdn forward (all launches of one call)"
-        traffic = _traffic("gdn_fwd_kernels_single_layer.md", FWD_SOURCES,
-                           args.workload + ("+ctx" if bwd else ""))
-    achieved = alg / (dur / 1e3) / 1e9
-    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": traffic, "kernel": kernel,
-            "peak_source": peak_kind, "alg_bytes_per_launch": alg,
-            "launch_ms": round(dur, 4)}
+    # the forward alone (no backward context) on the single-layer workload
+    # (B=4, T=4096, H=16, D=128): the configuration the forward's roofline
+    # target is set on; timed as its own loop after the step
+    fl = synth.WORKLOADS["layer"] if w.Dk == 128 and not w.varlen_total else w
+    fl = synth.Workload(**{**fl.__dict__, "seed": fl.seed + rank})
+    _, dl = _gdn_buffers(fl, dev, rank, False, save_ctx=False)
 
-    # end to end through the public API from pinned host buffers
+    def fwd_only():
+        api.gdn_chunk_fwd_qdq(dl["q"], dl["k"], dl["v"], dl["beta"], dl["g"], dl["h0"],
+                              state_mode=fl.state_mode, w_mode=fl.w_mode,
+                              out=(dl["o"], dl["ht"], dl["ctx"]), save_ctx=False,
+                              block_v=bv, neumann_degree=nd)
+
+    for _ in range(args.warmup):
+        fwd_only()
+    reps = max(args.steps, 50)
+    a, b = ev(), ev()
+    a.record(stream)
+    for _ in range(reps):
+        fwd_only()
+    b.record(stream)
+    torch.cuda.synchronize()
+    fwd_only_ms = _max_over_ranks(a.elapsed_time(b) / reps, ws, dev)
+    del dl
+
+    fwd_kernel = ("gdn forward, forward only: chunk prep + fused scan/outputs"
+                  if _fused(fl, bv, nd) else "gdn forward, forward only: prep, state scan, outputs")
+    roof = roofline_entry(fwd_alg_bytes(fl, False), fwd_alg_flops(fl), fwd_only_ms, fwd_kernel,
+                          _traffic("gdn_fwd_kernels_single_layer.md", FWD_SOURCES, "layer"),
+                          "bf16_tflops")
+    roof["workload"] = fl.name
+    roof_bwd = None
+    if bwd:
+        roof_bwd = roofline_entry(bwd_alg_bytes(w), bwd_alg_flops(w), bwd_ms,
+                                  "gdn backward (all launches of one call)",
+                                  _traffic("gdn_bwd_kernels_single_layer.md", BWD_SOURCES, args.workload),
+                                  "bf16_tflops_sustained")
+        roof_bwd["workload"] = w.name
+    roof_train_fwd = roofline_entry(fwd_alg_bytes(w, bwd), fwd_alg_flops(w), fwd_ms,
+                                    "gdn forward inside the step" + (" (saving the backward's context)"
+                                                                     if bwd else ""),
+                                    None, "bf16_tflops_sustained")
+    roof_train_fwd["workload"] = w.name
+
+    # end to end through the public API from pinned host buffers (one
+    # micro-batch per step: its inputs up, its results down)
     e2e = None
     if not args.no_e2e:
+        d0 = sets[0][1]
         names = [n for n in ("q", "k", "v", "beta", "g", "h0") if cpu[n] is not None]
         host_in = {n: cpu[n].pin_memory() for n in names}
         if bwd:
-            host_in["do"] = do.cpu().pin_memory()
-            host_in["dht"] = dht.cpu().pin_memory()
+            host_in["do"] = d0["do"].cpu().pin_memory()
+            host_in["dht"] = d0["dht"].cpu().pin_memory()
         dev_in = [{n: torch.empty_like(t, device=dev) for n, t in host_in.items()} for _ in range(2)]
+        ctxs = [sets[0][1]["ctx"], sets[1][1]["ctx"]]
 
         def result_set():
-            r = [torch.empty_like(o), torch.empty_like(ht)]
+            r = [torch.empty_like(d0["o"]), torch.empty_like(d0["ht"])]
             if bwd:
-                r += [torch.empty_like(q, dtype=torch.float32), torch.empty_like(k, dtype=torch.float32),
-                      torch.empty_like(v, dtype=torch.float32), torch.empty_like(beta),
-                      torch.empty_like(g), torch.empty_like(ht)]
+                r += [torch.empty_like(t) for t in d0["grads"]]
             return r
 
         res_d = [result_set(), result_set()]
@@ -451,23 +554,24 @@ def run_ours(args, ws, rank, local):
         def run(st):
             x, r = dev_in[st], res_d[st]
             api.gdn_chunk_fwd_qdq(x["q"], x["k"], x["v"], x["beta"], x["g"], x.get("h0"),
-                                  state_mode=sm, w_mode=wm, out=(r[0], r[1], ctx),
-                                  block_v=bv, neumann_degree=nd)
+                                  state_mode=sm, w_mode=wm, out=(r[0], r[1], ctxs[st]),
+                                  save_ctx=bwd, block_v=bv, neumann_degree=nd)
             if bwd:
-                api.gdn_chunk_bwd_ste(x["q"], x["k"], x["v"], x["beta"], x["g"], ctx, x["do"],
-                                      x["dht"], state_mode=sm, w_mode=wm, workspace=wsb,
+                api.gdn_chunk_bwd_ste(x["q"], x["k"], x["v"], x["beta"], x["g"], ctxs[st], x["do"],
+                                      x["dht"], state_mode=sm, w_mode=wm, workspace=d0["ws"],
                                       out=tuple(r[2:]), block_v=bv, neumann_degree=nd)
             return r
 
         e_ms, s_ms = e2e_pipelined(dev, ws, args.steps, args.warmup, host_in, dev_in, run, res_h)
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
         d2h = sum(t.numel() * t.element_size() for t in res_h[0])
-        e2e = {"value": round(tokens * ws / (e_ms / 1e3), 1), "unit": "tokens/s",
+        e2e = {"value": round(w.B * w.T * ws / (e_ms / 1e3), 1), "unit": "tokens/s",
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                "ms_per_step": round(e_ms, 4),
+               "step": "one micro-batch of the workload",
                "schedule": "pipelined: step i+1's upload and step i-1's download overlap step i's "
                            "compute (three streams, two device buffer sets)",
-               "serial_value": round(tokens * ws / (s_ms / 1e3), 1),
+               "serial_value": round(w.B * w.T * ws / (s_ms / 1e3), 1),
                "serial_ms_per_step": round(s_ms, 4)}
 
     cpu_base = None
@@ -483,12 +587,15 @@ def run_ours(args, ws, rank, local):
                    "Hv": w.Hv, "Dk": w.Dk, "Dv": w.Dv, "state_mode": sm, "w_mode": wm,
                    "chunk": 64, "block_v": bv,
                    "solve": "exact" if nd is None else "neumann degree %d" % nd,
-                   "global_batch_tokens": w.B * w.T * ws,
+                   "micro_batches_per_step": micro,
+                   "global_batch_tokens": tokens * ws,
                    "l2": "inputs larger than L2 (no flush needed)",
                    "fwd_ms": round(fwd_ms, 4), "bwd_ms": round(bwd_ms, 4) if bwd else None,
-                   "fwd_tflops_alg": round(fwd_alg_flops(w) / (fwd_ms / 1e3) / 1e12, 2)},
+                   "fwd_only_ms": round(fwd_only_ms, 4), "fwd_only_workload": fl.name,
+                   "fwd_only_tflops_alg": round(fwd_alg_flops(fl) / (fwd_only_ms / 1e3) / 1e12, 2)},
         "clocks": clk.summary(), "e2e": e2e, "gpu_launches": launches_per_step * args.steps,
-        "roofline": roof, "cpu_baseline": cpu_base,
+        "roofline": roof, "roofline_bwd": roof_bwd, "roofline_step_fwd": roof_train_fwd,
+        "cpu_baseline": cpu_base,
     }
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -580,7 +687,7 @@ def run_decode(args, ws, rank, local):
     ms_step = ms_total / args.steps
     tokens = w.B * w.T
     value = tokens * ws * args.steps / (ms_total / 1e3)
-    peak, peak_kind = _peaks()
+    peak, _, peak_kind = _peaks()
     alg = decode_alg_bytes(w)
     achieved = alg / (ms_step / 1e3) / 1e9
     roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -774,7 +881,7 @@ def run_token_serial(args, ws, rank, local):
     ms_step = ms_total / args.steps
     tokens = w.B * w.T
     value = tokens * ws * args.steps / (ms_total / 1e3)
-    peak, peak_kind = _peaks()
+    peak, _, peak_kind = _peaks()
     alg = token_serial_alg_bytes(w, ts.kda)
     achieved = alg / (ms_step / 1e3) / 1e9
 
@@ -933,13 +1040,15 @@ def main():
     ap.add_argument("--block-v", type=int, default=64, help="state-scale tile width")
     ap.add_argument("--neumann-degree", type=int, default=None,
                     help="Neumann approximate inverse of this degree instead of the exact solve")
+    ap.add_argument("--micro-batches", type=int, default=0,
+                    help="micro-batches of the workload per step (0: sized to ~50 ms per step)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     if args.mode is None:
         args.mode = "fwdbwd" if _backward_available() else "fwd"
     if args.workload is None:
-        args.workload = {"decode": "decode", "kda": "kda",
-                         "two_precision": "two_precision"}.get(args.mode, "layer")
+        args.workload = {"decode": "decode", "kda": "kda", "two_precision": "two_precision",
+                         "fwdbwd": "fwd_bwd"}.get(args.mode, "layer")
     args.bwd_launches = BWD_LAUNCHES
     ws, rank, local = _dist()
     if args.impl == "reference":
@@ -954,8 +1063,19 @@ def main():
         torch.distributed.destroy_process_group()
 
 
-FWD_LAUNCHES = 3   # kernels one forward call launches (chunk prep, state scan, outputs)
 BWD_LAUNCHES = 2   # kernels one backward call launches (reverse scan + chunk gradients)
+
+
+def _fused(w, block_v, neumann_degree):
+    """The two-launch fused forward applies (as in the library's dispatch)."""
+    return (w.Dk == 128 and w.Dv == 128 and w.state_mode != "none" and w.w_mode != "none"
+            and block_v == 64 and neumann_degree is None)
+
+
+def _fwd_launches(w, block_v, neumann_degree):
+    """Kernels one forward call launches: chunk prep + fused scan/outputs, or
+    chunk prep, state scan, outputs."""
+    return 2 if _fused(w, block_v, neumann_degree) else 3
 
 
 def _backward_available():

@@ -140,6 +140,15 @@ __device__ __forceinline__ float warp_reduce_scatter(float (&x)[NV], int lane) {
   return x[0];
 }
 
+// 2^x by the hardware approximation (relative error about 2^-22; subnormal
+// results flush to zero)
+__device__ __forceinline__ float ex2_approx_f(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kLog2eF = 1.4426950408889634f;
+
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

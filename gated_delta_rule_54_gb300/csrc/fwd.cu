@@ -37,6 +37,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include <cooperative_groups.h>
 
@@ -229,12 +230,32 @@ struct PrepSmem {
   static_assert(WST - TW >= kF32Tile, "Tw, Tu hold a second fp32 tile for the Neumann products");
 };
 
+// Layout of the variant for the fused scan (exact solve, no V and no U): the
+// W operand halves reuse A once the solve is done and the W code staging
+// reuses T once T diag(.) is split, so three CTAs fit on an SM.
+template <int DK>
+struct PrepSmemT {
+  static constexpr int K = 0;                            // bf16 [64][DK] (TMA)
+  static constexpr int A = K + kChunk * DK * 2;          // f32 [64][kSA]; then Tw hi, lo
+  static constexpr int TT = A + kF32Tile;                // f32 [64][kSA]; then W codes
+  static constexpr int TU = TT + kF32Tile;               // Tu hi, lo (the images written out)
+  static constexpr int TW = A;
+  static constexpr int WST = TT;
+  static constexpr int V = K;                            // (no V)
+  static constexpr int BG = TU + 2 * kChunk * 64 * 2;    // beta[64], g[64]
+  static constexpr int VEC = BG + 512;                   // gamma, e^gamma, beta e^gamma, beta
+  static constexpr int BYTES = VEC + 4 * 64 * 4 + 1024;  // + alignment slack
+  static_assert((A % 1024) == 0 && (TT % 1024) == 0 && (TU % 1024) == 0, "alignment");
+  static_assert(2 * kChunk * 64 * 2 <= kF32Tile && kChunk * DK <= kF32Tile, "aliases fit");
+  static_assert(3 * (BYTES + 2048) <= 233472, "three CTAs per SM");
+};
+
 // TOUT: the variant for the fused scan, which forms U itself: T diag(beta),
 // split into hi and lo bf16 halves, is written as two tile images to
 // p.tu_img, and U is not computed.
 template <int DK, int WM, bool TOUT>
-__global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __grid_constant__ FwdParams p) {
-  using S = PrepSmem<DK>;
+__global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kernel(const __grid_constant__ FwdParams p) {
+  using S = typename std::conditional<TOUT, PrepSmemT<DK>, PrepSmem<DK>>::type;
   extern __shared__ __align__(1024) unsigned char sm_raw[];
   unsigned char* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
   __shared__ float red[kPrepWarps];
@@ -342,9 +363,12 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __g
         const int i = row0 + gq + 8 * e2, j = col0 + nt * 8 + 2 * tq;
         float k0 = 0.f, k1 = 0.f;
         if (a_tile && i < L) {
-          const float gi = gam[i];
-          k0 = (j < i) ? expf(gi - gam[j]) * acc[nt][2 * e2] : 0.f;
-          k1 = (j + 1 < i) ? expf(gi - gam[j + 1]) * acc[nt][2 * e2 + 1] : 0.f;
+          // e^{gamma_i - gamma_j} as 2^{(gamma_i - gamma_j) log2 e} by the hardware exp2
+          // (about 2^-22 relative; the argument's rounding grows with the decay but the
+          // factor then shrinks as fast, so the absolute error of A stays ~1e-7)
+          const float gi = gam[i] * kLog2eF;
+          k0 = (j < i) ? ex2_approx_f(gi - gam[j] * kLog2eF) * acc[nt][2 * e2] : 0.f;
+          k1 = (j + 1 < i) ? ex2_approx_f(gi - gam[j + 1] * kLog2eF) * acc[nt][2 * e2 + 1] : 0.f;
         }
         if (gimg) st_bf16x2(gimg + swz<64>(i, j), k0, k1);
         // (tiles above the diagonal hold zeros: the Neumann products read all of A)
@@ -354,9 +378,9 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __g
   __syncthreads();
 
   // ---- a3: T = (I + A)^-1, or its Neumann polynomial ----
-  if (p.neumann < 0)
+  if (TOUT || p.neumann < 0)
     solve_unit_lower64<kPrepThreads>(As, Ts);
-  else
+  else if constexpr (!TOUT)
     neumann_lower64(As, Ts, reinterpret_cast<float*>(sm + S::TW), p.neumann);
 
   // ---- a4 operands: Tw = T diag(beta e^gamma), Tu = T diag(beta), split hi/lo;
@@ -413,15 +437,23 @@ __global__ void __launch_bounds__(kPrepThreads, 2) gdn_fwd_prep_kernel(const __g
 #pragma unroll
       for (int e2 = 0; e2 < 2; ++e2) {
         const int i = row0 + gq + 8 * e2, col = wc0 + nt * 8 + 2 * tq;
-        uint8_t c0, c1;
-        if (amax == 0.f) {
-          c0 = qdq_zero_code<WM>(wacc[nt][2 * e2]);
-          c1 = qdq_zero_code<WM>(wacc[nt][2 * e2 + 1]);
+        uint16_t c2;
+        if constexpr (WM == GDN_QDQ_E4M3) {
+          // rcp == 0 (amax 0, or no usable scale) gives signed-zero codes
+          float2 val;
+          c2 = e4m3_code2(wacc[nt][2 * e2], wacc[nt][2 * e2 + 1], rcp, val);
         } else {
-          c0 = qdq_code<WM>(wacc[nt][2 * e2], rcp);
-          c1 = qdq_code<WM>(wacc[nt][2 * e2 + 1], rcp);
+          uint8_t c0, c1;
+          if (amax == 0.f) {
+            c0 = qdq_zero_code<WM>(wacc[nt][2 * e2]);
+            c1 = qdq_zero_code<WM>(wacc[nt][2 * e2 + 1]);
+          } else {
+            c0 = qdq_code<WM>(wacc[nt][2 * e2], rcp);
+            c1 = qdq_code<WM>(wacc[nt][2 * e2 + 1], rcp);
+          }
+          c2 = (uint16_t)(c0 | (c1 << 8));
         }
-        *reinterpret_cast<uint16_t*>(Wst + i * DK + col) = (uint16_t)(c0 | (c1 << 8));
+        *reinterpret_cast<uint16_t*>(Wst + i * DK + col) = c2;
       }
     if (L == kChunk) {
       fence_proxy_async();
@@ -1234,8 +1266,8 @@ gdn_status launch_fused(const gdn_problem& p, const FwdParams& prm, const Dims& 
   if (d.B * d.T > 0 && d.n_slots > 0) {
     gdn_status s = GDN_OK;
     auto prep = [&](auto kern) {
-      if (set_smem(kern, PrepSmem<128>::BYTES) != GDN_OK) return GDN_ERR_CUDA;
-      kern<<<(unsigned)(d.n_slots * d.Hv), kPrepThreads, PrepSmem<128>::BYTES, st>>>(prm);
+      if (set_smem(kern, PrepSmemT<128>::BYTES) != GDN_OK) return GDN_ERR_CUDA;
+      kern<<<(unsigned)(d.n_slots * d.Hv), kPrepThreads, PrepSmemT<128>::BYTES, st>>>(prm);
       return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
     };
     s = p.w_mode == GDN_QDQ_E4M3 ? prep(gdn_fwd_prep_kernel<128, GDN_QDQ_E4M3, true>)

@@ -42,31 +42,34 @@ namespace {
 
 __device__ int g_fused_device_error;
 
-constexpr int kThreads = 512;
-constexpr int kWarps = kThreads / 32;
+constexpr int kEpiThreads = 512;               // 16 epilogue warps
+constexpr int kEpiWarps = kEpiThreads / 32;
+constexpr int kThreads = kEpiThreads + 32;     // + the producer warp (TMA and MMA issue)
 
 // shared memory (bytes from a 1024-aligned base)
 struct FSmem {
-  static constexpr int AQW = 0;                    // 2 buffers x [W^ ; Q]: 2 dk panels x 128 rows x 128 B
-  static constexpr int KT = AQW + 2 * 32768;       // 2 buffers x K (2 panels x 64 rows x 128 B)
-  static constexpr int VT = KT + 2 * 16384;        // V block [64 tok][64 v] bf16 (TMA, swizzled)
-  static constexpr int WC = VT + 8192;             // W codes [64][128] u8 (TMA)
-  static constexpr int ATU = WC + 8192;            // Tu hi, Tu lo images (bulk copy) ...
-  static constexpr int AP = ATU + 16384;           // ... then P lo, P hi, P lo
+  static constexpr int AQW = 0;                    // [W^ ; Q]: 2 dk panels x 128 rows x 128 B
+  static constexpr int KT = AQW + 32768;           // 2 buffers x K (2 panels x 64 rows x 128 B)
+  static constexpr int VT = KT + 2 * 16384;        // 2 buffers x V block [64 tok][64 v] bf16
+  static constexpr int WC = VT + 2 * 8192;         // 2 buffers x W codes [64][128] u8
+  static constexpr int ATU = WC + 2 * 8192;        // 2 buffers x Tu hi, Tu lo images; buffer 1 ...
+  static constexpr int AP = ATU + 2 * 16384;       // ... then P lo, P hi, P lo
   static constexpr int HB = AP + 24576;            // H^ codes as bf16 [128 dk][64 v]
   static constexpr int DP = HB + 16384;            // decayed Delta hi, lo [64 tok][64 v]
   static constexpr int DD = DP + 16384;            // Delta hi, lo
   static constexpr int CV = DD + 16384;            // 2 buffers x chunk vectors (1280 B)
   static constexpr int BYTES = CV + 2 * kCvecFloats * 4 + 1024;  // + alignment slack
   static_assert(BYTES <= 232448, "shared memory budget");
-  static_assert(AP == ATU + 16384, "[Tu_lo ; P_lo] read contiguously by the U product");
 };
 
-// TMEM accumulator columns
-constexpr uint32_t kD1 = 0, kD2 = 64, kD3 = 128, kD4 = 192, kD5 = 256, kTmemCols = 512;
+// TMEM accumulator columns: D1 and D5 double buffered (chunk parity)
+constexpr uint32_t kD1 = 0, kD2 = 128, kD3 = 192, kD4 = 256, kD5 = 320, kTmemCols = 512;
 
-// bytes of one chunk's inputs: K, Q (2 boxes each), V, W codes, Tu images, chunk vectors
-constexpr uint32_t kChunkTx = 2 * 8192 + 2 * 8192 + 8192 + 8192 + 16384 + kCvecFloats * 4;
+// bytes of the copy groups of one chunk
+constexpr uint32_t kVtTx = 8192 + 16384 + 8192;  // V block, Tu images, W codes
+constexpr uint32_t kKwTx = 2 * 8192;             // K (2 boxes)
+constexpr uint32_t kCvTx = kCvecFloats * 4;   // chunk vectors
+constexpr uint32_t kQTx = 2 * 8192;           // Q (2 boxes)
 
 // ---------------------------------------------------------------------------
 // tcgen05 helpers
@@ -86,11 +89,29 @@ constexpr uint32_t kIdKK = idesc(128, 64, 0, 0);  // A K-major, B K-major
 constexpr uint32_t kIdKM = idesc(128, 64, 0, 1);  // A K-major, B MN-major
 constexpr uint32_t kIdMM = idesc(128, 64, 1, 1);  // A MN-major, B MN-major
 
+// descriptor of the tile at smem address saddr + off: only the start-address
+// field moves (offsets keep the tile inside the 256 KB shared window)
+__device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t off) { return desc + (off >> 4); }
 __device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, bool acc) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
       "l"(a), "l"(b), "r"(id), "r"((uint32_t)acc));
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+// barrier among the epilogue warps only (the producer warp does not take part),
+// returning whether any of them passed v = true
+__device__ __forceinline__ bool epi_sync_or(bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, %2, p;\n"
+      " selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"((uint32_t)v), "n"(kEpiThreads)
+      : "memory");
+  return r != 0;
 }
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
@@ -199,21 +220,35 @@ __device__ __forceinline__ void quant16(float (&x)[16], float rcp, float s, bool
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
+// Warp 16 is the producer: one lane issues the TMA copies and the tensor-core
+// products.  Warps 0-15 run the epilogues; warp w reads TMEM lanes
+// 32 (w % 4) .. +31 (accumulator rows) and columns 16 (w / 4) .. +15.
+// Per chunk c the products and epilogues are ordered so that only the state
+// chain waits: QDQ(c) -> D1(c) = [W^ ; Q] H^ -> Delta(c) -> D2(c) = K^T Delta'
+// -> H_{c+1}; D4(c) (QK^T), D5(c) (P Delta) and D3(c+1) (U of the next chunk)
+// fill the tensor pipe in between, the next chunk's W^ conversion runs while
+// D2(c) executes, and the outputs of chunk c are stored after QDQ(c+1).
 template <int SM, int WM>
 __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid_constant__ FusedParams p) {
   extern __shared__ __align__(1024) unsigned char sm_raw[];
   unsigned char* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
-  __shared__ __align__(8) uint64_t bar_in[2];  // a chunk's inputs (per input buffer)
-  __shared__ __align__(8) uint64_t bar_u, bar_a, bar_s, bar_o, bar_end;  // MMA completions
+  // copies of buffer b: in_vt (V, Tu, W codes), in_kw (K), in_cv (chunk vectors); in_q (Q)
+  __shared__ __align__(8) uint64_t in_vt[2], in_kw[2], in_cv[2], in_q;
+  // products done: u (D3), a (D1), d4 (D4), s (D2), o (D5), end (everything)
+  __shared__ __align__(8) uint64_t b_u, b_a, b_d4, b_s, b_o, b_end;
+  // epilogue signals: H^ and W^ ready, P ready, Delta ready, outputs stored
+  __shared__ __align__(8) uint64_t e_hb, e_p, e_dl, e_out;
   __shared__ uint32_t tmem_slot;
-  __shared__ float red[kWarps];
+  __shared__ float red[kEpiWarps];
+  __shared__ int abort_flag;
 
   const int vb = blockIdx.x, h = blockIdx.y, n = blockIdx.z;
   const int hk = h / p.G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const bool producer = warp == kEpiWarps;
   const int quad = warp & 3;         // TMEM lane quadrant of this warp
   const int row = 32 * quad + lane;  // accumulator row (TMEM lane)
-  const int col0 = 16 * (warp >> 2); // this thread's 16 columns of the 64
+  const int col0 = 16 * ((warp >> 2) & 3);  // this thread's 16 columns of the 64
   const bool lo_rows = quad < 2;     // rows 0-63 (tokens of the W^ / U / Delta products)
   const int t_row = row & 63;        // token of this row in the chunk
 
@@ -231,15 +266,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
   }
   const int nch = (L + kChunk - 1) / kChunk;
 
-  unsigned char* VT = sm + FSmem::VT;
-  const uint8_t* WCs = sm + FSmem::WC;
-  unsigned char* ATU = sm + FSmem::ATU;
+  unsigned char* AQW = sm + FSmem::AQW;
   unsigned char* AP = sm + FSmem::AP;
   unsigned char* HB = sm + FSmem::HB;
   unsigned char* DP = sm + FSmem::DP;
   unsigned char* DD = sm + FSmem::DD;
-  auto AQWb = [&](int b) { return sm + FSmem::AQW + b * 32768; };
   auto KTb = [&](int b) { return sm + FSmem::KT + b * 16384; };
+  auto VTb = [&](int b) { return sm + FSmem::VT + b * 8192; };
+  auto WCb = [&](int b) { return sm + FSmem::WC + b * 8192; };
+  auto ATUb = [&](int b) { return sm + FSmem::ATU + b * 16384; };
   auto CVb = [&](int b) { return reinterpret_cast<float*>(sm + FSmem::CV + b * kCvecFloats * 4); };
 
   // ---- set-up: TMEM, barriers ----
@@ -250,310 +285,396 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
   }
   if (tid == 0) {
-    mbar_init(&bar_in[0], 1);
-    mbar_init(&bar_in[1], 1);
-    mbar_init(&bar_u, 1);
-    mbar_init(&bar_a, 1);
-    mbar_init(&bar_s, 1);
-    mbar_init(&bar_o, 1);
-    mbar_init(&bar_end, 1);
+    for (int bb = 0; bb < 2; ++bb) {
+      mbar_init(&in_vt[bb], 1);
+      mbar_init(&in_kw[bb], 1);
+      mbar_init(&in_cv[bb], 1);
+    }
+    mbar_init(&in_q, 1);
+    mbar_init(&b_u, 1);
+    mbar_init(&b_a, 1);
+    mbar_init(&b_d4, 1);
+    mbar_init(&b_s, 1);
+    mbar_init(&b_o, 1);
+    mbar_init(&b_end, 1);
+    mbar_init(&e_hb, kEpiWarps);
+    mbar_init(&e_p, kEpiWarps / 2);
+    mbar_init(&e_dl, kEpiWarps / 2);
+    mbar_init(&e_out, kEpiWarps / 2);
+    abort_flag = 0;
     fence_mbar_init();
   }
-
-  // TMA of chunk c's inputs, each issued once the buffer it fills is free
-  auto load_kqc = [&](int c) {  // K, Q, chunk vectors (double buffered); opens the chunk's tx
-    const int b = c & 1;
-    const int64_t tok = tok0 + (int64_t)c * kChunk;
-    mbar_expect_tx(&bar_in[b], kChunkTx);
-    bulk_load_1d(CVb(b), p.cvec + ((slot0 + c) * p.Hv + h) * kCvecFloats, kCvecFloats * 4,
-                 &bar_in[b]);
-#pragma unroll
-    for (int pn = 0; pn < 2; ++pn) {
-      tma_load_2d(KTb(b) + pn * 8192, &p.tm_k, hk * 128 + pn * 64, (int)tok, &bar_in[b]);
-      tma_load_2d(AQWb(b) + pn * 16384 + 8192, &p.tm_q, hk * 128 + pn * 64, (int)tok, &bar_in[b]);
-    }
-  };
-  auto load_w = [&](int c) {  // W codes
-    const int64_t tok = tok0 + (int64_t)c * kChunk;
-    tma_load_2d(sm + FSmem::WC, &p.tm_wc, h * 128, (int)tok, &bar_in[c & 1]);
-  };
-  auto load_vt = [&](int c) {  // V block and the Tu images
-    const int b = c & 1;
-    const int64_t tok = tok0 + (int64_t)c * kChunk;
-    tma_load_2d(VT, &p.tm_v, h * 128 + vb * 64, (int)tok, &bar_in[b]);
-    bulk_load_1d(ATU,
-                 reinterpret_cast<const unsigned char*>(p.tu_img) + ((slot0 + c) * p.Hv + h) * 16384,
-                 16384, &bar_in[b]);
-  };
-
-  // ---- the state: thread (row dk, col0) holds H[dk][col0 .. col0 + 15] ----
-  float hv[16];
-  {
-    const float* src = p.h0 ? p.h0 + (((int64_t)n * p.Hv + h) * 128 + row) * 128 + vb * 64 + col0
-                            : nullptr;
-#pragma unroll
-    for (int j = 0; j < 16; j += 4) {
-      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (src) x = *reinterpret_cast<const float4*>(src + j);
-      hv[j] = x.x;
-      hv[j + 1] = x.y;
-      hv[j + 2] = x.z;
-      hv[j + 3] = x.w;
-    }
-  }
-  auto amax_partial = [&]() {
-    float m = 0.f;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(hv[j]));
-    m = warp_max(m);
-    if (lane == 0) red[warp] = m;
-  };
-  amax_partial();
-
   tc_fence_before();
-  __syncthreads();  // TMEM address, barriers, red[] visible
+  __syncthreads();  // TMEM address, barriers visible
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t tl = tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)col0;  // this thread's lane
-
-  if (tid == 0 && nch > 0) {
-    load_kqc(0);
-    load_w(0);
-    load_vt(0);
-  }
-
   bool bad = false;
-  int c = 0;
-  for (; c < nch; ++c) {
-    const int b = c & 1;
-    const int64_t slot = slot0 + c;
-    const int64_t tok = tok0 + (int64_t)c * kChunk;
-    const int Lc = min(L - c * kChunk, kChunk);
-    const uint32_t ph = (uint32_t)c & 1u;
-    const float sW = p.w_scales[slot * p.Hv + h];
-    unsigned char* AQW = AQWb(b);
 
-    // ---- a6: state QDQ of the state entering chunk c ----
-    bad |= !mbar_wait(&bar_in[b], (uint32_t)(c >> 1) & 1u);
-    if (__syncthreads_or(bad)) break;  // inputs landed; red[] complete; the last chunk's reads done
-    float amax = red[0];
+  if (producer) {
+    // ======================= producer warp =======================
+    if (lane == 0 && nch > 0) {
+      auto tok_of = [&](int c) { return (int)(tok0 + (int64_t)c * kChunk); };
+      auto sh_of = [&](int c) { return (slot0 + c) * p.Hv + h; };
+      auto load_vt = [&](int c) {  // V block, Tu images and W codes of chunk c
+        const int b = c & 1;
+        mbar_expect_tx(&in_vt[b], kVtTx);
+        tma_load_2d(VTb(b), &p.tm_v, h * 128 + vb * 64, tok_of(c), &in_vt[b]);
+        bulk_load_1d(ATUb(b), reinterpret_cast<const unsigned char*>(p.tu_img) + sh_of(c) * 16384,
+                     16384, &in_vt[b]);
+        tma_load_2d(WCb(b), &p.tm_wc, h * 128, tok_of(c), &in_vt[b]);
+      };
+      auto load_kw = [&](int c) {  // K of chunk c
+        const int b = c & 1;
+        mbar_expect_tx(&in_kw[b], kKwTx);
 #pragma unroll
-    for (int w = 1; w < kWarps; ++w) amax = fmaxf(amax, red[w]);
-    float sH, rcp;
-    qdq_scale<SM>(amax, sH, rcp);
-    {
-      float vals[16];
-      uint32_t c4[4];
-      quant16<SM>(hv, rcp, sH, amax == 0.f, vals, c4);
-      // H^ codes as bf16 values: the MN-major B operand [dk][v]
-      st8_bf16(HB, row, col0 >> 3, vals);
-      st8_bf16(HB, row, (col0 >> 3) + 1, vals + 8);
-      if (p.h_codes) {
-        uint8_t* dst = p.h_codes + ((slot * p.Hv + h) * 128 + row) * 128 + vb * 64 + col0;
-        *reinterpret_cast<uint4*>(dst) = make_uint4(c4[0], c4[1], c4[2], c4[3]);
-        if (tid == 0) p.h_scales[(slot * p.Hv + h) * 2 + vb] = sH;
-      }
-    }
-    if (tid == 0 && c + 1 < nch) load_kqc(c + 1);  // buffers of chunk c - 1: free
-
-    // ---- W^ codes -> bf16 values in rows 0-63 of [W^ ; Q] ----
-    const float* cv = CVb(b);
-    {
-      const int r = tid >> 3, d0 = (tid & 7) * 16;  // row, first of 16 codes
-      const uint4 cw = *reinterpret_cast<const uint4*>(WCs + r * 128 + d0);
-      const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
-      float x[16];
+        for (int pn = 0; pn < 2; ++pn)
+          tma_load_2d(KTb(b) + pn * 8192, &p.tm_k, hk * 128 + pn * 64, tok_of(c), &in_kw[b]);
+      };
+      auto load_cv = [&](int c) {  // chunk vectors of chunk c
+        const int b = c & 1;
+        mbar_expect_tx(&in_cv[b], kCvTx);
+        bulk_load_1d(CVb(b), p.cvec + sh_of(c) * kCvecFloats, kCvecFloats * 4, &in_cv[b]);
+      };
+      auto load_q = [&](int c) {  // Q into rows 64-127 of both panels of [W^ ; Q]
+        mbar_expect_tx(&in_q, kQTx);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float4 a = qdq_code4_values<WM>(w4[i]);
-        x[4 * i] = a.x;
-        x[4 * i + 1] = a.y;
-        x[4 * i + 2] = a.z;
-        x[4 * i + 3] = a.w;
-      }
-      unsigned char* panel = AQW + (d0 >> 6) * 16384;
-      st8_bf16(panel, r, (d0 & 63) >> 3, x);
-      st8_bf16(panel, r, ((d0 & 63) >> 3) + 1, x + 8);
-    }
-    fence_proxy_async();  // generic-proxy writes of HB and AQW before the MMAs read them
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    // ---- the chunk's first products ----
-    if (tid == 0) {
-      if (c + 1 < nch) load_w(c + 1);  // W codes of this chunk are converted
-      const uint32_t aq = smem_u32(AQW), atu = smem_u32(ATU), vt = smem_u32(VT);
-      const uint32_t kt = smem_u32(KTb(b)), hb = smem_u32(HB);
+        for (int pn = 0; pn < 2; ++pn)
+          tma_load_2d(AQW + pn * 16384 + 8192, &p.tm_q, hk * 128 + pn * 64, tok_of(c), &in_q);
+      };
       // D3 = [Tu_hi ; *] V + [Tu_lo ; *] V  (U in rows 0-63)
+      auto issue_u = [&](int c) {
+        const int b = c & 1;
+        const uint64_t atu = sdesc(smem_u32(ATUb(b)), 16, 1024), vt = sdesc(smem_u32(VTb(b)), 8192, 1024);
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        umma(tmem + kD3, sdesc(atu + ks * 32, 16, 1024), sdesc(vt + ks * 2048, 8192, 1024), kIdKM,
-             ks > 0);
+        for (int ks = 0; ks < 4; ++ks)
+          umma(tmem + kD3, dadd(atu, ks * 32), dadd(vt, ks * 2048), kIdKM, ks > 0);
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        umma(tmem + kD3, sdesc(atu + 8192 + ks * 32, 16, 1024), sdesc(vt + ks * 2048, 8192, 1024),
-             kIdKM, true);
-      // D4 = [W^ ; Q] K^T  (QK^T in rows 64-127)
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        umma(tmem + kD4, sdesc(aq + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-             sdesc(kt + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), kIdKK, ks > 0);
-      umma_commit(&bar_u);
-      // D1 = [W^ ; Q] H^  (W^ H^ in rows 0-63, Q H^ in rows 64-127)
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks)
-        umma(tmem + kD1, sdesc(aq + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024),
-             sdesc(hb + ks * 2048, 8192, 1024), kIdKM, ks > 0);
-      umma_commit(&bar_a);
-    }
-
-    // ---- U (rows 0-63) and P (rows 64-127) ----
-    bad |= !mbar_wait(&bar_u, ph);
-    tc_fence_after();
-    if (tid == 0 && c + 1 < nch) load_vt(c + 1);  // D3 has read V and Tu
-    float u[16];
-    if (lo_rows) {
-      tmem_ld16(tl + kD3, u);
-    } else {
-      // P_ij = 2^{(gamma_i - gamma_j) log2 e} q_i.k_j for j <= i (i = t_row, j = col0 + jj)
-      float x[16];
-      tmem_ld16(tl + kD4, x);
-      constexpr float kLog2e = 1.4426950408889634f;
-      const float gi = cv[kCvGam + t_row];
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj) {
-        const int j = col0 + jj;
-        x[jj] = (j <= t_row) ? ex2_approx((gi - cv[kCvGam + j]) * kLog2e) * x[jj] : 0.f;
-      }
-      // [P_lo | P_hi | P_lo]: hi at +8 KB, lo at 0 and +16 KB
-      st16_split(AP + 8192, AP, t_row, col0, x);
-      *reinterpret_cast<uint4*>(AP + 16384 + sw_off(t_row, col0)) =
-          *reinterpret_cast<const uint4*>(AP + sw_off(t_row, col0));
-      *reinterpret_cast<uint4*>(AP + 16384 + sw_off(t_row, col0 + 8)) =
-          *reinterpret_cast<const uint4*>(AP + sw_off(t_row, col0 + 8));
-      if (p.pb && vb == 0) {
-        unsigned char* pimg = reinterpret_cast<unsigned char*>(p.pb) + (slot * p.Hv + h) * 8192;
-        float z[16];
-#pragma unroll
-        for (int jj = 0; jj < 16; ++jj) z[jj] = t_row < Lc ? x[jj] : 0.f;
-        st8_bf16(pimg, t_row, col0 >> 3, z);
-        st8_bf16(pimg, t_row, (col0 >> 3) + 1, z + 8);
-      }
-    }
-
-    // ---- a7: Delta = U - sW sH W^ H^ (rows 0-63); decayed Delta' for the state update ----
-    bad |= !mbar_wait(&bar_a, ph);
-    tc_fence_after();
-    if (lo_rows) {
-      float y[16];
-      tmem_ld16(tl + kD1, y);
-      const float sWH = sW * sH;
-      const bool valid = t_row < Lc;
-      const float di = valid ? cv[kCvDec + t_row] : 0.f;
-      float dl[16], dd[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        dl[j] = valid ? u[j] - sWH * y[j] : 0.f;
-        dd[j] = dl[j] * di;
-      }
-      st16_split(DD, DD + 8192, t_row, col0, dl);
-      st16_split(DP, DP + 8192, t_row, col0, dd);
-      if (p.db) {
-        // the Delta image: the hi half (Delta rounded to bf16), as stored in DD
-        unsigned char* dimg = reinterpret_cast<unsigned char*>(p.db) + ((slot * p.Hv + h) * 2 + vb) * 8192;
-        *reinterpret_cast<uint4*>(dimg + sw_off(t_row, col0)) =
-            *reinterpret_cast<const uint4*>(DD + sw_off(t_row, col0));
-        *reinterpret_cast<uint4*>(dimg + sw_off(t_row, col0 + 8)) =
-            *reinterpret_cast<const uint4*>(DD + sw_off(t_row, col0 + 8));
-      }
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    // ---- a9 state update and the P Delta product ----
-    if (tid == 0) {
-      const uint32_t kt = smem_u32(KTb(b)), dp = smem_u32(DP), dd = smem_u32(DD);
-      const uint32_t ap = smem_u32(AP);
-      // D2 = K^T Delta'_hi + K^T Delta'_lo (A: K tile read MN-major, M = dk)
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        umma(tmem + kD2, sdesc(kt + ks * 2048, 8192, 1024), sdesc(dp + ks * 2048, 8192, 1024), kIdMM,
-             ks > 0);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        umma(tmem + kD2, sdesc(kt + ks * 2048, 8192, 1024), sdesc(dp + 8192 + ks * 2048, 8192, 1024),
-             kIdMM, true);
-      umma_commit(&bar_s);
-      // D5 = [P_lo ; P_hi] Delta_hi + [P_lo ; P_hi] Delta_lo + [P_hi ; P_lo] Delta_hi
-      //      (rows 64-127: P Delta to ~16 bits)
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        umma(tmem + kD5, sdesc(ap + ks * 32, 16, 1024), sdesc(dd + ks * 2048, 8192, 1024), kIdKM,
-             ks > 0);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        umma(tmem + kD5, sdesc(ap + ks * 32, 16, 1024), sdesc(dd + 8192 + ks * 2048, 8192, 1024),
-             kIdKM, true);
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        umma(tmem + kD5, sdesc(ap + 8192 + ks * 32, 16, 1024), sdesc(dd + ks * 2048, 8192, 1024),
-             kIdKM, true);
-      umma_commit(&bar_o);
-    }
-
-    // ---- H <- e^{gamma_L} H^ + K~^T Delta ----
-    bad |= !mbar_wait(&bar_s, ph);
-    tc_fence_after();
-    {
-      float z[16];
-      tmem_ld16(tl + kD2, z);
-      const float egL = cv[kCvEg + 63];  // gamma is flat past the last valid row
-#pragma unroll
-      for (int j = 0; j < 16; ++j) hv[j] = hv[j] * egL + z[j];
-      amax_partial();
-    }
-
-    // ---- a8: O = scale (e^gamma sH Q H^ + P Delta) (rows 64-127) ----
-    if (!lo_rows) {
-      bad |= !mbar_wait(&bar_o, ph);
+        for (int ks = 0; ks < 4; ++ks)
+          umma(tmem + kD3, dadd(atu, 8192 + ks * 32), dadd(vt, ks * 2048), kIdKM, true);
+        umma_commit(&b_u);
+      };
+      load_vt(0);
+      load_kw(0);
+      load_cv(0);
+      load_q(0);
+      bad |= !mbar_wait(&in_vt[0], 0);
       tc_fence_after();
+      if (!bad) issue_u(0);
+      for (int c = 0; c < nch && !bad; ++c) {
+        const int b = c & 1;
+        const uint32_t ph = (uint32_t)c & 1u, phb = (uint32_t)(c >> 1) & 1u;
+        const bool more = c + 1 < nch;
+        // V, Tu and W codes of the next chunk: their buffer's last readers, D3(c - 1)
+        // and the W^ conversion of chunk c - 1, finished before the epilogues of
+        // chunk c - 1 signalled
+        if (more) load_vt(c + 1);
+        // D1 = [W^ ; Q] H^ once H^(c) and W^(c) are written and K(c), Q(c) have landed
+        bad |= !mbar_wait(&e_hb, ph);
+        bad |= !mbar_wait(&in_q, ph);
+        bad |= !mbar_wait(&in_kw[b], phb);
+        if (bad) break;
+        tc_fence_after();
+        const uint64_t aq = sdesc(smem_u32(AQW), 16, 1024), hb = sdesc(smem_u32(HB), 8192, 1024);
+        const uint64_t ktk = sdesc(smem_u32(KTb(b)), 16, 1024);
+        const uint32_t d1 = tmem + kD1 + 64 * (c & 1);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          umma(d1, dadd(aq, (ks >> 2) * 16384 + (ks & 3) * 32), dadd(hb, ks * 2048), kIdKM, ks > 0);
+        umma_commit(&b_a);
+        // D4 = [W^ ; Q] K^T (QK^T in rows 64-127)
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          umma(tmem + kD4, dadd(aq, (ks >> 2) * 16384 + (ks & 3) * 32),
+               dadd(ktk, (ks >> 2) * 8192 + (ks & 3) * 32), kIdKK, ks > 0);
+        umma_commit(&b_d4);
+        // K of the next chunk: H^(c) being ready means the state update of chunk
+        // c - 1 ran, so D2(c - 1), the last reader of that K buffer, is done
+        if (more) load_kw(c + 1);
+        // Q of the next chunk once D1(c) and D4(c) have read this one
+        if (more) {
+          bad |= !mbar_wait(&b_d4, ph);
+          if (!bad) load_q(c + 1);
+        }
+        // D2 = K^T Delta'_hi + K^T Delta'_lo (A: K tile read MN-major, M = dk)
+        bad |= !mbar_wait(&e_dl, ph);
+        if (bad) break;
+        tc_fence_after();
+        const uint64_t dp = sdesc(smem_u32(DP), 8192, 1024), dd = sdesc(smem_u32(DD), 8192, 1024);
+        const uint64_t ap = sdesc(smem_u32(AP), 16, 1024), ktm = sdesc(smem_u32(KTb(b)), 8192, 1024);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          umma(tmem + kD2, dadd(ktm, ks * 2048), dadd(dp, ks * 2048), kIdMM, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          umma(tmem + kD2, dadd(ktm, ks * 2048), dadd(dp, 8192 + ks * 2048), kIdMM, true);
+        umma_commit(&b_s);
+        // chunk vectors of the next chunk once the outputs of chunk c - 1 are stored
+        if (more) {
+          if (c >= 1) bad |= !mbar_wait(&e_out, ph ^ 1u);
+          if (!bad) load_cv(c + 1);
+        }
+        // D5 = [P_lo ; P_hi] Delta_hi + [P_lo ; P_hi] Delta_lo + [P_hi ; P_lo] Delta_hi
+        bad |= !mbar_wait(&e_p, ph);
+        if (bad) break;
+        tc_fence_after();
+        const uint32_t d5 = tmem + kD5 + 64 * (c & 1);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          umma(d5, dadd(ap, ks * 32), dadd(dd, ks * 2048), kIdKM, ks > 0);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          umma(d5, dadd(ap, ks * 32), dadd(dd, 8192 + ks * 2048), kIdKM, true);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          umma(d5, dadd(ap, 8192 + ks * 32), dadd(dd, ks * 2048), kIdKM, true);
+        umma_commit(&b_o);
+        // U of the next chunk (the Delta epilogue of chunk c has read D3(c))
+        if (more) {
+          bad |= !mbar_wait(&in_vt[b ^ 1], (uint32_t)((c + 1) >> 1) & 1u);
+          if (bad) break;
+          tc_fence_after();
+          issue_u(c + 1);
+        }
+      }
+      if (bad) abort_flag = 1;
+    }
+    __syncwarp();
+  } else {
+    // ======================= epilogue warps =======================
+    const uint32_t tl = tmem + ((uint32_t)(32 * quad) << 16) + (uint32_t)col0;  // this thread's lane
+    float hv[16];  // thread (row dk, col0) holds H[dk][col0 .. col0 + 15]
+    {
+      const float* src = p.h0 ? p.h0 + (((int64_t)n * p.Hv + h) * 128 + row) * 128 + vb * 64 + col0
+                              : nullptr;
+#pragma unroll
+      for (int j = 0; j < 16; j += 4) {
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (src) x = *reinterpret_cast<const float4*>(src + j);
+        hv[j] = x.x;
+        hv[j + 1] = x.y;
+        hv[j + 2] = x.z;
+        hv[j + 3] = x.w;
+      }
+    }
+    auto amax_partial = [&]() {
+      float m = 0.f;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(hv[j]));
+      m = warp_max(m);
+      if (lane == 0) red[warp] = m;
+    };
+    // W^ codes of chunk c -> bf16 values in rows 0-63 of [W^ ; Q]; nthr threads
+    // (index i) share the 64 x 128 codes, 16 at a time
+    auto convert_w = [&](int c, int i, int nthr) {
+      for (int e = i; e < 64 * 8; e += nthr) {
+        const int r = e >> 3, d0 = (e & 7) * 16;  // row, first of 16 codes
+        const uint4 cw = *reinterpret_cast<const uint4*>(WCb(c & 1) + r * 128 + d0);
+        const uint32_t w4[4] = {cw.x, cw.y, cw.z, cw.w};
+        float x[16];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float4 a = qdq_code4_values<WM>(w4[k]);
+          x[4 * k] = a.x;
+          x[4 * k + 1] = a.y;
+          x[4 * k + 2] = a.z;
+          x[4 * k + 3] = a.w;
+        }
+        unsigned char* panel = AQW + (d0 >> 6) * 16384;
+        st8_bf16(panel, r, (d0 & 63) >> 3, x);
+        st8_bf16(panel, r, ((d0 & 63) >> 3) + 1, x + 8);
+      }
+    };
+    // outputs of chunk c: O = scale (e^gamma sH Q H^ + P Delta), rows 64-127
+    auto store_out = [&](int c, float sH) {
+      bad |= !mbar_wait(&b_o, (uint32_t)c & 1u);
+      tc_fence_after();
+      const int Lc = min(L - c * kChunk, kChunk);
+      const float* cv = CVb(c & 1);
       float qh[16], pd[16];
-      tmem_ld16(tl + kD1, qh);
-      tmem_ld16(tl + kD5, pd);
+      tmem_ld16(tl + kD1 + 64 * (c & 1), qh);
+      tmem_ld16(tl + kD5 + 64 * (c & 1), pd);
       if (t_row < Lc) {
         const float ei = cv[kCvEg + t_row] * sH;
-        float* dst = p.o + ((tok + t_row) * p.Hv + h) * 128 + vb * 64 + col0;
+        float* dst = p.o + ((tok0 + (int64_t)c * kChunk + t_row) * p.Hv + h) * 128 + vb * 64 + col0;
 #pragma unroll
         for (int j = 0; j < 16; j += 4)
           *reinterpret_cast<float4*>(dst + j) =
               make_float4(p.scale * (ei * qh[j] + pd[j]), p.scale * (ei * qh[j + 1] + pd[j + 1]),
-                          p.scale * (ei * qh[j + 2] + pd[j + 2]), p.scale * (ei * qh[j + 3] + pd[j + 3]));
+                          p.scale * (ei * qh[j + 2] + pd[j + 2]),
+                          p.scale * (ei * qh[j + 3] + pd[j + 3]));
       }
-    }
-    tc_fence_before();  // the next chunk's products overwrite the accumulators read here
-  }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&e_out);
+    };
 
-  // ---- final state (unquantized) ----
-  if (!bad && p.ht) {
-    float* dst = p.ht + (((int64_t)n * p.Hv + h) * 128 + row) * 128 + vb * 64 + col0;
+    amax_partial();
+    if (nch > 0) {
+      bad |= !mbar_wait(&in_vt[0], 0);
+      convert_w(0, tid, kEpiThreads);
+    }
+    float sH_prev = 1.f;
+    int c = 0;
+    for (; c < nch; ++c) {
+      const int b = c & 1;
+      const int64_t slot = slot0 + c;
+      const int Lc = min(L - c * kChunk, kChunk);
+      const uint32_t ph = (uint32_t)c & 1u;
+      const float sW = p.w_scales[slot * p.Hv + h];
+
+      // ---- a6: state QDQ of the state entering chunk c (red[]: H_c's partial amax) ----
+      // (uniform decision: every epilogue thread leaves the loop together)
+      if (epi_sync_or(bad || *reinterpret_cast<volatile int*>(&abort_flag) != 0)) {
+        bad = true;
+        break;
+      }
+      float amax = red[0];
 #pragma unroll
-    for (int j = 0; j < 16; j += 4)
-      *reinterpret_cast<float4*>(dst + j) = make_float4(hv[j], hv[j + 1], hv[j + 2], hv[j + 3]);
+      for (int w = 1; w < kEpiWarps; ++w) amax = fmaxf(amax, red[w]);
+      float sH, rcp;
+      qdq_scale<SM>(amax, sH, rcp);
+      {
+        float vals[16];
+        uint32_t c4[4];
+        quant16<SM>(hv, rcp, sH, amax == 0.f, vals, c4);
+        st8_bf16(HB, row, col0 >> 3, vals);
+        st8_bf16(HB, row, (col0 >> 3) + 1, vals + 8);
+        if (p.h_codes) {
+          uint8_t* dst = p.h_codes + ((slot * p.Hv + h) * 128 + row) * 128 + vb * 64 + col0;
+          *reinterpret_cast<uint4*>(dst) = make_uint4(c4[0], c4[1], c4[2], c4[3]);
+          if (tid == 0) p.h_scales[(slot * p.Hv + h) * 2 + vb] = sH;
+        }
+      }
+      fence_proxy_async();  // H^ (and the W^ converted earlier) before D1 reads them
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&e_hb);
+
+      // ---- outputs of the previous chunk (its D1 and D5 buffers) ----
+      if (!lo_rows && c > 0) store_out(c - 1, sH_prev);
+
+
+      bad |= !mbar_wait(&in_cv[b], (uint32_t)(c >> 1) & 1u);  // this chunk's vectors
+      const float* cv = CVb(b);
+      float u[16];
+      if (lo_rows) {
+        // U (rows 0-63)
+        bad |= !mbar_wait(&b_u, ph);
+        tc_fence_after();
+        tmem_ld16(tl + kD3, u);
+      } else {
+        // P_ij = 2^{(gamma_i - gamma_j) log2 e} q_i.k_j for j <= i (i = t_row, j = col0 + jj)
+        bad |= !mbar_wait(&b_d4, ph);
+        tc_fence_after();
+        float x[16];
+        tmem_ld16(tl + kD4, x);
+        constexpr float kLog2e = 1.4426950408889634f;
+        const float gi = cv[kCvGam + t_row];
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const int j = col0 + jj;
+          x[jj] = (j <= t_row) ? ex2_approx((gi - cv[kCvGam + j]) * kLog2e) * x[jj] : 0.f;
+        }
+        // [P_lo | P_hi | P_lo]: hi at +8 KB, lo at 0 and +16 KB
+        st16_split(AP + 8192, AP, t_row, col0, x);
+        *reinterpret_cast<uint4*>(AP + 16384 + sw_off(t_row, col0)) =
+            *reinterpret_cast<const uint4*>(AP + sw_off(t_row, col0));
+        *reinterpret_cast<uint4*>(AP + 16384 + sw_off(t_row, col0 + 8)) =
+            *reinterpret_cast<const uint4*>(AP + sw_off(t_row, col0 + 8));
+        if (p.pb && vb == 0) {
+          unsigned char* pimg = reinterpret_cast<unsigned char*>(p.pb) + (slot * p.Hv + h) * 8192;
+          float z[16];
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj) z[jj] = t_row < Lc ? x[jj] : 0.f;
+          st8_bf16(pimg, t_row, col0 >> 3, z);
+          st8_bf16(pimg, t_row, (col0 >> 3) + 1, z + 8);
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&e_p);
+      }
+
+      // ---- a7: Delta = U - sW sH W^ H^ (rows 0-63); decayed Delta' for the state update ----
+      if (lo_rows) {
+        bad |= !mbar_wait(&b_a, ph);
+        tc_fence_after();
+        float y[16];
+        tmem_ld16(tl + kD1 + 64 * (c & 1), y);
+        const float sWH = sW * sH;
+        const bool valid = t_row < Lc;
+        const float di = valid ? cv[kCvDec + t_row] : 0.f;
+        float dl[16], dd[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          dl[j] = valid ? u[j] - sWH * y[j] : 0.f;
+          dd[j] = dl[j] * di;
+        }
+        st16_split(DD, DD + 8192, t_row, col0, dl);
+        st16_split(DP, DP + 8192, t_row, col0, dd);
+        if (p.db) {
+          // the Delta image: the hi half (Delta rounded to bf16), as stored in DD
+          unsigned char* dimg =
+              reinterpret_cast<unsigned char*>(p.db) + ((slot * p.Hv + h) * 2 + vb) * 8192;
+          *reinterpret_cast<uint4*>(dimg + sw_off(t_row, col0)) =
+              *reinterpret_cast<const uint4*>(DD + sw_off(t_row, col0));
+          *reinterpret_cast<uint4*>(dimg + sw_off(t_row, col0 + 8)) =
+              *reinterpret_cast<const uint4*>(DD + sw_off(t_row, col0 + 8));
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&e_dl);
+      }
+
+      // ---- the next chunk's W^, while D2 runs: [W^ ; Q] is free once D1 and D4 are done ----
+      if (c + 1 < nch) {
+        bad |= !mbar_wait(&b_d4, ph);
+        bad |= !mbar_wait(&in_vt[b ^ 1], (uint32_t)((c + 1) >> 1) & 1u);
+        convert_w(c + 1, tid, kEpiThreads);
+      }
+
+      // ---- a9: H <- e^{gamma_L} H^ + K~^T Delta ----
+      bad |= !mbar_wait(&b_s, ph);
+      tc_fence_after();
+      {
+        float z[16];
+        tmem_ld16(tl + kD2, z);
+        const float egL = cv[kCvEg + 63];  // gamma is flat past the last valid row
+#pragma unroll
+        for (int j = 0; j < 16; ++j) hv[j] = hv[j] * egL + z[j];
+        amax_partial();
+      }
+      tc_fence_before();
+      sH_prev = sH;
+    }
+    // the last chunk's outputs
+    if (!bad && !lo_rows && c == nch && nch > 0) store_out(nch - 1, sH_prev);
+    // ---- final state (unquantized) ----
+    if (!bad && c == nch && p.ht) {
+      float* dst = p.ht + (((int64_t)n * p.Hv + h) * 128 + row) * 128 + vb * 64 + col0;
+#pragma unroll
+      for (int j = 0; j < 16; j += 4)
+        *reinterpret_cast<float4*>(dst + j) = make_float4(hv[j], hv[j + 1], hv[j + 2], hv[j + 3]);
+    }
+    if (bad) abort_flag = 1;
   }
 
   // ---- tear-down: no product or copy may be in flight when TMEM is freed ----
-  if (tid == 0) {
-    if (bad) {
-      atomicOr(&g_fused_device_error, 1);
-      // the copies of the chunk the loop stopped at (bounded waits, as above)
-      if (c < nch) mbar_wait(&bar_in[c & 1], (uint32_t)(c >> 1) & 1u);
-      if (c + 1 < nch) mbar_wait(&bar_in[(c + 1) & 1], (uint32_t)((c + 1) >> 1) & 1u);
+  __syncthreads();
+  if (tid == 0 && abort_flag) atomicOr(&g_fused_device_error, 1);
+  if (producer && lane == 0) {
+    if (abort_flag) {
+      // copies still in flight land within the bounded waits
+      mbar_wait(&in_q, 0);
+      mbar_wait(&in_q, 1);
+      for (int bb = 0; bb < 2; ++bb) {
+        mbar_wait(&in_vt[bb], 0);
+        mbar_wait(&in_kw[bb], 0);
+        mbar_wait(&in_cv[bb], 0);
+      }
     }
-    umma_commit(&bar_end);  // completes once every product issued so far is done
-    mbar_wait(&bar_end, 0);
+    umma_commit(&b_end);  // completes once every product issued so far is done
+    mbar_wait(&b_end, 0);
   }
   tc_fence_before();
   __syncthreads();
