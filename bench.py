@@ -303,7 +303,8 @@ def _traffic(profile_md, source_files, workload_key):
     return float(m_tr.group(1))
 
 
-FWD_SOURCES = ["gated_delta_rule_54_gb300/csrc/fwd.cu", "gated_delta_rule_54_gb300/csrc/common.cuh"]
+FWD_SOURCES = ["gated_delta_rule_54_gb300/csrc/fwd.cu", "gated_delta_rule_54_gb300/csrc/fwd_fused.cu",
+               "gated_delta_rule_54_gb300/csrc/common.cuh"]
 BWD_SOURCES = ["gated_delta_rule_54_gb300/csrc/bwd.cu", "gated_delta_rule_54_gb300/csrc/common.cuh"]
 
 

@@ -49,13 +49,15 @@ CtxLayout ctx_layout(const gdn_problem& p) {
     L.w_full = take(sizeof(float) * tokens * d.Hv * d.Dk);
   }
   L.cvec = take(sizeof(float) * (size_t)d.n_slots * d.Hv * kCvecFloats);
+  // the fused forward's backward recomputes Gamma o KK^T and Delta on the
+  // tensor cores; the others read them back
+  const bool fused = fused_fwd(p);
   if (p.save_ctx) {
     L.tb = take((size_t)d.n_slots * d.Hv * kTileImgBytes);
-    L.gkk = take((size_t)d.n_slots * d.Hv * kTileImgBytes);
+    if (!fused) L.gkk = take((size_t)d.n_slots * d.Hv * kTileImgBytes);
     L.pb = take((size_t)d.n_slots * d.Hv * kTileImgBytes);
-    L.db = take((size_t)d.n_slots * d.Hv * (d.Dv / 64) * kTileImgBytes);
+    if (!fused) L.db = take((size_t)d.n_slots * d.Hv * (d.Dv / 64) * kTileImgBytes);
   }
-  const bool fused = fused_fwd(p);
   if (fused) L.tu_img = take((size_t)d.n_slots * d.Hv * 2 * kTileImgBytes);
   const size_t per_slot = (size_t)d.n_slots * d.Hv * d.Dk * d.Dv;
   if (p.state_mode != GDN_QDQ_NONE) {

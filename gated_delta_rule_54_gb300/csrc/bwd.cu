@@ -26,6 +26,7 @@
 // Gradients tolerate bf16 operands (no hi/lo splits): the backward has no
 // quantization decision to preserve.
 #define GDN_WGEMM_UNROLL 4  // see wgemm
+#include "bwd_tc.h"
 #include "common.cuh"
 #include "launch.h"
 
@@ -61,7 +62,8 @@ struct BwdParams {
   float* dbeta;
   float* dg;
   float* dh0;
-  __nv_bfloat16* ws_dh;  // [n_slots, Hv, Dk, Dv] state gradient entering each chunk
+  __nv_bfloat16* ws_dh;  // [n_slots, Hv, Dv / 64, Dk, 64] state gradient entering each chunk
+                         // (per value block, the swizzled [Dk][64] tile image)
   float* ws_dqk;         // [2, B*T, Hv, Dk] per-value-head dq, dk (grouped heads only)
   const int32_t* cu_seqlens;
   int64_t T, BT;
@@ -290,11 +292,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_kernel(const __grid_
     }
     __syncthreads();
 
-    // dH' entering this chunk's backward -> workspace (coalesced 16-byte rows)
-    for (int i = threadIdx.x; i < DK * 8; i += kThreads) {
-      const int d = i >> 3, c8 = i & 7;
-      const uint4 val = *reinterpret_cast<const uint4*>(dHb + d * 64 + ((c8 ^ (d & 7)) << 3));
-      *reinterpret_cast<uint4*>(p.ws_dh + ((slot * p.Hv + h) * DK + d) * p.Dv + vb * 64 + c8 * 8) = val;
+    // dH' entering this chunk's backward -> workspace: this value block's panel
+    // of the [DK][Dv] tile, stored as its swizzled shared-memory image
+    {
+      __nv_bfloat16* dst = p.ws_dh + ((slot * p.Hv + h) * (p.Dv / 64) + vb) * (DK * 64);
+      for (int i = threadIdx.x; i < DK * 8; i += kThreads)
+        reinterpret_cast<uint4*>(dst)[i] = reinterpret_cast<const uint4*>(dHb)[i];
     }
     // e^gamma dO
     for (int e = threadIdx.x; e < kChunk * 32; e += kThreads) {
@@ -519,12 +522,8 @@ __global__ void __launch_bounds__(kChunkWarps * 32, 1) gdn_bwd_chunk_kernel(cons
   //      block-0 products, group C is block 1; T, Gamma o KK^T, P, each
   //      block's Delta and the chunk vectors come from the forward ----
   auto load_block_vb = [&](int b) {
-    const __nv_bfloat16* src = p.ws_dh + ((slot * p.Hv + h) * DK) * p.Dv + b * 64;
-    __nv_bfloat16* dst = dHpb(b);
-    for (int i = threadIdx.x; i < DK * 8; i += kCT) {
-      const int d = i >> 3, c8 = i & 7;
-      cp_async16(smem_u32(dst + swz<64>(d, c8 * 8)), src + (int64_t)d * p.Dv + c8 * 8, 16);
-    }
+    // the scan stores each value block's dH' as its swizzled tile image
+    load_block<kCT>(dHpb(b), p.ws_dh + ((slot * p.Hv + h) * nvb + b) * (DK * 64), DK * 64 * 2);
     if constexpr (SM != GDN_QDQ_NONE) {
       const uint8_t* hs = p.h_codes + ((slot * p.Hv + h) * DK) * p.Dv + b * 64;
       uint8_t* hd = hcb(b);
@@ -1022,16 +1021,25 @@ gdn_status set_smem(K kern, int bytes) {
              : GDN_ERR_CUDA;
 }
 
+// tc: the tensor-core chunk kernel's arguments (Dk = Dv = 128, both sites
+// quantized, block_v 64, exact solve), or null for the warp-level chunk kernel
 template <int DK, int SM, int WM>
-gdn_status launch_bwd_t(const BwdParams& prm, const Dims& d, cudaStream_t st) {
+gdn_status launch_bwd_t(const BwdParams& prm, const Dims& d, const BwdTcParams* tc,
+                        cudaStream_t st) {
   using SS = ScanSmem<DK, WM>;
   using CS = ChunkSmem<DK>;
   auto k1 = gdn_bwd_scan_kernel<DK, WM>;
   auto k2 = gdn_bwd_chunk_kernel<DK, SM, WM>;
   if (set_smem(k1, SS::BYTES) != GDN_OK || set_smem(k2, CS::BYTES) != GDN_OK) return GDN_ERR_CUDA;
   k1<<<dim3((unsigned)(d.Dv / 64), (unsigned)d.Hv, (unsigned)d.N), kThreads, SS::BYTES, st>>>(prm);
-  if (d.B * d.T > 0 && d.n_slots > 0)
-    k2<<<dim3((unsigned)d.n_slots, (unsigned)d.Hv), kChunkWarps * 32, CS::BYTES, st>>>(prm);
+  if (d.B * d.T > 0 && d.n_slots > 0) {
+    if (tc) {
+      const gdn_status s = launch_bwd_chunk_tc(*tc, SM, WM, d.n_slots, st);
+      if (s != GDN_OK) return s;
+    } else {
+      k2<<<dim3((unsigned)d.n_slots, (unsigned)d.Hv), kChunkWarps * 32, CS::BYTES, st>>>(prm);
+    }
+  }
   if (prm.ws_dqk && d.B * d.T > 0) {
     const int64_t total = d.B * d.T * d.Hk * d.Dk;
     const int blocks = (int)((total + 255) / 256 < 152 * 16 ? (total + 255) / 256 : 152 * 16);
@@ -1043,9 +1051,9 @@ gdn_status launch_bwd_t(const BwdParams& prm, const Dims& d, cudaStream_t st) {
 
 template <int DK>
 gdn_status dispatch_bwd(const gdn_problem& p, const BwdParams& prm, const Dims& d,
-                        cudaStream_t st) {
+                        const BwdTcParams* tc, cudaStream_t st) {
 #define GDN_CASE(SMV, WMV) \
-  if (p.state_mode == SMV && p.w_mode == WMV) return launch_bwd_t<DK, SMV, WMV>(prm, d, st);
+  if (p.state_mode == SMV && p.w_mode == WMV) return launch_bwd_t<DK, SMV, WMV>(prm, d, tc, st);
   GDN_CASE(GDN_QDQ_E4M3, GDN_QDQ_E4M3)
   GDN_CASE(GDN_QDQ_INT8, GDN_QDQ_E4M3)
   GDN_CASE(GDN_QDQ_NONE, GDN_QDQ_NONE)
@@ -1070,7 +1078,9 @@ int bwd_device_error(bool reset) {
     const int z = 0;
     if (cudaMemcpyToSymbol(g_bwd_device_error, &z, sizeof(int)) != cudaSuccess) return -1;
   }
-  return v;
+  const int t = bwd_tc_device_error(reset);
+  if (t < 0) return -1;
+  return v | t;
 }
 
 size_t bwd_workspace_bytes(const gdn_problem& p, const Dims& d) {
@@ -1093,6 +1103,7 @@ gdn_status launch_bwd(const gdn_problem& p, const Dims& d, const void* q, const 
   prm.dht = dht;
   const CtxLayout L = ctx_layout(p);
   const unsigned char* base = static_cast<const unsigned char*>(ctx);
+  auto at = [&](int64_t off) { return off < 0 ? nullptr : base + off; };
   if (p.w_mode != GDN_QDQ_NONE) {
     prm.w_codes = base + L.w_codes;
     prm.w_scales = reinterpret_cast<const float*>(base + L.w_scales);
@@ -1105,10 +1116,10 @@ gdn_status launch_bwd(const gdn_problem& p, const Dims& d, const void* q, const 
   }
   if (p.w_mode == GDN_QDQ_NONE) prm.w_full = reinterpret_cast<const float*>(base + L.w_full);
   prm.cvec = reinterpret_cast<const float*>(base + L.cvec);
-  prm.tb = reinterpret_cast<const __nv_bfloat16*>(base + L.tb);
-  prm.gkk = reinterpret_cast<const __nv_bfloat16*>(base + L.gkk);
-  prm.pb = reinterpret_cast<const __nv_bfloat16*>(base + L.pb);
-  prm.db = reinterpret_cast<const __nv_bfloat16*>(base + L.db);
+  prm.tb = reinterpret_cast<const __nv_bfloat16*>(at(L.tb));
+  prm.gkk = reinterpret_cast<const __nv_bfloat16*>(at(L.gkk));
+  prm.pb = reinterpret_cast<const __nv_bfloat16*>(at(L.pb));
+  prm.db = reinterpret_cast<const __nv_bfloat16*>(at(L.db));
   prm.dq = dq;
   prm.dk = dk;
   prm.dv = dv;
@@ -1148,8 +1159,43 @@ gdn_status launch_bwd(const gdn_problem& p, const Dims& d, const void* q, const 
                     (uint64_t)d.Hv * DK, DK, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!ok) return GDN_ERR_CUDA;
   }
-  if (d.Dk == 128) return dispatch_bwd<128>(p, prm, d, st);
-  return dispatch_bwd<64>(p, prm, d, st);
+  if (fused_fwd(p)) {
+    // the tensor-core chunk kernel: P, Gamma o KK^T and Delta are recomputed
+    BwdTcParams tc{};
+    tc.tm_q = prm.tm_q;
+    tc.tm_k = prm.tm_k;
+    tc.tm_do = prm.tm_do;
+    tc.tm_wc = prm.tm_wc;
+    if (tok > 0 &&
+        !make_map(&tc.tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, v, (uint64_t)d.Hv * d.Dv, tok,
+                  (uint64_t)d.Hv * d.Dv * 2, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B))
+      return GDN_ERR_CUDA;
+    tc.h_codes = prm.h_codes;
+    tc.h_scales = prm.h_scales;
+    tc.w_scales = prm.w_scales;
+    tc.cvec = prm.cvec;
+    tc.tb = at(L.tb);
+    tc.tu_img = at(L.tu_img);
+    tc.ws_dh = prm.ws_dh;
+    tc.dq = prm.ws_dqk ? prm.ws_dqk : dq;
+    tc.dk = prm.ws_dqk ? prm.ws_dqk + prm.BT * d.Hv * d.Dk : dk;
+    tc.HH = prm.ws_dqk ? d.Hv : d.Hk;
+    tc.dv = dv;
+    tc.dbeta = dbeta;
+    tc.dg = dg;
+    tc.cu_seqlens = p.cu_seqlens;
+    tc.T = d.T;
+    tc.nt_fixed = d.nt_fixed;
+    tc.Hv = d.Hv;
+    tc.G = prm.G;
+    tc.N = prm.N;
+    tc.bv_log2 = prm.bv_log2;
+    tc.scale = p.scale;
+    if (!tc.tb || !tc.tu_img) return GDN_ERR_INVALID_ARG;
+    return dispatch_bwd<128>(p, prm, d, &tc, st);
+  }
+  if (d.Dk == 128) return dispatch_bwd<128>(p, prm, d, nullptr, st);
+  return dispatch_bwd<64>(p, prm, d, nullptr, st);
 }
 
 }  // namespace gdn

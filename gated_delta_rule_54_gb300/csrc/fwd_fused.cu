@@ -34,6 +34,7 @@
 
 #include "common.cuh"
 #include "fused.h"
+#include "tc.cuh"
 #include "launch.h"
 
 namespace gdn {
@@ -71,36 +72,10 @@ constexpr uint32_t kKwTx = 2 * 8192;             // K (2 boxes)
 constexpr uint32_t kCvTx = kCvecFloats * 4;   // chunk vectors
 constexpr uint32_t kQTx = 2 * 8192;           // Q (2 boxes)
 
-// ---------------------------------------------------------------------------
-// tcgen05 helpers
-// ---------------------------------------------------------------------------
-// shared-memory matrix descriptor: 128-byte swizzle, 8-row groups SBO apart,
-// LBO = distance between 64-element blocks along M/N (MN-major operands)
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  return (uint64_t)((saddr >> 4) & 0x3fffu) | ((uint64_t)((lbo >> 4) & 0x3fffu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3fffu) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
-// instruction descriptor, kind::f16: bf16 x bf16 -> f32, M x N, operand majors
-__host__ __device__ constexpr uint32_t idesc(int M, int N, int a_mn, int b_mn) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
-         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
 constexpr uint32_t kIdKK = idesc(128, 64, 0, 0);  // A K-major, B K-major
 constexpr uint32_t kIdKM = idesc(128, 64, 0, 1);  // A K-major, B MN-major
 constexpr uint32_t kIdMM = idesc(128, 64, 1, 1);  // A MN-major, B MN-major
 
-// descriptor of the tile at smem address saddr + off: only the start-address
-// field moves (offsets keep the tile inside the 256 KB shared window)
-__device__ __forceinline__ uint64_t dadd(uint64_t desc, uint32_t off) { return desc + (off >> 4); }
-__device__ __forceinline__ void umma(uint32_t d, uint64_t a, uint64_t b, uint32_t id, bool acc) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d),
-      "l"(a), "l"(b), "r"(id), "r"((uint32_t)acc));
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
-}
 // barrier among the epilogue warps only (the producer warp does not take part),
 // returning whether any of them passed v = true
 __device__ __forceinline__ bool epi_sync_or(bool v) {
@@ -112,72 +87,6 @@ __device__ __forceinline__ bool epi_sync_or(bool v) {
       : "r"((uint32_t)v), "n"(kEpiThreads)
       : "memory");
   return r != 0;
-}
-__device__ __forceinline__ void umma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
-                   smem_u32(bar))
-               : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-}
-// 16 consecutive fp32 columns of this thread's TMEM lane
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,"
-      "%15}, [%16];\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 2^x by the hardware approximation (relative error about 2^-22; subnormal
-// results flush to zero)
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// (hi, lo) bf16 pairs of (x0, x1): hi = bf16(x), lo = bf16(x - hi), packed
-__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  hi = pack_bf16(x0, x1);
-  const float h0 = __uint_as_float(hi << 16), h1 = __uint_as_float(hi & 0xffff0000u);
-  lo = pack_bf16(x0 - h0, x1 - h1);
-}
-
-// byte offset of element (row, col) in a tile of 128-byte rows (64 bf16),
-// 16-byte chunks swizzled by the row within its 8-row group
-__device__ __forceinline__ uint32_t sw_off(int row, int col) {
-  return (uint32_t)(row * 128 + ((((col >> 3) & 7) ^ (row & 7)) << 4) + (col & 7) * 2);
-}
-// eight bf16 values at (row, 8c .. 8c+7) of a swizzled tile: one 16-byte store
-__device__ __forceinline__ void st8_bf16(unsigned char* tile, int row, int c8, const float* x) {
-  uint4 u;
-  u.x = pack_bf16(x[0], x[1]);
-  u.y = pack_bf16(x[2], x[3]);
-  u.z = pack_bf16(x[4], x[5]);
-  u.w = pack_bf16(x[6], x[7]);
-  *reinterpret_cast<uint4*>(tile + sw_off(row, 8 * c8)) = u;
-}
-// sixteen values at (row, 16 c16 ..) split into hi and lo tiles
-__device__ __forceinline__ void st16_split(unsigned char* hi_tile, unsigned char* lo_tile, int row,
-                                           int col, const float* x) {
-  uint32_t h[8], l[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) split2(x[2 * i], x[2 * i + 1], h[i], l[i]);
-  *reinterpret_cast<uint4*>(hi_tile + sw_off(row, col)) = make_uint4(h[0], h[1], h[2], h[3]);
-  *reinterpret_cast<uint4*>(hi_tile + sw_off(row, col + 8)) = make_uint4(h[4], h[5], h[6], h[7]);
-  *reinterpret_cast<uint4*>(lo_tile + sw_off(row, col)) = make_uint4(l[0], l[1], l[2], l[3]);
-  *reinterpret_cast<uint4*>(lo_tile + sw_off(row, col + 8)) = make_uint4(l[4], l[5], l[6], l[7]);
 }
 
 // Sixteen state values quantized with scale reciprocal rcp: codes (packed
@@ -278,12 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
   auto CVb = [&](int b) { return reinterpret_cast<float*>(sm + FSmem::CV + b * kCvecFloats * 4); };
 
   // ---- set-up: TMEM, barriers ----
-  if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
-                     smem_u32(&tmem_slot)),
-                 "r"(kTmemCols));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
-  }
+  if (warp == 0) tmem_alloc(&tmem_slot, kTmemCols);
   if (tid == 0) {
     for (int bb = 0; bb < 2; ++bb) {
       mbar_init(&in_vt[bb], 1);
@@ -679,9 +583,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 0)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem),
-                 "r"(kTmemCols));
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace

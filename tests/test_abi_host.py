@@ -86,11 +86,12 @@ def test_sizes():
     ns = 2 * nt
     cv = al(4 * ns * 4 * 5 * 64)                                    # chunk vectors
     imgs = 3 * al(ns * 4 * 64 * 64 * 2) + al(ns * 4 * 2 * 64 * 64 * 2)  # T / GKK / P, Delta images
+    imgs_tc = 2 * al(ns * 4 * 64 * 64 * 2)   # T / P: the tensor-core backward recomputes the others
     tf = al(4 * ns * 4 * 64 * 64)                                   # fp32 T of the fused forward
     w = al(2 * 300 * 4 * 128) + al(4 * ns * 4)                      # W codes and scales
     h = al(ns * 4 * 128 * 128) + al(4 * ns * 4 * 2)                 # state codes and scales
     # Dk = Dv = 128, both sites quantized, block_v 64: the fused forward
-    assert lib.gdn_ctx_bytes(ctypes.byref(p)) == w + cv + imgs + tf + h
+    assert lib.gdn_ctx_bytes(ctypes.byref(p)) == w + cv + imgs_tc + tf + h
     # forward only: no backward tiles; the fused forward keeps the states on chip
     assert lib.gdn_ctx_bytes(ctypes.byref(_problem(save_ctx=0))) == w + cv + tf
     # the three-launch path (here block_v 32) hands the state codes to its output pass
@@ -102,7 +103,8 @@ def test_sizes():
     offs = [lib.gdn_ctx_offset(ctypes.byref(p), s) for s in range(12)]
     assert offs[0] == 0 and offs[2] == -1 and offs[11] == -1
     present = [o for o in offs if o >= 0]
-    assert present == sorted(present) and len(present) == 10
+    assert present == sorted(present) and len(present) == 8
+    assert offs[5] == -1 and offs[7] == -1   # no Gamma o KK^T or Delta images
     po = _problem(save_ctx=0)
     assert [lib.gdn_ctx_offset(ctypes.byref(po), s) >= 0 for s in range(12)] == \
         [True, True, False, True, False, False, False, False, True, False, False, False]

@@ -97,6 +97,14 @@ def test_bwd_lengths(T):
     _check(w)
 
 
+@pytest.mark.parametrize("T", [1, 63, 64, 65, 130])
+def test_bwd_lengths_tensor_core_path(T):
+    """Dk = Dv = 128 with both sites quantized and block_v 64 takes the tcgen05
+    chunk kernel (P, Gamma o KK^T and Delta recomputed): ragged chunk tails."""
+    w = synth.small(B=2, T=T, Hk=1, Hv=2, Dk=128, Dv=128, h0=True, seed=110 + T)
+    _check(w, scale=128 ** -0.5, with_dht=T % 2 == 1)
+
+
 def test_bwd_grouped_heads_int8():
     w = synth.small(B=1, T=150, Hk=2, Hv=6, Dk=128, Dv=128, state_mode="int8", h0=True, seed=22)
     _check(w)
