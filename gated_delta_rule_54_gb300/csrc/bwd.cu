@@ -1023,15 +1023,22 @@ gdn_status set_smem(K kern, int bytes) {
 
 // tc: the tensor-core chunk kernel's arguments (Dk = Dv = 128, both sites
 // quantized, block_v 64, exact solve), or null for the warp-level chunk kernel
+// scan: the tensor-core reverse scan's arguments (Dk = Dv = 128, W site
+// quantized), or null for the warp-level scan
 template <int DK, int SM, int WM>
 gdn_status launch_bwd_t(const BwdParams& prm, const Dims& d, const BwdTcParams* tc,
-                        cudaStream_t st) {
+                        const BwdScanTcParams* scan, cudaStream_t st) {
   using SS = ScanSmem<DK, WM>;
   using CS = ChunkSmem<DK>;
   auto k1 = gdn_bwd_scan_kernel<DK, WM>;
   auto k2 = gdn_bwd_chunk_kernel<DK, SM, WM>;
   if (set_smem(k1, SS::BYTES) != GDN_OK || set_smem(k2, CS::BYTES) != GDN_OK) return GDN_ERR_CUDA;
-  k1<<<dim3((unsigned)(d.Dv / 64), (unsigned)d.Hv, (unsigned)d.N), kThreads, SS::BYTES, st>>>(prm);
+  if (scan) {
+    const gdn_status s = launch_bwd_scan_tc(*scan, WM, st);
+    if (s != GDN_OK) return s;
+  } else {
+    k1<<<dim3((unsigned)(d.Dv / 64), (unsigned)d.Hv, (unsigned)d.N), kThreads, SS::BYTES, st>>>(prm);
+  }
   if (d.B * d.T > 0 && d.n_slots > 0) {
     if (tc) {
       const gdn_status s = launch_bwd_chunk_tc(*tc, SM, WM, d.n_slots, st);
@@ -1051,9 +1058,10 @@ gdn_status launch_bwd_t(const BwdParams& prm, const Dims& d, const BwdTcParams* 
 
 template <int DK>
 gdn_status dispatch_bwd(const gdn_problem& p, const BwdParams& prm, const Dims& d,
-                        const BwdTcParams* tc, cudaStream_t st) {
-#define GDN_CASE(SMV, WMV) \
-  if (p.state_mode == SMV && p.w_mode == WMV) return launch_bwd_t<DK, SMV, WMV>(prm, d, tc, st);
+                        const BwdTcParams* tc, const BwdScanTcParams* scan, cudaStream_t st) {
+#define GDN_CASE(SMV, WMV)                     \
+  if (p.state_mode == SMV && p.w_mode == WMV) \
+    return launch_bwd_t<DK, SMV, WMV>(prm, d, tc, scan, st);
   GDN_CASE(GDN_QDQ_E4M3, GDN_QDQ_E4M3)
   GDN_CASE(GDN_QDQ_INT8, GDN_QDQ_E4M3)
   GDN_CASE(GDN_QDQ_NONE, GDN_QDQ_NONE)
@@ -1078,9 +1086,9 @@ int bwd_device_error(bool reset) {
     const int z = 0;
     if (cudaMemcpyToSymbol(g_bwd_device_error, &z, sizeof(int)) != cudaSuccess) return -1;
   }
-  const int t = bwd_tc_device_error(reset);
-  if (t < 0) return -1;
-  return v | t;
+  const int t = bwd_tc_device_error(reset), u = bwd_scan_tc_device_error(reset);
+  if (t < 0 || u < 0) return -1;
+  return v | t | u;
 }
 
 size_t bwd_workspace_bytes(const gdn_problem& p, const Dims& d) {
@@ -1159,6 +1167,30 @@ gdn_status launch_bwd(const gdn_problem& p, const Dims& d, const void* q, const 
                     (uint64_t)d.Hv * DK, DK, 64, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (!ok) return GDN_ERR_CUDA;
   }
+  // the tensor-core reverse scan: Dk = Dv = 128 with the W site quantized
+  BwdScanTcParams scan{};
+  const bool scan_tc = d.Dk == 128 && d.Dv == 128 && p.w_mode != GDN_QDQ_NONE;
+  if (scan_tc) {
+    scan.tm_q = prm.tm_q;
+    scan.tm_k = prm.tm_k;
+    scan.tm_do = prm.tm_do;
+    scan.tm_wc = prm.tm_wc;
+    scan.pb = prm.pb;
+    scan.w_scales = prm.w_scales;
+    scan.cvec = prm.cvec;
+    scan.dht = dht;
+    scan.dh0 = dh0;
+    scan.ws_dh = prm.ws_dh;
+    scan.cu_seqlens = p.cu_seqlens;
+    scan.T = d.T;
+    scan.nt_fixed = d.nt_fixed;
+    scan.Hv = d.Hv;
+    scan.G = prm.G;
+    scan.N = prm.N;
+    scan.scale = p.scale;
+    if (!scan.pb) return GDN_ERR_INVALID_ARG;
+  }
+  const BwdScanTcParams* scan_arg = scan_tc ? &scan : nullptr;
   if (fused_fwd(p)) {
     // the tensor-core chunk kernel: P, Gamma o KK^T and Delta are recomputed
     BwdTcParams tc{};
@@ -1192,10 +1224,10 @@ gdn_status launch_bwd(const gdn_problem& p, const Dims& d, const void* q, const 
     tc.bv_log2 = prm.bv_log2;
     tc.scale = p.scale;
     if (!tc.tb || !tc.tu_img) return GDN_ERR_INVALID_ARG;
-    return dispatch_bwd<128>(p, prm, d, &tc, st);
+    return dispatch_bwd<128>(p, prm, d, &tc, scan_arg, st);
   }
-  if (d.Dk == 128) return dispatch_bwd<128>(p, prm, d, nullptr, st);
-  return dispatch_bwd<64>(p, prm, d, nullptr, st);
+  if (d.Dk == 128) return dispatch_bwd<128>(p, prm, d, nullptr, scan_arg, st);
+  return dispatch_bwd<64>(p, prm, d, nullptr, nullptr, st);
 }
 
 }  // namespace gdn

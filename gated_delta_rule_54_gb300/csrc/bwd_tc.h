@@ -39,6 +39,28 @@ struct BwdTcParams {
   float scale;
 };
 
+// Reverse scan of the state gradient on the tensor cores (Dk = Dv = 128, W
+// site quantized): one CTA per (sequence, value head) carries dH (fp32) through
+// the chunks in reverse and stores the dH' entering every chunk in the
+// workspace, as the swizzled [128][64] tile image of each value block.
+struct BwdScanTcParams {
+  CUtensorMap tm_q, tm_k, tm_do, tm_wc;  // as in BwdTcParams
+  const void* pb;          // [n_slots, Hv] 8 KiB P images (the forward's)
+  const float* w_scales;   // [n_slots, Hv]
+  const float* cvec;       // [n_slots, Hv, 5 * 64]
+  const float* dht;        // [N, Hv, 128, 128] or null (zero)
+  float* dh0;              // [N, Hv, 128, 128] or null
+  void* ws_dh;             // [n_slots, Hv] 32 KiB state-gradient panels
+  const int32_t* cu_seqlens;
+  int64_t T, nt_fixed;
+  int Hv, G, N;
+  float scale;
+};
+
+// grid (Hv, N); false on an unsupported W mode or a launch failure
+gdn_status launch_bwd_scan_tc(const BwdScanTcParams& p, int w_mode, cudaStream_t st);
+int bwd_scan_tc_device_error(bool reset);
+
 // grid (n_slots, Hv); false on an unsupported mode pair or a launch failure
 gdn_status launch_bwd_chunk_tc(const BwdTcParams& p, int state_mode, int w_mode, int64_t n_slots,
                                cudaStream_t st);
