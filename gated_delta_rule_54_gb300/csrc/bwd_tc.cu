@@ -33,6 +33,8 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "bwd_tc.h"
 #include "common.cuh"
 #include "launch.h"
@@ -58,25 +60,33 @@ struct BSmem {
   static constexpr int DH = HB + 32768;      // dH' [128 d][128 n]; then dDelta, Gm
   static constexpr int TU = DH + 32768;      // T diag(beta) hi, lo; then dW [64 tok][128 d]
   static constexpr int WB = TU + 16384;      // W codes [64 tok][128 d]; then dT, X
-  static constexpr int DB = WB + 16384;      // Delta [64 tok][128 n]; W codes (u8) before; then dKK
-  static constexpr int PB = DB + 16384;      // P [64][64]; state codes (u8, with GK) before
+  static constexpr int DB = WB + 16384;      // Delta [64 tok][128 n]; then dT, X / dKK
+  static constexpr int PB = DB + 16384;      // P [64][64]; then Gm
   static constexpr int GK = PB + 8192;       // Gamma o KK^T (strictly lower)
   static constexpr int TB = GK + 8192;       // T
-  static constexpr int CV = TB + 8192;       // chunk vectors
-  static constexpr int RACC = CV + kCvecFloats * 4;  // row partial sums [kSlots][64] + scalars
+  static constexpr int CV = TB + 8192;       // 2 x chunk vectors (this tile's, the next one's)
+  static constexpr int RACC = CV + 2 * kCvecFloats * 4;  // row partial sums [kSlots][64] + scalars
   static constexpr int kSlots = 36;
   static constexpr int BYTES = RACC + kSlots * 256 + 4 * (kWarps + 2) + 1024;
-  // aliases (live ranges do not overlap)
+  // aliases (live ranges do not overlap).  The next tile's inputs land in
+  // their buffers as these die: W codes after round 1; V, dO, state codes and
+  // dH' after round 3; T diag(beta) and Q after round 4; T after round 6; K
+  // after round 7.
   static constexpr int DDB = DH;             // dDelta [64 tok][128 n]  (rounds 2-3)
-  static constexpr int GMB = DH + 16384;     // Gm [64][64]              (rounds 2-7)
+  static constexpr int GMB = PB;             // Gm [64][64]              (rounds 2-7, over P)
   static constexpr int DWB = TU;             // dW [64 tok][128 d]       (rounds 3-4)
-  static constexpr int DTB = WB;             // dT [64][64]              (rounds 4-5)
-  static constexpr int XB = WB + 8192;       // X = T^T dT               (rounds 5-6)
-  static constexpr int DKKB = DB;            // dKK + dKK^T              (rounds 6-7)
-  static constexpr int WC8 = DB;             // W codes u8 [64][128]     (prologue)
-  static constexpr int HC8 = PB;             // state codes u8 [128][128] (prologue)
+  static constexpr int DTB = DB;             // dT [64][64]              (rounds 4-5)
+  static constexpr int XB = DB + 8192;       // X = T^T dT               (rounds 5-6)
+  static constexpr int DKKB = DB + 8192;     // dKK + dKK^T              (rounds 6-7, over X)
+  static constexpr int WC8 = WB + 8192;      // W codes u8 [64][128]     (upper half of W^)
+  static constexpr int HC8 = HB + 16384;     // state codes u8 [128][128] (upper half of H^)
   static_assert(BYTES <= 232448, "shared memory budget");
-  static_assert(GK == PB + 8192 && HC8 + 16384 <= TB, "state codes staging");
+};
+
+// a tile: one (chunk slot, value head)
+struct Tile {
+  int64_t ctok, sh;  // first token of the chunk, slot * Hv + h
+  int h, hk, Lc;     // value head, key head, valid rows
 };
 
 // bytes of the input copies of one chunk
@@ -161,49 +171,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
   unsigned char* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
   __shared__ __align__(8) uint64_t bar_in, bar_mma;
   __shared__ uint32_t tmem_slot;
+  __shared__ float scl[9];  // the tile's state scales (one per block_v columns), then sW
 
-  const int64_t slot = blockIdx.x;
-  const int h = blockIdx.y;
-  const int hk = h / p.G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q4 = warp & 3, cq = warp >> 2;  // row quadrant (TMEM lanes), column quarter
   const int gq = lane >> 2, tq = lane & 3;
   const int row0 = 16 * q4;                 // this warp's accumulator rows row0 .. row0 + 15
-
-  // chunk slot -> (sequence, chunk)
-  int n, c;
-  if (p.cu_seqlens) {
-    int lo = 0, hi = p.N - 1;
-    while (lo < hi) {  // last n with floor(cu[n] / 64) + n <= slot
-      const int mid = (lo + hi + 1) >> 1;
-      if ((int64_t)p.cu_seqlens[mid] / kChunk + mid <= slot) lo = mid; else hi = mid - 1;
-    }
-    n = lo;
-    c = (int)(slot - ((int64_t)p.cu_seqlens[n] / kChunk + n));
-  } else {
-    n = (int)(slot / p.nt_fixed);
-    c = (int)(slot % p.nt_fixed);
-  }
-  int64_t tok0;
-  int L;
-  if (p.cu_seqlens) {
-    tok0 = p.cu_seqlens[n];
-    L = (int)(p.cu_seqlens[n + 1] - tok0);
-  } else {
-    tok0 = (int64_t)n * p.T;
-    L = (int)p.T;
-  }
-  if (c < 0 || c * kChunk >= L) return;  // an unused slot (the whole CTA leaves)
-  const int Lc = min(L - c * kChunk, kChunk);
-  const int64_t ctok = tok0 + (int64_t)c * kChunk;
-  const int64_t sh = slot * p.Hv + h;
-
-  const float* cvs = reinterpret_cast<const float*>(sm + S::CV);
-  const float* gam = cvs + kCvGam;
-  const float* eg = cvs + kCvEg;
-  const float* dec = cvs + kCvDec;
-  const float* bet = cvs + kCvBet;
-  const float* beg = cvs + kCvBeg;
   float* racc = reinterpret_cast<float*>(sm + S::RACC);
   float* hd_part = racc + S::kSlots * 64;  // [kWarps] <H^, dH'> partials, then [2] sums of t_i
 
@@ -213,7 +186,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
     mbar_init(&bar_mma, 1);
     fence_mbar_init();
   }
-  for (int i = tid; i < S::kSlots * 64 + kWarps + 2; i += kThreads) racc[i] = 0.f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -221,26 +193,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
   const uint32_t tq_base = tmem + ((uint32_t)(32 * q4) << 16);  // this warp's lane quadrant
   const uint32_t sb = smem_u32(sm);
 
-  if (tid == 0) {
-    mbar_expect_tx(&bar_in, kInTx);
-    const int y = (int)ctok;
-#pragma unroll
-    for (int pn = 0; pn < 2; ++pn) {
-      tma_load_2d(sm + S::QS + pn * 8192, &p.tm_q, hk * 128 + pn * 64, y, &bar_in);
-      tma_load_2d(sm + S::KS + pn * 8192, &p.tm_k, hk * 128 + pn * 64, y, &bar_in);
-      tma_load_2d(sm + S::VS + pn * 8192, &p.tm_v, h * 128 + pn * 64, y, &bar_in);
-      tma_load_2d(sm + S::DOS + pn * 8192, &p.tm_do, h * 128 + pn * 64, y, &bar_in);
-    }
-    tma_load_2d(sm + S::WC8, &p.tm_wc, h * 128, y, &bar_in);
-    bulk_load_1d(sm + S::HC8, p.h_codes + sh * 16384, 16384, &bar_in);
-    bulk_load_1d(sm + S::TB, static_cast<const unsigned char*>(p.tb) + sh * 8192, 8192, &bar_in);
-    bulk_load_1d(sm + S::TU, static_cast<const unsigned char*>(p.tu_img) + sh * 16384, 16384, &bar_in);
-    bulk_load_1d(sm + S::DH, static_cast<const unsigned char*>(p.ws_dh) + sh * 32768, 32768, &bar_in);
-    bulk_load_1d(sm + S::CV, p.cvec + sh * kCvecFloats, kCvecFloats * 4, &bar_in);
-  }
-
-  // bounded wait on a round's barrier; on a timeout the error flag is set and
-  // the copies / products in flight are waited for once more before teardown
+  // bounded wait on a barrier; on a timeout the error flag is set and the
+  // copies / products in flight are waited for once more before teardown
   bool failed = false;
   auto wait_all = [&](uint64_t* bar, uint32_t parity) {
     const bool ok = mbar_wait(bar, parity);
@@ -262,450 +216,559 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
     tc_fence_after();
   };
 
-  wait_all(&bar_in, 0);
-  if (failed) goto teardown;
+  // ---- tiles: (chunk slot, value head), tile = slot * Hv + h, every gridDim.x-th ----
+  const int64_t n_tiles = p.n_slots * p.Hv;
+  auto decode = [&](int64_t t, Tile& ti) -> bool {
+    const int64_t slot = t / p.Hv;
+    int n, c;
+    if (p.cu_seqlens) {
+      int lo = 0, hi = p.N - 1;
+      while (lo < hi) {  // last n with floor(cu[n] / 64) + n <= slot
+        const int mid = (lo + hi + 1) >> 1;
+        if ((int64_t)p.cu_seqlens[mid] / kChunk + mid <= slot) lo = mid; else hi = mid - 1;
+      }
+      n = lo;
+      c = (int)(slot - ((int64_t)p.cu_seqlens[n] / kChunk + n));
+    } else {
+      n = (int)(slot / p.nt_fixed);
+      c = (int)(slot % p.nt_fixed);
+    }
+    const int64_t tok0 = p.cu_seqlens ? (int64_t)p.cu_seqlens[n] : (int64_t)n * p.T;
+    const int L = p.cu_seqlens ? (int)(p.cu_seqlens[n + 1] - tok0) : (int)p.T;
+    if (c < 0 || c * kChunk >= L) return false;  // an unused slot
+    ti.h = (int)(t % p.Hv);
+    ti.hk = ti.h / p.G;
+    ti.Lc = min(L - c * kChunk, kChunk);
+    ti.ctok = tok0 + (int64_t)c * kChunk;
+    ti.sh = t;
+    return true;
+  };
+  auto next_tile = [&](int64_t from, Tile& ti) -> int64_t {
+    for (int64_t t = from; t < n_tiles; t += gridDim.x)
+      if (decode(t, ti)) return t;
+    return -1;
+  };
+  // the input copies of tile ti in five groups, each issued (by thread 0) once
+  // the current tile no longer reads the buffers it fills; cb: the chunk-vector
+  // buffer.  Group 0 opens the barrier's next phase with the whole byte count.
+  auto load_group = [&](int g, const Tile& ti, int cb) {
+    if (tid != 0) return;
+    const int y = (int)ti.ctok;
+    const int64_t sh = ti.sh;
+    if (g == 0) {
+      mbar_expect_tx(&bar_in, kInTx);
+      tma_load_2d(sm + S::WC8, &p.tm_wc, ti.h * 128, y, &bar_in);
+      bulk_load_1d(sm + S::CV + cb * kCvecFloats * 4, p.cvec + sh * kCvecFloats, kCvecFloats * 4,
+                   &bar_in);
+    } else if (g == 1) {
+#pragma unroll
+      for (int pn = 0; pn < 2; ++pn) {
+        tma_load_2d(sm + S::VS + pn * 8192, &p.tm_v, ti.h * 128 + pn * 64, y, &bar_in);
+        tma_load_2d(sm + S::DOS + pn * 8192, &p.tm_do, ti.h * 128 + pn * 64, y, &bar_in);
+      }
+      bulk_load_1d(sm + S::HC8, p.h_codes + sh * 16384, 16384, &bar_in);
+      bulk_load_1d(sm + S::DH, static_cast<const unsigned char*>(p.ws_dh) + sh * 32768, 32768, &bar_in);
+    } else if (g == 2) {
+      bulk_load_1d(sm + S::TU, static_cast<const unsigned char*>(p.tu_img) + sh * 16384, 16384, &bar_in);
+#pragma unroll
+      for (int pn = 0; pn < 2; ++pn)
+        tma_load_2d(sm + S::QS + pn * 8192, &p.tm_q, ti.hk * 128 + pn * 64, y, &bar_in);
+    } else if (g == 3) {
+      bulk_load_1d(sm + S::TB, static_cast<const unsigned char*>(p.tb) + sh * 8192, 8192, &bar_in);
+    } else {
+#pragma unroll
+      for (int pn = 0; pn < 2; ++pn)
+        tma_load_2d(sm + S::KS + pn * 8192, &p.tm_k, ti.hk * 128 + pn * 64, y, &bar_in);
+    }
+  };
 
-  // ---- prologue: rows past the chunk end zeroed; W and state codes -> bf16 ----
-  if (Lc < kChunk) {
-    for (int i = tid; i < (kChunk - Lc) * 8 * 2; i += kThreads) {
-      const int r = Lc + (i >> 4), ch = i & 15;  // 16-byte chunk ch of row r (two panels)
-      const uint32_t off = (uint32_t)((ch >> 3) * 8192 + r * 128 + (ch & 7) * 16);
-      const uint4 z = make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(sm + S::QS + off) = z;
-      *reinterpret_cast<uint4*>(sm + S::KS + off) = z;
-      *reinterpret_cast<uint4*>(sm + S::VS + off) = z;
-      *reinterpret_cast<uint4*>(sm + S::DOS + off) = z;
-      if (ch < 8) *reinterpret_cast<uint4*>(sm + S::WC8 + r * 128 + ch * 16) = z;
-    }
-    __syncthreads();
-  }
-  {
-    // W codes u8 [64][128] -> bf16 panels; 8 codes per step
-    for (int i = tid; i < 64 * 16; i += kThreads) {
-      const int r = i >> 4, c8 = i & 15;
-      const uint2 u = *reinterpret_cast<const uint2*>(sm + S::WC8 + r * 128 + c8 * 8);
-      const float4 a = qdq_code4_values<WM>(u.x), b = qdq_code4_values<WM>(u.y);
-      *reinterpret_cast<uint4*>(sm + S::WB + pan_off(r, c8 * 8, 64)) =
-          make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
-    }
-    // state codes u8 [128 d][128 n] -> bf16 panels (values: codes; the scales
-    // enter the Delta epilogue, and the codes become values after round 1)
-    for (int i = tid; i < 128 * 16; i += kThreads) {
-      const int d = i >> 4, c8 = i & 15;
-      const uint2 u = *reinterpret_cast<const uint2*>(sm + S::HC8 + d * 128 + c8 * 8);
-      const float4 a = qdq_code4_values<SM>(u.x), b = qdq_code4_values<SM>(u.y);
-      *reinterpret_cast<uint4*>(sm + S::HB + pan_off(d, c8 * 8, 128)) =
-          make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(b.x, b.y), pack_bf16(b.z, b.w));
-    }
-  }
-  publish();
+  const uint32_t kId64 = idesc(64, 64, 0, 0), kId128KK = idesc(64, 128, 0, 0);
+  const uint32_t kId128KM = idesc(64, 128, 0, 1), kId128MM = idesc(64, 128, 1, 1);
+  const uint32_t kId64MM = idesc(64, 64, 1, 1);
+  auto dsc = [&](int region, uint32_t lbo) { return sdesc(sb + (uint32_t)region, lbo, 1024); };
+  uint32_t parity = 0, in_parity = 0;
+  auto round_end = [&]() {
+    if (tid == 0) umma_commit(&bar_mma);
+    wait_all(&bar_mma, parity);
+    parity ^= 1u;
+  };
 
-  {
-    const uint32_t kId64 = idesc(64, 64, 0, 0), kId128KK = idesc(64, 128, 0, 0);
-    const uint32_t kId128KM = idesc(64, 128, 0, 1), kId128MM = idesc(64, 128, 1, 1);
-    const uint32_t kId64MM = idesc(64, 64, 1, 1);
-    auto dsc = [&](int region, uint32_t lbo) { return sdesc(sb + (uint32_t)region, lbo, 1024); };
-    uint32_t parity = 0;
-    auto round_end = [&]() {
-      if (tid == 0) umma_commit(&bar_mma);
-      wait_all(&bar_mma, parity);
-      parity ^= 1u;
-    };
+  Tile cur;
+  int64_t t_cur = next_tile(blockIdx.x, cur);
+  if (t_cur >= 0)
+    for (int g = 0; g < 5; ++g) load_group(g, cur, 0);
+  for (int it = 0; t_cur >= 0; ++it) {
+    Tile nxt;
+    const int64_t t_nxt = next_tile(t_cur + gridDim.x, nxt);
+    const bool more = t_nxt >= 0;
+    const int cb = it & 1;
+    const int h = cur.h, hk = cur.hk, Lc = cur.Lc;
+    const int64_t ctok = cur.ctok, sh = cur.sh;
+    const float* cvs = reinterpret_cast<const float*>(sm + S::CV + cb * kCvecFloats * 4);
+    const float* gam = cvs + kCvGam;
+    const float* eg = cvs + kCvEg;
+    const float* dec = cvs + kCvDec;
+    const float* bet = cvs + kCvBet;
+    const float* beg = cvs + kCvBeg;
+    (void)hk;
+    for (int i = tid; i < S::kSlots * 64 + kWarps + 2; i += kThreads) racc[i] = 0.f;
+    if (tid < (128 >> p.bv_log2)) scl[tid] = p.h_scales[sh * (128 >> p.bv_log2) + tid];
+    if (tid == 32) scl[8] = p.w_scales[sh];
 
-    // =============== round 1: S, G, U, WH, K dH' ===============
-    if (tid == 0) {
-      mma_steps(tmem + 0, dsc(S::QS, 16), false, 8192, dsc(S::KS, 16), false, 8192, 8, kId64, false);
-      mma_steps(tmem + 64, dsc(S::KS, 16), false, 8192, dsc(S::KS, 16), false, 8192, 8, kId64, false);
-      mma_steps(tmem + 128, dsc(S::TU, 16), false, 0, dsc(S::VS, 8192), true, 0, 4, kId128KM, false);
-      mma_steps(tmem + 128, dsc(S::TU + 8192, 16), false, 0, dsc(S::VS, 8192), true, 0, 4, kId128KM,
-                true);
-      mma_steps(tmem + 256, dsc(S::WB, 16), false, 8192, dsc(S::HB, 16384), true, 0, 8, kId128KM, false);
-      mma_steps(tmem + 384, dsc(S::KS, 16), false, 8192, dsc(S::DH, 16384), true, 0, 8, kId128KM, false);
-    }
-    round_end();
+    wait_all(&bar_in, in_parity);
+    in_parity ^= 1u;
     if (failed) goto teardown;
-    {
-      // P and Gamma o KK^T (N = 64: columns 16 cq ..)
-      float s[2][4], g[2][4];
-      tmem_ld_frag<2>(tq_base + 0 + 16 * cq, s);
-      tmem_ld_frag<2>(tq_base + 64 + 16 * cq, g);
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int i = row0 + gq + 8 * e2, j = 16 * cq + 8 * nt + 2 * tq;
-          const float gi = gam[i];
-          const float x0 = __expf(gi - gam[j]), x1 = __expf(gi - gam[j + 1]);
-          st2(sm + S::PB, 64, i, j, j <= i ? x0 * s[nt][2 * e2] : 0.f,
-              j + 1 <= i ? x1 * s[nt][2 * e2 + 1] : 0.f);
-          st2(sm + S::GK, 64, i, j, j < i ? x0 * g[nt][2 * e2] : 0.f,
-              j + 1 < i ? x1 * g[nt][2 * e2 + 1] : 0.f);
-        }
-    }
-    {
-      // Delta = U - sW sH(n) WH (N = 128: columns 32 cq ..)
-      float u[4][4], wh[4][4];
-      tmem_ld_frag<4>(tq_base + 128 + 32 * cq, u);
-      tmem_ld_frag<4>(tq_base + 256 + 32 * cq, wh);
-      const float sW = p.w_scales[sh];
-      const float* hs = p.h_scales + sh * (128 >> p.bv_log2);
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int col = 32 * cq + 8 * nt + 2 * tq;
-        const float s0 = sW * hs[col >> p.bv_log2], s1 = sW * hs[(col + 1) >> p.bv_log2];
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int i = row0 + gq + 8 * e2;
-          st2(sm + S::DB, 64, i, col, u[nt][2 * e2] - s0 * wh[nt][2 * e2],
-              u[nt][2 * e2 + 1] - s1 * wh[nt][2 * e2 + 1]);
-        }
+
+    // ---- prologue: rows past the chunk end zeroed; W and state codes -> bf16
+    //      (the u8 codes sit in the upper halves of their bf16 tiles: all are
+    //      read into registers before any is written) ----
+    if (Lc < kChunk) {
+      for (int i = tid; i < (kChunk - Lc) * 8 * 2; i += kThreads) {
+        const int r = Lc + (i >> 4), ch = i & 15;  // 16-byte chunk ch of row r (two panels)
+        const uint32_t off = (uint32_t)((ch >> 3) * 8192 + r * 128 + (ch & 7) * 16);
+        const uint4 z = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(sm + S::QS + off) = z;
+        *reinterpret_cast<uint4*>(sm + S::KS + off) = z;
+        *reinterpret_cast<uint4*>(sm + S::VS + off) = z;
+        *reinterpret_cast<uint4*>(sm + S::DOS + off) = z;
       }
     }
     {
-      // state codes -> values (bf16 of code x scale), in place; <H^, dH'>
-      float hd = 0.f;
-      const float* hs = p.h_scales + sh * (128 >> p.bv_log2);
-      for (int i = tid; i < 2 * 128 * 8; i += kThreads) {
-        const int pn = i >> 10, d = (i >> 3) & 127, pc = i & 7;  // panel, row, physical chunk
-        const int col = pn * 64 + ((pc ^ (d & 7)) << 3);         // first logical column
-        const float sH = hs[col >> p.bv_log2];
-        const uint32_t off = (uint32_t)(pn * 16384 + d * 128 + pc * 16);
-        uint4 hv = *reinterpret_cast<const uint4*>(sm + S::HB + off);
-        const uint4 dv4 = *reinterpret_cast<const uint4*>(sm + S::DH + off);
-        uint32_t* hw = &hv.x;
-        const uint32_t* dw = &dv4.x;
-#pragma unroll
-        for (int w2 = 0; w2 < 4; ++w2) {
-          const float2 cv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hw[w2]));
-          const float2 dd = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dw[w2]));
-          const float v0 = cv.x * sH, v1 = cv.y * sH;
-          hw[w2] = pack_bf16(v0, v1);
-          hd += v0 * dd.x + v1 * dd.y;
-        }
-        *reinterpret_cast<uint4*>(sm + S::HB + off) = hv;
+      // W codes: thread tid holds row tid / 8, codes 16 (tid % 8) ..; state codes:
+      // row tid / 4, codes 32 (tid % 4) ..
+      const uint4 wc = *reinterpret_cast<const uint4*>(sm + S::WC8 + 16 * tid);
+      const uint4 hc0 = *reinterpret_cast<const uint4*>(sm + S::HC8 + 32 * tid);
+      const uint4 hc1 = *reinterpret_cast<const uint4*>(sm + S::HC8 + 32 * tid + 16);
+      __syncthreads();
+      const int wr = tid >> 3, wcol = (tid & 7) * 16;
+      const bool wz = wr >= Lc;  // W codes of rows past the chunk end belong to other tokens
+      auto put8 = [&](unsigned char* tile, int rows, int r, int col, uint32_t a, uint32_t b, bool zero,
+                      auto mode) {
+        constexpr int MODE = decltype(mode)::value;
+        const float4 x = qdq_code4_values<MODE>(a), y = qdq_code4_values<MODE>(b);
+        *reinterpret_cast<uint4*>(tile + pan_off(r, col, rows)) =
+            zero ? make_uint4(0, 0, 0, 0)
+                 : make_uint4(pack_bf16(x.x, x.y), pack_bf16(x.z, x.w), pack_bf16(y.x, y.y),
+                              pack_bf16(y.z, y.w));
+      };
+      using WMc = std::integral_constant<int, WM>;
+      using SMc = std::integral_constant<int, SM>;
+      put8(sm + S::WB, 64, wr, wcol, wc.x, wc.y, wz, WMc{});
+      put8(sm + S::WB, 64, wr, wcol + 8, wc.z, wc.w, wz, WMc{});
+      const int hr = tid >> 2, hcol = (tid & 3) * 32;
+      put8(sm + S::HB, 128, hr, hcol, hc0.x, hc0.y, false, SMc{});
+      put8(sm + S::HB, 128, hr, hcol + 8, hc0.z, hc0.w, false, SMc{});
+      put8(sm + S::HB, 128, hr, hcol + 16, hc1.x, hc1.y, false, SMc{});
+      put8(sm + S::HB, 128, hr, hcol + 24, hc1.z, hc1.w, false, SMc{});
+    }
+    publish();
+
+    {
+      // =============== round 1: S, G, U, WH, K dH' ===============
+      if (tid == 0) {
+        mma_steps(tmem + 0, dsc(S::QS, 16), false, 8192, dsc(S::KS, 16), false, 8192, 8, kId64, false);
+        mma_steps(tmem + 64, dsc(S::KS, 16), false, 8192, dsc(S::KS, 16), false, 8192, 8, kId64, false);
+        mma_steps(tmem + 128, dsc(S::TU, 16), false, 0, dsc(S::VS, 8192), true, 0, 4, kId128KM, false);
+        mma_steps(tmem + 128, dsc(S::TU + 8192, 16), false, 0, dsc(S::VS, 8192), true, 0, 4, kId128KM,
+                  true);
+        mma_steps(tmem + 256, dsc(S::WB, 16), false, 8192, dsc(S::HB, 16384), true, 0, 8, kId128KM, false);
+        mma_steps(tmem + 384, dsc(S::KS, 16), false, 8192, dsc(S::DH, 16384), true, 0, 8, kId128KM, false);
       }
+      round_end();
+      if (failed) goto teardown;
+      if (more) load_group(0, nxt, cb ^ 1);  // W codes, chunk vectors
+      {
+        // P and Gamma o KK^T (N = 64: columns 16 cq ..)
+        float s[2][4], g[2][4];
+        tmem_ld_frag<2>(tq_base + 0 + 16 * cq, s);
+        tmem_ld_frag<2>(tq_base + 64 + 16 * cq, g);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
-      if (lane == 0) hd_part[warp] = hd;
-    }
-    publish();
-
-    // =============== round 2: P^T dO, dO Delta^T, Delta dH'^T ===============
-    if (tid == 0) {
-      mma_steps(tmem + 0, dsc(S::PB, 8192), true, 0, dsc(S::DOS, 8192), true, 0, 4, kId128MM, false);
-      mma_steps(tmem + 128, dsc(S::DOS, 16), false, 8192, dsc(S::DB, 16), false, 8192, 8, kId64, false);
-      mma_steps(tmem + 192, dsc(S::DB, 16), false, 8192, dsc(S::DH, 16), false, 16384, 8, kId128KK,
-                false);
-    }
-    round_end();
-    if (failed) goto teardown;
-    float dQ[4][4], dK[4][4];
-    {
-      // dDelta = scale P^T dO + dec K dH'  -> bf16 (dH' is no longer read)
-      float a[4][4], b[4][4];
-      tmem_ld_frag<4>(tq_base + 0 + 32 * cq, a);
-      tmem_ld_frag<4>(tq_base + 384 + 32 * cq, b);
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int i = row0 + gq + 8 * e2, j = 16 * cq + 8 * nt + 2 * tq;
+            const float gi = gam[i];
+            const float x0 = __expf(gi - gam[j]), x1 = __expf(gi - gam[j + 1]);
+            st2(sm + S::PB, 64, i, j, j <= i ? x0 * s[nt][2 * e2] : 0.f,
+                j + 1 <= i ? x1 * s[nt][2 * e2 + 1] : 0.f);
+            st2(sm + S::GK, 64, i, j, j < i ? x0 * g[nt][2 * e2] : 0.f,
+                j + 1 < i ? x1 * g[nt][2 * e2 + 1] : 0.f);
+          }
+      }
+      {
+        // Delta = U - sW sH(n) WH (N = 128: columns 32 cq ..)
+        float u[4][4], wh[4][4];
+        tmem_ld_frag<4>(tq_base + 128 + 32 * cq, u);
+        tmem_ld_frag<4>(tq_base + 256 + 32 * cq, wh);
+        const float sW = scl[8];
+        const float* hs = scl;
 #pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int i = row0 + gq + 8 * e2, col = 32 * cq + 8 * nt + 2 * tq;
-          const float di = dec[i];
-          st2(sm + S::DDB, 64, i, col, p.scale * a[nt][2 * e2] + di * b[nt][2 * e2],
-              p.scale * a[nt][2 * e2 + 1] + di * b[nt][2 * e2 + 1]);
-        }
-    }
-    {
-      // dP = lower-incl(scale dO Delta^T); Gm = dP o Gamma; sums of dP * P
-      float x[2][4], pp[2][4];
-      tmem_ld_frag<2>(tq_base + 128 + 16 * cq, x);
+        for (int nt = 0; nt < 4; ++nt) {
+          const int col = 32 * cq + 8 * nt + 2 * tq;
+          const float s0 = sW * hs[col >> p.bv_log2], s1 = sW * hs[(col + 1) >> p.bv_log2];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int i = row0 + gq + 8 * e2, j = 16 * cq + 8 * nt + 2 * tq;
-          const float2 pv = ld2(sm + S::PB, 64, i, j);
-          const float gi = gam[i];
-          const float d0 = j <= i ? p.scale * x[nt][2 * e2] : 0.f;
-          const float d1 = j + 1 <= i ? p.scale * x[nt][2 * e2 + 1] : 0.f;
-          st2(sm + S::GMB, 64, i, j, j <= i ? d0 * __expf(gi - gam[j]) : 0.f,
-              j + 1 <= i ? d1 * __expf(gi - gam[j + 1]) : 0.f);
-          pp[nt][2 * e2] = d0 * pv.x;
-          pp[nt][2 * e2 + 1] = d1 * pv.y;
-        }
-      add_row_sums<2>(pp, racc, R_PPR + cq, row0, gq, tq);
-      add_col_sums<2>(pp, racc, R_PPC + q4, 16 * cq, gq, tq);
-    }
-    {
-      // dK = dec (Delta dH'^T); t_i = sum_d k_id dK_id
-      float a[4][4], kd[4][4];
-      tmem_ld_frag<4>(tq_base + 192 + 32 * cq, a);
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int i = row0 + gq + 8 * e2, d = 32 * cq + 8 * nt + 2 * tq;
-          const float2 kv = ld2(sm + S::KS, 64, i, d);
-          const float di = dec[i];
-          dK[nt][2 * e2] = di * a[nt][2 * e2];
-          dK[nt][2 * e2 + 1] = di * a[nt][2 * e2 + 1];
-          kd[nt][2 * e2] = dK[nt][2 * e2] * kv.x;
-          kd[nt][2 * e2 + 1] = dK[nt][2 * e2 + 1] * kv.y;
-        }
-      add_row_sums<4>(kd, racc, R_TT + cq, row0, gq, tq);
-    }
-    publish();
-
-    // =============== round 3: dO H^T, dDelta H^T, dDelta V^T, T^T dDelta ===============
-    if (tid == 0) {
-      mma_steps(tmem + 0, dsc(S::DOS, 16), false, 8192, dsc(S::HB, 16), false, 16384, 8, kId128KK,
-                false);
-      mma_steps(tmem + 128, dsc(S::DDB, 16), false, 8192, dsc(S::HB, 16), false, 16384, 8, kId128KK,
-                false);
-      mma_steps(tmem + 256, dsc(S::DDB, 16), false, 8192, dsc(S::VS, 16), false, 8192, 8, kId64, false);
-      mma_steps(tmem + 320, dsc(S::TB, 8192), true, 0, dsc(S::DDB, 8192), true, 0, 4, kId128MM, false);
-    }
-    round_end();
-    if (failed) goto teardown;
-    {
-      // dQ = scale e^g (dO H^T); sum_d q_id dQ_id
-      float a[4][4], qd[4][4];
-      tmem_ld_frag<4>(tq_base + 0 + 32 * cq, a);
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int i = row0 + gq + 8 * e2, d = 32 * cq + 8 * nt + 2 * tq;
-          const float2 qv = ld2(sm + S::QS, 64, i, d);
-          const float si = p.scale * eg[i];
-          dQ[nt][2 * e2] = si * a[nt][2 * e2];
-          dQ[nt][2 * e2 + 1] = si * a[nt][2 * e2 + 1];
-          qd[nt][2 * e2] = dQ[nt][2 * e2] * qv.x;
-          qd[nt][2 * e2 + 1] = dQ[nt][2 * e2 + 1] * qv.y;
-        }
-      add_row_sums<4>(qd, racc, R_OH + cq, row0, gq, tq);
-    }
-    {
-      // dW = -dDelta H^T -> bf16 (T diag(beta) is no longer read)
-      float a[4][4];
-      tmem_ld_frag<4>(tq_base + 128 + 32 * cq, a);
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int i = row0 + gq + 8 * e2, d = 32 * cq + 8 * nt + 2 * tq;
-          st2(sm + S::DWB, 64, i, d, -a[nt][2 * e2], -a[nt][2 * e2 + 1]);
-        }
-    }
-    {
-      // dV = beta (T^T dDelta); sum_n v_jn (T^T dDelta)_jn
-      float a[4][4], bv[4][4];
-      tmem_ld_frag<4>(tq_base + 320 + 32 * cq, a);
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int j = row0 + gq + 8 * e2, col = 32 * cq + 8 * nt + 2 * tq;
-          const float2 vv = ld2(sm + S::VS, 64, j, col);
-          bv[nt][2 * e2] = a[nt][2 * e2] * vv.x;
-          bv[nt][2 * e2 + 1] = a[nt][2 * e2 + 1] * vv.y;
-          if (j < Lc)
-            *reinterpret_cast<float2*>(p.dv + ((ctok + j) * p.Hv + h) * 128 + col) =
-                make_float2(bet[j] * a[nt][2 * e2], bet[j] * a[nt][2 * e2 + 1]);
-        }
-      add_row_sums<4>(bv, racc, R_BU + cq, row0, gq, tq);
-    }
-    publish();
-
-    // =============== round 4: dW K^T, T^T dW, Gm^T Q ===============
-    if (tid == 0) {
-      mma_steps(tmem + 0, dsc(S::DWB, 16), false, 8192, dsc(S::KS, 16), false, 8192, 8, kId64, false);
-      mma_steps(tmem + 64, dsc(S::TB, 8192), true, 0, dsc(S::DWB, 8192), true, 0, 4, kId128MM, false);
-      mma_steps(tmem + 384, dsc(S::GMB, 8192), true, 0, dsc(S::QS, 8192), true, 0, 4, kId128MM, false);
-    }
-    round_end();
-    if (failed) goto teardown;
-    {
-      // dT = (dDelta V^T) diag(beta) + (dW K^T) diag(beta e^g) -> bf16
-      float a[2][4], b[2][4];
-      tmem_ld_frag<2>(tq_base + 256 + 16 * cq, a);
-      tmem_ld_frag<2>(tq_base + 0 + 16 * cq, b);
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int i = row0 + gq + 8 * e2, j = 16 * cq + 8 * nt + 2 * tq;
-          st2(sm + S::DTB, 64, i, j, a[nt][2 * e2] * bet[j] + b[nt][2 * e2] * beg[j],
-              a[nt][2 * e2 + 1] * bet[j + 1] + b[nt][2 * e2 + 1] * beg[j + 1]);
-        }
-    }
-    {
-      // dK += beta e^g (T^T dW); sum_d k_id (T^T dW)_id
-      float a[4][4], kw[4][4];
-      tmem_ld_frag<4>(tq_base + 64 + 32 * cq, a);
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int i = row0 + gq + 8 * e2, d = 32 * cq + 8 * nt + 2 * tq;
-          const float2 kv = ld2(sm + S::KS, 64, i, d);
-          dK[nt][2 * e2] += beg[i] * a[nt][2 * e2];
-          dK[nt][2 * e2 + 1] += beg[i] * a[nt][2 * e2 + 1];
-          kw[nt][2 * e2] = a[nt][2 * e2] * kv.x;
-          kw[nt][2 * e2 + 1] = a[nt][2 * e2 + 1] * kv.y;
-        }
-      add_row_sums<4>(kw, racc, R_KW + cq, row0, gq, tq);
-    }
-    publish();
-
-    // =============== round 5: X = T^T dT ===============
-    if (tid == 0)
-      mma_steps(tmem + 0, dsc(S::TB, 8192), true, 0, dsc(S::DTB, 8192), true, 0, 4, kId64MM, false);
-    round_end();
-    if (failed) goto teardown;
-    {
-      float a[2][4];
-      tmem_ld_frag<2>(tq_base + 0 + 16 * cq, a);
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int i = row0 + gq + 8 * e2, j = 16 * cq + 8 * nt + 2 * tq;
-          st2(sm + S::XB, 64, i, j, a[nt][2 * e2], a[nt][2 * e2 + 1]);
-        }
-    }
-    publish();
-
-    // =============== round 6: X T^T ===============
-    if (tid == 0)
-      mma_steps(tmem + 64, dsc(S::XB, 16), false, 0, dsc(S::TB, 16), false, 0, 4, kId64, false);
-    round_end();
-    if (failed) goto teardown;
-    {
-      // dA = -(X T^T) strictly lower; dKK = dA beta_i Gamma_ij (symmetric tile);
-      // sums of dA * Gamma o KK^T and of dA * A
-      float a[2][4], ba[2][4], aa[2][4];
-      tmem_ld_frag<2>(tq_base + 64 + 16 * cq, a);
-#pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int e2 = 0; e2 < 2; ++e2) {
-          const int i = row0 + gq + 8 * e2, j = 16 * cq + 8 * nt + 2 * tq;
-          const float2 gv = ld2(sm + S::GK, 64, i, j);
-          const float gi = gam[i], bi = bet[i];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int jj = j + e;
-            const float da = jj < i ? -a[nt][2 * e2 + e] : 0.f;
-            const float gkk = e == 0 ? gv.x : gv.y;
-            ba[nt][2 * e2 + e] = da * gkk;
-            aa[nt][2 * e2 + e] = da * bi * gkk;
-            if (jj < i) {
-              const __nv_bfloat16 kk = __float2bfloat16(da * bi * __expf(gi - gam[jj]));
-              *reinterpret_cast<__nv_bfloat16*>(sm + S::DKKB + pan_off(i, jj, 64)) = kk;
-              *reinterpret_cast<__nv_bfloat16*>(sm + S::DKKB + pan_off(jj, i, 64)) = kk;
-            } else if (jj == i) {
-              *reinterpret_cast<__nv_bfloat16*>(sm + S::DKKB + pan_off(i, i, 64)) = __float2bfloat16(0.f);
-            }
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int i = row0 + gq + 8 * e2;
+            st2(sm + S::DB, 64, i, col, u[nt][2 * e2] - s0 * wh[nt][2 * e2],
+                u[nt][2 * e2 + 1] - s1 * wh[nt][2 * e2 + 1]);
           }
         }
-      add_row_sums<2>(ba, racc, R_BA + cq, row0, gq, tq);
-      add_row_sums<2>(aa, racc, R_AAR + cq, row0, gq, tq);
-      add_col_sums<2>(aa, racc, R_AAC + q4, 16 * cq, gq, tq);
-    }
-    publish();
-
-    // =============== round 7: Gm K, dKK K ===============
-    if (tid == 0) {
-      mma_steps(tmem + 128, dsc(S::GMB, 16), false, 0, dsc(S::KS, 8192), true, 0, 4, kId128KM, false);
-      mma_steps(tmem + 384, dsc(S::DKKB, 16), false, 0, dsc(S::KS, 8192), true, 0, 4, kId128KM, true);
-    }
-    round_end();
-    if (failed) goto teardown;
-    {
-      float a[4][4], b[4][4];
-      tmem_ld_frag<4>(tq_base + 128 + 32 * cq, a);
-      tmem_ld_frag<4>(tq_base + 384 + 32 * cq, b);
+      }
+      {
+        // state codes -> values (bf16 of code x scale), in place; <H^, dH'>
+        float hd = 0.f;
+        const float* hs = scl;
+        for (int i = tid; i < 2 * 128 * 8; i += kThreads) {
+          const int pn = i >> 10, d = (i >> 3) & 127, pc = i & 7;  // panel, row, physical chunk
+          const int col = pn * 64 + ((pc ^ (d & 7)) << 3);         // first logical column
+          const float sH = hs[col >> p.bv_log2];
+          const uint32_t off = (uint32_t)(pn * 16384 + d * 128 + pc * 16);
+          uint4 hv = *reinterpret_cast<const uint4*>(sm + S::HB + off);
+          const uint4 dv4 = *reinterpret_cast<const uint4*>(sm + S::DH + off);
+          uint32_t* hw = &hv.x;
+          const uint32_t* dw = &dv4.x;
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          dQ[nt][e] += a[nt][e];
-          dK[nt][e] += b[nt][e];
+          for (int w2 = 0; w2 < 4; ++w2) {
+            const float2 cv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&hw[w2]));
+            const float2 dd = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&dw[w2]));
+            const float v0 = cv.x * sH, v1 = cv.y * sH;
+            hw[w2] = pack_bf16(v0, v1);
+            hd += v0 * dd.x + v1 * dd.y;
+          }
+          *reinterpret_cast<uint4*>(sm + S::HB + off) = hv;
         }
-      // one writer per element; lane pairs (tq, tq ^ 1) swap halves so each
-      // lane stores four consecutive columns of one row
-      const bool odd = tq & 1;
-      const int i_own = row0 + gq + (odd ? 8 : 0);
 #pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int c4 = 32 * cq + 8 * nt + 2 * (tq & ~1);
-        const float sq0 = __shfl_xor_sync(0xffffffffu, odd ? dQ[nt][0] : dQ[nt][2], 1);
-        const float sq1 = __shfl_xor_sync(0xffffffffu, odd ? dQ[nt][1] : dQ[nt][3], 1);
-        const float sk0 = __shfl_xor_sync(0xffffffffu, odd ? dK[nt][0] : dK[nt][2], 1);
-        const float sk1 = __shfl_xor_sync(0xffffffffu, odd ? dK[nt][1] : dK[nt][3], 1);
-        const float4 vq = odd ? make_float4(sq0, sq1, dQ[nt][2], dQ[nt][3])
-                              : make_float4(dQ[nt][0], dQ[nt][1], sq0, sq1);
-        const float4 vk = odd ? make_float4(sk0, sk1, dK[nt][2], dK[nt][3])
-                              : make_float4(dK[nt][0], dK[nt][1], sk0, sk1);
-        if (i_own < Lc) {
-          const int64_t off = ((ctok + i_own) * p.HH + (p.G > 1 ? h : hk)) * 128 + c4;
-          *reinterpret_cast<float4*>(p.dq + off) = vq;
-          *reinterpret_cast<float4*>(p.dk + off) = vk;
+        for (int o = 16; o > 0; o >>= 1) hd += __shfl_xor_sync(0xffffffffu, hd, o);
+        if (lane == 0) hd_part[warp] = hd;
+      }
+      publish();
+
+      // =============== round 2: P^T dO, dO Delta^T, Delta dH'^T ===============
+      if (tid == 0) {
+        mma_steps(tmem + 0, dsc(S::PB, 8192), true, 0, dsc(S::DOS, 8192), true, 0, 4, kId128MM, false);
+        mma_steps(tmem + 128, dsc(S::DOS, 16), false, 8192, dsc(S::DB, 16), false, 8192, 8, kId64, false);
+        mma_steps(tmem + 192, dsc(S::DB, 16), false, 8192, dsc(S::DH, 16), false, 16384, 8, kId128KK,
+                  false);
+      }
+      round_end();
+      if (failed) goto teardown;
+      float dQ[4][4], dK[4][4];
+      {
+        // dDelta = scale P^T dO + dec K dH'  -> bf16 (dH' is no longer read)
+        float a[4][4], b[4][4];
+        tmem_ld_frag<4>(tq_base + 0 + 32 * cq, a);
+        tmem_ld_frag<4>(tq_base + 384 + 32 * cq, b);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int i = row0 + gq + 8 * e2, col = 32 * cq + 8 * nt + 2 * tq;
+            const float di = dec[i];
+            st2(sm + S::DDB, 64, i, col, p.scale * a[nt][2 * e2] + di * b[nt][2 * e2],
+                p.scale * a[nt][2 * e2 + 1] + di * b[nt][2 * e2 + 1]);
+          }
+      }
+      {
+        // dP = lower-incl(scale dO Delta^T); Gm = dP o Gamma; sums of dP * P
+        float x[2][4], pp[2][4];
+        tmem_ld_frag<2>(tq_base + 128 + 16 * cq, x);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int i = row0 + gq + 8 * e2, j = 16 * cq + 8 * nt + 2 * tq;
+            const float2 pv = ld2(sm + S::PB, 64, i, j);
+            const float gi = gam[i];
+            const float d0 = j <= i ? p.scale * x[nt][2 * e2] : 0.f;
+            const float d1 = j + 1 <= i ? p.scale * x[nt][2 * e2 + 1] : 0.f;
+            st2(sm + S::GMB, 64, i, j, j <= i ? d0 * __expf(gi - gam[j]) : 0.f,
+                j + 1 <= i ? d1 * __expf(gi - gam[j + 1]) : 0.f);
+            pp[nt][2 * e2] = d0 * pv.x;
+            pp[nt][2 * e2 + 1] = d1 * pv.y;
+          }
+        add_row_sums<2>(pp, racc, R_PPR + cq, row0, gq, tq);
+        add_col_sums<2>(pp, racc, R_PPC + q4, 16 * cq, gq, tq);
+      }
+      {
+        // dK = dec (Delta dH'^T); t_i = sum_d k_id dK_id
+        float a[4][4], kd[4][4];
+        tmem_ld_frag<4>(tq_base + 192 + 32 * cq, a);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int i = row0 + gq + 8 * e2, d = 32 * cq + 8 * nt + 2 * tq;
+            const float2 kv = ld2(sm + S::KS, 64, i, d);
+            const float di = dec[i];
+            dK[nt][2 * e2] = di * a[nt][2 * e2];
+            dK[nt][2 * e2 + 1] = di * a[nt][2 * e2 + 1];
+            kd[nt][2 * e2] = dK[nt][2 * e2] * kv.x;
+            kd[nt][2 * e2 + 1] = dK[nt][2 * e2 + 1] * kv.y;
+          }
+        add_row_sums<4>(kd, racc, R_TT + cq, row0, gq, tq);
+      }
+      publish();
+
+      // =============== round 3: dO H^T, dDelta H^T, dDelta V^T, T^T dDelta ===============
+      if (tid == 0) {
+        mma_steps(tmem + 0, dsc(S::DOS, 16), false, 8192, dsc(S::HB, 16), false, 16384, 8, kId128KK,
+                  false);
+        mma_steps(tmem + 128, dsc(S::DDB, 16), false, 8192, dsc(S::HB, 16), false, 16384, 8, kId128KK,
+                  false);
+        mma_steps(tmem + 256, dsc(S::DDB, 16), false, 8192, dsc(S::VS, 16), false, 8192, 8, kId64, false);
+        mma_steps(tmem + 320, dsc(S::TB, 8192), true, 0, dsc(S::DDB, 8192), true, 0, 4, kId128MM, false);
+      }
+      round_end();
+      if (failed) goto teardown;
+      {
+        // dQ = scale e^g (dO H^T); sum_d q_id dQ_id
+        float a[4][4], qd[4][4];
+        tmem_ld_frag<4>(tq_base + 0 + 32 * cq, a);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int i = row0 + gq + 8 * e2, d = 32 * cq + 8 * nt + 2 * tq;
+            const float2 qv = ld2(sm + S::QS, 64, i, d);
+            const float si = p.scale * eg[i];
+            dQ[nt][2 * e2] = si * a[nt][2 * e2];
+            dQ[nt][2 * e2 + 1] = si * a[nt][2 * e2 + 1];
+            qd[nt][2 * e2] = dQ[nt][2 * e2] * qv.x;
+            qd[nt][2 * e2 + 1] = dQ[nt][2 * e2 + 1] * qv.y;
+          }
+        add_row_sums<4>(qd, racc, R_OH + cq, row0, gq, tq);
+      }
+      {
+        // dW = -dDelta H^T -> bf16 (T diag(beta) is no longer read)
+        float a[4][4];
+        tmem_ld_frag<4>(tq_base + 128 + 32 * cq, a);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int i = row0 + gq + 8 * e2, d = 32 * cq + 8 * nt + 2 * tq;
+            st2(sm + S::DWB, 64, i, d, -a[nt][2 * e2], -a[nt][2 * e2 + 1]);
+          }
+      }
+      {
+        // dV = beta (T^T dDelta); sum_n v_jn (T^T dDelta)_jn
+        float a[4][4], bv[4][4];
+        tmem_ld_frag<4>(tq_base + 320 + 32 * cq, a);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int j = row0 + gq + 8 * e2, col = 32 * cq + 8 * nt + 2 * tq;
+            const float2 vv = ld2(sm + S::VS, 64, j, col);
+            bv[nt][2 * e2] = a[nt][2 * e2] * vv.x;
+            bv[nt][2 * e2 + 1] = a[nt][2 * e2 + 1] * vv.y;
+            if (j < Lc)
+              *reinterpret_cast<float2*>(p.dv + ((ctok + j) * p.Hv + h) * 128 + col) =
+                  make_float2(bet[j] * a[nt][2 * e2], bet[j] * a[nt][2 * e2 + 1]);
+          }
+        add_row_sums<4>(bv, racc, R_BU + cq, row0, gq, tq);
+      }
+      publish();
+
+      // =============== round 4: dW K^T, T^T dW, Gm^T Q ===============
+      if (more) load_group(1, nxt, cb ^ 1);  // V, dO, state codes, dH'
+      if (tid == 0) {
+        mma_steps(tmem + 0, dsc(S::DWB, 16), false, 8192, dsc(S::KS, 16), false, 8192, 8, kId64, false);
+        mma_steps(tmem + 64, dsc(S::TB, 8192), true, 0, dsc(S::DWB, 8192), true, 0, 4, kId128MM, false);
+        mma_steps(tmem + 384, dsc(S::GMB, 8192), true, 0, dsc(S::QS, 8192), true, 0, 4, kId128MM, false);
+      }
+      round_end();
+      if (failed) goto teardown;
+      if (more) load_group(2, nxt, cb ^ 1);  // T diag(beta), Q
+      {
+        // dT = (dDelta V^T) diag(beta) + (dW K^T) diag(beta e^g) -> bf16
+        float a[2][4], b[2][4];
+        tmem_ld_frag<2>(tq_base + 256 + 16 * cq, a);
+        tmem_ld_frag<2>(tq_base + 0 + 16 * cq, b);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int i = row0 + gq + 8 * e2, j = 16 * cq + 8 * nt + 2 * tq;
+            st2(sm + S::DTB, 64, i, j, a[nt][2 * e2] * bet[j] + b[nt][2 * e2] * beg[j],
+                a[nt][2 * e2 + 1] * bet[j + 1] + b[nt][2 * e2 + 1] * beg[j + 1]);
+          }
+      }
+      {
+        // dK += beta e^g (T^T dW); sum_d k_id (T^T dW)_id
+        float a[4][4], kw[4][4];
+        tmem_ld_frag<4>(tq_base + 64 + 32 * cq, a);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int i = row0 + gq + 8 * e2, d = 32 * cq + 8 * nt + 2 * tq;
+            const float2 kv = ld2(sm + S::KS, 64, i, d);
+            dK[nt][2 * e2] += beg[i] * a[nt][2 * e2];
+            dK[nt][2 * e2 + 1] += beg[i] * a[nt][2 * e2 + 1];
+            kw[nt][2 * e2] = a[nt][2 * e2] * kv.x;
+            kw[nt][2 * e2 + 1] = a[nt][2 * e2 + 1] * kv.y;
+          }
+        add_row_sums<4>(kw, racc, R_KW + cq, row0, gq, tq);
+      }
+      publish();
+
+      // =============== round 5: X = T^T dT ===============
+      if (tid == 0)
+        mma_steps(tmem + 0, dsc(S::TB, 8192), true, 0, dsc(S::DTB, 8192), true, 0, 4, kId64MM, false);
+      round_end();
+      if (failed) goto teardown;
+      {
+        float a[2][4];
+        tmem_ld_frag<2>(tq_base + 0 + 16 * cq, a);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int i = row0 + gq + 8 * e2, j = 16 * cq + 8 * nt + 2 * tq;
+            st2(sm + S::XB, 64, i, j, a[nt][2 * e2], a[nt][2 * e2 + 1]);
+          }
+      }
+      publish();
+
+      // =============== round 6: X T^T ===============
+      if (tid == 0)
+        mma_steps(tmem + 64, dsc(S::XB, 16), false, 0, dsc(S::TB, 16), false, 0, 4, kId64, false);
+      round_end();
+      if (failed) goto teardown;
+      if (more) load_group(3, nxt, cb ^ 1);  // T
+      {
+        // dA = -(X T^T) strictly lower; dKK = dA beta_i Gamma_ij (symmetric tile);
+        // sums of dA * Gamma o KK^T and of dA * A
+        float a[2][4], ba[2][4], aa[2][4];
+        tmem_ld_frag<2>(tq_base + 64 + 16 * cq, a);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e2 = 0; e2 < 2; ++e2) {
+            const int i = row0 + gq + 8 * e2, j = 16 * cq + 8 * nt + 2 * tq;
+            const float2 gv = ld2(sm + S::GK, 64, i, j);
+            const float gi = gam[i], bi = bet[i];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int jj = j + e;
+              const float da = jj < i ? -a[nt][2 * e2 + e] : 0.f;
+              const float gkk = e == 0 ? gv.x : gv.y;
+              ba[nt][2 * e2 + e] = da * gkk;
+              aa[nt][2 * e2 + e] = da * bi * gkk;
+              if (jj < i) {
+                const __nv_bfloat16 kk = __float2bfloat16(da * bi * __expf(gi - gam[jj]));
+                *reinterpret_cast<__nv_bfloat16*>(sm + S::DKKB + pan_off(i, jj, 64)) = kk;
+                *reinterpret_cast<__nv_bfloat16*>(sm + S::DKKB + pan_off(jj, i, 64)) = kk;
+              } else if (jj == i) {
+                *reinterpret_cast<__nv_bfloat16*>(sm + S::DKKB + pan_off(i, i, 64)) = __float2bfloat16(0.f);
+              }
+            }
+          }
+        add_row_sums<2>(ba, racc, R_BA + cq, row0, gq, tq);
+        add_row_sums<2>(aa, racc, R_AAR + cq, row0, gq, tq);
+        add_col_sums<2>(aa, racc, R_AAC + q4, 16 * cq, gq, tq);
+      }
+      publish();
+
+      // =============== round 7: Gm K, dKK K ===============
+      if (tid == 0) {
+        mma_steps(tmem + 128, dsc(S::GMB, 16), false, 0, dsc(S::KS, 8192), true, 0, 4, kId128KM, false);
+        mma_steps(tmem + 384, dsc(S::DKKB, 16), false, 0, dsc(S::KS, 8192), true, 0, 4, kId128KM, true);
+      }
+      round_end();
+      if (failed) goto teardown;
+      if (more) load_group(4, nxt, cb ^ 1);  // K
+      {
+        float a[4][4], b[4][4];
+        tmem_ld_frag<4>(tq_base + 128 + 32 * cq, a);
+        tmem_ld_frag<4>(tq_base + 384 + 32 * cq, b);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            dQ[nt][e] += a[nt][e];
+            dK[nt][e] += b[nt][e];
+          }
+        // one writer per element; lane pairs (tq, tq ^ 1) swap halves so each
+        // lane stores four consecutive columns of one row
+        const bool odd = tq & 1;
+        const int i_own = row0 + gq + (odd ? 8 : 0);
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+          const int c4 = 32 * cq + 8 * nt + 2 * (tq & ~1);
+          const float sq0 = __shfl_xor_sync(0xffffffffu, odd ? dQ[nt][0] : dQ[nt][2], 1);
+          const float sq1 = __shfl_xor_sync(0xffffffffu, odd ? dQ[nt][1] : dQ[nt][3], 1);
+          const float sk0 = __shfl_xor_sync(0xffffffffu, odd ? dK[nt][0] : dK[nt][2], 1);
+          const float sk1 = __shfl_xor_sync(0xffffffffu, odd ? dK[nt][1] : dK[nt][3], 1);
+          const float4 vq = odd ? make_float4(sq0, sq1, dQ[nt][2], dQ[nt][3])
+                                : make_float4(dQ[nt][0], dQ[nt][1], sq0, sq1);
+          const float4 vk = odd ? make_float4(sk0, sk1, dK[nt][2], dK[nt][3])
+                                : make_float4(dK[nt][0], dK[nt][1], sk0, sk1);
+          if (i_own < Lc) {
+            const int64_t off = ((ctok + i_own) * p.HH + (p.G > 1 ? h : hk)) * 128 + c4;
+            *reinterpret_cast<float4*>(p.dq + off) = vq;
+            *reinterpret_cast<float4*>(p.dk + off) = vk;
+          }
         }
       }
     }
-  }
 
-  // ---- dgamma -> dg (reverse cumsum), dbeta (warps 0-1, fixed-order sums) ----
-  __syncthreads();
-  if (warp < 2) {
-    const int i = tid;  // row 0..63
-    auto sum4 = [&](int s0) {
-      return (racc[s0 * 64 + i] + racc[(s0 + 1) * 64 + i]) +
-             (racc[(s0 + 2) * 64 + i] + racc[(s0 + 3) * 64 + i]);
-    };
-    const float rr = sum4(R_PPR), cc = sum4(R_PPC), ar = sum4(R_AAR), ac = sum4(R_AAC);
-    const float oh = sum4(R_OH), tt = sum4(R_TT), kw = sum4(R_KW), bu = sum4(R_BU);
-    const float ba = sum4(R_BA);
-    const float dgam = (rr - cc) + (ar - ac) + oh - tt + beg[i] * kw;
-    const float dbeta = bu + eg[i] * kw + ba;
-    // gamma_L (row 63) collects e^{gL} <H^, dH'> + sum_i t_i
-    float tsum = tt;
+    // ---- dgamma -> dg (reverse cumsum), dbeta (warps 0-1, fixed-order sums) ----
+    __syncthreads();
+    if (warp < 2) {
+      const int i = tid;  // row 0..63
+      auto sum4 = [&](int s0) {
+        return (racc[s0 * 64 + i] + racc[(s0 + 1) * 64 + i]) +
+               (racc[(s0 + 2) * 64 + i] + racc[(s0 + 3) * 64 + i]);
+      };
+      const float rr = sum4(R_PPR), cc = sum4(R_PPC), ar = sum4(R_AAR), ac = sum4(R_AAC);
+      const float oh = sum4(R_OH), tt = sum4(R_TT), kw = sum4(R_KW), bu = sum4(R_BU);
+      const float ba = sum4(R_BA);
+      const float dgam = (rr - cc) + (ar - ac) + oh - tt + beg[i] * kw;
+      const float dbeta = bu + eg[i] * kw + ba;
+      // gamma_L (row 63) collects e^{gL} <H^, dH'> + sum_i t_i
+      float tsum = tt;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) tsum += __shfl_xor_sync(0xffffffffu, tsum, o);
-    __syncwarp();
-    racc[i] = dgam;  // slot 0 row i: read above by this thread only
-    racc[64 + i] = dbeta;
-    if (lane == 0) hd_part[kWarps + warp] = tsum;
-  }
-  __syncthreads();
-  if (warp == 0) {
-    float hd = 0.f;
+      for (int o = 16; o > 0; o >>= 1) tsum += __shfl_xor_sync(0xffffffffu, tsum, o);
+      __syncwarp();
+      racc[i] = dgam;  // slot 0 row i: read above by this thread only
+      racc[64 + i] = dbeta;
+      if (lane == 0) hd_part[kWarps + warp] = tsum;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      float hd = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) hd += hd_part[w];
-    const float extra = eg[63] * hd + hd_part[kWarps] + hd_part[kWarps + 1];
-    const float x1 = racc[2 * lane + 1] + (lane == 31 ? extra : 0.f);
-    const float x0 = racc[2 * lane];
-    float s = x0 + x1;  // pair sum, then suffix scan over lanes
+      for (int w = 0; w < kWarps; ++w) hd += hd_part[w];
+      const float extra = eg[63] * hd + hd_part[kWarps] + hd_part[kWarps + 1];
+      const float x1 = racc[2 * lane + 1] + (lane == 31 ? extra : 0.f);
+      const float x0 = racc[2 * lane];
+      float s = x0 + x1;  // pair sum, then suffix scan over lanes
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_down_sync(0xffffffffu, s, o);
-      if (lane + o < 32) s += y;
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_down_sync(0xffffffffu, s, o);
+        if (lane + o < 32) s += y;
+      }
+      const float dg1 = s - x0, dg0 = s;
+      const int64_t base = (ctok + 2 * lane) * p.Hv + h;
+      if (2 * lane < Lc) {
+        p.dg[base] = dg0;
+        p.dbeta[base] = racc[64 + 2 * lane];
+      }
+      if (2 * lane + 1 < Lc) {
+        p.dg[base + p.Hv] = dg1;
+        p.dbeta[base + p.Hv] = racc[64 + 2 * lane + 1];
+      }
     }
-    const float dg1 = s - x0, dg0 = s;
-    const int64_t base = (ctok + 2 * lane) * p.Hv + h;
-    if (2 * lane < Lc) {
-      p.dg[base] = dg0;
-      p.dbeta[base] = racc[64 + 2 * lane];
-    }
-    if (2 * lane + 1 < Lc) {
-      p.dg[base + p.Hv] = dg1;
-      p.dbeta[base + p.Hv] = racc[64 + 2 * lane + 1];
-    }
+    __syncthreads();
+    t_cur = t_nxt;
+    cur = nxt;
   }
 
 teardown:
+  // after a bounded wait gave up, the next tile's copies may still be in flight
+  if (failed && tid == 0) mbar_wait(&bar_in, in_parity);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -717,11 +780,19 @@ teardown:
 gdn_status launch_bwd_chunk_tc(const BwdTcParams& p, int state_mode, int w_mode, int64_t n_slots,
                                cudaStream_t st) {
   if (n_slots <= 0) return GDN_OK;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return GDN_ERR_CUDA;
+  const int64_t tiles = n_slots * p.Hv;
+  const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);  // persistent: one CTA per SM
+  BwdTcParams q = p;
+  q.n_slots = n_slots;
   auto go = [&](auto kern) -> gdn_status {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BSmem::BYTES) !=
         cudaSuccess)
       return GDN_ERR_CUDA;
-    kern<<<dim3((unsigned)n_slots, (unsigned)p.Hv), kThreads, BSmem::BYTES, st>>>(p);
+    kern<<<grid, kThreads, BSmem::BYTES, st>>>(q);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
   };
   if (state_mode == GDN_QDQ_E4M3 && w_mode == GDN_QDQ_E4M3)

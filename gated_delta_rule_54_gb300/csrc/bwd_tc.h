@@ -34,6 +34,7 @@ struct BwdTcParams {
   float* dg;
   const int32_t* cu_seqlens;
   int64_t T, nt_fixed;
+  int64_t n_slots;         // chunk slots (set by the launcher)
   int Hv, G, N, HH;        // HH: heads of the dq / dk arrays (Hk, or Hv when grouped)
   int bv_log2;             // log2(block_v)
   float scale;
@@ -61,7 +62,8 @@ struct BwdScanTcParams {
 gdn_status launch_bwd_scan_tc(const BwdScanTcParams& p, int w_mode, cudaStream_t st);
 int bwd_scan_tc_device_error(bool reset);
 
-// grid (n_slots, Hv); false on an unsupported mode pair or a launch failure
+// persistent: one CTA per SM walks the (chunk slot, value head) tiles; false on
+// an unsupported mode pair or a launch failure
 gdn_status launch_bwd_chunk_tc(const BwdTcParams& p, int state_mode, int w_mode, int64_t n_slots,
                                cudaStream_t st);
 
