@@ -303,8 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
       tc_fence_after();
       {
         float a[4][4], k[4][4];
-        tmem_ld_frag<4>(tl + kA0 + 128 * b + 32 * cq, a);
-        tmem_ld_frag<4>(tl + kA1 + 32 * cq, k);
+        tmem_ld_frag_pair<4>(tl + kA0 + 128 * b + 32 * cq, a, tl + kA1 + 32 * cq, k);
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
@@ -327,13 +326,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
       bad |= !mbar_wait(&b_c2, ph);
       tc_fence_after();
       {
-        float z[16];
-        tmem_ld16(tl + kA2 + c0, z);
+        float z0[16], z1[16];
+        tmem_ld16_pair(tl + kA2 + c0, z0, tl + kA2 + c0 + 16, z1);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) dh[j] = egL * dh[j] + z[j];
-        tmem_ld16(tl + kA2 + c0 + 16, z);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) dh[16 + j] = egL * dh[16 + j] + z[j];
+        for (int j = 0; j < 16; ++j) {
+          dh[j] = egL * dh[j] + z0[j];
+          dh[16 + j] = egL * dh[16 + j] + z1[j];
+        }
       }
       tc_fence_before();
       if (it + 1 < nch) write_dh(it + 1);

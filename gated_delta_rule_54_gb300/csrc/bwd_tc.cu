@@ -27,7 +27,7 @@
 //   2  P^T dO, dO Delta^T, Delta dH'^T
 //   3  dO H^T, dDelta H^T, dDelta V^T, T^T dDelta
 //   4  dW K^T, T^T dW, Gm^T Q
-//   5  X = T^T dT;   6  X T^T;   7  Gm K, dKK K
+//   5  X = T^T dT;   6  X T^T;   7  Gm K, dKK K, dKK^T K
 // Warp w reads accumulator rows 16 (w % 4) .. +15 (its TMEM lane quadrant) and a
 // quarter of the columns, in the warp-level mma fragment layout.
 #include <cuda.h>
@@ -81,6 +81,7 @@ struct BSmem {
   static constexpr int WC8 = WB + 8192;      // W codes u8 [64][128]     (upper half of W^)
   static constexpr int HC8 = HB + 16384;     // state codes u8 [128][128] (upper half of H^)
   static_assert(BYTES <= 232448, "shared memory budget");
+  static_assert(PB == DB + 16384 && GK == PB + 8192, "the final stores stage 32 KiB from DB");
 };
 
 // a tile: one (chunk slot, value head)
@@ -143,12 +144,39 @@ __device__ __forceinline__ void add_col_sums(const float (&x)[NT][4], float* rac
     }
 }
 
-// two bf16 values at (row, col), (row, col + 1) (col even) of a panel tile
-__device__ __forceinline__ void st2(unsigned char* tile, int rows, int row, int col, float a, float b) {
-  *reinterpret_cast<uint32_t*>(tile + pan_off(row, col, rows)) = pack_bf16(a, b);
+// two bf16 values at a fragment's byte address in a panel tile
+__device__ __forceinline__ void st2o(unsigned char* at, float a, float b) {
+  *reinterpret_cast<uint32_t*>(at) = pack_bf16(a, b);
 }
-__device__ __forceinline__ float2 ld2(const unsigned char* tile, int rows, int row, int col) {
-  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(tile + pan_off(row, col, rows)));
+__device__ __forceinline__ float2 ld2o(const unsigned char* at) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(at));
+}
+
+// Stores a warp's [16 x 32] fp32 fragment tile (warp rows gq, gq + 8 and
+// columns 8 nt + 2 tq, + 1 of its 32) as whole 128-byte row segments: the
+// fragments pass through the warp's 2 KiB of shared memory `stage` (16-byte
+// chunks permuted by the row) and leave four rows per instruction.  dst(r) is
+// warp row r's first float; rows r >= nrows are not written.
+template <typename RowPtr>
+__device__ __forceinline__ void store_rows32(float* stage, const float (&v)[4][4], int gq, int tq,
+                                             int lane, int nrows, RowPtr dst) {
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+    for (int e2 = 0; e2 < 2; ++e2) {
+      const int r = gq + 8 * e2;
+      const int ch = 2 * nt + (tq >> 1);
+      *reinterpret_cast<float2*>(stage + r * 32 + ((ch ^ (r & 7)) << 2) + 2 * (tq & 1)) =
+          make_float2(v[nt][2 * e2], v[nt][2 * e2 + 1]);
+    }
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = 4 * k + (lane >> 3), ch = lane & 7;
+    const float4 x = *reinterpret_cast<const float4*>(stage + r * 32 + ((ch ^ (r & 7)) << 2));
+    if (r < nrows) *reinterpret_cast<float4*>(dst(r) + 4 * ch) = x;
+  }
+  __syncwarp();
 }
 
 // D (+)= A B over nk K steps of 16.  K-major operands: `panel` bytes between
@@ -172,6 +200,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
   __shared__ __align__(8) uint64_t bar_in, bar_mma;
   __shared__ uint32_t tmem_slot;
   __shared__ float scl[9];  // the tile's state scales (one per block_v columns), then sW
+  __shared__ Tile s_next;   // the next tile (decoded by thread 0 during this one)
+  __shared__ long long s_tnext;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q4 = warp & 3, cq = warp >> 2;  // row quadrant (TMEM lanes), column quarter
@@ -192,6 +222,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
   const uint32_t tmem = tmem_slot;
   const uint32_t tq_base = tmem + ((uint32_t)(32 * q4) << 16);  // this warp's lane quadrant
   const uint32_t sb = smem_u32(sm);
+  // byte offsets of this thread's fragment pairs (row row0 + gq, n tile nt) in
+  // 64-row panel tiles, for N = 64 (columns 16 cq ..) and N = 128 (32 cq ..)
+  // accumulators; row + 8 is 1024 bytes further
+  uint32_t fo64[2], fo128[4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) fo64[nt] = pan_off(row0 + gq, 16 * cq + 8 * nt + 2 * tq, 64);
+#pragma unroll
+  for (int nt = 0; nt < 4; ++nt) fo128[nt] = pan_off(row0 + gq, 32 * cq + 8 * nt + 2 * tq, 64);
 
   // bounded wait on a barrier; on a timeout the error flag is set and the
   // copies / products in flight are waited for once more before teardown
@@ -219,24 +257,25 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
   // ---- tiles: (chunk slot, value head), tile = slot * Hv + h, every gridDim.x-th ----
   const int64_t n_tiles = p.n_slots * p.Hv;
   auto decode = [&](int64_t t, Tile& ti) -> bool {
-    const int64_t slot = t / p.Hv;
+    const int t32 = (int)t;  // tiles < 2^31 (the launcher checks)
+    const int slot = t32 / p.Hv;
     int n, c;
     if (p.cu_seqlens) {
       int lo = 0, hi = p.N - 1;
       while (lo < hi) {  // last n with floor(cu[n] / 64) + n <= slot
         const int mid = (lo + hi + 1) >> 1;
-        if ((int64_t)p.cu_seqlens[mid] / kChunk + mid <= slot) lo = mid; else hi = mid - 1;
+        if (p.cu_seqlens[mid] / kChunk + mid <= slot) lo = mid; else hi = mid - 1;
       }
       n = lo;
-      c = (int)(slot - ((int64_t)p.cu_seqlens[n] / kChunk + n));
+      c = slot - (p.cu_seqlens[n] / kChunk + n);
     } else {
-      n = (int)(slot / p.nt_fixed);
-      c = (int)(slot % p.nt_fixed);
+      n = slot / (int)p.nt_fixed;
+      c = slot - n * (int)p.nt_fixed;
     }
     const int64_t tok0 = p.cu_seqlens ? (int64_t)p.cu_seqlens[n] : (int64_t)n * p.T;
     const int L = p.cu_seqlens ? (int)(p.cu_seqlens[n + 1] - tok0) : (int)p.T;
     if (c < 0 || c * kChunk >= L) return false;  // an unused slot
-    ti.h = (int)(t % p.Hv);
+    ti.h = t32 - slot * p.Hv;
     ti.hk = ti.h / p.G;
     ti.Lc = min(L - c * kChunk, kChunk);
     ti.ctok = tok0 + (int64_t)c * kChunk;
@@ -293,17 +332,25 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
     parity ^= 1u;
   };
 
+  // the scales of tile ti into registers of thread 0 (stored at the tile's start)
+  const int nbv = 128 >> p.bv_log2;
+  float nscl[9];
+  auto load_scales = [&](const Tile& ti) {
+    for (int j = 0; j < 8; ++j) nscl[j] = j < nbv ? p.h_scales[ti.sh * nbv + j] : 0.f;
+    nscl[8] = p.w_scales[ti.sh];
+  };
   Tile cur;
   int64_t t_cur = next_tile(blockIdx.x, cur);
-  if (t_cur >= 0)
+  if (t_cur >= 0 && tid == 0) {
     for (int g = 0; g < 5; ++g) load_group(g, cur, 0);
+    load_scales(cur);
+  }
   for (int it = 0; t_cur >= 0; ++it) {
-    Tile nxt;
-    const int64_t t_nxt = next_tile(t_cur + gridDim.x, nxt);
-    const bool more = t_nxt >= 0;
+    Tile nxt{};
+    bool more = false;  // thread 0: there is a next tile (nxt)
     const int cb = it & 1;
     const int h = cur.h, hk = cur.hk, Lc = cur.Lc;
-    const int64_t ctok = cur.ctok, sh = cur.sh;
+    const int64_t ctok = cur.ctok;
     const float* cvs = reinterpret_cast<const float*>(sm + S::CV + cb * kCvecFloats * 4);
     const float* gam = cvs + kCvGam;
     const float* eg = cvs + kCvEg;
@@ -312,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
     const float* beg = cvs + kCvBeg;
     (void)hk;
     for (int i = tid; i < S::kSlots * 64 + kWarps + 2; i += kThreads) racc[i] = 0.f;
-    if (tid < (128 >> p.bv_log2)) scl[tid] = p.h_scales[sh * (128 >> p.bv_log2) + tid];
-    if (tid == 32) scl[8] = p.w_scales[sh];
+    if (tid == 0)
+      for (int j = 0; j < 9; ++j) scl[j] = nscl[j];
 
     wait_all(&bar_in, in_parity);
     in_parity ^= 1u;
@@ -366,13 +413,19 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
     {
       // =============== round 1: S, G, U, WH, K dH' ===============
       if (tid == 0) {
+        mma_steps(tmem + 256, dsc(S::WB, 16), false, 8192, dsc(S::HB, 16384), true, 0, 8, kId128KM, false);
         mma_steps(tmem + 0, dsc(S::QS, 16), false, 8192, dsc(S::KS, 16), false, 8192, 8, kId64, false);
         mma_steps(tmem + 64, dsc(S::KS, 16), false, 8192, dsc(S::KS, 16), false, 8192, 8, kId64, false);
         mma_steps(tmem + 128, dsc(S::TU, 16), false, 0, dsc(S::VS, 8192), true, 0, 4, kId128KM, false);
         mma_steps(tmem + 128, dsc(S::TU + 8192, 16), false, 0, dsc(S::VS, 8192), true, 0, 4, kId128KM,
                   true);
-        mma_steps(tmem + 256, dsc(S::WB, 16), false, 8192, dsc(S::HB, 16384), true, 0, 8, kId128KM, false);
         mma_steps(tmem + 384, dsc(S::KS, 16), false, 8192, dsc(S::DH, 16384), true, 0, 8, kId128KM, false);
+        // the next tile (its latency overlaps the products): decode, scales
+        const int64_t t_nxt = next_tile(t_cur + gridDim.x, nxt);
+        more = t_nxt >= 0;
+        s_next = nxt;
+        s_tnext = t_nxt;
+        if (more) load_scales(nxt);
       }
       round_end();
       if (failed) goto teardown;
@@ -380,8 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
       {
         // P and Gamma o KK^T (N = 64: columns 16 cq ..)
         float s[2][4], g[2][4];
-        tmem_ld_frag<2>(tq_base + 0 + 16 * cq, s);
-        tmem_ld_frag<2>(tq_base + 64 + 16 * cq, g);
+        tmem_ld_frag_pair<2>(tq_base + 0 + 16 * cq, s, tq_base + 64 + 16 * cq, g);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -389,17 +441,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
             const int i = row0 + gq + 8 * e2, j = 16 * cq + 8 * nt + 2 * tq;
             const float gi = gam[i];
             const float x0 = __expf(gi - gam[j]), x1 = __expf(gi - gam[j + 1]);
-            st2(sm + S::PB, 64, i, j, j <= i ? x0 * s[nt][2 * e2] : 0.f,
+            st2o(sm + S::PB + fo64[nt] + 1024 * e2, j <= i ? x0 * s[nt][2 * e2] : 0.f,
                 j + 1 <= i ? x1 * s[nt][2 * e2 + 1] : 0.f);
-            st2(sm + S::GK, 64, i, j, j < i ? x0 * g[nt][2 * e2] : 0.f,
+            st2o(sm + S::GK + fo64[nt] + 1024 * e2, j < i ? x0 * g[nt][2 * e2] : 0.f,
                 j + 1 < i ? x1 * g[nt][2 * e2 + 1] : 0.f);
           }
       }
       {
         // Delta = U - sW sH(n) WH (N = 128: columns 32 cq ..)
         float u[4][4], wh[4][4];
-        tmem_ld_frag<4>(tq_base + 128 + 32 * cq, u);
-        tmem_ld_frag<4>(tq_base + 256 + 32 * cq, wh);
+        tmem_ld_frag_pair<4>(tq_base + 128 + 32 * cq, u, tq_base + 256 + 32 * cq, wh);
         const float sW = scl[8];
         const float* hs = scl;
 #pragma unroll
@@ -409,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             const int i = row0 + gq + 8 * e2;
-            st2(sm + S::DB, 64, i, col, u[nt][2 * e2] - s0 * wh[nt][2 * e2],
+            st2o(sm + S::DB + fo128[nt] + 1024 * e2, u[nt][2 * e2] - s0 * wh[nt][2 * e2],
                 u[nt][2 * e2 + 1] - s1 * wh[nt][2 * e2 + 1]);
           }
         }
@@ -456,15 +507,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
       {
         // dDelta = scale P^T dO + dec K dH'  -> bf16 (dH' is no longer read)
         float a[4][4], b[4][4];
-        tmem_ld_frag<4>(tq_base + 0 + 32 * cq, a);
-        tmem_ld_frag<4>(tq_base + 384 + 32 * cq, b);
+        tmem_ld_frag_pair<4>(tq_base + 0 + 32 * cq, a, tq_base + 384 + 32 * cq, b);
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             const int i = row0 + gq + 8 * e2, col = 32 * cq + 8 * nt + 2 * tq;
             const float di = dec[i];
-            st2(sm + S::DDB, 64, i, col, p.scale * a[nt][2 * e2] + di * b[nt][2 * e2],
+            st2o(sm + S::DDB + fo128[nt] + 1024 * e2, p.scale * a[nt][2 * e2] + di * b[nt][2 * e2],
                 p.scale * a[nt][2 * e2 + 1] + di * b[nt][2 * e2 + 1]);
           }
       }
@@ -477,11 +527,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             const int i = row0 + gq + 8 * e2, j = 16 * cq + 8 * nt + 2 * tq;
-            const float2 pv = ld2(sm + S::PB, 64, i, j);
+            const float2 pv = ld2o(sm + S::PB + fo64[nt] + 1024 * e2);
             const float gi = gam[i];
             const float d0 = j <= i ? p.scale * x[nt][2 * e2] : 0.f;
             const float d1 = j + 1 <= i ? p.scale * x[nt][2 * e2 + 1] : 0.f;
-            st2(sm + S::GMB, 64, i, j, j <= i ? d0 * __expf(gi - gam[j]) : 0.f,
+            st2o(sm + S::GMB + fo64[nt] + 1024 * e2, j <= i ? d0 * __expf(gi - gam[j]) : 0.f,
                 j + 1 <= i ? d1 * __expf(gi - gam[j + 1]) : 0.f);
             pp[nt][2 * e2] = d0 * pv.x;
             pp[nt][2 * e2 + 1] = d1 * pv.y;
@@ -498,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             const int i = row0 + gq + 8 * e2, d = 32 * cq + 8 * nt + 2 * tq;
-            const float2 kv = ld2(sm + S::KS, 64, i, d);
+            const float2 kv = ld2o(sm + S::KS + fo128[nt] + 1024 * e2);
             const float di = dec[i];
             dK[nt][2 * e2] = di * a[nt][2 * e2];
             dK[nt][2 * e2 + 1] = di * a[nt][2 * e2 + 1];
@@ -529,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             const int i = row0 + gq + 8 * e2, d = 32 * cq + 8 * nt + 2 * tq;
-            const float2 qv = ld2(sm + S::QS, 64, i, d);
+            const float2 qv = ld2o(sm + S::QS + fo128[nt] + 1024 * e2);
             const float si = p.scale * eg[i];
             dQ[nt][2 * e2] = si * a[nt][2 * e2];
             dQ[nt][2 * e2 + 1] = si * a[nt][2 * e2 + 1];
@@ -547,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             const int i = row0 + gq + 8 * e2, d = 32 * cq + 8 * nt + 2 * tq;
-            st2(sm + S::DWB, 64, i, d, -a[nt][2 * e2], -a[nt][2 * e2 + 1]);
+            st2o(sm + S::DWB + fo128[nt] + 1024 * e2, -a[nt][2 * e2], -a[nt][2 * e2 + 1]);
           }
       }
       {
@@ -559,14 +609,19 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             const int j = row0 + gq + 8 * e2, col = 32 * cq + 8 * nt + 2 * tq;
-            const float2 vv = ld2(sm + S::VS, 64, j, col);
+            const float2 vv = ld2o(sm + S::VS + fo128[nt] + 1024 * e2);
             bv[nt][2 * e2] = a[nt][2 * e2] * vv.x;
             bv[nt][2 * e2 + 1] = a[nt][2 * e2 + 1] * vv.y;
-            if (j < Lc)
-              *reinterpret_cast<float2*>(p.dv + ((ctok + j) * p.Hv + h) * 128 + col) =
-                  make_float2(bet[j] * a[nt][2 * e2], bet[j] * a[nt][2 * e2 + 1]);
+            a[nt][2 * e2] *= bet[j];
+            a[nt][2 * e2 + 1] *= bet[j];
           }
         add_row_sums<4>(bv, racc, R_BU + cq, row0, gq, tq);
+        // staging: Delta's tile and the dead half of dH' (8 warps each)
+        float* stage = reinterpret_cast<float*>(
+            sm + (warp < 8 ? S::DB + 2048 * warp : S::DH + 16384 + 2048 * (warp - 8)));
+        store_rows32(stage, a, gq, tq, lane, Lc - row0, [&](int r) {
+          return p.dv + ((ctok + row0 + r) * p.Hv + h) * 128 + 32 * cq;
+        });
       }
       publish();
 
@@ -583,14 +638,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
       {
         // dT = (dDelta V^T) diag(beta) + (dW K^T) diag(beta e^g) -> bf16
         float a[2][4], b[2][4];
-        tmem_ld_frag<2>(tq_base + 256 + 16 * cq, a);
-        tmem_ld_frag<2>(tq_base + 0 + 16 * cq, b);
+        tmem_ld_frag_pair<2>(tq_base + 256 + 16 * cq, a, tq_base + 0 + 16 * cq, b);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             const int i = row0 + gq + 8 * e2, j = 16 * cq + 8 * nt + 2 * tq;
-            st2(sm + S::DTB, 64, i, j, a[nt][2 * e2] * bet[j] + b[nt][2 * e2] * beg[j],
+            st2o(sm + S::DTB + fo64[nt] + 1024 * e2, a[nt][2 * e2] * bet[j] + b[nt][2 * e2] * beg[j],
                 a[nt][2 * e2 + 1] * bet[j + 1] + b[nt][2 * e2 + 1] * beg[j + 1]);
           }
       }
@@ -603,7 +657,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             const int i = row0 + gq + 8 * e2, d = 32 * cq + 8 * nt + 2 * tq;
-            const float2 kv = ld2(sm + S::KS, 64, i, d);
+            const float2 kv = ld2o(sm + S::KS + fo128[nt] + 1024 * e2);
             dK[nt][2 * e2] += beg[i] * a[nt][2 * e2];
             dK[nt][2 * e2 + 1] += beg[i] * a[nt][2 * e2 + 1];
             kw[nt][2 * e2] = a[nt][2 * e2] * kv.x;
@@ -626,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             const int i = row0 + gq + 8 * e2, j = 16 * cq + 8 * nt + 2 * tq;
-            st2(sm + S::XB, 64, i, j, a[nt][2 * e2], a[nt][2 * e2 + 1]);
+            st2o(sm + S::XB + fo64[nt] + 1024 * e2, a[nt][2 * e2], a[nt][2 * e2 + 1]);
           }
       }
       publish();
@@ -638,8 +692,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
       if (failed) goto teardown;
       if (more) load_group(3, nxt, cb ^ 1);  // T
       {
-        // dA = -(X T^T) strictly lower; dKK = dA beta_i Gamma_ij (symmetric tile);
-        // sums of dA * Gamma o KK^T and of dA * A
+        // dA = -(X T^T) strictly lower; dKK = dA beta_i Gamma_ij (strictly lower;
+        // round 7 reads it and its transpose); sums of dA * Gamma o KK^T and of dA * A
         float a[2][4], ba[2][4], aa[2][4];
         tmem_ld_frag<2>(tq_base + 64 + 16 * cq, a);
 #pragma unroll
@@ -647,8 +701,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
             const int i = row0 + gq + 8 * e2, j = 16 * cq + 8 * nt + 2 * tq;
-            const float2 gv = ld2(sm + S::GK, 64, i, j);
+            const float2 gv = ld2o(sm + S::GK + fo64[nt] + 1024 * e2);
             const float gi = gam[i], bi = bet[i];
+            float kk[2];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
               const int jj = j + e;
@@ -656,14 +711,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
               const float gkk = e == 0 ? gv.x : gv.y;
               ba[nt][2 * e2 + e] = da * gkk;
               aa[nt][2 * e2 + e] = da * bi * gkk;
-              if (jj < i) {
-                const __nv_bfloat16 kk = __float2bfloat16(da * bi * __expf(gi - gam[jj]));
-                *reinterpret_cast<__nv_bfloat16*>(sm + S::DKKB + pan_off(i, jj, 64)) = kk;
-                *reinterpret_cast<__nv_bfloat16*>(sm + S::DKKB + pan_off(jj, i, 64)) = kk;
-              } else if (jj == i) {
-                *reinterpret_cast<__nv_bfloat16*>(sm + S::DKKB + pan_off(i, i, 64)) = __float2bfloat16(0.f);
-              }
+              kk[e] = jj < i ? da * bi * __expf(gi - gam[jj]) : 0.f;
             }
+            st2o(sm + S::DKKB + fo64[nt] + 1024 * e2, kk[0], kk[1]);
           }
         add_row_sums<2>(ba, racc, R_BA + cq, row0, gq, tq);
         add_row_sums<2>(aa, racc, R_AAR + cq, row0, gq, tq);
@@ -671,18 +721,18 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
       }
       publish();
 
-      // =============== round 7: Gm K, dKK K ===============
+      // =============== round 7: Gm K, (dKK + dKK^T) K ===============
       if (tid == 0) {
         mma_steps(tmem + 128, dsc(S::GMB, 16), false, 0, dsc(S::KS, 8192), true, 0, 4, kId128KM, false);
         mma_steps(tmem + 384, dsc(S::DKKB, 16), false, 0, dsc(S::KS, 8192), true, 0, 4, kId128KM, true);
+        mma_steps(tmem + 384, dsc(S::DKKB, 8192), true, 0, dsc(S::KS, 8192), true, 0, 4, kId128MM, true);
       }
       round_end();
       if (failed) goto teardown;
       if (more) load_group(4, nxt, cb ^ 1);  // K
       {
         float a[4][4], b[4][4];
-        tmem_ld_frag<4>(tq_base + 128 + 32 * cq, a);
-        tmem_ld_frag<4>(tq_base + 384 + 32 * cq, b);
+        tmem_ld_frag_pair<4>(tq_base + 128 + 32 * cq, a, tq_base + 384 + 32 * cq, b);
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
@@ -690,27 +740,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
             dQ[nt][e] += a[nt][e];
             dK[nt][e] += b[nt][e];
           }
-        // one writer per element; lane pairs (tq, tq ^ 1) swap halves so each
-        // lane stores four consecutive columns of one row
-        const bool odd = tq & 1;
-        const int i_own = row0 + gq + (odd ? 8 : 0);
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-          const int c4 = 32 * cq + 8 * nt + 2 * (tq & ~1);
-          const float sq0 = __shfl_xor_sync(0xffffffffu, odd ? dQ[nt][0] : dQ[nt][2], 1);
-          const float sq1 = __shfl_xor_sync(0xffffffffu, odd ? dQ[nt][1] : dQ[nt][3], 1);
-          const float sk0 = __shfl_xor_sync(0xffffffffu, odd ? dK[nt][0] : dK[nt][2], 1);
-          const float sk1 = __shfl_xor_sync(0xffffffffu, odd ? dK[nt][1] : dK[nt][3], 1);
-          const float4 vq = odd ? make_float4(sq0, sq1, dQ[nt][2], dQ[nt][3])
-                                : make_float4(dQ[nt][0], dQ[nt][1], sq0, sq1);
-          const float4 vk = odd ? make_float4(sk0, sk1, dK[nt][2], dK[nt][3])
-                                : make_float4(dK[nt][0], dK[nt][1], sk0, sk1);
-          if (i_own < Lc) {
-            const int64_t off = ((ctok + i_own) * p.HH + (p.G > 1 ? h : hk)) * 128 + c4;
-            *reinterpret_cast<float4*>(p.dq + off) = vq;
-            *reinterpret_cast<float4*>(p.dk + off) = vk;
-          }
-        }
+        // whole rows through the warp's staging area (Delta / X / dKK, Gm and
+        // Gamma o KK^T tiles, all dead now): dq, then dk
+        float* stage = reinterpret_cast<float*>(sm + S::DB + 2048 * warp);
+        const int head = p.G > 1 ? h : hk;
+        store_rows32(stage, dQ, gq, tq, lane, Lc - row0, [&](int r) {
+          return p.dq + ((ctok + row0 + r) * p.HH + head) * 128 + 32 * cq;
+        });
+        store_rows32(stage, dK, gq, tq, lane, Lc - row0, [&](int r) {
+          return p.dk + ((ctok + row0 + r) * p.HH + head) * 128 + 32 * cq;
+        });
       }
     }
 
@@ -762,8 +801,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
       }
     }
     __syncthreads();
-    t_cur = t_nxt;
-    cur = nxt;
+    t_cur = s_tnext;
+    cur = s_next;
   }
 
 teardown:
@@ -785,6 +824,7 @@ gdn_status launch_bwd_chunk_tc(const BwdTcParams& p, int state_mode, int w_mode,
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return GDN_ERR_CUDA;
   const int64_t tiles = n_slots * p.Hv;
+  if (tiles >= ((int64_t)1 << 31)) return GDN_ERR_UNSUPPORTED_SHAPE;  // 32-bit tile indices
   const unsigned grid = (unsigned)(tiles < sms ? tiles : sms);  // persistent: one CTA per SM
   BwdTcParams q = p;
   q.n_slots = n_slots;

@@ -395,8 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
       const int Lc = min(L - c * kChunk, kChunk);
       const float* cv = CVb(c & 1);
       float qh[16], pd[16];
-      tmem_ld16(tl + kD1 + 64 * (c & 1), qh);
-      tmem_ld16(tl + kD5 + 64 * (c & 1), pd);
+      tmem_ld16_pair(tl + kD1 + 64 * (c & 1), qh, tl + kD5 + 64 * (c & 1), pd);
       if (t_row < Lc) {
         const float ei = cv[kCvEg + t_row] * sH;
         float* dst = p.o + ((tok0 + (int64_t)c * kChunk + t_row) * p.Hv + h) * 128 + vb * 64 + col0;
