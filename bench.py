@@ -304,8 +304,10 @@ def _traffic(profile_md, source_files, workload_key):
 
 
 FWD_SOURCES = ["gated_delta_rule_54_gb300/csrc/fwd.cu", "gated_delta_rule_54_gb300/csrc/fwd_fused.cu",
-               "gated_delta_rule_54_gb300/csrc/common.cuh"]
-BWD_SOURCES = ["gated_delta_rule_54_gb300/csrc/bwd.cu", "gated_delta_rule_54_gb300/csrc/common.cuh"]
+               "gated_delta_rule_54_gb300/csrc/common.cuh", "gated_delta_rule_54_gb300/csrc/tc.cuh"]
+BWD_SOURCES = ["gated_delta_rule_54_gb300/csrc/bwd.cu", "gated_delta_rule_54_gb300/csrc/bwd_tc.cu",
+               "gated_delta_rule_54_gb300/csrc/bwd_scan_tc.cu", "gated_delta_rule_54_gb300/csrc/common.cuh",
+               "gated_delta_rule_54_gb300/csrc/tc.cuh"]
 
 
 def fwd_alg_bytes(w, save_ctx):

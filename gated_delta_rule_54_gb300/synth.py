@@ -57,6 +57,10 @@ WORKLOADS = {
                        Hv=32, Dk=128, Dv=128, varlen_total=32768),
     "fwd_bwd": Workload("fwd+bwd B8 T4096 H16 D128 e4m3", B=8, T=4096, Hk=16, Hv=16,
                         Dk=128, Dv=128, h0=True, backward=True),
+    # one sequence of the single layer: the small case the detailed counter
+    # captures run on (inputs and gradients still larger than L2)
+    "layer_b1": Workload("single layer B1 T4096 H16 D128 e4m3", B=1, T=4096, Hk=16, Hv=16,
+                         Dk=128, Dv=128, h0=True, seed=5),
     # decode QAT: one token per sequence for 256 sequences whose carried states
     # (256 x 16 x 128 x 128 fp32 = 256 MiB) exceed L2
     "decode": Workload("decode step B256 T1 H16 D128 e4m3-state", B=256, T=1, Hk=16, Hv=16,
