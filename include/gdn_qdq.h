@@ -137,10 +137,12 @@ int64_t gdn_num_chunk_slots(const gdn_problem* p);
  *                                       beta e^gamma (rows past the chunk end:
  *                                       gamma flat, beta 0)
  *   t_img     bf16 [n_slots, Hv, 4096]  T = (I + A)^-1 (lower incl. diagonal)   (save_ctx)
- *   gkk_img   bf16 [n_slots, Hv, 4096]  Gamma o KK^T (strictly lower)           (save_ctx)
+ *   gkk_img   bf16 [n_slots, Hv, 4096]  Gamma o KK^T (strictly lower)           (save_ctx, not fused)
  *   p_img     bf16 [n_slots, Hv, 4096]  P = Gamma o QK^T (lower incl. diagonal) (save_ctx)
  *   d_img     bf16 [n_slots, Hv, Dv/64, 4096]  Delta = U - W^ H^ of each
- *                                       64-column value block                  (save_ctx)
+ *                                       64-column value block        (save_ctx, not fused)
+ *             ("fused": Dk = Dv = 128, both sites quantized, block_v 64, exact
+ *             solve; that backward recomputes Gamma o KK^T and Delta)
  *             each 64 x 64 tile stored as its shared-memory image: element
  *             (i, j) at i * 64 + 8 * ((j / 8) ^ (i % 8)) + j % 8; rows past
  *             the chunk end are zero (T: identity rows)
