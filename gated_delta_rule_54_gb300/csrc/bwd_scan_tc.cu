@@ -72,12 +72,6 @@ __device__ __forceinline__ bool epi_sync_or(bool v) {
 __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync 1, %0;\n" ::"n"(kEpiThreads) : "memory");
 }
-// shared -> global bulk copy (both 16-byte aligned, bytes a multiple of 16)
-__device__ __forceinline__ void bulk_store_1d(void* dst, const void* src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst),
-               "r"(smem_u32(src)), "r"(bytes)
-               : "memory");
-}
 
 template <int WM>
 __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __grid_constant__ BwdScanTcParams p) {
@@ -240,10 +234,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
       }
     }
     // dH (bf16) -> its shared-memory image; one thread then copies the image to
-    // the workspace slot of iteration it (the dH' entering that chunk)
+    // the workspace slot of iteration it (the dH' entering that chunk).  The
+    // previous copy has read the image: its wait sits in the loop, off the chain.
     auto write_dh = [&](int it) {
-      if (tid == 0) tma_store_wait_read();  // the previous copy has read the image
-      epi_sync();
       unsigned char* panel = sm + S::DH + (c0 >> 6) * 16384;
 #pragma unroll
       for (int k = 0; k < 4; ++k) st8_bf16(panel, drow, ((c0 & 63) >> 3) + k, dh + 8 * k);
@@ -321,6 +314,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
       // (read before signalling: the producer refills this chunk's buffers then)
       const float egL = cv[kCvEg + 63];  // gamma is flat past the last row
       if (lane == 0) mbar_arrive(&e_dd);
+      // while C2 runs: the last bulk copy of the dH image has been read, so the
+      // next write_dh may overwrite it
+      if (tid == 0) tma_store_wait_read();
+      epi_sync();
 
       // ---- dH <- e^{gamma_L} dH + C2 ----
       bad |= !mbar_wait(&b_c2, ph);

@@ -362,6 +362,13 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, int x, int y, con
                "r"(x), "r"(y), "r"(smem_u32(src))
                : "memory");
 }
+// shared -> global bulk copy (bulk async-group completion; both addresses
+// 16-byte aligned, bytes a multiple of 16)
+__device__ __forceinline__ void bulk_store_1d(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n" ::"l"(dst),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void tma_store_commit() {
   asm volatile("cp.async.bulk.commit_group;\n" ::: "memory");
 }

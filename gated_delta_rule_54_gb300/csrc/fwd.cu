@@ -44,6 +44,7 @@
 #include "common.cuh"
 #include "fused.h"
 #include "launch.h"
+#include "tc.cuh"
 
 namespace gdn {
 
@@ -260,6 +261,11 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
   unsigned char* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
   __shared__ float red[kPrepWarps];
   __shared__ __align__(8) uint64_t bar;
+  // the fused path's variant runs K K^T and W = Tw K on tcgen05 (accumulators
+  // in 128 TMEM columns, three CTAs per SM share the 512)
+  __shared__ __align__(8) uint64_t bar_mma;
+  __shared__ uint32_t tmem_slot;
+  __shared__ int tc_failed;
 
   const int64_t slot = blockIdx.x / p.Hv;
   const int h = blockIdx.x % p.Hv;
@@ -306,6 +312,15 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
                tok0, L, p.Hv, h, t);
   }
   cp_async_commit();
+  if constexpr (TOUT) {
+    if (warp == 0) tmem_alloc(&tmem_slot, 128);
+    if (threadIdx.x == 0) {
+      mbar_init(&bar_mma, 1);
+      tc_failed = 0;
+      fence_mbar_init();
+    }
+    tc_fence_before();
+  }
   __syncthreads();  // the mbarrier is initialised before anyone waits on it
   {
     const bool ok = mbar_wait(&bar, 0);
@@ -314,6 +329,10 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
       if (threadIdx.x == 0) {
         atomicOr(&g_fwd_device_error, 1);
         mbar_wait(&bar, 0);  // once more, bounded, for the copies in flight
+      }
+      if constexpr (TOUT) {
+        tc_fence_after();
+        if (warp == 0) tmem_dealloc(tmem_slot, 128);
       }
       return;
     }
@@ -350,7 +369,26 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
   const bool a_tile = col0 <= row0 + 15;
   float acc[4][4];
   zero_acc(acc);
-  if (a_tile) wgemm<4, false, false, DK, DK>(acc, Ks, row0, Ks, col0, 0, DK, lane);
+  uint32_t tmem = 0;
+  if constexpr (TOUT) {
+    // K K^T: M = 64, N = 64, K = DK (K-major panels), one commit
+    tc_fence_after();
+    tmem = tmem_slot;
+    if (threadIdx.x == 0) {
+      const uint64_t kd = sdesc(smem_u32(Ks), 16, 1024);
+      constexpr uint32_t id = idesc(64, 64, 0, 0);
+#pragma unroll
+      for (int ks = 0; ks < DK / 16; ++ks)
+        umma(tmem, dadd(kd, (ks >> 2) * 8192 + (ks & 3) * 32), dadd(kd, (ks >> 2) * 8192 + (ks & 3) * 32),
+             id, ks > 0);
+      umma_commit(&bar_mma);
+    }
+    if (!mbar_wait(&bar_mma, 0)) tc_failed = 1;
+    tc_fence_after();
+    tmem_ld_frag<4>(tmem + ((uint32_t)(32 * rt) << 16) + col0, acc);
+  } else {
+    if (a_tile) wgemm<4, false, false, DK, DK>(acc, Ks, row0, Ks, col0, 0, DK, lane);
+  }
   __syncthreads();
   {
     // Gamma o KK^T (strictly lower; rows >= L hold another sequence's keys: zero)
@@ -415,7 +453,31 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
   const int wc0 = ch * (DK / 2);
   float wacc[NTW][4];
   zero_acc(wacc);
-  wgemm_shared_b<NTW, false, true, 64, DK>(wacc, wacc, TwH, TwL, row0, Ks, wc0, 0, 64, lane);
+  if constexpr (TOUT) {
+    // W = Tw_hi K + Tw_lo K: M = 64, N = DK, K = 64 (K read MN-major)
+    static_assert(!TOUT || DK == 128, "the tensor-core prep is for Dk = 128");
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (threadIdx.x == 0) {
+      const uint64_t kd = sdesc(smem_u32(Ks), 8192, 1024);
+      const uint64_t th = sdesc(smem_u32(TwH), 16, 1024), tl = sdesc(smem_u32(TwL), 16, 1024);
+      constexpr uint32_t id = idesc(64, DK, 0, 1);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) umma(tmem, dadd(th, ks * 32), dadd(kd, ks * 2048), id, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) umma(tmem, dadd(tl, ks * 32), dadd(kd, ks * 2048), id, true);
+      umma_commit(&bar_mma);
+    }
+    if (!mbar_wait(&bar_mma, 1)) tc_failed = 1;
+    tc_fence_after();
+    const uint32_t tw = tmem + ((uint32_t)(32 * rt) << 16) + wc0;
+    tmem_ld_frag_pair<4>(tw, *reinterpret_cast<float(*)[4][4]>(&wacc[0][0]), tw + 32,
+                         *reinterpret_cast<float(*)[4][4]>(&wacc[4][0]));
+  } else {
+    wgemm_shared_b<NTW, false, true, 64, DK>(wacc, wacc, TwH, TwL, row0, Ks, wc0, 0, 64, lane);
+  }
 
   // ---- a5: W QDQ over the whole [L, DK] tile ----
   if constexpr (WM != GDN_QDQ_NONE) {
@@ -519,6 +581,17 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
     }
   }
   if (threadIdx.x == 0) tma_store_wait_all();
+  if constexpr (TOUT) {
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && tc_failed) {
+      atomicOr(&g_fwd_device_error, 1);
+      mbar_wait(&bar_mma, 1);  // once more, bounded, for the products in flight
+    }
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, 128);
+  }
 }
 
 // ===========================================================================

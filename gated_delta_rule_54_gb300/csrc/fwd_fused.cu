@@ -290,6 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
         for (int ks = 0; ks < 8; ++ks)
           umma(tmem + kD4, dadd(aq, (ks >> 2) * 16384 + (ks & 3) * 32),
                dadd(ktk, (ks >> 2) * 8192 + (ks & 3) * 32), kIdKK, ks > 0);
+        // the last bulk copy of a P image has read its tile before the P epilogue
+        // (which waits for D4) rewrites it
+        tma_store_wait_read();
         umma_commit(&b_d4);
         // K of the next chunk: H^(c) being ready means the state update of chunk
         // c - 1 ran, so D2(c - 1), the last reader of that K buffer, is done
@@ -321,6 +324,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
         bad |= !mbar_wait(&e_p, ph);
         if (bad) break;
         tc_fence_after();
+        // a full chunk's P image is its bf16 tile P_hi byte for byte: one bulk copy
+        if (p.pb && vb == 0 && L - c * kChunk >= kChunk) {
+          bulk_store_1d(static_cast<unsigned char*>(p.pb) + sh_of(c) * 8192, AP + 8192, 8192);
+          tma_store_commit();
+        }
         const uint32_t d5 = tmem + kD5 + 64 * (c & 1);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
@@ -483,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
             *reinterpret_cast<const uint4*>(AP + sw_off(t_row, col0));
         *reinterpret_cast<uint4*>(AP + 16384 + sw_off(t_row, col0 + 8)) =
             *reinterpret_cast<const uint4*>(AP + sw_off(t_row, col0 + 8));
-        if (p.pb && vb == 0) {
+        if (p.pb && vb == 0 && Lc < kChunk) {  // a partial chunk: rows past its end zero
           unsigned char* pimg = reinterpret_cast<unsigned char*>(p.pb) + (slot * p.Hv + h) * 8192;
           float z[16];
 #pragma unroll
@@ -578,6 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
     }
     umma_commit(&b_end);  // completes once every product issued so far is done
     mbar_wait(&b_end, 0);
+    tma_store_wait_all();  // the P images' bulk copies
   }
   tc_fence_before();
   __syncthreads();
