@@ -11,8 +11,10 @@
 // nothing).  No solve is needed: only P, K, Q, dO and the codes.
 //
 // One CTA per (sequence, value head) covers both 64-column value blocks (N =
-// 128) and walks the chunks in reverse; the fp32 dH lives in registers (thread
-// r of each warp quadrant holds row 32 (w % 4) + lane, 32 columns).  A producer
+// 128), or, when twice as many CTAs still fit on the SMs at once, one per
+// value block (the blocks' chains are independent); it walks the chunks in
+// reverse with the fp32 dH in registers (thread r of each warp quadrant holds
+// row 32 (w % 4) + lane, a quarter of the columns).  A producer
 // warp issues the TMA copies and the tcgen05 products; per chunk only two
 // products lie on the dependency chain:
 //   C1 = K dH                               (M = 64 tokens, N = 128, K = 128)
@@ -39,9 +41,6 @@ __device__ int g_scantc_device_error;
 constexpr int kEpiThreads = 512;
 constexpr int kEpiWarps = kEpiThreads / 32;
 constexpr int kThreads = kEpiThreads + 32;  // + the producer warp
-constexpr uint32_t kTmemCols = 512;
-// TMEM columns: P^T dO (two buffers), K dH, and the state-gradient product
-constexpr uint32_t kA0 = 0, kA1 = 256, kA2 = 384;
 
 struct SSmem {
   static constexpr int KT = 0;                  // 2 x K [64 tok][128 d]
@@ -57,7 +56,9 @@ struct SSmem {
   static constexpr int BYTES = CV + 2 * kCvecFloats * 4 + 1024;
   static_assert(BYTES <= 232448, "shared memory budget");
 };
-constexpr uint32_t kInTx = 3 * 16384 + 8192 + 8192 + kCvecFloats * 4;
+// copies of one chunk: K, Q, dO of the CTA's value blocks, P image, W codes, vectors
+template <int NB>
+__host__ __device__ constexpr uint32_t in_tx() { return 2 * 16384 + NB * 8192 + 8192 + 8192 + kCvecFloats * 4; }
 
 __device__ __forceinline__ bool epi_sync_or(bool v) {
   uint32_t r;
@@ -73,16 +74,24 @@ __device__ __forceinline__ void epi_sync() {
   asm volatile("bar.sync 1, %0;\n" ::"n"(kEpiThreads) : "memory");
 }
 
-template <int WM>
+// NB: 64-column value blocks per CTA (2: one CTA per (sequence, head); 1: two,
+// when that many CTAs still fit on the SMs at once)
+template <int WM, int NB>
 __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __grid_constant__ BwdScanTcParams p) {
   using S = SSmem;
+  constexpr int NW = 64 * NB;           // value columns of this CTA
+  constexpr int CW = NW / 4;            // dH columns per epilogue thread
+  constexpr uint32_t kTmemCols = 4 * NW;
+  // TMEM columns: P^T dO (two buffers), K dH, and the state-gradient product
+  constexpr uint32_t kA0 = 0, kA1 = 2 * NW, kA2 = 3 * NW;
   extern __shared__ __align__(1024) unsigned char sm_raw[];
   unsigned char* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
   __shared__ __align__(8) uint64_t in_full[2], dh_ready, conv_done, b_c1, e_dd, b_c2, b_end;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
-  const int h = blockIdx.x, n = blockIdx.y;
+  const int h = blockIdx.x / (2 / NB), n = blockIdx.y;
+  const int vb0 = NB == 1 ? (blockIdx.x & 1) * 64 : 0;  // first value column
   const int hk = h / p.G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const bool producer = warp == kEpiWarps;
@@ -135,28 +144,30 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
       auto load = [&](int it) {
         const int b = it & 1;
         const int y = (int)(tok0 + (int64_t)chunk_of(it) * kChunk);
-        mbar_expect_tx(&in_full[b], kInTx);
+        mbar_expect_tx(&in_full[b], in_tx<NB>());
 #pragma unroll
         for (int pn = 0; pn < 2; ++pn) {
           tma_load_2d(KTb(b) + pn * 8192, &p.tm_k, hk * 128 + pn * 64, y, &in_full[b]);
           tma_load_2d(QTb(b) + pn * 8192, &p.tm_q, hk * 128 + pn * 64, y, &in_full[b]);
-          tma_load_2d(DTb(b) + pn * 8192, &p.tm_do, h * 128 + pn * 64, y, &in_full[b]);
         }
+#pragma unroll
+        for (int pn = 0; pn < NB; ++pn)
+          tma_load_2d(DTb(b) + pn * 8192, &p.tm_do, h * 128 + vb0 + pn * 64, y, &in_full[b]);
         bulk_load_1d(PTb(b), static_cast<const unsigned char*>(p.pb) + sh_of(it) * 8192, 8192,
                      &in_full[b]);
         tma_load_2d(WCb(b), &p.tm_wc, h * 128, y, &in_full[b]);
         bulk_load_1d(sm + S::CV + b * kCvecFloats * 4, p.cvec + sh_of(it) * kCvecFloats,
                      kCvecFloats * 4, &in_full[b]);
       };
-      const uint32_t idPd = idesc(64, 128, 1, 1), idKd = idesc(64, 128, 0, 1);
-      const uint32_t idMM = idesc(128, 128, 1, 1);
+      const uint32_t idPd = idesc(64, NW, 1, 1), idKd = idesc(64, NW, 0, 1);
+      const uint32_t idMM = idesc(128, NW, 1, 1);
       // P^T dO of iteration it -> A0[it & 1]
       auto issue_pdo = [&](int it) {
         const int b = it & 1;
         const uint64_t a = sdesc(smem_u32(PTb(b)), 8192, 1024), d = sdesc(smem_u32(DTb(b)), 8192, 1024);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          umma(tmem + kA0 + 128 * b, dadd(a, ks * 2048), dadd(d, ks * 2048), idPd, ks > 0);
+          umma(tmem + kA0 + NW * b, dadd(a, ks * 2048), dadd(d, ks * 2048), idPd, ks > 0);
       };
       load(0);
       if (nch > 1) load(1);
@@ -216,15 +227,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
   } else {
     // ======================= epilogue warps =======================
     const int drow = 32 * q4 + lane;             // dH row (TMEM lane of C2)
-    const int c0 = 32 * cq;                      // this thread's 32 dH columns
+    const int c0 = CW * cq;                      // this thread's CW dH columns
     const uint32_t tl = tmem + ((uint32_t)(32 * q4) << 16);
     const int gq = lane >> 2, tq = lane & 3;
     const int row0 = 16 * q4;                    // rows of the M = 64 products
-    float dh[32];
+    float dh[CW];
     {
-      const float* src = p.dht ? p.dht + (((int64_t)n * p.Hv + h) * 128 + drow) * 128 + c0 : nullptr;
+      const float* src =
+          p.dht ? p.dht + (((int64_t)n * p.Hv + h) * 128 + drow) * 128 + vb0 + c0 : nullptr;
 #pragma unroll
-      for (int j = 0; j < 32; j += 4) {
+      for (int j = 0; j < CW; j += 4) {
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
         if (src) x = *reinterpret_cast<const float4*>(src + j);
         dh[j] = x.x;
@@ -239,14 +251,15 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
     auto write_dh = [&](int it) {
       unsigned char* panel = sm + S::DH + (c0 >> 6) * 16384;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) st8_bf16(panel, drow, ((c0 & 63) >> 3) + k, dh + 8 * k);
+      for (int k = 0; k < CW / 8; ++k) st8_bf16(panel, drow, ((c0 & 63) >> 3) + k, dh + 8 * k);
       fence_proxy_async();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&dh_ready);  // C1 may read the image
       epi_sync();
       if (tid == 0) {
-        bulk_store_1d(static_cast<unsigned char*>(p.ws_dh) + sh_of(it) * 32768, sm + S::DH, 32768);
+        bulk_store_1d(static_cast<unsigned char*>(p.ws_dh) + sh_of(it) * 32768 + (vb0 >> 6) * 16384,
+                      sm + S::DH, NB * 16384);
         tma_store_commit();
       }
     };
@@ -272,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
         *reinterpret_cast<uint4*>(sm + S::WB + pan_off(r, c8 * 8, 64)) =
             make_uint4(pack_bf16(a.x, a.y), pack_bf16(a.z, a.w), pack_bf16(bb.x, bb.y), pack_bf16(bb.z, bb.w));
       }
-      for (int i = tid; i < 2 * 64 * 8; i += kEpiThreads) {
+      for (int i = tid; i < NB * 64 * 8; i += kEpiThreads) {
         const int r = (i >> 3) & 63;  // physical chunk i & 7 of row r in panel i >> 9
         const uint32_t off = (uint32_t)((i >> 9) * 8192 + r * 128 + (i & 7) * 16);
         const float er = r < Lc ? p.scale * cv[kCvEg + r] : 0.f;
@@ -295,13 +308,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
       bad |= !mbar_wait(&b_c1, ph);
       tc_fence_after();
       {
-        float a[4][4], k[4][4];
-        tmem_ld_frag_pair<4>(tl + kA0 + 128 * b + 32 * cq, a, tl + kA1 + 32 * cq, k);
+        constexpr int NT = CW / 8;  // n tiles per thread
+        float a[NT][4], k[NT][4];
+        tmem_ld_frag_pair<NT>(tl + kA0 + NW * b + CW * cq, a, tl + kA1 + CW * cq, k);
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
-            const int i = row0 + gq + 8 * e2, col = 32 * cq + 8 * nt + 2 * tq;
+            const int i = row0 + gq + 8 * e2, col = CW * cq + 8 * nt + 2 * tq;
             const float di = i < Lc ? cv[kCvDec + i] : 0.f;
             const float v0 = -sW * (p.scale * a[nt][2 * e2] + di * k[nt][2 * e2]);
             const float v1 = -sW * (p.scale * a[nt][2 * e2 + 1] + di * k[nt][2 * e2 + 1]);
@@ -323,21 +337,28 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
       bad |= !mbar_wait(&b_c2, ph);
       tc_fence_after();
       {
-        float z0[16], z1[16];
-        tmem_ld16_pair(tl + kA2 + c0, z0, tl + kA2 + c0 + 16, z1);
+        if constexpr (NB == 2) {
+          float z0[16], z1[16];
+          tmem_ld16_pair(tl + kA2 + c0, z0, tl + kA2 + c0 + 16, z1);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          dh[j] = egL * dh[j] + z0[j];
-          dh[16 + j] = egL * dh[16 + j] + z1[j];
+          for (int j = 0; j < 16; ++j) {
+            dh[j] = egL * dh[j] + z0[j];
+            dh[16 + j] = egL * dh[16 + j] + z1[j];
+          }
+        } else {
+          float z0[16];
+          tmem_ld16(tl + kA2 + c0, z0);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) dh[j] = egL * dh[j] + z0[j];
         }
       }
       tc_fence_before();
       if (it + 1 < nch) write_dh(it + 1);
     }
     if (!bad && it == nch && p.dh0) {
-      float* dst = p.dh0 + (((int64_t)n * p.Hv + h) * 128 + drow) * 128 + c0;
+      float* dst = p.dh0 + (((int64_t)n * p.Hv + h) * 128 + drow) * 128 + vb0 + c0;
 #pragma unroll
-      for (int j = 0; j < 32; j += 4)
+      for (int j = 0; j < CW; j += 4)
         *reinterpret_cast<float4*>(dst + j) = make_float4(dh[j], dh[j + 1], dh[j + 2], dh[j + 3]);
     }
     if (tid == 0) tma_store_wait_all();  // the workspace copies are complete
@@ -366,16 +387,27 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
 }  // namespace
 
 gdn_status launch_bwd_scan_tc(const BwdScanTcParams& p, int w_mode, cudaStream_t st) {
-  const dim3 grid((unsigned)p.Hv, (unsigned)p.N);
-  auto run = [&](auto kern) -> gdn_status {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return GDN_ERR_CUDA;
+  // one CTA per value block while the chains still fit on the SMs at once
+  // (each chain is serial: more CTAs on free SMs shorten it), else per head
+  const bool split = (int64_t)p.Hv * p.N * 2 <= sms;
+  auto run = [&](auto kern, unsigned gx) -> gdn_status {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SSmem::BYTES) !=
         cudaSuccess)
       return GDN_ERR_CUDA;
-    kern<<<grid, kThreads, SSmem::BYTES, st>>>(p);
+    kern<<<dim3(gx, (unsigned)p.N), kThreads, SSmem::BYTES, st>>>(p);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
   };
-  if (w_mode == GDN_QDQ_E4M3) return run(gdn_bwd_scan_tc_kernel<GDN_QDQ_E4M3>);
-  if (w_mode == GDN_QDQ_INT8) return run(gdn_bwd_scan_tc_kernel<GDN_QDQ_INT8>);
+  const unsigned hv = (unsigned)p.Hv;
+  if (w_mode == GDN_QDQ_E4M3)
+    return split ? run(gdn_bwd_scan_tc_kernel<GDN_QDQ_E4M3, 1>, 2 * hv)
+                 : run(gdn_bwd_scan_tc_kernel<GDN_QDQ_E4M3, 2>, hv);
+  if (w_mode == GDN_QDQ_INT8)
+    return split ? run(gdn_bwd_scan_tc_kernel<GDN_QDQ_INT8, 1>, 2 * hv)
+                 : run(gdn_bwd_scan_tc_kernel<GDN_QDQ_INT8, 2>, hv);
   return GDN_ERR_UNSUPPORTED_MODE;
 }
 
