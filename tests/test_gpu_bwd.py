@@ -105,6 +105,14 @@ def test_bwd_lengths_tensor_core_path(T):
     _check(w, scale=128 ** -0.5, with_dht=T % 2 == 1)
 
 
+def test_bwd_scan_two_blocks_per_cta():
+    """80 (sequence, head) chains are more than fit twice on the SMs, so the
+    reverse scan covers both value blocks in one CTA (the small cases above
+    take one block per CTA)."""
+    w = synth.small(B=5, T=70, Hk=16, Hv=16, Dk=128, Dv=128, h0=True, seed=61)
+    _check(w)
+
+
 def test_bwd_grouped_heads_int8():
     w = synth.small(B=1, T=150, Hk=2, Hv=6, Dk=128, Dv=128, state_mode="int8", h0=True, seed=22)
     _check(w)
