@@ -25,6 +25,10 @@ so inside a window the outputs follow the ordinary recurrence started from the
 quantized snapshot of the anchor, and the anchor itself is the unquantized
 recurrence.  With the read quantizer disabled R == A and the profile is the
 plain gated delta rule.
+
+``two_precision_torch`` is the same loop in differentiable torch with the read
+quantizer as an identity straight-through estimator: its autograd is the
+backward ("window-wise adjoint") the kernels are checked against.
 """
 from __future__ import annotations
 
@@ -91,3 +95,59 @@ def two_precision(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, read_mo
             o[b, t] = scale * np.einsum("hkv,hk->hv", R, qt)
         ht[n] = A
     return o, ht
+
+
+def two_precision_torch(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0, read_mode="e4m3",
+                        flush=16):
+    """The same profile in differentiable fp64 torch, for the backward: the read
+    copy is Q_read through the identity straight-through estimator (the
+    gradient of R's snapshot reaches the anchor unchanged), everything else is
+    the exact recurrence, so autograd gives the window-wise adjoint the page
+    describes ("[5/8] ReplaySSM state QAT and two-precision GDN", "What does
+    this PR do?": a window-wise adjoint during backward).  Plain Python loops:
+    small cases only.  Inputs as two_precision (torch fp64 tensors); returns
+    (o [B, T, Hv, Dv], ht [N, Hv, Dk, Dv])."""
+    import torch
+
+    from .chunked import qdq_ste
+
+    if flush < 1:
+        raise ValueError("flush period must be >= 1")
+    if read_mode not in ("none", "e4m3"):
+        raise ValueError("the read quantizer is E4M3 or disabled")
+    B, T, Hk, Dk = k.shape
+    Hv, Dv = v.shape[2], v.shape[3]
+    G = Hv // Hk
+    if cu_seqlens is not None:
+        cu = [int(x) for x in _np(cu_seqlens)]
+        seqs = [(0, cu[n], cu[n + 1]) for n in range(len(cu) - 1)]
+    else:
+        seqs = [(b, 0, T) for b in range(B)]
+    N = len(seqs)
+    if h0 is None:
+        h0 = torch.zeros(N, Hv, Dk, Dv, dtype=torch.float64)
+    out = {}
+    hts = []
+    for n, (b, t0, t1) in enumerate(seqs):
+        hn = []
+        for h in range(Hv):
+            hk = h // G
+            A = h0[n, h]
+            R = A
+            for t in range(t0, t1):
+                if (t - t0) % flush == 0:
+                    # one scale per column of H over all Dk key rows
+                    R = qdq_ste(A[None], read_mode, 1)[0]
+                a = torch.exp(g[b, t, h])
+                kt = k[b, t, hk]
+                A = a * A
+                A = A + beta[b, t, h] * torch.outer(kt, v[b, t, h] - A.transpose(0, 1) @ kt)
+                R = a * R
+                R = R + beta[b, t, h] * torch.outer(kt, v[b, t, h] - R.transpose(0, 1) @ kt)
+                out[(b, t, h)] = scale * (R.transpose(0, 1) @ q[b, t, hk])
+            hn.append(A)
+        hts.append(torch.stack(hn, 0))
+    zero = torch.zeros(Dv, dtype=torch.float64)
+    o = torch.stack([torch.stack([torch.stack([out.get((b, t, h), zero) for h in range(Hv)], 0)
+                                  for t in range(T)], 0) for b in range(B)], 0)
+    return o, torch.stack(hts, 0)

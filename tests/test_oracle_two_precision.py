@@ -137,3 +137,108 @@ def test_two_precision_scales_exactly_with_values_and_state(rm):
         o2, ht2 = two_precision(d["q"], d["k"], v2, d["beta"], d["g"], d["h0"] * f, read_mode=rm)
         assert np.array_equal(np.asarray(o2), np.asarray(o) * f)
         assert np.array_equal(np.asarray(ht2), np.asarray(ht) * f)
+
+
+# ---- the differentiable form and its backward (window-wise adjoint) ----
+
+import torch  # noqa: E402
+
+from oracle.chunked import qdq_ste  # noqa: E402
+from oracle.recurrent_torch import recurrent_torch  # noqa: E402
+from oracle.two_precision import two_precision_torch  # noqa: E402
+
+
+def _t64(d, names=("q", "k", "v", "beta", "g", "h0")):
+    return [None if d[n] is None else d[n].to(torch.float32).to(torch.float64) for n in names]
+
+
+@pytest.mark.parametrize("lengths,read_mode", [(None, "e4m3"), (None, "none"), ([1, 16, 37, 5], "e4m3")])
+def test_torch_form_is_the_profile(lengths, read_mode):
+    d = _case(lengths=lengths, seed=5)
+    o1, h1 = two_precision(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"],
+                           cu_seqlens=d["cu_seqlens"], read_mode=read_mode, scale=0.5)
+    o2, h2 = two_precision_torch(*_t64(d), cu_seqlens=d["cu_seqlens"], read_mode=read_mode, scale=0.5)
+    assert np.abs(o1 - o2.numpy()).max() <= 1e-12 * np.abs(o1).max()
+    assert np.abs(h1 - h2.numpy()).max() <= 1e-12 * np.abs(h1).max()
+
+
+def _grads(fn, xs, do, dht):
+    xs = [x.clone().requires_grad_(True) for x in xs]
+    o, ht = fn(*xs)
+    ((o * do).sum() + (ht * dht).sum()).backward()
+    return [torch.zeros_like(x) if x.grad is None else x.grad for x in xs]
+
+
+def _upstream(d, seed):
+    gen = torch.Generator().manual_seed(seed)
+    o_shape = d["v"].shape
+    do = torch.randn(*o_shape, generator=gen, dtype=torch.float64)
+    dht = torch.randn(*d["h0"].shape, generator=gen, dtype=torch.float64) * 0.1
+    return do, dht
+
+
+def test_torch_read_disabled_gradients_are_the_token_recurrence():
+    """With the read quantizer off R == A: the backward is the plain recurrence's."""
+    d = _case(seed=6, T=40)
+    do, dht = _upstream(d, 6)
+    xs = _t64(d)
+    g1 = _grads(lambda *x: two_precision_torch(*x, read_mode="none", scale=0.5, flush=16), xs, do, dht)
+    g2 = _grads(lambda *x: recurrent_torch(*x, scale=0.5, state_mode="none"), xs, do, dht)
+    for a, b in zip(g1, g2):
+        assert torch.abs(a - b).max() <= 1e-12 * torch.abs(b).max()
+
+
+def test_torch_single_window_gradients():
+    """One flush (W >= T): o follows the plain recurrence from Q_read(h0) and ht
+    the plain recurrence from h0, so the backward is the sum of the two plain
+    recurrences' gradients, the first passing its h0 gradient through the
+    identity straight-through estimator."""
+    d = _case(seed=7, T=30)
+    do, dht = _upstream(d, 7)
+    xs = _t64(d)
+    g1 = _grads(lambda *x: two_precision_torch(*x, read_mode="e4m3", scale=0.5, flush=64), xs, do, dht)
+
+    def o_path(q, k, v, beta, g, h0):
+        hq = torch.stack([qdq_ste(h0[:, h], "e4m3", 1) for h in range(h0.shape[1])], 1)
+        o, _ = recurrent_torch(q, k, v, beta, g, hq, scale=0.5, state_mode="none")
+        return o, torch.zeros_like(h0)
+
+    def ht_path(q, k, v, beta, g, h0):
+        _, ht = recurrent_torch(q, k, v, beta, g, h0, scale=0.5, state_mode="none")
+        return torch.zeros_like(d["v"], dtype=torch.float64), ht
+
+    ga = _grads(o_path, xs, do, dht)
+    gb = _grads(ht_path, xs, do, dht)
+    for x, a, b in zip(("q", "k", "v", "beta", "g", "h0"), g1, [p + r for p, r in zip(ga, gb)]):
+        assert torch.abs(a - b).max() <= 1e-12 * torch.abs(b).max(), x
+
+
+def test_torch_step_adjoint_closed_form():
+    """One token, Dk = Dv = 1, read copy off: H1 = a (1 - b k^2) H0 + b k v,
+    o = s H1 q, loss c H1 with c = s do q + dht; the gradients written out by
+    hand."""
+    rng = np.random.default_rng(8)
+    q0, k0, v0, b0, g0, h00, do0, dh0 = rng.normal(size=8)
+    b0 = 1.0 / (1.0 + np.exp(-b0))
+    s = 0.7
+    T = lambda x: torch.tensor([[[[x]]]], dtype=torch.float64)
+    xs = [T(q0), T(k0), T(v0), torch.tensor([[[b0]]], dtype=torch.float64),
+          torch.tensor([[[g0]]], dtype=torch.float64), T(h00)]
+    grads = _grads(lambda *x: two_precision_torch(*x, read_mode="none", scale=s, flush=16), xs,
+                   T(do0)[0], T(dh0))
+    a = np.exp(g0)
+    h1 = a * (1 - b0 * k0 * k0) * h00 + b0 * k0 * v0
+    c = s * do0 * q0 + dh0
+    want = {"q": s * do0 * h1, "k": c * (b0 * v0 - 2 * a * b0 * k0 * h00),
+            "v": c * b0 * k0, "beta": c * k0 * (v0 - a * k0 * h00),
+            "g": c * a * (1 - b0 * k0 * k0) * h00, "h0": c * a * (1 - b0 * k0 * k0)}
+    for name, got in zip(("q", "k", "v", "beta", "g", "h0"), grads):
+        assert abs(float(got.reshape(-1)[0]) - want[name]) <= 1e-12 * max(1.0, abs(want[name])), name
+
+
+def test_torch_read_disabled_gradcheck():
+    w = synth.small(B=1, T=5, Hk=1, Hv=1, Dk=4, Dv=3, h0=True, seed=9)
+    d = synth.make_inputs(w)
+    xs = [x.clone().requires_grad_(True) for x in _t64(d)]
+    assert torch.autograd.gradcheck(
+        lambda *x: two_precision_torch(*x, read_mode="none", scale=0.5, flush=2), xs)
