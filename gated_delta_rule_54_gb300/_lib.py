@@ -85,7 +85,11 @@ SIGNATURES = {
     "gdn_decode_validate": (ctypes.c_int, [_DP]),
     "gdn_decode_qdq": (ctypes.c_int, [_DP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "gdn_two_precision_validate": (ctypes.c_int, [_TP]),
-    "gdn_two_precision_fwd": (ctypes.c_int, [_TP, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "gdn_two_precision_anchor_bytes": (_SZ, [_TP]),
+    "gdn_two_precision_fwd": (ctypes.c_int, [_TP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "gdn_two_precision_bwd_workspace_bytes": (_SZ, [_TP]),
+    "gdn_two_precision_bwd": (ctypes.c_int, [_TP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
+                                             _P, _P, _P, _SZ, _P]),
 }
 
 _lock = threading.Lock()

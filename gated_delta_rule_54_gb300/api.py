@@ -183,13 +183,20 @@ def make_two_precision_problem(q, k, v, cu_seqlens=None, scale=1.0, read_mode="e
     return p
 
 
+def gdn_two_precision_anchor_bytes(p: GdnTwoPrecisionProblem) -> int:
+    return int(load().gdn_two_precision_anchor_bytes(ctypes.byref(p)))
+
+
 def gdn_two_precision_fwd(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0,
-                          read_mode="e4m3", flush=16, output_final_state=True, out=None):
+                          read_mode="e4m3", flush=16, output_final_state=True, out=None,
+                          save_anchors=False):
     """Two-precision GDN forward: fp32 recurrence anchor, E4M3 read copy (one scale per
     value row over the 128 key channels) re-derived from the anchor every ``flush`` tokens
     and read by the outputs only.  q, k [B,T,Hk,128] bf16; v [B,T,Hv,Dv] bf16; beta, g
     [B,T,Hv] f32; h0 [N,Hv,128,Dv] f32 or None.  Returns (o [B,T,Hv,Dv] f32,
-    ht [N,Hv,128,Dv] f32 = the anchor, or None); ``out`` may pass preallocated (o, ht)."""
+    ht [N,Hv,128,Dv] f32 = the anchor, or None); ``out`` may pass preallocated (o, ht).
+    With ``save_anchors`` a third value is returned: the anchor entering every window,
+    which gdn_two_precision_bwd takes."""
     lib = load()
     dev = q.device
     for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g), ("h0", h0),
@@ -204,10 +211,52 @@ def gdn_two_precision_fwd(q, k, v, beta, g, h0=None, cu_seqlens=None, scale=1.0,
         o = torch.empty(B, T, Hv, Dv, device=dev, dtype=torch.float32)
         ht = (torch.empty(p.N, Hv, k.shape[3], Dv, device=dev, dtype=torch.float32)
               if output_final_state else None)
+    anchors = None
+    if save_anchors:
+        nb = int(lib.gdn_two_precision_anchor_bytes(ctypes.byref(p)))
+        anchors = torch.empty(max(nb // 4, 4), device=dev, dtype=torch.float32)
     st = lib.gdn_two_precision_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
-                                   _ptr(g), _ptr(h0), _ptr(o), _ptr(ht), _stream(dev))
+                                   _ptr(g), _ptr(h0), _ptr(o), _ptr(ht), _ptr(anchors),
+                                   _stream(dev))
     check("gdn_two_precision_fwd", st)
-    return o, ht
+    return (o, ht, anchors) if save_anchors else (o, ht)
+
+
+def gdn_two_precision_bwd(q, k, v, beta, g, anchors, do, dht=None, cu_seqlens=None, scale=1.0,
+                          read_mode="e4m3", flush=16, need_dh0=True, workspace=None, out=None):
+    """Window-wise adjoint of the two-precision forward (identity straight-through at the
+    read copy).  ``anchors`` from gdn_two_precision_fwd(..., save_anchors=True) on the
+    same inputs; do [B,T,Hv,Dv] f32; dht [N,Hv,128,Dv] f32 or None.  Returns
+    (dq, dk, dv, dbeta, dg, dh0 or None); ``out`` may pass them preallocated."""
+    lib = load()
+    dev = q.device
+    for name, t in (("q", q), ("k", k), ("v", v), ("beta", beta), ("g", g),
+                    ("anchors", anchors), ("do", do), ("dht", dht), ("cu_seqlens", cu_seqlens)):
+        _check_dev(name, t, dev)
+    if do.dtype != torch.float32:
+        raise GdnError("gdn_two_precision_bwd", -2)
+    p = make_two_precision_problem(q, k, v, cu_seqlens, scale, read_mode, flush)
+    check("gdn_two_precision_validate", lib.gdn_two_precision_validate(ctypes.byref(p)))
+    f32 = dict(device=dev, dtype=torch.float32)
+    if out is not None:
+        dq, dk, dv, dbeta, dg, dh0 = out
+    else:
+        dq = torch.empty(k.shape, **f32)
+        dk = torch.empty(k.shape, **f32)
+        dv = torch.empty(v.shape, **f32)
+        dbeta = torch.empty(beta.shape, **f32)
+        dg = torch.empty(g.shape, **f32)
+        dh0 = torch.empty(p.N, v.shape[2], k.shape[3], v.shape[3], **f32) if need_dh0 else None
+    need = int(lib.gdn_two_precision_bwd_workspace_bytes(ctypes.byref(p)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), device=dev, dtype=torch.uint8)
+    st = lib.gdn_two_precision_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+                                   _ptr(g), _ptr(anchors), _ptr(do), _ptr(dht), _ptr(dq),
+                                   _ptr(dk), _ptr(dv), _ptr(dbeta), _ptr(dg), _ptr(dh0),
+                                   _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                                   _stream(dev))
+    check("gdn_two_precision_bwd", st)
+    return dq, dk, dv, dbeta, dg, dh0
 
 
 def make_decode_problem(q, k, v, scale=1.0, state_mode="e4m3", block_v=64,

@@ -21,7 +21,7 @@ OUT = os.path.join(PKG, "libgdn_qdq.so")
 BUILD_DIR = os.path.join(PKG, "_build")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 SOURCES = ["api.cu", "qdq.cu", "fwd.cu", "fwd_fused.cu", "bwd.cu", "bwd_tc.cu", "bwd_scan_tc.cu", "bwd_noalloc.cu",
-           "decode.cu", "kda.cu", "two_precision.cu"]
+           "decode.cu", "kda.cu", "two_precision.cu", "two_precision_bwd.cu"]
 
 
 def _nvcc() -> str:

@@ -22,21 +22,20 @@
 // ring.
 #include "common.cuh"
 #include "launch.h"
+#include "two_precision.cuh"
 
 namespace gdn {
 
 namespace {
 
 constexpr int kTpWarps = 4;   // warps per CTA
-constexpr int kTpCols = 4;    // value columns per warp
 constexpr int kTpRing = 4;    // tokens in flight per warp
-constexpr int kTpDk = 128;
-constexpr int kTpRows = kTpDk / 32;  // key rows per lane
 
 struct TpParams {
   const __nv_bfloat16 *q, *k, *v;
   const float *beta, *g, *h0;
   float *o, *ht;
+  float* anchors;  // [slots, Hv, 128, Dv] the anchor entering every window, or null
   const int32_t* cu_seqlens;
   int64_t T;
   int Hk, Hv, Dv, flush;
@@ -99,23 +98,18 @@ __global__ void __launch_bounds__(kTpWarps * 32) gdn_two_precision_kernel(const 
     return tv;
   };
 
-  // R <- Q_read(A): per column, the amax over all key rows (a warp max)
+  // R <- Q_read(A)
   auto flush_read = [&]() {
-    if constexpr (READQ) {
+    if constexpr (READQ) tp_read_copy<RM>(A, R);
+  };
+  // the anchor entering window w, kept for the backward
+  const int64_t slot0 = tp_anchor_slot(tok0, n, 0, p.flush);
+  auto save_anchor = [&](int w) {
+    if (!p.anchors) return;
+    float* dst = p.anchors + (((slot0 + w) * p.Hv + h) * kTpDk + kTpRows * lane) * p.Dv + c0;
 #pragma unroll
-      for (int c = 0; c < kTpCols; ++c) {
-        float m = 0.f;
-#pragma unroll
-        for (int r = 0; r < kTpRows; ++r) m = fmaxf(m, fabsf(A[r][c]));
-        m = warp_max(m);
-        float s, rcp;
-        qdq_scale<RM>(m, s, rcp);
-#pragma unroll
-        for (int r = 0; r < kTpRows; ++r)
-          R[r][c] = m == 0.f ? A[r][c]
-                             : __fmul_rn(qdq_code_value<RM>(qdq_code<RM>(A[r][c], rcp)), s);
-      }
-    }
+    for (int r = 0; r < kTpRows; ++r)
+      *reinterpret_cast<float4*>(dst + (int64_t)r * p.Dv) = make_float4(A[r][0], A[r][1], A[r][2], A[r][3]);
   };
 
   TokVec ring[kTpRing];
@@ -125,6 +119,7 @@ __global__ void __launch_bounds__(kTpWarps * 32) gdn_two_precision_kernel(const 
   // the first token's column sums A^T k, R^T k
   float kSA[kTpCols], kSR[kTpCols];
   if (L > 0) {
+    save_anchor(0);
     flush_read();
     float kr[kTpRows];
     bf16x4(ring[0].k, kr);
@@ -180,6 +175,7 @@ __global__ void __launch_bounds__(kTpWarps * 32) gdn_two_precision_kernel(const 
         for (int r = 0; r < kTpRows; ++r) x[J_O + c] = fmaf(qr[r], READQ ? R[r][c] : A[r][c], x[J_O + c]);
       const bool more = lt + 1 < L;
       if (more && --left == 0) {  // the next token starts a window
+        save_anchor((lt + 1) / p.flush);
         flush_read();
         left = p.flush;
       }
@@ -218,7 +214,8 @@ __global__ void __launch_bounds__(kTpWarps * 32) gdn_two_precision_kernel(const 
 
 gdn_status launch_two_precision(const gdn_two_precision_problem& p, int64_t N, const void* q,
                                 const void* k, const void* v, const float* beta, const float* g,
-                                const float* h0, float* o, float* ht, cudaStream_t st) {
+                                const float* h0, float* o, float* ht, float* anchors,
+                                cudaStream_t st) {
   TpParams prm{};
   prm.q = static_cast<const __nv_bfloat16*>(q);
   prm.k = static_cast<const __nv_bfloat16*>(k);
@@ -228,6 +225,7 @@ gdn_status launch_two_precision(const gdn_two_precision_problem& p, int64_t N, c
   prm.h0 = h0;
   prm.o = o;
   prm.ht = ht;
+  prm.anchors = anchors;
   prm.cu_seqlens = p.cu_seqlens;
   prm.T = p.T;
   prm.Hk = p.Hk;
@@ -242,6 +240,8 @@ gdn_status launch_two_precision(const gdn_two_precision_problem& p, int64_t N, c
     gdn_two_precision_kernel<GDN_QDQ_NONE><<<grid, kTpWarps * 32, 0, st>>>(prm);
   return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
+
+}  // namespace
 
 gdn_status validate_two_precision(const gdn_two_precision_problem* p) {
   if (!p) return GDN_ERR_INVALID_ARG;
@@ -270,7 +270,9 @@ gdn_status validate_two_precision(const gdn_two_precision_problem* p) {
   return GDN_OK;
 }
 
-}  // namespace
+int64_t two_precision_anchor_slots(const gdn_two_precision_problem* p) {
+  return p->B * p->T / p->flush + p->N;
+}
 
 }  // namespace gdn
 
@@ -282,18 +284,24 @@ gdn_status gdn_two_precision_validate(const gdn_two_precision_problem* p) {
   return validate_two_precision(p);
 }
 
+size_t gdn_two_precision_anchor_bytes(const gdn_two_precision_problem* p) {
+  if (validate_two_precision(p) != GDN_OK) return 0;
+  return (size_t)two_precision_anchor_slots(p) * p->Hv * kTpDk * p->Dv * sizeof(float);
+}
+
 gdn_status gdn_two_precision_fwd(const gdn_two_precision_problem* p, const void* q,
                                  const void* k, const void* v, const float* beta,
                                  const float* g, const float* h0, float* o, float* ht,
-                                 void* stream) {
+                                 float* anchors, void* stream) {
   const gdn_status s = validate_two_precision(p);
   if (s != GDN_OK) return s;
   if (p->B * p->T > 0 && (!q || !k || !v || !beta || !g || !o)) return GDN_ERR_INVALID_ARG;
   for (const void* ptr : {q, k, v, (const void*)beta, (const void*)g, (const void*)h0,
-                          (const void*)o, (const void*)ht, (const void*)p->cu_seqlens})
+                          (const void*)o, (const void*)ht, (const void*)anchors,
+                          (const void*)p->cu_seqlens})
     if (ptr && ((uintptr_t)ptr & 15)) return GDN_ERR_MISALIGNED;
   if (p->N == 0 || (p->B * p->T == 0 && !ht)) return GDN_OK;
-  return launch_two_precision(*p, p->N, q, k, v, beta, g, h0, o, ht,
+  return launch_two_precision(*p, p->N, q, k, v, beta, g, h0, o, ht, anchors,
                               static_cast<cudaStream_t>(stream));
 }
 

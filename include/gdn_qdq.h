@@ -49,7 +49,7 @@
 extern "C" {
 #endif
 
-#define GDN_QDQ_ABI_VERSION 6
+#define GDN_QDQ_ABI_VERSION 7
 
 typedef enum {
   GDN_QDQ_NONE = 0, /* site not quantized                                   */
@@ -373,6 +373,10 @@ gdn_status gdn_decode_qdq(const gdn_decode_problem* p, const void* q, const void
  *   q, k  bf16 [B, T, Hk, 128]     v bf16 [B, T, Hv, Dv]   beta, g f32 [B, T, Hv]
  *   h0    f32  [N, Hv, 128, Dv] or NULL (zeros)
  *   o     f32  [B, T, Hv, Dv] (written)     ht f32 [N, Hv, 128, Dv] or NULL (written)
+ *   anchors f32 [gdn_two_precision_anchor_bytes(p) / 4] or NULL: when given, the
+ *         anchor A entering every window (the state before token w*W of each
+ *         sequence, w = 0, 1, ...) is written there for gdn_two_precision_bwd
+ *         (caller allocated; the layout is private to the library)
  * Dk must be 128 (GDN_ERR_UNSUPPORTED_SHAPE), Dv 64 or 128; read_mode NONE or
  * E4M3 (INT8: GDN_ERR_UNSUPPORTED_MODE); flush >= 1; N <= 65535; packed
  * sequences and grouped heads as for the chunked forward; all pointers 16-byte
@@ -393,10 +397,43 @@ typedef struct {
 /* Host-only validation of a two-precision problem (no CUDA call). */
 gdn_status gdn_two_precision_validate(const gdn_two_precision_problem* p);
 
+/* Bytes of the forward's anchor buffer: (B*T / W + N) windows' anchors
+ * [Hv, 128, Dv] f32, or 0 if p is invalid. */
+size_t gdn_two_precision_anchor_bytes(const gdn_two_precision_problem* p);
+
 gdn_status gdn_two_precision_fwd(const gdn_two_precision_problem* p, const void* q,
                                  const void* k, const void* v, const float* beta,
                                  const float* g, const float* h0, float* o, float* ht,
-                                 void* stream);
+                                 float* anchors, void* stream);
+
+/*
+ * Backward of the two-precision profile: the window-wise adjoint (same page
+ * and section: "a window-wise adjoint during backward").  Reading implemented:
+ * the read copy passes its gradient to the anchor unchanged (identity
+ * straight-through estimator at every flush), every other step is
+ * differentiated exactly, so for L = <dO, o> + <dht, ht> each window's
+ * adjoint runs from its end back to its start through both states, and at the
+ * window start the read state's gradient is added to the anchor's.  Each window
+ * is recomputed from the anchor the forward saved at its start.
+ *   anchors  the forward's (same inputs, same problem, anchors != NULL)
+ *   dO    f32 [B, T, Hv, Dv]           dht f32 [N, Hv, 128, Dv] or NULL (zeros)
+ *   dq,dk f32 [B, T, Hk, 128]  (summed over the value heads sharing a key head)
+ *   dv    f32 [B, T, Hv, Dv]           dbeta, dg f32 [B, T, Hv]
+ *   dh0   f32 [N, Hv, 128, Dv] or NULL
+ * All outputs are overwritten; the sums over value columns are taken in a fixed
+ * order (bitwise repeatable).  Packed sequences must cover tokens 0..T-1.
+ * min(flush, T) must be <= 256 (GDN_ERR_UNSUPPORTED_SHAPE), otherwise as the
+ * forward.  `workspace`: gdn_two_precision_bwd_workspace_bytes(p) bytes,
+ * 256-byte aligned (GDN_ERR_WORKSPACE_TOO_SMALL when smaller).
+ */
+size_t gdn_two_precision_bwd_workspace_bytes(const gdn_two_precision_problem* p);
+
+gdn_status gdn_two_precision_bwd(const gdn_two_precision_problem* p, const void* q,
+                                 const void* k, const void* v, const float* beta,
+                                 const float* g, const float* anchors, const float* dO,
+                                 const float* dht, float* dq, float* dk, float* dv,
+                                 float* dbeta, float* dg, float* dh0, void* workspace,
+                                 size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }

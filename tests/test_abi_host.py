@@ -167,7 +167,7 @@ def test_status_strings():
     for code in range(-7, 1):
         s = lib.gdn_status_string(code).decode()
         assert s.startswith("GDN_")
-    assert lib.gdn_abi_version() == 6
+    assert lib.gdn_abi_version() == 7
 
 
 def _dproblem(**kw):
@@ -233,23 +233,62 @@ def test_two_precision_entry_rejects_before_launch():
     P = ctypes.c_void_p
     f = P(4096)
     call = lambda p, *a: lib.gdn_two_precision_fwd(ctypes.byref(p), *a)
-    assert call(_tproblem(read_mode=2), f, f, f, f, f, None, f, f, None) == -4
-    assert call(_tproblem(), None, f, f, f, f, None, f, f, None) == -1          # null q
-    assert call(_tproblem(), f, f, f, f, f, None, None, f, None) == -1          # null o
-    assert call(_tproblem(), f, f, f, f, f, P(4104), f, f, None) == -7          # misaligned h0
+    assert call(_tproblem(read_mode=2), f, f, f, f, f, None, f, f, None, None) == -4
+    assert call(_tproblem(), None, f, f, f, f, None, f, f, None, None) == -1          # null q
+    assert call(_tproblem(), f, f, f, f, f, None, None, f, None, None) == -1          # null o
+    assert call(_tproblem(), f, f, f, f, f, P(4104), f, f, None, None) == -7          # misaligned h0
+    assert call(_tproblem(), f, f, f, f, f, None, f, f, P(4100), None) == -7          # misaligned anchors
     # packed sequences: B == 1 and N >= 1
     assert lib.gdn_two_precision_validate(ctypes.byref(_tproblem(B=2, N=3, cu_seqlens=f))) == -1
     assert lib.gdn_two_precision_validate(ctypes.byref(_tproblem(B=1, N=3, cu_seqlens=f))) == 0
     # nothing to do: no sequences, or no tokens and no final state
-    assert call(_tproblem(B=0, N=0), None, None, None, None, None, None, None, None, None) == 0
-    assert call(_tproblem(T=0), None, None, None, None, None, None, None, None, None) == 0
+    assert call(_tproblem(B=0, N=0), None, None, None, None, None, None, None, None, None, None) == 0
+    assert call(_tproblem(T=0), None, None, None, None, None, None, None, None, None, None) == 0
+
+
+def test_two_precision_anchor_and_workspace_sizes():
+    lib = _lib.load()
+    p = _tproblem()
+    nwin = p.B * p.T // p.flush + p.N        # an anchor [Hv, 128, Dv] per window slot
+    assert lib.gdn_two_precision_anchor_bytes(ctypes.byref(p)) == nwin * p.Hv * 128 * p.Dv * 4
+    assert lib.gdn_two_precision_anchor_bytes(ctypes.byref(_tproblem(read_mode=2))) == 0
+    assert lib.gdn_two_precision_bwd_workspace_bytes(ctypes.byref(p)) > 0
+    # grouped heads add the per-value-head dq and dk
+    g1 = lib.gdn_two_precision_bwd_workspace_bytes(ctypes.byref(_tproblem(Hk=4, Hv=4)))
+    g2 = lib.gdn_two_precision_bwd_workspace_bytes(ctypes.byref(_tproblem(Hk=2, Hv=4)))
+    assert g2 >= g1 + 2 * p.B * p.T * 4 * 128 * 4
+    # windows longer than 256 tokens (and than the sequence) are not replayed
+    assert lib.gdn_two_precision_bwd_workspace_bytes(ctypes.byref(_tproblem(T=1000, flush=300))) == 0
+    assert lib.gdn_two_precision_bwd_workspace_bytes(ctypes.byref(_tproblem(T=200, flush=300))) > 0
+
+
+def test_two_precision_bwd_rejects_before_launch():
+    lib = _lib.load()
+    P = ctypes.c_void_p
+    f = P(4096)
+    ws_ok = lib.gdn_two_precision_bwd_workspace_bytes(ctypes.byref(_tproblem()))
+
+    def call(p, q=f, anchors=f, dO=f, dq=f, dht=None, ws=f, ws_bytes=ws_ok):
+        return lib.gdn_two_precision_bwd(ctypes.byref(p), q, f, f, f, f, anchors, dO, dht, dq, f, f,
+                                         f, f, None, ws, ws_bytes, None)
+    assert call(_tproblem(read_mode=2)) == -4
+    assert call(_tproblem(T=1000, flush=300)) == -3
+    assert call(_tproblem(), q=None) == -1
+    assert call(_tproblem(), anchors=None) == -1       # the forward's anchors are required
+    assert call(_tproblem(), dO=None) == -1
+    assert call(_tproblem(), dq=P(4100)) == -7
+    assert call(_tproblem(), dht=P(4104)) == -7
+    assert call(_tproblem(), ws_bytes=ws_ok - 1) == -5
+    assert call(_tproblem(), ws=None) == -5
+    assert call(_tproblem(B=0, N=0), q=None, anchors=None, dO=None, dq=None, ws=None, ws_bytes=0) == 0
 
 
 def test_no_host_fallback_for_cpu_tensors():
     """Every compute entry point of the binding refuses host tensors: there is no
     CPU path behind the library."""
-    from gated_delta_rule_54_gb300 import (gdn_chunk_fwd_qdq, gdn_decode_qdq, gdn_two_precision_fwd,
-                                           kda_recurrent_fwd_qdq, fake_qdq_e4m3, synth)
+    from gated_delta_rule_54_gb300 import (gdn_chunk_fwd_qdq, gdn_decode_qdq, gdn_two_precision_bwd,
+                                           gdn_two_precision_fwd, kda_recurrent_fwd_qdq,
+                                           fake_qdq_e4m3, synth)
     d = synth.make_inputs(synth.small(B=1, T=8, Hk=1, Hv=1, Dk=64, Dv=64, h0=True, seed=1))
     with pytest.raises(ValueError, match="CUDA tensor"):
         gdn_chunk_fwd_qdq(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"])
@@ -257,6 +296,9 @@ def test_no_host_fallback_for_cpu_tensors():
         gdn_decode_qdq(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"])
     with pytest.raises(ValueError, match="CUDA tensor"):
         gdn_two_precision_fwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"])
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        gdn_two_precision_bwd(d["q"], d["k"], d["v"], d["beta"], d["g"], d["h0"],
+                              torch.zeros(d["v"].shape))
     gk = d["g"][..., None].expand(*d["g"].shape, 64).contiguous()
     with pytest.raises(ValueError, match="CUDA tensor"):
         kda_recurrent_fwd_qdq(d["q"], d["k"], d["v"], d["beta"], gk, d["h0"])
