@@ -15,7 +15,8 @@ reported as ``roofline``; the backward's roofline is ``roofline_bwd``.
 (256 sequences, one token each, carried fp32 states of 256 MiB);
 ``--mode kda`` the KDA recurrence and ``--mode two_precision`` the
 two-precision profile (fp32 anchor, E4M3 read copy), both B=4, T=4096,
-H=16.  Inputs are synthetic (seeded) and resident in HBM when the timed
+H=16; ``--mode two_precision_bwd`` that profile's training step (forward
+saving the window anchors, then the window-wise adjoint).  Inputs are synthetic (seeded) and resident in HBM when the timed
 region starts; every micro-batch's inputs exceed the 129 MB L2, so no flush
 is needed between them.
 
@@ -779,6 +780,7 @@ TP_METRIC = ("two-precision GDN fwd tokens/s at B=4,T=4096,H=16,D=128 (fp32 anch
              "16-token flush); % of roofline")
 KDA_SOURCES = ["gated_delta_rule_54_gb300/csrc/kda.cu", "gated_delta_rule_54_gb300/csrc/common.cuh"]
 TP_SOURCES = ["gated_delta_rule_54_gb300/csrc/two_precision.cu",
+              "gated_delta_rule_54_gb300/csrc/two_precision.cuh",
               "gated_delta_rule_54_gb300/csrc/common.cuh"]
 TP_FLUSH = 16
 
@@ -937,6 +939,185 @@ def run_token_serial(args, ws, rank, local):
 
 
 # ----------------------------------------------------------------------------
+# two-precision training step (--mode two_precision_bwd): the forward saving
+# its window anchors, then the window-wise adjoint
+# ----------------------------------------------------------------------------
+TPB_METRIC = ("two-precision GDN fwd+bwd tokens/s at B=4,T=4096,H=16,D=128 (fp32 anchor, E4M3 "
+              "read copy, 16-token flush, window-wise adjoint); % of roofline")
+TPB_SOURCES = ["gated_delta_rule_54_gb300/csrc/two_precision_bwd.cu",
+               "gated_delta_rule_54_gb300/csrc/two_precision.cuh",
+               "gated_delta_rule_54_gb300/csrc/common.cuh"]
+
+
+def tp_anchor_bytes(w, flush=TP_FLUSH):
+    """The forward's saved anchors: one fp32 [Hv, Dk, Dv] per window slot."""
+    return (w.B * w.T // flush + w.B) * w.Hv * w.Dk * w.Dv * 4
+
+
+def tp_bwd_alg_bytes(w, flush=TP_FLUSH):
+    """Algorithmic HBM bytes of one backward launch: q, k, v (bf16), beta, g,
+    dO (f32) and the anchors read once; dq, dk, dv, dbeta, dg written once;
+    dht read and dh0 written."""
+    tok = w.B * w.T
+    b = tok * (w.Hk * w.Dk * 2 * 2 + w.Hv * w.Dv * 2 + w.Hv * 4 * 2 + w.Hv * w.Dv * 4)
+    b += tok * (w.Hk * w.Dk * 4 * 2 + w.Hv * w.Dv * 4 + w.Hv * 4 * 2)
+    return b + tp_anchor_bytes(w, flush) + w.B * w.Hv * w.Dk * w.Dv * 4 * 2
+
+
+def tp_upstream(w, seed):
+    gen = torch.Generator().manual_seed(seed)
+    do = torch.randn(w.B, w.T, w.Hv, w.Dv, generator=gen)
+    dht = torch.randn(w.B, w.Hv, w.Dk, w.Dv, generator=gen) * 0.1
+    return do, dht
+
+
+def tp_bwd_cpu_sample(w, cpu, do, dht, Ts):
+    """The oracle's autograd (fp64) on one sequence x Ts tokens, all heads."""
+    from oracle.two_precision import two_precision_torch
+    sl = lambda t: t[:1, :Ts]
+    xs = [sl(cpu[n]).to(torch.float32).double().requires_grad_(True)
+          for n in ("q", "k", "v", "beta", "g")]
+    xs.append(cpu["h0"][:1].double().requires_grad_(True))
+    t0 = time.time()
+    o, ht = two_precision_torch(*xs, read_mode=w.state_mode, flush=TP_FLUSH)
+    loss = (o * sl(do).double()).sum() + (ht * dht[:1].double()).sum()
+    torch.autograd.grad(loss, xs)
+    return Ts, time.time() - t0
+
+
+def run_tp_bwd(args, ws, rank, local):
+    from gated_delta_rule_54_gb300 import api, synth
+    from gated_delta_rule_54_gb300._lib import load
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    load()
+    w = synth.WORKLOADS[args.workload]
+    w = synth.Workload(**{**w.__dict__, "seed": w.seed + rank})
+    cpu = synth.make_inputs(w)
+    do_h, dht_h = tp_upstream(w, 1000 + w.seed)
+    names = ("q", "k", "v", "beta", "g", "h0")
+    d = {n: cpu[n].to(dev) for n in names}
+    d["do"], d["dht"] = do_h.to(dev), dht_h.to(dev)
+    rm = w.state_mode
+    f32 = dict(device=dev, dtype=torch.float32)
+
+    def buffers():
+        return {"o": torch.empty(w.B, w.T, w.Hv, w.Dv, **f32),
+                "ht": torch.empty(w.B, w.Hv, w.Dk, w.Dv, **f32),
+                "grads": (torch.empty(w.B, w.T, w.Hk, w.Dk, **f32),
+                          torch.empty(w.B, w.T, w.Hk, w.Dk, **f32),
+                          torch.empty(w.B, w.T, w.Hv, w.Dv, **f32),
+                          torch.empty(w.B, w.T, w.Hv, **f32), torch.empty(w.B, w.T, w.Hv, **f32),
+                          torch.empty(w.B, w.Hv, w.Dk, w.Dv, **f32))}
+
+    def fwd(x, bufs):
+        return api.gdn_two_precision_fwd(x["q"], x["k"], x["v"], x["beta"], x["g"], x["h0"],
+                                         read_mode=rm, flush=TP_FLUSH, save_anchors=True,
+                                         out=(bufs["o"], bufs["ht"]))
+
+    def bwd(x, anchors, bufs):
+        return api.gdn_two_precision_bwd(x["q"], x["k"], x["v"], x["beta"], x["g"], anchors,
+                                         x["do"], x["dht"], read_mode=rm, flush=TP_FLUSH,
+                                         out=bufs["grads"])
+
+    bufs = buffers()
+
+    def step(x, b):
+        _, _, anchors = fwd(x, b)
+        return bwd(x, anchors, b)
+
+    stream = torch.cuda.current_stream(dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        step(d, bufs)
+    torch.cuda.synchronize()
+    _barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(dev) as clk:
+        a, b = ev(), ev()
+        a.record(stream)
+        for _ in range(args.steps):
+            step(d, bufs)
+        b.record(stream)
+        torch.cuda.synchronize()
+    _barrier(ws)
+    ms_total = _max_over_ranks(a.elapsed_time(b), ws, dev)
+    ms_step = ms_total / args.steps
+    # the backward alone (its launches from one forward's anchors)
+    _, _, anchors = fwd(d, bufs)
+    for _ in range(2):
+        bwd(d, anchors, bufs)
+    torch.cuda.synchronize()
+    a, b = ev(), ev()
+    a.record(stream)
+    for _ in range(args.steps):
+        bwd(d, anchors, bufs)
+    b.record(stream)
+    torch.cuda.synchronize()
+    bwd_ms = _max_over_ranks(a.elapsed_time(b), ws, dev) / args.steps
+    tokens = w.B * w.T
+    value = tokens * ws * args.steps / (ms_total / 1e3)
+    peak, _, peak_kind = _peaks()
+    alg = tp_bwd_alg_bytes(w)
+    achieved = alg / (bwd_ms / 1e3) / 1e9
+    G = w.Hv // w.Hk
+
+    e2e = None
+    if not args.no_e2e:
+        host_in = {n: cpu[n].pin_memory() for n in names}
+        host_in["do"], host_in["dht"] = do_h.pin_memory(), dht_h.pin_memory()
+        dev_in = [{n: torch.empty_like(t, device=dev) for n, t in host_in.items()} for _ in range(2)]
+        res_d = [buffers() for _ in range(2)]
+        res_h = [[torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                  for t in (r["o"], r["ht"]) + r["grads"]] for r in res_d]
+
+        def run(st):
+            step(dev_in[st], res_d[st])
+            return [res_d[st]["o"], res_d[st]["ht"]] + list(res_d[st]["grads"])
+
+        e_ms, s_ms = e2e_pipelined(dev, ws, args.steps, args.warmup, host_in, dev_in, run, res_h)
+        e2e = {"value": round(tokens * ws / (e_ms / 1e3), 1), "unit": "tokens/s",
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in.values()),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in res_h[0]),
+               "ms_per_step": round(e_ms, 4),
+               "schedule": "pipelined: step i+1's upload and step i-1's download overlap step i's "
+                           "compute (three streams, two device buffer sets)",
+               "serial_value": round(tokens * ws / (s_ms / 1e3), 1),
+               "serial_ms_per_step": round(s_ms, 4)}
+
+    cpu_base = None
+    if rank == 0 and not args.no_cpu_baseline:
+        Ts, dt = tp_bwd_cpu_sample(w, cpu, do_h, dht_h, 32)
+        cpu_base = {"value": round(Ts / dt, 2), "unit": "tokens/s", "cores": torch.get_num_threads(),
+                    "kind": "oracle",
+                    "sample": "1 sequence x %d tokens, all %d heads, fp64 two-precision oracle "
+                              "forward + autograd backward" % (Ts, w.Hv)}
+    line = {
+        "metric": TPB_METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; q,k L2-normalised N(0,1), v N(0,1), beta=sigmoid, "
+                "g=-softplus(N(0,1)), h0 N(0, 0.1^2); dO N(0,1), dht N(0, 0.1^2))",
+        "config": {"workload": w.name, "mode": "two_precision_bwd", "B": w.B, "T": w.T,
+                   "Hk": w.Hk, "Hv": w.Hv, "Dk": w.Dk, "Dv": w.Dv, "read_mode": rm,
+                   "flush": TP_FLUSH, "l2": "inputs larger than L2 (no flush needed)"},
+        "clocks": clk.summary(), "e2e": e2e,
+        "gpu_launches": args.steps * (2 + (2 if G > 1 else 0)),
+        "fwd_ms": round(ms_step - bwd_ms, 4), "bwd_ms": round(bwd_ms, 4),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4),
+                     "traffic": _traffic("gdn_two_precision_bwd_kernel_two_precision_layer.md",
+                                         TPB_SOURCES, args.workload),
+                     "kernel": "gdn_two_precision_bwd_kernel", "peak_source": peak_kind,
+                     "alg_bytes_per_launch": alg, "launch_ms": round(bwd_ms, 4)},
+        "cpu_baseline": cpu_base,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------
 # reference arm: the oracle on the host cores
 # ----------------------------------------------------------------------------
 def run_reference(args, ws, rank):
@@ -964,6 +1145,32 @@ def run_reference(args, ws, rank):
                        "Hv": w.Hv, "Dk": w.Dk, "Dv": w.Dv, "state_mode": w.state_mode},
             "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s",
                              "cores": torch.get_num_threads(), "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}), flush=True)
+        return
+    if args.mode == "two_precision_bwd":
+        cpu = synth.make_inputs(w)
+        do_h, dht_h = tp_upstream(w, 1000 + w.seed)
+        for _ in range(args.warmup):
+            tp_bwd_cpu_sample(w, cpu, do_h, dht_h, 4)
+        done = el = 0.0
+        for _ in range(args.steps):
+            n, dt = tp_bwd_cpu_sample(w, cpu, do_h, dht_h, 16)
+            done += n
+            el += dt
+        value = done / el
+        print(json.dumps({
+            "impl": "reference", "metric": TPB_METRIC, "value": round(value, 2), "unit": "tokens/s",
+            "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el * 1e3 / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "mode": "two_precision_bwd", "B": w.B, "T": w.T,
+                       "Hk": w.Hk, "Hv": w.Hv, "Dk": w.Dk, "Dv": w.Dv, "read_mode": w.state_mode,
+                       "flush": TP_FLUSH},
+            "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s",
+                             "cores": torch.get_num_threads(), "kind": "oracle",
+                             "sample": "1 sequence x 16 tokens, all %d heads per step (fp64 "
+                                       "two-precision oracle forward + autograd backward)" % w.Hv},
             "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}), flush=True)
         return
@@ -1036,7 +1243,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=None)
     ap.add_argument("--mode", default=None,
-                    choices=["fwd", "fwdbwd", "decode", "kda", "two_precision"])
+                    choices=["fwd", "fwdbwd", "decode", "kda", "two_precision",
+                             "two_precision_bwd"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
@@ -1051,6 +1259,7 @@ def main():
         args.mode = "fwdbwd" if _backward_available() else "fwd"
     if args.workload is None:
         args.workload = {"decode": "decode", "kda": "kda", "two_precision": "two_precision",
+                         "two_precision_bwd": "two_precision",
                          "fwdbwd": "fwd_bwd"}.get(args.mode, "layer")
     args.bwd_launches = BWD_LAUNCHES
     ws, rank, local = _dist()
@@ -1060,6 +1269,8 @@ def main():
         run_decode(args, ws, rank, local)
     elif args.mode in ("kda", "two_precision"):
         run_token_serial(args, ws, rank, local)
+    elif args.mode == "two_precision_bwd":
+        run_tp_bwd(args, ws, rank, local)
     else:
         run_ours(args, ws, rank, local)
     if ws > 1:

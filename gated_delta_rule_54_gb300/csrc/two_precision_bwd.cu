@@ -42,7 +42,7 @@ namespace {
 constexpr int kBwWarps = 4;
 constexpr int kBwThreads = kBwWarps * 32;
 constexpr int kBwCtaCols = kBwWarps * kTpCols;  // value columns per CTA
-constexpr int kBwSub = 16;                       // tokens staged at a time
+constexpr int kBwSub = 8;                        // tokens staged at a time (>= the cluster size)
 constexpr int kBwCk = 4;                         // tokens between saved states
 constexpr int kBwMaxWindow = 256;                // longest window replayed: min(W, T)
 constexpr int kBwMaxCtas = 1024;                 // persistent grid (bounds the scratch)
@@ -175,7 +175,7 @@ __device__ __forceinline__ void tp_cluster_sum(TpBwdSmem& S, const TpBwdParams& 
 }
 
 template <int RM>
-__global__ void __launch_bounds__(kBwThreads, 3) gdn_two_precision_bwd_kernel(const TpBwdParams p) {
+__global__ void __launch_bounds__(kBwThreads, 4) gdn_two_precision_bwd_kernel(const TpBwdParams p) {
   constexpr bool RQ = RM != GDN_QDQ_NONE;
   constexpr int NF = RQ ? 8 : 4;    // replay sums: k^T A (0..3), k^T R (4..7)
   constexpr int NB = RQ ? 16 : 8;   // reverse sums: k^T dA, [k^T dR], dA^T A, [dR^T R]
@@ -331,37 +331,30 @@ __global__ void __launch_bounds__(kBwThreads, 3) gdn_two_precision_bwd_kernel(co
         const int nt = min(kBwSub, wl - sb);
         tp_stage(S, p, tw + sb, nt, h, hk, ccol, true, sclg + (int64_t)sb * kBwSclFloats);
         __syncthreads();
-        float cA[kTpRows][kTpCols], cR[kTpRows][kTpCols];
         for (int jj = nt - 1; jj >= 0; --jj) {
           const int j = sb + jj;
           const int g0 = j & ~(kBwCk - 1);
-          if (jj == nt - 1 || ((j + 1) & (kBwCk - 1)) == 0) {  // a new group of four
+          // the pre-step states of token j, rebuilt from the pair saved at g0
+          // (read again for every token: fewer live registers)
+          float xA[kTpRows][kTpCols], xR[kTpRows][kTpCols];
+          {
             const float* ck = scr + (int64_t)(j / kBwCk) * kBwCkFloats + threadIdx.x * 16;
 #pragma unroll
             for (int r = 0; r < kTpRows; ++r) {
               const float4 x = __ldcg(reinterpret_cast<const float4*>(ck) + r);
-              cA[r][0] = x.x;
-              cA[r][1] = x.y;
-              cA[r][2] = x.z;
-              cA[r][3] = x.w;
+              xA[r][0] = x.x;
+              xA[r][1] = x.y;
+              xA[r][2] = x.z;
+              xA[r][3] = x.w;
               if constexpr (RQ) {
                 const float4 y = __ldcg(reinterpret_cast<const float4*>(ck + kBwThreads * 16) + r);
-                cR[r][0] = y.x;
-                cR[r][1] = y.y;
-                cR[r][2] = y.z;
-                cR[r][3] = y.w;
+                xR[r][0] = y.x;
+                xR[r][1] = y.y;
+                xR[r][2] = y.z;
+                xR[r][3] = y.w;
               }
             }
           }
-          // the pre-step states of token j, rebuilt from the saved pair
-          float xA[kTpRows][kTpCols], xR[kTpRows][kTpCols];
-#pragma unroll
-          for (int r = 0; r < kTpRows; ++r)
-#pragma unroll
-            for (int c = 0; c < kTpCols; ++c) {
-              xA[r][c] = cA[r][c];
-              if constexpr (RQ) xR[r][c] = cR[r][c];
-            }
           for (int i = g0; i < j; ++i) {
             const int ii = i - sb;
             const float4 k4 = *reinterpret_cast<const float4*>(&S.k[ii][kTpRows * lane]);

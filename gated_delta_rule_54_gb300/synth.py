@@ -72,6 +72,11 @@ WORKLOADS = {
     # read quantizer), 16-token flushes
     "two_precision": Workload("two-precision B4 T4096 H16 D128 e4m3-read flush16", B=4, T=4096,
                               Hk=16, Hv=16, Dk=128, Dv=128, w_mode="none", h0=True, seed=7),
+    # the same launch shape on shorter sequences: the small case of the detailed
+    # counter captures of the two-precision kernels
+    "two_precision_t1k": Workload("two-precision B4 T1024 H16 D128 e4m3-read flush16", B=4,
+                                  T=1024, Hk=16, Hv=16, Dk=128, Dv=128, w_mode="none", h0=True,
+                                  seed=7),
 }
 
 
