@@ -83,6 +83,7 @@ struct FwdParams {
   int bv_log2;  // log2(block_v)
   int neumann;  // -1: exact solve; d >= 0: Neumann polynomial of degree d
   int64_t nt_fixed;
+  int64_t n_slots;  // chunk slots of the call
   float scale;
 };
 
@@ -267,13 +268,17 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
   __shared__ uint32_t tmem_slot;
   __shared__ int tc_failed;
 
-  const int64_t slot = blockIdx.x / p.Hv;
-  const int h = blockIdx.x % p.Hv;
-  ChunkRef cr;
-  if (!chunk_of_slot(p, slot, cr)) return;
-  const int hk = h / p.G;
-  const int L = cr.L;
-  const int64_t tok0 = cr.tok;
+  // The fused path's variant is persistent: CTA b takes the chunk-heads b,
+  // b + grid, ... and loads the next one's K, beta and g while it finishes the
+  // current one (K is free once W = Tw K has run).  The other variant has one
+  // CTA per chunk-head.
+  const int64_t units = p.n_slots * p.Hv;
+  // the next chunk-head at or after u that holds tokens (units if none)
+  auto next_unit = [&](int64_t u, ChunkRef& r) {
+    for (; u < units; u += gridDim.x)
+      if (chunk_of_slot(p, u / p.Hv, r)) return u;
+    return units;
+  };
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gq = lane >> 2, tq = lane & 3;
   const int nvb = p.Dv / 64;
@@ -296,22 +301,32 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
 
   // K and V as TMA boxes (rows >= L hold another sequence's tokens: they only
   // meet zero beta, so they reach neither A, W nor U); beta and g zero-filled
+  auto issue_loads = [&](int64_t u, const ChunkRef& r) {
+    const int hh = (int)(u % p.Hv);
+    if (threadIdx.x == 0) {
+      mbar_expect_tx(&bar, kChunk * DK * 2 + (TOUT ? 0 : nvb * kChunk * 64 * 2));
+#pragma unroll
+      for (int pn = 0; pn < DK / 64; ++pn)
+        tma_load_2d(Ks + pn * kChunk * 64, &p.tm_k, (hh / p.G) * DK + pn * 64, (int)r.tok, &bar);
+      for (int vb = 0; vb < (TOUT ? 0 : nvb); ++vb)
+        tma_load_2d(Vs + vb * kChunk * 64, &p.tm_v, hh * p.Dv + vb * 64, (int)r.tok, &bar);
+    }
+    if (threadIdx.x < 2 * kChunk) {
+      const int t = threadIdx.x & 63;
+      load_vec64(bsrc + (threadIdx.x < kChunk ? 0 : 64), threadIdx.x < kChunk ? p.beta : p.g,
+                 r.tok, r.L, p.Hv, hh, t);
+    }
+    cp_async_commit();
+  };
+  ChunkRef cr;
+  int64_t u = next_unit(blockIdx.x, cr);
+  if (u >= units) return;
   if (threadIdx.x == 0) {
     mbar_init(&bar, 1);
     fence_mbar_init();
-    mbar_expect_tx(&bar, kChunk * DK * 2 + (TOUT ? 0 : nvb * kChunk * 64 * 2));
-#pragma unroll
-    for (int pn = 0; pn < DK / 64; ++pn)
-      tma_load_2d(Ks + pn * kChunk * 64, &p.tm_k, hk * DK + pn * 64, (int)tok0, &bar);
-    for (int vb = 0; vb < (TOUT ? 0 : nvb); ++vb)
-      tma_load_2d(Vs + vb * kChunk * 64, &p.tm_v, h * p.Dv + vb * 64, (int)tok0, &bar);
   }
-  if (threadIdx.x < 2 * kChunk) {
-    const int t = threadIdx.x & 63;
-    load_vec64(bsrc + (threadIdx.x < kChunk ? 0 : 64), threadIdx.x < kChunk ? p.beta : p.g,
-               tok0, L, p.Hv, h, t);
-  }
-  cp_async_commit();
+  __syncthreads();  // the mbarrier is initialised before the first copy signals it
+  issue_loads(u, cr);
   if constexpr (TOUT) {
     if (warp == 0) tmem_alloc(&tmem_slot, 128);
     if (threadIdx.x == 0) {
@@ -321,21 +336,27 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
     }
     tc_fence_before();
   }
-  __syncthreads();  // the mbarrier is initialised before anyone waits on it
+  __syncthreads();  // the MMA barrier and the TMEM columns are set up
+  uint32_t ld_phase = 0;
+  for (; u < units;) {
+  const int64_t slot = u / p.Hv;
+  const int h = (int)(u % p.Hv);
+  const int hk = h / p.G;
+  const int L = cr.L;
+  const int64_t tok0 = cr.tok;
+  int64_t nu = units;  // the next chunk-head of this CTA
+  ChunkRef ncr{};
   {
-    const bool ok = mbar_wait(&bar, 0);
+    const bool ok = mbar_wait(&bar, ld_phase);
     cp_async_wait<0>();
     if (__syncthreads_or(!ok)) {
       if (threadIdx.x == 0) {
         atomicOr(&g_fwd_device_error, 1);
-        mbar_wait(&bar, 0);  // once more, bounded, for the copies in flight
+        mbar_wait(&bar, ld_phase);  // once more, bounded, for the copies in flight
       }
-      if constexpr (TOUT) {
-        tc_fence_after();
-        if (warp == 0) tmem_dealloc(tmem_slot, 128);
-      }
-      return;
+      break;
     }
+    ld_phase ^= 1u;
   }
 
   if (warp == 0) {
@@ -413,6 +434,8 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
         *reinterpret_cast<float2*>(As + i * kSA + j) = make_float2(bet[i] * k0, bet[i] * k1);
       }
   }
+  // the previous chunk-head's W-code and Tu image stores have read T and Tu
+  if (threadIdx.x == 0) tma_store_wait_read();
   __syncthreads();
 
   // ---- a3: T = (I + A)^-1, or its Neumann polynomial ----
@@ -441,12 +464,6 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
     st_bf16x2(TuL + swz<64>(i, j), b0, b1);
   }
   __syncthreads();
-  if constexpr (TOUT) {
-    // the Tu hi and lo images (contiguous in shared memory) for the fused scan
-    uint4* dst = reinterpret_cast<uint4*>(p.tu_img + (slot * p.Hv + h) * (2 * kChunk * kChunk));
-    const uint4* src = reinterpret_cast<const uint4*>(TuH);
-    for (int e = threadIdx.x; e < 2 * kChunk * kChunk * 2 / 16; e += kPrepThreads) dst[e] = src[e];
-  }
 
   // ---- a4: W = Tw K [64 x DK] (warp: 16 rows x DK/2 columns), hi and lo passes ----
   constexpr int NTW = DK / 16;
@@ -461,6 +478,9 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
     __syncthreads();
     tc_fence_after();
     if (threadIdx.x == 0) {
+      bulk_store_1d(p.tu_img + (slot * p.Hv + h) * (2 * kChunk * kChunk), TuH,
+                    2 * kChunk * kChunk * 2);
+      tma_store_commit();
       const uint64_t kd = sdesc(smem_u32(Ks), 8192, 1024);
       const uint64_t th = sdesc(smem_u32(TwH), 16, 1024), tl = sdesc(smem_u32(TwL), 16, 1024);
       constexpr uint32_t id = idesc(64, DK, 0, 1);
@@ -472,6 +492,9 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
     }
     if (!mbar_wait(&bar_mma, 1)) tc_failed = 1;
     tc_fence_after();
+    // K and beta, g are free: the next chunk-head's arrive during the rest of this one
+    nu = next_unit(u + gridDim.x, ncr);
+    if (nu < units) issue_loads(nu, ncr);
     const uint32_t tw = tmem + ((uint32_t)(32 * rt) << 16) + wc0;
     tmem_ld_frag_pair<4>(tw, *reinterpret_cast<float(*)[4][4]>(&wacc[0][0]), tw + 32,
                          *reinterpret_cast<float(*)[4][4]>(&wacc[4][0]));
@@ -481,6 +504,14 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
 
   // ---- a5: W QDQ over the whole [L, DK] tile ----
   if constexpr (WM != GDN_QDQ_NONE) {
+    // Dk = 128: the codes are staged with the 128-byte swizzle (16-byte chunk
+    // c of row i at c ^ (i % 8)), so a warp's eight rows fall in distinct banks,
+    // and leave through the swizzled tensor map
+    constexpr bool WSW = DK == 128;
+    static_assert(!WSW || (S::WST % 1024) == 0, "swizzled W-code staging is 1024-byte aligned");
+    auto wst_off = [&](int i, int col) {
+      return WSW ? i * DK + (((col >> 4) ^ (i & 7)) << 4) + (col & 15) : i * DK + col;
+    };
     float m = 0.f;
 #pragma unroll
     for (int nt = 0; nt < NTW; ++nt)
@@ -515,13 +546,13 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
           }
           c2 = (uint16_t)(c0 | (c1 << 8));
         }
-        *reinterpret_cast<uint16_t*>(Wst + i * DK + col) = c2;
+        *reinterpret_cast<uint16_t*>(Wst + wst_off(i, col)) = c2;
       }
     if (L == kChunk) {
       fence_proxy_async();
       __syncthreads();
       if (threadIdx.x == 0) {
-        tma_store_2d(&p.tm_wc, h * DK, (int)tok0, Wst);
+        tma_store_2d(WSW ? &p.tm_wc_sw : &p.tm_wc, h * DK, (int)tok0, Wst);
         tma_store_commit();
       }
     } else {
@@ -530,7 +561,7 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
       for (int i = threadIdx.x; i < L * CPR; i += kPrepThreads) {
         const int r = i / CPR, c16 = i % CPR;
         *reinterpret_cast<uint4*>(p.w_codes + ((tok0 + r) * p.Hv + h) * DK + c16 * 16) =
-            *reinterpret_cast<const uint4*>(Wst + r * DK + c16 * 16);
+            *reinterpret_cast<const uint4*>(Wst + wst_off(r, c16 * 16));
       }
     }
     if (threadIdx.x == 0) p.w_scales[slot * p.Hv + h] = sW;
@@ -580,6 +611,19 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
       }
     }
   }
+  if constexpr (TOUT) {
+    tc_fence_before();  // this chunk-head's TMEM reads precede the next one's products
+  } else {
+    nu = next_unit(u + gridDim.x, ncr);  // (none: one CTA per chunk-head)
+    if (nu < units) {
+      __syncthreads();  // K and V have been read
+      issue_loads(nu, ncr);
+    }
+  }
+  u = nu;
+  cr = ncr;
+  }  // chunk-heads of this CTA
+
   if (threadIdx.x == 0) tma_store_wait_all();
   if constexpr (TOUT) {
     tc_fence_before();
@@ -590,7 +634,7 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
     }
     __syncthreads();
     tc_fence_after();
-    if (warp == 0) tmem_dealloc(tmem, 128);
+    if (warp == 0) tmem_dealloc(tmem_slot, 128);
   }
 }
 
@@ -1338,9 +1382,16 @@ gdn_status launch_fused(const gdn_problem& p, const FwdParams& prm, const Dims& 
                         cudaStream_t st) {
   if (d.B * d.T > 0 && d.n_slots > 0) {
     gdn_status s = GDN_OK;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+      return GDN_ERR_CUDA;
+    // persistent: three CTAs per SM walk the chunk-heads
+    const int64_t units = d.n_slots * d.Hv;
+    const unsigned grid = (unsigned)std::min<int64_t>(units, 3 * (int64_t)sms);
     auto prep = [&](auto kern) {
       if (set_smem(kern, PrepSmemT<128>::BYTES) != GDN_OK) return GDN_ERR_CUDA;
-      kern<<<(unsigned)(d.n_slots * d.Hv), kPrepThreads, PrepSmemT<128>::BYTES, st>>>(prm);
+      kern<<<grid, kPrepThreads, PrepSmemT<128>::BYTES, st>>>(prm);
       return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
     };
     s = p.w_mode == GDN_QDQ_E4M3 ? prep(gdn_fwd_prep_kernel<128, GDN_QDQ_E4M3, true>)
@@ -1452,6 +1503,7 @@ gdn_status launch_fwd(const gdn_problem& p, const Dims& d, const void* q, const 
   prm.G = d.Hv / d.Hk;
   prm.N = (int)d.N;
   prm.nt_fixed = d.nt_fixed;
+  prm.n_slots = d.n_slots;
   prm.scale = p.scale;
   prm.block_v = p.block_v;
   prm.bv_log2 = p.block_v == 16 ? 4 : (p.block_v == 32 ? 5 : (p.block_v == 64 ? 6 : 7));
