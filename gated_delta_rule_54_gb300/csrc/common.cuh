@@ -7,6 +7,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "../../include/gdn_qdq.h"
 
 namespace gdn {
@@ -595,30 +597,52 @@ constexpr int kF32Tile = 64 * kSA * 4;  // bytes
 // T = (I + A)^-1 for a strictly lower-triangular fp32 A [64][kSA] in shared
 // memory, written to Ts (lower triangle and diagonal; the strictly upper part
 // of Ts is left undefined).  Blocked forward substitution: the four 16x16
-// diagonal blocks by right-looking substitution (one thread per column; after
-// x_j is known its contribution is pushed to all later rows, so the dependent
-// chain is 16 FMAs long), then T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32
+// diagonal blocks row by row (one thread per column, each row of A read as
+// four 16-byte loads), then T_10 = -T_11 A_10 T_00 and T_32 = -T_33 A_32
 // T_22, then the lower-left 32x32 block T_LL = -T_LR A_LL T_UL.  The block
 // products give each thread four consecutive columns (one 16-byte load of the
-// right operand per step).  The strictly upper part of As is scratch.  All
+// right operand per step) and read their row of the left operand as 16-byte
+// loads up front: the solve is bound by shared-memory wavefronts.  The strictly upper part of As is scratch.  All
 // NTHREADS threads of the CTA call this; it synchronizes internally and Ts is
 // complete on return.
 // ---------------------------------------------------------------------------
 template <int NTHREADS>
 __device__ __forceinline__ void solve_unit_lower64(float* As, float* Ts) {
   static_assert(NTHREADS == 256 || NTHREADS == 512, "thread count");
+  static_assert(kSA % 4 == 0, "rows of As, Ts start on 16 bytes");
   const int tid = threadIdx.x;
+  // row i of a [*, kSA] fp32 tile, columns c0 .. c0 + 4 N - 1, as N float4 loads
+  auto row4 = [](const float* base, int i, int c0, auto n, float* out) {
+    constexpr int N = decltype(n)::value;
+#pragma unroll
+    for (int q = 0; q < N; ++q) {
+      const float4 v = *reinterpret_cast<const float4*>(base + i * kSA + c0 + 4 * q);
+      out[4 * q] = v.x;
+      out[4 * q + 1] = v.y;
+      out[4 * q + 2] = v.z;
+      out[4 * q + 3] = v.w;
+    }
+  };
+  using I4 = std::integral_constant<int, 4>;
+  using I8 = std::integral_constant<int, 8>;
   if (tid < 64) {
+    // column cc of the inverse of diagonal block b, row by row: x_r = -sum_{j<r} A_rj x_j
+    // (x_j = 0 above the diagonal, x_cc = 1); row r of A read as float4s
     const int b = tid >> 4, cc = tid & 15;
     const float* Ab = As + (16 * b) * kSA + 16 * b;
-    float x[16], acc[16];
+    float x[16];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) acc[r] = 0.f;
+    for (int r = 0; r < 16; ++r) {
+      float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      x[j] = (j == cc) ? 1.f : ((j < cc) ? 0.f : -acc[j]);
-#pragma unroll
-      for (int r = j + 1; r < 16; ++r) acc[r] = fmaf(Ab[r * kSA + j], x[j], acc[r]);
+      for (int q = 0; q < (r + 3) / 4; ++q) {
+        const float4 a = *reinterpret_cast<const float4*>(Ab + r * kSA + 4 * q);
+        if (4 * q < r) s0 = fmaf(a.x, x[4 * q], s0);
+        if (4 * q + 1 < r) s1 = fmaf(a.y, x[4 * q + 1], s1);
+        if (4 * q + 2 < r) s0 = fmaf(a.z, x[4 * q + 2], s0);
+        if (4 * q + 3 < r) s1 = fmaf(a.w, x[4 * q + 3], s1);
+      }
+      x[r] = (r == cc) ? 1.f : ((r < cc) ? 0.f : -(s0 + s1));
     }
 #pragma unroll
     for (int r = 0; r < 16; ++r) Ts[(16 * b + r) * kSA + 16 * b + cc] = x[r];
@@ -627,16 +651,16 @@ __device__ __forceinline__ void solve_unit_lower64(float* As, float* Ts) {
   // X = A_10 T_00 -> As[0:16][16:32];  Y = A_32 T_22 -> As[32:48][48:64]
   if (tid < 128) {
     const int base = 32 * (tid >> 6), i = (tid >> 2) & 15, j0 = (tid & 3) * 4;
-    const float* a = As + (base + 16 + i) * kSA + base;
+    float a[16];
+    row4(As, base + 16 + i, base, I4{}, a);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
-      const float av = a[kk];
       const float4 t = *reinterpret_cast<const float4*>(Ts + (base + kk) * kSA + base + j0);
-      acc.x = fmaf(av, t.x, acc.x);
-      acc.y = fmaf(av, t.y, acc.y);
-      acc.z = fmaf(av, t.z, acc.z);
-      acc.w = fmaf(av, t.w, acc.w);
+      acc.x = fmaf(a[kk], t.x, acc.x);
+      acc.y = fmaf(a[kk], t.y, acc.y);
+      acc.z = fmaf(a[kk], t.z, acc.z);
+      acc.w = fmaf(a[kk], t.w, acc.w);
     }
     *reinterpret_cast<float4*>(As + (base + i) * kSA + base + 16 + j0) = acc;
   }
@@ -644,16 +668,16 @@ __device__ __forceinline__ void solve_unit_lower64(float* As, float* Ts) {
   // T_10 = -T_11 X;  T_32 = -T_33 Y
   if (tid < 128) {
     const int base = 32 * (tid >> 6), i = (tid >> 2) & 15, j0 = (tid & 3) * 4;
-    const float* t = Ts + (base + 16 + i) * kSA + base + 16;
+    float t[16];
+    row4(Ts, base + 16 + i, base + 16, I4{}, t);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int kk = 0; kk < 16; ++kk) {
-      const float tv = t[kk];
       const float4 x = *reinterpret_cast<const float4*>(As + (base + kk) * kSA + base + 16 + j0);
-      acc.x = fmaf(tv, x.x, acc.x);
-      acc.y = fmaf(tv, x.y, acc.y);
-      acc.z = fmaf(tv, x.z, acc.z);
-      acc.w = fmaf(tv, x.w, acc.w);
+      acc.x = fmaf(t[kk], x.x, acc.x);
+      acc.y = fmaf(t[kk], x.y, acc.y);
+      acc.z = fmaf(t[kk], x.z, acc.z);
+      acc.w = fmaf(t[kk], x.w, acc.w);
     }
     *reinterpret_cast<float4*>(Ts + (base + 16 + i) * kSA + base + j0) =
         make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
@@ -662,8 +686,9 @@ __device__ __forceinline__ void solve_unit_lower64(float* As, float* Ts) {
   // Z = A_LL T_UL -> As[0:32][32:64]; T_UL's upper block T_01 is zero (skipped)
   if (tid < 256) {
     const int i = tid >> 3, j0 = (tid & 7) * 4;
-    const float* a = As + (32 + i) * kSA;
     const bool upper_cols = j0 >= 16;
+    float a[32];
+    row4(As, 32 + i, 0, I8{}, a);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int kk = 0; kk < 32; ++kk) {
@@ -681,27 +706,28 @@ __device__ __forceinline__ void solve_unit_lower64(float* As, float* Ts) {
   // T_LL = -T_LR Z; rows i < 16 of T_LR end at column 16 (its upper block is undefined)
   if (tid < 256) {
     const int i = tid >> 3, j0 = (tid & 7) * 4;
-    const float* t = Ts + (32 + i) * kSA + 32;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     if (i < 16) {
+      float t[16];
+      row4(Ts, 32 + i, 32, I4{}, t);
 #pragma unroll
       for (int kk = 0; kk < 16; ++kk) {
-        const float tv = t[kk];
         const float4 z = *reinterpret_cast<const float4*>(As + kk * kSA + 32 + j0);
-        acc.x = fmaf(tv, z.x, acc.x);
-        acc.y = fmaf(tv, z.y, acc.y);
-        acc.z = fmaf(tv, z.z, acc.z);
-        acc.w = fmaf(tv, z.w, acc.w);
+        acc.x = fmaf(t[kk], z.x, acc.x);
+        acc.y = fmaf(t[kk], z.y, acc.y);
+        acc.z = fmaf(t[kk], z.z, acc.z);
+        acc.w = fmaf(t[kk], z.w, acc.w);
       }
     } else {
+      float t[32];
+      row4(Ts, 32 + i, 32, I8{}, t);
 #pragma unroll
       for (int kk = 0; kk < 32; ++kk) {
-        const float tv = t[kk];
         const float4 z = *reinterpret_cast<const float4*>(As + kk * kSA + 32 + j0);
-        acc.x = fmaf(tv, z.x, acc.x);
-        acc.y = fmaf(tv, z.y, acc.y);
-        acc.z = fmaf(tv, z.z, acc.z);
-        acc.w = fmaf(tv, z.w, acc.w);
+        acc.x = fmaf(t[kk], z.x, acc.x);
+        acc.y = fmaf(t[kk], z.y, acc.y);
+        acc.z = fmaf(t[kk], z.z, acc.z);
+        acc.w = fmaf(t[kk], z.w, acc.w);
       }
     }
     *reinterpret_cast<float4*>(Ts + (32 + i) * kSA + j0) =
