@@ -174,6 +174,23 @@ __device__ __forceinline__ void tp_cluster_sum(TpBwdSmem& S, const TpBwdParams& 
   }
 }
 
+// split cluster barrier: a CTA's shared-memory writes before its arrive are
+// visible to the cluster after the matching wait
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// a staged block whose column sums the cluster has not yet collected
+struct TpPending {
+  int64_t t0;
+  float* out;
+  int nt, h, hh, buf;
+  bool scalars, valid;
+};
+
 template <int RM>
 __global__ void __launch_bounds__(kBwThreads, 4) gdn_two_precision_bwd_kernel(const TpBwdParams p) {
   constexpr bool RQ = RM != GDN_QDQ_NONE;
@@ -193,6 +210,23 @@ __global__ void __launch_bounds__(kBwThreads, 4) gdn_two_precision_bwd_kernel(co
   float* scr = p.scratch + ((int64_t)blockIdx.y * gridDim.x + blockIdx.x) * p.scratch_floats;
   float* sclg = scr + p.scl_off;
   int buf = 0;
+  // The cluster sums of a staged block are collected one block later: the
+  // CTA sums go to csum[buf] and the CTA arrives on the cluster barrier; at
+  // the end of the next block it waits (by then every CTA has arrived), reads
+  // the cluster's sums and only then overwrites the other buffer, which every
+  // CTA finished reading before that arrival.
+  TpPending pend{};
+  auto finish_block = [&](int nt, int64_t t0, int h, int hh, float* out, bool scalars) {
+    __syncthreads();  // this block's per-warp terms are written
+    if (pend.valid) {
+      cluster_wait();
+      tp_cluster_sum(S, p, pend.buf, pend.nt, pend.t0, pend.h, pend.hh, pend.out, pend.scalars);
+    }
+    tp_cta_sum(S, buf, nt, scalars);
+    cluster_arrive();
+    pend = TpPending{t0, out, nt, h, hh, buf, scalars, true};
+    buf ^= 1;
+  };
 
   for (int64_t u = blockIdx.y; u < (int64_t)p.Hv * p.N; u += gridDim.y) {
     const int h = (int)(u % p.Hv), n = (int)(u / p.Hv);
@@ -316,11 +350,7 @@ __global__ void __launch_bounds__(kBwThreads, 4) gdn_two_precision_bwd_kernel(co
             *reinterpret_cast<float4*>(&S.red[warp][jj][kTpRows * lane]) =
                 make_float4(dq[0], dq[1], dq[2], dq[3]);
           }
-          __syncthreads();
-          tp_cta_sum(S, buf, nt, false);
-          cl.sync();
-          tp_cluster_sum(S, p, buf, nt, tw + sb, h, hh, p.dq, false);
-          buf ^= 1;
+          finish_block(nt, tw + sb, h, hh, p.dq, false);
         }
       }
 
@@ -472,11 +502,7 @@ __global__ void __launch_bounds__(kBwThreads, 4) gdn_two_precision_bwd_kernel(co
               if constexpr (RQ) dR[r][c] = a * fmaf(-b * sdR[c], kr[r], dR[r][c]);
             }
         }
-        __syncthreads();
-        tp_cta_sum(S, buf, nt, true);
-        cl.sync();
-        tp_cluster_sum(S, p, buf, nt, tw + sb, h, hh, p.dk, true);
-        buf ^= 1;
+        finish_block(nt, tw + sb, h, hh, p.dk, true);
       }
       // the window's read copy came from the anchor (straight through)
       if constexpr (RQ) {
@@ -496,6 +522,10 @@ __global__ void __launch_bounds__(kBwThreads, 4) gdn_two_precision_bwd_kernel(co
         *reinterpret_cast<float4*>(p.dh0 + sbase + (int64_t)r * p.Dv) =
             make_float4(dA[r][0], dA[r][1], dA[r][2], dA[r][3]);
     }
+  }
+  if (pend.valid) {
+    cluster_wait();
+    tp_cluster_sum(S, p, pend.buf, pend.nt, pend.t0, pend.h, pend.hh, pend.out, pend.scalars);
   }
   // the cluster's CTAs read each other's shared memory up to their last sums:
   // none may exit before all are done
