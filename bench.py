@@ -606,9 +606,29 @@ def run_ours(args, ws, rank, local):
 
 
 def cpu_baseline(w, cpu, bwd, budget_s=20.0):
-    """The fp64 chunked oracle, as it stands, on whole sequences of the workload
-    (all heads), until the budget is used; tokens/s scaled from the sample."""
+    """The oracle, as it stands, on whole sequences of the workload (all heads),
+    until the budget is used; tokens/s scaled from the sample.  Forward and
+    backward: the fp64 chunked form with autograd.  Forward only: the fp64 token
+    recurrence (C, OpenMP over (sequence, value head); it has no W site, so the
+    state QDQ is its only quantizer)."""
     from oracle.chunked import chunked
+    if not bwd:
+        import oracle
+        t0 = time.time()
+        done = 0
+        for n in range(w.B):
+            sl = slice(n, n + 1)
+            oracle.recurrent(*[cpu[x][sl] for x in ("q", "k", "v", "beta", "g")],
+                             cpu["h0"][sl] if cpu["h0"] is not None else None,
+                             state_mode=w.state_mode)
+            done += 1
+            if time.time() - t0 > budget_s * 0.5:
+                break
+        dt = time.time() - t0
+        return {"value": round(done * w.T / dt, 2), "unit": "tokens/s",
+                "cores": oracle.num_threads(), "kind": "oracle",
+                "sample": "%d of %d sequences (T=%d, all %d heads), fp64 token recurrence "
+                          "(C, OpenMP)" % (done, w.B, w.T, w.Hv)}
     t0 = time.time()
     done = 0
     for n in range(w.B):
@@ -1204,13 +1224,15 @@ def run_reference(args, ws, rank):
     cpu = synth.make_inputs(ws_)
     xs = [cpu[x] for x in ("q", "k", "v", "beta", "g", "h0")]
 
+    import oracle
+
     def step():
         if bwd:
             ys = [a.double().requires_grad_(True) if a is not None else None for a in xs]
             o, ht = chunked(*ys, state_mode=w.state_mode, w_mode=w.w_mode)
             (o.sum() + ht.sum()).backward()
-        else:
-            chunked(*xs, state_mode=w.state_mode, w_mode=w.w_mode)
+        else:  # the forward baseline: the fp64 token recurrence in C
+            oracle.recurrent(*xs, state_mode=w.state_mode)
 
     for _ in range(args.warmup):
         step()
@@ -1219,8 +1241,9 @@ def run_reference(args, ws, rank):
         step()
     dt = time.time() - t0
     value = T_s * args.steps / dt
-    sample = "1 sequence x %d tokens, all %d heads per step (fp64 chunked oracle %s)" % (
-        T_s, w.Hv, "fwd+autograd bwd" if bwd else "fwd")
+    sample = "1 sequence x %d tokens, all %d heads per step (%s)" % (
+        T_s, w.Hv, "fp64 chunked oracle, fwd+autograd bwd" if bwd
+        else "fp64 token recurrence, C with OpenMP over (sequence, head)")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s",
             "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt * 1e3 / args.steps, 3), "higher_is_better": True,
@@ -1229,7 +1252,7 @@ def run_reference(args, ws, rank):
                        "Hv": w.Hv, "Dk": w.Dk, "Dv": w.Dv, "state_mode": w.state_mode,
                        "w_mode": w.w_mode},
             "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s",
-                             "cores": torch.get_num_threads(), "kind": "oracle", "sample": sample},
+                             "cores": torch.get_num_threads() if bwd else oracle.num_threads(), "kind": "oracle", "sample": sample},
             "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
