@@ -447,19 +447,24 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
   // ---- a4 operands: Tw = T diag(beta e^gamma), Tu = T diag(beta), split hi/lo;
   //      T itself as the backward's tile image ----
   __nv_bfloat16* timg = p.tb ? p.tb + (slot * p.Hv + h) * (kTileImgBytes / 2) : nullptr;
+  // a thread keeps its column pair j, j + 1 (the row advances by 8 per pass):
+  // its diagonal factors are read once
+  static_assert(kPrepThreads % 32 == 0, "column pair fixed per thread");
+  const int jc = (threadIdx.x & 31) * 2;
+  const float bw0 = beg[jc], bw1 = beg[jc + 1], bu0 = bet[jc], bu1 = bet[jc + 1];
   for (int e = threadIdx.x; e < 64 * 32; e += kPrepThreads) {
-    const int i = e >> 5, j = (e & 31) * 2;
+    const int i = e >> 5, j = jc;
     const float2 tt = *reinterpret_cast<const float2*>(Ts + i * kSA + j);
     const float t0 = (j <= i) ? tt.x : 0.f;
     const float t1 = (j + 1 <= i) ? tt.y : 0.f;
     if (timg) st_bf16x2(timg + swz<64>(i, j), t0, t1);
     float a0, a1, b0, b1;
-    split_bf16(t0 * beg[j], a0, b0);
-    split_bf16(t1 * beg[j + 1], a1, b1);
+    split_bf16(t0 * bw0, a0, b0);
+    split_bf16(t1 * bw1, a1, b1);
     st_bf16x2(TwH + swz<64>(i, j), a0, a1);
     st_bf16x2(TwL + swz<64>(i, j), b0, b1);
-    split_bf16(t0 * bet[j], a0, b0);
-    split_bf16(t1 * bet[j + 1], a1, b1);
+    split_bf16(t0 * bu0, a0, b0);
+    split_bf16(t1 * bu1, a1, b1);
     st_bf16x2(TuH + swz<64>(i, j), a0, a1);
     st_bf16x2(TuL + swz<64>(i, j), b0, b1);
   }
