@@ -683,55 +683,63 @@ __device__ __forceinline__ void solve_unit_lower64(float* As, float* Ts) {
         make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
   }
   __syncthreads();
-  // Z = A_LL T_UL -> As[0:32][32:64]; T_UL's upper block T_01 is zero (skipped)
-  if (tid < 256) {
+  // Z = A_LL T_UL -> As[0:32][32:64]; T_UL's upper block T_01 is zero (skipped).
+  // A thread computes rows i and i + 16 at four columns: each 16-byte load of
+  // T serves both rows.
+  if (tid < 128) {
     const int i = tid >> 3, j0 = (tid & 7) * 4;
     const bool upper_cols = j0 >= 16;
-    float a[32];
-    row4(As, 32 + i, 0, I8{}, a);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 c0 = make_float4(0.f, 0.f, 0.f, 0.f), c1 = c0;
 #pragma unroll
-    for (int kk = 0; kk < 32; ++kk) {
-      const float av = (kk < 16 && upper_cols) ? 0.f : a[kk];
-      float4 t = *reinterpret_cast<const float4*>(Ts + kk * kSA + j0);
-      if (kk < 16 && upper_cols) t = make_float4(0.f, 0.f, 0.f, 0.f);
-      acc.x = fmaf(av, t.x, acc.x);
-      acc.y = fmaf(av, t.y, acc.y);
-      acc.z = fmaf(av, t.z, acc.z);
-      acc.w = fmaf(av, t.w, acc.w);
-    }
-    *reinterpret_cast<float4*>(As + i * kSA + 32 + j0) = acc;
-  }
-  __syncthreads();
-  // T_LL = -T_LR Z; rows i < 16 of T_LR end at column 16 (its upper block is undefined)
-  if (tid < 256) {
-    const int i = tid >> 3, j0 = (tid & 7) * 4;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (i < 16) {
-      float t[16];
-      row4(Ts, 32 + i, 32, I4{}, t);
+    for (int half = 0; half < 2; ++half) {  // K columns 16 half .. + 15
+      if (half == 0 && upper_cols) continue;
+      float a0[16], a1[16];
+      row4(As, 32 + i, 16 * half, I4{}, a0);
+      row4(As, 48 + i, 16 * half, I4{}, a1);
 #pragma unroll
       for (int kk = 0; kk < 16; ++kk) {
-        const float4 z = *reinterpret_cast<const float4*>(As + kk * kSA + 32 + j0);
-        acc.x = fmaf(t[kk], z.x, acc.x);
-        acc.y = fmaf(t[kk], z.y, acc.y);
-        acc.z = fmaf(t[kk], z.z, acc.z);
-        acc.w = fmaf(t[kk], z.w, acc.w);
-      }
-    } else {
-      float t[32];
-      row4(Ts, 32 + i, 32, I8{}, t);
-#pragma unroll
-      for (int kk = 0; kk < 32; ++kk) {
-        const float4 z = *reinterpret_cast<const float4*>(As + kk * kSA + 32 + j0);
-        acc.x = fmaf(t[kk], z.x, acc.x);
-        acc.y = fmaf(t[kk], z.y, acc.y);
-        acc.z = fmaf(t[kk], z.z, acc.z);
-        acc.w = fmaf(t[kk], z.w, acc.w);
+        const float4 t = *reinterpret_cast<const float4*>(Ts + (16 * half + kk) * kSA + j0);
+        c0.x = fmaf(a0[kk], t.x, c0.x);
+        c0.y = fmaf(a0[kk], t.y, c0.y);
+        c0.z = fmaf(a0[kk], t.z, c0.z);
+        c0.w = fmaf(a0[kk], t.w, c0.w);
+        c1.x = fmaf(a1[kk], t.x, c1.x);
+        c1.y = fmaf(a1[kk], t.y, c1.y);
+        c1.z = fmaf(a1[kk], t.z, c1.z);
+        c1.w = fmaf(a1[kk], t.w, c1.w);
       }
     }
-    *reinterpret_cast<float4*>(Ts + (32 + i) * kSA + j0) =
-        make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    *reinterpret_cast<float4*>(As + i * kSA + 32 + j0) = c0;
+    *reinterpret_cast<float4*>(As + (i + 16) * kSA + 32 + j0) = c1;
+  }
+  __syncthreads();
+  // T_LL = -T_LR Z; rows i < 16 of T_LR end at column 16 (its upper block is
+  // undefined); a thread computes rows i and i + 16
+  if (tid < 128) {
+    const int i = tid >> 3, j0 = (tid & 7) * 4;
+    float4 c0 = make_float4(0.f, 0.f, 0.f, 0.f), c1 = c0;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {  // K rows 16 half .. + 15 of Z
+      float t0[16], t1[16];
+      if (half == 0) row4(Ts, 32 + i, 32, I4{}, t0);
+      row4(Ts, 48 + i, 32 + 16 * half, I4{}, t1);
+#pragma unroll
+      for (int kk = 0; kk < 16; ++kk) {
+        const float4 z = *reinterpret_cast<const float4*>(As + (16 * half + kk) * kSA + 32 + j0);
+        if (half == 0) {
+          c0.x = fmaf(t0[kk], z.x, c0.x);
+          c0.y = fmaf(t0[kk], z.y, c0.y);
+          c0.z = fmaf(t0[kk], z.z, c0.z);
+          c0.w = fmaf(t0[kk], z.w, c0.w);
+        }
+        c1.x = fmaf(t1[kk], z.x, c1.x);
+        c1.y = fmaf(t1[kk], z.y, c1.y);
+        c1.z = fmaf(t1[kk], z.z, c1.z);
+        c1.w = fmaf(t1[kk], z.w, c1.w);
+      }
+    }
+    *reinterpret_cast<float4*>(Ts + (32 + i) * kSA + j0) = make_float4(-c0.x, -c0.y, -c0.z, -c0.w);
+    *reinterpret_cast<float4*>(Ts + (48 + i) * kSA + j0) = make_float4(-c1.x, -c1.y, -c1.z, -c1.w);
   }
   __syncthreads();
 }
