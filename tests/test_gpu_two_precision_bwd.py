@@ -158,3 +158,33 @@ def test_two_precision_bwd_full_size_sampled_head():
         r = _grads_oracle(sub, do[:1, :, h:h + 1], dht[:1, h:h + 1], "e4m3", 16, 1.0)
         gs = [x[:1, :, h:h + 1] for x in g[:5]] + [g[5][:1, h:h + 1]]
         _compare(gs, r, "e4m3", "full size, head %d:" % h)
+
+
+def _random_case(seed):
+    rng = np.random.default_rng(1000 + seed)
+    Dv = int(rng.choice([64, 128]))
+    Hk = int(rng.choice([1, 2]))
+    Hv = Hk * int(rng.choice([1, 2]))
+    packed = bool(rng.integers(2))
+    flush = int(rng.choice([1, 2, 3, 4, 7, 16, 17, 40, 64, 100, 256]))
+    rm = str(rng.choice(["e4m3", "none"]))
+    if packed:
+        lengths = [int(x) for x in rng.integers(0, 90, size=int(rng.integers(1, 5)))]
+        w = synth.small(B=1, T=0, Hk=Hk, Hv=Hv, Dk=128, Dv=Dv, w_mode="none", h0=True,
+                        seed=200 + seed)
+    else:
+        lengths = None
+        w = synth.small(B=int(rng.integers(1, 3)), T=int(rng.integers(1, 140)), Hk=Hk, Hv=Hv,
+                        Dk=128, Dv=Dv, w_mode="none", h0=True, seed=200 + seed)
+    return w, lengths, rm, flush, float(rng.choice([1.0, 0.125])), bool(rng.integers(2)), \
+        bool(rng.integers(2))
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_two_precision_bwd_randomized(seed):
+    """Seeded random mixes of shapes, flush periods (1 .. 256), packed lengths
+    (zeros included), grouped heads, read modes, scale and present / absent h0
+    and dht, each against the oracle's autograd."""
+    w, lengths, rm, flush, scale, h0, dht = _random_case(seed)
+    _check(w, lengths=lengths, rm=rm, flush=flush, scale=scale, h0=h0, with_dht=dht,
+           seed=300 + seed)
