@@ -187,3 +187,36 @@ def test_autograd_op_matches_the_oracle_gradients():
         assert x.grad.dtype == x.dtype and torch.isfinite(gx).all()
         # bf16 gradients of q, k, v add a 2^-9 relative rounding to the STE bound
         assert rel <= GRAD_L2 + (2.0 ** -8 if x.dtype == torch.bfloat16 else 0.0), (n, rel)
+
+
+def _random_case(seed):
+    rng = np.random.default_rng(2000 + seed)
+    Dk = int(rng.choice([64, 128]))
+    Dv = int(rng.choice([64, 128]))
+    Hk = int(rng.choice([1, 2]))
+    Hv = Hk * int(rng.choice([1, 2]))
+    sm, wm = MODES[int(rng.integers(len(MODES)))]
+    block_v = int(rng.choice([16, 32, 64] + ([128] if Dv == 128 else [])))
+    packed = bool(rng.integers(2))
+    if packed:
+        lengths = [int(x) for x in rng.integers(0, 160, size=int(rng.integers(1, 5)))]
+        if sum(lengths) == 0:
+            lengths[0] = 1
+        w = synth.small(B=1, T=0, Hk=Hk, Hv=Hv, Dk=Dk, Dv=Dv, state_mode=sm, w_mode=wm, h0=True,
+                        seed=400 + seed)
+    else:
+        lengths = None
+        w = synth.small(B=int(rng.integers(1, 3)), T=int(rng.integers(1, 200)), Hk=Hk, Hv=Hv,
+                        Dk=Dk, Dv=Dv, state_mode=sm, w_mode=wm, h0=bool(rng.integers(2)),
+                        seed=400 + seed)
+    return w, lengths, block_v, float(rng.choice([1.0, Dk ** -0.5])), bool(rng.integers(2))
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_bwd_randomized(seed):
+    """Seeded random mixes of head dims, grouped heads, both QDQ sites' modes,
+    state-scale widths, packed lengths (empty sequences included), scale and
+    dht presence: every gradient within the relative L2 bound of the oracle's
+    autograd (this covers the tensor-core and the warp-level paths alike)."""
+    w, lengths, block_v, scale, with_dht = _random_case(seed)
+    _check(w, lengths=lengths, scale=scale, with_dht=with_dht, block_v=block_v)
