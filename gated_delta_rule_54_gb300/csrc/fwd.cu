@@ -392,10 +392,11 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
   zero_acc(acc);
   uint32_t tmem = 0;
   if constexpr (TOUT) {
-    // K K^T: M = 64, N = 64, K = DK (K-major panels), one commit
+    // K K^T: M = 64, N = 64, K = DK (K-major panels), one commit; issued from
+    // warp 1 so that it starts while warp 0 forms gamma
     tc_fence_after();
     tmem = tmem_slot;
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 32) {
       const uint64_t kd = sdesc(smem_u32(Ks), 16, 1024);
       constexpr uint32_t id = idesc(64, 64, 0, 0);
 #pragma unroll
