@@ -151,10 +151,11 @@ __device__ __forceinline__ float ex2_approx_f(float x) {
 }
 constexpr float kLog2eF = 1.4426950408889634f;
 
+// Maximum over the warp of non-negative, non-NaN values (every caller passes
+// maxima of |x| seeded with 0): such floats order like their bit patterns, so
+// one integer max reduction gives the exact result.
 __device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-  return v;
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
 }
 
 // ---------------------------------------------------------------------------
