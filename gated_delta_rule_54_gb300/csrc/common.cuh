@@ -387,6 +387,17 @@ __device__ __forceinline__ void tma_store_wait_all() {
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
 }
+// Programmatic dependent launch.  launch_dependents lets the next kernel of the
+// stream, when it was launched with programmatic stream serialization, be
+// scheduled before this one ends; grid_dep_wait (a no-op in a kernel launched
+// without it) returns once the preceding kernel has completed and its memory
+// operations are visible.
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;\n" ::: "memory");
+}
 
 }  // namespace gdn
 

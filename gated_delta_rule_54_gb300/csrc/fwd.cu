@@ -273,6 +273,9 @@ __global__ void __launch_bounds__(kPrepThreads, TOUT ? 3 : 2) gdn_fwd_prep_kerne
   // current one (K is free once W = Tw K has run).  The other variant has one
   // CTA per chunk-head.
   const int64_t units = p.n_slots * p.Hv;
+  // the fused scan that follows may take the SMs this CTA leaves (it waits for
+  // the whole grid before reading any output of it)
+  if constexpr (TOUT) grid_dep_launch();
   // the next chunk-head at or after u that holds tokens (units if none)
   auto next_unit = [&](int64_t u, ChunkRef& r) {
     for (; u < units; u += gridDim.x)

@@ -12,22 +12,28 @@
 //   O = scale (diag(e^gamma) Q H^ + (lower-incl(e^{gamma_i-gamma_j} q_i.k_j)) Delta);
 //   H <- e^{gamma_L} H^ + (diag(e^{gamma_L - gamma}) K)^T Delta.
 //
-// One CTA (8 warps) per (sequence, value head, 64-column value block) walks
-// its chunks.  Everything is M = 128 tcgen05 products of bf16 operands:
+// One CTA (16 epilogue warps + 1 producer warp) per (sequence, value head,
+// 64-column value block) walks its chunks.  Everything is M = 128 tcgen05
+// products of bf16 operands:
 //   D3 = [Tu_hi ; *] V + [Tu_lo ; *] V            rows 0-63: U
 //   D4 = [W^ ; Q] K^T                             rows 64-127: QK^T -> P
 //   D1 = [W^ ; Q] H^                              rows 0-63: W^ H^, rows 64-127: Q H^
-//   D2 = K^T Delta'_hi + K^T Delta'_lo            the state update (M = Dk)
-//   D5 = [* ; P_hi] Delta_hi + [* ; P_hi] Delta_lo + [* ; P_lo] Delta_hi
-//                                                 rows 64-127: P Delta
+//   D2 = K^T [Delta'_hi | Delta'_lo]              N = 128; the state update (M = Dk)
+//                                                 is the sum of its two column halves
+//   D5 = [* ; P_hi] [Delta_hi | Delta_lo] + [* ; P_lo] Delta_hi (into columns 0-63)
+//                                                 rows 64-127: P Delta, again the sum
+//                                                 of the two column halves
 // (a "*" half reads whatever lies next to the operand in shared memory: those
-// accumulator rows are never read).  Quantized W and H enter as their codes
+// accumulator rows are never read).  A [hi | lo] operand is one N = 128 B
+// operand: its halves lie a panel stride apart, so one product reads the A
+// tile once for both.  Quantized W and H enter as their codes
 // (E4M3 values and INT8 integers are exact in bf16) with the scales applied in
 // the epilogues; operands that are not bf16-exact (T diag(beta), P, Delta,
 // the decayed Delta) are split into hi + lo bf16 halves, so the products keep
-// about 16 mantissa bits.  Thread r (TMEM lane r) of each warp pair holds 32
-// columns of accumulator row r; the fp32 state row dk of this value block
-// lives in the registers of the two threads of lane dk.
+// about 16 mantissa bits.  The four warps of TMEM lane quadrant q each read 16
+// columns of accumulator rows 32q .. 32q + 31 (one row per thread); the fp32
+// state row dk of this value block lives in the registers of the four threads
+// of lane dk.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -63,8 +69,9 @@ struct FSmem {
   static_assert(BYTES <= 232448, "shared memory budget");
 };
 
-// TMEM accumulator columns: D1 and D5 double buffered (chunk parity)
-constexpr uint32_t kD1 = 0, kD2 = 128, kD3 = 192, kD4 = 256, kD5 = 320, kTmemCols = 512;
+// TMEM accumulator columns: D1 double buffered (chunk parity); D2 and D5 are
+// N = 128 products
+constexpr uint32_t kD1 = 0, kD2 = 128, kD3 = 256, kD4 = 320, kD5 = 384, kTmemCols = 512;
 
 // bytes of the copy groups of one chunk
 constexpr uint32_t kVtTx = 8192 + 16384 + 8192;  // V block, Tu images, W codes
@@ -75,6 +82,9 @@ constexpr uint32_t kQTx = 2 * 8192;           // Q (2 boxes)
 constexpr uint32_t kIdKK = idesc(128, 64, 0, 0);  // A K-major, B K-major
 constexpr uint32_t kIdKM = idesc(128, 64, 0, 1);  // A K-major, B MN-major
 constexpr uint32_t kIdMM = idesc(128, 64, 1, 1);  // A MN-major, B MN-major
+// N = 128: a B operand of two 64-column panels 8 KB apart ([hi | lo] halves)
+constexpr uint32_t kIdKM2 = idesc(128, 128, 0, 1);
+constexpr uint32_t kIdMM2 = idesc(128, 128, 1, 1);
 
 // barrier among the epilogue warps only (the producer warp does not take part),
 // returning whether any of them passed v = true
@@ -257,10 +267,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
           umma(tmem + kD3, dadd(atu, 8192 + ks * 32), dadd(vt, ks * 2048), kIdKM, true);
         umma_commit(&b_u);
       };
-      load_vt(0);
       load_kw(0);
-      load_cv(0);
       load_q(0);
+      // the chunk prep's outputs (Tu images, W codes, chunk vectors) are complete
+      grid_dep_wait();
+      load_vt(0);
+      load_cv(0);
       bad |= !mbar_wait(&in_vt[0], 0);
       tc_fence_after();
       if (!bad) issue_u(0);
@@ -302,25 +314,23 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
           bad |= !mbar_wait(&b_d4, ph);
           if (!bad) load_q(c + 1);
         }
-        // D2 = K^T Delta'_hi + K^T Delta'_lo (A: K tile read MN-major, M = dk)
+        // D2 = K^T [Delta'_hi | Delta'_lo] (A: K tile read MN-major, M = dk)
         bad |= !mbar_wait(&e_dl, ph);
         if (bad) break;
         tc_fence_after();
         const uint64_t dp = sdesc(smem_u32(DP), 8192, 1024), dd = sdesc(smem_u32(DD), 8192, 1024);
         const uint64_t ap = sdesc(smem_u32(AP), 16, 1024), ktm = sdesc(smem_u32(KTb(b)), 8192, 1024);
+        // one N = 128 product: K^T Delta'_hi in columns 0-63, K^T Delta'_lo in 64-127
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          umma(tmem + kD2, dadd(ktm, ks * 2048), dadd(dp, ks * 2048), kIdMM, ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          umma(tmem + kD2, dadd(ktm, ks * 2048), dadd(dp, 8192 + ks * 2048), kIdMM, true);
+          umma(tmem + kD2, dadd(ktm, ks * 2048), dadd(dp, ks * 2048), kIdMM2, ks > 0);
         umma_commit(&b_s);
         // chunk vectors of the next chunk once the outputs of chunk c - 1 are stored
         if (more) {
           if (c >= 1) bad |= !mbar_wait(&e_out, ph ^ 1u);
           if (!bad) load_cv(c + 1);
         }
-        // D5 = [P_lo ; P_hi] Delta_hi + [P_lo ; P_hi] Delta_lo + [P_hi ; P_lo] Delta_hi
+        // D5 = [P_lo ; P_hi] [Delta_hi | Delta_lo] + [P_hi ; P_lo] Delta_hi
         bad |= !mbar_wait(&e_p, ph);
         if (bad) break;
         tc_fence_after();
@@ -329,13 +339,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
           bulk_store_1d(static_cast<unsigned char*>(p.pb) + sh_of(c) * 8192, AP + 8192, 8192);
           tma_store_commit();
         }
-        const uint32_t d5 = tmem + kD5 + 64 * (c & 1);
+        // [P_lo ; P_hi] [Delta_hi | Delta_lo] as one N = 128 product, then
+        // [P_hi ; P_lo] Delta_hi into columns 0-63.  The P epilogue of chunk c + 1
+        // reads D5(c) before it signals, so one buffer serves.
+        const uint32_t d5 = tmem + kD5;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          umma(d5, dadd(ap, ks * 32), dadd(dd, ks * 2048), kIdKM, ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          umma(d5, dadd(ap, ks * 32), dadd(dd, 8192 + ks * 2048), kIdKM, true);
+          umma(d5, dadd(ap, ks * 32), dadd(dd, ks * 2048), kIdKM2, ks > 0);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
           umma(d5, dadd(ap, 8192 + ks * 32), dadd(dd, ks * 2048), kIdKM, true);
@@ -368,6 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
         hv[j + 3] = x.w;
       }
     }
+    grid_dep_wait();  // the W scales below are the chunk prep's
     auto amax_partial = [&]() {
       float m = 0.f;
 #pragma unroll
@@ -403,7 +414,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
       const int Lc = min(L - c * kChunk, kChunk);
       const float* cv = CVb(c & 1);
       float qh[16], pd[16];
-      tmem_ld16_pair(tl + kD1 + 64 * (c & 1), qh, tl + kD5 + 64 * (c & 1), pd);
+      {
+        float pl[16];
+        tmem_ld16_pair(tl + kD5, pd, tl + kD5 + 64, pl);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pd[j] += pl[j];
+      }
+      tmem_ld16(tl + kD1 + 64 * (c & 1), qh);
       if (t_row < Lc) {
         const float ei = cv[kCvEg + t_row] * sH;
         float* dst = p.o + ((tok0 + (int64_t)c * kChunk + t_row) * p.Hv + h) * 128 + vb * 64 + col0;
@@ -548,11 +565,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
       bad |= !mbar_wait(&b_s, ph);
       tc_fence_after();
       {
-        float z[16];
-        tmem_ld16(tl + kD2, z);
+        float z[16], zl[16];
+        tmem_ld16_pair(tl + kD2, z, tl + kD2 + 64, zl);
         const float egL = cv[kCvEg + 63];  // gamma is flat past the last valid row
 #pragma unroll
-        for (int j = 0; j < 16; ++j) hv[j] = hv[j] * egL + z[j];
+        for (int j = 0; j < 16; ++j) hv[j] = hv[j] * egL + (z[j] + zl[j]);
         amax_partial();
       }
       tc_fence_before();
@@ -602,8 +619,19 @@ gdn_status launch_fused_scan(const FusedParams& p, int state_mode, int w_mode, c
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FSmem::BYTES) !=
         cudaSuccess)
       return GDN_ERR_CUDA;
-    kern<<<grid, kThreads, FSmem::BYTES, st>>>(p);
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    // programmatic stream serialization: CTAs take the SMs the chunk prep
+    // leaves, set up and load their first K and Q, then wait for the prep
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = FSmem::BYTES;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
   };
   if (state_mode == GDN_QDQ_E4M3 && w_mode == GDN_QDQ_E4M3)
     return run(gdn_fwd_fused_kernel<GDN_QDQ_E4M3, GDN_QDQ_E4M3>);
