@@ -60,8 +60,8 @@ struct FSmem {
   static constexpr int VT = KT + 2 * 16384;        // 2 buffers x V block [64 tok][64 v] bf16
   static constexpr int WC = VT + 2 * 8192;         // 2 buffers x W codes [64][128] u8
   static constexpr int ATU = WC + 2 * 8192;        // 2 buffers x Tu hi, Tu lo images; buffer 1 ...
-  static constexpr int AP = ATU + 2 * 16384;       // ... then P lo, P hi, P lo
-  static constexpr int HB = AP + 24576;            // H^ codes as bf16 [128 dk][64 v]
+  static constexpr int AP = ATU + 2 * 16384;       // ... then P lo, P hi
+  static constexpr int HB = AP + 16384;            // H^ codes as bf16 [128 dk][64 v]
   static constexpr int DP = HB + 16384;            // decayed Delta hi, lo [64 tok][64 v]
   static constexpr int DD = DP + 16384;            // Delta hi, lo
   static constexpr int CV = DD + 16384;            // 2 buffers x chunk vectors (1280 B)
@@ -330,7 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
           if (c >= 1) bad |= !mbar_wait(&e_out, ph ^ 1u);
           if (!bad) load_cv(c + 1);
         }
-        // D5 = [P_lo ; P_hi] [Delta_hi | Delta_lo] + [P_hi ; P_lo] Delta_hi
+        // D5 = [P_lo ; P_hi] [Delta_hi | Delta_lo] + [* ; P_lo] Delta_hi
         bad |= !mbar_wait(&e_p, ph);
         if (bad) break;
         tc_fence_after();
@@ -340,7 +340,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
           tma_store_commit();
         }
         // [P_lo ; P_hi] [Delta_hi | Delta_lo] as one N = 128 product, then
-        // [P_hi ; P_lo] Delta_hi into columns 0-63.  The P epilogue of chunk c + 1
+        // [* ; P_lo] Delta_hi into columns 0-63 (the A tile starts one panel
+        // below P_lo, in the second Tu buffer, so its rows 64-127 are P_lo).  The P epilogue of chunk c + 1
         // reads D5(c) before it signals, so one buffer serves.
         const uint32_t d5 = tmem + kD5;
 #pragma unroll
@@ -348,7 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
           umma(d5, dadd(ap, ks * 32), dadd(dd, ks * 2048), kIdKM2, ks > 0);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
-          umma(d5, dadd(ap, 8192 + ks * 32), dadd(dd, ks * 2048), kIdKM, true);
+          umma(d5, dadd(ap, ks * 32) - (8192 >> 4), dadd(dd, ks * 2048), kIdKM, true);
         umma_commit(&b_o);
         // U of the next chunk (the Delta epilogue of chunk c has read D3(c))
         if (more) {
@@ -502,12 +503,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
           const int j = col0 + jj;
           x[jj] = (j <= t_row) ? ex2_approx((gi - cv[kCvGam + j]) * kLog2e) * x[jj] : 0.f;
         }
-        // [P_lo | P_hi | P_lo]: hi at +8 KB, lo at 0 and +16 KB
+        // [P_lo | P_hi]: lo at 0, hi at +8 KB
         st16_split(AP + 8192, AP, t_row, col0, x);
-        *reinterpret_cast<uint4*>(AP + 16384 + sw_off(t_row, col0)) =
-            *reinterpret_cast<const uint4*>(AP + sw_off(t_row, col0));
-        *reinterpret_cast<uint4*>(AP + 16384 + sw_off(t_row, col0 + 8)) =
-            *reinterpret_cast<const uint4*>(AP + sw_off(t_row, col0 + 8));
         if (p.pb && vb == 0 && Lc < kChunk) {  // a partial chunk: rows past its end zero
           unsigned char* pimg = reinterpret_cast<unsigned char*>(p.pb) + (slot * p.Hv + h) * 8192;
           float z[16];
@@ -554,11 +551,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
         if (lane == 0) mbar_arrive(&e_dl);
       }
 
-      // ---- the next chunk's W^, while D2 runs: [W^ ; Q] is free once D1 and D4 are done ----
-      if (c + 1 < nch) {
+      // ---- the next chunk's W^, while D2 runs: [W^ ; Q] is free once D1 and D4 are done.
+      // The warps of rows 64-127 convert it: the other half is on the chain
+      // (Delta -> D2 -> state) ----
+      if (c + 1 < nch && !lo_rows) {
         bad |= !mbar_wait(&b_d4, ph);
         bad |= !mbar_wait(&in_vt[b ^ 1], (uint32_t)((c + 1) >> 1) & 1u);
-        convert_w(c + 1, tid, kEpiThreads);
+        convert_w(c + 1, ((warp >> 2) * 2 + (warp & 1)) * 32 + lane, kEpiThreads / 2);
       }
 
       // ---- a9: H <- e^{gamma_L} H^ + K~^T Delta ----
