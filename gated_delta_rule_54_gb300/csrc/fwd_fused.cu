@@ -15,7 +15,9 @@
 // One CTA (16 epilogue warps + 1 producer warp) per (sequence, value head,
 // 64-column value block) walks its chunks.  Everything is M = 128 tcgen05
 // products of bf16 operands:
-//   D3 = [Tu_hi ; *] V + [Tu_lo ; *] V            rows 0-63: U
+//   D3 = [Tu_hi ; Tu_lo] V                        rows 0-63: Tu_hi V, rows 64-127: Tu_lo V;
+//                                                 U = their sum (the second half crosses
+//                                                 to the rows-0-63 warps in shared memory)
 //   D4 = [W^ ; Q] K^T                             rows 64-127: QK^T -> P
 //   D1 = [W^ ; Q] H^                              rows 0-63: W^ H^, rows 64-127: Q H^
 //   D2 = K^T [Delta'_hi | Delta'_lo]              N = 128; the state update (M = Dk)
@@ -64,7 +66,8 @@ struct FSmem {
   static constexpr int HB = AP + 16384;            // H^ codes as bf16 [128 dk][64 v]
   static constexpr int DP = HB + 16384;            // decayed Delta hi, lo [64 tok][64 v]
   static constexpr int DD = DP + 16384;            // Delta hi, lo
-  static constexpr int CV = DD + 16384;            // 2 buffers x chunk vectors (1280 B)
+  static constexpr int ULO = DD + 16384;           // Tu_lo V, fp32 [64 tok][64 v] (16-byte chunks swizzled by row)
+  static constexpr int CV = ULO + 16384;           // 2 buffers x chunk vectors (1280 B)
   static constexpr int BYTES = CV + 2 * kCvecFloats * 4 + 1024;  // + alignment slack
   static_assert(BYTES <= 232448, "shared memory budget");
 };
@@ -156,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
   // products done: u (D3), a (D1), d4 (D4), s (D2), o (D5), end (everything)
   __shared__ __align__(8) uint64_t b_u, b_a, b_d4, b_s, b_o, b_end;
   // epilogue signals: H^ and W^ ready, P ready, Delta ready, outputs stored
-  __shared__ __align__(8) uint64_t e_hb, e_p, e_dl, e_out;
+  __shared__ __align__(8) uint64_t e_hb, e_p, e_dl, e_out, e_ulo;
   __shared__ uint32_t tmem_slot;
   __shared__ float red[kEpiWarps];
   __shared__ int abort_flag;
@@ -215,6 +218,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
     mbar_init(&e_p, kEpiWarps / 2);
     mbar_init(&e_dl, kEpiWarps / 2);
     mbar_init(&e_out, kEpiWarps / 2);
+    mbar_init(&e_ulo, kEpiWarps / 2);
     abort_flag = 0;
     fence_mbar_init();
   }
@@ -255,16 +259,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
         for (int pn = 0; pn < 2; ++pn)
           tma_load_2d(AQW + pn * 16384 + 8192, &p.tm_q, hk * 128 + pn * 64, tok_of(c), &in_q);
       };
-      // D3 = [Tu_hi ; *] V + [Tu_lo ; *] V  (U in rows 0-63)
+      // D3 = [Tu_hi ; Tu_lo] V  (Tu_hi V in rows 0-63, Tu_lo V in rows 64-127)
       auto issue_u = [&](int c) {
         const int b = c & 1;
         const uint64_t atu = sdesc(smem_u32(ATUb(b)), 16, 1024), vt = sdesc(smem_u32(VTb(b)), 8192, 1024);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
           umma(tmem + kD3, dadd(atu, ks * 32), dadd(vt, ks * 2048), kIdKM, ks > 0);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          umma(tmem + kD3, dadd(atu, 8192 + ks * 32), dadd(vt, ks * 2048), kIdKM, true);
         umma_commit(&b_u);
       };
       load_kw(0);
@@ -478,6 +479,23 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
       __syncwarp();
       if (lane == 0) mbar_arrive(&e_hb);
 
+      // ---- Tu_lo V (D3 rows 64-127) to the warps of rows 0-63 ----
+      float* ulo = reinterpret_cast<float*>(sm + FSmem::ULO) + t_row * 64;
+      auto ulo_chunk = [&](int j) { return ((col0 >> 2) + j) ^ (t_row & 7); };
+      if (!lo_rows) {
+        bad |= !mbar_wait(&b_u, ph);
+        tc_fence_after();
+        float x[16];
+        tmem_ld16(tl + kD3, x);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<float4*>(ulo + 4 * ulo_chunk(j)) =
+              make_float4(x[4 * j], x[4 * j + 1], x[4 * j + 2], x[4 * j + 3]);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&e_ulo);
+      }
+
       // ---- outputs of the previous chunk (its D1 and D5 buffers) ----
       if (!lo_rows && c > 0) store_out(c - 1, sH_prev);
 
@@ -486,10 +504,19 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
       const float* cv = CVb(b);
       float u[16];
       if (lo_rows) {
-        // U (rows 0-63)
+        // U (rows 0-63) = Tu_hi V (D3 rows 0-63) + Tu_lo V (from the other warps)
         bad |= !mbar_wait(&b_u, ph);
         tc_fence_after();
         tmem_ld16(tl + kD3, u);
+        bad |= !mbar_wait(&e_ulo, ph);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float4 a = *reinterpret_cast<const float4*>(ulo + 4 * ulo_chunk(j));
+          u[4 * j] += a.x;
+          u[4 * j + 1] += a.y;
+          u[4 * j + 2] += a.z;
+          u[4 * j + 3] += a.w;
+        }
       } else {
         // P_ij = 2^{(gamma_i - gamma_j) log2 e} q_i.k_j for j <= i (i = t_row, j = col0 + jj)
         bad |= !mbar_wait(&b_d4, ph);
