@@ -20,8 +20,11 @@
 //   C1 = K dH                               (M = 64 tokens, N = 128, K = 128)
 //   C2 = Q^T (scale e^gamma dO) + Wc^T dDelta'   (M = 128 = Dk, N = 128, K = 64;
 //        dDelta' = -sW dDelta in bf16; the first term is off the chain)
-// The W code / dO conversions of a chunk run while its C1 executes, and
-// P^T dO of the next chunk is issued behind them.
+// The W code / dO conversions of a chunk run while its C1 executes, and its
+// Q^T product runs while the dDelta epilogue does; P^T dO of the next chunk
+// is issued behind the chunk's C2, into the window of the dH update (the
+// tensor pipe runs products in issue order, so a product queued ahead of C2
+// would delay it).
 // The dH' entering each chunk (bf16) leaves by one bulk copy of its 32 KiB
 // shared-memory image.
 #include <cuda.h>
@@ -199,13 +202,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
           for (int ks = 0; ks < 4; ++ks)
             umma(tmem + kA2, dadd(a, ks * 2048), dadd(e, ks * 2048), idMM, ks > 0);
         }
-        // P^T dO of the next chunk (its A0 buffer was last read two chunks ago)
-        if (it + 1 < nch) {
-          bad |= !mbar_wait(&in_full[b ^ 1], (uint32_t)((it + 1) >> 1) & 1u);
-          if (bad) break;
-          tc_fence_after();
-          issue_pdo(it + 1);
-        }
         // C2 += Wc^T dDelta'
         bad |= !mbar_wait(&e_dd, ph);
         if (bad) break;
@@ -217,9 +213,21 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
             umma(tmem + kA2, dadd(a, ks * 2048), dadd(d, ks * 2048), idMM, true);
           umma_commit(&b_c2);
         }
-        // this chunk's buffer is free (C1 and both P^T dO / Q^T products that
-        // read it completed before the dDelta epilogue signalled)
-        if (it + 2 < nch) load(it + 2);
+        // P^T dO of the next chunk (its A0 buffer was last read two chunks ago),
+        // behind C2: it runs while the epilogues update dH
+        if (it + 1 < nch) {
+          bad |= !mbar_wait(&in_full[b ^ 1], (uint32_t)((it + 1) >> 1) & 1u);
+          if (bad) break;
+          tc_fence_after();
+          issue_pdo(it + 1);
+        }
+        // this chunk's buffers are free once every product that reads them is
+        // done: C2's commit covers Q^T (scale e^gamma dO), which C1's does not
+        // (P^T dO of this chunk ran before the previous C2)
+        if (it + 2 < nch) {
+          bad |= !mbar_wait(&b_c2, ph);
+          if (!bad) load(it + 2);
+        }
       }
       if (bad) abort_flag = 1;
     }

@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
   using S = BSmem;
   extern __shared__ __align__(1024) unsigned char sm_raw[];
   unsigned char* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
-  __shared__ __align__(8) uint64_t bar_in, bar_mma;
+  __shared__ __align__(8) uint64_t bar_in, bar_mma, bar_end;
   __shared__ uint32_t tmem_slot;
   __shared__ float scl[9];  // the tile's state scales (one per block_v columns), then sW
   __shared__ Tile s_next;   // the next tile (decoded by thread 0 during this one)
@@ -214,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
   if (tid == 0) {
     mbar_init(&bar_in, 1);
     mbar_init(&bar_mma, 1);
+    mbar_init(&bar_end, 1);
     fence_mbar_init();
   }
   tc_fence_before();
@@ -459,7 +460,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
           const float s0 = sW * hs[col >> p.bv_log2], s1 = sW * hs[(col + 1) >> p.bv_log2];
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
-            const int i = row0 + gq + 8 * e2;
             st2o(sm + S::DB + fo128[nt] + 1024 * e2, u[nt][2 * e2] - s0 * wh[nt][2 * e2],
                 u[nt][2 * e2 + 1] - s1 * wh[nt][2 * e2 + 1]);
           }
@@ -512,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
-            const int i = row0 + gq + 8 * e2, col = 32 * cq + 8 * nt + 2 * tq;
+            const int i = row0 + gq + 8 * e2;
             const float di = dec[i];
             st2o(sm + S::DDB + fo128[nt] + 1024 * e2, p.scale * a[nt][2 * e2] + di * b[nt][2 * e2],
                 p.scale * a[nt][2 * e2 + 1] + di * b[nt][2 * e2 + 1]);
@@ -547,7 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
-            const int i = row0 + gq + 8 * e2, d = 32 * cq + 8 * nt + 2 * tq;
+            const int i = row0 + gq + 8 * e2;
             const float2 kv = ld2o(sm + S::KS + fo128[nt] + 1024 * e2);
             const float di = dec[i];
             dK[nt][2 * e2] = di * a[nt][2 * e2];
@@ -578,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
-            const int i = row0 + gq + 8 * e2, d = 32 * cq + 8 * nt + 2 * tq;
+            const int i = row0 + gq + 8 * e2;
             const float2 qv = ld2o(sm + S::QS + fo128[nt] + 1024 * e2);
             const float si = p.scale * eg[i];
             dQ[nt][2 * e2] = si * a[nt][2 * e2];
@@ -596,7 +596,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
-            const int i = row0 + gq + 8 * e2, d = 32 * cq + 8 * nt + 2 * tq;
             st2o(sm + S::DWB + fo128[nt] + 1024 * e2, -a[nt][2 * e2], -a[nt][2 * e2 + 1]);
           }
       }
@@ -608,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
-            const int j = row0 + gq + 8 * e2, col = 32 * cq + 8 * nt + 2 * tq;
+            const int j = row0 + gq + 8 * e2;
             const float2 vv = ld2o(sm + S::VS + fo128[nt] + 1024 * e2);
             bv[nt][2 * e2] = a[nt][2 * e2] * vv.x;
             bv[nt][2 * e2 + 1] = a[nt][2 * e2 + 1] * vv.y;
@@ -643,7 +642,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
-            const int i = row0 + gq + 8 * e2, j = 16 * cq + 8 * nt + 2 * tq;
+            const int j = 16 * cq + 8 * nt + 2 * tq;
             st2o(sm + S::DTB + fo64[nt] + 1024 * e2, a[nt][2 * e2] * bet[j] + b[nt][2 * e2] * beg[j],
                 a[nt][2 * e2 + 1] * bet[j + 1] + b[nt][2 * e2 + 1] * beg[j + 1]);
           }
@@ -656,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
-            const int i = row0 + gq + 8 * e2, d = 32 * cq + 8 * nt + 2 * tq;
+            const int i = row0 + gq + 8 * e2;
             const float2 kv = ld2o(sm + S::KS + fo128[nt] + 1024 * e2);
             dK[nt][2 * e2] += beg[i] * a[nt][2 * e2];
             dK[nt][2 * e2 + 1] += beg[i] * a[nt][2 * e2 + 1];
@@ -679,7 +678,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int e2 = 0; e2 < 2; ++e2) {
-            const int i = row0 + gq + 8 * e2, j = 16 * cq + 8 * nt + 2 * tq;
             st2o(sm + S::XB + fo64[nt] + 1024 * e2, a[nt][2 * e2], a[nt][2 * e2 + 1]);
           }
       }
@@ -806,8 +804,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
   }
 
 teardown:
-  // after a bounded wait gave up, the next tile's copies may still be in flight
-  if (failed && tid == 0) mbar_wait(&bar_in, in_parity);
+  // after a bounded wait gave up, the next tile's copies may still be in flight;
+  // no product may be in flight when TMEM is freed
+  if (tid == 0) {
+    if (failed) mbar_wait(&bar_in, in_parity);
+    umma_commit(&bar_end);
+    mbar_wait(&bar_end, 0);
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
