@@ -89,7 +89,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
   constexpr uint32_t kA0 = 0, kA1 = 2 * NW, kA2 = 3 * NW;
   extern __shared__ __align__(1024) unsigned char sm_raw[];
   unsigned char* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
-  __shared__ __align__(8) uint64_t in_full[2], dh_ready, conv_done, b_c1, e_dd, b_c2, b_end;
+  __shared__ __align__(8) uint64_t in_full[2], dh_ready, conv_done, b_c1, b_q, e_dd, b_c2, b_end;
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
@@ -129,6 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
     mbar_init(&dh_ready, kEpiWarps);
     mbar_init(&conv_done, kEpiWarps);
     mbar_init(&b_c1, 1);
+    mbar_init(&b_q, 1);
     mbar_init(&e_dd, kEpiWarps);
     mbar_init(&b_c2, 1);
     mbar_init(&b_end, 1);
@@ -144,15 +145,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
   if (producer) {
     // ======================= producer warp =======================
     if (lane == 0 && nch > 0) {
-      auto load = [&](int it) {
+      // the copies of iteration it but Q (the barrier expects all bytes), then Q
+      auto load_rest = [&](int it) {
         const int b = it & 1;
         const int y = (int)(tok0 + (int64_t)chunk_of(it) * kChunk);
         mbar_expect_tx(&in_full[b], in_tx<NB>());
 #pragma unroll
-        for (int pn = 0; pn < 2; ++pn) {
+        for (int pn = 0; pn < 2; ++pn)
           tma_load_2d(KTb(b) + pn * 8192, &p.tm_k, hk * 128 + pn * 64, y, &in_full[b]);
-          tma_load_2d(QTb(b) + pn * 8192, &p.tm_q, hk * 128 + pn * 64, y, &in_full[b]);
-        }
 #pragma unroll
         for (int pn = 0; pn < NB; ++pn)
           tma_load_2d(DTb(b) + pn * 8192, &p.tm_do, h * 128 + vb0 + pn * 64, y, &in_full[b]);
@@ -161,6 +161,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
         tma_load_2d(WCb(b), &p.tm_wc, h * 128, y, &in_full[b]);
         bulk_load_1d(sm + S::CV + b * kCvecFloats * 4, p.cvec + sh_of(it) * kCvecFloats,
                      kCvecFloats * 4, &in_full[b]);
+      };
+      auto load_q = [&](int it) {
+        const int b = it & 1;
+        const int y = (int)(tok0 + (int64_t)chunk_of(it) * kChunk);
+#pragma unroll
+        for (int pn = 0; pn < 2; ++pn)
+          tma_load_2d(QTb(b) + pn * 8192, &p.tm_q, hk * 128 + pn * 64, y, &in_full[b]);
       };
       const uint32_t idPd = idesc(64, NW, 1, 1), idKd = idesc(64, NW, 0, 1);
       const uint32_t idMM = idesc(128, NW, 1, 1);
@@ -172,8 +179,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
         for (int ks = 0; ks < 4; ++ks)
           umma(tmem + kA0 + NW * b, dadd(a, ks * 2048), dadd(d, ks * 2048), idPd, ks > 0);
       };
-      load(0);
-      if (nch > 1) load(1);
+      load_rest(0);
+      load_q(0);
+      if (nch > 1) {
+        load_rest(1);
+        load_q(1);
+      }
       bad |= !mbar_wait(&in_full[0], 0);
       tc_fence_after();
       if (!bad) issue_pdo(0);
@@ -201,6 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)
             umma(tmem + kA2, dadd(a, ks * 2048), dadd(e, ks * 2048), idMM, ks > 0);
+          if (it + 2 < nch) umma_commit(&b_q);  // waited for below, before Q(it + 2) lands here
         }
         // C2 += Wc^T dDelta'
         bad |= !mbar_wait(&e_dd, ph);
@@ -221,12 +233,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
           tc_fence_after();
           issue_pdo(it + 1);
         }
-        // this chunk's buffers are free once every product that reads them is
-        // done: C2's commit covers Q^T (scale e^gamma dO), which C1's does not
-        // (P^T dO of this chunk ran before the previous C2)
+        // this chunk's buffers: C1 (and P^T dO of this chunk, before the
+        // previous C2) had read all but Q when the dDelta epilogue signalled;
+        // Q is free once Q^T (scale e^gamma dO) is done
         if (it + 2 < nch) {
-          bad |= !mbar_wait(&b_c2, ph);
-          if (!bad) load(it + 2);
+          load_rest(it + 2);
+          bad |= !mbar_wait(&b_q, ph);
+          if (!bad) load_q(it + 2);
         }
       }
       if (bad) abort_flag = 1;

@@ -84,7 +84,6 @@ constexpr uint32_t kQTx = 2 * 8192;           // Q (2 boxes)
 
 constexpr uint32_t kIdKK = idesc(128, 64, 0, 0);  // A K-major, B K-major
 constexpr uint32_t kIdKM = idesc(128, 64, 0, 1);  // A K-major, B MN-major
-constexpr uint32_t kIdMM = idesc(128, 64, 1, 1);  // A MN-major, B MN-major
 // N = 128: a B operand of two 64-column panels 8 KB apart ([hi | lo] halves)
 constexpr uint32_t kIdKM2 = idesc(128, 128, 0, 1);
 constexpr uint32_t kIdMM2 = idesc(128, 128, 1, 1);
@@ -150,7 +149,8 @@ __device__ __forceinline__ void quant16(float (&x)[16], float rcp, float s, bool
 // -> H_{c+1}; D4(c) (QK^T), D5(c) (P Delta) and D3(c+1) (U of the next chunk)
 // fill the tensor pipe in between, the next chunk's W^ conversion runs while
 // D2(c) executes, and the outputs of chunk c are stored after QDQ(c+1).
-template <int SM, int WM>
+// CTX: the backward's context (state codes and scales, P images) is saved.
+template <int SM, int WM, bool CTX>
 __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid_constant__ FusedParams p) {
   extern __shared__ __align__(1024) unsigned char sm_raw[];
   unsigned char* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
@@ -303,9 +303,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
         for (int ks = 0; ks < 8; ++ks)
           umma(tmem + kD4, dadd(aq, (ks >> 2) * 16384 + (ks & 3) * 32),
                dadd(ktk, (ks >> 2) * 8192 + (ks & 3) * 32), kIdKK, ks > 0);
-        // the last bulk copy of a P image has read its tile before the P epilogue
-        // (which waits for D4) rewrites it
-        tma_store_wait_read();
         umma_commit(&b_d4);
         // K of the next chunk: H^(c) being ready means the state update of chunk
         // c - 1 ran, so D2(c - 1), the last reader of that K buffer, is done
@@ -335,11 +332,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
         bad |= !mbar_wait(&e_p, ph);
         if (bad) break;
         tc_fence_after();
-        // a full chunk's P image is its bf16 tile P_hi byte for byte: one bulk copy
-        if (p.pb && vb == 0 && L - c * kChunk >= kChunk) {
-          bulk_store_1d(static_cast<unsigned char*>(p.pb) + sh_of(c) * 8192, AP + 8192, 8192);
-          tma_store_commit();
-        }
         // [P_lo ; P_hi] [Delta_hi | Delta_lo] as one N = 128 product, then
         // [* ; P_lo] Delta_hi into columns 0-63 (the A tile starts one panel
         // below P_lo, in the second Tu buffer, so its rows 64-127 are P_lo).  The P epilogue of chunk c + 1
@@ -443,6 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
       bad |= !mbar_wait(&in_vt[0], 0);
       convert_w(0, tid, kEpiThreads);
     }
+    constexpr bool all_convert = CTX;
     float sH_prev = 1.f;
     int c = 0;
     for (; c < nch; ++c) {
@@ -463,21 +456,24 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
       for (int w = 1; w < kEpiWarps; ++w) amax = fmaxf(amax, red[w]);
       float sH, rcp;
       qdq_scale<SM>(amax, sH, rcp);
+      uint32_t c4[4];
       {
         float vals[16];
-        uint32_t c4[4];
         quant16<SM>(hv, rcp, sH, amax == 0.f, vals, c4);
         st8_bf16(HB, row, col0 >> 3, vals);
         st8_bf16(HB, row, (col0 >> 3) + 1, vals + 8);
-        if (p.h_codes) {
-          uint8_t* dst = p.h_codes + ((slot * p.Hv + h) * 128 + row) * 128 + vb * 64 + col0;
-          *reinterpret_cast<uint4*>(dst) = make_uint4(c4[0], c4[1], c4[2], c4[3]);
-          if (tid == 0) p.h_scales[(slot * p.Hv + h) * 2 + vb] = sH;
-        }
       }
       fence_proxy_async();  // H^ (and the W^ converted earlier) before D1 reads them
       __syncwarp();
       if (lane == 0) mbar_arrive(&e_hb);
+      // the backward's copy of the state codes, after the signal (the arrival
+      // orders this thread's earlier writes, so a global store before it would
+      // hold it back)
+      if (CTX && p.h_codes) {
+        uint8_t* dst = p.h_codes + ((slot * p.Hv + h) * 128 + row) * 128 + vb * 64 + col0;
+        *reinterpret_cast<uint4*>(dst) = make_uint4(c4[0], c4[1], c4[2], c4[3]);
+        if (tid == 0) p.h_scales[(slot * p.Hv + h) * 2 + vb] = sH;
+      }
 
       // ---- Tu_lo V (D3 rows 64-127) to the warps of rows 0-63 ----
       float* ulo = reinterpret_cast<float*>(sm + FSmem::ULO) + t_row * 64;
@@ -532,7 +528,13 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
         }
         // [P_lo | P_hi]: lo at 0, hi at +8 KB
         st16_split(AP + 8192, AP, t_row, col0, x);
-        if (p.pb && vb == 0 && Lc < kChunk) {  // a partial chunk: rows past its end zero
+        fence_proxy_async();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&e_p);
+        // the P image the backward reads: P_hi (the bf16 rounding of P) in the
+        // tile's swizzled layout, rows past the chunk end zero, after the signal
+        if (CTX && p.pb && vb == 0) {
           unsigned char* pimg = reinterpret_cast<unsigned char*>(p.pb) + (slot * p.Hv + h) * 8192;
           float z[16];
 #pragma unroll
@@ -540,10 +542,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
           st8_bf16(pimg, t_row, col0 >> 3, z);
           st8_bf16(pimg, t_row, (col0 >> 3) + 1, z + 8);
         }
-        fence_proxy_async();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&e_p);
       }
 
       // ---- a7: Delta = U - sW sH W^ H^ (rows 0-63); decayed Delta' for the state update ----
@@ -563,28 +561,30 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
         }
         st16_split(DD, DD + 8192, t_row, col0, dl);
         st16_split(DP, DP + 8192, t_row, col0, dd);
-        if (p.db) {
-          // the Delta image: the hi half (Delta rounded to bf16), as stored in DD
-          unsigned char* dimg =
-              reinterpret_cast<unsigned char*>(p.db) + ((slot * p.Hv + h) * 2 + vb) * 8192;
-          *reinterpret_cast<uint4*>(dimg + sw_off(t_row, col0)) =
-              *reinterpret_cast<const uint4*>(DD + sw_off(t_row, col0));
-          *reinterpret_cast<uint4*>(dimg + sw_off(t_row, col0 + 8)) =
-              *reinterpret_cast<const uint4*>(DD + sw_off(t_row, col0 + 8));
-        }
         fence_proxy_async();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&e_dl);
+        if (CTX && p.db) {
+          // the Delta image: the hi half (Delta rounded to bf16, as in DD), after the signal
+          unsigned char* dimg =
+              reinterpret_cast<unsigned char*>(p.db) + ((slot * p.Hv + h) * 2 + vb) * 8192;
+          st8_bf16(dimg, t_row, col0 >> 3, dl);
+          st8_bf16(dimg, t_row, (col0 >> 3) + 1, dl + 8);
+        }
       }
 
       // ---- the next chunk's W^, while D2 runs: [W^ ; Q] is free once D1 and D4 are done.
-      // The warps of rows 64-127 convert it: the other half is on the chain
-      // (Delta -> D2 -> state) ----
-      if (c + 1 < nch && !lo_rows) {
+      // Without the backward's context the warps of rows 64-127 convert it (the
+      // others carry the chain Delta -> D2 -> state); with it, those warps also
+      // store the P image, and all warps share the conversion ----
+      if (c + 1 < nch && (all_convert || !lo_rows)) {
         bad |= !mbar_wait(&b_d4, ph);
         bad |= !mbar_wait(&in_vt[b ^ 1], (uint32_t)((c + 1) >> 1) & 1u);
-        convert_w(c + 1, ((warp >> 2) * 2 + (warp & 1)) * 32 + lane, kEpiThreads / 2);
+        if (all_convert)
+          convert_w(c + 1, tid, kEpiThreads);
+        else
+          convert_w(c + 1, ((warp >> 2) * 2 + (warp & 1)) * 32 + lane, kEpiThreads / 2);
       }
 
       // ---- a9: H <- e^{gamma_L} H^ + K~^T Delta ----
@@ -629,7 +629,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
     }
     umma_commit(&b_end);  // completes once every product issued so far is done
     mbar_wait(&b_end, 0);
-    tma_store_wait_all();  // the P images' bulk copies
   }
   tc_fence_before();
   __syncthreads();
@@ -659,14 +658,21 @@ gdn_status launch_fused_scan(const FusedParams& p, int state_mode, int w_mode, c
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
   };
+  // the context (P images, state codes) is saved or not: one variant each
+  const bool ctx = p.pb != nullptr;
+  auto pick = [&](auto with_ctx, auto without) { return ctx ? run(with_ctx) : run(without); };
   if (state_mode == GDN_QDQ_E4M3 && w_mode == GDN_QDQ_E4M3)
-    return run(gdn_fwd_fused_kernel<GDN_QDQ_E4M3, GDN_QDQ_E4M3>);
+    return pick(gdn_fwd_fused_kernel<GDN_QDQ_E4M3, GDN_QDQ_E4M3, true>,
+                gdn_fwd_fused_kernel<GDN_QDQ_E4M3, GDN_QDQ_E4M3, false>);
   if (state_mode == GDN_QDQ_INT8 && w_mode == GDN_QDQ_E4M3)
-    return run(gdn_fwd_fused_kernel<GDN_QDQ_INT8, GDN_QDQ_E4M3>);
+    return pick(gdn_fwd_fused_kernel<GDN_QDQ_INT8, GDN_QDQ_E4M3, true>,
+                gdn_fwd_fused_kernel<GDN_QDQ_INT8, GDN_QDQ_E4M3, false>);
   if (state_mode == GDN_QDQ_INT8 && w_mode == GDN_QDQ_INT8)
-    return run(gdn_fwd_fused_kernel<GDN_QDQ_INT8, GDN_QDQ_INT8>);
+    return pick(gdn_fwd_fused_kernel<GDN_QDQ_INT8, GDN_QDQ_INT8, true>,
+                gdn_fwd_fused_kernel<GDN_QDQ_INT8, GDN_QDQ_INT8, false>);
   if (state_mode == GDN_QDQ_E4M3 && w_mode == GDN_QDQ_INT8)
-    return run(gdn_fwd_fused_kernel<GDN_QDQ_E4M3, GDN_QDQ_INT8>);
+    return pick(gdn_fwd_fused_kernel<GDN_QDQ_E4M3, GDN_QDQ_INT8, true>,
+                gdn_fwd_fused_kernel<GDN_QDQ_E4M3, GDN_QDQ_INT8, false>);
   return GDN_ERR_UNSUPPORTED_MODE;
 }
 
