@@ -234,16 +234,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
 
   // bounded wait on a barrier; on a timeout the error flag is set and the
   // copies / products in flight are waited for once more before teardown
+  // (a thread whose wait gave up carries on with garbage; the CTA barrier that
+  // ends the round makes the decision uniform, and every thread then leaves)
   bool failed = false;
   auto wait_all = [&](uint64_t* bar, uint32_t parity) {
-    const bool ok = mbar_wait(bar, parity);
-    if (__syncthreads_or(!ok)) {
-      if (tid == 0) {
-        atomicOr(&g_bwdtc_device_error, 1);
-        mbar_wait(bar, parity);
-      }
-      failed = true;
-    }
+    if (!mbar_wait(bar, parity)) failed = true;
     tc_fence_after();
   };
   // the round's shared-memory operands are written: make them visible to the
@@ -251,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
   auto publish = [&]() {
     fence_proxy_async();
     tc_fence_before();
-    __syncthreads();
+    if (__syncthreads_or(failed)) failed = true;
     tc_fence_after();
   };
 
@@ -365,7 +360,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
 
     wait_all(&bar_in, in_parity);
     in_parity ^= 1u;
-    if (failed) goto teardown;
 
     // ---- prologue: rows past the chunk end zeroed; W and state codes -> bf16
     //      (the u8 codes sit in the upper halves of their bf16 tiles: all are
@@ -410,6 +404,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
       put8(sm + S::HB, 128, hr, hcol + 24, hc1.z, hc1.w, false, SMc{});
     }
     publish();
+    if (failed) goto teardown;
 
     {
       // =============== round 1: S, G, U, WH, K dH' ===============
@@ -429,7 +424,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
         if (more) load_scales(nxt);
       }
       round_end();
-      if (failed) goto teardown;
       if (more) load_group(0, nxt, cb ^ 1);  // W codes, chunk vectors
       {
         // P and Gamma o KK^T (N = 64: columns 16 cq ..)
@@ -493,6 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
         if (lane == 0) hd_part[warp] = hd;
       }
       publish();
+      if (failed) goto teardown;
 
       // =============== round 2: P^T dO, dO Delta^T, Delta dH'^T ===============
       if (tid == 0) {
@@ -502,7 +497,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
                   false);
       }
       round_end();
-      if (failed) goto teardown;
       float dQ[4][4], dK[4][4];
       {
         // dDelta = scale P^T dO + dec K dH'  -> bf16 (dH' is no longer read)
@@ -558,6 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
         add_row_sums<4>(kd, racc, R_TT + cq, row0, gq, tq);
       }
       publish();
+      if (failed) goto teardown;
 
       // =============== round 3: dO H^T, dDelta H^T, dDelta V^T, T^T dDelta ===============
       if (tid == 0) {
@@ -569,7 +564,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
         mma_steps(tmem + 320, dsc(S::TB, 8192), true, 0, dsc(S::DDB, 8192), true, 0, 4, kId128MM, false);
       }
       round_end();
-      if (failed) goto teardown;
       {
         // dQ = scale e^g (dO H^T); sum_d q_id dQ_id
         float a[4][4], qd[4][4];
@@ -623,6 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
         });
       }
       publish();
+      if (failed) goto teardown;
 
       // =============== round 4: dW K^T, T^T dW, Gm^T Q ===============
       if (more) load_group(1, nxt, cb ^ 1);  // V, dO, state codes, dH'
@@ -632,7 +627,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
         mma_steps(tmem + 384, dsc(S::GMB, 8192), true, 0, dsc(S::QS, 8192), true, 0, 4, kId128MM, false);
       }
       round_end();
-      if (failed) goto teardown;
       if (more) load_group(2, nxt, cb ^ 1);  // T diag(beta), Q
       {
         // dT = (dDelta V^T) diag(beta) + (dW K^T) diag(beta e^g) -> bf16
@@ -665,12 +659,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
         add_row_sums<4>(kw, racc, R_KW + cq, row0, gq, tq);
       }
       publish();
+      if (failed) goto teardown;
 
       // =============== round 5: X = T^T dT ===============
       if (tid == 0)
         mma_steps(tmem + 0, dsc(S::TB, 8192), true, 0, dsc(S::DTB, 8192), true, 0, 4, kId64MM, false);
       round_end();
-      if (failed) goto teardown;
       {
         float a[2][4];
         tmem_ld_frag<2>(tq_base + 0 + 16 * cq, a);
@@ -682,12 +676,12 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
           }
       }
       publish();
+      if (failed) goto teardown;
 
       // =============== round 6: X T^T ===============
       if (tid == 0)
         mma_steps(tmem + 64, dsc(S::XB, 16), false, 0, dsc(S::TB, 16), false, 0, 4, kId64, false);
       round_end();
-      if (failed) goto teardown;
       if (more) load_group(3, nxt, cb ^ 1);  // T
       {
         // dA = -(X T^T) strictly lower; dKK = dA beta_i Gamma_ij (strictly lower;
@@ -718,6 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
         add_col_sums<2>(aa, racc, R_AAC + q4, 16 * cq, gq, tq);
       }
       publish();
+      if (failed) goto teardown;
 
       // =============== round 7: Gm K, (dKK + dKK^T) K ===============
       if (tid == 0) {
@@ -726,7 +721,6 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
         mma_steps(tmem + 384, dsc(S::DKKB, 8192), true, 0, dsc(S::KS, 8192), true, 0, 4, kId128MM, true);
       }
       round_end();
-      if (failed) goto teardown;
       if (more) load_group(4, nxt, cb ^ 1);  // K
       {
         float a[4][4], b[4][4];
@@ -752,7 +746,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_chunk_tc_kernel(const __g
     }
 
     // ---- dgamma -> dg (reverse cumsum), dbeta (warps 0-1, fixed-order sums) ----
-    __syncthreads();
+    if (__syncthreads_or(failed)) failed = true;
+    if (failed) goto teardown;
     if (warp < 2) {
       const int i = tid;  // row 0..63
       auto sum4 = [&](int s0) {
@@ -807,7 +802,11 @@ teardown:
   // after a bounded wait gave up, the next tile's copies may still be in flight;
   // no product may be in flight when TMEM is freed
   if (tid == 0) {
-    if (failed) mbar_wait(&bar_in, in_parity);
+    if (failed) {
+      atomicOr(&g_bwdtc_device_error, 1);
+      mbar_wait(&bar_in, in_parity ^ 1u);
+      mbar_wait(&bar_in, in_parity);
+    }
     umma_commit(&bar_end);
     mbar_wait(&bar_end, 0);
   }
