@@ -201,11 +201,13 @@ def test_fwd_without_optional_outputs_and_zero_tokens():
     assert o.numel() == 0 and torch.equal(ht, h0)
 
 
-@pytest.mark.parametrize("sm,wm", [("e4m3", "e4m3"), ("int8", "e4m3")])
+@pytest.mark.parametrize("sm,wm", [("e4m3", "e4m3"), ("int8", "e4m3"), ("int8", "int8"),
+                                   ("e4m3", "int8")])
 def test_fwd_forward_only_equals_training_forward(sm, wm):
     """Without the backward's context (save_ctx = 0: no T, Gamma o KK^T, P, Delta
-    images and, on the fused path, no state codes) the forward computes exactly
-    the same o and ht."""
+    images and, on the fused path, no state codes; the fused kernel then runs as
+    its own variant, with the work split differently between its warps) the
+    forward computes exactly the same o and ht, in every mode pair."""
     for w, lens in ((synth.small(B=2, T=200, Hk=2, Hv=4, Dk=128, Dv=128, state_mode=sm, w_mode=wm,
                                  h0=True, seed=12), None),
                     (synth.small(B=1, T=0, Hk=1, Hv=2, Dk=128, Dv=128, state_mode=sm, w_mode=wm,
