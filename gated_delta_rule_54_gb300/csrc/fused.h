@@ -40,7 +40,10 @@ struct FusedParams {
 };
 
 // grid (2, Hv, N); false: unsupported mode pair or launch failure
-gdn_status launch_fused_scan(const FusedParams& p, int state_mode, int w_mode, cudaStream_t st);
+// after_prep: the chunk prep was launched just before on st (the scan then
+// starts as its programmatic dependent; otherwise as an ordinary launch)
+gdn_status launch_fused_scan(const FusedParams& p, int state_mode, int w_mode, cudaStream_t st,
+                             bool after_prep);
 
 // nonzero if a fused-scan kernel's bounded wait gave up (cleared when reset)
 int fused_device_error(bool reset);

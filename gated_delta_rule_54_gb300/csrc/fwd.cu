@@ -1389,7 +1389,8 @@ gdn_status dispatch_modes(const gdn_problem& p, const FwdParams& prm, const Dims
 // prep (T kept in fp32, no U) and the fused scan + outputs.
 gdn_status launch_fused(const gdn_problem& p, const FwdParams& prm, const Dims& d,
                         cudaStream_t st) {
-  if (d.B * d.T > 0 && d.n_slots > 0) {
+  const bool prep = d.B * d.T > 0 && d.n_slots > 0;
+  if (prep) {
     gdn_status s = GDN_OK;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -1429,7 +1430,7 @@ gdn_status launch_fused(const gdn_problem& p, const FwdParams& prm, const Dims& 
   f.G = prm.G;
   f.N = prm.N;
   f.scale = prm.scale;
-  return launch_fused_scan(f, p.state_mode, p.w_mode, st);
+  return launch_fused_scan(f, p.state_mode, p.w_mode, st, prep);
 }
 
 }  // namespace

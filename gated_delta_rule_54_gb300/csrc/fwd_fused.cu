@@ -638,14 +638,17 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_fwd_fused_kernel(const __grid
 
 }  // namespace
 
-gdn_status launch_fused_scan(const FusedParams& p, int state_mode, int w_mode, cudaStream_t st) {
+gdn_status launch_fused_scan(const FusedParams& p, int state_mode, int w_mode, cudaStream_t st,
+                             bool after_prep) {
   const dim3 grid(2, (unsigned)p.Hv, (unsigned)p.N);
   auto run = [&](auto kern) -> gdn_status {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FSmem::BYTES) !=
         cudaSuccess)
       return GDN_ERR_CUDA;
     // programmatic stream serialization: CTAs take the SMs the chunk prep
-    // leaves, set up and load their first K and Q, then wait for the prep
+    // leaves, set up and load their first K and Q, then wait for the prep.
+    // Only behind the prep: the inputs read before that wait were written by
+    // work that completed before the prep started.
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(kThreads);
@@ -655,7 +658,7 @@ gdn_status launch_fused_scan(const FusedParams& p, int state_mode, int w_mode, c
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = after_prep ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kern, p) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
   };
   // the context (P images, state codes) is saved or not: one variant each
