@@ -233,9 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_bwd_scan_tc_kernel(const __gr
           tc_fence_after();
           issue_pdo(it + 1);
         }
-        // this chunk's buffers: C1 (and P^T dO of this chunk, before the
-        // previous C2) had read all but Q when the dDelta epilogue signalled;
-        // Q is free once Q^T (scale e^gamma dO) is done
+        // this chunk's buffers: C1 and P^T dO of this chunk (issued before C1,
+        // so covered by its commit) had read all but Q when the dDelta
+        // epilogue signalled; Q is free once Q^T (scale e^gamma dO) is done
         if (it + 2 < nch) {
           load_rest(it + 2);
           bad |= !mbar_wait(&b_q, ph);
